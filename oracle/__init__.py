@@ -1,0 +1,191 @@
+"""CPU oracle for com.microsoft.PagedAttention (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+import this package. The product path never does; it shares no code with the CUDA
+implementation.
+
+``paged_attention_oracle.c`` is the definition of the operator written out in fp64
+(com.microsoft.PagedAttention README, "Description", "Inputs", "Attributes"): the
+cache write, then causal grouped-query attention of every query row over its
+sequence's history read back through ``block_table``, rounded once to the 16-bit type.
+This module compiles it with gcc (OpenMP over (sequence, head) pairs) and marshals
+numpy arrays into it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "paged_attention_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ERRORS = {
+    -1: "bad shape", -2: "bad cumulative_sequence_length / past_seqlens",
+    -3: "slot out of range", -4: "two tokens write one slot",
+    -5: "block_table entry out of range for an active page", -6: "out of memory",
+    -7: "sequence longer than max_blocks_per_sequence * block_size",
+}
+
+
+class OracleError(RuntimeError):
+    def __init__(self, code: int):
+        super().__init__(f"oracle rejected the input: {ERRORS.get(code, code)} ({code})")
+        self.code = code
+
+
+def build(force: bool = False) -> str:
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"],
+                       check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _bind(path: str):
+    lib = ctypes.CDLL(path)
+    i32, f32, p, u16, dbl = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_uint16, ctypes.c_double
+    lib.oracle_f16_to_double.argtypes = [u16]
+    lib.oracle_f16_to_double.restype = dbl
+    lib.oracle_bf16_to_double.argtypes = [u16]
+    lib.oracle_bf16_to_double.restype = dbl
+    lib.oracle_double_to_f16.argtypes = [dbl]
+    lib.oracle_double_to_f16.restype = u16
+    lib.oracle_double_to_bf16.argtypes = [dbl]
+    lib.oracle_double_to_bf16.restype = u16
+    lib.oracle_scatter.argtypes = [i32] * 8 + [p] * 9
+    lib.oracle_scatter.restype = ctypes.c_int
+    lib.oracle_attention.argtypes = [ctypes.c_int] + [i32] * 9 + [p] * 6 + [f32, p, p, p, ctypes.c_int]
+    lib.oracle_attention.restype = ctypes.c_int
+    lib.oracle_attention_rows.argtypes = ([ctypes.c_int] + [i32] * 9 + [p] * 6 + [f32, i32] +
+                                          [p] * 4 + [ctypes.c_int])
+    lib.oracle_attention_rows.restype = ctypes.c_int
+    lib.oracle_max_threads.argtypes = []
+    lib.oracle_max_threads.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = _bind(_LIB)
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+def max_threads() -> int:
+    return _load().oracle_max_threads()
+
+
+# ---- scalar conversions (exposed for the pins) -------------------------------------
+
+def f16_to_double(bits) -> np.ndarray:
+    lib = _load()
+    return np.array([lib.oracle_f16_to_double(int(b)) for b in np.ravel(bits)])
+
+
+def bf16_to_double(bits) -> np.ndarray:
+    lib = _load()
+    return np.array([lib.oracle_bf16_to_double(int(b)) for b in np.ravel(bits)])
+
+
+def double_to_f16(x) -> np.ndarray:
+    lib = _load()
+    return np.array([lib.oracle_double_to_f16(float(v)) for v in np.ravel(x)], dtype=np.uint16)
+
+
+def double_to_bf16(x) -> np.ndarray:
+    lib = _load()
+    return np.array([lib.oracle_double_to_bf16(float(v)) for v in np.ravel(x)], dtype=np.uint16)
+
+
+# ---- the operator ------------------------------------------------------------------
+
+def _dims(p):
+    N = int(p.query.shape[0])
+    B = int(np.asarray(p.past_seqlens).shape[0])
+    return (N, B, int(p.num_heads), int(p.kv_num_heads), int(p.head_size), int(p.num_blocks),
+            int(p.block_size), int(np.asarray(p.block_table).shape[1]))
+
+
+def scatter(p):
+    """Step 1 on copies of the caches. Returns (key_cache, value_cache)."""
+    lib = _load()
+    kc = np.array(p.key_cache, dtype=np.uint16, copy=True)
+    vc = np.array(p.value_cache, dtype=np.uint16, copy=True)
+    q = _c(p.query, np.uint16)
+    k = _c(p.key, np.uint16)
+    v = _c(p.value, np.uint16)
+    cum = _c(p.cumulative_sequence_length, np.int32)
+    past = _c(p.past_seqlens, np.int32)
+    bt = _c(p.block_table, np.int32)
+    sm = _c(p.slot_mapping, np.int32)
+    rc = lib.oracle_scatter(*_dims(p), _ptr(q), _ptr(k), _ptr(v), _ptr(kc), _ptr(vc), _ptr(cum),
+                            _ptr(past), _ptr(bt), _ptr(sm))
+    if rc:
+        raise OracleError(rc)
+    return kc, vc
+
+
+def attention(p, key_cache, value_cache, nthreads: int = 0):
+    """Step 2 given caches after the write. Returns (out f64 (N, nh, hs), lse (N, nh), out_bits (N, nh*hs))."""
+    lib = _load()
+    N, B, nh, kvh, hs, nblk, bs, mb = _dims(p)
+    q = _c(p.query, np.uint16)
+    out = np.zeros((N, nh, hs), dtype=np.float64)
+    lse = np.zeros((N, nh), dtype=np.float64)
+    bits = np.zeros((N, nh * hs), dtype=np.uint16)
+    dt = 1 if p.dtype == "bf16" else 0
+    rc = lib.oracle_attention(dt, N, B, nh, kvh, hs, nblk, bs, mb, int(q.shape[1]), _ptr(q),
+                              _ptr(_c(key_cache, np.uint16)), _ptr(_c(value_cache, np.uint16)),
+                              _ptr(_c(p.cumulative_sequence_length, np.int32)),
+                              _ptr(_c(p.past_seqlens, np.int32)), _ptr(_c(p.block_table, np.int32)),
+                              float(p.scale), _ptr(out), _ptr(lse), _ptr(bits), nthreads)
+    if rc:
+        raise OracleError(rc)
+    return out, lse, bits
+
+
+def attention_rows(p, key_cache, value_cache, tokens, heads, nthreads: int = 0):
+    """Step 2 for selected (token, head) pairs only. Returns (out (n, hs), lse (n,))."""
+    lib = _load()
+    N, B, nh, kvh, hs, nblk, bs, mb = _dims(p)
+    q = _c(p.query, np.uint16)
+    tokens = _c(tokens, np.int32)
+    heads = _c(heads, np.int32)
+    n = int(tokens.shape[0])
+    out = np.zeros((n, hs), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    dt = 1 if p.dtype == "bf16" else 0
+    rc = lib.oracle_attention_rows(dt, N, B, nh, kvh, hs, nblk, bs, mb, int(q.shape[1]), _ptr(q),
+                                   _ptr(_c(key_cache, np.uint16)), _ptr(_c(value_cache, np.uint16)),
+                                   _ptr(_c(p.cumulative_sequence_length, np.int32)),
+                                   _ptr(_c(p.past_seqlens, np.int32)), _ptr(_c(p.block_table, np.int32)),
+                                   float(p.scale), n, _ptr(tokens), _ptr(heads), _ptr(out), _ptr(lse),
+                                   nthreads)
+    if rc:
+        raise OracleError(rc)
+    return out, lse
+
+
+def paged_attention(p, nthreads: int = 0):
+    """The whole operator: returns dict(key_cache, value_cache, out, lse, out_bits)."""
+    kc, vc = scatter(p)
+    out, lse, bits = attention(p, kc, vc, nthreads)
+    return {"key_cache": kc, "value_cache": vc, "out": out, "lse": lse, "out_bits": bits}

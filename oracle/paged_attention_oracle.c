@@ -1,0 +1,329 @@
+/*
+ * ORACLE for com.microsoft.PagedAttention over packed variable-length batches.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may include, link, load or
+ * call this file: only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg use it. It shares no code with the CUDA implementation.
+ *
+ * It is the plain definition of the operator, written out with fp64 accumulation:
+ *
+ *   1. Cache write (com.microsoft.PagedAttention README, "Description" and the
+ *      `slot_mapping` row of "Inputs"): every new token's K and V rows are copied into
+ *      the cache slot `slot_mapping[i]`, or, when slot_mapping is omitted, into the slot
+ *      of its logical position past_seqlens[b] + j, i.e. block_table[b][p / block_size]
+ *      * block_size + p % block_size. A slot of -1 suppresses the write.
+ *   2. Attention ("Description": the step's K/V are scattered into the cache, then
+ *      attended with that history; "block_table remains required because it defines
+ *      the read path"): query row j of sequence b and head h attends, causally, the
+ *      keys t = 0 .. past_b + j of its sequence, all read from the updated cache
+ *      through block_table, with KV head g = h / (num_heads / kv_num_heads):
+ *        s_t = scale * <q, k_t>,  scale = attribute, or 1/sqrt(head_size) if it is 0
+ *              ("Attributes", `scale`)
+ *        o   = sum_t exp(s_t - m) v_t / sum_t exp(s_t - m),  m = max_t s_t
+ *        lse = m + ln(sum_t exp(s_t - m))   (natural log, scale included)
+ *      then o is rounded once to the 16-bit type (the "downcast at the final write"
+ *      of the WS2 CP-Aware Attention Contract, "Reduction Semantics").
+ *
+ * Readings where the pages leave a step open: bottom-right causal alignment (row j
+ * sees keys up to past_b + j, past being the committed length before the call: "Add
+ * Qwen3.8 packed hybrid PagedAttention export for ORT GenAI Engine", "Shared inputs"
+ * table); GQA groups are contiguous (WS2 CP-Aware Attention Contract, "Qwen3-8B TP=2
+ * CP=2 Example": each rank keeps 16 of 32 query heads with 4 of 8 KV heads); packed
+ * rows are [Q (nh*hs) | K (kvh*hs) | V (kvh*hs)], head-major inside each part
+ * (com.microsoft.PagedAttention README, "Inputs", `query`).
+ *
+ * Caller errors that the pages leave undefined (a slot out of range, two tokens
+ * writing one slot, a block_table entry out of range for an active page) are reported
+ * as negative return codes instead of being computed.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum {
+  ORACLE_OK = 0,
+  ORACLE_BAD_SHAPE = -1,
+  ORACLE_BAD_CUM = -2,
+  ORACLE_BAD_SLOT = -3,
+  ORACLE_DUPLICATE_SLOT = -4,
+  ORACLE_BAD_BLOCK = -5,
+  ORACLE_NO_MEMORY = -6,
+  ORACLE_TOO_LONG = -7,
+};
+
+/* ---- 16-bit float formats ------------------------------------------------------- */
+
+static uint64_t dbits(double x) { uint64_t u; memcpy(&u, &x, 8); return u; }
+
+/* IEEE 754 binary16 -> double (exact) */
+double oracle_f16_to_double(uint16_t h) {
+  int sign = (h >> 15) & 1, e = (h >> 10) & 0x1F, m = h & 0x3FF;
+  double v;
+  if (e == 0) v = ldexp((double)m, -24);                       /* subnormal: m * 2^-24 */
+  else if (e == 31) v = m ? NAN : INFINITY;
+  else v = ldexp((double)(m | 0x400), e - 25);                 /* 1.m * 2^(e-15) */
+  return sign ? -v : v;
+}
+
+/* bfloat16 (the top half of an IEEE binary32) -> double (exact) */
+double oracle_bf16_to_double(uint16_t h) {
+  int sign = (h >> 15) & 1, e = (h >> 7) & 0xFF, m = h & 0x7F;
+  double v;
+  if (e == 0) v = ldexp((double)m, -133);                      /* subnormal: m * 2^-133 */
+  else if (e == 255) v = m ? NAN : INFINITY;
+  else v = ldexp((double)(m | 0x80), e - 134);                 /* 1.m * 2^(e-127) */
+  return sign ? -v : v;
+}
+
+/* Round a double to a format with `mbits` stored significand bits and exponent bias
+ * `bias` (normal exponents 1 .. 2*bias), round to nearest, ties to even, directly from
+ * the 53-bit significand (one rounding). */
+static uint16_t round_to_small_float(double x, int mbits, int bias, int ebits) {
+  uint64_t u = dbits(x);
+  uint16_t sign = (uint16_t)((u >> 63) << 15);
+  uint16_t inf = (uint16_t)(((1u << ebits) - 1u) << mbits);
+  int ef = (int)((u >> 52) & 0x7FF);
+  uint64_t frac = u & ((1ULL << 52) - 1);
+  if (ef == 0x7FF) return frac ? (uint16_t)(sign | inf | (1u << (mbits - 1))) : (uint16_t)(sign | inf);
+  if (ef == 0) return sign; /* double subnormals are far below either format's range */
+  int e = ef - 1023;
+  if (e > bias) return (uint16_t)(sign | inf);
+  uint64_t sig = frac | (1ULL << 52);
+  int min_e = 1 - bias;
+  int shift = 52 - mbits + (e < min_e ? (min_e - e) : 0);
+  if (shift > 60) return sign;
+  uint64_t kept = sig >> shift, rem = sig & ((1ULL << shift) - 1), half = 1ULL << (shift - 1);
+  if (rem > half || (rem == half && (kept & 1))) kept += 1;
+  uint32_t h;
+  if (e >= min_e) h = ((uint32_t)(e + bias) << mbits) + (uint32_t)(kept - (1ULL << mbits));
+  else h = (uint32_t)kept; /* subnormal, possibly rounded up into the smallest normal */
+  if (h >= inf) h = inf;
+  return (uint16_t)(sign | h);
+}
+
+uint16_t oracle_double_to_f16(double x) { return round_to_small_float(x, 10, 15, 5); }
+uint16_t oracle_double_to_bf16(double x) { return round_to_small_float(x, 7, 127, 8); }
+
+/* value table for all 65536 bit patterns of the element type (0 = fp16, 1 = bf16) */
+static double* make_table(int dtype) {
+  double* t = (double*)malloc(65536 * sizeof(double));
+  if (!t) return NULL;
+  for (int i = 0; i < 65536; ++i)
+    t[i] = dtype == 1 ? oracle_bf16_to_double((uint16_t)i) : oracle_f16_to_double((uint16_t)i);
+  return t;
+}
+
+/* ---- input checks shared by both steps ----------------------------------------- */
+
+static int check_batch(int32_t N, int32_t B, int32_t nh, int32_t kvh, int32_t hs,
+                       int32_t num_blocks, int32_t bs, int32_t max_blocks,
+                       const int32_t* cum, const int32_t* past) {
+  if (N < 0 || B < 0 || nh <= 0 || kvh <= 0 || hs <= 0 || nh % kvh || num_blocks < 0 || bs <= 0 ||
+      max_blocks < 0)
+    return ORACLE_BAD_SHAPE;
+  if (cum[0] != 0 || cum[B] != N) return ORACLE_BAD_CUM;
+  for (int b = 0; b < B; ++b) {
+    if (cum[b + 1] < cum[b] || past[b] < 0) return ORACLE_BAD_CUM;
+    int64_t kv = (int64_t)past[b] + (cum[b + 1] - cum[b]);
+    if ((kv + bs - 1) / bs > max_blocks) return ORACLE_TOO_LONG;
+  }
+  return ORACLE_OK;
+}
+
+/* ---- step 1: cache write -------------------------------------------------------- */
+
+int oracle_scatter(int32_t N, int32_t B, int32_t nh, int32_t kvh, int32_t hs, int32_t num_blocks,
+                   int32_t bs, int32_t max_blocks, const uint16_t* query, const uint16_t* key,
+                   const uint16_t* value, uint16_t* key_cache, uint16_t* value_cache,
+                   const int32_t* cum, const int32_t* past, const int32_t* block_table,
+                   const int32_t* slot_mapping) {
+  int rc = check_batch(N, B, nh, kvh, hs, num_blocks, bs, max_blocks, cum, past);
+  if (rc) return rc;
+  const int64_t row = (int64_t)kvh * hs;              /* one token's K (or V) row */
+  const int64_t nslots = (int64_t)num_blocks * bs;
+  const int packed = key == NULL;
+  const int64_t qw = packed ? (int64_t)(nh + 2 * kvh) * hs : (int64_t)nh * hs;
+  unsigned char* used = (unsigned char*)calloc(nslots > 0 ? (size_t)nslots : 1, 1);
+  if (!used) return ORACLE_NO_MEMORY;
+  for (int b = 0; b < B; ++b) {
+    for (int32_t i = cum[b]; i < cum[b + 1]; ++i) {
+      int64_t slot;
+      if (slot_mapping) {
+        slot = slot_mapping[i];
+      } else {
+        int64_t p = (int64_t)past[b] + (i - cum[b]);          /* logical position */
+        int64_t blk = block_table[(int64_t)b * max_blocks + p / bs];
+        if (blk < 0 || blk >= num_blocks) { free(used); return ORACLE_BAD_BLOCK; }
+        slot = blk * bs + p % bs;
+      }
+      if (slot == -1) continue;                                 /* write suppressed */
+      if (slot < 0 || slot >= nslots) { free(used); return ORACLE_BAD_SLOT; }
+      if (used[slot]) { free(used); return ORACLE_DUPLICATE_SLOT; }
+      used[slot] = 1;
+      const uint16_t* k_src = packed ? query + i * qw + (int64_t)nh * hs : key + i * row;
+      const uint16_t* v_src = packed ? query + i * qw + (int64_t)(nh + kvh) * hs : value + i * row;
+      /* cache[slot / bs][slot % bs][:][:] is the contiguous row at flat slot index */
+      memcpy(key_cache + slot * row, k_src, (size_t)row * 2);
+      memcpy(value_cache + slot * row, v_src, (size_t)row * 2);
+    }
+  }
+  free(used);
+  return ORACLE_OK;
+}
+
+/* ---- step 2: attention for one (token, head) ----------------------------------- */
+
+/* Attention of packed query row i (sequence b, position j in it) for head h. rows[t] is
+ * the flat cache row of logical key t. Writes hs outputs and the lse. scores is
+ * scratch of at least past_b + j + 1 doubles. */
+static void attend_one(const double* tab, const uint16_t* query, int64_t qw, int32_t i, int32_t h,
+                       int32_t g, int32_t kvh, int32_t hs, int64_t limit, const int64_t* rows,
+                       const uint16_t* key_cache, const uint16_t* value_cache, double scale,
+                       double* scores, double* out, double* lse) {
+  const uint16_t* q = query + (int64_t)i * qw + (int64_t)h * hs;
+  double m = -INFINITY;
+  for (int64_t t = 0; t <= limit; ++t) {
+    const uint16_t* k = key_cache + (rows[t] * kvh + g) * hs;
+    double dot = 0.0;
+    for (int d = 0; d < hs; ++d) dot += tab[q[d]] * tab[k[d]];
+    scores[t] = scale * dot;
+    if (scores[t] > m) m = scores[t];
+  }
+  double den = 0.0;
+  for (int d = 0; d < hs; ++d) out[d] = 0.0;
+  for (int64_t t = 0; t <= limit; ++t) {
+    double w = exp(scores[t] - m);
+    den += w;
+    const uint16_t* v = value_cache + (rows[t] * kvh + g) * hs;
+    for (int d = 0; d < hs; ++d) out[d] += w * tab[v[d]];
+  }
+  for (int d = 0; d < hs; ++d) out[d] /= den;
+  *lse = m + log(den);
+}
+
+/* flat cache rows of the logical keys 0 .. L-1 of sequence b, through block_table */
+static int gather_rows(int32_t b, int64_t L, int32_t bs, int32_t max_blocks, int32_t num_blocks,
+                       const int32_t* block_table, int64_t* rows) {
+  for (int64_t t = 0; t < L; ++t) {
+    int64_t blk = block_table[(int64_t)b * max_blocks + t / bs];
+    if (blk < 0 || blk >= num_blocks) return ORACLE_BAD_BLOCK;
+    rows[t] = blk * bs + t % bs;
+  }
+  return ORACLE_OK;
+}
+
+static double resolve_scale(float scale, int32_t hs) {
+  return scale == 0.0f ? 1.0 / sqrt((double)hs) : (double)scale;
+}
+
+/* Attention for every packed row and head. out: N x nh x hs doubles; lse: N x nh;
+ * out_bits (optional): N x nh x hs 16-bit results rounded once. The caches passed in
+ * are the ones after the cache write. nthreads <= 0: the OpenMP default. */
+int oracle_attention(int dtype, int32_t N, int32_t B, int32_t nh, int32_t kvh, int32_t hs,
+                     int32_t num_blocks, int32_t bs, int32_t max_blocks, int32_t query_width,
+                     const uint16_t* query, const uint16_t* key_cache, const uint16_t* value_cache,
+                     const int32_t* cum, const int32_t* past, const int32_t* block_table, float scale,
+                     double* out, double* lse, uint16_t* out_bits, int nthreads) {
+  int rc = check_batch(N, B, nh, kvh, hs, num_blocks, bs, max_blocks, cum, past);
+  if (rc) return rc;
+  double* tab = make_table(dtype);
+  if (!tab) return ORACLE_NO_MEMORY;
+  const int32_t G = nh / kvh;
+  const double sc = resolve_scale(scale, hs);
+  int err = ORACLE_OK;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (int32_t b = 0; b < B; ++b) {
+    for (int32_t h = 0; h < nh; ++h) {
+      int32_t q_len = cum[b + 1] - cum[b];
+      if (q_len == 0) continue;
+      int64_t L = (int64_t)past[b] + q_len;
+      int64_t* rows = (int64_t*)malloc((size_t)L * sizeof(int64_t));
+      double* scores = (double*)malloc((size_t)L * sizeof(double));
+      if (!rows || !scores) {
+#pragma omp atomic write
+        err = ORACLE_NO_MEMORY;
+      } else if (gather_rows(b, L, bs, max_blocks, num_blocks, block_table, rows) != ORACLE_OK) {
+#pragma omp atomic write
+        err = ORACLE_BAD_BLOCK;
+      } else {
+        for (int32_t j = 0; j < q_len; ++j) {
+          int32_t i = cum[b] + j;
+          double* o = out + ((int64_t)i * nh + h) * hs;
+          attend_one(tab, query, query_width, i, h, h / G, kvh, hs, (int64_t)past[b] + j, rows,
+                     key_cache, value_cache, sc, scores, o, lse + (int64_t)i * nh + h);
+          if (out_bits)
+            for (int d = 0; d < hs; ++d)
+              out_bits[((int64_t)i * nh + h) * hs + d] =
+                  dtype == 1 ? oracle_double_to_bf16(o[d]) : oracle_double_to_f16(o[d]);
+        }
+      }
+      free(rows);
+      free(scores);
+    }
+  }
+  free(tab);
+  return err;
+}
+
+/* The same attention for a list of (token, head) pairs only: out n_sel x hs, lse n_sel.
+ * Lets large workloads be checked on sampled outputs. */
+int oracle_attention_rows(int dtype, int32_t N, int32_t B, int32_t nh, int32_t kvh, int32_t hs,
+                          int32_t num_blocks, int32_t bs, int32_t max_blocks, int32_t query_width,
+                          const uint16_t* query, const uint16_t* key_cache,
+                          const uint16_t* value_cache, const int32_t* cum, const int32_t* past,
+                          const int32_t* block_table, float scale, int32_t n_sel,
+                          const int32_t* sel_token, const int32_t* sel_head, double* out,
+                          double* lse, int nthreads) {
+  int rc = check_batch(N, B, nh, kvh, hs, num_blocks, bs, max_blocks, cum, past);
+  if (rc) return rc;
+  for (int32_t s = 0; s < n_sel; ++s)
+    if (sel_token[s] < 0 || sel_token[s] >= N || sel_head[s] < 0 || sel_head[s] >= nh)
+      return ORACLE_BAD_SHAPE;
+  double* tab = make_table(dtype);
+  if (!tab) return ORACLE_NO_MEMORY;
+  const int32_t G = nh / kvh;
+  const double sc = resolve_scale(scale, hs);
+  int err = ORACLE_OK;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int32_t s = 0; s < n_sel; ++s) {
+    int32_t i = sel_token[s], h = sel_head[s];
+    int32_t b = 0;
+    while (cum[b + 1] <= i) ++b;                    /* the sequence that owns row i */
+    int32_t j = i - cum[b];
+    int64_t L = (int64_t)past[b] + j + 1;           /* keys this row can see */
+    int64_t* rows = (int64_t*)malloc((size_t)L * sizeof(int64_t));
+    double* scores = (double*)malloc((size_t)L * sizeof(double));
+    if (!rows || !scores) {
+#pragma omp atomic write
+      err = ORACLE_NO_MEMORY;
+    } else if (gather_rows(b, L, bs, max_blocks, num_blocks, block_table, rows) != ORACLE_OK) {
+#pragma omp atomic write
+      err = ORACLE_BAD_BLOCK;
+    } else {
+      attend_one(tab, query, query_width, i, h, h / G, kvh, hs, L - 1, rows, key_cache,
+                 value_cache, sc, scores, out + (int64_t)s * hs, lse + s);
+    }
+    free(rows);
+    free(scores);
+  }
+  free(tab);
+  return err;
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

@@ -1,0 +1,81 @@
+"""Plant plausible mistakes in (a copy of) the oracle and check that the pins catch each.
+
+Every mutant is the oracle's C source with one textual edit, compiled on the CPU into a
+temporary library and swapped in for the duration of the test. A mutant that passes
+every pin would mean the pins do not constrain that part of the oracle.
+"""
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+MUTANTS = [
+    ("GQA head mapping h % kvh instead of h / G", "h / G", "h % kvh"),
+    ("causal limit one short", "(int64_t)past[b] + j, rows", "(int64_t)past[b] + j - 1, rows"),
+    ("scale dropped from the scores", "scores[t] = scale * dot;", "scores[t] = dot;"),
+    ("default scale 1/head_size", "1.0 / sqrt((double)hs)", "1.0 / (double)hs"),
+    ("wrong sign in the max shift", "double w = exp(scores[t] - m);", "double w = exp(scores[t] + m);"),
+    ("lse in base 2", "*lse = m + log(den);", "*lse = m + log2(den);"),
+    ("offsets reversed inside a page", "rows[t] = blk * bs + t % bs;", "rows[t] = blk * bs + (bs - 1 - t % bs);"),
+    ("slot ignores past_seqlens", "int64_t p = (int64_t)past[b] + (i - cum[b]);", "int64_t p = (i - cum[b]);"),
+    ("packed K taken from the wrong head offset", "query + i * qw + (int64_t)nh * hs : key",
+     "query + i * qw + (int64_t)(nh - 1) * hs : key"),
+    ("-1 slots not skipped", "if (slot == -1) continue;", ""),
+    ("rounding truncates", "if (rem > half || (rem == half && (kept & 1))) kept += 1;", ""),
+    ("PV unweighted", "out[d] += w * tab[v[d]];", "out[d] += tab[v[d]];"),
+    ("normalisation dropped", "for (int d = 0; d < hs; ++d) out[d] /= den;", ""),
+    ("fp16 exponent bias off by one", "ldexp((double)(m | 0x400), e - 25)", "ldexp((double)(m | 0x400), e - 24)"),
+    ("bf16 decoded as the low half", "int sign = (h >> 15) & 1, e = (h >> 7) & 0xFF, m = h & 0x7F;",
+     "int sign = (h >> 15) & 1, e = (h >> 6) & 0xFF, m = h & 0x3F;"),
+    ("V read from the K cache", "const uint16_t* v = value_cache + (rows[t] * kvh + g) * hs;",
+     "const uint16_t* v = key_cache + (rows[t] * kvh + g) * hs;"),
+]
+
+# a fast battery of pins (each raises on failure)
+BATTERY = [
+    lambda: pins.test_prefill_from_empty_matches_sdpa_causal("fp16", 4, 2, 64, 16),
+    lambda: pins.test_prefill_from_empty_matches_sdpa_causal("bf16", 6, 2, 32, 8),
+    lambda: pins.test_decode_matches_sdpa_without_mask("bf16"),
+    lambda: pins.test_chunked_prefill_matches_sdpa_bottom_right_mask("fp16"),
+    lambda: pins.test_single_token_no_past_returns_its_own_v("fp16"),
+    lambda: pins.test_single_token_no_past_returns_its_own_v("bf16"),
+    lambda: pins.test_two_keys_closed_forms("fp16"),
+    lambda: pins.test_constant_v_returns_v("bf16"),
+    lambda: pins.test_slot_golden_table(),
+    lambda: pins.test_minus_one_slots_leave_cache_untouched_and_reads_use_cache(),
+    lambda: pins.test_packed_qkv_equals_separate(),
+    lambda: pins.test_scale_zero_means_inverse_sqrt_head_size(),
+]
+
+
+def _compile_mutant(tmp_path, old, new):
+    src = open(oracle._SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor not found: {old!r}"
+    c = tmp_path / "mutant.c"
+    c.write_text(src.replace(old, new))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fopenmp", "-fPIC", "-shared", str(c), "-o", str(so), "-lm"],
+                   check=True)
+    return str(so)
+
+
+def test_battery_passes_on_the_real_oracle():
+    for pin in BATTERY:
+        pin()
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_each_planted_mistake_fails_a_pin(tmp_path, monkeypatch, name, old, new):
+    lib = oracle._bind(_compile_mutant(tmp_path, old, new))
+    monkeypatch.setattr(oracle, "_lib", lib)
+    caught = []
+    with np.errstate(all="ignore"):
+        for k, pin in enumerate(BATTERY):
+            try:
+                pin()
+            except (AssertionError, oracle.OracleError, ValueError, FloatingPointError):
+                caught.append(k)
+    assert caught, f"no pin caught the mutant: {name}"
