@@ -1,0 +1,163 @@
+/*
+ * pagedattn.h - C ABI of the GB300 (sm_103a) PagedAttention library (libpagedattn.so).
+ *
+ * The operation is com.microsoft.PagedAttention as stated in the
+ * "com.microsoft.PagedAttention" README ("Description", "Inputs", "Outputs",
+ * "Attributes"): the K/V rows of this step's tokens are written into a block-based
+ * (paged) cache, then each sequence's query rows attend causally, with grouped-query
+ * heads, to that sequence's history read back through block_table.
+ *
+ * Conventions for every entry point:
+ *   - Tensor arguments are DEVICE pointers to dense row-major arrays owned by the
+ *     caller. The library allocates no memory. Floating tensors share one element type
+ *     T (pa_dtype); index tensors are int32. Every T pointer must be 16-byte aligned,
+ *     every int32 pointer 4-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is enqueued
+ *     asynchronously; apart from pa_read_device_error no call synchronises, reads device
+ *     memory back, or allocates, so a call can be captured in a CUDA graph.
+ *   - Argument errors are found on the host before anything is launched and reported as
+ *     PA_ERR_* codes. Inconsistencies that only device data can reveal (a
+ *     cumulative_sequence_length that is not a prefix sum, an out-of-range block or
+ *     slot) never fault: the affected work is skipped and a bit is set in the workspace's
+ *     device error word, which pa_read_device_error returns.
+ *   - Calls that share a workspace must be ordered (same stream, or synchronised).
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_ABI_VERSION 1
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARGUMENT = 1,   /* null/misaligned pointer, inconsistent sizes, key xor value */
+  PA_ERR_UNSUPPORTED = 2,        /* a valid request this build does not implement (head_size, block_size, dtype) */
+  PA_ERR_WORKSPACE_TOO_SMALL = 3,
+  PA_ERR_CUDA = 4                /* a CUDA runtime call or launch failed */
+} pa_status;
+
+typedef enum pa_dtype {
+  PA_FLOAT16 = 0,
+  PA_BFLOAT16 = 1
+} pa_dtype;
+
+/* Bits of the device error word (pa_read_device_error). */
+#define PA_DEVERR_BAD_BATCH 1u  /* cumulative_sequence_length / past_seqlens inconsistent: nothing was computed or written */
+#define PA_DEVERR_BAD_BLOCK 2u  /* a block_table entry of an active page is outside [0, num_blocks): that page read as zeros */
+#define PA_DEVERR_BAD_SLOT 4u   /* a slot (given or derived) is outside [0, num_blocks*block_size) and not -1: write skipped */
+#define PA_DEVERR_TIMEOUT 8u    /* a pipeline wait inside a kernel gave up (results of that work item are undefined) */
+
+/* Routing of sequences to kernels (pa_dims.route). */
+#define PA_ROUTE_AUTO 0          /* q_len * (num_heads / kv_num_heads) <= 16: split-KV decode kernel; else prefill kernel */
+#define PA_ROUTE_ALL_PREFILL 1   /* every sequence on the tcgen05 prefill kernel */
+
+/* Host-side sizes of one invocation. */
+typedef struct pa_dims {
+  int32_t num_tokens;              /* N: rows of query, key, value, output and slot_mapping */
+  int32_t batch_size;              /* B: sequences; cumulative_sequence_length has B + 1 entries */
+  int32_t head_size;               /* 64 or 128 */
+  int32_t num_blocks;              /* pages in each cache */
+  int32_t block_size;              /* tokens per page: a positive multiple of 16 */
+  int32_t max_blocks_per_sequence; /* columns of block_table */
+  int32_t dtype;                   /* pa_dtype of T */
+  int32_t decode_split_keys;       /* 0: automatic; else keys per split-KV decode work item (a multiple of 64) */
+  int32_t route;                   /* PA_ROUTE_* */
+} pa_dims;
+
+/*
+ * Bytes of device workspace pa_paged_attention needs for these sizes (0 on invalid
+ * sizes). Pure host arithmetic; needs no GPU. The workspace holds the device-built work
+ * plan, the split-KV partial results (fp32 output rows and their log-sum-exp) and the
+ * device error word. It must be 256-byte aligned.
+ */
+size_t pa_workspace_size(const pa_dims* dims, int32_t num_heads, int32_t kv_num_heads);
+
+/*
+ * com.microsoft.PagedAttention ("com.microsoft.PagedAttention" README).
+ *
+ *   query        T (N, num_heads*head_size), or (N, (num_heads + 2*kv_num_heads)*head_size)
+ *                holding packed [Q | K | V] rows when key and value are NULL ("Inputs", `query`).
+ *                Within each part the heads are consecutive blocks of head_size.
+ *   key, value   T (N, kv_num_heads*head_size), or both NULL ("Inputs", `key`, `value`).
+ *   key_cache,   T (num_blocks, block_size, kv_num_heads, head_size), updated in place: row
+ *   value_cache  i of key/value is copied to flat slot s = block_id*block_size + offset
+ *                ("Inputs", `key_cache`, `value_cache`; "Outputs": both caches are updated).
+ *   cumulative_sequence_length  int32 (B+1): exclusive prefix sums; sequence b owns rows
+ *                [cum[b], cum[b+1]).
+ *   past_seqlens int32 (B): cached history length of each sequence before this call.
+ *   block_table  int32 (B, max_blocks_per_sequence): logical block -> physical block; it
+ *                defines the read path. Entries past ceil((past+q_len)/block_size) are
+ *                never read.
+ *   slot_mapping int32 (N) or NULL: the slot of each row, -1 = do not write. When NULL the
+ *                slot is derived: p = past_seqlens[b] + j for row j of sequence b,
+ *                s = block_table[b][p / block_size]*block_size + p % block_size.
+ *   num_heads, kv_num_heads  attributes; num_heads % kv_num_heads == 0; query head h
+ *                reads KV head h / (num_heads / kv_num_heads).
+ *   scale        attribute; 0 selects 1/sqrt(head_size) ("Attributes", `scale`).
+ *   output       T (N, num_heads*head_size), must not overlap any input.
+ *
+ * Row j of sequence b attends the keys at logical positions 0 .. past_seqlens[b] + j
+ * (bottom-right causal), all read from the caches after this call's writes. Softmax
+ * and accumulation are fp32; the output is rounded once to T.
+ *
+ * Returns PA_OK once the work is enqueued on `stream`.
+ */
+pa_status pa_paged_attention(const void* query, const void* key, const void* value,
+                             void* key_cache, void* value_cache,
+                             const int32_t* cumulative_sequence_length,
+                             const int32_t* past_seqlens, const int32_t* block_table,
+                             const int32_t* slot_mapping, int32_t num_heads, int32_t kv_num_heads,
+                             float scale, void* output, const pa_dims* dims, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* Stages of pa_paged_attention, in the order they must run. */
+#define PA_STAGE_PLAN 1u        /* device work partitioner: classify sequences, build work lists */
+#define PA_STAGE_CACHE_WRITE 2u /* scatter this step's K/V rows into the caches */
+#define PA_STAGE_PREFILL 4u     /* tcgen05/TMEM attention for prefill-class sequences */
+#define PA_STAGE_DECODE 8u      /* split-KV attention for decode-class sequences */
+#define PA_STAGE_MERGE 16u      /* deterministic (out, lse) merge of decode splits */
+#define PA_STAGE_ALL 31u
+
+/*
+ * Same arguments as pa_paged_attention; runs only the stages in `stages` (PA_STAGE_*
+ * bits), in the order above. A stage reads what earlier stages left in the workspace,
+ * so a caller that splits a call across several pa_paged_attention_stages calls must
+ * pass the same arguments and workspace to each and keep them in stage order. Used to
+ * time or test one kernel at a time. Otherwise identical to pa_paged_attention.
+ */
+pa_status pa_paged_attention_stages(const void* query, const void* key, const void* value,
+                                    void* key_cache, void* value_cache,
+                                    const int32_t* cumulative_sequence_length,
+                                    const int32_t* past_seqlens, const int32_t* block_table,
+                                    const int32_t* slot_mapping, int32_t num_heads,
+                                    int32_t kv_num_heads, float scale, void* output,
+                                    const pa_dims* dims, void* workspace, size_t workspace_bytes,
+                                    void* stream, uint32_t stages);
+
+/* Static description of a status code. Never NULL. */
+const char* pa_status_string(pa_status status);
+
+/*
+ * Debug/test helper: waits for `stream`, copies the workspace's device error word
+ * (PA_DEVERR_* bits, accumulated since the workspace was last cleared) into
+ * *error_bits, then clears it. This is the only entry point that synchronises.
+ */
+pa_status pa_read_device_error(void* workspace, void* stream, uint32_t* error_bits);
+
+/* Number of kernels this library has launched in this process (monotonic). */
+uint64_t pa_kernel_launch_count(void);
+
+/* PA_ABI_VERSION of the loaded library. */
+int32_t pa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

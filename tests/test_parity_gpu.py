@@ -1,0 +1,203 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle.
+
+Caches must match bit for bit (the write is a copy); outputs must satisfy
+|gpu - oracle| <= 2e-3 + 1e-2 |oracle| elementwise, the oracle taken in fp64 before
+rounding. Small cases are checked in full; the full-size workloads on every cache byte
+and on sampled output rows that the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import varlen_paged_kv_gb300 as pa
+import workloads as w
+from gpu_utils import assert_close, bits_of, make_workspace, run_gpu, upload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA is required for the gpu tests")
+    from varlen_paged_kv_gb300 import build
+    build.build()
+
+
+def check(p, **opts):
+    ref = oracle.paged_attention(p)
+    r = run_gpu(p, **opts)
+    assert r["err"] == 0, f"device error bits {r['err']}"
+    assert np.array_equal(r["key_cache"], ref["key_cache"]), "key cache differs"
+    assert np.array_equal(r["value_cache"], ref["value_cache"]), "value cache differs"
+    N, nh, hs = p.num_tokens, p.num_heads, p.head_size
+    assert_close(r["out_bits"].reshape(N, nh, hs), ref["out"], p.dtype, p.name)
+    return r, ref
+
+
+# ---- the tiny workload ----------------------------------------------------------------
+
+def test_tiny_workload_auto_route():
+    check(w.config(1))
+
+
+def test_tiny_workload_on_the_prefill_kernel():
+    check(w.config(1), route=pa.ROUTE_ALL_PREFILL)
+
+
+def test_tiny_workload_forced_splits():
+    check(w.config(1), decode_split_keys=64)
+
+
+# ---- shapes spanning tiles, ragged tails, page sizes and routes --------------------------
+
+CASES = {
+    # name: (dtype, nh, kvh, hs, bs, past, q_lens, packed, explicit_slots_with_drops)
+    "decode-single-split": ("fp16", 32, 8, 128, 256, [0, 5, 300, 1000], [1, 1, 1, 1], False, 0),
+    "decode-q-up-to-4": ("bf16", 32, 8, 128, 16, [4000, 0, 17], [1, 3, 4], False, 0),
+    "decode-mha-q16": ("fp16", 8, 8, 64, 32, [100, 33], [16, 7], False, 0),
+    "decode-gqa16": ("bf16", 16, 1, 128, 64, [500, 1], [1, 1], False, 0),
+    "prefill-ragged": ("bf16", 32, 8, 128, 256, [0, 0], [300, 129], False, 0),
+    "chunked-prefill": ("fp16", 32, 8, 128, 256, [1000, 17, 255], [200, 64, 513], False, 0),
+    "mixed-packed-drops": ("fp16", 32, 8, 128, 256, [0, 900, 50, 3000], [130, 1, 40, 2], True, 9),
+    "head64-pages16": ("fp16", 4, 2, 64, 16, [0, 5, 20, 100], [70, 3, 7, 1], False, 0),
+    "pages48": ("bf16", 8, 2, 128, 48, [100, 0], [50, 1], False, 0),
+    "pages512": ("fp16", 16, 4, 128, 512, [700], [300], False, 0),
+    "empty-sequences": ("fp16", 8, 2, 128, 32, [5, 0, 10, 7], [0, 9, 0, 1], False, 0),
+    "gqa8-q2": ("bf16", 32, 4, 128, 16, [60], [2], False, 0),
+    "rows-over-16-go-prefill": ("fp16", 32, 8, 128, 32, [40], [5], True, 0),
+    "bf16-long-history-chunk": ("bf16", 8, 2, 128, 128, [2500], [257], False, 0),
+}
+
+
+def _case(name, seed=7):
+    dt, nh, kvh, hs, bs, past, q, packed, drops = CASES[name]
+    return w.make_problem(name=name, seed=seed, dtype=dt, num_heads=nh, kv_num_heads=kvh, head_size=hs,
+                          block_size=bs, past=past, q_lens=q, packed=packed,
+                          slot_mode="explicit" if drops else "omitted", drop_count=drops, num_blocks=None)
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_cases_auto_route(name):
+    check(_case(name))
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_cases_prefill_route(name):
+    check(_case(name), route=pa.ROUTE_ALL_PREFILL)
+
+
+@pytest.mark.parametrize("split", [64, 128, 448])
+@pytest.mark.parametrize("name", ["decode-q-up-to-4", "decode-single-split", "decode-gqa16", "mixed-packed-drops"])
+def test_decode_split_lengths(name, split):
+    check(_case(name), decode_split_keys=split)
+
+
+def test_scale_attribute_including_negative():
+    for scale in (0.05, -0.3):
+        p = _case("chunked-prefill")
+        p.scale = scale
+        check(p)
+        p = _case("decode-q-up-to-4")
+        p.scale = scale
+        check(p)
+
+
+# ---- invariants on the GPU ------------------------------------------------------------------
+
+def test_bitwise_deterministic():
+    for name in ("mixed-packed-drops", "chunked-prefill"):
+        p = _case(name)
+        a = run_gpu(p, decode_split_keys=128)
+        b = run_gpu(p, decode_split_keys=128)
+        assert np.array_equal(a["out_bits"], b["out_bits"])
+
+
+def test_physical_page_permutation_is_bitwise_invisible():
+    p = _case("chunked-prefill")
+    perm = np.random.default_rng(3).permutation(p.num_blocks)
+    q = p.copy()
+    q.key_cache = np.empty_like(p.key_cache)
+    q.value_cache = np.empty_like(p.value_cache)
+    q.key_cache[perm] = p.key_cache
+    q.value_cache[perm] = p.value_cache
+    q.block_table = np.where(p.block_table >= 0, perm[np.maximum(p.block_table, 0)], -1).astype(np.int32)
+    a = run_gpu(p)
+    b = run_gpu(q)
+    assert np.array_equal(a["out_bits"], b["out_bits"])
+
+
+def test_packed_qkv_bitwise_equals_separate():
+    p = _case("chunked-prefill")
+    q = p.copy()
+    q.query = np.concatenate([p.query, p.key, p.value], axis=1)
+    q.key = q.value = None
+    a = run_gpu(p)
+    b = run_gpu(q)
+    assert np.array_equal(a["out_bits"], b["out_bits"])
+    assert np.array_equal(a["key_cache"], b["key_cache"]) and np.array_equal(a["value_cache"], b["value_cache"])
+
+
+def test_single_token_without_history_returns_its_own_v_bitwise():
+    p = w.make_problem(name="t", seed=5, dtype="bf16", num_heads=8, kv_num_heads=2, head_size=128, block_size=16,
+                       past=[0, 0, 0], q_lens=[1, 1, 1])
+    for route in (pa.ROUTE_AUTO, pa.ROUTE_ALL_PREFILL):
+        r = run_gpu(p, route=route)
+        out = r["out_bits"].reshape(3, 8, 128)
+        v = p.value.reshape(3, 2, 128)
+        for h in range(8):
+            assert np.array_equal(out[:, h], v[:, h // 4])
+
+
+# ---- full-size workloads: every cache byte, sampled output rows ------------------------------
+
+def _sample_rows(p, n, seed):
+    rng = np.random.default_rng(seed)
+    toks = rng.integers(0, p.num_tokens, n)
+    # always include each sequence's first and last row
+    cum = p.cumulative_sequence_length
+    firsts = [cum[b] for b in range(p.batch_size) if cum[b + 1] > cum[b]]
+    lasts = [cum[b + 1] - 1 for b in range(p.batch_size) if cum[b + 1] > cum[b]]
+    toks = np.concatenate([toks, firsts, lasts]).astype(np.int32)
+    heads = rng.integers(0, p.num_heads, toks.shape[0]).astype(np.int32)
+    return toks, heads
+
+
+@pytest.mark.parametrize("k", [2, 3, 4, 5])
+def test_full_size_workload(k):
+    p = w.config(k)
+    kc, vc = oracle.scatter(p)
+    r = run_gpu(p)
+    assert r["err"] == 0
+    assert np.array_equal(r["key_cache"], kc) and np.array_equal(r["value_cache"], vc)
+    toks, heads = _sample_rows(p, 96, k)
+    ref, _ = oracle.attention_rows(p, kc, vc, toks, heads)
+    got = r["out_bits"].reshape(p.num_tokens, p.num_heads, p.head_size)[toks, heads]
+    assert_close(got, ref, p.dtype, p.name)
+
+
+# ---- device-side error reporting (no faults) ----------------------------------------------------
+
+def test_out_of_range_block_is_reported_and_read_as_zeros():
+    p = _case("decode-q-up-to-4")
+    p.block_table = p.block_table.copy()
+    p.block_table[0, 0] = 10 ** 6
+    r = run_gpu(p)
+    assert r["err"] & pa.DEVERR_BAD_BLOCK
+
+
+def test_inconsistent_batch_is_refused_without_writes():
+    p = _case("chunked-prefill")
+    p.cumulative_sequence_length = p.cumulative_sequence_length.copy()
+    p.cumulative_sequence_length[-1] -= 1  # does not end at num_tokens
+    d = upload(p)
+    before = bits_of(d["key_cache"]).copy()
+    ws = make_workspace(p)
+    out = torch.full((p.num_tokens, p.num_heads * p.head_size), 7.0, dtype=d["query"].dtype, device="cuda")
+    pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
+                       d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], None,
+                       num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, output=out, workspace=ws)
+    assert pa.read_device_error(ws) & pa.DEVERR_BAD_BATCH
+    assert np.array_equal(bits_of(d["key_cache"]), before)
+    assert torch.all(out == 7.0)

@@ -1,0 +1,278 @@
+// C ABI of the library (include/pagedattn.h): argument checks, workspace carving, TMA
+// tensor-map encoding and the launch sequence plan -> cache write -> prefill -> decode ->
+// merge on the caller's stream. No allocation, no host/device synchronisation.
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D map over a cache viewed as (head_size, kv_heads, slots); box = 64 x 1 x rows, 128B swizzle
+bool cache_map(CUtensorMap* m, void* base, pa_dtype dt, int hs, int kvh, int64_t slots, int rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)hs, (cuuint64_t)kvh, (cuuint64_t)slots};
+  cuuint64_t strides[2] = {(cuuint64_t)hs * 2, (cuuint64_t)kvh * hs * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, dt == PA_BFLOAT16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims,
+             strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D map over the query rows (row width in elements, rows); box = 64 x 128, 128B swizzle
+bool query_map(CUtensorMap* m, const void* base, pa_dtype dt, int64_t width, int64_t rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)width * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)pa::kPreTileQ};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, dt == PA_BFLOAT16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+             const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int gcd(int a, int b) {
+  while (b) {
+    int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+struct DeviceInfo {
+  int dev = 0;
+  int sms = 0;
+};
+
+bool device_info(DeviceInfo* info) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  static std::mutex mu;
+  static int cached_sms[64] = {0};
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 64) return false;
+  if (!cached_sms[dev]) {
+    if (cudaDeviceGetAttribute(&cached_sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+  }
+  info->dev = dev;
+  info->sms = cached_sms[dev];
+  return true;
+}
+
+// Sizes-only validation (no pointers, no CUDA calls).
+pa_status check_dims(const pa_dims* d, int32_t nh, int32_t kvh) {
+  if (!d) return PA_ERR_INVALID_ARGUMENT;
+  if (d->num_tokens < 0 || d->batch_size < 0 || d->num_blocks < 0 || d->max_blocks_per_sequence < 0)
+    return PA_ERR_INVALID_ARGUMENT;
+  if (d->num_tokens > 0 && d->batch_size == 0) return PA_ERR_INVALID_ARGUMENT;
+  if (nh <= 0 || kvh <= 0 || nh % kvh != 0) return PA_ERR_INVALID_ARGUMENT;
+  if (d->block_size <= 0 || d->head_size <= 0) return PA_ERR_INVALID_ARGUMENT;
+  if (d->dtype != PA_FLOAT16 && d->dtype != PA_BFLOAT16) return PA_ERR_UNSUPPORTED;
+  if (d->head_size != 64 && d->head_size != 128) return PA_ERR_UNSUPPORTED;
+  if (d->block_size % 16 != 0) return PA_ERR_UNSUPPORTED;
+  if (d->route != PA_ROUTE_AUTO && d->route != PA_ROUTE_ALL_PREFILL) return PA_ERR_INVALID_ARGUMENT;
+  if (d->decode_split_keys < 0 || d->decode_split_keys % pa::kDecTile != 0) return PA_ERR_INVALID_ARGUMENT;
+  if ((int64_t)d->num_blocks * d->block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if ((int64_t)d->max_blocks_per_sequence * d->block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if ((int64_t)nh * d->head_size > 65536 || kvh > 65536) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+pa_status launch_all(const pa::Args& args, const pa_dims* d, const void* query, void* kc, void* vc, uint32_t stages,
+                     cudaStream_t stream) {
+  DeviceInfo info;
+  if (!device_info(&info)) return PA_ERR_CUDA;
+  const pa_dtype dt = (pa_dtype)d->dtype;
+  const bool bf16 = dt == PA_BFLOAT16;
+  const int hs = args.hs;
+  const int64_t slots = (int64_t)d->num_blocks * d->block_size;
+
+  if (stages & PA_STAGE_PLAN) {
+    ++g_launches;
+    if (pa::launch_plan(args, stream) != cudaSuccess) return PA_ERR_CUDA;
+  }
+  if ((stages & PA_STAGE_CACHE_WRITE) && args.N > 0) {
+    const int64_t work = (int64_t)args.N * 2 * (args.kv_row / 8);
+    const int64_t blocks = std::min<int64_t>((work + 255) / 256, (int64_t)info.sms * 16);
+    ++g_launches;
+    if (pa::launch_cache_write(args, (int)blocks, stream) != cudaSuccess) return PA_ERR_CUDA;
+  }
+  const bool can_decode = d->route == PA_ROUTE_AUTO;
+  if ((stages & PA_STAGE_PREFILL) && args.N > 0 && slots > 0) {
+    const int seg = gcd(d->block_size, pa::kPreTileK);
+    CUtensorMap tq, tk, tv;
+    if (!query_map(&tq, query, dt, args.q_stride, args.N) || !cache_map(&tk, kc, dt, hs, args.kvh, slots, seg) ||
+        !cache_map(&tv, vc, dt, hs, args.kvh, slots, seg))
+      return PA_ERR_CUDA;
+    const int grid = (int)std::min<int64_t>((int64_t)args.max_tiles * args.nh, info.sms);
+    if (grid > 0) {
+      ++g_launches;
+      if (pa::launch_prefill(args, bf16, tq, tk, tv, seg, grid, stream) != cudaSuccess) return PA_ERR_CUDA;
+    }
+  }
+  if ((stages & PA_STAGE_DECODE) && can_decode && args.N > 0 && slots > 0) {
+    const int seg = gcd(d->block_size, pa::kDecTile);
+    CUtensorMap tk, tv;
+    if (!cache_map(&tk, kc, dt, hs, args.kvh, slots, seg) || !cache_map(&tv, vc, dt, hs, args.kvh, slots, seg))
+      return PA_ERR_CUDA;
+    const int grid = (int)std::min<int64_t>(args.max_items, 2 * info.sms);
+    if (grid > 0) {
+      ++g_launches;
+      if (pa::launch_decode(args, bf16, tk, tv, seg, grid, stream) != cudaSuccess) return PA_ERR_CUDA;
+    }
+  }
+  if ((stages & PA_STAGE_MERGE) && can_decode && args.N > 0 && args.max_merge > 0) {
+    const int64_t warps = (int64_t)args.max_merge * args.nh;
+    const int grid = (int)std::min<int64_t>((warps + 3) / 4, (int64_t)info.sms * 8);
+    ++g_launches;
+    if (pa::launch_merge(args, bf16, grid, stream) != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pa_workspace_size(const pa_dims* dims, int32_t num_heads, int32_t kv_num_heads) {
+  if (check_dims(dims, num_heads, kv_num_heads) != PA_OK) return 0;
+  return pa::ws_layout(dims->num_tokens, dims->batch_size, kv_num_heads, dims->head_size,
+                       dims->max_blocks_per_sequence, dims->block_size, dims->decode_split_keys)
+      .total;
+}
+
+pa_status pa_paged_attention_stages(const void* query, const void* key, const void* value, void* key_cache,
+                                    void* value_cache, const int32_t* cumulative_sequence_length,
+                                    const int32_t* past_seqlens, const int32_t* block_table,
+                                    const int32_t* slot_mapping, int32_t num_heads, int32_t kv_num_heads, float scale,
+                                    void* output, const pa_dims* dims, void* workspace, size_t workspace_bytes,
+                                    void* stream, uint32_t stages) {
+  pa_status st = check_dims(dims, num_heads, kv_num_heads);
+  if (st != PA_OK) return st;
+  if ((key == nullptr) != (value == nullptr)) return PA_ERR_INVALID_ARGUMENT;
+  if (stages & ~PA_STAGE_ALL) return PA_ERR_INVALID_ARGUMENT;
+  const int32_t N = dims->num_tokens, B = dims->batch_size, hs = dims->head_size;
+  if (N == 0) return PA_OK;  // no rows: nothing is written or read
+  if (!query || !key_cache || !value_cache || !cumulative_sequence_length || !past_seqlens || !block_table ||
+      !output || !workspace)
+    return PA_ERR_INVALID_ARGUMENT;
+  if (!aligned(query, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) || !aligned(output, 16) ||
+      (key && (!aligned(key, 16) || !aligned(value, 16))) || !aligned(cumulative_sequence_length, 4) ||
+      !aligned(past_seqlens, 4) || !aligned(block_table, 4) || (slot_mapping && !aligned(slot_mapping, 4)) ||
+      !aligned(workspace, 256))
+    return PA_ERR_INVALID_ARGUMENT;
+  if (dims->max_blocks_per_sequence == 0 || dims->num_blocks == 0) return PA_ERR_INVALID_ARGUMENT;
+  const pa::WsLayout L = pa::ws_layout(N, B, kv_num_heads, hs, dims->max_blocks_per_sequence, dims->block_size,
+                                       dims->decode_split_keys);
+  if (workspace_bytes < L.total) return PA_ERR_WORKSPACE_TOO_SMALL;
+
+  pa::Args a{};
+  a.query = query;
+  a.key = key;
+  a.value = value;
+  a.key_cache = key_cache;
+  a.value_cache = value_cache;
+  a.cum = cumulative_sequence_length;
+  a.past = past_seqlens;
+  a.block_table = block_table;
+  a.slot_mapping = slot_mapping;
+  a.output = output;
+  a.N = N;
+  a.B = B;
+  a.nh = num_heads;
+  a.kvh = kv_num_heads;
+  a.G = num_heads / kv_num_heads;
+  a.hs = hs;
+  a.num_blocks = dims->num_blocks;
+  a.bs = dims->block_size;
+  a.max_blocks = dims->max_blocks_per_sequence;
+  a.packed = key == nullptr;
+  a.kv_row = kv_num_heads * hs;
+  a.q_stride = a.packed ? (num_heads + 2 * kv_num_heads) * hs : num_heads * hs;
+  a.k_offset = a.packed ? num_heads * hs : 0;
+  a.v_offset = a.packed ? (num_heads + kv_num_heads) * hs : 0;
+  a.forced_split = dims->decode_split_keys;
+  a.route = dims->route;
+  const float sc = scale == 0.0f ? 1.0f / sqrtf((float)hs) : scale;
+  a.scale_log2 = sc * 1.4426950408889634f;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.hdr = reinterpret_cast<pa::WsHeader*>(ws + L.header);
+  a.items = reinterpret_cast<pa::DecodeItem*>(ws + L.items);
+  a.tiles = reinterpret_cast<pa::PrefillTile*>(ws + L.tiles);
+  a.tiles_unsorted = reinterpret_cast<pa::PrefillTile*>(ws + L.tiles_unsorted);
+  a.merge = reinterpret_cast<pa::MergeRow*>(ws + L.merge);
+  a.part_o = reinterpret_cast<float*>(ws + L.part_o);
+  a.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
+  a.max_items = L.max_items;
+  a.max_tiles = L.max_tiles;
+  a.max_merge = L.max_merge;
+
+  return launch_all(a, dims, query, key_cache, value_cache, stages, static_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_paged_attention(const void* query, const void* key, const void* value, void* key_cache,
+                             void* value_cache, const int32_t* cumulative_sequence_length,
+                             const int32_t* past_seqlens, const int32_t* block_table, const int32_t* slot_mapping,
+                             int32_t num_heads, int32_t kv_num_heads, float scale, void* output,
+                             const pa_dims* dims, void* workspace, size_t workspace_bytes, void* stream) {
+  return pa_paged_attention_stages(query, key, value, key_cache, value_cache, cumulative_sequence_length,
+                                   past_seqlens, block_table, slot_mapping, num_heads, kv_num_heads, scale, output,
+                                   dims, workspace, workspace_bytes, stream, PA_STAGE_ALL);
+}
+
+const char* pa_status_string(pa_status status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case PA_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+pa_status pa_read_device_error(void* workspace, void* stream, uint32_t* error_bits) {
+  if (!workspace || !error_bits) return PA_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaMemset(workspace, 0, sizeof(v)) != cudaSuccess) return PA_ERR_CUDA;
+  *error_bits = v;
+  return PA_OK;
+}
+
+uint64_t pa_kernel_launch_count(void) { return g_launches.load(); }
+
+int32_t pa_abi_version(void) { return PA_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,394 @@
+// Shared definitions of the GB300 PagedAttention kernels: workspace layout, work-item
+// records, and inline-PTX wrappers for mbarrier, TMA (cp.async.bulk.tensor), tcgen05
+// (TMEM allocation, MMA, loads/stores) and the warp-level ldmatrix / mma.sync used by
+// the decode kernel.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pagedattn.h"
+
+namespace pa {
+
+// ---- tiling constants ---------------------------------------------------------------
+constexpr int kDecTile = 64;          // keys per decode pipeline stage
+constexpr int kDecStages = 3;         // decode K/V ring depth
+constexpr int kDecWarps = 4;          // decode consumer warps (16 keys of a tile each)
+constexpr int kDecRows = 16;          // query rows per decode work item (one m16 MMA tile)
+constexpr int kDecTargetCtas = 1024;  // decode work items aimed for when splits are automatic
+constexpr int kDecMinSplit = 256;     // smallest automatic split, keys
+constexpr int kPreTileQ = 128;        // query rows per prefill tile (MMA M)
+constexpr int kPreTileK = 128;        // keys per prefill KV tile (MMA N of Q K^T, K of P V)
+constexpr int kSortCap = 4096;        // prefill tiles the planner sorts by cost
+
+// ---- workspace records ----------------------------------------------------------------
+struct WsHeader {
+  uint32_t error;           // PA_DEVERR_* bits
+  int32_t valid;            // 1 when the planner accepted the batch
+  int32_t n_decode_items;
+  int32_t n_prefill_tiles;
+  int32_t n_merge_rows;
+  int32_t split_keys;
+  int32_t pad[58];
+};
+static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
+
+struct DecodeItem {     // one (sequence, KV head, key range) of a decode-class sequence
+  int32_t b, g, key_begin, key_end;
+  int32_t partial;      // partial-result slot, or -1 when this item is the whole sequence
+  int32_t n_split;
+  int32_t pad[2];
+};
+
+struct PrefillTile {    // 128 query rows [j0, j0+128) of sequence b (all heads)
+  int32_t b, j0;
+};
+
+struct MergeRow {       // a decode-class query row whose splits need merging
+  int32_t token, b;
+  int32_t first_item;   // item of (b, KV head 0, split 0); head g's splits start at first_item + g*n_split
+  int32_t n_split;
+};
+
+struct WsLayout {
+  size_t header, items, tiles, tiles_unsorted, merge, part_o, part_lse, total;
+  int32_t max_items, max_tiles, max_merge;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+__host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Upper bounds of the device-built lists, from host-known sizes only.
+//  - decode pairs (sequence, split): automatic splits are >= total_keys / target_pairs,
+//    so sum_b ceil(kv_b / split) <= target_pairs + B; forced splits give at most
+//    ceil(max_kv / split) per sequence;
+//  - prefill tiles: sum_b ceil(q_b / 128) <= N / 128 + B;
+//  - merge rows: decode-class sequences have q_len <= 16.
+__host__ __device__ inline WsLayout ws_layout(int32_t N, int32_t B, int32_t kvh, int32_t hs,
+                                               int32_t max_blocks, int32_t bs, int32_t forced_split) {
+  WsLayout L;
+  int64_t pairs;
+  if (forced_split > 0) {
+    pairs = (int64_t)B * ceil_div((int64_t)max_blocks * bs, forced_split);
+  } else {
+    pairs = ceil_div(kDecTargetCtas, kvh) + B;
+  }
+  int64_t items = pairs * kvh;
+  int64_t tiles = ceil_div(N, kPreTileQ) + (B < N ? B : N);
+  int64_t merge = (int64_t)N < 16 * (int64_t)B ? N : 16 * (int64_t)B;
+  L.max_items = (int32_t)items;
+  L.max_tiles = (int32_t)tiles;
+  L.max_merge = (int32_t)merge;
+  size_t off = 0;
+  L.header = off; off += sizeof(WsHeader);
+  L.items = off; off = align_up(off + sizeof(DecodeItem) * (size_t)items, 256);
+  L.tiles = off; off = align_up(off + sizeof(PrefillTile) * (size_t)tiles, 256);
+  L.tiles_unsorted = off; off = align_up(off + sizeof(PrefillTile) * (size_t)tiles, 256);
+  L.merge = off; off = align_up(off + sizeof(MergeRow) * (size_t)merge, 256);
+  L.part_o = off; off = align_up(off + sizeof(float) * (size_t)items * kDecRows * hs, 256);
+  L.part_lse = off; off = align_up(off + sizeof(float) * (size_t)items * kDecRows, 256);
+  L.total = off;
+  return L;
+}
+
+// ---- arguments shared by the kernels ----------------------------------------------------
+struct Args {
+  const void* query;
+  const void* key;
+  const void* value;
+  void* key_cache;
+  void* value_cache;
+  const int32_t* cum;
+  const int32_t* past;
+  const int32_t* block_table;
+  const int32_t* slot_mapping;
+  void* output;
+  int32_t N, B, nh, kvh, G, hs, num_blocks, bs, max_blocks;
+  int32_t q_stride;       // elements per query row
+  int32_t kv_row;         // kvh * hs
+  int32_t k_offset;       // element offset of K inside a query row (packed) or 0
+  int32_t v_offset;
+  int32_t packed;
+  int32_t forced_split;
+  int32_t route;
+  float scale_log2;       // scale * log2(e)
+  WsHeader* hdr;
+  DecodeItem* items;
+  PrefillTile* tiles;
+  PrefillTile* tiles_unsorted;
+  MergeRow* merge;
+  float* part_o;
+  float* part_lse;
+  int32_t max_items, max_tiles, max_merge;
+};
+
+// ---- shared-memory layouts (bytes) of the attention kernels --------------------------
+// Decode: a ring of K+V tiles, the warp-combine buffer, per-warp (m, l), barriers.
+template <int HS>
+struct DecSmem {
+  static constexpr int kHalves = HS / 64;
+  static constexpr int kTileBytes = kDecTile * HS * 2;      // one K (or V) tile
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kComb = kDecStages * kStageBytes;     // float [16][HS]
+  static constexpr int kMw = kComb + kDecRows * HS * 4;      // float [4][16]
+  static constexpr int kLw = kMw + kDecWarps * kDecRows * 4; // float [4][16]
+  static constexpr int kBars = kLw + kDecWarps * kDecRows * 4;
+  static constexpr int kAbort = kBars + 2 * kDecStages * 8;
+  static constexpr int kBytes = kAbort + 16 + 1024;          // + alignment slack
+};
+
+// Prefill: Q tile, two K and two V tiles, barriers, the TMEM address slot.
+template <int HS>
+struct PreSmem {
+  static constexpr int kQBytes = kPreTileQ * HS * 2;
+  static constexpr int kKVBytes = kPreTileK * HS * 2;
+  static constexpr int kHalfBytes = kPreTileK * 128;  // one 64-column slab of a tile
+  static constexpr int kQ = 0;
+  static constexpr int kK0 = kQ + kQBytes;
+  static constexpr int kV0 = kK0 + 2 * kKVBytes;
+  static constexpr int kBars = kV0 + 2 * kKVBytes;
+  // barriers: q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_done, o_free
+  static constexpr int kNumBars = 16;
+  static constexpr int kTmemSlot = kBars + kNumBars * 8;
+  static constexpr int kAbort = kTmemSlot + 4;
+  static constexpr int kBytes = kAbort + 12 + 1024;
+};
+
+// ---- host launchers, one per kernel family (defined next to their kernels) -----------------
+cudaError_t launch_plan(const Args& a, cudaStream_t s);
+cudaError_t launch_cache_write(const Args& a, int grid, cudaStream_t s);
+cudaError_t launch_prefill(const Args& a, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, int seg, int grid, cudaStream_t s);
+cudaError_t launch_decode(const Args& a, bool bf16, const CUtensorMap& tk, const CUtensorMap& tv, int seg, int grid,
+                          cudaStream_t s);
+cudaError_t launch_merge(const Args& a, bool bf16, int grid, cudaStream_t s);
+
+// ---- small device helpers -----------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {  // MUFU.EX2 (ex2.approx, flush-to-zero)
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {  // lo -> bits 0..15
+  if constexpr (BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+// ---- mbarrier ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a pipeline wait gives up after ~2 s
+
+// Wait for the phase of parity `parity` to complete, at most ~2 s. On time-out (or when
+// another thread of the CTA already gave up, *abort != 0) it sets *abort and the
+// PA_DEVERR_TIMEOUT bit and returns false; callers then skip their remaining waits so
+// the CTA drains and exits instead of hanging.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        atomicOr(err, PA_DEVERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---- TMA ----------------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                            int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---- warp-level tensor core path (decode) -------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+template <bool BF16>
+__device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  if constexpr (BF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
+// ---- tcgen05 (5th-generation tensor cores, tensor memory) ------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {  // whole warp
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {  // whole warp
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {  // whole warp
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Arrive on `bar` once every tcgen05.mma this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+// D[tmem] (+)= A[smem desc] * B[smem desc]
+__device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc]
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor for a 128-byte-swizzled operand (the layout TMA writes
+// with CU_TENSOR_MAP_SWIZZLE_128B: rows of 128 bytes, 16-byte chunks XOR-permuted by row % 8,
+// 8-row atoms of 1024 bytes). lbo / sbo are the byte strides between atoms along the
+// leading / strided dimension. Bits: start >> 4 [0,14), lbo >> 4 [16,30), sbo >> 4 [32,46),
+// version 1 at bit 46, layout SWIZZLE_128B (2) at [61,64).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of tcgen05.mma.kind::f16 with fp32 accumulation: D format F32 at
+// bit 4, A/B format (0 f16, 1 bf16) at bits 7 / 10, B major-ness (0 K-major, 1 MN-major) at
+// bit 16, N >> 3 at bits [17,23), M >> 4 at bits [24,29).
+__host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool b_mn_major) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// tcgen05.ld 32x32b.x32: this thread's TMEM lane, 32 consecutive 32-bit columns from taddr;
+// the wait is in the same asm so the registers are valid when it returns.
+__device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// tcgen05.ld 32x32b.x64: this thread's TMEM lane, 64 consecutive 32-bit columns from taddr;
+// the wait is in the same asm so the registers are valid when it returns.
+__device__ __forceinline__ void tmem_ld_x64(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+}
+
+// tcgen05.st 32x32b.x32: 32 consecutive 32-bit columns of this thread's TMEM lane; waits for completion.
+__device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n"
+      "tcgen05.wait::st.sync.aligned;\n"
+      :
+      : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+}  // namespace pa

@@ -1,0 +1,398 @@
+// Split-KV decode attention and the deterministic (out, lse) merge.
+//
+// Decode-class sequences have q_len * G <= 16 query rows per KV head, so one work item
+// (sequence b, KV head g, key range) holds all of them in a single 16-row MMA tile:
+// row r = j * G + hq is query row j of the sequence for query head g * G + hq. The
+// operation is memory bound (every K and V element of the history is read once), so the
+// kernel is built around streaming pages:
+//   - one producer warp brings 64-key K and V tiles of the item into a 3-stage shared
+//     memory ring with TMA (a 3-D tensor map over (head_size, kv_heads, slots): one box
+//     per page segment, located through block_table; 128-byte swizzle so ldmatrix reads
+//     are bank-conflict free);
+//   - four consumer warps each take 16 keys of every tile: S = Q K^T and O += P V on the
+//     warp-level tensor cores (mma.sync m16n8k16, fp32 accumulation), with an online
+//     softmax in registers (row max over the quad by shuffles, base-2 exponentials);
+//   - at the end of the item the four warps' (m, l, O) are combined in a fixed order in
+//     shared memory. A single-split item writes the output row rounded once to T; a split
+//     writes its normalised fp32 partial row and its natural-log lse.
+// The merge kernel then combines the splits of a row in split order (the (out, lse)
+// reduction of the WS2 CP-Aware Attention Contract, "Reduction Semantics": fp32, fixed
+// order, downcast at the final write).
+#include "common.cuh"
+
+namespace pa {
+
+__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// combined max and denominator of one row over the four warps' (m, l) (base 2)
+__device__ __forceinline__ void row_stats(const float* mw, const float* lw, int row, float& M, float& L) {
+  M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, mw[w * kDecRows + row]);
+  L = 0.f;
+#pragma unroll
+  for (int w = 0; w < kDecWarps; ++w) {
+    const float m = mw[w * kDecRows + row];
+    if (m != -INFINITY) L += lw[w * kDecRows + row] * fast_exp2(m - M);
+  }
+}
+
+template <int HS, bool BF16>
+__global__ void __launch_bounds__(160, 2)
+    decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const int seg_rows) {
+  using L = DecSmem<HS>;
+  constexpr int NKS = HS / 16;  // k-steps of Q K^T
+  constexpr int ND = HS / 8;    // n-tiles of P V
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  float* comb = reinterpret_cast<float*>(smem + L::kComb);
+  float* mw = reinterpret_cast<float*>(smem + L::kMw);
+  float* lw = reinterpret_cast<float*>(smem + L::kLw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBars);
+  uint64_t* empty = full + kDecStages;
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
+  uint32_t* err = &a.hdr->error;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kDecStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kDecWarps);
+    }
+    *abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int n_items = a.hdr->n_decode_items;
+
+  if (warp == kDecWarps) {
+    // ================= producer warp: TMA page loads =================
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    const int nseg = kDecTile / seg_rows;
+    const int oob = a.num_blocks * a.bs;  // a row coordinate past the end: TMA fills zeros
+    uint32_t cnt = 0;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+      const DecodeItem item = a.items[it];
+      const int kv_len = a.past[item.b] + (a.cum[item.b + 1] - a.cum[item.b]);
+      const int* bt = a.block_table + (int64_t)item.b * a.max_blocks;
+      for (int k0 = item.key_begin; k0 < item.key_end; k0 += kDecTile, ++cnt) {
+        const int s = cnt % kDecStages;
+        const uint32_t ph = (cnt / kDecStages) & 1;
+        if (lane == 0) {
+          mbar_wait(&empty[s], ph ^ 1, abort, err);
+          mbar_arrive_expect_tx(&full[s], L::kStageBytes);
+        }
+        __syncwarp();
+        if (lane < nseg) {
+          const int key = k0 + lane * seg_rows;
+          int z = oob;
+          if (key < kv_len) {
+            const int blk = bt[key / a.bs];
+            if (blk >= 0 && blk < a.num_blocks) z = blk * a.bs + key % a.bs;
+            else atomicOr(err, PA_DEVERR_BAD_BLOCK);
+          }
+          uint8_t* kdst = smem + s * L::kStageBytes + lane * seg_rows * 128;
+#pragma unroll
+          for (int h = 0; h < L::kHalves; ++h) {
+            tma_load_3d(kdst + h * kDecTile * 128, &tmK, &full[s], h * 64, item.g, z);
+            tma_load_3d(kdst + L::kTileBytes + h * kDecTile * 128, &tmV, &full[s], h * 64, item.g, z);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    return;
+  }
+
+  // ================= consumer warps =================
+  const int w = warp;
+  const int tq = lane & 3, gq = lane >> 2;  // quad position, row within the 8-row group
+  const int r0 = gq, r1 = gq + 8;           // the two rows this thread holds in MMA fragments
+  uint32_t cnt = 0;
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const DecodeItem item = a.items[it];
+    const int c0 = a.cum[item.b];
+    const int q_len = a.cum[item.b + 1] - c0;
+    const int past = a.past[item.b];
+    const int n_rows = q_len * a.G;
+
+    // Q fragments (A operand, row-major 16 x HS), straight from global memory
+    uint32_t qa[NKS][4];
+    {
+      const uint16_t* q = reinterpret_cast<const uint16_t*>(a.query);
+      const uint16_t* p0 = nullptr;
+      const uint16_t* p1 = nullptr;
+      if (r0 < n_rows)
+        p0 = q + (int64_t)(c0 + r0 / a.G) * a.q_stride + (int64_t)(item.g * a.G + r0 % a.G) * HS + tq * 2;
+      if (r1 < n_rows)
+        p1 = q + (int64_t)(c0 + r1 / a.G) * a.q_stride + (int64_t)(item.g * a.G + r1 % a.G) * HS + tq * 2;
+#pragma unroll
+      for (int ks = 0; ks < NKS; ++ks) {
+        qa[ks][0] = p0 ? __ldg(reinterpret_cast<const uint32_t*>(p0 + ks * 16)) : 0u;
+        qa[ks][2] = p0 ? __ldg(reinterpret_cast<const uint32_t*>(p0 + ks * 16 + 8)) : 0u;
+        qa[ks][1] = p1 ? __ldg(reinterpret_cast<const uint32_t*>(p1 + ks * 16)) : 0u;
+        qa[ks][3] = p1 ? __ldg(reinterpret_cast<const uint32_t*>(p1 + ks * 16 + 8)) : 0u;
+      }
+    }
+    // causal limits (inclusive) of the two rows; padding rows borrow the last row's
+    const int lim0 = past + min(r0 / a.G, q_len - 1);
+    const int lim1 = past + min(r1 / a.G, q_len - 1);
+
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o[ND][4];
+#pragma unroll
+    for (int d = 0; d < ND; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
+
+    for (int k0 = item.key_begin; k0 < item.key_end; k0 += kDecTile, ++cnt) {
+      const int s = cnt % kDecStages;
+      const uint32_t ph = (cnt / kDecStages) & 1;
+      mbar_wait(&full[s], ph, abort, err);
+      const int kw = k0 + 16 * w;  // first key of this warp's 16
+      if (kw < item.key_end) {
+        const uint32_t kb = smem_u32(smem + s * L::kStageBytes);
+        const uint32_t vb = kb + L::kTileBytes;
+        // ---- S (16 x 16) = Q K^T ----
+        float sc[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+        {
+          const int mi = lane >> 3, rr = lane & 7;
+          const int kr = 16 * w + (mi >> 1) * 8 + rr;  // key row inside the tile
+#pragma unroll
+          for (int ks = 0; ks < NKS; ++ks) {
+            const int c = 2 * ks + (mi & 1);             // 16-byte chunk along head_size
+            const uint32_t addr = kb + (c >> 3) * (kDecTile * 128) + kr * 128 + (((c & 7) ^ (kr & 7)) << 4);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(addr, b0, b1, b2, b3);
+            mma16816<BF16>(sc[0], qa[ks], b0, b1);
+            mma16816<BF16>(sc[1], qa[ks], b2, b3);
+          }
+        }
+        // ---- online softmax (base 2) ----
+        const bool ragged = (k0 + kDecTile > item.key_end) || (k0 + kDecTile - 1 > past);
+        float x[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float v = sc[n][e] * a.scale_log2;
+            if (ragged) {
+              const int key = kw + n * 8 + tq * 2 + (e & 1);
+              const int lim = e < 2 ? lim0 : lim1;
+              if (key >= item.key_end || key > lim) v = -INFINITY;
+            }
+            x[n][e] = v;
+          }
+        }
+        float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+        float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float ms0 = mn0 == -INFINITY ? 0.f : mn0;  // a row with no key yet stays empty
+        const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = fast_exp2(m0 - ms0), al1 = fast_exp2(m1 - ms1);
+        m0 = mn0;
+        m1 = mn1;
+        float p[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          p[n][0] = fast_exp2(x[n][0] - ms0);
+          p[n][1] = fast_exp2(x[n][1] - ms0);
+          p[n][2] = fast_exp2(x[n][2] - ms1);
+          p[n][3] = fast_exp2(x[n][3] - ms1);
+        }
+        l0 = l0 * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+        l1 = l1 * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+        uint32_t pa[4];
+        pa[0] = pack2<BF16>(p[0][0], p[0][1]);
+        pa[1] = pack2<BF16>(p[0][2], p[0][3]);
+        pa[2] = pack2<BF16>(p[1][0], p[1][1]);
+        pa[3] = pack2<BF16>(p[1][2], p[1][3]);
+#pragma unroll
+        for (int d = 0; d < ND; ++d) {
+          o[d][0] *= al0;
+          o[d][1] *= al0;
+          o[d][2] *= al1;
+          o[d][3] *= al1;
+        }
+        // ---- O (16 x HS) += P (16 x 16) V (16 x HS) ----
+        // keys this thread contributes in the transposed V fragments: kw + 2tq + {0,1}, +8
+        uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
+        if (ragged) {  // keys past the item may be unwritten cache slots: keep NaN out of 0 * V
+          const int ka = kw + tq * 2, kb2 = ka + 8;
+          vmask_lo = (ka < item.key_end ? 0x0000ffffu : 0u) | (ka + 1 < item.key_end ? 0xffff0000u : 0u);
+          vmask_hi = (kb2 < item.key_end ? 0x0000ffffu : 0u) | (kb2 + 1 < item.key_end ? 0xffff0000u : 0u);
+        }
+        {
+          const int mi = lane >> 3, rr = lane & 7;
+          const int kr = 16 * w + (mi & 1) * 8 + rr;
+#pragma unroll
+          for (int dp = 0; dp < ND / 2; ++dp) {
+            const int c = 2 * dp + (mi >> 1);
+            const uint32_t addr = vb + (c >> 3) * (kDecTile * 128) + kr * 128 + (((c & 7) ^ (kr & 7)) << 4);
+            uint32_t v0, v1, v2, v3;
+            ldsm_x4_t(addr, v0, v1, v2, v3);
+            v0 &= vmask_lo;
+            v2 &= vmask_lo;
+            v1 &= vmask_hi;
+            v3 &= vmask_hi;
+            mma16816<BF16>(o[2 * dp], pa, v0, v1);
+            mma16816<BF16>(o[2 * dp + 1], pa, v2, v3);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+
+    // ---- combine the four warps' partial states in a fixed order ----
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    if (tq == 0) {
+      mw[w * kDecRows + r0] = m0;
+      mw[w * kDecRows + r1] = m1;
+      lw[w * kDecRows + r0] = l0;
+      lw[w * kDecRows + r1] = l1;
+    }
+    consumer_bar();
+    float M0, L0, M1, L1;
+    row_stats(mw, lw, r0, M0, L0);
+    row_stats(mw, lw, r1, M1, L1);
+    const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M0);
+    const float f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M1);
+#pragma unroll 1
+    for (int ww = 0; ww < kDecWarps; ++ww) {
+      if (w == ww) {
+#pragma unroll
+        for (int d = 0; d < ND; ++d) {
+          float* c0p = comb + r0 * HS + d * 8 + tq * 2;
+          float* c1p = comb + r1 * HS + d * 8 + tq * 2;
+          if (ww == 0) {
+            c0p[0] = o[d][0] * f0;
+            c0p[1] = o[d][1] * f0;
+            c1p[0] = o[d][2] * f1;
+            c1p[1] = o[d][3] * f1;
+          } else {
+            c0p[0] += o[d][0] * f0;
+            c0p[1] += o[d][1] * f0;
+            c1p[0] += o[d][2] * f1;
+            c1p[1] += o[d][3] * f1;
+          }
+        }
+      }
+      consumer_bar();
+    }
+    // ---- write: thread t owns row t / 8, HS / 8 consecutive columns ----
+    {
+      const int t = threadIdx.x;  // 0..127
+      const int row = t >> 3;
+      constexpr int CW = HS / 8;
+      const int col = (t & 7) * CW;
+      if (row < n_rows) {
+        float M, Lr;
+        row_stats(mw, lw, row, M, Lr);
+        const float inv = Lr > 0.f ? 1.f / Lr : 0.f;
+        const float* src = comb + row * HS + col;
+        if (item.partial < 0) {
+          const int tok = c0 + row / a.G;
+          const int head = item.g * a.G + row % a.G;
+          uint16_t* dst = reinterpret_cast<uint16_t*>(a.output) + ((int64_t)tok * a.nh + head) * HS + col;
+#pragma unroll
+          for (int v = 0; v < CW; v += 8) {
+            uint4 pk;
+            pk.x = pack2<BF16>(src[v + 0] * inv, src[v + 1] * inv);
+            pk.y = pack2<BF16>(src[v + 2] * inv, src[v + 3] * inv);
+            pk.z = pack2<BF16>(src[v + 4] * inv, src[v + 5] * inv);
+            pk.w = pack2<BF16>(src[v + 6] * inv, src[v + 7] * inv);
+            *reinterpret_cast<uint4*>(dst + v) = pk;
+          }
+        } else {
+          float* dst = a.part_o + ((int64_t)item.partial * kDecRows + row) * HS + col;
+#pragma unroll
+          for (int v = 0; v < CW; v += 4)
+            *reinterpret_cast<float4*>(dst + v) =
+                make_float4(src[v] * inv, src[v + 1] * inv, src[v + 2] * inv, src[v + 3] * inv);
+          if ((t & 7) == 0)
+            a.part_lse[(int64_t)item.partial * kDecRows + row] =
+                Lr > 0.f ? (M + fast_log2(Lr)) * 0.69314718055994531f : -INFINITY;
+        }
+      }
+    }
+    consumer_bar();  // comb, mw, lw are reused by the next item
+  }
+}
+
+// One warp per (merged row, query head): lse-weighted mean of the splits' partial rows,
+// splits taken in order, fp32, rounded once to T.
+template <int HS, bool BF16>
+__global__ void __launch_bounds__(128) merge_kernel(const Args a) {
+  const int n_tasks = a.hdr->n_merge_rows * a.nh;
+  const int lane = threadIdx.x & 31;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  constexpr int PER = HS / 32;
+  for (int task = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < n_tasks; task += nwarps) {
+    const MergeRow mr = a.merge[task / a.nh];
+    const int h = task % a.nh;
+    const int g = h / a.G, hq = h % a.G;
+    const int row = (mr.token - a.cum[mr.b]) * a.G + hq;
+    const int first = mr.first_item + g * mr.n_split;
+    float M = -INFINITY;
+    for (int s = 0; s < mr.n_split; ++s) M = fmaxf(M, a.part_lse[(int64_t)(first + s) * kDecRows + row]);
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    float den = 0.f;
+    for (int s = 0; s < mr.n_split; ++s) {
+      const int64_t pr = (int64_t)(first + s) * kDecRows + row;
+      const float lse = a.part_lse[pr];
+      const float wgt = lse == -INFINITY ? 0.f : fast_exp2((lse - M) * 1.4426950408889634f);
+      den += wgt;
+      const float* src = a.part_o + pr * HS + lane * PER;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] += wgt * src[e];
+    }
+    const float inv = 1.f / den;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(a.output) + ((int64_t)mr.token * a.nh + h) * HS + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = pack2<BF16>(acc[e] * inv, acc[e + 1] * inv);
+  }
+}
+
+// ---- host launchers (kernels are launched from the translation unit that defines them) ----
+template <int HS, bool BF16>
+static cudaError_t launch_decode_t(const Args& a, const CUtensorMap& tk, const CUtensorMap& tv, int seg, int grid,
+                                   cudaStream_t s) {
+  constexpr int smem = DecSmem<HS>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<HS, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  decode_kernel<HS, BF16><<<grid, 160, smem, s>>>(a, tk, tv, seg);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const Args& a, bool bf16, const CUtensorMap& tk, const CUtensorMap& tv, int seg, int grid,
+                          cudaStream_t s) {
+  if (a.hs == 64) return bf16 ? launch_decode_t<64, true>(a, tk, tv, seg, grid, s) : launch_decode_t<64, false>(a, tk, tv, seg, grid, s);
+  return bf16 ? launch_decode_t<128, true>(a, tk, tv, seg, grid, s) : launch_decode_t<128, false>(a, tk, tv, seg, grid, s);
+}
+
+cudaError_t launch_merge(const Args& a, bool bf16, int grid, cudaStream_t s) {
+  if (a.hs == 64) {
+    if (bf16) merge_kernel<64, true><<<grid, 128, 0, s>>>(a);
+    else merge_kernel<64, false><<<grid, 128, 0, s>>>(a);
+  } else {
+    if (bf16) merge_kernel<128, true><<<grid, 128, 0, s>>>(a);
+    else merge_kernel<128, false><<<grid, 128, 0, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pa

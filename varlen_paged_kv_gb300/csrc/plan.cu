@@ -1,0 +1,295 @@
+// Device work partitioner. One CTA reads cumulative_sequence_length and past_seqlens
+// (which stay on the device: the host never sees them) and writes the work lists the
+// attention kernels consume:
+//   - decode-class sequences (q_len * G <= 16 query rows per KV head): split-KV items
+//     (sequence, KV head, key range), with one split length for the whole batch chosen so
+//     that about kDecTargetCtas items exist, never below kDecMinSplit keys, always a
+//     multiple of the 64-key decode tile; items of one sequence are contiguous, head-major;
+//   - prefill-class sequences: 128-row query tiles, sorted by their number of 128-key KV
+//     tiles, largest first, so the persistent prefill grid takes the long causal tiles
+//     first (longest-processing-time order);
+//   - the query rows whose decode splits must be merged.
+// The lists depend only on the inputs and on compile-time constants, so results are
+// bitwise reproducible. If the batch description is inconsistent (cum not a prefix sum
+// ending at N, a negative past, a sequence longer than its block_table row) nothing is
+// scheduled and PA_DEVERR_BAD_BATCH is raised.
+#include "common.cuh"
+
+namespace pa {
+
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+__device__ __forceinline__ bool is_decode_class(int64_t q, const Args& a) {
+  return a.route == PA_ROUTE_AUTO && q >= 1 && q * a.G <= kDecRows;
+}
+
+// exclusive scan of three ints across the block; tot[] gets the block totals
+__device__ void block_scan3(const int v[3], int ex[3], int tot[3], int (*s_warp)[32]) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int inc[3];
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    int x = v[k];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    inc[k] = x;
+    if (lane == 31) s_warp[k][wid] = x;
+  }
+  __syncthreads();
+  if (wid == 0) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      int x = lane < nw ? s_warp[k][lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      s_warp[k][lane] = x;  // inclusive prefix of warp totals
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    int before = wid > 0 ? s_warp[k][wid - 1] : 0;
+    ex[k] = before + inc[k] - v[k];
+    tot[k] = s_warp[k][nw - 1];
+  }
+  __syncthreads();
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
+  __shared__ int s_bad;
+  __shared__ unsigned long long s_dec_keys;
+  __shared__ int s_warp[3][32];
+  __shared__ int s_carry[3];
+  __shared__ unsigned long long s_key[kSortCap];
+
+  const int tid = threadIdx.x;
+  WsHeader* hdr = a.hdr;
+  if (tid == 0) {
+    s_bad = 0;
+    s_dec_keys = 0;
+    s_carry[0] = s_carry[1] = s_carry[2] = 0;
+    hdr->error = 0;  // error bits describe the most recent call
+  }
+  __syncthreads();
+
+  // ---- validate the batch description and total the decode keys ----
+  const int64_t max_kv = (int64_t)a.max_blocks * a.bs;
+  if (tid == 0 && (a.cum[0] != 0 || a.cum[a.B] != a.N)) s_bad = 1;
+  for (int b = tid; b < a.B; b += blockDim.x) {
+    const int64_t q = (int64_t)a.cum[b + 1] - a.cum[b];
+    const int64_t kv = (int64_t)a.past[b] + q;
+    if (q < 0 || a.past[b] < 0 || kv > max_kv) {
+      atomicOr(&s_bad, 1);
+    } else if (is_decode_class(q, a)) {
+      atomicAdd(&s_dec_keys, (unsigned long long)kv);
+    }
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (tid == 0) {
+      atomicOr(&hdr->error, PA_DEVERR_BAD_BATCH);
+      hdr->valid = 0;
+      hdr->n_decode_items = hdr->n_prefill_tiles = hdr->n_merge_rows = 0;
+    }
+    return;
+  }
+
+  // ---- one split length for the batch ----
+  int64_t split;
+  if (a.forced_split > 0) {
+    split = a.forced_split;
+  } else {
+    const int64_t pairs = ceil_div(kDecTargetCtas, a.kvh);
+    split = ceil_div((int64_t)s_dec_keys, pairs);
+    split = ceil_div(split, kDecTile) * kDecTile;
+    if (split < kDecMinSplit) split = kDecMinSplit;
+  }
+
+  // ---- per-sequence counts, prefix sums, and the lists ----
+  for (int base = 0; base < a.B; base += blockDim.x) {
+    const int b = base + tid;
+    const int carry0 = s_carry[0], carry1 = s_carry[1], carry2 = s_carry[2];
+    int v[3] = {0, 0, 0};
+    int64_t q = 0, kv = 0, nsplit = 0;
+    if (b < a.B) {
+      q = (int64_t)a.cum[b + 1] - a.cum[b];
+      kv = (int64_t)a.past[b] + q;
+      if (is_decode_class(q, a)) {
+        nsplit = ceil_div(kv, split);
+        v[0] = (int)(nsplit * a.kvh);
+        if (nsplit > 1) v[2] = (int)q;
+      } else if (q > 0) {
+        v[1] = (int)ceil_div(q, kPreTileQ);
+      }
+    }
+    int ex[3], tot[3];
+    block_scan3(v, ex, tot, s_warp);
+    if (b < a.B) {
+      const int dbase = carry0 + ex[0];
+      const int tbase = carry1 + ex[1];
+      const int mbase = carry2 + ex[2];
+      for (int g = 0; g < (v[0] ? a.kvh : 0); ++g) {
+        for (int s = 0; s < nsplit; ++s) {
+          const int idx = dbase + g * (int)nsplit + s;
+          if (idx >= a.max_items) break;
+          DecodeItem it;
+          it.b = b;
+          it.g = g;
+          it.key_begin = (int)(s * split);
+          it.key_end = (int)(((s + 1) * split < kv) ? (s + 1) * split : kv);
+          it.partial = nsplit > 1 ? idx : -1;
+          it.n_split = (int)nsplit;
+          it.pad[0] = 0;
+          it.pad[1] = 0;
+          a.items[idx] = it;
+        }
+      }
+      for (int t = 0; t < v[1]; ++t) {
+        const int idx = tbase + t;
+        if (idx < a.max_tiles) a.tiles_unsorted[idx] = PrefillTile{b, t * kPreTileQ};
+      }
+      for (int j = 0; j < v[2]; ++j) {
+        const int idx = mbase + j;
+        if (idx < a.max_merge) a.merge[idx] = MergeRow{a.cum[b] + j, b, dbase, (int)nsplit};
+      }
+    }
+    __syncthreads();  // every thread has read the carries of this round
+    if (tid == 0) {
+      s_carry[0] += tot[0];
+      s_carry[1] += tot[1];
+      s_carry[2] += tot[2];
+    }
+    __syncthreads();
+  }
+
+  const int n_items = s_carry[0], n_tiles = s_carry[1], n_merge = s_carry[2];
+  if (n_items > a.max_items || n_tiles > a.max_tiles || n_merge > a.max_merge) {
+    // cannot happen for a batch that passed validation (the bounds are proven in
+    // ws_layout); refuse rather than run a truncated plan
+    if (tid == 0) {
+      atomicOr(&hdr->error, PA_DEVERR_BAD_BATCH);
+      hdr->valid = 0;
+      hdr->n_decode_items = hdr->n_prefill_tiles = hdr->n_merge_rows = 0;
+    }
+    return;
+  }
+
+  // ---- prefill tiles: sort by KV-tile count, descending (ties: list order) ----
+  if (n_tiles <= kSortCap) {
+    int n2 = 1;
+    while (n2 < n_tiles) n2 <<= 1;
+    for (int i = tid; i < n2; i += blockDim.x) {
+      unsigned long long key = ~0ull;
+      if (i < n_tiles) {
+        const PrefillTile t = a.tiles_unsorted[i];
+        const int64_t q = (int64_t)a.cum[t.b + 1] - a.cum[t.b];
+        const int64_t last = ((int64_t)t.j0 + kPreTileQ < q) ? (int64_t)t.j0 + kPreTileQ : q;
+        const int64_t cost = ceil_div((int64_t)a.past[t.b] + last, kPreTileK);
+        key = ((unsigned long long)(0xFFFFFFFFull - (unsigned long long)cost) << 32) | (unsigned)i;
+      }
+      s_key[i] = key;
+    }
+    __syncthreads();
+    for (int k = 2; k <= n2; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = tid; i < n2; i += blockDim.x) {
+          const int ixj = i ^ j;
+          if (ixj > i) {
+            const unsigned long long x = s_key[i], y = s_key[ixj];
+            const bool ascending = (i & k) == 0;
+            if ((x > y) == ascending) {
+              s_key[i] = y;
+              s_key[ixj] = x;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int i = tid; i < n_tiles; i += blockDim.x) a.tiles[i] = a.tiles_unsorted[(unsigned)(s_key[i] & 0xFFFFFFFFull)];
+  } else {
+    for (int i = tid; i < n_tiles; i += blockDim.x) a.tiles[i] = a.tiles_unsorted[i];
+  }
+  if (tid == 0) {
+    hdr->valid = 1;
+    hdr->n_decode_items = n_items;
+    hdr->n_prefill_tiles = n_tiles;
+    hdr->n_merge_rows = n_merge;
+    hdr->split_keys = (int)split;
+  }
+}
+
+// ---- cache write ----------------------------------------------------------------------------
+// One thread per 16-byte chunk of a token's K or V row. Consecutive threads cover
+// consecutive chunks of one row, so loads and stores are coalesced 16-byte accesses.
+// The slot is slot_mapping[i], or derived from the token's logical position
+// past_seqlens[b] + j through block_table. -1 skips; out-of-range slots and blocks are
+// skipped and flagged.
+__global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
+  if (!a.hdr->valid) return;
+  const int chunks = a.kv_row / 8;  // 16-byte chunks in one K (or V) row
+  const int64_t per_tok = 2 * (int64_t)chunks;
+  const int64_t total = (int64_t)a.N * per_tok;
+  const int64_t nslots = (int64_t)a.num_blocks * a.bs;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int tok = (int)(idx / per_tok);
+    const int r = (int)(idx - (int64_t)tok * per_tok);
+    const int which = r >= chunks;  // 0: K row, 1: V row
+    const int c = which ? r - chunks : r;
+    int64_t slot;
+    if (a.slot_mapping) {
+      slot = a.slot_mapping[tok];
+    } else {
+      int lo = 0, hi = a.B - 1;  // last b with cum[b] <= tok
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.cum[mid] <= tok) lo = mid; else hi = mid - 1;
+      }
+      const int64_t p = (int64_t)a.past[lo] + (tok - a.cum[lo]);
+      const int blk = a.block_table[(int64_t)lo * a.max_blocks + p / a.bs];
+      if (blk < 0 || blk >= a.num_blocks) {
+        if (c == 0) atomicOr(&a.hdr->error, PA_DEVERR_BAD_BLOCK);
+        continue;
+      }
+      slot = (int64_t)blk * a.bs + p % a.bs;
+    }
+    if (slot == -1) continue;
+    if (slot < 0 || slot >= nslots) {
+      if (c == 0) atomicOr(&a.hdr->error, PA_DEVERR_BAD_SLOT);
+      continue;
+    }
+    const uint16_t* src;
+    if (a.packed) {
+      src = reinterpret_cast<const uint16_t*>(a.query) + (int64_t)tok * a.q_stride + (which ? a.v_offset : a.k_offset);
+    } else {
+      src = reinterpret_cast<const uint16_t*>(which ? a.value : a.key) + (int64_t)tok * a.kv_row;
+    }
+    uint16_t* dst = reinterpret_cast<uint16_t*>(which ? a.value_cache : a.key_cache) + slot * a.kv_row;
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + c);
+    reinterpret_cast<uint4*>(dst)[c] = v;
+  }
+}
+
+// ---- host launchers ----
+cudaError_t launch_plan(const Args& a, cudaStream_t s) {
+  plan_kernel<<<1, kPlanThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cache_write(const Args& a, int grid, cudaStream_t s) {
+  cache_write_kernel<<<grid, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace pa
