@@ -1,0 +1,470 @@
+"""Benchmark of the paged-attention hot path on GB300.
+
+One step = one call of the operator (plan, cache write, prefill, split-KV decode, merge)
+over one batch of seeded synthetic inputs already resident in HBM. The headline line is
+the decode batch workload (64 sequences, one new token each, history uniform in
+[512, 4096], 32 query / 8 KV heads, head_size 128, 256-token pages, fp16): decode KV
+GB/s = the K and V history bytes the step must read (each element once) / step time.
+The other workloads (causal prefill 4 x 2048 bf16, the mixed continuous batch, long
+decode with 16-token pages) are measured in the same run under "secondary".
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+N > 1 runs under torchrun, one rank per GPU, each rank on its own batch (weak scaling,
+no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+MAIN = 2
+SECONDARY = (3, 4, 5)
+METRIC = "paged-attn decode KV GB/s & prefill TFLOP/s vs GB300 peak; packed tokens/s"
+
+
+# ---- algorithmic work of one step ---------------------------------------------------------
+
+def kv_history_bytes(p) -> int:
+    """K and V of every sequence's history (past + new rows), each element read once."""
+    return int(p.kv_lens.sum()) * p.kv_num_heads * p.head_size * 2 * 2
+
+
+def step_bytes(p) -> int:
+    """History K/V read + new K/V rows read and written + queries read + output written."""
+    N, nh, kvh, hs = p.num_tokens, p.num_heads, p.kv_num_heads, p.head_size
+    written = N if p.slot_mapping is None else int((p.slot_mapping >= 0).sum())
+    return kv_history_bytes(p) + N * nh * hs * 2 * 2 + (N + written) * kvh * hs * 2 * 2
+
+
+def causal_flops(p, sequences=None) -> int:
+    """4 * head_size * num_heads * (query, key) pairs inside the causal mask (QK^T and PV)."""
+    total = 0
+    for b in (range(p.batch_size) if sequences is None else sequences):
+        q, past = int(p.q_lens[b]), int(p.past_seqlens[b])
+        total += q * past + q * (q + 1) // 2
+    return 4 * p.head_size * p.num_heads * total
+
+
+def decode_sequences(p):
+    G = p.num_heads // p.kv_num_heads
+    return [b for b in range(p.batch_size) if 1 <= p.q_lens[b] and p.q_lens[b] * G <= 16]
+
+
+def prefill_sequences(p):
+    d = set(decode_sequences(p))
+    return [b for b in range(p.batch_size) if p.q_lens[b] > 0 and b not in d]
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---- clocks during the timed region ---------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def __enter__(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[4:9]))
+                except ValueError:
+                    pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [r[0] for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2][1:]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---- the CUDA arm ---------------------------------------------------------------------------------
+
+class Runner:
+    """Holds one workload resident on the GPU and enqueues steps through the C ABI with
+    pre-marshalled arguments (so host overhead stays far below the GPU time of a step)."""
+
+    def __init__(self, p, device):
+        import torch
+
+        import varlen_paged_kv_gb300 as pa
+        self.torch, self.pa, self.p = torch, pa, p
+        dt = {"fp16": torch.float16, "bf16": torch.bfloat16}[p.dtype]
+
+        def t16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(dt)
+
+        def t32(a):
+            return None if a is None else torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+        self.host = {k: getattr(p, k) for k in ("query", "key", "value")}
+        self.q, self.k, self.v = t16(p.query), (None if p.key is None else t16(p.key)), (None if p.value is None else t16(p.value))
+        self.kc, self.vc = t16(p.key_cache), t16(p.value_cache)
+        self.cum, self.past = t32(p.cumulative_sequence_length), t32(p.past_seqlens)
+        self.bt, self.sm = t32(p.block_table), t32(p.slot_mapping)
+        self.out = torch.empty((p.num_tokens, p.num_heads * p.head_size), dtype=dt, device=device)
+        self.dims = pa.make_dims(p.num_tokens, p.batch_size, p.head_size, p.num_blocks, p.block_size,
+                                 p.max_blocks_per_sequence, dt)
+        self.ws = torch.zeros(pa.workspace_size(self.dims, p.num_heads, p.kv_num_heads), dtype=torch.uint8,
+                              device=device)
+        self.stream = torch.cuda.current_stream(device)
+        self.lib = pa.load_library()
+        vp = ctypes.c_void_p
+
+        def ptr(t):
+            return None if t is None else vp(t.data_ptr())
+
+        self.args = (ptr(self.q), ptr(self.k), ptr(self.v), ptr(self.kc), ptr(self.vc), ptr(self.cum),
+                     ptr(self.past), ptr(self.bt), ptr(self.sm), p.num_heads, p.kv_num_heads,
+                     ctypes.c_float(p.scale), ptr(self.out), ctypes.byref(self.dims), ptr(self.ws),
+                     self.ws.numel(), vp(self.stream.cuda_stream))
+
+    def call(self, stages):
+        st = self.lib.pa_paged_attention_stages(*self.args, stages)
+        if st:
+            raise RuntimeError(f"pa_paged_attention_stages: status {st}")
+
+    def step(self):
+        self.call(self.pa.STAGE_ALL)
+
+    def timed(self, steps, warmup, kernel_stage, clocks=None):
+        """Times `steps` steps; kernel_stage's launches are bracketed by their own events.
+        Returns (seconds per step, seconds per kernel launch, launches per step)."""
+        torch, pa = self.torch, self.pa
+        before = [s for s in (pa.STAGE_PLAN, pa.STAGE_CACHE_WRITE, pa.STAGE_PREFILL, pa.STAGE_DECODE,
+                              pa.STAGE_MERGE) if s < kernel_stage]
+        after = [s for s in (pa.STAGE_PLAN, pa.STAGE_CACHE_WRITE, pa.STAGE_PREFILL, pa.STAGE_DECODE,
+                             pa.STAGE_MERGE) if s > kernel_stage]
+        mask_before, mask_after = sum(before), sum(after)
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n0 = pa.kernel_launch_count()
+        if clocks is not None:
+            clocks.__enter__()
+        torch.cuda.synchronize()
+        start.record(self.stream)
+        for i in range(steps):
+            self.call(mask_before)
+            ev[i][0].record(self.stream)
+            self.call(kernel_stage)
+            ev[i][1].record(self.stream)
+            self.call(mask_after)
+        end.record(self.stream)
+        torch.cuda.synchronize()
+        if clocks is not None:
+            clocks.__exit__(None, None, None)
+        launches = pa.kernel_launch_count() - n0
+        total = start.elapsed_time(end) / 1e3
+        kern = sum(a.elapsed_time(b) for a, b in ev) / 1e3 / steps
+        return total / steps, kern, launches
+
+    def e2e(self, steps, warmup):
+        """The public Python API with host buffers: per step, H2D of the step's inputs from
+        pinned memory, the call, D2H of the output; the caches stay resident."""
+        torch, pa = self.torch, self.pa
+        p = self.p
+        pins = {}
+        for name, dev in (("query", self.q), ("key", self.k), ("value", self.v), ("cum", self.cum),
+                          ("past", self.past), ("bt", self.bt), ("sm", self.sm)):
+            if dev is not None:
+                pins[name] = (torch.empty(dev.shape, dtype=dev.dtype, pin_memory=True), dev)
+                pins[name][0].copy_(dev.cpu())
+        out_host = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
+        h2d = sum(h.numel() * h.element_size() for h, _ in pins.values())
+        d2h = out_host.numel() * out_host.element_size()
+
+        def one():
+            for h, d in pins.values():
+                d.copy_(h, non_blocking=True)
+            pa.paged_attention(self.q, self.k, self.v, self.kc, self.vc, self.cum, self.past, self.bt, self.sm,
+                               num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, scale=p.scale,
+                               output=self.out, workspace=self.ws)
+            out_host.copy_(self.out, non_blocking=True)
+
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            one()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / steps, h2d, d2h
+
+
+def kernel_roofline(p, kind, seconds_per_launch, pk):
+    if kind == "hbm":
+        units = kv_history_bytes(p)
+        achieved = units / seconds_per_launch / 1e9
+        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                "peak_source": f"{pk['source']} hbm_gbs", "algorithmic_bytes_per_launch": units}
+    flops = causal_flops(p, prefill_sequences(p))
+    achieved = flops / seconds_per_launch / 1e12
+    return {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": None,
+            "peak_source": f"{pk['source']} bf16_tflops (burst; fp16 nominal rate equals bf16)",
+            "algorithmic_flops_per_launch": flops}
+
+
+def reduce_over_ranks(local_seconds: float, local_units: float):
+    """max step time and summed units over ranks (identity when not distributed)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return local_seconds, local_units
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def oracle_baseline(p, reps=1):
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.paged_attention(p)
+    dt = (time.perf_counter() - t0) / reps
+    return dt, oracle.max_threads()
+
+
+WORKLOAD_TEXT = {
+    2: "decode batch: B=64, 1 new token each, past U[512,4096], 32/8 heads, head_size 128, 256-token pages, "
+       "fp16, separate K/V, slots derived",
+    3: "causal prefill: B=4 x 2048 new tokens, past 0, 32/8 heads, head_size 128, 256-token pages, bf16",
+    4: "mixed continuous batch: 8 prefill chunks of 512 (past U[0,8192]) + 24 decode tokens (past "
+       "U[1024,16384]), 32/8 heads, head_size 128, 256-token pages, fp16, packed [Q|K|V], 10% slots -1",
+    5: "long-context decode: B=8, 1 new token each, past U[32768,131072], 32/8 heads, head_size 128, "
+       "16-token pages, bf16",
+}
+
+
+def measure(r, steps, warmup, pk, clocks=None):
+    """Times one workload; the dominant kernel (prefill for workloads with prefill rows,
+    else decode) is bracketed by its own events inside the timed region."""
+    q = r.p
+    if prefill_sequences(q):
+        s, kt, launches = r.timed(steps, warmup, r.pa.STAGE_PREFILL, clocks=clocks)
+        roof = kernel_roofline(q, "tensor", kt, pk)
+        roof["kernel"] = "prefill_kernel (tcgen05/TMEM, TMA)"
+    else:
+        s, kt, launches = r.timed(steps, warmup, r.pa.STAGE_DECODE, clocks=clocks)
+        roof = kernel_roofline(q, "hbm", kt, pk)
+        roof["kernel"] = "decode_kernel (split-KV, TMA + mma.sync)"
+    roof["ms_per_launch"] = round(kt * 1e3, 4)
+    return s, roof, launches
+
+
+def headline(q, sec):
+    """(value, unit) of a workload's own metric: decode KV GB/s for decode-only batches,
+    causal TFLOP/s for prefill-only batches, packed tokens/s for mixed ones."""
+    if not prefill_sequences(q):
+        return kv_history_bytes(q) / sec / 1e9, "GB/s"
+    if not decode_sequences(q):
+        return causal_flops(q) / sec / 1e12, "TFLOP/s"
+    return q.num_tokens / sec, "tokens/s"
+
+
+def run_cuda(args):
+    import torch
+    import torch.distributed as dist
+    from varlen_paged_kv_gb300 import build as _build
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    pk = peaks()
+
+    k = args.workload
+    p = wl.config(k) if rank == 0 else wl.make_problem(**_rank_recipe(k, rank))
+    r = Runner(p, device)
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sec, roof, launches = measure(r, args.steps, args.warmup, pk, clocks=sampler)
+    value, unit = headline(p, sec)
+    sec_max, value_all = reduce_over_ranks(sec, value * sec)   # units of work summed over ranks
+    value = value_all / sec_max
+    e2e_sec, h2d, d2h = r.e2e(max(args.steps // 4, 10), args.warmup)
+    e2e_max, e2e_units = reduce_over_ranks(e2e_sec, headline(p, e2e_sec)[0] * e2e_sec)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(sec_max * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": p.dtype, "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[k], "name": p.name, "num_tokens": p.num_tokens,
+                   "batch_size": p.batch_size, "num_blocks": p.num_blocks,
+                   "kv_history_bytes_per_step": kv_history_bytes(p),
+                   "causal_flops_per_step": causal_flops(p),
+                   "l2": ("inputs larger than L2: each step streams %.0f MB of K/V history (L2 129 MB)"
+                          % (kv_history_bytes(p) / 1e6)) if k != 3 else
+                         "compute-bound workload; its %.0f MB of K/V fit in L2" % (kv_history_bytes(p) / 1e6),
+                   "parallelism": f"replicas x{world} (one batch per GPU)"},
+        "roofline": roof,
+        "e2e": {"value": round(e2e_units / e2e_max, 1), "unit": unit, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_max * 1e3, 4)},
+        "gpu_launches": int(launches),
+        "clocks": sampler.summary(),
+    }
+    if rank == 0 and not args.no_secondary:
+        sec_lines = {}
+        for kk in SECONDARY:
+            if kk == k:
+                continue
+            q = wl.config(kk)
+            rq = Runner(q, device)
+            s, roof_q, _ = measure(rq, max(args.steps // 10, 10), args.warmup, pk)
+            v, u = headline(q, s)
+            entry = {"workload": WORKLOAD_TEXT[kk], "value": round(v, 1), "unit": u, "ms_per_step": round(s * 1e3, 4),
+                     "packed_tokens_per_s": round(q.num_tokens / s, 1), "roofline": roof_q}
+            if kk == 4:
+                t_flop = causal_flops(q) / (pk["bf16_tflops"] * 1e12)
+                t_byte = step_bytes(q) / (pk["hbm_gbs"] * 1e9)
+                entry["fraction_of_max_roofline_time"] = round(max(t_flop, t_byte) / s, 4)
+            sec_lines[q.name] = entry
+            del rq
+            torch.cuda.empty_cache()
+        line["secondary"] = sec_lines
+    if rank == 0 and args.no_cpu_baseline:
+        line["cpu_baseline"] = None
+        print(json.dumps(line), flush=True)
+    elif rank == 0:
+        dt, cores = oracle_baseline(p)
+        cv, cu = headline(p, dt)
+        line["cpu_baseline"] = {"value": round(cv, 4), "unit": cu, "cores": cores, "kind": "oracle",
+                                "sample": "the whole %s workload (cache write + attention), fp64 C oracle, one run, "
+                                          "%.2f s" % (p.name, dt)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def _rank_recipe(k, rank):
+    """Rank r > 0 runs its own batch of the same workload recipe (seed shifted by 100 r)."""
+    seed = 1000 + k + 100 * rank
+    if k == 2:
+        past = wl.uniform_int(seed, wl.S_PAST, 64, 512, 4096)
+        return dict(name=wl.CONFIG_NAMES[2], seed=seed, dtype="fp16", num_heads=32, kv_num_heads=8, head_size=128,
+                    block_size=256, past=past, q_lens=np.ones(64, np.int64), max_blocks_per_sequence=17)
+    if k == 3:
+        return dict(name=wl.CONFIG_NAMES[3], seed=seed, dtype="bf16", num_heads=32, kv_num_heads=8, head_size=128,
+                    block_size=256, past=np.zeros(4, np.int64), q_lens=np.full(4, 2048, np.int64))
+    raise ValueError("multi-GPU runs use workload 2 or 3")
+
+
+def run_reference(args):
+    """The oracle, as it stands, on the host cores: each step is the whole workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    p = wl.config(args.workload)
+    for _ in range(args.warmup):
+        oracle.paged_attention(p)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.paged_attention(p)
+    sec = (time.perf_counter() - t0) / args.steps
+    value, unit = headline(p, sec)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": unit, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": p.name},
+        "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": "the whole %s workload per step (cache write + attention)" % p.name},
+        "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    ap.add_argument("--workload", type=int, default=MAIN, choices=[2, 3, 4, 5],
+                    help="workload of the headline line (2: the decode batch the metric is quoted on)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        if args.steps > 50:
+            args.steps = 10
+        run_reference(args)
+    else:
+        run_cuda(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -201,6 +201,17 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {  // lo -> bits 0
   }
 }
 
+// p as two bf16 values hi + lo with hi = bf16(p), lo = bf16(p - hi): their sum carries
+// about 16 significant bits, so P V computed as hi V + lo V keeps the softmax weights'
+// rounding error near 2^-17 instead of bf16's 2^-9.
+__device__ __forceinline__ void split_bf16x2(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 // ---- mbarrier ---------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

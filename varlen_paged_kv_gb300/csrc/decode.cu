@@ -11,7 +11,8 @@
 //     are bank-conflict free);
 //   - four consumer warps each take 16 keys of every tile: S = Q K^T and O += P V on the
 //     warp-level tensor cores (mma.sync m16n8k16, fp32 accumulation), with an online
-//     softmax in registers (row max over the quad by shuffles, base-2 exponentials);
+//     softmax in registers (row max over the quad by shuffles, base-2 exponentials; for
+//     bf16 the weights P enter P V as a bf16 hi + lo pair, two products);
 //   - at the end of the item the four warps' (m, l, O) are combined in a fixed order in
 //     shared memory. A single-split item writes the output row rounded once to T; a split
 //     writes its normalised fp32 partial row and its natural-log lse.
@@ -210,11 +211,19 @@ __global__ void __launch_bounds__(160, 2)
         }
         l0 = l0 * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
         l1 = l1 * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
-        uint32_t pa[4];
-        pa[0] = pack2<BF16>(p[0][0], p[0][1]);
-        pa[1] = pack2<BF16>(p[0][2], p[0][3]);
-        pa[2] = pack2<BF16>(p[1][0], p[1][1]);
-        pa[3] = pack2<BF16>(p[1][2], p[1][3]);
+        // P as the MMA A fragment; bf16 carries it as hi + lo (two products), fp16 as one
+        uint32_t pa[4], pl[4];
+        if constexpr (BF16) {
+          split_bf16x2(p[0][0], p[0][1], pa[0], pl[0]);
+          split_bf16x2(p[0][2], p[0][3], pa[1], pl[1]);
+          split_bf16x2(p[1][0], p[1][1], pa[2], pl[2]);
+          split_bf16x2(p[1][2], p[1][3], pa[3], pl[3]);
+        } else {
+          pa[0] = pack2<false>(p[0][0], p[0][1]);
+          pa[1] = pack2<false>(p[0][2], p[0][3]);
+          pa[2] = pack2<false>(p[1][0], p[1][1]);
+          pa[3] = pack2<false>(p[1][2], p[1][3]);
+        }
 #pragma unroll
         for (int d = 0; d < ND; ++d) {
           o[d][0] *= al0;
@@ -245,6 +254,10 @@ __global__ void __launch_bounds__(160, 2)
             v3 &= vmask_hi;
             mma16816<BF16>(o[2 * dp], pa, v0, v1);
             mma16816<BF16>(o[2 * dp + 1], pa, v2, v3);
+            if constexpr (BF16) {
+              mma16816<BF16>(o[2 * dp], pl, v0, v1);
+              mma16816<BF16>(o[2 * dp + 1], pl, v2, v3);
+            }
           }
         }
       }

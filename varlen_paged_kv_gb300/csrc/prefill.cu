@@ -19,8 +19,10 @@
 //   warps 2..5  softmax: thread i owns TMEM lane / query row i; loads its S row, masks,
 //               updates the running max (the O rescale is skipped until the max has
 //               grown by more than 2^8, which is exact because the final division uses
-//               the same stale max), writes P as 16-bit pairs into TMEM, and at the end
-//               normalises O and stores the row.
+//               the same stale max), writes P as 16-bit pairs into TMEM (bf16: as a hi
+//               and a lo part, bf16(p) and bf16(p - hi), multiplied by V separately, so
+//               the weights keep ~16 bits instead of 8), and at the end normalises O and
+//               stores the row.
 // TMEM: S0 at column 0, S1 at 128, O at 256 (512 columns allocated).
 #include "common.cuh"
 
@@ -189,6 +191,7 @@ __global__ void __launch_bounds__(192, 1)
             // 64-column slabs of head_size 16 KB apart (MN dimension)
             const uint64_t vdesc = sdesc_sw128(v_base + kk * 16 * 128, L::kHalfBytes, 1024);
             tc_mma_ts(tmem + kOCol, p_tmem + kk * 8, vdesc, IDESC_PV, (i > 0 || kk > 0) ? 1u : 0u);
+            if constexpr (BF16) tc_mma_ts(tmem + kOCol, p_tmem + 64 + kk * 8, vdesc, IDESC_PV, 1u);
           }
           tc_commit(&v_empty[st]);
           tc_commit(o_done);
@@ -269,17 +272,21 @@ __global__ void __launch_bounds__(192, 1)
           l *= alpha;
         }
         // P = exp2(x - m) as 16-bit pairs, written over the first 64 columns of this S buffer
+        // (bf16: P = hi + lo, hi over columns 0..63 and lo over 64..127 of the S buffer)
 #pragma unroll
         for (int hcol = 0; hcol < 2; ++hcol) {
           uint32_t pw[32];
+          uint32_t pl[BF16 ? 32 : 1];
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const float p0 = fast_exp2(x[hcol * 64 + 2 * c] - m_used);
             const float p1 = fast_exp2(x[hcol * 64 + 2 * c + 1] - m_used);
             l += p0 + p1;
-            pw[c] = pack2<BF16>(p0, p1);
+            if constexpr (BF16) split_bf16x2(p0, p1, pw[c], pl[c]);
+            else pw[c] = pack2<false>(p0, p1);
           }
           tmem_st_x32(s_tmem + hcol * 32, pw);
+          if constexpr (BF16) tmem_st_x32(s_tmem + 64 + hcol * 32, pl);
         }
         if (t > 0) {
           // O holds P_0..P_{t-2} V; wait for P_{t-1} V before rescaling it
