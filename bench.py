@@ -156,8 +156,10 @@ class Runner:
         self.cum, self.past = t32(p.cumulative_sequence_length), t32(p.past_seqlens)
         self.bt, self.sm = t32(p.block_table), t32(p.slot_mapping)
         self.out = torch.empty((p.num_tokens, p.num_heads * p.head_size), dtype=dt, device=device)
+        # the caller knows its batch composition: pass the bound on new tokens per sequence
+        self.max_q = int(p.q_lens.max()) if p.batch_size else 0
         self.dims = pa.make_dims(p.num_tokens, p.batch_size, p.head_size, p.num_blocks, p.block_size,
-                                 p.max_blocks_per_sequence, dt)
+                                 p.max_blocks_per_sequence, dt, max_query_len=self.max_q)
         self.ws = torch.zeros(pa.workspace_size(self.dims, p.num_heads, p.kv_num_heads), dtype=torch.uint8,
                               device=device)
         self.stream = torch.cuda.current_stream(device)
@@ -184,10 +186,9 @@ class Runner:
         """Times `steps` steps; kernel_stage's launches are bracketed by their own events.
         Returns (seconds per step, seconds per kernel launch, launches per step)."""
         torch, pa = self.torch, self.pa
-        before = [s for s in (pa.STAGE_PLAN, pa.STAGE_CACHE_WRITE, pa.STAGE_PREFILL, pa.STAGE_DECODE,
-                              pa.STAGE_MERGE) if s < kernel_stage]
-        after = [s for s in (pa.STAGE_PLAN, pa.STAGE_CACHE_WRITE, pa.STAGE_PREFILL, pa.STAGE_DECODE,
-                             pa.STAGE_MERGE) if s > kernel_stage]
+        stages = (pa.STAGE_PLAN, pa.STAGE_CACHE_WRITE, pa.STAGE_PREFILL, pa.STAGE_DECODE)
+        before = [s for s in stages if s < kernel_stage]
+        after = [s for s in stages if s > kernel_stage]
         mask_before, mask_after = sum(before), sum(after)
         for _ in range(warmup):
             self.step()
@@ -234,7 +235,7 @@ class Runner:
                 d.copy_(h, non_blocking=True)
             pa.paged_attention(self.q, self.k, self.v, self.kc, self.vc, self.cum, self.past, self.bt, self.sm,
                                num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, scale=p.scale,
-                               output=self.out, workspace=self.ws)
+                               output=self.out, workspace=self.ws, max_query_len=self.max_q)
             out_host.copy_(self.out, non_blocking=True)
 
         for _ in range(warmup):

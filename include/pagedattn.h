@@ -66,8 +66,15 @@ typedef struct pa_dims {
   int32_t block_size;              /* tokens per page: a positive multiple of 16 */
   int32_t max_blocks_per_sequence; /* columns of block_table */
   int32_t dtype;                   /* pa_dtype of T */
-  int32_t decode_split_keys;       /* 0: automatic; else keys per split-KV decode work item (a multiple of 64) */
+  int32_t decode_split_keys;       /* 0: balanced automatic partition; else keys per split-KV decode work
+                                      item (a multiple of 64; a test hook) */
   int32_t route;                   /* PA_ROUTE_* */
+  int32_t max_query_len;           /* 0: unknown; else a host-side bound on every sequence's new-token count
+                                      (the CPU-resident launch bound of the packed contract's
+                                      attention_metadata). With route AUTO and max_query_len *
+                                      (num_heads / kv_num_heads) <= 16 no prefill kernel is launched. The
+                                      plan stage checks it: a sequence above the bound is a
+                                      PA_DEVERR_BAD_BATCH. */
 } pa_dims;
 
 /*
@@ -120,9 +127,9 @@ pa_status pa_paged_attention(const void* query, const void* key, const void* val
 #define PA_STAGE_PLAN 1u        /* device work partitioner: classify sequences, build work lists */
 #define PA_STAGE_CACHE_WRITE 2u /* scatter this step's K/V rows into the caches */
 #define PA_STAGE_PREFILL 4u     /* tcgen05/TMEM attention for prefill-class sequences */
-#define PA_STAGE_DECODE 8u      /* split-KV attention for decode-class sequences */
-#define PA_STAGE_MERGE 16u      /* deterministic (out, lse) merge of decode splits */
-#define PA_STAGE_ALL 31u
+#define PA_STAGE_DECODE 8u      /* split-KV attention for decode-class sequences, including the
+                                   deterministic (out, lse) merge of the splits */
+#define PA_STAGE_ALL 15u
 
 /*
  * Same arguments as pa_paged_attention; runs only the stages in `stages` (PA_STAGE_*

@@ -177,6 +177,39 @@ def test_full_size_workload(k):
     assert_close(got, ref, p.dtype, p.name)
 
 
+def test_max_query_len_hint_skips_prefill_and_is_checked():
+    p = _case("decode-q-up-to-4")  # q_len <= 4, G = 4: every sequence decode-class
+    ref = oracle.paged_attention(p)
+    d = upload(p)
+    ws = make_workspace(p)
+    n0 = pa.kernel_launch_count()
+    out = pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
+                             d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], None,
+                             num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, workspace=ws, max_query_len=4)
+    assert pa.read_device_error(ws) == 0
+    assert pa.kernel_launch_count() - n0 == 3  # plan, cache write, decode
+    assert_close(bits_of(out).reshape(p.num_tokens, p.num_heads, p.head_size), ref["out"], p.dtype, "hint")
+    # a bound below the real q_len is refused on the device, nothing written
+    d = upload(p)
+    pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
+                       d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], None,
+                       num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, workspace=ws, max_query_len=2)
+    assert pa.read_device_error(ws) & pa.DEVERR_BAD_BATCH
+    assert np.array_equal(bits_of(d["key_cache"]), p.key_cache)
+
+
+def test_balanced_partition_splits_long_units_across_ctas():
+    # two sequences with long histories and many short ones: the long units are cut across
+    # several CTAs and merged by the last one; results must not depend on the cut
+    past = [60000, 5, 17, 33000, 300, 1, 2, 3]
+    p = w.make_problem(name="skew", seed=9, dtype="bf16", num_heads=16, kv_num_heads=4, head_size=128,
+                       block_size=16, past=past, q_lens=[1, 2, 1, 3, 1, 4, 1, 1])
+    check(p)
+    a = run_gpu(p)
+    b = run_gpu(p)
+    assert np.array_equal(a["out_bits"], b["out_bits"])
+
+
 # ---- device-side error reporting (no faults) ----------------------------------------------------
 
 def test_out_of_range_block_is_reported_and_read_as_zeros():

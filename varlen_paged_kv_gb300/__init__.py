@@ -18,8 +18,8 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIBRARY_PATH = os.path.join(_HERE, "libpagedattn.so")
 
-STAGE_PLAN, STAGE_CACHE_WRITE, STAGE_PREFILL, STAGE_DECODE, STAGE_MERGE = 1, 2, 4, 8, 16
-STAGE_ALL = 31
+STAGE_PLAN, STAGE_CACHE_WRITE, STAGE_PREFILL, STAGE_DECODE = 1, 2, 4, 8
+STAGE_ALL = 15
 ROUTE_AUTO, ROUTE_ALL_PREFILL = 0, 1
 DEVERR_BAD_BATCH, DEVERR_BAD_BLOCK, DEVERR_BAD_SLOT, DEVERR_TIMEOUT = 1, 2, 4, 8
 
@@ -39,7 +39,7 @@ class PagedAttentionError(RuntimeError):
 class PaDims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_tokens", "batch_size", "head_size", "num_blocks", "block_size",
-        "max_blocks_per_sequence", "dtype", "decode_split_keys", "route")]
+        "max_blocks_per_sequence", "dtype", "decode_split_keys", "route", "max_query_len")]
 
 
 def load_library():
@@ -72,10 +72,10 @@ def load_library():
 
 
 def make_dims(num_tokens, batch_size, head_size, num_blocks, block_size, max_blocks_per_sequence, dtype,
-              decode_split_keys=0, route=ROUTE_AUTO) -> PaDims:
+              decode_split_keys=0, route=ROUTE_AUTO, max_query_len=0) -> PaDims:
     code = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
     return PaDims(int(num_tokens), int(batch_size), int(head_size), int(num_blocks), int(block_size),
-                  int(max_blocks_per_sequence), code, int(decode_split_keys), int(route))
+                  int(max_blocks_per_sequence), code, int(decode_split_keys), int(route), int(max_query_len))
 
 
 def workspace_size(dims: PaDims, num_heads: int, kv_num_heads: int) -> int:
@@ -107,10 +107,13 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
                     block_table: torch.Tensor, slot_mapping: Optional[torch.Tensor] = None, *,
                     num_heads: int, kv_num_heads: int, scale: float = 0.0,
                     output: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                    decode_split_keys: int = 0, route: int = ROUTE_AUTO, stages: int = STAGE_ALL,
-                    stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+                    decode_split_keys: int = 0, route: int = ROUTE_AUTO, max_query_len: int = 0,
+                    stages: int = STAGE_ALL, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """com.microsoft.PagedAttention on CUDA tensors. Writes key_cache / value_cache in
-    place and returns ``output`` (num_tokens, num_heads * head_size)."""
+    place and returns ``output`` (num_tokens, num_heads * head_size).
+
+    ``max_query_len`` (optional) is a host-side bound on every sequence's new-token count;
+    it lets decode-only batches skip the prefill launch and is checked on the device."""
     lib = load_library()
     if query.dtype not in _DTYPES:
         raise TypeError("query must be float16 or bfloat16")
@@ -136,7 +139,7 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
     if cumulative_sequence_length.shape[0] != B + 1 or block_table.shape[0] != B:
         raise ValueError("cumulative_sequence_length must have batch_size + 1 entries, block_table batch_size rows")
     dims = make_dims(N, B, head_size, num_blocks, block_size, block_table.shape[1], query.dtype,
-                     decode_split_keys, route)
+                     decode_split_keys, route, max_query_len)
     if output is None:
         output = torch.empty((N, num_heads * head_size), dtype=query.dtype, device=query.device)
     if workspace is None:

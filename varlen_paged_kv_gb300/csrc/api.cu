@@ -101,16 +101,18 @@ pa_status check_dims(const pa_dims* d, int32_t nh, int32_t kvh) {
   if (d->block_size % 16 != 0) return PA_ERR_UNSUPPORTED;
   if (d->route != PA_ROUTE_AUTO && d->route != PA_ROUTE_ALL_PREFILL) return PA_ERR_INVALID_ARGUMENT;
   if (d->decode_split_keys < 0 || d->decode_split_keys % pa::kDecTile != 0) return PA_ERR_INVALID_ARGUMENT;
+  if (d->max_query_len < 0) return PA_ERR_INVALID_ARGUMENT;
   if ((int64_t)d->num_blocks * d->block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
   if ((int64_t)d->max_blocks_per_sequence * d->block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
   if ((int64_t)nh * d->head_size > 65536 || kvh > 65536) return PA_ERR_UNSUPPORTED;
   return PA_OK;
 }
 
-pa_status launch_all(const pa::Args& args, const pa_dims* d, const void* query, void* kc, void* vc, uint32_t stages,
+pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* kc, void* vc, uint32_t stages,
                      cudaStream_t stream) {
   DeviceInfo info;
   if (!device_info(&info)) return PA_ERR_CUDA;
+  args.dec_ctas = std::min(pa::kDecCtasPerSm * info.sms, pa::kMaxDecCtas);
   const pa_dtype dt = (pa_dtype)d->dtype;
   const bool bf16 = dt == PA_BFLOAT16;
   const int hs = args.hs;
@@ -127,7 +129,9 @@ pa_status launch_all(const pa::Args& args, const pa_dims* d, const void* query, 
     if (pa::launch_cache_write(args, (int)blocks, stream) != cudaSuccess) return PA_ERR_CUDA;
   }
   const bool can_decode = d->route == PA_ROUTE_AUTO;
-  if ((stages & PA_STAGE_PREFILL) && args.N > 0 && slots > 0) {
+  // a host bound max_query_len with max_query_len * G <= 16 proves every sequence decode-class
+  const bool can_prefill = !(can_decode && d->max_query_len > 0 && (int64_t)d->max_query_len * args.G <= pa::kDecRows);
+  if ((stages & PA_STAGE_PREFILL) && can_prefill && args.N > 0 && slots > 0) {
     const int seg = gcd(d->block_size, pa::kPreTileK);
     CUtensorMap tq, tk, tv;
     if (!query_map(&tq, query, dt, args.q_stride, args.N) || !cache_map(&tk, kc, dt, hs, args.kvh, slots, seg) ||
@@ -144,17 +148,8 @@ pa_status launch_all(const pa::Args& args, const pa_dims* d, const void* query, 
     CUtensorMap tk, tv;
     if (!cache_map(&tk, kc, dt, hs, args.kvh, slots, seg) || !cache_map(&tv, vc, dt, hs, args.kvh, slots, seg))
       return PA_ERR_CUDA;
-    const int grid = (int)std::min<int64_t>(args.max_items, 2 * info.sms);
-    if (grid > 0) {
-      ++g_launches;
-      if (pa::launch_decode(args, bf16, tk, tv, seg, grid, stream) != cudaSuccess) return PA_ERR_CUDA;
-    }
-  }
-  if ((stages & PA_STAGE_MERGE) && can_decode && args.N > 0 && args.max_merge > 0) {
-    const int64_t warps = (int64_t)args.max_merge * args.nh;
-    const int grid = (int)std::min<int64_t>((warps + 3) / 4, (int64_t)info.sms * 8);
     ++g_launches;
-    if (pa::launch_merge(args, bf16, grid, stream) != cudaSuccess) return PA_ERR_CUDA;
+    if (pa::launch_decode(args, bf16, tk, tv, seg, stream) != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;
 }
@@ -222,6 +217,7 @@ pa_status pa_paged_attention_stages(const void* query, const void* key, const vo
   a.v_offset = a.packed ? (num_heads + kv_num_heads) * hs : 0;
   a.forced_split = dims->decode_split_keys;
   a.route = dims->route;
+  a.max_query_len = dims->max_query_len;
   const float sc = scale == 0.0f ? 1.0f / sqrtf((float)hs) : scale;
   a.scale_log2 = sc * 1.4426950408889634f;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -229,12 +225,12 @@ pa_status pa_paged_attention_stages(const void* query, const void* key, const vo
   a.items = reinterpret_cast<pa::DecodeItem*>(ws + L.items);
   a.tiles = reinterpret_cast<pa::PrefillTile*>(ws + L.tiles);
   a.tiles_unsorted = reinterpret_cast<pa::PrefillTile*>(ws + L.tiles_unsorted);
-  a.merge = reinterpret_cast<pa::MergeRow*>(ws + L.merge);
+  a.cta_begin = reinterpret_cast<int32_t*>(ws + L.cta_begin);
+  a.unit_done = reinterpret_cast<int32_t*>(ws + L.unit_done);
   a.part_o = reinterpret_cast<float*>(ws + L.part_o);
   a.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   a.max_items = L.max_items;
   a.max_tiles = L.max_tiles;
-  a.max_merge = L.max_merge;
 
   return launch_all(a, dims, query, key_cache, value_cache, stages, static_cast<cudaStream_t>(stream));
 }

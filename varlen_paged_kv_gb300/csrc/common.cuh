@@ -19,8 +19,8 @@ constexpr int kDecTile = 64;          // keys per decode pipeline stage
 constexpr int kDecStages = 3;         // decode K/V ring depth
 constexpr int kDecWarps = 4;          // decode consumer warps (16 keys of a tile each)
 constexpr int kDecRows = 16;          // query rows per decode work item (one m16 MMA tile)
-constexpr int kDecTargetCtas = 1024;  // decode work items aimed for when splits are automatic
-constexpr int kDecMinSplit = 256;     // smallest automatic split, keys
+constexpr int kDecCtasPerSm = 2;      // resident decode CTAs per SM (shared-memory bound)
+constexpr int kMaxDecCtas = 1024;     // upper bound of the decode grid
 constexpr int kPreTileQ = 128;        // query rows per prefill tile (MMA M)
 constexpr int kPreTileK = 128;        // keys per prefill KV tile (MMA N of Q K^T, K of P V)
 constexpr int kSortCap = 4096;        // prefill tiles the planner sorts by cost
@@ -31,64 +31,56 @@ struct WsHeader {
   int32_t valid;            // 1 when the planner accepted the batch
   int32_t n_decode_items;
   int32_t n_prefill_tiles;
-  int32_t n_merge_rows;
-  int32_t split_keys;
-  int32_t pad[58];
+  int32_t dec_ctas;         // decode grid the item ranges were cut for
+  int32_t pad[59];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
-struct DecodeItem {     // one (sequence, KV head, key range) of a decode-class sequence
+// One (sequence b, KV head g, key range) of a decode-class sequence. The (b, g) pair is a
+// "unit"; a unit cut into several items has each item write an fp32 partial, and the
+// last item to finish (counted in unit_done) merges them in key order.
+struct DecodeItem {
   int32_t b, g, key_begin, key_end;
-  int32_t partial;      // partial-result slot, or -1 when this item is the whole sequence
-  int32_t n_split;
-  int32_t pad[2];
+  int32_t unit;         // b * kv_num_heads + g
+  int32_t unit_first;   // index of the unit's first item (its items are consecutive)
+  int32_t n_split;      // items in the unit; 1 = the item writes the output itself
+  int32_t pad;
 };
 
 struct PrefillTile {    // 128 query rows [j0, j0+128) of sequence b (all heads)
   int32_t b, j0;
 };
 
-struct MergeRow {       // a decode-class query row whose splits need merging
-  int32_t token, b;
-  int32_t first_item;   // item of (b, KV head 0, split 0); head g's splits start at first_item + g*n_split
-  int32_t n_split;
-};
-
 struct WsLayout {
-  size_t header, items, tiles, tiles_unsorted, merge, part_o, part_lse, total;
-  int32_t max_items, max_tiles, max_merge;
+  size_t header, items, cta_begin, unit_done, tiles, tiles_unsorted, part_o, part_lse, total;
+  int32_t max_items, max_tiles;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Upper bounds of the device-built lists, from host-known sizes only.
-//  - decode pairs (sequence, split): automatic splits are >= total_keys / target_pairs,
-//    so sum_b ceil(kv_b / split) <= target_pairs + B; forced splits give at most
-//    ceil(max_kv / split) per sequence;
-//  - prefill tiles: sum_b ceil(q_b / 128) <= N / 128 + B;
-//  - merge rows: decode-class sequences have q_len <= 16.
+//  - decode items, balanced partition: the concatenated key tiles of all units are cut
+//    into at most kMaxDecCtas contiguous ranges, so items <= kMaxDecCtas + units;
+//  - decode items, forced split length S: at most ceil(max_kv / S) per unit;
+//  - prefill tiles: sum_b ceil(q_b / 128) <= N / 128 + B.
 __host__ __device__ inline WsLayout ws_layout(int32_t N, int32_t B, int32_t kvh, int32_t hs,
                                                int32_t max_blocks, int32_t bs, int32_t forced_split) {
   WsLayout L;
-  int64_t pairs;
-  if (forced_split > 0) {
-    pairs = (int64_t)B * ceil_div((int64_t)max_blocks * bs, forced_split);
-  } else {
-    pairs = ceil_div(kDecTargetCtas, kvh) + B;
-  }
-  int64_t items = pairs * kvh;
+  const int64_t units = (int64_t)B * kvh;
+  int64_t items;
+  if (forced_split > 0) items = units * ceil_div((int64_t)max_blocks * bs, forced_split);
+  else items = kMaxDecCtas + units;
   int64_t tiles = ceil_div(N, kPreTileQ) + (B < N ? B : N);
-  int64_t merge = (int64_t)N < 16 * (int64_t)B ? N : 16 * (int64_t)B;
   L.max_items = (int32_t)items;
   L.max_tiles = (int32_t)tiles;
-  L.max_merge = (int32_t)merge;
   size_t off = 0;
   L.header = off; off += sizeof(WsHeader);
   L.items = off; off = align_up(off + sizeof(DecodeItem) * (size_t)items, 256);
+  L.cta_begin = off; off = align_up(off + sizeof(int32_t) * (kMaxDecCtas + 1), 256);
+  L.unit_done = off; off = align_up(off + sizeof(int32_t) * (size_t)units, 256);
   L.tiles = off; off = align_up(off + sizeof(PrefillTile) * (size_t)tiles, 256);
   L.tiles_unsorted = off; off = align_up(off + sizeof(PrefillTile) * (size_t)tiles, 256);
-  L.merge = off; off = align_up(off + sizeof(MergeRow) * (size_t)merge, 256);
   L.part_o = off; off = align_up(off + sizeof(float) * (size_t)items * kDecRows * hs, 256);
   L.part_lse = off; off = align_up(off + sizeof(float) * (size_t)items * kDecRows, 256);
   L.total = off;
@@ -113,17 +105,20 @@ struct Args {
   int32_t k_offset;       // element offset of K inside a query row (packed) or 0
   int32_t v_offset;
   int32_t packed;
-  int32_t forced_split;
+  int32_t forced_split;   // > 0: decode units cut into items of this many keys
   int32_t route;
+  int32_t max_query_len;  // > 0: host bound on every q_len (checked by the planner)
+  int32_t dec_ctas;       // decode grid size
   float scale_log2;       // scale * log2(e)
   WsHeader* hdr;
   DecodeItem* items;
+  int32_t* cta_begin;     // decode CTA c owns items [cta_begin[c], cta_begin[c + 1])
+  int32_t* unit_done;     // per unit: items finished (for the fused merge)
   PrefillTile* tiles;
   PrefillTile* tiles_unsorted;
-  MergeRow* merge;
   float* part_o;
   float* part_lse;
-  int32_t max_items, max_tiles, max_merge;
+  int32_t max_items, max_tiles;
 };
 
 // ---- shared-memory layouts (bytes) of the attention kernels --------------------------
@@ -133,8 +128,9 @@ struct DecSmem {
   static constexpr int kHalves = HS / 64;
   static constexpr int kTileBytes = kDecTile * HS * 2;      // one K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kComb = kDecStages * kStageBytes;     // float [16][HS]
-  static constexpr int kMw = kComb + kDecRows * HS * 4;      // float [4][16]
+  static constexpr int kCombStride = HS + 4;                 // floats; the pad spreads rows over banks
+  static constexpr int kComb = kDecStages * kStageBytes;     // float [16][kCombStride]
+  static constexpr int kMw = kComb + kDecRows * kCombStride * 4;  // float [4][16]
   static constexpr int kLw = kMw + kDecWarps * kDecRows * 4; // float [4][16]
   static constexpr int kBars = kLw + kDecWarps * kDecRows * 4;
   static constexpr int kAbort = kBars + 2 * kDecStages * 8;
@@ -163,9 +159,8 @@ cudaError_t launch_plan(const Args& a, cudaStream_t s);
 cudaError_t launch_cache_write(const Args& a, int grid, cudaStream_t s);
 cudaError_t launch_prefill(const Args& a, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, int seg, int grid, cudaStream_t s);
-cudaError_t launch_decode(const Args& a, bool bf16, const CUtensorMap& tk, const CUtensorMap& tv, int seg, int grid,
+cudaError_t launch_decode(const Args& a, bool bf16, const CUtensorMap& tk, const CUtensorMap& tv, int seg,
                           cudaStream_t s);
-cudaError_t launch_merge(const Args& a, bool bf16, int grid, cudaStream_t s);
 
 // ---- small device helpers -----------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

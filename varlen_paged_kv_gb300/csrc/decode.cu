@@ -14,11 +14,13 @@
 //     softmax in registers (row max over the quad by shuffles, base-2 exponentials; for
 //     bf16 the weights P enter P V as a bf16 hi + lo pair, two products);
 //   - at the end of the item the four warps' (m, l, O) are combined in a fixed order in
-//     shared memory. A single-split item writes the output row rounded once to T; a split
-//     writes its normalised fp32 partial row and its natural-log lse.
-// The merge kernel then combines the splits of a row in split order (the (out, lse)
-// reduction of the WS2 CP-Aware Attention Contract, "Reduction Semantics": fp32, fixed
-// order, downcast at the final write).
+//     shared memory. An item that is its whole unit writes the output row rounded once to
+//     T; otherwise it writes its normalised fp32 partial row and natural-log lse, and the
+//     last item of the unit to finish (an atomic arrival count) merges the unit's partials
+//     in key order: the (out, lse) reduction of the WS2 CP-Aware Attention Contract,
+//     "Reduction Semantics" (fp32, fixed order, downcast at the final write).
+// CTA c processes the items [cta_begin[c], cta_begin[c+1]) that the planner cut so that
+// every CTA streams the same number of keys.
 #include "common.cuh"
 
 namespace pa {
@@ -45,6 +47,7 @@ __global__ void __launch_bounds__(160, 2)
   using L = DecSmem<HS>;
   constexpr int NKS = HS / 16;  // k-steps of Q K^T
   constexpr int ND = HS / 8;    // n-tiles of P V
+  constexpr int kCombStride = L::kCombStride;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   float* comb = reinterpret_cast<float*>(smem + L::kComb);
@@ -53,6 +56,7 @@ __global__ void __launch_bounds__(160, 2)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBars);
   uint64_t* empty = full + kDecStages;
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
+  volatile int* s_last = reinterpret_cast<volatile int*>(smem + L::kAbort + 4);
   uint32_t* err = &a.hdr->error;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -65,7 +69,7 @@ __global__ void __launch_bounds__(160, 2)
     fence_mbar_init();
   }
   __syncthreads();
-  const int n_items = a.hdr->n_decode_items;
+  const int it_begin = a.cta_begin[blockIdx.x], it_end = a.cta_begin[blockIdx.x + 1];
 
   if (warp == kDecWarps) {
     // ================= producer warp: TMA page loads =================
@@ -76,7 +80,7 @@ __global__ void __launch_bounds__(160, 2)
     const int nseg = kDecTile / seg_rows;
     const int oob = a.num_blocks * a.bs;  // a row coordinate past the end: TMA fills zeros
     uint32_t cnt = 0;
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    for (int it = it_begin; it < it_end; ++it) {
       const DecodeItem item = a.items[it];
       const int kv_len = a.past[item.b] + (a.cum[item.b + 1] - a.cum[item.b]);
       const int* bt = a.block_table + (int64_t)item.b * a.max_blocks;
@@ -114,7 +118,7 @@ __global__ void __launch_bounds__(160, 2)
   const int tq = lane & 3, gq = lane >> 2;  // quad position, row within the 8-row group
   const int r0 = gq, r1 = gq + 8;           // the two rows this thread holds in MMA fragments
   uint32_t cnt = 0;
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+  for (int it = it_begin; it < it_end; ++it) {
     const DecodeItem item = a.items[it];
     const int c0 = a.cum[item.b];
     const int q_len = a.cum[item.b + 1] - c0;
@@ -287,8 +291,8 @@ __global__ void __launch_bounds__(160, 2)
       if (w == ww) {
 #pragma unroll
         for (int d = 0; d < ND; ++d) {
-          float* c0p = comb + r0 * HS + d * 8 + tq * 2;
-          float* c1p = comb + r1 * HS + d * 8 + tq * 2;
+          float* c0p = comb + r0 * kCombStride + d * 8 + tq * 2;
+          float* c1p = comb + r1 * kCombStride + d * 8 + tq * 2;
           if (ww == 0) {
             c0p[0] = o[d][0] * f0;
             c0p[1] = o[d][1] * f0;
@@ -310,15 +314,16 @@ __global__ void __launch_bounds__(160, 2)
       const int row = t >> 3;
       constexpr int CW = HS / 8;
       const int col = (t & 7) * CW;
-      if (row < n_rows) {
-        float M, Lr;
-        row_stats(mw, lw, row, M, Lr);
-        const float inv = Lr > 0.f ? 1.f / Lr : 0.f;
-        const float* src = comb + row * HS + col;
-        if (item.partial < 0) {
-          const int tok = c0 + row / a.G;
-          const int head = item.g * a.G + row % a.G;
-          uint16_t* dst = reinterpret_cast<uint16_t*>(a.output) + ((int64_t)tok * a.nh + head) * HS + col;
+      const bool mine = row < n_rows;
+      const int tok = c0 + row / a.G;
+      const int head = item.g * a.G + row % a.G;
+      uint16_t* dst = reinterpret_cast<uint16_t*>(a.output) + ((int64_t)tok * a.nh + head) * HS + col;
+      float M = 0.f, Lr = 0.f;
+      if (mine) row_stats(mw, lw, row, M, Lr);
+      const float inv = Lr > 0.f ? 1.f / Lr : 0.f;
+      const float* src = comb + row * kCombStride + col;
+      if (item.n_split == 1) {
+        if (mine) {
 #pragma unroll
           for (int v = 0; v < CW; v += 8) {
             uint4 pk;
@@ -328,15 +333,57 @@ __global__ void __launch_bounds__(160, 2)
             pk.w = pack2<BF16>(src[v + 6] * inv, src[v + 7] * inv);
             *reinterpret_cast<uint4*>(dst + v) = pk;
           }
-        } else {
-          float* dst = a.part_o + ((int64_t)item.partial * kDecRows + row) * HS + col;
+        }
+      } else {
+        if (mine) {
+          float* pdst = a.part_o + ((int64_t)it * kDecRows + row) * HS + col;
 #pragma unroll
           for (int v = 0; v < CW; v += 4)
-            *reinterpret_cast<float4*>(dst + v) =
+            *reinterpret_cast<float4*>(pdst + v) =
                 make_float4(src[v] * inv, src[v + 1] * inv, src[v + 2] * inv, src[v + 3] * inv);
           if ((t & 7) == 0)
-            a.part_lse[(int64_t)item.partial * kDecRows + row] =
+            a.part_lse[(int64_t)it * kDecRows + row] =
                 Lr > 0.f ? (M + fast_log2(Lr)) * 0.69314718055994531f : -INFINITY;
+        }
+        __threadfence();  // this thread's partial is visible device-wide before the arrival
+        consumer_bar();
+        if (t == 0) *s_last = atomicAdd(&a.unit_done[item.unit], 1) == item.n_split - 1;
+        consumer_bar();
+        if (*s_last && mine) {
+          // the unit's other items have all arrived: merge its partials in key order
+          __threadfence();
+          float Mx = -INFINITY;
+          for (int s2 = 0; s2 < item.n_split; ++s2)
+            Mx = fmaxf(Mx, __ldcg(a.part_lse + (int64_t)(item.unit_first + s2) * kDecRows + row));
+          float acc[CW];
+#pragma unroll
+          for (int v = 0; v < CW; ++v) acc[v] = 0.f;
+          float den = 0.f;
+          for (int s2 = 0; s2 < item.n_split; ++s2) {
+            const int64_t pr = (int64_t)(item.unit_first + s2) * kDecRows + row;
+            const float lse = __ldcg(a.part_lse + pr);
+            const float wgt = lse == -INFINITY ? 0.f : fast_exp2((lse - Mx) * 1.4426950408889634f);
+            den += wgt;
+            const float4* ps = reinterpret_cast<const float4*>(a.part_o + pr * HS + col);
+#pragma unroll
+            for (int v = 0; v < CW / 4; ++v) {
+              const float4 x4 = __ldcg(ps + v);
+              acc[4 * v + 0] += wgt * x4.x;
+              acc[4 * v + 1] += wgt * x4.y;
+              acc[4 * v + 2] += wgt * x4.z;
+              acc[4 * v + 3] += wgt * x4.w;
+            }
+          }
+          const float dinv = 1.f / den;
+#pragma unroll
+          for (int v = 0; v < CW; v += 8) {
+            uint4 pk;
+            pk.x = pack2<BF16>(acc[v + 0] * dinv, acc[v + 1] * dinv);
+            pk.y = pack2<BF16>(acc[v + 2] * dinv, acc[v + 3] * dinv);
+            pk.z = pack2<BF16>(acc[v + 4] * dinv, acc[v + 5] * dinv);
+            pk.w = pack2<BF16>(acc[v + 6] * dinv, acc[v + 7] * dinv);
+            *reinterpret_cast<uint4*>(dst + v) = pk;
+          }
         }
       }
     }
@@ -344,68 +391,21 @@ __global__ void __launch_bounds__(160, 2)
   }
 }
 
-// One warp per (merged row, query head): lse-weighted mean of the splits' partial rows,
-// splits taken in order, fp32, rounded once to T.
-template <int HS, bool BF16>
-__global__ void __launch_bounds__(128) merge_kernel(const Args a) {
-  const int n_tasks = a.hdr->n_merge_rows * a.nh;
-  const int lane = threadIdx.x & 31;
-  const int nwarps = (gridDim.x * blockDim.x) >> 5;
-  constexpr int PER = HS / 32;
-  for (int task = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < n_tasks; task += nwarps) {
-    const MergeRow mr = a.merge[task / a.nh];
-    const int h = task % a.nh;
-    const int g = h / a.G, hq = h % a.G;
-    const int row = (mr.token - a.cum[mr.b]) * a.G + hq;
-    const int first = mr.first_item + g * mr.n_split;
-    float M = -INFINITY;
-    for (int s = 0; s < mr.n_split; ++s) M = fmaxf(M, a.part_lse[(int64_t)(first + s) * kDecRows + row]);
-    float acc[PER];
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    float den = 0.f;
-    for (int s = 0; s < mr.n_split; ++s) {
-      const int64_t pr = (int64_t)(first + s) * kDecRows + row;
-      const float lse = a.part_lse[pr];
-      const float wgt = lse == -INFINITY ? 0.f : fast_exp2((lse - M) * 1.4426950408889634f);
-      den += wgt;
-      const float* src = a.part_o + pr * HS + lane * PER;
-#pragma unroll
-      for (int e = 0; e < PER; ++e) acc[e] += wgt * src[e];
-    }
-    const float inv = 1.f / den;
-    uint16_t* dst = reinterpret_cast<uint16_t*>(a.output) + ((int64_t)mr.token * a.nh + h) * HS + lane * PER;
-#pragma unroll
-    for (int e = 0; e < PER; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = pack2<BF16>(acc[e] * inv, acc[e + 1] * inv);
-  }
-}
-
 // ---- host launchers (kernels are launched from the translation unit that defines them) ----
 template <int HS, bool BF16>
-static cudaError_t launch_decode_t(const Args& a, const CUtensorMap& tk, const CUtensorMap& tv, int seg, int grid,
+static cudaError_t launch_decode_t(const Args& a, const CUtensorMap& tk, const CUtensorMap& tv, int seg,
                                    cudaStream_t s) {
   constexpr int smem = DecSmem<HS>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<HS, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<HS, BF16><<<grid, 160, smem, s>>>(a, tk, tv, seg);
+  decode_kernel<HS, BF16><<<a.dec_ctas, 160, smem, s>>>(a, tk, tv, seg);
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode(const Args& a, bool bf16, const CUtensorMap& tk, const CUtensorMap& tv, int seg, int grid,
+cudaError_t launch_decode(const Args& a, bool bf16, const CUtensorMap& tk, const CUtensorMap& tv, int seg,
                           cudaStream_t s) {
-  if (a.hs == 64) return bf16 ? launch_decode_t<64, true>(a, tk, tv, seg, grid, s) : launch_decode_t<64, false>(a, tk, tv, seg, grid, s);
-  return bf16 ? launch_decode_t<128, true>(a, tk, tv, seg, grid, s) : launch_decode_t<128, false>(a, tk, tv, seg, grid, s);
-}
-
-cudaError_t launch_merge(const Args& a, bool bf16, int grid, cudaStream_t s) {
-  if (a.hs == 64) {
-    if (bf16) merge_kernel<64, true><<<grid, 128, 0, s>>>(a);
-    else merge_kernel<64, false><<<grid, 128, 0, s>>>(a);
-  } else {
-    if (bf16) merge_kernel<128, true><<<grid, 128, 0, s>>>(a);
-    else merge_kernel<128, false><<<grid, 128, 0, s>>>(a);
-  }
-  return cudaGetLastError();
+  if (a.hs == 64) return bf16 ? launch_decode_t<64, true>(a, tk, tv, seg, s) : launch_decode_t<64, false>(a, tk, tv, seg, s);
+  return bf16 ? launch_decode_t<128, true>(a, tk, tv, seg, s) : launch_decode_t<128, false>(a, tk, tv, seg, s);
 }
 
 }  // namespace pa

@@ -1,18 +1,23 @@
 // Device work partitioner. One CTA reads cumulative_sequence_length and past_seqlens
 // (which stay on the device: the host never sees them) and writes the work lists the
 // attention kernels consume:
-//   - decode-class sequences (q_len * G <= 16 query rows per KV head): split-KV items
-//     (sequence, KV head, key range), with one split length for the whole batch chosen so
-//     that about kDecTargetCtas items exist, never below kDecMinSplit keys, always a
-//     multiple of the 64-key decode tile; items of one sequence are contiguous, head-major;
+//   - decode-class sequences (q_len * G <= 16 query rows per KV head): each (sequence,
+//     KV head) pair is a unit of ceil(kv_len / 64) key tiles. The units' tiles, laid end
+//     to end, are cut into dec_ctas equal contiguous ranges, one per resident decode CTA;
+//     a unit crossing a cut becomes several items whose partial results are merged by
+//     the last of them to finish. Every CTA thus streams the same number of keys
+//     (within one tile). With a forced split length the units are instead cut every S
+//     keys and the items dealt to the CTAs in contiguous blocks (a test hook);
 //   - prefill-class sequences: 128-row query tiles, sorted by their number of 128-key KV
 //     tiles, largest first, so the persistent prefill grid takes the long causal tiles
-//     first (longest-processing-time order);
-//   - the query rows whose decode splits must be merged.
-// The lists depend only on the inputs and on compile-time constants, so results are
-// bitwise reproducible. If the batch description is inconsistent (cum not a prefix sum
-// ending at N, a negative past, a sequence longer than its block_table row) nothing is
+//     first (longest-processing-time order).
+// The lists depend only on the inputs, the decode grid size and compile-time constants,
+// so results are bitwise reproducible on a given GPU. If the batch description is
+// inconsistent (cum not a prefix sum ending at N, a negative past, a sequence longer than
+// its block_table row, a q_len above the host's max_query_len bound) nothing is
 // scheduled and PA_DEVERR_BAD_BATCH is raised.
+#include <limits.h>
+
 #include "common.cuh"
 
 namespace pa {
@@ -63,126 +68,154 @@ __device__ void block_scan3(const int v[3], int ex[3], int tot[3], int (*s_warp)
   __syncthreads();
 }
 
+// decode CTA whose key-tile range holds tile t: largest c with floor(c W / P) <= t
+__device__ __forceinline__ int cta_of(int64_t t, int64_t W, int64_t P) { return (int)(((t + 1) * P - 1) / W); }
+__device__ __forceinline__ int64_t cta_start(int64_t c, int64_t W, int64_t P) { return c * W / P; }
+
+__device__ __forceinline__ void refuse(WsHeader* hdr) {
+  atomicOr(&hdr->error, PA_DEVERR_BAD_BATCH);
+  hdr->valid = 0;
+  hdr->n_decode_items = hdr->n_prefill_tiles = 0;
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
   __shared__ int s_bad;
-  __shared__ unsigned long long s_dec_keys;
+  __shared__ unsigned long long s_dec_tiles;
   __shared__ int s_warp[3][32];
   __shared__ int s_carry[3];
+  __shared__ int s_cta_begin[kMaxDecCtas + 1];
   __shared__ unsigned long long s_key[kSortCap];
 
   const int tid = threadIdx.x;
   WsHeader* hdr = a.hdr;
+  const int64_t P = a.dec_ctas;
   if (tid == 0) {
     s_bad = 0;
-    s_dec_keys = 0;
+    s_dec_tiles = 0;
     s_carry[0] = s_carry[1] = s_carry[2] = 0;
     hdr->error = 0;  // error bits describe the most recent call
   }
+  for (int c = tid; c <= P; c += blockDim.x) s_cta_begin[c] = INT_MAX;
   __syncthreads();
 
-  // ---- validate the batch description and total the decode keys ----
+  // ---- validate the batch description; count the decode key tiles ----
   const int64_t max_kv = (int64_t)a.max_blocks * a.bs;
   if (tid == 0 && (a.cum[0] != 0 || a.cum[a.B] != a.N)) s_bad = 1;
   for (int b = tid; b < a.B; b += blockDim.x) {
     const int64_t q = (int64_t)a.cum[b + 1] - a.cum[b];
     const int64_t kv = (int64_t)a.past[b] + q;
-    if (q < 0 || a.past[b] < 0 || kv > max_kv) {
+    if (q < 0 || a.past[b] < 0 || kv > max_kv || (a.max_query_len > 0 && q > a.max_query_len)) {
       atomicOr(&s_bad, 1);
     } else if (is_decode_class(q, a)) {
-      atomicAdd(&s_dec_keys, (unsigned long long)kv);
+      atomicAdd(&s_dec_tiles, (unsigned long long)ceil_div(kv, kDecTile));
     }
   }
+  for (int u = tid; u < a.B * a.kvh; u += blockDim.x) a.unit_done[u] = 0;
   __syncthreads();
   if (s_bad) {
-    if (tid == 0) {
-      atomicOr(&hdr->error, PA_DEVERR_BAD_BATCH);
-      hdr->valid = 0;
-      hdr->n_decode_items = hdr->n_prefill_tiles = hdr->n_merge_rows = 0;
-    }
+    if (tid == 0) refuse(hdr);
     return;
   }
-
-  // ---- one split length for the batch ----
-  int64_t split;
-  if (a.forced_split > 0) {
-    split = a.forced_split;
-  } else {
-    const int64_t pairs = ceil_div(kDecTargetCtas, a.kvh);
-    split = ceil_div((int64_t)s_dec_keys, pairs);
-    split = ceil_div(split, kDecTile) * kDecTile;
-    if (split < kDecMinSplit) split = kDecMinSplit;
-  }
+  const int64_t W = (int64_t)s_dec_tiles * a.kvh;  // decode key tiles of all units, end to end
+  const bool balanced = a.forced_split <= 0;
 
   // ---- per-sequence counts, prefix sums, and the lists ----
   for (int base = 0; base < a.B; base += blockDim.x) {
     const int b = base + tid;
     const int carry0 = s_carry[0], carry1 = s_carry[1], carry2 = s_carry[2];
-    int v[3] = {0, 0, 0};
-    int64_t q = 0, kv = 0, nsplit = 0;
+    int64_t q = 0, kv = 0, nt = 0;
+    bool dec = false;
+    int v[3] = {0, 0, 0};  // [decode tiles of b's units, prefill tiles, -]
     if (b < a.B) {
       q = (int64_t)a.cum[b + 1] - a.cum[b];
       kv = (int64_t)a.past[b] + q;
-      if (is_decode_class(q, a)) {
-        nsplit = ceil_div(kv, split);
-        v[0] = (int)(nsplit * a.kvh);
-        if (nsplit > 1) v[2] = (int)q;
+      dec = is_decode_class(q, a);
+      if (dec) {
+        nt = ceil_div(kv, kDecTile);
+        v[0] = (int)(nt * a.kvh);
       } else if (q > 0) {
         v[1] = (int)ceil_div(q, kPreTileQ);
       }
     }
     int ex[3], tot[3];
     block_scan3(v, ex, tot, s_warp);
+    const int64_t T_b = (int64_t)carry0 + ex[0];  // first decode tile of (b, head 0)
+    // items of this sequence
+    int w[3] = {0, 0, 0};
+    if (dec) {
+      if (balanced) {
+        for (int g = 0; g < a.kvh; ++g) {
+          const int64_t u0 = T_b + g * nt, u1 = u0 + nt;
+          w[0] += cta_of(u1 - 1, W, P) - cta_of(u0, W, P) + 1;
+        }
+      } else {
+        w[0] = (int)(a.kvh * ceil_div(kv, a.forced_split));
+      }
+    }
+    int ex2[3], tot2[3];
+    block_scan3(w, ex2, tot2, s_warp);
     if (b < a.B) {
-      const int dbase = carry0 + ex[0];
-      const int tbase = carry1 + ex[1];
-      const int mbase = carry2 + ex[2];
-      for (int g = 0; g < (v[0] ? a.kvh : 0); ++g) {
-        for (int s = 0; s < nsplit; ++s) {
-          const int idx = dbase + g * (int)nsplit + s;
-          if (idx >= a.max_items) break;
-          DecodeItem it;
-          it.b = b;
-          it.g = g;
-          it.key_begin = (int)(s * split);
-          it.key_end = (int)(((s + 1) * split < kv) ? (s + 1) * split : kv);
-          it.partial = nsplit > 1 ? idx : -1;
-          it.n_split = (int)nsplit;
-          it.pad[0] = 0;
-          it.pad[1] = 0;
-          a.items[idx] = it;
+      int idx = carry2 + ex2[0];
+      if (dec) {
+        for (int g = 0; g < a.kvh; ++g) {
+          const int unit_first = idx;
+          if (balanced) {
+            const int64_t u0 = T_b + g * nt, u1 = u0 + nt;
+            const int c0 = cta_of(u0, W, P), c1 = cta_of(u1 - 1, W, P);
+            for (int c = c0; c <= c1; ++c, ++idx) {
+              const int64_t lo = max(u0, cta_start(c, W, P)), hi = min(u1, cta_start(c + 1, W, P));
+              if (idx < a.max_items)
+                a.items[idx] = DecodeItem{b, g, (int)((lo - u0) * kDecTile), (int)min((hi - u0) * kDecTile, kv),
+                                          b * a.kvh + g, unit_first, c1 - c0 + 1, 0};
+              if (cta_start(c, W, P) >= u0) s_cta_begin[c] = idx;  // CTA c's range starts in this unit
+            }
+          } else {
+            const int64_t S = a.forced_split;
+            const int ns = (int)ceil_div(kv, S);
+            for (int s2 = 0; s2 < ns; ++s2, ++idx) {
+              if (idx < a.max_items)
+                a.items[idx] = DecodeItem{b, g, (int)(s2 * S), (int)min((s2 + 1) * S, kv), b * a.kvh + g,
+                                          unit_first, ns, 0};
+            }
+          }
         }
       }
       for (int t = 0; t < v[1]; ++t) {
-        const int idx = tbase + t;
-        if (idx < a.max_tiles) a.tiles_unsorted[idx] = PrefillTile{b, t * kPreTileQ};
-      }
-      for (int j = 0; j < v[2]; ++j) {
-        const int idx = mbase + j;
-        if (idx < a.max_merge) a.merge[idx] = MergeRow{a.cum[b] + j, b, dbase, (int)nsplit};
+        const int ti = carry1 + ex[1] + t;
+        if (ti < a.max_tiles) a.tiles_unsorted[ti] = PrefillTile{b, t * kPreTileQ};
       }
     }
     __syncthreads();  // every thread has read the carries of this round
     if (tid == 0) {
       s_carry[0] += tot[0];
       s_carry[1] += tot[1];
-      s_carry[2] += tot[2];
+      s_carry[2] += tot2[0];
     }
     __syncthreads();
   }
 
-  const int n_items = s_carry[0], n_tiles = s_carry[1], n_merge = s_carry[2];
-  if (n_items > a.max_items || n_tiles > a.max_tiles || n_merge > a.max_merge) {
+  const int n_items = s_carry[2], n_tiles = s_carry[1];
+  if (n_items > a.max_items || n_tiles > a.max_tiles) {
     // cannot happen for a batch that passed validation (the bounds are proven in
     // ws_layout); refuse rather than run a truncated plan
-    if (tid == 0) {
-      atomicOr(&hdr->error, PA_DEVERR_BAD_BATCH);
-      hdr->valid = 0;
-      hdr->n_decode_items = hdr->n_prefill_tiles = hdr->n_merge_rows = 0;
-    }
+    if (tid == 0) refuse(hdr);
     return;
   }
+
+  // ---- item range of every decode CTA ----
+  if (balanced) {
+    if (tid == 0) {
+      s_cta_begin[P] = n_items;
+      for (int64_t c = P - 1; c >= 0; --c)  // CTAs with an empty range (fewer tiles than CTAs)
+        if (s_cta_begin[c] == INT_MAX) s_cta_begin[c] = s_cta_begin[c + 1];
+    }
+  } else {
+    for (int64_t c = tid; c <= P; c += blockDim.x) s_cta_begin[c] = (int)(c * n_items / P);
+  }
+  __syncthreads();
+  for (int c = tid; c <= P; c += blockDim.x) a.cta_begin[c] = s_cta_begin[c];
 
   // ---- prefill tiles: sort by KV-tile count, descending (ties: list order) ----
   if (n_tiles <= kSortCap) {
@@ -224,8 +257,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
     hdr->valid = 1;
     hdr->n_decode_items = n_items;
     hdr->n_prefill_tiles = n_tiles;
-    hdr->n_merge_rows = n_merge;
-    hdr->split_keys = (int)split;
+    hdr->dec_ctas = (int)P;
   }
 }
 
