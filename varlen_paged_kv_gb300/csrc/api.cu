@@ -137,7 +137,8 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
     if (!query_map(&tq, query, dt, args.q_stride, args.N) || !cache_map(&tk, kc, dt, hs, args.kvh, slots, seg) ||
         !cache_map(&tv, vc, dt, hs, args.kvh, slots, seg))
       return PA_ERR_CUDA;
-    const int grid = (int)std::min<int64_t>((int64_t)args.max_tiles * args.nh, info.sms);
+    const int heads_per_unit = (args.G % 2 == 0) ? 2 : 1;  // two heads of one KV group share a unit
+    const int grid = (int)std::min<int64_t>((int64_t)args.max_tiles * (args.nh / heads_per_unit), info.sms);
     if (grid > 0) {
       ++g_launches;
       if (pa::launch_prefill(args, bf16, tq, tk, tv, seg, grid, stream) != cudaSuccess) return PA_ERR_CUDA;

@@ -140,15 +140,16 @@ struct DecSmem {
 // Prefill: Q tile, two K and two V tiles, barriers, the TMEM address slot.
 template <int HS>
 struct PreSmem {
-  static constexpr int kQBytes = kPreTileQ * HS * 2;
+  static constexpr int kQBytes = kPreTileQ * HS * 2;  // one query tile (one head)
   static constexpr int kKVBytes = kPreTileK * HS * 2;
   static constexpr int kHalfBytes = kPreTileK * 128;  // one 64-column slab of a tile
-  static constexpr int kQ = 0;
-  static constexpr int kK0 = kQ + kQBytes;
+  static constexpr int kQ = 0;                        // Q of head A, then Q of head B
+  static constexpr int kK0 = kQ + 2 * kQBytes;
   static constexpr int kV0 = kK0 + 2 * kKVBytes;
   static constexpr int kBars = kV0 + 2 * kKVBytes;
-  // barriers: q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_done, o_free
-  static constexpr int kNumBars = 16;
+  // q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2], and per head (A, B):
+  // s_full, p_full, o_done, o_free
+  static constexpr int kNumBars = 18;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kBytes = kAbort + 12 + 1024;
