@@ -20,10 +20,11 @@
 //               (where the softmax wrote it over S) and V from shared memory; fp32
 //               accumulators in TMEM.
 //   warps 2..5  softmax of head A, warps 6..9 softmax of head B: thread i owns TMEM lane /
-//               query row i. Per tile: a first pass over S for the row max, the running
-//               max update (O is rescaled only when the max grew by more than 2^8, exact
-//               because the final division uses the same stale max), a second pass
-//               computing P = exp2(s * scale * log2 e - m) and writing it over S as 16-bit
+//               query row i. Per tile: one 128-column TMEM load of the S row, keys past the
+//               row's causal limit replaced by -inf, the row max (three-input max on four
+//               independent chains), the running max update (O is rescaled only when the
+//               max grew by more than 2^8, exact because the final division uses the same
+//               stale max), then P = exp2(s * scale * log2 e - m) written over S as 16-bit
 //               pairs: for bf16 as a hi part bf16(p) and a lo part bf16(p - hi), multiplied
 //               by V separately, so the weights keep ~16 significant bits instead of 8.
 //               At the end of the unit the row of O is normalised and stored.
@@ -44,7 +45,7 @@ __device__ __forceinline__ uint32_t o_col(int x) { return x ? 384u : 256u; }
 __device__ __forceinline__ uint32_t p_col(int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); }
 
 template <int HS, bool BF16>
-__global__ void __launch_bounds__(kPreThreads, 1)
+__global__ void __maxnreg__(200)
     prefill_kernel(const Args a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const int seg_rows) {
   using L = PreSmem<HS>;
@@ -274,26 +275,31 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           tc_fence_after();
           const int key0 = t * kPreTileK;
           const bool masked = (key0 + kPreTileK - 1 > lim_tile0) || (key0 + kPreTileK > kv_len);
-          // ---- pass 1: the row's max of s * c (taken on raw s: max, or min for c < 0) ----
-          float mr = c > 0.f ? -INFINITY : INFINITY;
-#pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t r[32];
-            tmem_ld_x32(s_tmem + cc * 32, r);
-            if (c > 0.f) {
+          uint32_t r[kPreTileK];
+          tmem_ld_x128(s_tmem, r);
+          // keys past this row's limit become -inf for s * c (so both the max and exp2 ignore them)
+          const float sentinel = c > 0.f ? -INFINITY : INFINITY;
+          if (masked) {
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const float v = __uint_as_float(r[e]);
-                mr = (masked && key0 + cc * 32 + e > lim) ? mr : fmaxf(mr, v);
-              }
-            } else {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const float v = __uint_as_float(r[e]);
-                mr = (masked && key0 + cc * 32 + e > lim) ? mr : fminf(mr, v);
-              }
-            }
+            for (int e = 0; e < kPreTileK; ++e)
+              if (key0 + e > lim) r[e] = __float_as_uint(sentinel);
           }
+          // ---- the row's max of s * c, taken on raw s (max, or min for c < 0), four chains ----
+          float mc[4] = {sentinel, sentinel, sentinel, sentinel};
+          if (c > 0.f) {
+#pragma unroll
+            for (int e = 0; e < kPreTileK; e += 8)
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mc[k] = fmax3(mc[k], __uint_as_float(r[e + 2 * k]), __uint_as_float(r[e + 2 * k + 1]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < kPreTileK; e += 8)
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mc[k] = fmin3(mc[k], __uint_as_float(r[e + 2 * k]), __uint_as_float(r[e + 2 * k + 1]));
+          }
+          const float mr = c > 0.f ? fmax3(fmaxf(mc[0], mc[1]), mc[2], mc[3]) : fmin3(fminf(mc[0], mc[1]), mc[2], mc[3]);
           const float m_tile = mr * c;
           const float m_new = fmaxf(m_used, m_tile);
           const bool any_grow = __any_sync(0xffffffffu, m_new > m_used + 8.0f);  // first tile: m_used = -inf
@@ -303,23 +309,18 @@ __global__ void __launch_bounds__(kPreThreads, 1)
             m_used = m_new;
             l *= alpha;
           }
-          // ---- pass 2: P = exp2(s * c - m), written over S in place ----
+          // ---- P = exp2(s * c - m), written over S in place, 32 columns at a time ----
           const float neg_m = -m_used;
-#pragma unroll 1
+          float lc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
-            uint32_t r[32];
-            tmem_ld_x32(s_tmem + cc * 32, r);
             uint32_t w[32];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              float p0 = fast_exp2(fmaf(__uint_as_float(r[2 * e]), c, neg_m));
-              float p1 = fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), c, neg_m));
-              if (masked) {
-                const int k = key0 + cc * 32 + 2 * e;
-                p0 = k > lim ? 0.f : p0;
-                p1 = k + 1 > lim ? 0.f : p1;
-              }
-              l += p0 + p1;
+              const float p0 = fast_exp2(fmaf(__uint_as_float(r[cc * 32 + 2 * e]), c, neg_m));
+              const float p1 = fast_exp2(fmaf(__uint_as_float(r[cc * 32 + 2 * e + 1]), c, neg_m));
+              lc[(2 * e) & 3] += p0;
+              lc[(2 * e + 1) & 3] += p1;
               if constexpr (BF16) {
                 split_bf16x2(p0, p1, w[e], w[16 + e]);
               } else {
@@ -327,8 +328,10 @@ __global__ void __launch_bounds__(kPreThreads, 1)
                 w[16 + e] = 0u;
               }
             }
-            tmem_st_x32(s_tmem + cc * 32, w);
+            tmem_st_x32_nowait(s_tmem + cc * 32, w);
           }
+          l += (lc[0] + lc[1]) + (lc[2] + lc[3]);
+          tmem_wait_st();
           if (t > 0) {
             // O holds P_0..P_{t-2} V; wait for P_{t-1} V before rescaling it
             mbar_wait(&o_done[x], (gt - 1) & 1, abort, err);
@@ -355,12 +358,12 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           const bool store = tile.j0 + row < q_len;
           uint16_t* dst = reinterpret_cast<uint16_t*>(a.output) + ((int64_t)(c0 + tile.j0 + row) * a.nh + h) * HS;
 #pragma unroll 1
-          for (int cc = 0; cc < HS; cc += 32) {
-            uint32_t ov[32];
-            tmem_ld_x32(o_tmem + cc, ov);
+          for (int cc = 0; cc < HS; cc += 128) {
+            uint32_t ov[128];
+            tmem_ld_x128(o_tmem + cc, ov);
             if (store) {
 #pragma unroll
-              for (int v = 0; v < 32; v += 8) {
+              for (int v = 0; v < 128; v += 8) {
                 uint4 pk;
                 pk.x = pack2<BF16>(__uint_as_float(ov[v + 0]) * inv, __uint_as_float(ov[v + 1]) * inv);
                 pk.y = pack2<BF16>(__uint_as_float(ov[v + 2]) * inv, __uint_as_float(ov[v + 3]) * inv);
