@@ -150,6 +150,10 @@ pa_status pa_paged_attention_stages(const void* query, const void* key, const vo
 /* Static description of a status code. Never NULL. */
 const char* pa_status_string(pa_status status);
 
+/* Message of the last PA_ERR_CUDA returned to the calling host thread (the failing call and
+ * the CUDA error string), "no error" before any. Valid until the thread's next failing call. */
+const char* pa_last_error(void);
+
 /*
  * Debug/test helper: waits for `stream`, copies the workspace's device error word
  * (PA_DEVERR_* bits, accumulated since the workspace was last cleared) into

@@ -32,7 +32,10 @@ _lib = None
 
 class PagedAttentionError(RuntimeError):
     def __init__(self, status: int, where: str):
-        super().__init__(f"{where}: {_STATUS.get(status, status)}")
+        detail = ""
+        if status == 4 and _lib is not None:
+            detail = " (" + _lib.pa_last_error().decode(errors="replace") + ")"
+        super().__init__(f"{where}: {_STATUS.get(status, status)}{detail}")
         self.status = status
 
 
@@ -61,6 +64,8 @@ def load_library():
     lib.pa_paged_attention_stages.restype = ctypes.c_int
     lib.pa_status_string.argtypes = [ctypes.c_int]
     lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_last_error.argtypes = []
+    lib.pa_last_error.restype = ctypes.c_char_p
     lib.pa_read_device_error.argtypes = [p, p, ctypes.POINTER(u32)]
     lib.pa_read_device_error.restype = ctypes.c_int
     lib.pa_kernel_launch_count.argtypes = []

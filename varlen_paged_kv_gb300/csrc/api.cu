@@ -2,6 +2,7 @@
 // tensor-map encoding and the launch sequence plan -> cache write -> prefill -> decode ->
 // merge on the caller's stream. No allocation, no host/device synchronisation.
 #include <algorithm>
+#include <cstdio>
 #include <atomic>
 #include <mutex>
 
@@ -11,6 +12,15 @@
 namespace {
 
 std::atomic<uint64_t> g_launches{0};
+thread_local const char* g_last_error = "no error";
+
+// record a failing CUDA call's message (per host thread) and map it to PA_ERR_CUDA
+pa_status cuda_fail(cudaError_t e, const char* what) {
+  static thread_local char buf[256];
+  snprintf(buf, sizeof(buf), "%s: %s", what, cudaGetErrorString(e));
+  g_last_error = buf;
+  return PA_ERR_CUDA;
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -111,7 +121,7 @@ pa_status check_dims(const pa_dims* d, int32_t nh, int32_t kvh) {
 pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* kc, void* vc, uint32_t stages,
                      cudaStream_t stream) {
   DeviceInfo info;
-  if (!device_info(&info)) return PA_ERR_CUDA;
+  if (!device_info(&info)) return cuda_fail(cudaGetLastError(), "device query");
   args.dec_ctas = std::min(pa::kDecCtasPerSm * info.sms, pa::kMaxDecCtas);
   const pa_dtype dt = (pa_dtype)d->dtype;
   const bool bf16 = dt == PA_BFLOAT16;
@@ -120,13 +130,13 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
 
   if (stages & PA_STAGE_PLAN) {
     ++g_launches;
-    if (pa::launch_plan(args, stream) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaError_t e = pa::launch_plan(args, stream)) return cuda_fail(e, "plan_kernel launch");
   }
   if ((stages & PA_STAGE_CACHE_WRITE) && args.N > 0) {
     const int64_t work = (int64_t)args.N * 2 * (args.kv_row / 8);
     const int64_t blocks = std::min<int64_t>((work + 255) / 256, (int64_t)info.sms * 16);
     ++g_launches;
-    if (pa::launch_cache_write(args, (int)blocks, stream) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaError_t e = pa::launch_cache_write(args, (int)blocks, stream)) return cuda_fail(e, "cache_write_kernel launch");
   }
   const bool can_decode = d->route == PA_ROUTE_AUTO;
   // a host bound max_query_len with max_query_len * G <= 16 proves every sequence decode-class
@@ -135,22 +145,27 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
     const int seg = gcd(d->block_size, pa::kPreTileK);
     CUtensorMap tq, tk, tv;
     if (!query_map(&tq, query, dt, args.q_stride, args.N) || !cache_map(&tk, kc, dt, hs, args.kvh, slots, seg) ||
-        !cache_map(&tv, vc, dt, hs, args.kvh, slots, seg))
+        !cache_map(&tv, vc, dt, hs, args.kvh, slots, seg)) {
+      g_last_error = "cuTensorMapEncodeTiled failed (prefill maps)";
       return PA_ERR_CUDA;
+    }
     const int heads_per_unit = (args.G % 2 == 0) ? 2 : 1;  // two heads of one KV group share a unit
     const int grid = (int)std::min<int64_t>((int64_t)args.max_tiles * (args.nh / heads_per_unit), info.sms);
     if (grid > 0) {
       ++g_launches;
-      if (pa::launch_prefill(args, bf16, tq, tk, tv, seg, grid, stream) != cudaSuccess) return PA_ERR_CUDA;
+      if (cudaError_t e = pa::launch_prefill(args, bf16, tq, tk, tv, seg, grid, stream))
+        return cuda_fail(e, "prefill_kernel launch");
     }
   }
   if ((stages & PA_STAGE_DECODE) && can_decode && args.N > 0 && slots > 0) {
     const int seg = gcd(d->block_size, pa::kDecTile);
     CUtensorMap tk, tv;
-    if (!cache_map(&tk, kc, dt, hs, args.kvh, slots, seg) || !cache_map(&tv, vc, dt, hs, args.kvh, slots, seg))
+    if (!cache_map(&tk, kc, dt, hs, args.kvh, slots, seg) || !cache_map(&tv, vc, dt, hs, args.kvh, slots, seg)) {
+      g_last_error = "cuTensorMapEncodeTiled failed (decode maps)";
       return PA_ERR_CUDA;
+    }
     ++g_launches;
-    if (pa::launch_decode(args, bf16, tk, tv, seg, stream) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaError_t e = pa::launch_decode(args, bf16, tk, tv, seg, stream)) return cuda_fail(e, "decode_kernel launch");
   }
   return PA_OK;
 }
@@ -246,6 +261,8 @@ pa_status pa_paged_attention(const void* query, const void* key, const void* val
                                    dims, workspace, workspace_bytes, stream, PA_STAGE_ALL);
 }
 
+const char* pa_last_error(void) { return g_last_error; }
+
 const char* pa_status_string(pa_status status) {
   switch (status) {
     case PA_OK: return "ok";
@@ -260,10 +277,10 @@ const char* pa_status_string(pa_status status) {
 pa_status pa_read_device_error(void* workspace, void* stream, uint32_t* error_bits) {
   if (!workspace || !error_bits) return PA_ERR_INVALID_ARGUMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaError_t e = cudaStreamSynchronize(s)) return cuda_fail(e, "cudaStreamSynchronize");
   uint32_t v = 0;
-  if (cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
-  if (cudaMemset(workspace, 0, sizeof(v)) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaError_t e = cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost)) return cuda_fail(e, "cudaMemcpy");
+  if (cudaError_t e = cudaMemset(workspace, 0, sizeof(v))) return cuda_fail(e, "cudaMemset");
   *error_bits = v;
   return PA_OK;
 }

@@ -422,6 +422,14 @@ __device__ __forceinline__ void tmem_st_x32_nowait(uint32_t taddr, const uint32_
       : "memory");
 }
 
+// tcgen05.st 32x32b.x8 of eight registers without waiting (see tmem_st_x32_nowait)
+__device__ __forceinline__ void tmem_st_x8_nowait(uint32_t taddr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3,
+                                                  uint32_t r4, uint32_t r5, uint32_t r6, uint32_t r7) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"r"(taddr), "r"(r0),
+               "r"(r1), "r"(r2), "r"(r3), "r"(r4), "r"(r5), "r"(r6), "r"(r7)
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // three-input max / min (sm_100+)

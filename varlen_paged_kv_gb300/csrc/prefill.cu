@@ -34,7 +34,7 @@
 namespace pa {
 
 constexpr uint32_t kTmemCols = 512;
-constexpr int kPreThreads = 320;
+constexpr int kPreThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2..5 softmax A, 6..9 softmax B
 
 __device__ __forceinline__ uint32_t s_col(int x) { return x ? 128u : 0u; }
 __device__ __forceinline__ uint32_t o_col(int x) { return x ? 384u : 256u; }
@@ -45,7 +45,7 @@ __device__ __forceinline__ uint32_t o_col(int x) { return x ? 384u : 256u; }
 __device__ __forceinline__ uint32_t p_col(int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); }
 
 template <int HS, bool BF16>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kPreThreads, 1)
     prefill_kernel(const Args a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const int seg_rows) {
   using L = PreSmem<HS>;
@@ -309,28 +309,30 @@ __global__ void __maxnreg__(200)
             m_used = m_new;
             l *= alpha;
           }
-          // ---- P = exp2(s * c - m), written over S in place, 32 columns at a time ----
+          // ---- P = exp2(s * c - m), written over S in place, 16 keys at a time: the hi (and,
+          // for bf16, lo) word of each key pair replaces that pair's two score registers ----
           const float neg_m = -m_used;
-          float lc[4] = {0.f, 0.f, 0.f, 0.f};
+          float lc[2] = {0.f, 0.f};
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t w[32];
+          for (int kk = 0; kk < kPreTileK / 16; ++kk) {
+            uint32_t* q = r + kk * 16;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float p0 = fast_exp2(fmaf(__uint_as_float(r[cc * 32 + 2 * e]), c, neg_m));
-              const float p1 = fast_exp2(fmaf(__uint_as_float(r[cc * 32 + 2 * e + 1]), c, neg_m));
-              lc[(2 * e) & 3] += p0;
-              lc[(2 * e + 1) & 3] += p1;
+            for (int e = 0; e < 8; ++e) {
+              const float p0 = fast_exp2(fmaf(__uint_as_float(q[2 * e]), c, neg_m));
+              const float p1 = fast_exp2(fmaf(__uint_as_float(q[2 * e + 1]), c, neg_m));
+              lc[0] += p0;
+              lc[1] += p1;
               if constexpr (BF16) {
-                split_bf16x2(p0, p1, w[e], w[16 + e]);
+                split_bf16x2(p0, p1, q[2 * e], q[2 * e + 1]);
               } else {
-                w[e] = pack2<false>(p0, p1);
-                w[16 + e] = 0u;
+                q[2 * e] = pack2<false>(p0, p1);
               }
             }
-            tmem_st_x32_nowait(s_tmem + cc * 32, w);
+            tmem_st_x8_nowait(s_tmem + p_col(kk), q[0], q[2], q[4], q[6], q[8], q[10], q[12], q[14]);
+            if constexpr (BF16)
+              tmem_st_x8_nowait(s_tmem + p_col(kk) + 16, q[1], q[3], q[5], q[7], q[9], q[11], q[13], q[15]);
           }
-          l += (lc[0] + lc[1]) + (lc[2] + lc[3]);
+          l += lc[0] + lc[1];
           tmem_wait_st();
           if (t > 0) {
             // O holds P_0..P_{t-2} V; wait for P_{t-1} V before rescaling it
@@ -358,12 +360,12 @@ __global__ void __maxnreg__(200)
           const bool store = tile.j0 + row < q_len;
           uint16_t* dst = reinterpret_cast<uint16_t*>(a.output) + ((int64_t)(c0 + tile.j0 + row) * a.nh + h) * HS;
 #pragma unroll 1
-          for (int cc = 0; cc < HS; cc += 128) {
-            uint32_t ov[128];
-            tmem_ld_x128(o_tmem + cc, ov);
+          for (int cc = 0; cc < HS; cc += 64) {
+            uint32_t ov[64];
+            tmem_ld_x64(o_tmem + cc, ov);
             if (store) {
 #pragma unroll
-              for (int v = 0; v < 128; v += 8) {
+              for (int v = 0; v < 64; v += 8) {
                 uint4 pk;
                 pk.x = pack2<BF16>(__uint_as_float(ov[v + 0]) * inv, __uint_as_float(ov[v + 1]) * inv);
                 pk.y = pack2<BF16>(__uint_as_float(ov[v + 2]) * inv, __uint_as_float(ov[v + 3]) * inv);
