@@ -152,7 +152,12 @@ struct PreSmem {
   static constexpr int kNumBars = 18;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
-  static constexpr int kBytes = kAbort + 12 + 1024;
+  // row-max exchange between the two warps that share a TMEM lane quarter:
+  // float [tile parity][head][row][column half]
+  static constexpr int kXmax = kAbort + 12;
+  // row-sum exchange at the end of a unit: float [head][row][column half]
+  static constexpr int kXsum = kXmax + 2 * 2 * kPreTileQ * 2 * 4;
+  static constexpr int kBytes = kXsum + 2 * kPreTileQ * 2 * 4 + 1024;
 };
 
 // ---- host launchers, one per kernel family (defined next to their kernels) -----------------
@@ -253,6 +258,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       }
     }
   }
+}
+
+// barrier `id` (1..15) among `count` threads (a multiple of 32)
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

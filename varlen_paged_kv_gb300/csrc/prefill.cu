@@ -8,7 +8,7 @@
 // (bottom-right causal: row j sees keys 0 .. past + j) with the online softmax of
 // FlashAttention.
 //
-// Roles (320 threads, persistent over the planner's tile list, longest tiles first):
+// Roles (640 threads, persistent over the planner's tile list, longest tiles first):
 //   warp 0      TMA producer: the two Q tiles once per unit (2-D map over the query rows),
 //               then K and V tiles into a 2-deep ring, each tile gathered page segment by
 //               page segment through block_table (3-D map over (head_size, kv_heads,
@@ -19,22 +19,29 @@
 //               Q K^T takes both operands from shared memory; P V takes P from TMEM
 //               (where the softmax wrote it over S) and V from shared memory; fp32
 //               accumulators in TMEM.
-//   warps 2..5  softmax of head A, warps 6..9 softmax of head B: thread i owns TMEM lane /
-//               query row i. Per tile: one 128-column TMEM load of the S row, keys past the
-//               row's causal limit replaced by -inf, the row max (three-input max on four
-//               independent chains), the running max update (O is rescaled only when the
+//   warps 2..9  softmax of head A, warps 10..17 softmax of head B: two warps per TMEM lane
+//               quarter, so each thread owns half (64 columns) of query row (TMEM lane) i.
+//               Per tile: one 64-column TMEM load, keys past the row's causal limit replaced
+//               by -inf, the partial row max (three-input max on four independent chains)
+//               exchanged with the partner warp through shared memory, the running max
+//               update (O is rescaled only when the
 //               max grew by more than 2^8, exact because the final division uses the same
 //               stale max), then P = exp2(s * scale * log2 e - m) written over S as 16-bit
 //               pairs: for bf16 as a hi part bf16(p) and a lo part bf16(p - hi), multiplied
 //               by V separately, so the weights keep ~16 significant bits instead of 8.
-//               At the end of the unit the row of O is normalised and stored.
+//               At the end of the unit the partner threads add their row sums and each
+//               normalises and stores its half of the row of O.
+//   warps 18,19 idle (the block is a whole number of warpgroups).
 // TMEM: S_A at column 0, S_B at 128, O_A at 256, O_B at 384 (512 columns allocated).
 #include "common.cuh"
 
 namespace pa {
 
 constexpr uint32_t kTmemCols = 512;
-constexpr int kPreThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2..5 softmax A, 6..9 softmax B
+// warp 0 TMA, warp 1 MMA, warps 2..9 softmax of head A, 10..17 of head B, 18..19 idle (the
+// block is a whole number of warpgroups, the unit registers are allocated in)
+constexpr int kPreThreads = 640;
+constexpr int kSoftWarpsPerHead = 8;  // two warps per TMEM lane quarter, 64 score columns each
 
 __device__ __forceinline__ uint32_t s_col(int x) { return x ? 128u : 0u; }
 __device__ __forceinline__ uint32_t o_col(int x) { return x ? 384u : 256u; }
@@ -81,9 +88,9 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&p_full[i], 32 * kSoftWarpsPerHead);
       mbar_init(&o_done[i], 1);
-      mbar_init(&o_free[i], 128);
+      mbar_init(&o_free[i], 32 * kSoftWarpsPerHead);
     }
     *abort = 0;
     fence_mbar_init();
@@ -249,15 +256,25 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       if (pair) issue_pv(1, n_kv - 1);
       gs += n_kv;
     }
-  } else {
-    // ======================= softmax: warps 2..5 head A, 6..9 head B =======================
-    const int x = (warp - 2) >> 2;
+  } else if (warp < 2 + 2 * kSoftWarpsPerHead) {
+    // ======================= softmax: warps 2..9 head A, 10..17 head B =======================
+    // Two warps share each TMEM lane quarter (rows), one per half of the 128 score columns;
+    // they exchange their partial row maxima through shared memory once per tile.
+    const int sw = warp - 2;
+    const int x = sw / kSoftWarpsPerHead;  // head
+    const int hsel = (sw >> 2) & 1;        // column half
     if (x == 0 || pair) {
+      constexpr int COLS = kPreTileK / 2;  // score columns per thread
+      constexpr int OCOLS = HS / 2;        // output columns per thread
       const int quarter = warp & 3;
       const int row = quarter * 32 + lane;
       const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-      const uint32_t s_tmem = tmem + lane_off + s_col(x);
-      const uint32_t o_tmem = tmem + lane_off + o_col(x);
+      const uint32_t s_base = tmem + lane_off + s_col(x);
+      const uint32_t s_tmem = s_base + hsel * COLS;
+      const uint32_t o_tmem = tmem + lane_off + o_col(x) + hsel * OCOLS;
+      float* xmax = reinterpret_cast<float*>(smem + L::kXmax);
+      float* xsum = reinterpret_cast<float*>(smem + L::kXsum);
+      const int bar_id = 2 + x;
       const float c = a.scale_log2;
       uint32_t gs = 0;
       for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
@@ -273,34 +290,37 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           const uint32_t gt = gs + t;
           mbar_wait(&s_full[x], gt & 1, abort, err);
           tc_fence_after();
-          const int key0 = t * kPreTileK;
-          const bool masked = (key0 + kPreTileK - 1 > lim_tile0) || (key0 + kPreTileK > kv_len);
-          uint32_t r[kPreTileK];
-          tmem_ld_x128(s_tmem, r);
+          const int key0 = t * kPreTileK + hsel * COLS;  // first key of this thread's columns
+          const bool masked = (t * kPreTileK + kPreTileK - 1 > lim_tile0) || (t * kPreTileK + kPreTileK > kv_len);
+          uint32_t r[COLS];
+          tmem_ld_x64(s_tmem, r);
           // keys past this row's limit become -inf for s * c (so both the max and exp2 ignore them)
           const float sentinel = c > 0.f ? -INFINITY : INFINITY;
           if (masked) {
 #pragma unroll
-            for (int e = 0; e < kPreTileK; ++e)
+            for (int e = 0; e < COLS; ++e)
               if (key0 + e > lim) r[e] = __float_as_uint(sentinel);
           }
-          // ---- the row's max of s * c, taken on raw s (max, or min for c < 0), four chains ----
+          // ---- the row's max of s * c, on raw s (max, or min for c < 0), four chains ----
           float mc[4] = {sentinel, sentinel, sentinel, sentinel};
           if (c > 0.f) {
 #pragma unroll
-            for (int e = 0; e < kPreTileK; e += 8)
+            for (int e = 0; e < COLS; e += 8)
 #pragma unroll
               for (int k = 0; k < 4; ++k)
                 mc[k] = fmax3(mc[k], __uint_as_float(r[e + 2 * k]), __uint_as_float(r[e + 2 * k + 1]));
           } else {
 #pragma unroll
-            for (int e = 0; e < kPreTileK; e += 8)
+            for (int e = 0; e < COLS; e += 8)
 #pragma unroll
               for (int k = 0; k < 4; ++k)
                 mc[k] = fmin3(mc[k], __uint_as_float(r[e + 2 * k]), __uint_as_float(r[e + 2 * k + 1]));
           }
           const float mr = c > 0.f ? fmax3(fmaxf(mc[0], mc[1]), mc[2], mc[3]) : fmin3(fminf(mc[0], mc[1]), mc[2], mc[3]);
-          const float m_tile = mr * c;
+          float* xm = xmax + ((gt & 1) * 2 + x) * (kPreTileQ * 2) + row * 2;
+          xm[hsel] = mr * c;
+          named_bar_sync(bar_id, 32 * kSoftWarpsPerHead);
+          const float m_tile = fmaxf(xm[0], xm[1]);
           const float m_new = fmaxf(m_used, m_tile);
           const bool any_grow = __any_sync(0xffffffffu, m_new > m_used + 8.0f);  // first tile: m_used = -inf
           float alpha = 1.f;
@@ -314,8 +334,8 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           const float neg_m = -m_used;
           float lc[2] = {0.f, 0.f};
 #pragma unroll
-          for (int kk = 0; kk < kPreTileK / 16; ++kk) {
-            uint32_t* q = r + kk * 16;
+          for (int g2 = 0; g2 < COLS / 16; ++g2) {
+            uint32_t* q = r + g2 * 16;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const float p0 = fast_exp2(fmaf(__uint_as_float(q[2 * e]), c, neg_m));
@@ -328,9 +348,10 @@ __global__ void __launch_bounds__(kPreThreads, 1)
                 q[2 * e] = pack2<false>(p0, p1);
               }
             }
-            tmem_st_x8_nowait(s_tmem + p_col(kk), q[0], q[2], q[4], q[6], q[8], q[10], q[12], q[14]);
+            const int kk = hsel * (COLS / 16) + g2;  // 16-key block of the tile
+            tmem_st_x8_nowait(s_base + p_col(kk), q[0], q[2], q[4], q[6], q[8], q[10], q[12], q[14]);
             if constexpr (BF16)
-              tmem_st_x8_nowait(s_tmem + p_col(kk) + 16, q[1], q[3], q[5], q[7], q[9], q[11], q[13], q[15]);
+              tmem_st_x8_nowait(s_base + p_col(kk) + 16, q[1], q[3], q[5], q[7], q[9], q[11], q[13], q[15]);
           }
           l += lc[0] + lc[1];
           tmem_wait_st();
@@ -340,7 +361,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
             if (any_grow) {
               tc_fence_after();
 #pragma unroll 1
-              for (int cc = 0; cc < HS; cc += 32) {
+              for (int cc = 0; cc < OCOLS; cc += 32) {
                 uint32_t ov[32];
                 tmem_ld_x32(o_tmem + cc, ov);
 #pragma unroll
@@ -356,16 +377,20 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         mbar_wait(&o_done[x], (gs + n_kv - 1) & 1, abort, err);
         tc_fence_after();
         {
-          const float inv = 1.f / l;
+          float* xs = xsum + x * (kPreTileQ * 2) + row * 2;
+          xs[hsel] = l;
+          named_bar_sync(bar_id, 32 * kSoftWarpsPerHead);
+          const float inv = 1.f / (xs[0] + xs[1]);
           const bool store = tile.j0 + row < q_len;
-          uint16_t* dst = reinterpret_cast<uint16_t*>(a.output) + ((int64_t)(c0 + tile.j0 + row) * a.nh + h) * HS;
+          uint16_t* dst =
+              reinterpret_cast<uint16_t*>(a.output) + ((int64_t)(c0 + tile.j0 + row) * a.nh + h) * HS + hsel * OCOLS;
 #pragma unroll 1
-          for (int cc = 0; cc < HS; cc += 64) {
-            uint32_t ov[64];
-            tmem_ld_x64(o_tmem + cc, ov);
+          for (int cc = 0; cc < OCOLS; cc += 32) {
+            uint32_t ov[32];
+            tmem_ld_x32(o_tmem + cc, ov);
             if (store) {
 #pragma unroll
-              for (int v = 0; v < 64; v += 8) {
+              for (int v = 0; v < 32; v += 8) {
                 uint4 pk;
                 pk.x = pack2<BF16>(__uint_as_float(ov[v + 0]) * inv, __uint_as_float(ov[v + 1]) * inv);
                 pk.y = pack2<BF16>(__uint_as_float(ov[v + 2]) * inv, __uint_as_float(ov[v + 3]) * inv);
