@@ -123,6 +123,38 @@ pa_status pa_paged_attention(const void* query, const void* key, const void* val
                              float scale, void* output, const pa_dims* dims, void* workspace,
                              size_t workspace_bytes, void* stream);
 
+/* Bytes of the device workspace built into the library for
+ * pa_paged_attention_static_workspace (one array per GPU that loads the library). */
+#define PA_STATIC_WORKSPACE_BYTES (16u << 20)
+
+/*
+ * pa_paged_attention for callers that cannot allocate device memory - for example a
+ * plugin whose device memory belongs to a host framework that offers it no allocator,
+ * or a latency-critical path that must not call cudaMalloc. Same arguments as
+ * pa_paged_attention without the workspace: the call uses a workspace of
+ * PA_STATIC_WORKSPACE_BYTES built into the library, which every GPU that loads the
+ * library holds until the process exits. The pages have no counterpart to this entry
+ * point: it is a deployment convenience, not part of the operator.
+ *
+ *   - Returns PA_ERR_WORKSPACE_TOO_SMALL, without launching anything, when
+ *     pa_workspace_size(dims, num_heads, kv_num_heads) exceeds PA_STATIC_WORKSPACE_BYTES
+ *     (use pa_paged_attention with your own workspace for such sizes).
+ *   - Allocates nothing and calls no allocating routine. The first call on each device
+ *     looks up the built-in array's device address (cudaGetSymbolAddress) and caches it;
+ *     make that first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps the last call's contents;
+ *     each call's plan stage rewrites everything later stages read, so nothing needs
+ *     clearing. Calls whose GPU work overlaps race on the array: order them (one stream,
+ *     or synchronise between them).
+ */
+pa_status pa_paged_attention_static_workspace(const void* query, const void* key, const void* value,
+                                              void* key_cache, void* value_cache,
+                                              const int32_t* cumulative_sequence_length,
+                                              const int32_t* past_seqlens, const int32_t* block_table,
+                                              const int32_t* slot_mapping, int32_t num_heads,
+                                              int32_t kv_num_heads, float scale, void* output,
+                                              const pa_dims* dims, void* stream);
+
 /* Stages of pa_paged_attention, in the order they must run. */
 #define PA_STAGE_PLAN 1u        /* device work partitioner: classify sequences, build work lists */
 #define PA_STAGE_CACHE_WRITE 2u /* scatter this step's K/V rows into the caches */
