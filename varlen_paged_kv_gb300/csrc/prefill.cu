@@ -172,7 +172,12 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
-    const uint32_t q_base = smem_u32(smem + L::kQ);
+    // Shared-memory descriptors of the tile bases; an MMA's operand descriptor is its base
+    // plus the operand's byte offset >> 4 (the start-address field, bits 0..13, never carries:
+    // shared addresses stay below 2^18), so issuing an MMA costs a couple of additions.
+    const uint64_t qdesc0 = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);
+    const uint64_t kdesc0 = sdesc_sw128(smem_u32(smem + L::kK0), 16, 1024);
+    const uint64_t vdesc0 = sdesc_sw128(smem_u32(smem + L::kV0), L::kHalfBytes, 1024);
     uint32_t gs = 0, unit_cnt = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++unit_cnt) {
       const PrefillTile tile = a.tiles[u / units_per_tile];
@@ -185,15 +190,16 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       auto issue_qk = [&](int x, int t) {
         const uint32_t gt = gs + t;
         const int st = gt & 1;
-        if (lane == 0) {
-          const uint32_t k_base = smem_u32(smem + L::kK0 + st * L::kKVBytes);
-          const uint32_t qx = q_base + x * L::kQBytes;
+        const uint64_t qd = qdesc0 + (uint64_t)((x * L::kQBytes) >> 4);
+        const uint64_t kd = kdesc0 + (uint64_t)((st * L::kKVBytes) >> 4);
+        const uint32_t d_tmem = tmem + s_col(x);
+        if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < KSTEPS; ++kk) {
             // 16 columns of head_size: slab kk / 4, 32-byte step kk % 4 inside the 128-byte row
-            const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
-            tc_mma_ss(tmem + s_col(x), sdesc_sw128(qx + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024),
-                      IDESC_QK, kk > 0 ? 1u : 0u);
+            constexpr uint32_t kSlab = L::kHalfBytes >> 4;
+            const uint64_t off = (uint64_t)((kk >> 2) * kSlab + (kk & 3) * 2);
+            tc_mma_ss(d_tmem, qd + off, kd + off, IDESC_QK, kk > 0 ? 1u : 0u);
           }
           tc_commit(&s_full[x]);
           if (x == hpu - 1) {  // both heads have read this K tile
@@ -225,16 +231,18 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           fence_proxy_async_smem();
         }
         __syncwarp();
-        if (lane == 0) {
-          const uint32_t v_base = smem_u32(vtile);
-          const uint32_t p_tmem = tmem + s_col(x);
+        const uint64_t vd = vdesc0 + (uint64_t)((st * L::kKVBytes) >> 4);
+        const uint32_t p_tmem = tmem + s_col(x);
+        const uint32_t d_tmem = tmem + o_col(x);
+        const uint32_t acc0 = i > 0 ? 1u : 0u;
+        if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kPreTileK / 16; ++kk) {
             // 16 keys of V: rows 16kk.. (K dimension, 8-row atoms 1024 B apart), the two
             // 64-column slabs of head_size 16 KB apart (MN dimension)
-            const uint64_t vdesc = sdesc_sw128(v_base + kk * 16 * 128, L::kHalfBytes, 1024);
-            tc_mma_ts(tmem + o_col(x), p_tmem + p_col(kk), vdesc, IDESC_PV, (i > 0 || kk > 0) ? 1u : 0u);
-            if constexpr (BF16) tc_mma_ts(tmem + o_col(x), p_tmem + p_col(kk) + 16, vdesc, IDESC_PV, 1u);
+            const uint64_t vdesc = vd + (uint64_t)(kk * ((16 * 128) >> 4));
+            tc_mma_ts(d_tmem, p_tmem + p_col(kk), vdesc, IDESC_PV, kk > 0 ? 1u : acc0);
+            if constexpr (BF16) tc_mma_ts(d_tmem, p_tmem + p_col(kk) + 16, vdesc, IDESC_PV, 1u);
           }
           tc_commit(&o_done[x]);
           if (x == hpu - 1) tc_commit(&v_empty[st]);  // both heads have read this V tile
