@@ -51,6 +51,17 @@ __device__ __forceinline__ uint32_t o_col(int x) { return x ? 384u : 256u; }
 // columns and lo pairs (bf16) in the last 16.
 __device__ __forceinline__ uint32_t p_col(int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); }
 
+// Unit k of this CTA. Units are dealt out in rounds of gridDim.x, alternately in CTA order
+// and in reverse; with the units sorted by decreasing cost this pairs a CTA's expensive
+// units with cheap ones, and the per-CTA totals come out close to those of the greedy
+// longest-first assignment (a plain round robin gives the first CTAs the most work in
+// every round). Strictly increasing in k, so a CTA's loop ends at its first unit past the
+// end.
+__device__ __forceinline__ int snake_unit(int k) {
+  const int g = (int)gridDim.x;
+  return k * g + ((k & 1) ? g - 1 - (int)blockIdx.x : (int)blockIdx.x);
+}
+
 template <int HS, bool BF16>
 __global__ void __launch_bounds__(kPreThreads, 1)
     prefill_kernel(const Args a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -119,7 +130,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     }
     const int nseg = kPreTileK / seg_rows;
     uint32_t gs = 0, unit_cnt = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++unit_cnt) {
+    for (int u = snake_unit(0); u < n_units; u = snake_unit(++unit_cnt)) {
       const PrefillTile tile = a.tiles[u / units_per_tile];
       const int h0 = (u % units_per_tile) * hpu, g = h0 / a.G;
       const int c0 = a.cum[tile.b], q_len = a.cum[tile.b + 1] - c0, past = a.past[tile.b];
@@ -179,7 +190,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     const uint64_t kdesc0 = sdesc_sw128(smem_u32(smem + L::kK0), 16, 1024);
     const uint64_t vdesc0 = sdesc_sw128(smem_u32(smem + L::kV0), L::kHalfBytes, 1024);
     uint32_t gs = 0, unit_cnt = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++unit_cnt) {
+    for (int u = snake_unit(0); u < n_units; u = snake_unit(++unit_cnt)) {
       const PrefillTile tile = a.tiles[u / units_per_tile];
       const int c0 = a.cum[tile.b], q_len = a.cum[tile.b + 1] - c0, past = a.past[tile.b];
       const int kv_len = past + q_len;
@@ -285,7 +296,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       const int bar_id = 2 + x;
       const float c = a.scale_log2;
       uint32_t gs = 0;
-      for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      for (int k = 0, u = snake_unit(0); u < n_units; u = snake_unit(++k)) {
         const PrefillTile tile = a.tiles[u / units_per_tile];
         const int h = (u % units_per_tile) * hpu + x;
         const int c0 = a.cum[tile.b], q_len = a.cum[tile.b + 1] - c0, past = a.past[tile.b];
