@@ -234,3 +234,53 @@ def test_inconsistent_batch_is_refused_without_writes():
     assert pa.read_device_error(ws) & pa.DEVERR_BAD_BATCH
     assert np.array_equal(bits_of(d["key_cache"]), before)
     assert torch.all(out == 7.0)
+
+
+# ---- bf16 V outside fp16's range, and unwritten cache rows --------------------------------
+
+def _scale_bf16_rows(bits, rows, exp_shift):
+    """Replaces the bf16 values v of the given rows by |v| * 2**exp_shift, exactly (sign bit
+    and exponent field)."""
+    out = bits.copy()
+    sel = out[rows].astype(np.int32) & 0x7FFF
+    nonzero = (sel & 0x7F80) != 0
+    sel = np.where(nonzero, sel + (exp_shift << 7), sel)
+    assert np.all((sel & 0x7F80) < 0x7F80) and np.all(sel >= 0)  # stays finite, no sign flip
+    out[rows] = sel.astype(np.uint16)
+    return out
+
+
+def test_bf16_values_beyond_fp16_range():
+    # sequence 0 has three 128-key tiles; six of its tokens in the middle tile get values
+    # 2^17 |N(0,1)|, mostly beyond fp16's largest finite value, while the other tiles stay
+    # small, so one unit mixes both kinds of tile. The large values are all positive: with
+    # both signs the outputs would be small differences of terms near 1e5, and no fp32
+    # computation meets a tolerance relative to such a difference.
+    p = _case("prefill-ragged")
+    assert p.dtype == "bf16"
+    p.value = _scale_bf16_rows(p.value, np.arange(130, 136), 17)
+    check(p)
+    check(p, route=pa.ROUTE_ALL_PREFILL)
+
+
+def _poison_unread_cache_rows(p, bits):
+    """Sets every cache row no sequence reads (past its length, or in pages it does not
+    own) to the 16-bit pattern `bits` in both caches."""
+    used = np.zeros((p.num_blocks, p.block_size), bool)
+    for b in range(p.batch_size):
+        keys = np.arange(int(p.kv_lens[b]))
+        used[p.block_table[b, keys // p.block_size], keys % p.block_size] = True
+    p.key_cache = p.key_cache.copy()
+    p.value_cache = p.value_cache.copy()
+    p.key_cache[~used] = bits
+    p.value_cache[~used] = bits
+
+
+@pytest.mark.parametrize("name", ["prefill-ragged", "chunked-prefill", "pages48", "head64-pages16"])
+def test_nan_in_unread_cache_rows_does_not_leak(name):
+    # the last KV tile of a sequence reaches past its length into cache rows that may never
+    # have been written; P is 0 there, but 0 * NaN is NaN, so those rows must not reach P V
+    p = _case(name)
+    _poison_unread_cache_rows(p, 0x7FC0 if p.dtype == "bf16" else 0x7E00)
+    check(p)
+    check(p, route=pa.ROUTE_ALL_PREFILL)

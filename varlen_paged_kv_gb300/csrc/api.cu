@@ -1,6 +1,6 @@
 // C ABI of the library (include/pagedattn.h): argument checks, workspace carving, TMA
-// tensor-map encoding and the launch sequence plan -> cache write -> prefill -> decode ->
-// merge on the caller's stream. No allocation, no host/device synchronisation.
+// tensor-map encoding and the launch sequence plan -> cache write -> (bf16: fp16 copy of
+// the prefill sequences' V) -> prefill -> decode (with its merge) on the caller's stream. No allocation, no host/device synchronisation.
 #include <algorithm>
 #include <cstdio>
 #include <atomic>
@@ -118,6 +118,22 @@ pa_status check_dims(const pa_dims* d, int32_t nh, int32_t kvh) {
   return PA_OK;
 }
 
+// Whether any sequence may take the prefill kernel: with the automatic route, a host bound
+// max_query_len with max_query_len * G <= 16 proves every sequence decode-class.
+bool prefill_possible(const pa_dims* d, int32_t G) {
+  return !(d->route == PA_ROUTE_AUTO && d->max_query_len > 0 && (int64_t)d->max_query_len * G <= pa::kDecRows);
+}
+
+// Rows of the fp16 copy of V that bf16 prefill reads: room for an average of four keys of
+// history (past and new) per new token, at most the cache's size. A call whose
+// prefill-class sequences hold more keys than that, or whose V holds a value fp16 cannot
+// represent, takes the two-product path on the bf16 cache instead (same results within
+// rounding, slower).
+int64_t mirror_keys(const pa_dims* d, int32_t nh, int32_t kvh) {
+  if (d->dtype != PA_BFLOAT16 || !prefill_possible(d, nh / kvh)) return 0;
+  return std::min<int64_t>(4 * (int64_t)d->num_tokens, (int64_t)d->num_blocks * d->block_size);
+}
+
 pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* kc, void* vc, uint32_t stages,
                      cudaStream_t stream) {
   DeviceInfo info;
@@ -139,21 +155,34 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
     if (cudaError_t e = pa::launch_cache_write(args, (int)blocks, stream)) return cuda_fail(e, "cache_write_kernel launch");
   }
   const bool can_decode = d->route == PA_ROUTE_AUTO;
-  // a host bound max_query_len with max_query_len * G <= 16 proves every sequence decode-class
-  const bool can_prefill = !(can_decode && d->max_query_len > 0 && (int64_t)d->max_query_len * args.G <= pa::kDecRows);
+  const bool can_prefill = prefill_possible(d, args.G);
   if ((stages & PA_STAGE_PREFILL) && can_prefill && args.N > 0 && slots > 0) {
+    if (args.mirror_keys > 0) {  // the fp16 copy of V (the planner decides whether it is used)
+      const int64_t warps = (int64_t)args.mirror_keys;
+      const int64_t blocks = std::min<int64_t>((warps + 7) / 8, (int64_t)info.sms * 8);
+      ++g_launches;
+      if (cudaError_t e = pa::launch_v_mirror(args, (int)blocks, stream)) return cuda_fail(e, "v_mirror_kernel launch");
+    }
     const int seg = gcd(d->block_size, pa::kPreTileK);
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, tvm;
     if (!query_map(&tq, query, dt, args.q_stride, args.N) || !cache_map(&tk, kc, dt, hs, args.kvh, slots, seg) ||
         !cache_map(&tv, vc, dt, hs, args.kvh, slots, seg)) {
       g_last_error = "cuTensorMapEncodeTiled failed (prefill maps)";
       return PA_ERR_CUDA;
     }
+    if (args.mirror_keys > 0) {
+      if (!cache_map(&tvm, args.mirror, PA_FLOAT16, hs, args.kvh, args.mirror_keys, seg)) {
+        g_last_error = "cuTensorMapEncodeTiled failed (V copy map)";
+        return PA_ERR_CUDA;
+      }
+    } else {
+      tvm = tv;  // never read
+    }
     const int heads_per_unit = (args.G % 2 == 0) ? 2 : 1;  // two heads of one KV group share a unit
     const int grid = (int)std::min<int64_t>((int64_t)args.max_tiles * (args.nh / heads_per_unit), info.sms);
     if (grid > 0) {
       ++g_launches;
-      if (cudaError_t e = pa::launch_prefill(args, bf16, tq, tk, tv, seg, grid, stream))
+      if (cudaError_t e = pa::launch_prefill(args, bf16, tq, tk, tv, tvm, seg, grid, stream))
         return cuda_fail(e, "prefill_kernel launch");
     }
   }
@@ -177,7 +206,8 @@ extern "C" {
 size_t pa_workspace_size(const pa_dims* dims, int32_t num_heads, int32_t kv_num_heads) {
   if (check_dims(dims, num_heads, kv_num_heads) != PA_OK) return 0;
   return pa::ws_layout(dims->num_tokens, dims->batch_size, kv_num_heads, dims->head_size,
-                       dims->max_blocks_per_sequence, dims->block_size, dims->decode_split_keys)
+                       dims->max_blocks_per_sequence, dims->block_size, dims->decode_split_keys,
+                       mirror_keys(dims, num_heads, kv_num_heads))
       .total;
 }
 
@@ -202,8 +232,9 @@ pa_status pa_paged_attention_stages(const void* query, const void* key, const vo
       !aligned(workspace, 256))
     return PA_ERR_INVALID_ARGUMENT;
   if (dims->max_blocks_per_sequence == 0 || dims->num_blocks == 0) return PA_ERR_INVALID_ARGUMENT;
+  const int64_t mkeys = mirror_keys(dims, num_heads, kv_num_heads);
   const pa::WsLayout L = pa::ws_layout(N, B, kv_num_heads, hs, dims->max_blocks_per_sequence, dims->block_size,
-                                       dims->decode_split_keys);
+                                       dims->decode_split_keys, mkeys);
   if (workspace_bytes < L.total) return PA_ERR_WORKSPACE_TOO_SMALL;
 
   pa::Args a{};
@@ -245,6 +276,10 @@ pa_status pa_paged_attention_stages(const void* query, const void* key, const vo
   a.unit_done = reinterpret_cast<int32_t*>(ws + L.unit_done);
   a.part_o = reinterpret_cast<float*>(ws + L.part_o);
   a.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
+  a.mirror_base = reinterpret_cast<int32_t*>(ws + L.mirror_base);
+  a.mirror = reinterpret_cast<uint16_t*>(ws + L.mirror);
+  a.mirror_seq = reinterpret_cast<int2*>(ws + L.mirror_seq);
+  a.mirror_keys = (int32_t)mkeys;
   a.max_items = L.max_items;
   a.max_tiles = L.max_tiles;
 

@@ -32,7 +32,11 @@ struct WsHeader {
   int32_t n_decode_items;
   int32_t n_prefill_tiles;
   int32_t dec_ctas;         // decode grid the item ranges were cut for
-  int32_t pad[59];
+  int32_t v_mirror;         // 1: bf16 prefill reads V from the fp16 copy (planner)
+  uint32_t v_mirror_bad;    // set by the copy kernel when a value does not fit fp16
+  int32_t mirror_rows;      // rows of the copy in use
+  int32_t mirror_seqs;      // sequences copied (entries of mirror_seq)
+  int32_t pad[55];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
@@ -52,7 +56,8 @@ struct PrefillTile {    // 128 query rows [j0, j0+128) of sequence b (all heads)
 };
 
 struct WsLayout {
-  size_t header, items, cta_begin, unit_done, tiles, tiles_unsorted, part_o, part_lse, total;
+  size_t header, items, cta_begin, unit_done, tiles, tiles_unsorted, part_o, part_lse, mirror_base, mirror_seq,
+      mirror, total;
   int32_t max_items, max_tiles;
 };
 
@@ -64,8 +69,10 @@ __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + 
 //    into at most kMaxDecCtas contiguous ranges, so items <= kMaxDecCtas + units;
 //  - decode items, forced split length S: at most ceil(max_kv / S) per unit;
 //  - prefill tiles: sum_b ceil(q_b / 128) <= N / 128 + B.
+// mirror_keys: rows of the fp16 copy of V that bf16 prefill reads (0: none).
 __host__ __device__ inline WsLayout ws_layout(int32_t N, int32_t B, int32_t kvh, int32_t hs,
-                                               int32_t max_blocks, int32_t bs, int32_t forced_split) {
+                                               int32_t max_blocks, int32_t bs, int32_t forced_split,
+                                               int64_t mirror_keys) {
   WsLayout L;
   const int64_t units = (int64_t)B * kvh;
   int64_t items;
@@ -83,6 +90,9 @@ __host__ __device__ inline WsLayout ws_layout(int32_t N, int32_t B, int32_t kvh,
   L.tiles_unsorted = off; off = align_up(off + sizeof(PrefillTile) * (size_t)tiles, 256);
   L.part_o = off; off = align_up(off + sizeof(float) * (size_t)items * kDecRows * hs, 256);
   L.part_lse = off; off = align_up(off + sizeof(float) * (size_t)items * kDecRows, 256);
+  L.mirror_base = off; off = align_up(off + sizeof(int32_t) * ((size_t)B + 1), 256);
+  L.mirror_seq = off; off = align_up(off + 2 * sizeof(int32_t) * ((size_t)B + 1), 256);
+  L.mirror = off; off = align_up(off + (size_t)mirror_keys * kvh * hs * 2, 256);
   L.total = off;
   return L;
 }
@@ -118,6 +128,10 @@ struct Args {
   PrefillTile* tiles_unsorted;
   float* part_o;
   float* part_lse;
+  int32_t* mirror_base;   // per prefill-class sequence b: its first row in the V copy
+  int2* mirror_seq;       // k-th copied sequence: (b, first row), in row order
+  uint16_t* mirror;       // fp16 copy of the V history of the prefill-class sequences (bf16)
+  int32_t mirror_keys;    // rows the copy holds (0: no copy)
   int32_t max_items, max_tiles;
 };
 
@@ -163,8 +177,9 @@ struct PreSmem {
 // ---- host launchers, one per kernel family (defined next to their kernels) -----------------
 cudaError_t launch_plan(const Args& a, cudaStream_t s);
 cudaError_t launch_cache_write(const Args& a, int grid, cudaStream_t s);
+cudaError_t launch_v_mirror(const Args& a, int grid, cudaStream_t s);
 cudaError_t launch_prefill(const Args& a, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, int seg, int grid, cudaStream_t s);
+                           const CUtensorMap& tv, const CUtensorMap& tvm, int seg, int grid, cudaStream_t s);
 cudaError_t launch_decode(const Args& a, bool bf16, const CUtensorMap& tk, const CUtensorMap& tv, int seg,
                           cudaStream_t s);
 
@@ -200,6 +215,23 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {  // lo -> bits 0
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
   }
+}
+
+// Two bf16 values (bits 0..15 and 16..31) as two fp16 values in the same positions:
+// exact for magnitudes in [2^-14, 65504]; below that fp16 keeps fewer bits (absolute error
+// at most 2^-25); from 65520 up the result is inf, and NaN stays NaN.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
+  uint32_t h;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(hi), "f"(lo));
+  return h;
+}
+
+// per-half unsigned maximum of two 16-bit pairs
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 // p as two bf16 values hi + lo with hi = bf16(p), lo = bf16(p - hi): their sum carries

@@ -68,6 +68,32 @@ __device__ void block_scan3(const int v[3], int ex[3], int tot[3], int (*s_warp)
   __syncthreads();
 }
 
+// exclusive scan of one int64 across the block; *tot gets the block total
+__device__ void block_scan_i64(int64_t v, int64_t* ex, int64_t* tot, long long* s_w) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_w[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    long long y = lane < nw ? s_w[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      long long z = __shfl_up_sync(0xffffffffu, y, o);
+      if (lane >= o) y += z;
+    }
+    s_w[lane] = y;
+  }
+  __syncthreads();
+  *ex = (wid > 0 ? s_w[wid - 1] : 0) + x - v;
+  *tot = s_w[nw - 1];
+  __syncthreads();
+}
+
 // decode CTA whose key-tile range holds tile t: largest c with floor(c W / P) <= t
 __device__ __forceinline__ int cta_of(int64_t t, int64_t W, int64_t P) { return (int)(((t + 1) * P - 1) / W); }
 __device__ __forceinline__ int64_t cta_start(int64_t c, int64_t W, int64_t P) { return c * W / P; }
@@ -87,6 +113,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
   __shared__ int s_carry[3];
   __shared__ int s_cta_begin[kMaxDecCtas + 1];
   __shared__ unsigned long long s_key[kSortCap];
+  __shared__ long long s_w64[32];
+  __shared__ long long s_mirror_carry;
+  __shared__ int s_mseq_carry;
 
   const int tid = threadIdx.x;
   WsHeader* hdr = a.hdr;
@@ -95,7 +124,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
     s_bad = 0;
     s_dec_tiles = 0;
     s_carry[0] = s_carry[1] = s_carry[2] = 0;
+    s_mirror_carry = 0;
+    s_mseq_carry = 0;
     hdr->error = 0;  // error bits describe the most recent call
+    hdr->v_mirror = 0;
+    hdr->v_mirror_bad = 0;
+    hdr->mirror_rows = 0;
   }
   for (int c = tid; c <= P; c += blockDim.x) s_cta_begin[c] = INT_MAX;
   __syncthreads();
@@ -139,8 +173,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
         v[1] = (int)ceil_div(q, kPreTileQ);
       }
     }
+    v[2] = v[1] > 0 ? 1 : 0;  // prefill-class sequences (rank among them, for the V copy)
     int ex[3], tot[3];
     block_scan3(v, ex, tot, s_warp);
+    // rows of the fp16 V copy: every key of every prefill-class sequence, in sequence order
+    int64_t m_ex = 0, m_tot = 0;
+    if (a.mirror_keys > 0) {
+      block_scan_i64(v[1] > 0 ? kv : 0, &m_ex, &m_tot, s_w64);
+      const int64_t mb = s_mirror_carry + m_ex;
+      if (v[1] > 0 && mb + kv <= a.mirror_keys) {
+        a.mirror_base[b] = (int)mb;
+        a.mirror_seq[s_mseq_carry + ex[2]] = make_int2(b, (int)mb);
+      }
+    }
     const int64_t T_b = (int64_t)carry0 + ex[0];  // first decode tile of (b, head 0)
     // items of this sequence
     int w[3] = {0, 0, 0};
@@ -192,6 +237,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
       s_carry[0] += tot[0];
       s_carry[1] += tot[1];
       s_carry[2] += tot2[0];
+      s_mirror_carry += m_tot;
+      s_mseq_carry += tot[2];
     }
     __syncthreads();
   }
@@ -254,6 +301,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
     for (int i = tid; i < n_tiles; i += blockDim.x) a.tiles[i] = a.tiles_unsorted[i];
   }
   if (tid == 0) {
+    if (a.mirror_keys > 0 && s_mirror_carry > 0 && s_mirror_carry <= a.mirror_keys) {
+      hdr->v_mirror = 1;
+      hdr->mirror_rows = (int)s_mirror_carry;
+      hdr->mirror_seqs = s_mseq_carry;
+    }
     hdr->valid = 1;
     hdr->n_decode_items = n_items;
     hdr->n_prefill_tiles = n_tiles;
@@ -313,6 +365,59 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
   }
 }
 
+// ---- fp16 copy of V for bf16 prefill ----------------------------------------------------
+// Row r of the copy is key r - mirror_base[b] of prefill-class sequence b, read from the
+// value cache after this call's cache write (so through block_table, as the attention
+// reads it). One warp per row, 16-byte loads and stores. A value fp16 cannot represent
+// (|v| >= 65520, inf, NaN) sets v_mirror_bad, and the prefill kernel then reads the bf16
+// cache instead; a block outside the pool is flagged and its rows are zeros (as the
+// attention reads them from the cache).
+__global__ void __launch_bounds__(256) v_mirror_kernel(const Args a) {
+  const WsHeader* hdr = a.hdr;
+  if (!hdr->valid || !hdr->v_mirror) return;
+  const int rows = hdr->mirror_rows;
+  const int lane = threadIdx.x & 31;
+  const int chunks = a.kv_row / 8;  // 16-byte chunks of a row
+  uint32_t big = 0;                 // per-half max of |fp16| bits over this lane's values
+  const int n = hdr->mirror_seqs;
+  for (int r = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); r < rows; r += (int)((gridDim.x * blockDim.x) >> 5)) {
+    int lo = 0, hi = n - 1;  // the last copied sequence whose first row is <= r
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.mirror_seq[mid].y <= r) lo = mid; else hi = mid - 1;
+    }
+    const int b = a.mirror_seq[lo].x;
+    const int key = r - a.mirror_seq[lo].y;
+    const int blk = a.block_table[(int64_t)b * a.max_blocks + key / a.bs];
+    const uint4* src = nullptr;
+    if (blk >= 0 && blk < a.num_blocks)
+      src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.value_cache) +
+                                           ((int64_t)blk * a.bs + key % a.bs) * a.kv_row);
+    else if (lane == 0)
+      atomicOr(&a.hdr->error, PA_DEVERR_BAD_BLOCK);
+    uint4* dst = reinterpret_cast<uint4*>(a.mirror + (int64_t)r * a.kv_row);
+    for (int c0 = lane; c0 < chunks; c0 += 128) {  // four loads in flight before the stores
+      uint4 w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = c0 + 32 * j;
+        w[j] = (src && c < chunks) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        w[j].x = bf16x2_to_f16x2(w[j].x);
+        w[j].y = bf16x2_to_f16x2(w[j].y);
+        w[j].z = bf16x2_to_f16x2(w[j].z);
+        w[j].w = bf16x2_to_f16x2(w[j].w);
+        big = max_u16x2(big, max_u16x2(max_u16x2(w[j].x & 0x7FFF7FFFu, w[j].y & 0x7FFF7FFFu),
+                                       max_u16x2(w[j].z & 0x7FFF7FFFu, w[j].w & 0x7FFF7FFFu)));
+        if (c0 + 32 * j < chunks) dst[c0 + 32 * j] = w[j];
+      }
+    }
+  }
+  if ((big & 0xFFFFu) >= 0x7C00u || (big >> 16) >= 0x7C00u) atomicOr(&a.hdr->v_mirror_bad, 1u);
+}
+
 // ---- host launchers ----
 cudaError_t launch_plan(const Args& a, cudaStream_t s) {
   plan_kernel<<<1, kPlanThreads, 0, s>>>(a);
@@ -321,6 +426,11 @@ cudaError_t launch_plan(const Args& a, cudaStream_t s) {
 
 cudaError_t launch_cache_write(const Args& a, int grid, cudaStream_t s) {
   cache_write_kernel<<<grid, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_v_mirror(const Args& a, int grid, cudaStream_t s) {
+  v_mirror_kernel<<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -65,12 +65,14 @@ __device__ __forceinline__ int snake_unit(int k) {
 template <int HS, bool BF16>
 __global__ void __launch_bounds__(kPreThreads, 1)
     prefill_kernel(const Args a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const int seg_rows) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmVm,
+                   const int seg_rows) {
   using L = PreSmem<HS>;
   constexpr int HALVES = HS / 64;
   constexpr int KSTEPS = HS / 16;  // k-steps of Q K^T
   constexpr uint32_t IDESC_QK = idesc_f16(BF16, kPreTileQ, kPreTileK, false);
   constexpr uint32_t IDESC_PV = idesc_f16(BF16, kPreTileQ, HS, true);
+  constexpr uint32_t IDESC_PV16 = idesc_f16(false, kPreTileQ, HS, true);  // fp16 P times the fp16 V copy
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -116,6 +118,9 @@ __global__ void __launch_bounds__(kPreThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   const bool pair = (a.G & 1) == 0;  // two query heads of one KV head per unit
+  // bf16: V from the fp16 copy (one fp16 P V product per 16 keys), unless the planner found
+  // no room for it or the copy met a value fp16 cannot hold (then bf16 V, P as hi + lo)
+  const bool v16 = BF16 && a.hdr->v_mirror && !a.hdr->v_mirror_bad;
   const int hpu = pair ? 2 : 1;
   const int units_per_tile = a.nh / hpu;
   const int n_units = a.hdr->n_prefill_tiles * units_per_tile;
@@ -127,6 +132,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      if (v16) tma_prefetch_desc(&tmVm);
     }
     const int nseg = kPreTileK / seg_rows;
     uint32_t gs = 0, unit_cnt = 0;
@@ -137,6 +143,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       const int kv_len = past + q_len;
       const int n_kv = (int)ceil_div(past + min(tile.j0 + kPreTileQ, q_len), kPreTileK);
       const int* bt = a.block_table + (int64_t)tile.b * a.max_blocks;
+      const int mirror_row0 = v16 ? a.mirror_base[tile.b] : 0;
       if (lane == 0) {
         if (unit_cnt > 0) mbar_wait(q_empty, (unit_cnt - 1) & 1, abort, err);
         mbar_arrive_expect_tx(q_full, hpu * L::kQBytes);
@@ -150,12 +157,14 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         const int st = gs & 1;
         const uint32_t ph = (gs >> 1) & 1;
         int z = (int)cache_rows;  // past the end: zero fill
+        int zv = v16 ? a.mirror_keys : z;
         if (lane < nseg) {
           const int key = t * kPreTileK + lane * seg_rows;
           if (key < kv_len) {
             const int blk = bt[key / a.bs];
             if (blk >= 0 && blk < a.num_blocks) z = blk * a.bs + key % a.bs;
-            else atomicOr(err, PA_DEVERR_BAD_BLOCK);
+            else if (!v16) atomicOr(err, PA_DEVERR_BAD_BLOCK);  // (the copy kernel flags it otherwise)
+            zv = v16 ? mirror_row0 + key : z;
           }
         }
         if (lane == 0) {
@@ -176,7 +185,8 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         if (lane < nseg) {
           uint8_t* dst = smem + L::kV0 + st * L::kKVBytes + lane * seg_rows * 128;
 #pragma unroll
-          for (int hh = 0; hh < HALVES; ++hh) tma_load_3d(dst + hh * L::kHalfBytes, &tmV, &v_full[st], hh * 64, g, z);
+          for (int hh = 0; hh < HALVES; ++hh)
+            tma_load_3d(dst + hh * L::kHalfBytes, v16 ? &tmVm : &tmV, &v_full[st], hh * 64, g, zv);
         }
         __syncwarp();
       }
@@ -247,13 +257,21 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         const uint32_t d_tmem = tmem + o_col(x);
         const uint32_t acc0 = i > 0 ? 1u : 0u;
         if (elect_one()) {
+          // 16 keys of V per MMA: rows 16kk.. (K dimension, 8-row atoms 1024 B apart), the
+          // two 64-column slabs of head_size 16 KB apart (MN dimension)
+          if (BF16 && !v16) {
 #pragma unroll
-          for (int kk = 0; kk < kPreTileK / 16; ++kk) {
-            // 16 keys of V: rows 16kk.. (K dimension, 8-row atoms 1024 B apart), the two
-            // 64-column slabs of head_size 16 KB apart (MN dimension)
-            const uint64_t vdesc = vd + (uint64_t)(kk * ((16 * 128) >> 4));
-            tc_mma_ts(d_tmem, p_tmem + p_col(kk), vdesc, IDESC_PV, kk > 0 ? 1u : acc0);
-            if constexpr (BF16) tc_mma_ts(d_tmem, p_tmem + p_col(kk) + 16, vdesc, IDESC_PV, 1u);
+            for (int kk = 0; kk < kPreTileK / 16; ++kk) {
+              const uint64_t vdesc = vd + (uint64_t)(kk * ((16 * 128) >> 4));
+              tc_mma_ts(d_tmem, p_tmem + p_col(kk), vdesc, IDESC_PV, kk > 0 ? 1u : acc0);
+              tc_mma_ts(d_tmem, p_tmem + p_col(kk) + 16, vdesc, IDESC_PV, 1u);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kPreTileK / 16; ++kk) {
+              const uint64_t vdesc = vd + (uint64_t)(kk * ((16 * 128) >> 4));
+              tc_mma_ts(d_tmem, p_tmem + p_col(kk), vdesc, BF16 ? IDESC_PV16 : IDESC_PV, kk > 0 ? 1u : acc0);
+            }
           }
           tc_commit(&o_done[x]);
           if (x == hpu - 1) tc_commit(&v_empty[st]);  // both heads have read this V tile
@@ -348,29 +366,42 @@ __global__ void __launch_bounds__(kPreThreads, 1)
             m_used = m_new;
             l *= alpha;
           }
-          // ---- P = exp2(s * c - m), written over S in place, 16 keys at a time: the hi (and,
-          // for bf16, lo) word of each key pair replaces that pair's two score registers ----
+          // ---- P = exp2(s * c - m), written over S in place, 16 keys at a time: the fp16
+          // word (or, against bf16 V, the bf16 hi and lo words) of each key pair replaces
+          // that pair's two score registers ----
           const float neg_m = -m_used;
           float lc[2] = {0.f, 0.f};
+          if (BF16 && !v16) {
 #pragma unroll
-          for (int g2 = 0; g2 < COLS / 16; ++g2) {
-            uint32_t* q = r + g2 * 16;
+            for (int g2 = 0; g2 < COLS / 16; ++g2) {
+              uint32_t* q = r + g2 * 16;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float p0 = fast_exp2(fmaf(__uint_as_float(q[2 * e]), c, neg_m));
-              const float p1 = fast_exp2(fmaf(__uint_as_float(q[2 * e + 1]), c, neg_m));
-              lc[0] += p0;
-              lc[1] += p1;
-              if constexpr (BF16) {
+              for (int e = 0; e < 8; ++e) {
+                const float p0 = fast_exp2(fmaf(__uint_as_float(q[2 * e]), c, neg_m));
+                const float p1 = fast_exp2(fmaf(__uint_as_float(q[2 * e + 1]), c, neg_m));
+                lc[0] += p0;
+                lc[1] += p1;
                 split_bf16x2(p0, p1, q[2 * e], q[2 * e + 1]);
-              } else {
+              }
+              const int kk = hsel * (COLS / 16) + g2;  // 16-key block of the tile
+              tmem_st_x8_nowait(s_base + p_col(kk), q[0], q[2], q[4], q[6], q[8], q[10], q[12], q[14]);
+              tmem_st_x8_nowait(s_base + p_col(kk) + 16, q[1], q[3], q[5], q[7], q[9], q[11], q[13], q[15]);
+            }
+          } else {
+#pragma unroll
+            for (int g2 = 0; g2 < COLS / 16; ++g2) {
+              uint32_t* q = r + g2 * 16;
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float p0 = fast_exp2(fmaf(__uint_as_float(q[2 * e]), c, neg_m));
+                const float p1 = fast_exp2(fmaf(__uint_as_float(q[2 * e + 1]), c, neg_m));
+                lc[0] += p0;
+                lc[1] += p1;
                 q[2 * e] = pack2<false>(p0, p1);
               }
+              const int kk = hsel * (COLS / 16) + g2;  // 16-key block of the tile
+              tmem_st_x8_nowait(s_base + p_col(kk), q[0], q[2], q[4], q[6], q[8], q[10], q[12], q[14]);
             }
-            const int kk = hsel * (COLS / 16) + g2;  // 16-key block of the tile
-            tmem_st_x8_nowait(s_base + p_col(kk), q[0], q[2], q[4], q[6], q[8], q[10], q[12], q[14]);
-            if constexpr (BF16)
-              tmem_st_x8_nowait(s_base + p_col(kk) + 16, q[1], q[3], q[5], q[7], q[9], q[11], q[13], q[15]);
           }
           l += lc[0] + lc[1];
           tmem_wait_st();
@@ -439,19 +470,21 @@ __global__ void __launch_bounds__(kPreThreads, 1)
 // ---- host launcher ----
 template <int HS, bool BF16>
 static cudaError_t launch_prefill_t(const Args& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                    int seg, int grid, cudaStream_t s) {
+                                    const CUtensorMap& tvm, int seg, int grid, cudaStream_t s) {
   constexpr int smem = PreSmem<HS>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<HS, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  prefill_kernel<HS, BF16><<<grid, kPreThreads, smem, s>>>(a, tq, tk, tv, seg);
+  prefill_kernel<HS, BF16><<<grid, kPreThreads, smem, s>>>(a, tq, tk, tv, tvm, seg);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(const Args& a, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           int seg, int grid, cudaStream_t s) {
+                           const CUtensorMap& tvm, int seg, int grid, cudaStream_t s) {
   if (a.hs == 64)
-    return bf16 ? launch_prefill_t<64, true>(a, tq, tk, tv, seg, grid, s) : launch_prefill_t<64, false>(a, tq, tk, tv, seg, grid, s);
-  return bf16 ? launch_prefill_t<128, true>(a, tq, tk, tv, seg, grid, s) : launch_prefill_t<128, false>(a, tq, tk, tv, seg, grid, s);
+    return bf16 ? launch_prefill_t<64, true>(a, tq, tk, tv, tvm, seg, grid, s)
+                : launch_prefill_t<64, false>(a, tq, tk, tv, tvm, seg, grid, s);
+  return bf16 ? launch_prefill_t<128, true>(a, tq, tk, tv, tvm, seg, grid, s)
+              : launch_prefill_t<128, false>(a, tq, tk, tv, tvm, seg, grid, s);
 }
 
 }  // namespace pa
