@@ -94,9 +94,31 @@ __device__ void block_scan_i64(int64_t v, int64_t* ex, int64_t* tot, long long* 
   __syncthreads();
 }
 
-// decode CTA whose key-tile range holds tile t: largest c with floor(c W / P) <= t
-__device__ __forceinline__ int cta_of(int64_t t, int64_t W, int64_t P) { return (int)(((t + 1) * P - 1) / W); }
-__device__ __forceinline__ int64_t cta_start(int64_t c, int64_t W, int64_t P) { return c * W / P; }
+// In-place suffix minimum of v[0 .. n) (n <= blockDim.x) across the block.
+__device__ void block_suffix_min(int* v, int n, int* s_w) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
+  int x = tid < n ? v[tid] : INT_MAX;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_down_sync(0xffffffffu, x, o);
+    if (lane + o < 32) x = min(x, y);
+  }
+  if (lane == 0) s_w[wid] = x;  // minimum of the warp's entries
+  __syncthreads();
+  if (wid == 0) {
+    int y = lane < nw ? s_w[lane] : INT_MAX;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int z = __shfl_down_sync(0xffffffffu, y, o);
+      if (lane + o < 32) y = min(y, z);
+    }
+    s_w[lane] = y;  // suffix minimum over warps lane ..
+  }
+  __syncthreads();
+  if (wid + 1 < nw) x = min(x, s_w[wid + 1]);
+  if (tid < n) v[tid] = x;
+  __syncthreads();
+}
 
 __device__ __forceinline__ void refuse(WsHeader* hdr) {
   atomicOr(&hdr->error, PA_DEVERR_BAD_BATCH);
@@ -112,7 +134,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
   __shared__ int s_warp[3][32];
   __shared__ int s_carry[3];
   __shared__ int s_cta_begin[kMaxDecCtas + 1];
-  __shared__ unsigned long long s_key[kSortCap];
+  // the sort keys of the prefill tiles; before the sort, the per-round tables of the
+  // decode partition (CTA starts, per-sequence first tile, tiles and length)
+  __shared__ __align__(16) unsigned long long s_key[kSortCap];
   __shared__ long long s_w64[32];
   __shared__ long long s_mirror_carry;
   __shared__ int s_mseq_carry;
@@ -137,31 +161,52 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
   // ---- validate the batch description; count the decode key tiles ----
   const int64_t max_kv = (int64_t)a.max_blocks * a.bs;
   if (tid == 0 && (a.cum[0] != 0 || a.cum[a.B] != a.N)) s_bad = 1;
+  long long dec_tiles = 0;
   for (int b = tid; b < a.B; b += blockDim.x) {
     const int64_t q = (int64_t)a.cum[b + 1] - a.cum[b];
     const int64_t kv = (int64_t)a.past[b] + q;
     if (q < 0 || a.past[b] < 0 || kv > max_kv || (a.max_query_len > 0 && q > a.max_query_len)) {
       atomicOr(&s_bad, 1);
     } else if (is_decode_class(q, a)) {
-      atomicAdd(&s_dec_tiles, (unsigned long long)ceil_div(kv, kDecTile));
+      dec_tiles += ceil_div(kv, kDecTile);
     }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) dec_tiles += __shfl_xor_sync(0xffffffffu, dec_tiles, o);
+  if ((tid & 31) == 0 && dec_tiles) atomicAdd(&s_dec_tiles, (unsigned long long)dec_tiles);
   for (int u = tid; u < a.B * a.kvh; u += blockDim.x) a.unit_done[u] = 0;
   __syncthreads();
   if (s_bad) {
     if (tid == 0) refuse(hdr);
     return;
   }
-  const int64_t W = (int64_t)s_dec_tiles * a.kvh;  // decode key tiles of all units, end to end
   const bool balanced = a.forced_split <= 0;
+  // The W decode key tiles of all units, laid end to end, are cut into P equal ranges:
+  // CTA c owns tiles [s_start[c], s_start[c + 1]), s_start[c] = floor(c W / P).
+  int64_t* s_start = reinterpret_cast<int64_t*>(s_key);   // [kMaxDecCtas + 1]
+  int64_t* s_T = s_start + (kMaxDecCtas + 1);              // [kPlanThreads] first tile of (b, head 0)
+  int* s_nt = reinterpret_cast<int*>(s_T + kPlanThreads);   // [kPlanThreads] tiles per unit (0: not decode)
+  int* s_kv = s_nt + kPlanThreads;                          // [kPlanThreads] keys
+  static_assert((kMaxDecCtas + 1 + kPlanThreads) * 8 + 2 * kPlanThreads * 4 <= kSortCap * 8, "tables fit s_key");
+  const int64_t W = (int64_t)s_dec_tiles * a.kvh;
+  for (int64_t c = tid; c <= P; c += blockDim.x) s_start[c] = c * W / P;  // one division per thread
+  const float pw = W > 0 ? (float)P / (float)W : 0.f;
+  // the CTA whose range holds tile t (the largest c with s_start[c] <= t): a float
+  // estimate corrected against the table
+  auto cta_of = [&](int64_t t) {
+    int c = min((int)((float)t * pw), (int)P - 1);
+    while (c > 0 && s_start[c] > t) --c;
+    while (c + 1 < P && s_start[c + 1] <= t) ++c;
+    return c;
+  };
 
   // ---- per-sequence counts, prefix sums, and the lists ----
   for (int base = 0; base < a.B; base += blockDim.x) {
     const int b = base + tid;
-    const int carry0 = s_carry[0], carry1 = s_carry[1], carry2 = s_carry[2];
+    const int carry0 = s_carry[0], carry1 = s_carry[1];
     int64_t q = 0, kv = 0, nt = 0;
     bool dec = false;
-    int v[3] = {0, 0, 0};  // [decode tiles of b's units, prefill tiles, -]
+    int v[3] = {0, 0, 0};  // [decode tiles of b's units, prefill tiles, prefill-class]
     if (b < a.B) {
       q = (int64_t)a.cum[b + 1] - a.cum[b];
       kv = (int64_t)a.past[b] + q;
@@ -186,57 +231,72 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
         a.mirror_seq[s_mseq_carry + ex[2]] = make_int2(b, (int)mb);
       }
     }
-    const int64_t T_b = (int64_t)carry0 + ex[0];  // first decode tile of (b, head 0)
-    // items of this sequence
-    int w[3] = {0, 0, 0};
-    if (dec) {
-      if (balanced) {
-        for (int g = 0; g < a.kvh; ++g) {
-          const int64_t u0 = T_b + g * nt, u1 = u0 + nt;
-          w[0] += cta_of(u1 - 1, W, P) - cta_of(u0, W, P) + 1;
-        }
-      } else {
-        w[0] = (int)(a.kvh * ceil_div(kv, a.forced_split));
-      }
-    }
-    int ex2[3], tot2[3];
-    block_scan3(w, ex2, tot2, s_warp);
+    s_T[tid] = (int64_t)carry0 + ex[0];
+    s_nt[tid] = dec ? (int)nt : 0;
+    s_kv[tid] = (int)kv;
     if (b < a.B) {
-      int idx = carry2 + ex2[0];
-      if (dec) {
-        for (int g = 0; g < a.kvh; ++g) {
-          const int unit_first = idx;
-          if (balanced) {
-            const int64_t u0 = T_b + g * nt, u1 = u0 + nt;
-            const int c0 = cta_of(u0, W, P), c1 = cta_of(u1 - 1, W, P);
-            for (int c = c0; c <= c1; ++c, ++idx) {
-              const int64_t lo = max(u0, cta_start(c, W, P)), hi = min(u1, cta_start(c + 1, W, P));
-              if (idx < a.max_items)
-                a.items[idx] = DecodeItem{b, g, (int)((lo - u0) * kDecTile), (int)min((hi - u0) * kDecTile, kv),
-                                          b * a.kvh + g, unit_first, c1 - c0 + 1, 0};
-              if (cta_start(c, W, P) >= u0) s_cta_begin[c] = idx;  // CTA c's range starts in this unit
-            }
-          } else {
-            const int64_t S = a.forced_split;
-            const int ns = (int)ceil_div(kv, S);
-            for (int s2 = 0; s2 < ns; ++s2, ++idx) {
-              if (idx < a.max_items)
-                a.items[idx] = DecodeItem{b, g, (int)(s2 * S), (int)min((s2 + 1) * S, kv), b * a.kvh + g,
-                                          unit_first, ns, 0};
-            }
-          }
-        }
-      }
       for (int t = 0; t < v[1]; ++t) {
         const int ti = carry1 + ex[1] + t;
         if (ti < a.max_tiles) a.tiles_unsorted[ti] = PrefillTile{b, t * kPreTileQ};
       }
     }
+    __syncthreads();
+    // ---- decode items of this round's units, one (sequence, KV head) unit per thread ----
+    const int units = min((int)blockDim.x, a.B - base) * a.kvh;
+    for (int ub = 0; ub < units; ub += blockDim.x) {
+      const int u = ub + tid;
+      int sb = 0, g = 0, n_u = 0, kv_u = 0, c0 = 0, c1 = -1, w = 0;
+      int64_t u0 = 0;
+      if (u < units) {
+        sb = u / a.kvh;
+        g = u - sb * a.kvh;
+        n_u = s_nt[sb];
+        if (n_u > 0) {
+          kv_u = s_kv[sb];
+          u0 = s_T[sb] + (int64_t)g * n_u;
+          if (balanced) {
+            c0 = cta_of(u0);
+            c1 = cta_of(u0 + n_u - 1);
+            w = c1 - c0 + 1;
+          } else {
+            w = (int)ceil_div(kv_u, a.forced_split);
+          }
+        }
+      }
+      int wv[3] = {w, 0, 0}, exw[3], totw[3];
+      block_scan3(wv, exw, totw, s_warp);
+      int idx = s_carry[2] + exw[0];
+      if (w > 0) {
+        const int bb = base + sb, unit = bb * a.kvh + g, unit_first = idx;
+        if (balanced) {
+          const int64_t u1 = u0 + n_u;
+          int64_t cs = s_start[c0];
+          for (int c = c0; c <= c1; ++c, ++idx) {
+            const int64_t ce = s_start[c + 1];
+            const int64_t lo = max(u0, cs), hi = min(u1, ce);
+            if (idx < a.max_items)
+              a.items[idx] = DecodeItem{bb, g, (int)((lo - u0) * kDecTile), (int)min((hi - u0) * kDecTile, (int64_t)kv_u),
+                                        unit, unit_first, w, 0};
+            if (cs >= u0) s_cta_begin[c] = idx;  // CTA c's range starts in this unit
+            cs = ce;
+          }
+        } else {
+          const int64_t S = a.forced_split;
+          for (int s2 = 0; s2 < w; ++s2, ++idx) {
+            if (idx < a.max_items)
+              a.items[idx] = DecodeItem{bb, g, (int)(s2 * S), (int)min((s2 + 1) * S, (int64_t)kv_u), unit, unit_first,
+                                        w, 0};
+          }
+        }
+      }
+      __syncthreads();  // every thread has read s_carry[2]
+      if (tid == 0) s_carry[2] += totw[0];
+      __syncthreads();
+    }
     __syncthreads();  // every thread has read the carries of this round
     if (tid == 0) {
       s_carry[0] += tot[0];
       s_carry[1] += tot[1];
-      s_carry[2] += tot2[0];
       s_mirror_carry += m_tot;
       s_mseq_carry += tot[2];
     }
@@ -253,11 +313,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
 
   // ---- item range of every decode CTA ----
   if (balanced) {
-    if (tid == 0) {
-      s_cta_begin[P] = n_items;
-      for (int64_t c = P - 1; c >= 0; --c)  // CTAs with an empty range (fewer tiles than CTAs)
-        if (s_cta_begin[c] == INT_MAX) s_cta_begin[c] = s_cta_begin[c + 1];
-    }
+    // a CTA with an empty range (fewer tiles than CTAs) starts where the next range does
+    __syncthreads();
+    block_suffix_min(s_cta_begin, (int)P, s_warp[0]);
+    for (int c = tid; c < P; c += blockDim.x) s_cta_begin[c] = min(s_cta_begin[c], n_items);
+    if (tid == 0) s_cta_begin[P] = n_items;
   } else {
     for (int64_t c = tid; c <= P; c += blockDim.x) s_cta_begin[c] = (int)(c * n_items / P);
   }
