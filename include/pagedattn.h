@@ -80,8 +80,13 @@ typedef struct pa_dims {
 /*
  * Bytes of device workspace pa_paged_attention needs for these sizes (0 on invalid
  * sizes). Pure host arithmetic; needs no GPU. The workspace holds the device-built work
- * plan, the split-KV partial results (fp32 output rows and their log-sum-exp) and the
- * device error word. It must be 256-byte aligned.
+ * plan, the split-KV partial results (fp32 output rows and their log-sum-exp), the
+ * device error word and, for bf16 when prefill is possible, an fp16 copy of the V rows of
+ * the prefill-class sequences with room for 4 * num_tokens keys (at most the cache's size).
+ * The prefill kernel reads V from that copy (one fp16 P V product per 16 keys) when the
+ * call's prefill-class sequences fit it and every copied value is representable in fp16;
+ * otherwise it reads the bf16 cache and splits P into two bf16 terms. It must be 256-byte
+ * aligned.
  */
 size_t pa_workspace_size(const pa_dims* dims, int32_t num_heads, int32_t kv_num_heads);
 
@@ -157,7 +162,8 @@ pa_status pa_paged_attention_static_workspace(const void* query, const void* key
 
 /* Stages of pa_paged_attention, in the order they must run. */
 #define PA_STAGE_PLAN 1u        /* device work partitioner: classify sequences, build work lists */
-#define PA_STAGE_CACHE_WRITE 2u /* scatter this step's K/V rows into the caches */
+#define PA_STAGE_CACHE_WRITE 2u /* scatter this step's K/V rows into the caches; for bf16, then
+                                   the fp16 copy of the prefill sequences' V the prefill reads */
 #define PA_STAGE_PREFILL 4u     /* tcgen05/TMEM attention for prefill-class sequences */
 #define PA_STAGE_DECODE 8u      /* split-KV attention for decode-class sequences, including the
                                    deterministic (out, lse) merge of the splits */

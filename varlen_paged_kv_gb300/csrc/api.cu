@@ -148,21 +148,22 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
     ++g_launches;
     if (cudaError_t e = pa::launch_plan(args, stream)) return cuda_fail(e, "plan_kernel launch");
   }
-  if ((stages & PA_STAGE_CACHE_WRITE) && args.N > 0) {
-    const int64_t work = (int64_t)args.N * 2 * (args.kv_row / 8);
-    const int64_t blocks = std::min<int64_t>((work + 255) / 256, (int64_t)info.sms * 16);
-    ++g_launches;
-    if (cudaError_t e = pa::launch_cache_write(args, (int)blocks, stream)) return cuda_fail(e, "cache_write_kernel launch");
-  }
   const bool can_decode = d->route == PA_ROUTE_AUTO;
   const bool can_prefill = prefill_possible(d, args.G);
-  if ((stages & PA_STAGE_PREFILL) && can_prefill && args.N > 0 && slots > 0) {
-    if (args.mirror_keys > 0) {  // the fp16 copy of V (the planner decides whether it is used)
+  if ((stages & PA_STAGE_CACHE_WRITE) && args.N > 0) {
+    const int64_t blocks = std::min<int64_t>(((int64_t)args.N + 7) / 8, (int64_t)info.sms * 8);  // a warp per token
+    ++g_launches;
+    if (cudaError_t e = pa::launch_cache_write(args, (int)blocks, stream)) return cuda_fail(e, "cache_write_kernel launch");
+    if (can_prefill && args.mirror_keys > 0 && slots > 0) {
+      // bf16: the fp16 copy of the prefill sequences' V, read from the cache just written
+      // (the planner decides whether it is made and used)
       const int64_t warps = (int64_t)args.mirror_keys;
-      const int64_t blocks = std::min<int64_t>((warps + 7) / 8, (int64_t)info.sms * 8);
+      const int64_t vb = std::min<int64_t>((warps + 7) / 8, (int64_t)info.sms * 8);
       ++g_launches;
-      if (cudaError_t e = pa::launch_v_mirror(args, (int)blocks, stream)) return cuda_fail(e, "v_mirror_kernel launch");
+      if (cudaError_t e = pa::launch_v_mirror(args, (int)vb, stream)) return cuda_fail(e, "v_mirror_kernel launch");
     }
+  }
+  if ((stages & PA_STAGE_PREFILL) && can_prefill && args.N > 0 && slots > 0) {
     const int seg = gcd(d->block_size, pa::kPreTileK);
     CUtensorMap tq, tk, tv, tvm;
     if (!query_map(&tq, query, dt, args.q_stride, args.N) || !cache_map(&tk, kc, dt, hs, args.kvh, slots, seg) ||

@@ -374,54 +374,70 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
 }
 
 // ---- cache write ----------------------------------------------------------------------------
-// One thread per 16-byte chunk of a token's K or V row. Consecutive threads cover
-// consecutive chunks of one row, so loads and stores are coalesced 16-byte accesses.
-// The slot is slot_mapping[i], or derived from the token's logical position
-// past_seqlens[b] + j through block_table. -1 skips; out-of-range slots and blocks are
-// skipped and flagged.
+// One warp per token: the slot is found once (slot_mapping[i], or the token's logical
+// position past_seqlens[b] + j through block_table), then the lanes copy the token's K and
+// V rows with 16-byte loads and stores, all loads of a row issued before its stores. -1
+// skips the token; out-of-range slots and blocks are skipped and flagged.
 __global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
   if (!a.hdr->valid) return;
+  const int lane = threadIdx.x & 31;
   const int chunks = a.kv_row / 8;  // 16-byte chunks in one K (or V) row
-  const int64_t per_tok = 2 * (int64_t)chunks;
-  const int64_t total = (int64_t)a.N * per_tok;
   const int64_t nslots = (int64_t)a.num_blocks * a.bs;
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int tok = (int)(idx / per_tok);
-    const int r = (int)(idx - (int64_t)tok * per_tok);
-    const int which = r >= chunks;  // 0: K row, 1: V row
-    const int c = which ? r - chunks : r;
+  const int warps = (int)((gridDim.x * blockDim.x) >> 5);
+  int b = 0;  // sequence of the previous token (tokens only grow within a warp)
+  for (int tok = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); tok < a.N; tok += warps) {
     int64_t slot;
     if (a.slot_mapping) {
       slot = a.slot_mapping[tok];
     } else {
-      int lo = 0, hi = a.B - 1;  // last b with cum[b] <= tok
+      int lo = b, hi = a.B - 1;  // last b with cum[b] <= tok
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (a.cum[mid] <= tok) lo = mid; else hi = mid - 1;
       }
-      const int64_t p = (int64_t)a.past[lo] + (tok - a.cum[lo]);
-      const int blk = a.block_table[(int64_t)lo * a.max_blocks + p / a.bs];
+      b = lo;
+      const int p = a.past[b] + (tok - a.cum[b]);
+      const int blk = a.block_table[(int64_t)b * a.max_blocks + p / a.bs];
       if (blk < 0 || blk >= a.num_blocks) {
-        if (c == 0) atomicOr(&a.hdr->error, PA_DEVERR_BAD_BLOCK);
+        if (lane == 0) atomicOr(&a.hdr->error, PA_DEVERR_BAD_BLOCK);
         continue;
       }
       slot = (int64_t)blk * a.bs + p % a.bs;
     }
     if (slot == -1) continue;
     if (slot < 0 || slot >= nslots) {
-      if (c == 0) atomicOr(&a.hdr->error, PA_DEVERR_BAD_SLOT);
+      if (lane == 0) atomicOr(&a.hdr->error, PA_DEVERR_BAD_SLOT);
       continue;
     }
-    const uint16_t* src;
+    const uint16_t *src_k, *src_v;
     if (a.packed) {
-      src = reinterpret_cast<const uint16_t*>(a.query) + (int64_t)tok * a.q_stride + (which ? a.v_offset : a.k_offset);
+      src_k = reinterpret_cast<const uint16_t*>(a.query) + (int64_t)tok * a.q_stride + a.k_offset;
+      src_v = reinterpret_cast<const uint16_t*>(a.query) + (int64_t)tok * a.q_stride + a.v_offset;
     } else {
-      src = reinterpret_cast<const uint16_t*>(which ? a.value : a.key) + (int64_t)tok * a.kv_row;
+      src_k = reinterpret_cast<const uint16_t*>(a.key) + (int64_t)tok * a.kv_row;
+      src_v = reinterpret_cast<const uint16_t*>(a.value) + (int64_t)tok * a.kv_row;
     }
-    uint16_t* dst = reinterpret_cast<uint16_t*>(which ? a.value_cache : a.key_cache) + slot * a.kv_row;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + c);
-    reinterpret_cast<uint4*>(dst)[c] = v;
+    uint4* dst_k = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.key_cache) + slot * a.kv_row);
+    uint4* dst_v = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.value_cache) + slot * a.kv_row);
+    for (int c0 = lane; c0 < chunks; c0 += 128) {
+      uint4 k[4], v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = c0 + 32 * j;
+        if (c < chunks) {
+          k[j] = __ldg(reinterpret_cast<const uint4*>(src_k) + c);
+          v[j] = __ldg(reinterpret_cast<const uint4*>(src_v) + c);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = c0 + 32 * j;
+        if (c < chunks) {
+          dst_k[c] = k[j];
+          dst_v[c] = v[j];
+        }
+      }
+    }
   }
 }
 
