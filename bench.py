@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import hashlib
 import json
 import math
 import os
@@ -248,17 +249,42 @@ class Runner:
         return (time.perf_counter() - t0) / steps, h2d, d2h
 
 
+# DRAM bytes (read + write) of one launch of the dominant kernel, from one ncu capture
+# (profiles/<kernel>_<workload>.md), with a hash of the kernel's sources at capture time:
+# the figure is reported only while the sources are unchanged, else traffic is null.
+NCU_TRAFFIC = {
+    ("decode_kernel", "decode-b64"): (623060736, "371fa9c26a118813"),
+    ("prefill_kernel", "causal-prefill-4x2048"): (129106432, "6abb481eb8e8e3ae"),
+}
+KERNEL_SOURCES = {"decode_kernel": ("decode.cu", "common.cuh"), "prefill_kernel": ("prefill.cu", "common.cuh")}
+
+
+def source_hash(kernel):
+    m = hashlib.sha1()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "varlen_paged_kv_gb300", "csrc", f), "rb") as fh:
+            m.update(fh.read())
+    return m.hexdigest()[:16]
+
+
+def ncu_traffic(kernel, name):
+    entry = NCU_TRAFFIC.get((kernel, name))
+    if entry is None or source_hash(kernel) != entry[1]:
+        return None
+    return entry[0]
+
+
 def kernel_roofline(p, kind, seconds_per_launch, pk):
     if kind == "hbm":
         units = kv_history_bytes(p)
         achieved = units / seconds_per_launch / 1e9
         return {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": ncu_traffic("decode_kernel", p.name),
                 "peak_source": f"{pk['source']} hbm_gbs", "algorithmic_bytes_per_launch": units}
     flops = causal_flops(p, prefill_sequences(p))
     achieved = flops / seconds_per_launch / 1e12
     return {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": None,
+            "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": ncu_traffic("prefill_kernel", p.name),
             "peak_source": f"{pk['source']} bf16_tflops (burst; fp16 nominal rate equals bf16)",
             "algorithmic_flops_per_launch": flops}
 
