@@ -51,8 +51,15 @@ struct DecodeItem {
   int32_t pad;
 };
 
-struct PrefillTile {    // 128 query rows [j0, j0+128) of sequence b (all heads)
+// 128 query rows [j0, j0 + 128) of sequence b (all heads), with the sequence's geometry,
+// so the prefill kernel reads one record per unit and no further lookups.
+struct __align__(32) PrefillTile {
   int32_t b, j0;
+  int32_t c0;           // cumulative_sequence_length[b]: the sequence's first packed row
+  int32_t q_len, past;
+  int32_t n_kv;         // 128-key tiles the query tile reads (causal)
+  int32_t mirror_row0;  // the sequence's first row in the fp16 V copy (when it is used)
+  int32_t pad;
 };
 
 struct WsLayout {
@@ -323,6 +330,12 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
       ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
       : "memory");
+}
+// bring a tile into L2 ahead of its load (no shared memory, no barrier)
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
+               : "memory");
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -223,10 +223,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
     block_scan3(v, ex, tot, s_warp);
     // rows of the fp16 V copy: every key of every prefill-class sequence, in sequence order
     int64_t m_ex = 0, m_tot = 0;
+    int mrow0 = 0;
     if (a.mirror_keys > 0) {
       block_scan_i64(v[1] > 0 ? kv : 0, &m_ex, &m_tot, s_w64);
       const int64_t mb = s_mirror_carry + m_ex;
       if (v[1] > 0 && mb + kv <= a.mirror_keys) {
+        mrow0 = (int)mb;
         a.mirror_base[b] = (int)mb;
         a.mirror_seq[s_mseq_carry + ex[2]] = make_int2(b, (int)mb);
       }
@@ -237,7 +239,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
     if (b < a.B) {
       for (int t = 0; t < v[1]; ++t) {
         const int ti = carry1 + ex[1] + t;
-        if (ti < a.max_tiles) a.tiles_unsorted[ti] = PrefillTile{b, t * kPreTileQ};
+        if (ti < a.max_tiles) {
+          const int j0 = t * kPreTileQ;
+          const int n_kv = (int)ceil_div((int64_t)a.past[b] + min((int64_t)j0 + kPreTileQ, q), kPreTileK);
+          a.tiles_unsorted[ti] = PrefillTile{b, j0, a.cum[b], (int)q, a.past[b], n_kv, mrow0, 0};
+        }
       }
     }
     __syncthreads();
@@ -331,10 +337,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
     for (int i = tid; i < n2; i += blockDim.x) {
       unsigned long long key = ~0ull;
       if (i < n_tiles) {
-        const PrefillTile t = a.tiles_unsorted[i];
-        const int64_t q = (int64_t)a.cum[t.b + 1] - a.cum[t.b];
-        const int64_t last = ((int64_t)t.j0 + kPreTileQ < q) ? (int64_t)t.j0 + kPreTileQ : q;
-        const int64_t cost = ceil_div((int64_t)a.past[t.b] + last, kPreTileK);
+        const int64_t cost = a.tiles_unsorted[i].n_kv;
         key = ((unsigned long long)(0xFFFFFFFFull - (unsigned long long)cost) << 32) | (unsigned)i;
       }
       s_key[i] = key;

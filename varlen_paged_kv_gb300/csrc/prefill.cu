@@ -62,6 +62,12 @@ __device__ __forceinline__ int snake_unit(int k) {
   return k * g + ((k & 1) ? g - 1 - (int)blockIdx.x : (int)blockIdx.x);
 }
 
+// the record of unit u (all zeros past the end)
+__device__ __forceinline__ PrefillTile load_tile(const Args& a, int u, int n_units, int units_per_tile) {
+  if (u >= n_units) return PrefillTile{};
+  return a.tiles[u / units_per_tile];
+}
+
 template <int HS, bool BF16>
 __global__ void __launch_bounds__(kPreThreads, 1)
     prefill_kernel(const Args a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -136,14 +142,20 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     }
     const int nseg = kPreTileK / seg_rows;
     uint32_t gs = 0, unit_cnt = 0;
+    // records of the current and the next two units, each loaded two units ahead of use
+    PrefillTile next = load_tile(a, snake_unit(0), n_units, units_per_tile);
+    PrefillTile next2 = load_tile(a, snake_unit(1), n_units, units_per_tile);
     for (int u = snake_unit(0); u < n_units; u = snake_unit(++unit_cnt)) {
-      const PrefillTile tile = a.tiles[u / units_per_tile];
+      const PrefillTile tile = next;
+      next = next2;
+      const int un = snake_unit(unit_cnt + 1);
+      next2 = load_tile(a, snake_unit(unit_cnt + 2), n_units, units_per_tile);
       const int h0 = (u % units_per_tile) * hpu, g = h0 / a.G;
-      const int c0 = a.cum[tile.b], q_len = a.cum[tile.b + 1] - c0, past = a.past[tile.b];
+      const int c0 = tile.c0, q_len = tile.q_len, past = tile.past;
       const int kv_len = past + q_len;
-      const int n_kv = (int)ceil_div(past + min(tile.j0 + kPreTileQ, q_len), kPreTileK);
+      const int n_kv = tile.n_kv;
       const int* bt = a.block_table + (int64_t)tile.b * a.max_blocks;
-      const int mirror_row0 = v16 ? a.mirror_base[tile.b] : 0;
+      const int mirror_row0 = tile.mirror_row0;
       if (lane == 0) {
         if (unit_cnt > 0) mbar_wait(q_empty, (unit_cnt - 1) & 1, abort, err);
         mbar_arrive_expect_tx(q_full, hpu * L::kQBytes);
@@ -152,6 +164,13 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           for (int hh = 0; hh < HALVES; ++hh)
             tma_load_2d(smem + L::kQ + x * L::kQBytes + hh * L::kHalfBytes, &tmQ, q_full, (h0 + x) * HS + hh * 64,
                         c0 + tile.j0);
+        if (un < n_units) {
+          // the next unit's Q into L2 now, so its load at the unit boundary is short
+          const int h0n = (un % units_per_tile) * hpu;
+          for (int x = 0; x < hpu; ++x)
+#pragma unroll
+            for (int hh = 0; hh < HALVES; ++hh) tma_prefetch_l2_2d(&tmQ, (h0n + x) * HS + hh * 64, next.c0 + next.j0);
+        }
       }
       for (int t = 0; t < n_kv; ++t, ++gs) {
         const int st = gs & 1;
@@ -200,11 +219,12 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     const uint64_t kdesc0 = sdesc_sw128(smem_u32(smem + L::kK0), 16, 1024);
     const uint64_t vdesc0 = sdesc_sw128(smem_u32(smem + L::kV0), L::kHalfBytes, 1024);
     uint32_t gs = 0, unit_cnt = 0;
+    PrefillTile next = load_tile(a, snake_unit(0), n_units, units_per_tile);
     for (int u = snake_unit(0); u < n_units; u = snake_unit(++unit_cnt)) {
-      const PrefillTile tile = a.tiles[u / units_per_tile];
-      const int c0 = a.cum[tile.b], q_len = a.cum[tile.b + 1] - c0, past = a.past[tile.b];
-      const int kv_len = past + q_len;
-      const int n_kv = (int)ceil_div(past + min(tile.j0 + kPreTileQ, q_len), kPreTileK);
+      const PrefillTile tile = next;  // loaded one unit ahead
+      next = load_tile(a, snake_unit(unit_cnt + 1), n_units, units_per_tile);
+      const int kv_len = tile.past + tile.q_len;
+      const int n_kv = tile.n_kv;
       mbar_wait(q_full, unit_cnt & 1, abort, err);
       tc_fence_after();
 
@@ -314,12 +334,13 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       const int bar_id = 2 + x;
       const float c = a.scale_log2;
       uint32_t gs = 0;
+      PrefillTile next = load_tile(a, snake_unit(0), n_units, units_per_tile);
       for (int k = 0, u = snake_unit(0); u < n_units; u = snake_unit(++k)) {
-        const PrefillTile tile = a.tiles[u / units_per_tile];
+        const PrefillTile tile = next;  // loaded during the previous unit's epilogue
         const int h = (u % units_per_tile) * hpu + x;
-        const int c0 = a.cum[tile.b], q_len = a.cum[tile.b + 1] - c0, past = a.past[tile.b];
+        const int c0 = tile.c0, q_len = tile.q_len, past = tile.past;
         const int kv_len = past + q_len;
-        const int n_kv = (int)ceil_div(past + min(tile.j0 + kPreTileQ, q_len), kPreTileK);
+        const int n_kv = tile.n_kv;
         const int lim = min(past + tile.j0 + row, kv_len - 1);  // last key this row sees
         const int lim_tile0 = past + tile.j0;                   // the smallest limit of the unit
         float m_used = -INFINITY, l = 0.f;
@@ -424,6 +445,9 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           mbar_arrive(&p_full[x]);
         }
         // ---- epilogue: wait for the last P V, normalise, store the valid rows ----
+        // (the next unit's record is loaded here, where few registers are live, and
+        // arrives while this unit's output is written)
+        next = load_tile(a, snake_unit(k + 1), n_units, units_per_tile);
         mbar_wait(&o_done[x], (gs + n_kv - 1) & 1, abort, err);
         tc_fence_after();
         {
