@@ -316,7 +316,8 @@ __global__ void __launch_bounds__(kPreThreads, 1)
   } else if (warp < 2 + 2 * kSoftWarpsPerHead) {
     // ======================= softmax: warps 2..9 head A, 10..17 head B =======================
     // Two warps share each TMEM lane quarter (rows), one per half of the 128 score columns;
-    // they exchange their partial row maxima through shared memory once per tile.
+    // they exchange their partial row maxima through shared memory once per tile, meeting
+    // at a 64-thread named barrier of their own.
     const int sw = warp - 2;
     const int x = sw / kSoftWarpsPerHead;  // head
     const int hsel = (sw >> 2) & 1;        // column half
@@ -331,7 +332,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       const uint32_t o_tmem = tmem + lane_off + o_col(x) + hsel * OCOLS;
       float* xmax = reinterpret_cast<float*>(smem + L::kXmax);
       float* xsum = reinterpret_cast<float*>(smem + L::kXsum);
-      const int bar_id = 2 + x;
+      const int pair_bar = 2 + x * 4 + quarter;  // named barrier of the two warps of this lane quarter
       const float c = a.scale_log2;
       uint32_t gs = 0;
       PrefillTile next = load_tile(a, snake_unit(0), n_units, units_per_tile);
@@ -377,7 +378,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           const float mr = c > 0.f ? fmax3(fmaxf(mc[0], mc[1]), mc[2], mc[3]) : fmin3(fminf(mc[0], mc[1]), mc[2], mc[3]);
           float* xm = xmax + ((gt & 1) * 2 + x) * (kPreTileQ * 2) + row * 2;
           xm[hsel] = mr * c;
-          named_bar_sync(bar_id, 32 * kSoftWarpsPerHead);
+          named_bar_sync(pair_bar, 64);
           const float m_tile = fmaxf(xm[0], xm[1]);
           const float m_new = fmaxf(m_used, m_tile);
           const bool any_grow = __any_sync(0xffffffffu, m_new > m_used + 8.0f);  // first tile: m_used = -inf
@@ -391,40 +392,64 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           // word (or, against bf16 V, the bf16 hi and lo words) of each key pair replaces
           // that pair's two score registers ----
           const float neg_m = -m_used;
-          float lc[2] = {0.f, 0.f};
-          if (BF16 && !v16) {
+          if constexpr (BF16) {
+            float lc[2] = {0.f, 0.f};
+            if (!v16) {
 #pragma unroll
-            for (int g2 = 0; g2 < COLS / 16; ++g2) {
-              uint32_t* q = r + g2 * 16;
+              for (int g2 = 0; g2 < COLS / 16; ++g2) {
+                uint32_t* q = r + g2 * 16;
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float p0 = fast_exp2(fmaf(__uint_as_float(q[2 * e]), c, neg_m));
-                const float p1 = fast_exp2(fmaf(__uint_as_float(q[2 * e + 1]), c, neg_m));
-                lc[0] += p0;
-                lc[1] += p1;
-                split_bf16x2(p0, p1, q[2 * e], q[2 * e + 1]);
+                for (int e = 0; e < 8; ++e) {
+                  const float p0 = fast_exp2(fmaf(__uint_as_float(q[2 * e]), c, neg_m));
+                  const float p1 = fast_exp2(fmaf(__uint_as_float(q[2 * e + 1]), c, neg_m));
+                  lc[0] += p0;
+                  lc[1] += p1;
+                  split_bf16x2(p0, p1, q[2 * e], q[2 * e + 1]);
+                }
+                const int kk = hsel * (COLS / 16) + g2;  // 16-key block of the tile
+                tmem_st_x8_nowait(s_base + p_col(kk), q[0], q[2], q[4], q[6], q[8], q[10], q[12], q[14]);
+                tmem_st_x8_nowait(s_base + p_col(kk) + 16, q[1], q[3], q[5], q[7], q[9], q[11], q[13], q[15]);
               }
-              const int kk = hsel * (COLS / 16) + g2;  // 16-key block of the tile
-              tmem_st_x8_nowait(s_base + p_col(kk), q[0], q[2], q[4], q[6], q[8], q[10], q[12], q[14]);
-              tmem_st_x8_nowait(s_base + p_col(kk) + 16, q[1], q[3], q[5], q[7], q[9], q[11], q[13], q[15]);
+            } else {
+#pragma unroll
+              for (int g2 = 0; g2 < COLS / 16; ++g2) {
+                uint32_t* q = r + g2 * 16;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const float p0 = fast_exp2(fmaf(__uint_as_float(q[2 * e]), c, neg_m));
+                  const float p1 = fast_exp2(fmaf(__uint_as_float(q[2 * e + 1]), c, neg_m));
+                  lc[0] += p0;
+                  lc[1] += p1;
+                  q[2 * e] = pack2<false>(p0, p1);
+                }
+                const int kk = hsel * (COLS / 16) + g2;
+                tmem_st_x8_nowait(s_base + p_col(kk), q[0], q[2], q[4], q[6], q[8], q[10], q[12], q[14]);
+              }
             }
+            l += lc[0] + lc[1];
           } else {
+            // s * c - m and the row sums on packed fp32 pairs (one instruction per key pair)
+            const uint64_t c2 = f2_make(c, c), nm2 = f2_make(neg_m, neg_m);
+            uint64_t lsum[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
 #pragma unroll
             for (int g2 = 0; g2 < COLS / 16; ++g2) {
               uint32_t* q = r + g2 * 16;
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
-                const float p0 = fast_exp2(fmaf(__uint_as_float(q[2 * e]), c, neg_m));
-                const float p1 = fast_exp2(fmaf(__uint_as_float(q[2 * e + 1]), c, neg_m));
-                lc[0] += p0;
-                lc[1] += p1;
+                float x0, x1;
+                f2_split(f2_fma(f2_make(__uint_as_float(q[2 * e]), __uint_as_float(q[2 * e + 1])), c2, nm2), x0, x1);
+                const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                lsum[e & 1] = f2_add(lsum[e & 1], f2_make(p0, p1));
                 q[2 * e] = pack2<false>(p0, p1);
               }
-              const int kk = hsel * (COLS / 16) + g2;  // 16-key block of the tile
+              const int kk = hsel * (COLS / 16) + g2;
               tmem_st_x8_nowait(s_base + p_col(kk), q[0], q[2], q[4], q[6], q[8], q[10], q[12], q[14]);
             }
+            float a0, a1, b0, b1;
+            f2_split(lsum[0], a0, a1);
+            f2_split(lsum[1], b0, b1);
+            l += (a0 + b0) + (a1 + b1);
           }
-          l += lc[0] + lc[1];
           tmem_wait_st();
           if (t > 0) {
             // O holds P_0..P_{t-2} V; wait for P_{t-1} V before rescaling it
@@ -453,7 +478,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         {
           float* xs = xsum + x * (kPreTileQ * 2) + row * 2;
           xs[hsel] = l;
-          named_bar_sync(bar_id, 32 * kSoftWarpsPerHead);
+          named_bar_sync(pair_bar, 64);
           const float inv = 1.f / (xs[0] + xs[1]);
           const bool store = tile.j0 + row < q_len;
           uint16_t* dst =
