@@ -181,6 +181,35 @@ struct PreSmem {
   static constexpr int kBytes = kXsum + 2 * kPreTileQ * 2 * 4 + 1024;
 };
 
+// ---- programmatic dependent launch ---------------------------------------------------------
+// Every kernel is launched so that it may start while its predecessor in the stream is still
+// finishing: its launch and prologue (barrier set-up, TMEM allocation) overlap the
+// predecessor's tail. Each kernel calls pdl_wait() on every path before it first touches
+// memory that an earlier kernel reads or writes; that wait returns once the predecessor has
+// completed and its writes are visible, and since the predecessor waited for its own
+// predecessor, completion is transitive along the stream. pdl_launch_dependents() lets the
+// next kernel launch (its CTAs then sit in their own pdl_wait until this grid completes).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Actual>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Actual&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Actual&&>(args)...);
+}
+
 // ---- host launchers, one per kernel family (defined next to their kernels) -----------------
 cudaError_t launch_plan(const Args& a, cudaStream_t s);
 cudaError_t launch_cache_write(const Args& a, int grid, cudaStream_t s);

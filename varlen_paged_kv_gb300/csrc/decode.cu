@@ -69,6 +69,8 @@ __global__ void __launch_bounds__(160, 2)
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_wait();  // the work lists and caches written by the earlier kernels of this call
+  pdl_launch_dependents();
   const int it_begin = a.cta_begin[blockIdx.x], it_end = a.cta_begin[blockIdx.x + 1];
 
   if (warp == kDecWarps) {
@@ -398,8 +400,7 @@ static cudaError_t launch_decode_t(const Args& a, const CUtensorMap& tk, const C
   constexpr int smem = DecSmem<HS>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<HS, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<HS, BF16><<<a.dec_ctas, 160, smem, s>>>(a, tk, tv, seg);
-  return cudaGetLastError();
+  return launch_pdl(decode_kernel<HS, BF16>, dim3(a.dec_ctas), dim3(160), smem, s, a, tk, tv, seg);
 }
 
 cudaError_t launch_decode(const Args& a, bool bf16, const CUtensorMap& tk, const CUtensorMap& tv, int seg,

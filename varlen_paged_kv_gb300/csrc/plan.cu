@@ -144,6 +144,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
   const int tid = threadIdx.x;
   WsHeader* hdr = a.hdr;
   const int64_t P = a.dec_ctas;
+  pdl_wait();  // the previous call's kernels may still read this workspace
+  pdl_launch_dependents();
   if (tid == 0) {
     s_bad = 0;
     s_dec_tiles = 0;
@@ -382,6 +384,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
 // V rows with 16-byte loads and stores, all loads of a row issued before its stores. -1
 // skips the token; out-of-range slots and blocks are skipped and flagged.
 __global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
+  pdl_wait();
+  pdl_launch_dependents();
   if (!a.hdr->valid) return;
   const int lane = threadIdx.x & 31;
   const int chunks = a.kv_row / 8;  // 16-byte chunks in one K (or V) row
@@ -452,6 +456,8 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
 // cache instead; a block outside the pool is flagged and its rows are zeros (as the
 // attention reads them from the cache).
 __global__ void __launch_bounds__(256) v_mirror_kernel(const Args a) {
+  pdl_wait();
+  pdl_launch_dependents();
   const WsHeader* hdr = a.hdr;
   if (!hdr->valid || !hdr->v_mirror) return;
   const int rows = hdr->mirror_rows;
@@ -499,18 +505,15 @@ __global__ void __launch_bounds__(256) v_mirror_kernel(const Args a) {
 
 // ---- host launchers ----
 cudaError_t launch_plan(const Args& a, cudaStream_t s) {
-  plan_kernel<<<1, kPlanThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, a);
 }
 
 cudaError_t launch_cache_write(const Args& a, int grid, cudaStream_t s) {
-  cache_write_kernel<<<grid, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(cache_write_kernel, dim3(grid), dim3(256), 0, s, a);
 }
 
 cudaError_t launch_v_mirror(const Args& a, int grid, cudaStream_t s) {
-  v_mirror_kernel<<<grid, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(v_mirror_kernel, dim3(grid), dim3(256), 0, s, a);
 }
 
 }  // namespace pa

@@ -122,6 +122,8 @@ __global__ void __launch_bounds__(kPreThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the work list, caches and V copy written by the earlier kernels of this call
+  pdl_launch_dependents();
 
   const bool pair = (a.G & 1) == 0;  // two query heads of one KV head per unit
   // bf16: V from the fp16 copy (one fp16 P V product per 16 keys), unless the planner found
@@ -523,8 +525,7 @@ static cudaError_t launch_prefill_t(const Args& a, const CUtensorMap& tq, const 
   constexpr int smem = PreSmem<HS>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<HS, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  prefill_kernel<HS, BF16><<<grid, kPreThreads, smem, s>>>(a, tq, tk, tv, tvm, seg);
-  return cudaGetLastError();
+  return launch_pdl(prefill_kernel<HS, BF16>, dim3(grid), dim3(kPreThreads), smem, s, a, tq, tk, tv, tvm, seg);
 }
 
 cudaError_t launch_prefill(const Args& a, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
