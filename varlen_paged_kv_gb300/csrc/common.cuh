@@ -43,7 +43,7 @@ static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 // One (sequence b, KV head g, key range) of a decode-class sequence. The (b, g) pair is a
 // "unit"; a unit cut into several items has each item write an fp32 partial, and the
 // last item to finish (counted in unit_done) merges them in key order.
-struct DecodeItem {
+struct __align__(16) DecodeItem {
   int32_t b, g, key_begin, key_end;
   int32_t unit;         // b * kv_num_heads + g
   int32_t unit_first;   // index of the unit's first item (its items are consecutive)

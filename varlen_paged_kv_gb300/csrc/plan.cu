@@ -68,6 +68,15 @@ __device__ void block_scan3(const int v[3], int ex[3], int tot[3], int (*s_warp)
   __syncthreads();
 }
 
+// one decode item as two 16-byte stores (an aggregate assignment of the record went
+// through a local-memory temporary and cost microseconds per thousand items)
+__device__ __forceinline__ void store_item(DecodeItem* dst, int b, int g, int key_begin, int key_end, int unit,
+                                           int unit_first, int n_split) {
+  int4* d = reinterpret_cast<int4*>(dst);
+  d[0] = make_int4(b, g, key_begin, key_end);
+  d[1] = make_int4(unit, unit_first, n_split, 0);
+}
+
 // exclusive scan of one int64 across the block; *tot gets the block total
 __device__ void block_scan_i64(int64_t v, int64_t* ex, int64_t* tot, long long* s_w) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -283,8 +292,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
             const int64_t ce = s_start[c + 1];
             const int64_t lo = max(u0, cs), hi = min(u1, ce);
             if (idx < a.max_items)
-              a.items[idx] = DecodeItem{bb, g, (int)((lo - u0) * kDecTile), (int)min((hi - u0) * kDecTile, (int64_t)kv_u),
-                                        unit, unit_first, w, 0};
+              store_item(a.items + idx, bb, g, (int)((lo - u0) * kDecTile), (int)min((hi - u0) * kDecTile, (int64_t)kv_u),
+                         unit, unit_first, w);
             if (cs >= u0) s_cta_begin[c] = idx;  // CTA c's range starts in this unit
             cs = ce;
           }
@@ -292,8 +301,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
           const int64_t S = a.forced_split;
           for (int s2 = 0; s2 < w; ++s2, ++idx) {
             if (idx < a.max_items)
-              a.items[idx] = DecodeItem{bb, g, (int)(s2 * S), (int)min((s2 + 1) * S, (int64_t)kv_u), unit, unit_first,
-                                        w, 0};
+              store_item(a.items + idx, bb, g, (int)(s2 * S), (int)min((s2 + 1) * S, (int64_t)kv_u), unit, unit_first, w);
           }
         }
       }
