@@ -41,14 +41,16 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
 // One (sequence b, KV head g, key range) of a decode-class sequence. The (b, g) pair is a
-// "unit"; a unit cut into several items has each item write an fp32 partial, and the
-// last item to finish (counted in unit_done) merges them in key order.
+// "unit" (index b * kv_num_heads + g); a unit cut into several items has each item write
+// an fp32 partial, and the last item to finish (counted in unit_done) merges them in key
+// order.
 struct __align__(16) DecodeItem {
   int32_t b, g, key_begin, key_end;
-  int32_t unit;         // b * kv_num_heads + g
   int32_t unit_first;   // index of the unit's first item (its items are consecutive)
   int32_t n_split;      // items in the unit; 1 = the item writes the output itself
-  int32_t pad;
+  int32_t c0;           // cumulative_sequence_length[b]
+  int32_t q_len, past;  // the sequence's new rows and history (so the kernel needs no lookups)
+  int32_t pad[3];
 };
 
 // 128 query rows [j0, j0 + 128) of sequence b (all heads), with the sequence's geometry,

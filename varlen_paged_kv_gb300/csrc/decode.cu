@@ -40,6 +40,40 @@ __device__ __forceinline__ void row_stats(const float* mw, const float* lw, int 
   }
 }
 
+// the record of item it (all zeros from it_end on)
+__device__ __forceinline__ DecodeItem load_item(const Args& a, int it, int it_end) {
+  if (it >= it_end) return DecodeItem{};
+  const int4* p = reinterpret_cast<const int4*>(a.items + it);
+  const int4 x = p[0], y = p[1], z = p[2];
+  DecodeItem d;
+  d.b = x.x; d.g = x.y; d.key_begin = x.z; d.key_end = x.w;
+  d.unit_first = y.x; d.n_split = y.y; d.c0 = y.z; d.q_len = y.w;
+  d.past = z.x; d.pad[0] = d.pad[1] = d.pad[2] = 0;
+  return d;
+}
+
+// Q fragments of an item (A operand, row-major 16 x HS, row r = j * G + hq), straight from
+// global memory; rows past the item's q_len * G are zeros
+template <int HS>
+__device__ __forceinline__ void load_q(const Args& a, const DecodeItem& item, int r0, int r1, int tq,
+                                       uint32_t (&qa)[HS / 16][4]) {
+  const int n_rows = item.q_len * a.G;
+  const uint16_t* q = reinterpret_cast<const uint16_t*>(a.query);
+  const uint16_t* p0 = nullptr;
+  const uint16_t* p1 = nullptr;
+  if (r0 < n_rows)
+    p0 = q + (int64_t)(item.c0 + r0 / a.G) * a.q_stride + (int64_t)(item.g * a.G + r0 % a.G) * HS + tq * 2;
+  if (r1 < n_rows)
+    p1 = q + (int64_t)(item.c0 + r1 / a.G) * a.q_stride + (int64_t)(item.g * a.G + r1 % a.G) * HS + tq * 2;
+#pragma unroll
+  for (int ks = 0; ks < HS / 16; ++ks) {
+    qa[ks][0] = p0 ? __ldg(reinterpret_cast<const uint32_t*>(p0 + ks * 16)) : 0u;
+    qa[ks][2] = p0 ? __ldg(reinterpret_cast<const uint32_t*>(p0 + ks * 16 + 8)) : 0u;
+    qa[ks][1] = p1 ? __ldg(reinterpret_cast<const uint32_t*>(p1 + ks * 16)) : 0u;
+    qa[ks][3] = p1 ? __ldg(reinterpret_cast<const uint32_t*>(p1 + ks * 16 + 8)) : 0u;
+  }
+}
+
 template <int HS, bool BF16>
 __global__ void __launch_bounds__(160, 2)
     decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -82,9 +116,11 @@ __global__ void __launch_bounds__(160, 2)
     const int nseg = kDecTile / seg_rows;
     const int oob = a.num_blocks * a.bs;  // a row coordinate past the end: TMA fills zeros
     uint32_t cnt = 0;
+    DecodeItem next = load_item(a, it_begin, it_end);
     for (int it = it_begin; it < it_end; ++it) {
-      const DecodeItem item = a.items[it];
-      const int kv_len = a.past[item.b] + (a.cum[item.b + 1] - a.cum[item.b]);
+      const DecodeItem item = next;  // loaded one item ahead
+      next = load_item(a, it + 1, it_end);
+      const int kv_len = item.past + item.q_len;
       const int* bt = a.block_table + (int64_t)item.b * a.max_blocks;
       for (int k0 = item.key_begin; k0 < item.key_end; k0 += kDecTile, ++cnt) {
         const int s = cnt % kDecStages;
@@ -120,31 +156,14 @@ __global__ void __launch_bounds__(160, 2)
   const int tq = lane & 3, gq = lane >> 2;  // quad position, row within the 8-row group
   const int r0 = gq, r1 = gq + 8;           // the two rows this thread holds in MMA fragments
   uint32_t cnt = 0;
+  DecodeItem next = load_item(a, it_begin, it_end);
   for (int it = it_begin; it < it_end; ++it) {
-    const DecodeItem item = a.items[it];
-    const int c0 = a.cum[item.b];
-    const int q_len = a.cum[item.b + 1] - c0;
-    const int past = a.past[item.b];
+    const DecodeItem item = next;  // loaded one item ahead
+    next = load_item(a, it + 1, it_end);
+    const int c0 = item.c0, q_len = item.q_len, past = item.past;
     const int n_rows = q_len * a.G;
-
-    // Q fragments (A operand, row-major 16 x HS), straight from global memory
     uint32_t qa[NKS][4];
-    {
-      const uint16_t* q = reinterpret_cast<const uint16_t*>(a.query);
-      const uint16_t* p0 = nullptr;
-      const uint16_t* p1 = nullptr;
-      if (r0 < n_rows)
-        p0 = q + (int64_t)(c0 + r0 / a.G) * a.q_stride + (int64_t)(item.g * a.G + r0 % a.G) * HS + tq * 2;
-      if (r1 < n_rows)
-        p1 = q + (int64_t)(c0 + r1 / a.G) * a.q_stride + (int64_t)(item.g * a.G + r1 % a.G) * HS + tq * 2;
-#pragma unroll
-      for (int ks = 0; ks < NKS; ++ks) {
-        qa[ks][0] = p0 ? __ldg(reinterpret_cast<const uint32_t*>(p0 + ks * 16)) : 0u;
-        qa[ks][2] = p0 ? __ldg(reinterpret_cast<const uint32_t*>(p0 + ks * 16 + 8)) : 0u;
-        qa[ks][1] = p1 ? __ldg(reinterpret_cast<const uint32_t*>(p1 + ks * 16)) : 0u;
-        qa[ks][3] = p1 ? __ldg(reinterpret_cast<const uint32_t*>(p1 + ks * 16 + 8)) : 0u;
-      }
-    }
+    load_q<HS>(a, item, r0, r1, tq, qa);
     // causal limits (inclusive) of the two rows; padding rows borrow the last row's
     const int lim0 = past + min(r0 / a.G, q_len - 1);
     const int lim1 = past + min(r1 / a.G, q_len - 1);
@@ -293,18 +312,16 @@ __global__ void __launch_bounds__(160, 2)
       if (w == ww) {
 #pragma unroll
         for (int d = 0; d < ND; ++d) {
-          float* c0p = comb + r0 * kCombStride + d * 8 + tq * 2;
-          float* c1p = comb + r1 * kCombStride + d * 8 + tq * 2;
+          float2* c0p = reinterpret_cast<float2*>(comb + r0 * kCombStride + d * 8 + tq * 2);
+          float2* c1p = reinterpret_cast<float2*>(comb + r1 * kCombStride + d * 8 + tq * 2);
+          const float2 a0 = make_float2(o[d][0] * f0, o[d][1] * f0), a1 = make_float2(o[d][2] * f1, o[d][3] * f1);
           if (ww == 0) {
-            c0p[0] = o[d][0] * f0;
-            c0p[1] = o[d][1] * f0;
-            c1p[0] = o[d][2] * f1;
-            c1p[1] = o[d][3] * f1;
+            *c0p = a0;
+            *c1p = a1;
           } else {
-            c0p[0] += o[d][0] * f0;
-            c0p[1] += o[d][1] * f0;
-            c1p[0] += o[d][2] * f1;
-            c1p[1] += o[d][3] * f1;
+            const float2 b0 = *c0p, b1 = *c1p;
+            *c0p = make_float2(b0.x + a0.x, b0.y + a0.y);
+            *c1p = make_float2(b1.x + a1.x, b1.y + a1.y);
           }
         }
       }
@@ -347,13 +364,17 @@ __global__ void __launch_bounds__(160, 2)
             a.part_lse[(int64_t)it * kDecRows + row] =
                 Lr > 0.f ? (M + fast_log2(Lr)) * 0.69314718055994531f : -INFINITY;
         }
-        __threadfence();  // this thread's partial is visible device-wide before the arrival
-        consumer_bar();
-        if (t == 0) *s_last = atomicAdd(&a.unit_done[item.unit], 1) == item.n_split - 1;
+        consumer_bar();  // every consumer thread's partial is written
+        if (t == 0) {
+          // one fence after the barrier publishes the CTA's partial (fence cumulativity), and
+          // one after the arrival orders the merge's reads of the other items' partials
+          __threadfence();
+          *s_last = atomicAdd(&a.unit_done[item.b * a.kvh + item.g], 1) == item.n_split - 1;
+          __threadfence();
+        }
         consumer_bar();
         if (*s_last && mine) {
           // the unit's other items have all arrived: merge its partials in key order
-          __threadfence();
           float Mx = -INFINITY;
           for (int s2 = 0; s2 < item.n_split; ++s2)
             Mx = fmaxf(Mx, __ldcg(a.part_lse + (int64_t)(item.unit_first + s2) * kDecRows + row));

@@ -68,13 +68,14 @@ __device__ void block_scan3(const int v[3], int ex[3], int tot[3], int (*s_warp)
   __syncthreads();
 }
 
-// one decode item as two 16-byte stores (an aggregate assignment of the record went
+// one decode item as three 16-byte stores (an aggregate assignment of the record went
 // through a local-memory temporary and cost microseconds per thousand items)
-__device__ __forceinline__ void store_item(DecodeItem* dst, int b, int g, int key_begin, int key_end, int unit,
-                                           int unit_first, int n_split) {
+__device__ __forceinline__ void store_item(DecodeItem* dst, int b, int g, int key_begin, int key_end,
+                                           int unit_first, int n_split, int c0, int q_len, int past) {
   int4* d = reinterpret_cast<int4*>(dst);
   d[0] = make_int4(b, g, key_begin, key_end);
-  d[1] = make_int4(unit, unit_first, n_split, 0);
+  d[1] = make_int4(unit_first, n_split, c0, q_len);
+  d[2] = make_int4(past, 0, 0, 0);
 }
 
 // exclusive scan of one int64 across the block; *tot gets the block total
@@ -195,10 +196,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
   // The W decode key tiles of all units, laid end to end, are cut into P equal ranges:
   // CTA c owns tiles [s_start[c], s_start[c + 1]), s_start[c] = floor(c W / P).
   int64_t* s_start = reinterpret_cast<int64_t*>(s_key);   // [kMaxDecCtas + 1]
-  int64_t* s_T = s_start + (kMaxDecCtas + 1);              // [kPlanThreads] first tile of (b, head 0)
-  int* s_nt = reinterpret_cast<int*>(s_T + kPlanThreads);   // [kPlanThreads] tiles per unit (0: not decode)
-  int* s_kv = s_nt + kPlanThreads;                          // [kPlanThreads] keys
-  static_assert((kMaxDecCtas + 1 + kPlanThreads) * 8 + 2 * kPlanThreads * 4 <= kSortCap * 8, "tables fit s_key");
+  int* s_T = reinterpret_cast<int*>(s_start + (kMaxDecCtas + 1));  // [kPlanThreads] first tile of (b, head 0)
+  int* s_nt = s_T + kPlanThreads;     // [kPlanThreads] tiles per unit (0: not decode)
+  int* s_kv = s_nt + kPlanThreads;    // [kPlanThreads] keys
+  int* s_c0 = s_kv + kPlanThreads;    // [kPlanThreads] first packed row
+  int* s_past = s_c0 + kPlanThreads;  // [kPlanThreads] history
+  static_assert((kMaxDecCtas + 1) * 8 + 5 * kPlanThreads * 4 <= kSortCap * 8, "tables fit s_key");
   const int64_t W = (int64_t)s_dec_tiles * a.kvh;
   for (int64_t c = tid; c <= P; c += blockDim.x) s_start[c] = c * W / P;  // one division per thread
   const float pw = W > 0 ? (float)P / (float)W : 0.f;
@@ -244,9 +247,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
         a.mirror_seq[s_mseq_carry + ex[2]] = make_int2(b, (int)mb);
       }
     }
-    s_T[tid] = (int64_t)carry0 + ex[0];
+    s_T[tid] = carry0 + ex[0];
     s_nt[tid] = dec ? (int)nt : 0;
     s_kv[tid] = (int)kv;
+    s_c0[tid] = b < a.B ? a.cum[b] : 0;
+    s_past[tid] = (int)(kv - q);
     if (b < a.B) {
       for (int t = 0; t < v[1]; ++t) {
         const int ti = carry1 + ex[1] + t;
@@ -284,7 +289,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
       block_scan3(wv, exw, totw, s_warp);
       int idx = s_carry[2] + exw[0];
       if (w > 0) {
-        const int bb = base + sb, unit = bb * a.kvh + g, unit_first = idx;
+        const int bb = base + sb, unit_first = idx;
+        const int row0 = s_c0[sb], past = s_past[sb], q_u = kv_u - past;
         if (balanced) {
           const int64_t u1 = u0 + n_u;
           int64_t cs = s_start[c0];
@@ -293,7 +299,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
             const int64_t lo = max(u0, cs), hi = min(u1, ce);
             if (idx < a.max_items)
               store_item(a.items + idx, bb, g, (int)((lo - u0) * kDecTile), (int)min((hi - u0) * kDecTile, (int64_t)kv_u),
-                         unit, unit_first, w);
+                         unit_first, w, row0, q_u, past);
             if (cs >= u0) s_cta_begin[c] = idx;  // CTA c's range starts in this unit
             cs = ce;
           }
@@ -301,7 +307,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
           const int64_t S = a.forced_split;
           for (int s2 = 0; s2 < w; ++s2, ++idx) {
             if (idx < a.max_items)
-              store_item(a.items + idx, bb, g, (int)(s2 * S), (int)min((s2 + 1) * S, (int64_t)kv_u), unit, unit_first, w);
+              store_item(a.items + idx, bb, g, (int)(s2 * S), (int)min((s2 + 1) * S, (int64_t)kv_u), unit_first, w, row0,
+                         q_u, past);
           }
         }
       }
