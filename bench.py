@@ -8,6 +8,11 @@ GB/s = the K and V history bytes the step must read (each element once) / step t
 The other workloads (causal prefill 4 x 2048 bf16, the mixed continuous batch, long
 decode with 16-token pages) are measured in the same run under "secondary".
 
+Timing: the step time comes from K whole steps, one call each, between CUDA events on
+the launching stream; the dominant kernel's time from K more steps split into three calls
+around that kernel (the kernel bracketed by its own events); e2e from pipelined steps
+through the Python API with pinned host buffers (wall clock).
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 N > 1 runs under torchrun, one rank per GPU, each rank on its own batch (weak scaling,
 no collective on the data path).
@@ -216,35 +221,79 @@ class Runner:
         kern = sum(a.elapsed_time(b) for a, b in ev) / 1e3 / steps
         return total / steps, kern, launches
 
+    def whole(self, steps, warmup, clocks=None):
+        """Times `steps` whole steps, one call each (how a caller runs the operator).
+        Returns (seconds per step, launches per step)."""
+        torch, pa = self.torch, self.pa
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n0 = pa.kernel_launch_count()
+        if clocks is not None:
+            clocks.__enter__()
+        torch.cuda.synchronize()
+        start.record(self.stream)
+        for _ in range(steps):
+            self.step()
+        end.record(self.stream)
+        torch.cuda.synchronize()
+        if clocks is not None:
+            clocks.__exit__(None, None, None)
+        launches = pa.kernel_launch_count() - n0
+        return start.elapsed_time(end) / 1e3 / steps, launches / steps
+
     def e2e(self, steps, warmup):
         """The public Python API with host buffers: per step, H2D of the step's inputs from
-        pinned memory, the call, D2H of the output; the caches stay resident."""
+        pinned memory, the call, D2H of the output; the caches stay resident. Steps are
+        pipelined as a serving loop runs them: the inputs of step i+1 travel on one copy
+        stream and the output of step i on another while step i+1 computes (two sets of
+        device input and output buffers), so every step's copies are inside the timed region
+        but overlap other steps' compute."""
         torch, pa = self.torch, self.pa
         p = self.p
-        pins = {}
-        for name, dev in (("query", self.q), ("key", self.k), ("value", self.v), ("cum", self.cum),
-                          ("past", self.past), ("bt", self.bt), ("sm", self.sm)):
-            if dev is not None:
-                pins[name] = (torch.empty(dev.shape, dtype=dev.dtype, pin_memory=True), dev)
-                pins[name][0].copy_(dev.cpu())
-        out_host = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
-        h2d = sum(h.numel() * h.element_size() for h, _ in pins.values())
-        d2h = out_host.numel() * out_host.element_size()
+        names = ("query", "key", "value", "cum", "past", "bt", "sm")
+        devs = dict(zip(names, (self.q, self.k, self.v, self.cum, self.past, self.bt, self.sm)))
+        pins = {n: torch.empty(d.shape, dtype=d.dtype, pin_memory=True) for n, d in devs.items() if d is not None}
+        for n, h in pins.items():
+            h.copy_(devs[n].cpu())
+        # two sets of device inputs and outputs (set 0 is the runner's own tensors)
+        sets = [dict(devs), {n: (torch.empty_like(d) if d is not None else None) for n, d in devs.items()}]
+        outs = [self.out, torch.empty_like(self.out)]
+        out_host = [torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True) for _ in range(2)]
+        h2d = sum(h.numel() * h.element_size() for h in pins.values())
+        d2h = out_host[0].numel() * out_host[0].element_size()
+        comp = torch.cuda.current_stream()
+        up, down = torch.cuda.Stream(), torch.cuda.Stream()
+        ready = [torch.cuda.Event() for _ in range(2)]
+        computed = [torch.cuda.Event() for _ in range(2)]
+        drained = [torch.cuda.Event() for _ in range(2)]
 
-        def one():
-            for h, d in pins.values():
-                d.copy_(h, non_blocking=True)
-            pa.paged_attention(self.q, self.k, self.v, self.kc, self.vc, self.cum, self.past, self.bt, self.sm,
-                               num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, scale=p.scale,
-                               output=self.out, workspace=self.ws, max_query_len=self.max_q)
-            out_host.copy_(self.out, non_blocking=True)
+        def one(i):
+            k = i & 1
+            d = sets[k]
+            with torch.cuda.stream(up):
+                up.wait_event(computed[k])  # step i-2 has finished reading this set
+                for n, h in pins.items():
+                    d[n].copy_(h, non_blocking=True)
+                ready[k].record(up)
+            comp.wait_event(ready[k])
+            comp.wait_event(drained[k])  # step i-2's output has left this buffer
+            pa.paged_attention(d["query"], d["key"], d["value"], self.kc, self.vc, d["cum"], d["past"], d["bt"],
+                               d["sm"], num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, scale=p.scale,
+                               output=outs[k], workspace=self.ws, max_query_len=self.max_q)
+            computed[k].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(computed[k])
+                out_host[k].copy_(outs[k], non_blocking=True)
+                drained[k].record(down)
 
-        for _ in range(warmup):
-            one()
+        for i in range(warmup):
+            one(i)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for _ in range(steps):
-            one()
+        for i in range(steps):
+            one(i)
         torch.cuda.synchronize()
         return (time.perf_counter() - t0) / steps, h2d, d2h
 
@@ -325,19 +374,22 @@ WORKLOAD_TEXT = {
 
 
 def measure(r, steps, warmup, pk, clocks=None):
-    """Times one workload; the dominant kernel (prefill for workloads with prefill rows,
-    else decode) is bracketed by its own events inside the timed region."""
+    """Times one workload: whole steps (one call each) for the step time, then the same
+    steps split around the dominant kernel (prefill for workloads with prefill rows, else
+    decode), which is bracketed by its own events. Returns (seconds per step, roofline,
+    kernel launches in the whole-step timed region)."""
     q = r.p
+    sec, per_step = r.whole(steps, warmup, clocks=clocks)
     if prefill_sequences(q):
-        s, kt, launches = r.timed(steps, warmup, r.pa.STAGE_PREFILL, clocks=clocks)
+        _, kt, _ = r.timed(steps, warmup, r.pa.STAGE_PREFILL)
         roof = kernel_roofline(q, "tensor", kt, pk)
         roof["kernel"] = "prefill_kernel (tcgen05/TMEM, TMA)"
     else:
-        s, kt, launches = r.timed(steps, warmup, r.pa.STAGE_DECODE, clocks=clocks)
+        _, kt, _ = r.timed(steps, warmup, r.pa.STAGE_DECODE)
         roof = kernel_roofline(q, "hbm", kt, pk)
         roof["kernel"] = "decode_kernel (split-KV, TMA + mma.sync)"
     roof["ms_per_launch"] = round(kt * 1e3, 4)
-    return s, roof, launches
+    return sec, roof, per_step * steps
 
 
 def headline(q, sec):
