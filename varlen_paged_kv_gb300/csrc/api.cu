@@ -266,6 +266,7 @@ pa_status pa_paged_attention_stages(const void* query, const void* key, const vo
   a.forced_split = dims->decode_split_keys;
   a.route = dims->route;
   a.max_query_len = dims->max_query_len;
+  a.out_v8 = aligned(output, 32);
   const float sc = scale == 0.0f ? 1.0f / sqrtf((float)hs) : scale;
   a.scale_log2 = sc * 1.4426950408889634f;
   uint8_t* ws = static_cast<uint8_t*>(workspace);

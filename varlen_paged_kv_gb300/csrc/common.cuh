@@ -128,6 +128,7 @@ struct Args {
   int32_t route;
   int32_t max_query_len;  // > 0: host bound on every q_len (checked by the planner)
   int32_t dec_ctas;       // decode grid size
+  int32_t out_v8;         // output 32-byte aligned (prefill stores 32-byte chunks)
   float scale_log2;       // scale * log2(e)
   WsHeader* hdr;
   DecodeItem* items;
@@ -301,6 +302,13 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
+}
+
+// 32 bytes (8 words) to global memory in one store; dst 32-byte aligned
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
 }
 
 // one lane of the (fully active) warp, chosen by the hardware; the rest of the warp skips

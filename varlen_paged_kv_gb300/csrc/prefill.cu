@@ -485,25 +485,26 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           const bool store = tile.j0 + row < q_len;
           uint16_t* dst =
               reinterpret_cast<uint16_t*>(a.output) + ((int64_t)(c0 + tile.j0 + row) * a.nh + h) * HS + hsel * OCOLS;
-#pragma unroll 1
-          for (int cc = 0; cc < OCOLS; cc += 32) {
-            uint32_t ov[32];
-            tmem_ld_x32(o_tmem + cc, ov);
-            if (store) {
+          // this thread's half row of O in registers, then O is released to the next unit
+          uint32_t ov[OCOLS];
+          if constexpr (OCOLS == 64) tmem_ld_x64(o_tmem, ov);
+          else tmem_ld_x32(o_tmem, ov);
+          tc_fence_before();
+          mbar_arrive(&o_free[x]);
+          if (store) {
 #pragma unroll
-              for (int v = 0; v < 32; v += 8) {
-                uint4 pk;
-                pk.x = pack2<BF16>(__uint_as_float(ov[v + 0]) * inv, __uint_as_float(ov[v + 1]) * inv);
-                pk.y = pack2<BF16>(__uint_as_float(ov[v + 2]) * inv, __uint_as_float(ov[v + 3]) * inv);
-                pk.z = pack2<BF16>(__uint_as_float(ov[v + 4]) * inv, __uint_as_float(ov[v + 5]) * inv);
-                pk.w = pack2<BF16>(__uint_as_float(ov[v + 6]) * inv, __uint_as_float(ov[v + 7]) * inv);
-                *reinterpret_cast<uint4*>(dst + cc + v) = pk;
-              }
+            for (int v = 0; v < OCOLS / 2; ++v)  // packed in place (word v from words 2v, 2v + 1)
+              ov[v] = pack2<BF16>(__uint_as_float(ov[2 * v]) * inv, __uint_as_float(ov[2 * v + 1]) * inv);
+            if (a.out_v8) {  // 32-byte stores where the output allows them: half the store wavefronts
+#pragma unroll
+              for (int v = 0; v < OCOLS / 2; v += 8) st_global_v8(dst + 2 * v, &ov[v]);
+            } else {
+#pragma unroll
+              for (int v = 0; v < OCOLS / 2; v += 4)
+                *reinterpret_cast<uint4*>(dst + 2 * v) = make_uint4(ov[v], ov[v + 1], ov[v + 2], ov[v + 3]);
             }
           }
         }
-        tc_fence_before();
-        mbar_arrive(&o_free[x]);
         gs += n_kv;
       }
     }
