@@ -311,6 +311,13 @@ __device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
                : "memory");
 }
 
+// atomic add with acquire-release semantics at GPU scope; returns the old value
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // one lane of the (fully active) warp, chosen by the hardware; the rest of the warp skips
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred = 0;

@@ -366,11 +366,10 @@ __global__ void __launch_bounds__(160, 2)
         }
         consumer_bar();  // every consumer thread's partial is written
         if (t == 0) {
-          // one fence after the barrier publishes the CTA's partial (fence cumulativity), and
-          // one after the arrival orders the merge's reads of the other items' partials
-          __threadfence();
-          *s_last = atomicAdd(&a.unit_done[item.b * a.kvh + item.g], 1) == item.n_split - 1;
-          __threadfence();
+          // acq_rel at gpu scope after the barrier: the release publishes the CTA's partial
+          // (cumulative over the writes the barrier ordered before it), the acquire orders the
+          // merge's reads of the other items' partials after their arrivals
+          *s_last = atom_add_acq_rel_gpu(&a.unit_done[item.b * a.kvh + item.g], 1) == item.n_split - 1;
         }
         consumer_bar();
         if (*s_last && mine) {
