@@ -32,7 +32,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 1
+#define PA_ABI_VERSION 2
 
 typedef enum pa_status {
   PA_OK = 0,
@@ -184,6 +184,24 @@ pa_status pa_paged_attention_stages(const void* query, const void* key, const vo
                                     int32_t kv_num_heads, float scale, void* output,
                                     const pa_dims* dims, void* workspace, size_t workspace_bytes,
                                     void* stream, uint32_t stages);
+
+/*
+ * pa_paged_attention that also exports the log-sum-exp of every output row: lse is
+ * float32 (N, num_heads), row i head h = ln sum_t exp(scale * <q_ih, k_t>) over the keys
+ * the row attends, the natural-log, scale-included "attention-domain lse" that the
+ * (out, lse) merge of context-parallel partials consumes (WS2 CP-Aware Attention
+ * Contract, "Reduction Semantics"). lse must be 4-byte aligned and must not overlap any
+ * other argument; NULL behaves as pa_paged_attention. Computed in fp32 from the same
+ * running max and sum that normalise the output.
+ */
+pa_status pa_paged_attention_lse(const void* query, const void* key, const void* value,
+                                 void* key_cache, void* value_cache,
+                                 const int32_t* cumulative_sequence_length,
+                                 const int32_t* past_seqlens, const int32_t* block_table,
+                                 const int32_t* slot_mapping, int32_t num_heads,
+                                 int32_t kv_num_heads, float scale, void* output, float* lse,
+                                 const pa_dims* dims, void* workspace, size_t workspace_bytes,
+                                 void* stream);
 
 /* Static description of a status code. Never NULL. */
 const char* pa_status_string(pa_status status);

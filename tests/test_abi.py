@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.pa_abi_version() == 1
+    assert lib.pa_abi_version() == 2
     for code in range(5):
         assert lib.pa_status_string(code)
     assert lib.pa_status_string(99) == b"unknown status"
@@ -76,6 +76,20 @@ def test_typed_errors_before_any_launch(lib):
     assert _call(lib, good, output=0) == 1                                # null output
     assert _call(lib, good, ws_bytes=100) == 3                            # workspace too small
     assert _call(lib, pa.make_dims(0, 0, 128, 607, 256, 17, torch.float16)) == 0    # nothing to do
+
+
+def test_lse_entry_point_checks_before_any_launch(lib):
+    good = pa.make_dims(64, 64, 128, 607, 256, 17, torch.float16)
+    ws_bytes = lib.pa_workspace_size(ctypes.byref(good), 32, 8)
+    p = ctypes.c_void_p
+
+    def call(lse, dims=good):
+        return lib.pa_paged_attention_lse(p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE),
+                                          None, 32, 8, 0.0, p(FAKE), lse, ctypes.byref(dims), p(FAKE), ws_bytes,
+                                          None)
+    assert call(p(FAKE + 2)) == 1                                         # misaligned lse
+    assert call(p(FAKE), pa.make_dims(64, 64, 80, 607, 256, 17, torch.float16)) == 2   # head_size
+    assert call(p(FAKE), pa.make_dims(0, 0, 128, 607, 256, 17, torch.float16)) == 0   # nothing to do
 
 
 def test_python_binding_refuses_cpu_tensors(lib):

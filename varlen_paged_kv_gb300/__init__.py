@@ -62,6 +62,8 @@ def load_library():
     lib.pa_paged_attention.restype = ctypes.c_int
     lib.pa_paged_attention_stages.argtypes = common + [u32]
     lib.pa_paged_attention_stages.restype = ctypes.c_int
+    lib.pa_paged_attention_lse.argtypes = common[:13] + [p] + common[13:]
+    lib.pa_paged_attention_lse.restype = ctypes.c_int
     lib.pa_status_string.argtypes = [ctypes.c_int]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_last_error.argtypes = []
@@ -113,12 +115,15 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
                     num_heads: int, kv_num_heads: int, scale: float = 0.0,
                     output: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                     decode_split_keys: int = 0, route: int = ROUTE_AUTO, max_query_len: int = 0,
-                    stages: int = STAGE_ALL, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+                    stages: int = STAGE_ALL, stream: Optional[torch.cuda.Stream] = None,
+                    lse: Optional[torch.Tensor] = None) -> torch.Tensor:
     """com.microsoft.PagedAttention on CUDA tensors. Writes key_cache / value_cache in
     place and returns ``output`` (num_tokens, num_heads * head_size).
 
     ``max_query_len`` (optional) is a host-side bound on every sequence's new-token count;
-    it lets decode-only batches skip the prefill launch and is checked on the device."""
+    it lets decode-only batches skip the prefill launch and is checked on the device.
+    ``lse`` (optional, float32 (num_tokens, num_heads)) receives each output row's natural-log
+    log-sum-exp of the scaled scores (whole calls only)."""
     lib = load_library()
     if query.dtype not in _DTYPES:
         raise TypeError("query must be float16 or bfloat16")
@@ -129,8 +134,13 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
                     ("block_table", block_table), ("slot_mapping", slot_mapping)):
         if t is not None and t.dtype != torch.int32:
             raise TypeError(f"{name} must be int32")
+    if lse is not None:
+        if lse.dtype != torch.float32 or tuple(lse.shape) != (query.shape[0], num_heads):
+            raise ValueError("lse must be float32 (num_tokens, num_heads)")
+        if stages != STAGE_ALL:
+            raise ValueError("lse is exported by whole calls only")
     for t in (query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
-              slot_mapping, output, workspace):
+              slot_mapping, output, workspace, lse):
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError("all tensors must be contiguous CUDA tensors")
     N = query.shape[0]
@@ -151,11 +161,18 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
         ws = lib.pa_workspace_size(ctypes.byref(dims), num_heads, kv_num_heads)
         workspace = torch.empty(max(int(ws), 256), dtype=torch.uint8, device=query.device)
     s = (stream or torch.cuda.current_stream(query.device)).cuda_stream
-    st = lib.pa_paged_attention_stages(
-        _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
-        _ptr(cumulative_sequence_length), _ptr(past_seqlens), _ptr(block_table), _ptr(slot_mapping),
-        int(num_heads), int(kv_num_heads), float(scale), _ptr(output), ctypes.byref(dims),
-        _ptr(workspace), int(workspace.numel()), ctypes.c_void_p(s), int(stages))
+    if lse is not None:
+        st = lib.pa_paged_attention_lse(
+            _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
+            _ptr(cumulative_sequence_length), _ptr(past_seqlens), _ptr(block_table), _ptr(slot_mapping),
+            int(num_heads), int(kv_num_heads), float(scale), _ptr(output), _ptr(lse), ctypes.byref(dims),
+            _ptr(workspace), int(workspace.numel()), ctypes.c_void_p(s))
+    else:
+        st = lib.pa_paged_attention_stages(
+            _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
+            _ptr(cumulative_sequence_length), _ptr(past_seqlens), _ptr(block_table), _ptr(slot_mapping),
+            int(num_heads), int(kv_num_heads), float(scale), _ptr(output), ctypes.byref(dims),
+            _ptr(workspace), int(workspace.numel()), ctypes.c_void_p(s), int(stages))
     if st:
         raise PagedAttentionError(st, "pa_paged_attention")
     return output

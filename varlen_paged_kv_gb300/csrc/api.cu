@@ -212,12 +212,15 @@ size_t pa_workspace_size(const pa_dims* dims, int32_t num_heads, int32_t kv_num_
       .total;
 }
 
-pa_status pa_paged_attention_stages(const void* query, const void* key, const void* value, void* key_cache,
-                                    void* value_cache, const int32_t* cumulative_sequence_length,
-                                    const int32_t* past_seqlens, const int32_t* block_table,
-                                    const int32_t* slot_mapping, int32_t num_heads, int32_t kv_num_heads, float scale,
-                                    void* output, const pa_dims* dims, void* workspace, size_t workspace_bytes,
-                                    void* stream, uint32_t stages) {
+}  // extern "C"
+
+namespace {
+
+pa_status run(const void* query, const void* key, const void* value, void* key_cache, void* value_cache,
+              const int32_t* cumulative_sequence_length, const int32_t* past_seqlens, const int32_t* block_table,
+              const int32_t* slot_mapping, int32_t num_heads, int32_t kv_num_heads, float scale, void* output,
+              float* lse, const pa_dims* dims, void* workspace, size_t workspace_bytes, void* stream,
+              uint32_t stages) {
   pa_status st = check_dims(dims, num_heads, kv_num_heads);
   if (st != PA_OK) return st;
   if ((key == nullptr) != (value == nullptr)) return PA_ERR_INVALID_ARGUMENT;
@@ -228,7 +231,8 @@ pa_status pa_paged_attention_stages(const void* query, const void* key, const vo
       !output || !workspace)
     return PA_ERR_INVALID_ARGUMENT;
   if (!aligned(query, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) || !aligned(output, 16) ||
-      (key && (!aligned(key, 16) || !aligned(value, 16))) || !aligned(cumulative_sequence_length, 4) ||
+      (key && (!aligned(key, 16) || !aligned(value, 16))) || (lse && !aligned(lse, 4)) ||
+      !aligned(cumulative_sequence_length, 4) ||
       !aligned(past_seqlens, 4) || !aligned(block_table, 4) || (slot_mapping && !aligned(slot_mapping, 4)) ||
       !aligned(workspace, 256))
     return PA_ERR_INVALID_ARGUMENT;
@@ -249,6 +253,7 @@ pa_status pa_paged_attention_stages(const void* query, const void* key, const vo
   a.block_table = block_table;
   a.slot_mapping = slot_mapping;
   a.output = output;
+  a.lse = lse;
   a.N = N;
   a.B = B;
   a.nh = num_heads;
@@ -288,14 +293,40 @@ pa_status pa_paged_attention_stages(const void* query, const void* key, const vo
   return launch_all(a, dims, query, key_cache, value_cache, stages, static_cast<cudaStream_t>(stream));
 }
 
+}  // namespace
+
+extern "C" {
+
+pa_status pa_paged_attention_stages(const void* query, const void* key, const void* value, void* key_cache,
+                                    void* value_cache, const int32_t* cumulative_sequence_length,
+                                    const int32_t* past_seqlens, const int32_t* block_table,
+                                    const int32_t* slot_mapping, int32_t num_heads, int32_t kv_num_heads, float scale,
+                                    void* output, const pa_dims* dims, void* workspace, size_t workspace_bytes,
+                                    void* stream, uint32_t stages) {
+  return run(query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
+             slot_mapping, num_heads, kv_num_heads, scale, output, nullptr, dims, workspace, workspace_bytes, stream,
+             stages);
+}
+
 pa_status pa_paged_attention(const void* query, const void* key, const void* value, void* key_cache,
                              void* value_cache, const int32_t* cumulative_sequence_length,
                              const int32_t* past_seqlens, const int32_t* block_table, const int32_t* slot_mapping,
                              int32_t num_heads, int32_t kv_num_heads, float scale, void* output,
                              const pa_dims* dims, void* workspace, size_t workspace_bytes, void* stream) {
-  return pa_paged_attention_stages(query, key, value, key_cache, value_cache, cumulative_sequence_length,
-                                   past_seqlens, block_table, slot_mapping, num_heads, kv_num_heads, scale, output,
-                                   dims, workspace, workspace_bytes, stream, PA_STAGE_ALL);
+  return run(query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
+             slot_mapping, num_heads, kv_num_heads, scale, output, nullptr, dims, workspace, workspace_bytes, stream,
+             PA_STAGE_ALL);
+}
+
+pa_status pa_paged_attention_lse(const void* query, const void* key, const void* value, void* key_cache,
+                                 void* value_cache, const int32_t* cumulative_sequence_length,
+                                 const int32_t* past_seqlens, const int32_t* block_table,
+                                 const int32_t* slot_mapping, int32_t num_heads, int32_t kv_num_heads, float scale,
+                                 void* output, float* lse, const pa_dims* dims, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  return run(query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
+             slot_mapping, num_heads, kv_num_heads, scale, output, lse, dims, workspace, workspace_bytes, stream,
+             PA_STAGE_ALL);
 }
 
 const char* pa_last_error(void) { return g_last_error; }

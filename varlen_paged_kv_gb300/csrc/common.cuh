@@ -118,6 +118,7 @@ struct Args {
   const int32_t* block_table;
   const int32_t* slot_mapping;
   void* output;
+  float* lse;             // (N, nh) natural-log lse of each output row, or null
   int32_t N, B, nh, kvh, G, hs, num_blocks, bs, max_blocks;
   int32_t q_stride;       // elements per query row
   int32_t kv_row;         // kvh * hs

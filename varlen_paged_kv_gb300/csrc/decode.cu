@@ -342,6 +342,8 @@ __global__ void __launch_bounds__(160, 2)
       const float inv = Lr > 0.f ? 1.f / Lr : 0.f;
       const float* src = comb + row * kCombStride + col;
       if (item.n_split == 1) {
+        if (mine && a.lse && (t & 7) == 0)  // natural log; M is the base-2 max of s * scale
+          a.lse[(int64_t)tok * a.nh + head] = Lr > 0.f ? (M + fast_log2(Lr)) * 0.69314718055994531f : -INFINITY;
         if (mine) {
 #pragma unroll
           for (int v = 0; v < CW; v += 8) {
@@ -397,6 +399,7 @@ __global__ void __launch_bounds__(160, 2)
             }
           }
           const float dinv = 1.f / den;
+          if (a.lse && (t & 7) == 0) a.lse[(int64_t)tok * a.nh + head] = Mx + fast_log2(den) * 0.69314718055994531f;
 #pragma unroll
           for (int v = 0; v < CW; v += 8) {
             uint4 pk;

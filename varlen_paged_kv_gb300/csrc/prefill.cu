@@ -481,8 +481,11 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           float* xs = xsum + x * (kPreTileQ * 2) + row * 2;
           xs[hsel] = l;
           named_bar_sync(pair_bar, 64);
-          const float inv = 1.f / (xs[0] + xs[1]);
+          const float l_row = xs[0] + xs[1];
+          const float inv = 1.f / l_row;
           const bool store = tile.j0 + row < q_len;
+          if (a.lse && store && hsel == 0)  // natural log; m_used is the base-2 max of s * scale
+            a.lse[(int64_t)(c0 + tile.j0 + row) * a.nh + h] = (m_used + fast_log2(l_row)) * 0.69314718055994531f;
           uint16_t* dst =
               reinterpret_cast<uint16_t*>(a.output) + ((int64_t)(c0 + tile.j0 + row) * a.nh + h) * HS + hsel * OCOLS;
           // this thread's half row of O in registers, then O is released to the next unit
