@@ -105,7 +105,8 @@ size_t pa_workspace_size(const pa_dims* dims, int32_t num_heads, int32_t kv_num_
  *   past_seqlens int32 (B): cached history length of each sequence before this call.
  *   block_table  int32 (B, max_blocks_per_sequence): logical block -> physical block; it
  *                defines the read path. Entries past ceil((past+q_len)/block_size) are
- *                never read.
+ *                never read. Rows may share physical pages (a read-only shared prefix),
+ *                provided no row of this call writes into a shared page.
  *   slot_mapping int32 (N) or NULL: the slot of each row, -1 = do not write. When NULL the
  *                slot is derived: p = past_seqlens[b] + j for row j of sequence b,
  *                s = block_table[b][p / block_size]*block_size + p % block_size.

@@ -284,3 +284,33 @@ def test_nan_in_unread_cache_rows_does_not_leak(name):
     _poison_unread_cache_rows(p, 0x7FC0 if p.dtype == "bf16" else 0x7E00)
     check(p)
     check(p, route=pa.ROUTE_ALL_PREFILL)
+
+
+# ---- shared-prefix pages: several block_table rows point at the same physical pages ----
+
+def _share_prefix(p, seqs, n_pages):
+    """Makes sequences `seqs` read their first n_pages logical pages from seqs[0]'s physical
+    pages (a read-only shared prefix; every sequence's history must cover those pages, so
+    this call's writes land in pages of its own)."""
+    bt = p.block_table.copy()
+    for b in seqs:
+        assert int(p.past_seqlens[b]) >= n_pages * p.block_size
+        bt[b, :n_pages] = bt[seqs[0], :n_pages]
+    p.block_table = bt
+    return p
+
+
+@pytest.mark.parametrize("route", [pa.ROUTE_AUTO, pa.ROUTE_ALL_PREFILL])
+def test_shared_prefix_pages_decode(route):
+    p = w.make_problem(name="shared-decode", seed=31, dtype="fp16", num_heads=32, kv_num_heads=8, head_size=128,
+                       block_size=64, past=[600, 700, 640, 1000], q_lens=[1, 2, 1, 4])
+    check(_share_prefix(p, [0, 1, 2, 3], 9), route=route)
+    check(p, decode_split_keys=128)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_shared_prefix_pages_chunked_prefill(dtype):
+    # three chunks continuing one 512-token prompt prefix held once in the pool
+    p = w.make_problem(name="shared-prefill", seed=32, dtype=dtype, num_heads=16, kv_num_heads=4, head_size=128,
+                       block_size=256, past=[512, 512, 768], q_lens=[100, 200, 17])
+    check(_share_prefix(p, [0, 1, 2], 2))
