@@ -187,7 +187,7 @@ def test_max_query_len_hint_skips_prefill_and_is_checked():
                              d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], None,
                              num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, workspace=ws, max_query_len=4)
     assert pa.read_device_error(ws) == 0
-    assert pa.kernel_launch_count() - n0 == 3  # plan, cache write, decode
+    assert pa.kernel_launch_count() - n0 == 2  # plan, decode (which writes this call's rows)
     assert_close(bits_of(out).reshape(p.num_tokens, p.num_heads, p.head_size), ref["out"], p.dtype, "hint")
     # a bound below the real q_len is refused on the device, nothing written
     d = upload(p)
@@ -314,3 +314,49 @@ def test_shared_prefix_pages_chunked_prefill(dtype):
     p = w.make_problem(name="shared-prefill", seed=32, dtype=dtype, num_heads=16, kv_num_heads=4, head_size=128,
                        block_size=256, past=[512, 512, 768], q_lens=[100, 200, 17])
     check(_share_prefix(p, [0, 1, 2], 2))
+
+
+# ---- decode-only batches whose new rows the decode kernel writes itself ----
+
+def _run_hinted(p, split=0, ws=None):
+    d = upload(p)
+    ws = make_workspace(p, split) if ws is None else ws
+    out = pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
+                             d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], d["slot_mapping"],
+                             num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, scale=p.scale,
+                             decode_split_keys=split, workspace=ws, max_query_len=int(p.q_lens.max()))
+    return d, out, ws
+
+
+@pytest.mark.parametrize("split", [0, 64])
+@pytest.mark.parametrize("name", ["decode-single-split", "decode-q-up-to-4", "decode-gqa16", "gqa8-q2"])
+def test_decode_only_batch_rows_written_by_the_decode_kernel(name, split):
+    # max_query_len <= 4 proves the batch decode-only; with derived slots the item that
+    # reads each new row writes it, and no cache-write kernel runs
+    p = _case(name)
+    assert int(p.q_lens.max()) <= 4 and p.slot_mapping is None
+    ref = oracle.paged_attention(p)
+    d, out, ws = _run_hinted(p, split)
+    assert pa.read_device_error(ws) == 0
+    assert np.array_equal(bits_of(d["key_cache"]), ref["key_cache"]), "key cache differs"
+    assert np.array_equal(bits_of(d["value_cache"]), ref["value_cache"]), "value cache differs"
+    assert_close(bits_of(out).reshape(p.num_tokens, p.num_heads, p.head_size), ref["out"], p.dtype, name)
+
+
+def test_refused_batch_runs_no_stale_plan():
+    # a workspace left holding a valid plan must not let a refused batch write or compute
+    p = _case("decode-q-up-to-4")
+    _, _, ws = _run_hinted(p)
+    bad = _case("decode-q-up-to-4")
+    bad.cumulative_sequence_length = bad.cumulative_sequence_length.copy()
+    bad.cumulative_sequence_length[-1] -= 1
+    d = upload(bad)
+    before = bits_of(d["key_cache"]).copy(), bits_of(d["value_cache"]).copy()
+    out = torch.full((bad.num_tokens, bad.num_heads * bad.head_size), 7.0, dtype=d["query"].dtype, device="cuda")
+    pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
+                       d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], None,
+                       num_heads=bad.num_heads, kv_num_heads=bad.kv_num_heads, output=out, workspace=ws,
+                       max_query_len=int(bad.q_lens.max()))
+    assert pa.read_device_error(ws) & pa.DEVERR_BAD_BATCH
+    assert np.array_equal(bits_of(d["key_cache"]), before[0]) and np.array_equal(bits_of(d["value_cache"]), before[1])
+    assert torch.all(out == 7.0)
