@@ -187,7 +187,7 @@ def test_max_query_len_hint_skips_prefill_and_is_checked():
                              d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], None,
                              num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, workspace=ws, max_query_len=4)
     assert pa.read_device_error(ws) == 0
-    assert pa.kernel_launch_count() - n0 == 2  # plan, decode (which writes this call's rows)
+    assert pa.kernel_launch_count() - n0 == 3  # plan, cache write, decode
     assert_close(bits_of(out).reshape(p.num_tokens, p.num_heads, p.head_size), ref["out"], p.dtype, "hint")
     # a bound below the real q_len is refused on the device, nothing written
     d = upload(p)
@@ -316,7 +316,7 @@ def test_shared_prefix_pages_chunked_prefill(dtype):
     check(_share_prefix(p, [0, 1, 2], 2))
 
 
-# ---- decode-only batches whose new rows the decode kernel writes itself ----
+# ---- decode-only batches run with the max_query_len bound ----
 
 def _run_hinted(p, split=0, ws=None):
     d = upload(p)
@@ -330,9 +330,8 @@ def _run_hinted(p, split=0, ws=None):
 
 @pytest.mark.parametrize("split", [0, 64])
 @pytest.mark.parametrize("name", ["decode-single-split", "decode-q-up-to-4", "decode-gqa16", "gqa8-q2"])
-def test_decode_only_batch_rows_written_by_the_decode_kernel(name, split):
-    # max_query_len <= 4 proves the batch decode-only; with derived slots the item that
-    # reads each new row writes it, and no cache-write kernel runs
+def test_decode_only_batches_with_the_query_bound(name, split):
+    # max_query_len <= 4 proves these batches decode-only (no prefill launch)
     p = _case(name)
     assert int(p.q_lens.max()) <= 4 and p.slot_mapping is None
     ref = oracle.paged_attention(p)

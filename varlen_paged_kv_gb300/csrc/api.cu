@@ -150,12 +150,7 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
   }
   const bool can_decode = d->route == PA_ROUTE_AUTO;
   const bool can_prefill = prefill_possible(d, args.G);
-  // A decode-only batch (proven by the max_query_len bound) with derived slots and at most
-  // 4 new rows per sequence has its rows written by the decode kernel, by the item that
-  // reads them, when this call runs both stages.
-  args.decode_writes_new = can_decode && !can_prefill && args.slot_mapping == nullptr && d->max_query_len > 0 &&
-                           d->max_query_len <= 4 && (stages & PA_STAGE_CACHE_WRITE) && (stages & PA_STAGE_DECODE);
-  if ((stages & PA_STAGE_CACHE_WRITE) && args.N > 0 && !args.decode_writes_new) {
+  if ((stages & PA_STAGE_CACHE_WRITE) && args.N > 0) {
     const int64_t blocks = std::min<int64_t>(((int64_t)args.N + 7) / 8, (int64_t)info.sms * 8);  // a warp per token
     ++g_launches;
     if (cudaError_t e = pa::launch_cache_write(args, (int)blocks, stream)) return cuda_fail(e, "cache_write_kernel launch");

@@ -130,7 +130,6 @@ struct Args {
   int32_t max_query_len;  // > 0: host bound on every q_len (checked by the planner)
   int32_t dec_ctas;       // decode grid size
   int32_t out_v8;         // output 32-byte aligned (prefill stores 32-byte chunks)
-  int32_t decode_writes_new;  // decode kernel writes this call's K/V rows (no cache-write kernel)
   float scale_log2;       // scale * log2(e)
   WsHeader* hdr;
   DecodeItem* items;
@@ -379,10 +378,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // barrier `id` (1..15) among `count` threads (a multiple of 32)
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -74,49 +74,6 @@ __device__ __forceinline__ void load_q(const Args& a, const DecodeItem& item, in
   }
 }
 
-// This call's K and V rows among the keys [k0, k0 + 64) of an item, copied from the inputs
-// into the caches (head item.g only) by the producer warp before it loads the tile. Used
-// for decode-only batches with derived slots and at most 4 new rows per sequence: each new
-// key of head g is read only by the item whose range holds it, so the item that reads a
-// row writes it and the separate cache-write kernel is not launched. An out-of-range
-// block is skipped (the tile load reads it as zeros and flags it).
-template <int HS>
-__device__ __forceinline__ void write_new_rows(const Args& a, const DecodeItem& item, int k0, int lane) {
-  const int kv_len = item.past + item.q_len;
-  const int n0 = max(k0, max(item.key_begin, item.past));
-  const int n1 = min(k0 + kDecTile, min(item.key_end, kv_len));
-  if (n1 <= n0) return;
-  constexpr int CH = HS / 8;                 // 16-byte chunks of one head's row
-  const int total = (n1 - n0) * 2 * CH;      // K and V chunks; at most 4 rows, so <= 4 per lane
-  const int* bt = a.block_table + (int64_t)item.b * a.max_blocks;
-  uint4 v[4];
-  uint4* dst[4];
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int i = lane + 32 * r;
-    dst[r] = nullptr;
-    if (i < total) {
-      const int rr = i / (2 * CH), rem = i % (2 * CH), which = rem / CH, ch = rem % CH;
-      const int key = n0 + rr;
-      const int blk = bt[key / a.bs];
-      if (blk >= 0 && blk < a.num_blocks) {
-        const int64_t tok = item.c0 + (key - item.past);
-        const uint16_t* src = a.packed
-            ? reinterpret_cast<const uint16_t*>(a.query) + tok * a.q_stride + (which ? a.v_offset : a.k_offset)
-            : reinterpret_cast<const uint16_t*>(which ? a.value : a.key) + tok * a.kv_row;
-        v[r] = __ldg(reinterpret_cast<const uint4*>(src + item.g * HS) + ch);
-        dst[r] = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(which ? a.value_cache : a.key_cache) +
-                                          ((int64_t)blk * a.bs + key % a.bs) * a.kv_row + item.g * HS) + ch;
-      }
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < 4; ++r)
-    if (dst[r]) *dst[r] = v[r];
-  fence_proxy_async_global();  // the rows, seen by the tile's TMA load
-  __syncwarp();
-}
-
 template <int HS, bool BF16>
 __global__ void __launch_bounds__(160, 2)
     decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -169,14 +126,12 @@ __global__ void __launch_bounds__(160, 2)
       for (int k0 = item.key_begin; k0 < item.key_end; k0 += kDecTile, ++cnt) {
         const int s = cnt % kDecStages;
         const uint32_t ph = (cnt / kDecStages) & 1;
-        if (a.decode_writes_new) write_new_rows<HS>(a, item, k0, lane);
         if (lane == 0) {
           mbar_wait(&empty[s], ph ^ 1, abort, err);
           mbar_arrive_expect_tx(&full[s], L::kStageBytes);
         }
         __syncwarp();
         if (lane < nseg) {
-          if (a.decode_writes_new) fence_proxy_async_global();
           const int key = k0 + lane * seg_rows;
           int z = oob;
           if (key < kv_len) {
