@@ -359,3 +359,26 @@ def test_refused_batch_runs_no_stale_plan():
     assert pa.read_device_error(ws) & pa.DEVERR_BAD_BATCH
     assert np.array_equal(bits_of(d["key_cache"]), before[0]) and np.array_equal(bits_of(d["value_cache"]), before[1])
     assert torch.all(out == 7.0)
+
+
+# ---- batches larger than one planner round (1024 sequences) and than the tile sort ----
+
+def test_many_sequences_mixed_across_planner_rounds():
+    # 2600 sequences: decode rows with short histories plus prefill-class chunks spread over
+    # all three planner rounds (carries of the scans, item indices, the V-copy layout)
+    B = 2600
+    past = w.uniform_int(41, 1, B, 0, 200)
+    q = np.where(np.arange(B) % 97 == 5, 40, 1).astype(np.int64)
+    p = w.make_problem(name="many-mixed", seed=41, dtype="bf16", num_heads=8, kv_num_heads=2, head_size=64,
+                       block_size=16, past=past, q_lens=q)
+    check(p)
+
+
+def test_more_prefill_tiles_than_the_sort_holds():
+    # 4200 prefill-class sequences (q_len 5, 4 query heads per KV head: 20 rows) make 4200
+    # query tiles, past the planner's 4096-entry sort: the tiles run in list order
+    B = 4200
+    past = w.uniform_int(42, 1, B, 0, 40)
+    p = w.make_problem(name="many-tiles", seed=42, dtype="fp16", num_heads=8, kv_num_heads=2, head_size=64,
+                       block_size=16, past=past, q_lens=np.full(B, 5, np.int64))
+    check(p)
