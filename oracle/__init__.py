@@ -67,6 +67,11 @@ def _bind(path: str):
     lib.oracle_attention_rows.argtypes = ([ctypes.c_int] + [i32] * 9 + [p] * 6 + [f32, i32] +
                                           [p] * 4 + [ctypes.c_int])
     lib.oracle_attention_rows.restype = ctypes.c_int
+    lib.oracle_qk_prep.argtypes = ([ctypes.c_int] + [i32] * 5 + [ctypes.c_int64] + [p] * 6 + [dbl, i32, dbl] +
+                                   [p, p])
+    lib.oracle_qk_prep.restype = ctypes.c_int
+    lib.oracle_round_array.argtypes = [ctypes.c_int, p, ctypes.c_int64, p]
+    lib.oracle_round_array.restype = None
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -184,8 +189,63 @@ def attention_rows(p, key_cache, value_cache, tokens, heads, nthreads: int = 0):
     return out, lse
 
 
-def paged_attention(p, nthreads: int = 0):
-    """The whole operator: returns dict(key_cache, value_cache, out, lse, out_bits)."""
+# ---- Q/K preparation (RMSNorm, rotary embedding) before the cache write -------------
+# prep: dict(q_norm_weight=uint16 bits (hs,) or None, k_norm_weight=... or None, eps=float,
+#            rotary_dim=int (0: none), theta=float)
+
+def qk_prep_f64(p, prep):
+    """The prepared Q (N, nh, hs) and K (N, kvh, hs), unrounded (oracle_qk_prep)."""
+    lib = _load()
+    N, B, nh, kvh, hs = _dims(p)[:5]
+    q = _c(p.query, np.uint16)
+    k = _c(p.key, np.uint16)
+    oq = np.zeros((N, nh, hs), dtype=np.float64)
+    ok = np.zeros((N, kvh, hs), dtype=np.float64)
+    qw = _c(prep.get("q_norm_weight"), np.uint16)
+    kw = _c(prep.get("k_norm_weight"), np.uint16)
+    dt = 1 if p.dtype == "bf16" else 0
+    rc = lib.oracle_qk_prep(dt, N, B, nh, kvh, hs, int(q.shape[1]), _ptr(q), _ptr(k),
+                            _ptr(_c(p.cumulative_sequence_length, np.int32)), _ptr(_c(p.past_seqlens, np.int32)),
+                            _ptr(qw), _ptr(kw), float(prep.get("eps", 1e-6)), int(prep.get("rotary_dim", 0)),
+                            float(prep.get("theta", 10000.0)), _ptr(oq), _ptr(ok))
+    if rc:
+        raise OracleError(rc)
+    return oq, ok
+
+
+def round_bits(x, dtype: str) -> np.ndarray:
+    """fp64 values rounded once to fp16 / bf16 bits (round to nearest even)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.zeros(x.shape, dtype=np.uint16)
+    _load().oracle_round_array(1 if dtype == "bf16" else 0, _ptr(x), int(x.size), _ptr(out))
+    return out
+
+
+def apply_qk_prep(p, prep):
+    """A copy of the problem whose query and key rows are the prepared ones rounded to T
+    (V and everything else unchanged): the operator with preparation is the operator on it."""
+    import copy
+    N, B, nh, kvh, hs = _dims(p)[:5]
+    oq, ok = qk_prep_f64(p, prep)
+    qb = round_bits(oq, p.dtype).reshape(N, nh * hs)
+    kb = round_bits(ok, p.dtype).reshape(N, kvh * hs)
+    r = copy.copy(p)
+    if p.key is None:  # packed [Q | K | V] rows
+        rows = np.array(p.query, dtype=np.uint16, copy=True)
+        rows[:, :nh * hs] = qb
+        rows[:, nh * hs:(nh + kvh) * hs] = kb
+        r.query = rows
+    else:
+        r.query = qb
+        r.key = kb
+    return r
+
+
+def paged_attention(p, nthreads: int = 0, prep=None):
+    """The whole operator: returns dict(key_cache, value_cache, out, lse, out_bits). With
+    `prep`, the query and key rows are prepared (RMSNorm, rotary embedding) first."""
+    if prep is not None:
+        p = apply_qk_prep(p, prep)
     kc, vc = scatter(p)
     out, lse, bits = attention(p, kc, vc, nthreads)
     return {"key_cache": kc, "value_cache": vc, "out": out, "lse": lse, "out_bits": bits}

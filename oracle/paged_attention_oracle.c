@@ -327,3 +327,95 @@ int oracle_max_threads(void) {
   return 1;
 #endif
 }
+
+/* ---- Q/K preparation before the cache write ----------------------------------------
+ * Not part of the operator statement: the RMSNorm of each query and key head vector
+ * followed by the rotary position embedding, which the Qwen3.8 export issue ("Add Qwen3.8
+ * packed hybrid PagedAttention export for ORT GenAI Engine") applies before
+ * PagedAttention and which the README ("Description") lists among what the package does
+ * not do. For every row i (sequence b, j = i - cum[b], position p = past_b + j) and every
+ * head vector x of head_size values:
+ *   RMSNorm, when a weight w is given:  x_c <- x_c / sqrt(mean_c x_c^2 + eps) * w_c
+ *   rotary embedding, when rotary_dim d > 0, pairing component u with u + d/2
+ *   ("rotate half"): for u < d/2
+ *     a_u = fl32(fl32(p) * fl32(base^(-2u/d)))
+ *     (x_u, x_{u+d/2}) <- (x_u cos a_u - x_{u+d/2} sin a_u, x_{u+d/2} cos a_u + x_u sin a_u)
+ *   components from d on are unchanged.
+ * Everything is fp64 except the angle a_u: the fp32 product of the position and the
+ * fp32 frequency, the way fp32 frameworks form the rotary table (at positions near 1e5
+ * the exact angle differs from it by ~1e-2 rad, far more than the rounding of the
+ * result). The values are returned unrounded: out_q (N, nh, hs), out_k (N, kvh, hs).
+ */
+static void prep_vector(const double* x, double* y, int32_t hs, const double* w, double eps, int32_t d,
+                        const double* ca, const double* sa) {
+  double r = 1.0;
+  if (w) {
+    double ss = 0.0;
+    for (int32_t c = 0; c < hs; ++c) ss += x[c] * x[c];
+    r = 1.0 / sqrt(ss / hs + eps);
+  }
+  for (int32_t c = 0; c < hs; ++c) y[c] = w ? x[c] * r * w[c] : x[c];
+  for (int32_t u = 0; u < d / 2; ++u) {
+    const double a = y[u], b = y[u + d / 2];
+    y[u] = a * ca[u] - b * sa[u];
+    y[u + d / 2] = b * ca[u] + a * sa[u];
+  }
+}
+
+int oracle_qk_prep(int dtype, int32_t N, int32_t B, int32_t nh, int32_t kvh, int32_t hs, int64_t q_width,
+                   const uint16_t* query, const uint16_t* key, const int32_t* cum, const int32_t* past,
+                   const uint16_t* q_weight, const uint16_t* k_weight, double eps, int32_t rotary_dim, double base,
+                   double* out_q, double* out_k) {
+  if (N < 0 || B <= 0 || nh <= 0 || kvh <= 0 || hs <= 0 || rotary_dim < 0 || rotary_dim > hs || rotary_dim % 2)
+    return ORACLE_BAD_SHAPE;
+  if (cum[0] != 0 || cum[B] != N) return ORACLE_BAD_CUM;
+  double* tab = make_table(dtype);
+  double* wq = malloc(sizeof(double) * hs);
+  double* wk = malloc(sizeof(double) * hs);
+  if (!tab || !wq || !wk) { free(tab); free(wq); free(wk); return ORACLE_NO_MEMORY; }
+  for (int32_t c = 0; c < hs; ++c) {
+    if (q_weight) wq[c] = tab[q_weight[c]];
+    if (k_weight) wk[c] = tab[k_weight[c]];
+  }
+  int err = ORACLE_OK;
+  for (int32_t b = 0; b < B && !err; ++b) {
+    if (cum[b + 1] < cum[b]) err = ORACLE_BAD_CUM;
+  }
+  if (!err) {
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int32_t i = 0; i < N; ++i) {
+      int32_t lo = 0, hi = B - 1;  /* the last b with cum[b] <= i */
+      while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) / 2;
+        if (cum[mid] <= i) lo = mid; else hi = mid - 1;
+      }
+      const int64_t pos = (int64_t)past[lo] + (i - cum[lo]);
+      double ca[512], sa[512], x[1024];
+      for (int32_t u = 0; u < rotary_dim / 2; ++u) {
+        const float freq = (float)pow(base, -2.0 * u / rotary_dim);
+        const float ang = (float)pos * freq;
+        ca[u] = cos((double)ang);
+        sa[u] = sin((double)ang);
+      }
+      const uint16_t* qrow = query + (int64_t)i * q_width;
+      const uint16_t* krow = key ? key + (int64_t)i * kvh * hs : qrow + (int64_t)nh * hs;
+      for (int32_t h = 0; h < nh; ++h) {
+        for (int32_t c = 0; c < hs; ++c) x[c] = tab[qrow[(int64_t)h * hs + c]];
+        prep_vector(x, out_q + ((int64_t)i * nh + h) * hs, hs, q_weight ? wq : NULL, eps, rotary_dim, ca, sa);
+      }
+      for (int32_t g = 0; g < kvh; ++g) {
+        for (int32_t c = 0; c < hs; ++c) x[c] = tab[krow[(int64_t)g * hs + c]];
+        prep_vector(x, out_k + ((int64_t)i * kvh + g) * hs, hs, k_weight ? wk : NULL, eps, rotary_dim, ca, sa);
+      }
+    }
+  }
+  free(tab);
+  free(wq);
+  free(wk);
+  return err;
+}
+
+/* n values rounded once to fp16 (dtype 0) or bf16 (dtype 1), round to nearest even */
+void oracle_round_array(int dtype, const double* x, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = dtype ? oracle_double_to_bf16(x[i]) : oracle_double_to_f16(x[i]);
+}

@@ -11,6 +11,7 @@ import pytest
 
 import oracle
 import test_oracle_pins as pins
+import test_oracle_prep_pins as prep_pins
 
 MUTANTS = [
     ("GQA head mapping h % kvh instead of h / G", "h / G", "h % kvh"),
@@ -32,7 +33,18 @@ MUTANTS = [
      "int sign = (h >> 15) & 1, e = (h >> 6) & 0xFF, m = h & 0x3F;"),
     ("V read from the K cache", "const uint16_t* v = value_cache + (rows[t] * kvh + g) * hs;",
      "const uint16_t* v = key_cache + (rows[t] * kvh + g) * hs;"),
+    ("rotation sign flipped", "y[u] = a * ca[u] - b * sa[u];", "y[u] = a * ca[u] + b * sa[u];"),
+    ("rotation pairs neighbours", "const double a = y[u], b = y[u + d / 2];\n    y[u] = a * ca[u] - b * sa[u];\n    y[u + d / 2] = b * ca[u] + a * sa[u];",
+     "if (2 * u + 1 >= d) continue;\n    const double a = y[2 * u], b = y[2 * u + 1];\n    y[2 * u] = a * ca[u] - b * sa[u];\n    y[2 * u + 1] = b * ca[u] + a * sa[u];"),
+    ("rotary angle in fp64", "const float ang = (float)pos * freq;", "const double ang = (double)pos * pow(base, -2.0 * u / rotary_dim);"),
+    ("frequency exponent without the factor 2", "(float)pow(base, -2.0 * u / rotary_dim)", "(float)pow(base, -1.0 * u / rotary_dim)"),
+    ("RMSNorm without the square root", "r = 1.0 / sqrt(ss / hs + eps);", "r = 1.0 / (ss / hs + eps);"),
+    ("RMSNorm eps dropped", "r = 1.0 / sqrt(ss / hs + eps);", "r = 1.0 / sqrt(ss / hs);"),
+    ("position without past_seqlens", "const int64_t pos = (int64_t)past[lo] + (i - cum[lo]);",
+     "const int64_t pos = (int64_t)(i - cum[lo]);"),
 ]
+
+PREP_MUTANTS = MUTANTS[-7:]
 
 # a fast battery of pins (each raises on failure)
 BATTERY = [
@@ -48,6 +60,12 @@ BATTERY = [
     lambda: pins.test_minus_one_slots_leave_cache_untouched_and_reads_use_cache(),
     lambda: pins.test_packed_qkv_equals_separate(),
     lambda: pins.test_scale_zero_means_inverse_sqrt_head_size(),
+    lambda: prep_pins.test_position_zero_is_identity(),
+    lambda: prep_pins.test_rotation_keeps_every_pair_length(32),
+    lambda: prep_pins.test_scores_depend_on_the_position_difference_only(),
+    lambda: prep_pins.test_rms_norm_with_unit_and_general_weights(),
+    lambda: prep_pins.test_single_component_rotates_into_its_half_partner(1),
+    lambda: prep_pins.test_single_component_rotates_into_its_half_partner(7),
 ]
 
 
