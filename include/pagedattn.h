@@ -32,7 +32,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 2
+#define PA_ABI_VERSION 3
 
 typedef enum pa_status {
   PA_OK = 0,
@@ -75,7 +75,34 @@ typedef struct pa_dims {
                                       (num_heads / kv_num_heads) <= 16 no prefill kernel is launched. The
                                       plan stage checks it: a sequence above the bound is a
                                       PA_DEVERR_BAD_BATCH. */
+  int32_t qk_prep;                 /* non-zero: calls pass a pa_qk_prep, and the workspace also holds the
+                                      prepared query rows (num_tokens * num_heads * head_size values of T) */
 } pa_dims;
+
+/*
+ * Q/K preparation before the cache write (pa_paged_attention_ex): not part of the
+ * operator statement, but the step the Qwen3.8 export issue ("Add Qwen3.8 packed hybrid
+ * PagedAttention export for ORT GenAI Engine") runs right before PagedAttention and the
+ * README ("Description") lists as not done by its package. For row j of sequence b, at
+ * position p = past_seqlens[b] + j, every query head vector and every key head vector x
+ * (head_size values) becomes
+ *   RMSNorm (when its weight is given):  x_c <- x_c / sqrt(mean_c x_c^2 + norm_eps) * w_c
+ *   then the rotary embedding (when rotary_dim = d > 0), pairing component u with u + d/2:
+ *     a_u = fl32(fl32(p) * fl32(rope_theta^(-2u/d)))   (an fp32 rotary table)
+ *     (x_u, x_{u+d/2}) <- (x_u cos a_u - x_{u+d/2} sin a_u,  x_{u+d/2} cos a_u + x_u sin a_u)
+ *   components from d on unchanged; the result is rounded once to T.
+ * The prepared K is what the cache receives; attention reads the prepared Q; V is
+ * unchanged. Computed in fp32 (sincosf of the fp32 angle).
+ */
+typedef struct pa_qk_prep {
+  const void* q_norm_weight;  /* T (head_size) device array, or NULL: no RMSNorm of the query heads */
+  const void* k_norm_weight;  /* T (head_size) device array, or NULL: no RMSNorm of the key heads */
+  float norm_eps;             /* RMSNorm epsilon (> 0 when a weight is given) */
+  float rope_theta;           /* base of the rotary frequencies (> 0 when rotary_dim > 0) */
+  int32_t rotary_dim;         /* 0, or an even multiple of head_size / 16 up to head_size (8 .. 128 in steps
+                                 of 8 for head_size 128) */
+  int32_t reserved;           /* 0 */
+} pa_qk_prep;
 
 /*
  * Bytes of device workspace pa_paged_attention needs for these sizes (0 on invalid
@@ -203,6 +230,21 @@ pa_status pa_paged_attention_lse(const void* query, const void* key, const void*
                                  int32_t kv_num_heads, float scale, void* output, float* lse,
                                  const pa_dims* dims, void* workspace, size_t workspace_bytes,
                                  void* stream);
+
+/*
+ * pa_paged_attention with both extensions: lse (see pa_paged_attention_lse; may be NULL)
+ * and prep, the Q/K preparation above (may be NULL; when given, dims->qk_prep must be
+ * non-zero and the workspace sized with it, else PA_ERR_INVALID_ARGUMENT; an unsupported
+ * rotary_dim is PA_ERR_UNSUPPORTED). The norm weights must be 16-byte aligned.
+ */
+pa_status pa_paged_attention_ex(const void* query, const void* key, const void* value,
+                                void* key_cache, void* value_cache,
+                                const int32_t* cumulative_sequence_length,
+                                const int32_t* past_seqlens, const int32_t* block_table,
+                                const int32_t* slot_mapping, int32_t num_heads,
+                                int32_t kv_num_heads, float scale, void* output, float* lse,
+                                const pa_qk_prep* prep, const pa_dims* dims, void* workspace,
+                                size_t workspace_bytes, void* stream);
 
 /* Static description of a status code. Never NULL. */
 const char* pa_status_string(pa_status status);

@@ -42,7 +42,13 @@ class PagedAttentionError(RuntimeError):
 class PaDims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_tokens", "batch_size", "head_size", "num_blocks", "block_size",
-        "max_blocks_per_sequence", "dtype", "decode_split_keys", "route", "max_query_len")]
+        "max_blocks_per_sequence", "dtype", "decode_split_keys", "route", "max_query_len", "qk_prep")]
+
+
+class PaQkPrep(ctypes.Structure):
+    _fields_ = [("q_norm_weight", ctypes.c_void_p), ("k_norm_weight", ctypes.c_void_p),
+                ("norm_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("rotary_dim", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 def load_library():
@@ -64,6 +70,8 @@ def load_library():
     lib.pa_paged_attention_stages.restype = ctypes.c_int
     lib.pa_paged_attention_lse.argtypes = common[:13] + [p] + common[13:]
     lib.pa_paged_attention_lse.restype = ctypes.c_int
+    lib.pa_paged_attention_ex.argtypes = common[:13] + [p, ctypes.POINTER(PaQkPrep)] + common[13:]
+    lib.pa_paged_attention_ex.restype = ctypes.c_int
     lib.pa_status_string.argtypes = [ctypes.c_int]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_last_error.argtypes = []
@@ -79,10 +87,11 @@ def load_library():
 
 
 def make_dims(num_tokens, batch_size, head_size, num_blocks, block_size, max_blocks_per_sequence, dtype,
-              decode_split_keys=0, route=ROUTE_AUTO, max_query_len=0) -> PaDims:
+              decode_split_keys=0, route=ROUTE_AUTO, max_query_len=0, qk_prep=False) -> PaDims:
     code = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
     return PaDims(int(num_tokens), int(batch_size), int(head_size), int(num_blocks), int(block_size),
-                  int(max_blocks_per_sequence), code, int(decode_split_keys), int(route), int(max_query_len))
+                  int(max_blocks_per_sequence), code, int(decode_split_keys), int(route), int(max_query_len),
+                  int(bool(qk_prep)))
 
 
 def workspace_size(dims: PaDims, num_heads: int, kv_num_heads: int) -> int:
@@ -116,14 +125,18 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
                     output: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                     decode_split_keys: int = 0, route: int = ROUTE_AUTO, max_query_len: int = 0,
                     stages: int = STAGE_ALL, stream: Optional[torch.cuda.Stream] = None,
-                    lse: Optional[torch.Tensor] = None) -> torch.Tensor:
+                    lse: Optional[torch.Tensor] = None, qk_prep: Optional[dict] = None) -> torch.Tensor:
     """com.microsoft.PagedAttention on CUDA tensors. Writes key_cache / value_cache in
     place and returns ``output`` (num_tokens, num_heads * head_size).
 
     ``max_query_len`` (optional) is a host-side bound on every sequence's new-token count;
     it lets decode-only batches skip the prefill launch and is checked on the device.
     ``lse`` (optional, float32 (num_tokens, num_heads)) receives each output row's natural-log
-    log-sum-exp of the scaled scores (whole calls only)."""
+    log-sum-exp of the scaled scores (whole calls only).
+    ``qk_prep`` (optional, whole calls only): dict(q_norm_weight=tensor (head_size,) of the
+    query dtype or None, k_norm_weight=... or None, eps=float, rotary_dim=int, theta=float):
+    RMSNorm of the query and key heads, then the rotary embedding at each row's position,
+    before the cache write (pa_qk_prep)."""
     lib = load_library()
     if query.dtype not in _DTYPES:
         raise TypeError("query must be float16 or bfloat16")
@@ -139,6 +152,20 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
             raise ValueError("lse must be float32 (num_tokens, num_heads)")
         if stages != STAGE_ALL:
             raise ValueError("lse is exported by whole calls only")
+    prep = None
+    if qk_prep is not None:
+        if stages != STAGE_ALL:
+            raise ValueError("qk_prep applies to whole calls only")
+        for k in ("q_norm_weight", "k_norm_weight"):
+            t = qk_prep.get(k)
+            if t is not None and (t.dtype != query.dtype or t.numel() != key_cache.shape[3] or not t.is_cuda or
+                                  not t.is_contiguous()):
+                raise ValueError(f"{k} must be a contiguous CUDA tensor of head_size values of the query dtype")
+        def addr(t):
+            return None if t is None else t.data_ptr()
+        prep = PaQkPrep(addr(qk_prep.get("q_norm_weight")), addr(qk_prep.get("k_norm_weight")),
+                        float(qk_prep.get("eps", 1e-6)), float(qk_prep.get("theta", 10000.0)),
+                        int(qk_prep.get("rotary_dim", 0)), 0)
     for t in (query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
               slot_mapping, output, workspace, lse):
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
@@ -154,14 +181,20 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
     if cumulative_sequence_length.shape[0] != B + 1 or block_table.shape[0] != B:
         raise ValueError("cumulative_sequence_length must have batch_size + 1 entries, block_table batch_size rows")
     dims = make_dims(N, B, head_size, num_blocks, block_size, block_table.shape[1], query.dtype,
-                     decode_split_keys, route, max_query_len)
+                     decode_split_keys, route, max_query_len, qk_prep is not None)
     if output is None:
         output = torch.empty((N, num_heads * head_size), dtype=query.dtype, device=query.device)
     if workspace is None:
         ws = lib.pa_workspace_size(ctypes.byref(dims), num_heads, kv_num_heads)
         workspace = torch.empty(max(int(ws), 256), dtype=torch.uint8, device=query.device)
     s = (stream or torch.cuda.current_stream(query.device)).cuda_stream
-    if lse is not None:
+    if prep is not None:
+        st = lib.pa_paged_attention_ex(
+            _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
+            _ptr(cumulative_sequence_length), _ptr(past_seqlens), _ptr(block_table), _ptr(slot_mapping),
+            int(num_heads), int(kv_num_heads), float(scale), _ptr(output), _ptr(lse), ctypes.byref(prep),
+            ctypes.byref(dims), _ptr(workspace), int(workspace.numel()), ctypes.c_void_p(s))
+    elif lse is not None:
         st = lib.pa_paged_attention_lse(
             _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
             _ptr(cumulative_sequence_length), _ptr(past_seqlens), _ptr(block_table), _ptr(slot_mapping),
@@ -178,5 +211,5 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
     return output
 
 
-__all__ = ["paged_attention", "workspace_size", "make_dims", "read_device_error", "kernel_launch_count",
+__all__ = ["paged_attention", "workspace_size", "make_dims", "PaQkPrep", "read_device_error", "kernel_launch_count",
            "load_library", "PagedAttentionError", "PaDims", "LIBRARY_PATH"]

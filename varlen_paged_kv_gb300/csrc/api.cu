@@ -134,6 +134,11 @@ int64_t mirror_keys(const pa_dims* d, int32_t nh, int32_t kvh) {
   return std::min<int64_t>(4 * (int64_t)d->num_tokens, (int64_t)d->num_blocks * d->block_size);
 }
 
+// 16-bit values of the prepared query rows the workspace holds (dims->qk_prep)
+int64_t qprep_values(const pa_dims* d, int32_t nh) {
+  return d->qk_prep ? (int64_t)d->num_tokens * nh * d->head_size : 0;
+}
+
 pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* kc, void* vc, uint32_t stages,
                      cudaStream_t stream) {
   DeviceInfo info;
@@ -163,10 +168,17 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
       if (cudaError_t e = pa::launch_v_mirror(args, (int)vb, stream)) return cuda_fail(e, "v_mirror_kernel launch");
     }
   }
+  // attention reads the prepared query rows when the cache-write stage prepared them
+  pa::Args aq = args;
+  if (args.prep) {
+    aq.query = args.qprep;
+    aq.q_stride = args.nh * hs;
+    query = args.qprep;
+  }
   if ((stages & PA_STAGE_PREFILL) && can_prefill && args.N > 0 && slots > 0) {
     const int seg = gcd(d->block_size, pa::kPreTileK);
     CUtensorMap tq, tk, tv, tvm;
-    if (!query_map(&tq, query, dt, args.q_stride, args.N) || !cache_map(&tk, kc, dt, hs, args.kvh, slots, seg) ||
+    if (!query_map(&tq, query, dt, aq.q_stride, args.N) || !cache_map(&tk, kc, dt, hs, args.kvh, slots, seg) ||
         !cache_map(&tv, vc, dt, hs, args.kvh, slots, seg)) {
       g_last_error = "cuTensorMapEncodeTiled failed (prefill maps)";
       return PA_ERR_CUDA;
@@ -183,7 +195,7 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
     const int grid = (int)std::min<int64_t>((int64_t)args.max_tiles * (args.nh / heads_per_unit), info.sms);
     if (grid > 0) {
       ++g_launches;
-      if (cudaError_t e = pa::launch_prefill(args, bf16, tq, tk, tv, tvm, seg, grid, stream))
+      if (cudaError_t e = pa::launch_prefill(aq, bf16, tq, tk, tv, tvm, seg, grid, stream))
         return cuda_fail(e, "prefill_kernel launch");
     }
   }
@@ -195,7 +207,7 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
       return PA_ERR_CUDA;
     }
     ++g_launches;
-    if (cudaError_t e = pa::launch_decode(args, bf16, tk, tv, seg, stream)) return cuda_fail(e, "decode_kernel launch");
+    if (cudaError_t e = pa::launch_decode(aq, bf16, tk, tv, seg, stream)) return cuda_fail(e, "decode_kernel launch");
   }
   return PA_OK;
 }
@@ -208,7 +220,7 @@ size_t pa_workspace_size(const pa_dims* dims, int32_t num_heads, int32_t kv_num_
   if (check_dims(dims, num_heads, kv_num_heads) != PA_OK) return 0;
   return pa::ws_layout(dims->num_tokens, dims->batch_size, kv_num_heads, dims->head_size,
                        dims->max_blocks_per_sequence, dims->block_size, dims->decode_split_keys,
-                       mirror_keys(dims, num_heads, kv_num_heads))
+                       mirror_keys(dims, num_heads, kv_num_heads), qprep_values(dims, num_heads))
       .total;
 }
 
@@ -219,10 +231,20 @@ namespace {
 pa_status run(const void* query, const void* key, const void* value, void* key_cache, void* value_cache,
               const int32_t* cumulative_sequence_length, const int32_t* past_seqlens, const int32_t* block_table,
               const int32_t* slot_mapping, int32_t num_heads, int32_t kv_num_heads, float scale, void* output,
-              float* lse, const pa_dims* dims, void* workspace, size_t workspace_bytes, void* stream,
-              uint32_t stages) {
+              float* lse, const pa_qk_prep* prep, const pa_dims* dims, void* workspace, size_t workspace_bytes,
+              void* stream, uint32_t stages) {
   pa_status st = check_dims(dims, num_heads, kv_num_heads);
   if (st != PA_OK) return st;
+  if (prep) {
+    if (!dims->qk_prep || prep->reserved != 0) return PA_ERR_INVALID_ARGUMENT;
+    const int32_t d = prep->rotary_dim, step = dims->head_size / 16;
+    if (d < 0 || d > dims->head_size || d % step != 0 || d % 2 != 0) return PA_ERR_UNSUPPORTED;
+    if (d > 0 && !(prep->rope_theta > 0.f)) return PA_ERR_INVALID_ARGUMENT;
+    if ((prep->q_norm_weight || prep->k_norm_weight) && !(prep->norm_eps > 0.f)) return PA_ERR_INVALID_ARGUMENT;
+    if ((prep->q_norm_weight && !aligned(prep->q_norm_weight, 16)) ||
+        (prep->k_norm_weight && !aligned(prep->k_norm_weight, 16)))
+      return PA_ERR_INVALID_ARGUMENT;
+  }
   if ((key == nullptr) != (value == nullptr)) return PA_ERR_INVALID_ARGUMENT;
   if (stages & ~PA_STAGE_ALL) return PA_ERR_INVALID_ARGUMENT;
   const int32_t N = dims->num_tokens, B = dims->batch_size, hs = dims->head_size;
@@ -239,7 +261,7 @@ pa_status run(const void* query, const void* key, const void* value, void* key_c
   if (dims->max_blocks_per_sequence == 0 || dims->num_blocks == 0) return PA_ERR_INVALID_ARGUMENT;
   const int64_t mkeys = mirror_keys(dims, num_heads, kv_num_heads);
   const pa::WsLayout L = pa::ws_layout(N, B, kv_num_heads, hs, dims->max_blocks_per_sequence, dims->block_size,
-                                       dims->decode_split_keys, mkeys);
+                                       dims->decode_split_keys, mkeys, qprep_values(dims, num_heads));
   if (workspace_bytes < L.total) return PA_ERR_WORKSPACE_TOO_SMALL;
 
   pa::Args a{};
@@ -272,6 +294,7 @@ pa_status run(const void* query, const void* key, const void* value, void* key_c
   a.route = dims->route;
   a.max_query_len = dims->max_query_len;
   a.out_v8 = aligned(output, 32);
+  a.bf16 = dims->dtype == PA_BFLOAT16;
   const float sc = scale == 0.0f ? 1.0f / sqrtf((float)hs) : scale;
   a.scale_log2 = sc * 1.4426950408889634f;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -287,6 +310,17 @@ pa_status run(const void* query, const void* key, const void* value, void* key_c
   a.mirror = reinterpret_cast<uint16_t*>(ws + L.mirror);
   a.mirror_seq = reinterpret_cast<int2*>(ws + L.mirror_seq);
   a.mirror_keys = (int32_t)mkeys;
+  if (prep) {
+    a.prep = 1;
+    a.rotary_dim = prep->rotary_dim;
+    a.norm_eps = prep->norm_eps;
+    a.q_norm_w = static_cast<const uint16_t*>(prep->q_norm_weight);
+    a.k_norm_w = static_cast<const uint16_t*>(prep->k_norm_weight);
+    a.qprep = reinterpret_cast<uint16_t*>(ws + L.qprep);
+    // the fp32 rotary table fl32(theta^(-2u/d)), formed in double and rounded once
+    for (int u = 0; u < prep->rotary_dim / 2; ++u)
+      a.inv_freq[u] = (float)pow((double)prep->rope_theta, -2.0 * u / prep->rotary_dim);
+  }
   a.max_items = L.max_items;
   a.max_tiles = L.max_tiles;
 
@@ -304,8 +338,8 @@ pa_status pa_paged_attention_stages(const void* query, const void* key, const vo
                                     void* output, const pa_dims* dims, void* workspace, size_t workspace_bytes,
                                     void* stream, uint32_t stages) {
   return run(query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
-             slot_mapping, num_heads, kv_num_heads, scale, output, nullptr, dims, workspace, workspace_bytes, stream,
-             stages);
+             slot_mapping, num_heads, kv_num_heads, scale, output, nullptr, nullptr, dims, workspace, workspace_bytes,
+             stream, stages);
 }
 
 pa_status pa_paged_attention(const void* query, const void* key, const void* value, void* key_cache,
@@ -314,8 +348,8 @@ pa_status pa_paged_attention(const void* query, const void* key, const void* val
                              int32_t num_heads, int32_t kv_num_heads, float scale, void* output,
                              const pa_dims* dims, void* workspace, size_t workspace_bytes, void* stream) {
   return run(query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
-             slot_mapping, num_heads, kv_num_heads, scale, output, nullptr, dims, workspace, workspace_bytes, stream,
-             PA_STAGE_ALL);
+             slot_mapping, num_heads, kv_num_heads, scale, output, nullptr, nullptr, dims, workspace, workspace_bytes,
+             stream, PA_STAGE_ALL);
 }
 
 pa_status pa_paged_attention_lse(const void* query, const void* key, const void* value, void* key_cache,
@@ -325,7 +359,18 @@ pa_status pa_paged_attention_lse(const void* query, const void* key, const void*
                                  void* output, float* lse, const pa_dims* dims, void* workspace,
                                  size_t workspace_bytes, void* stream) {
   return run(query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
-             slot_mapping, num_heads, kv_num_heads, scale, output, lse, dims, workspace, workspace_bytes, stream,
+             slot_mapping, num_heads, kv_num_heads, scale, output, lse, nullptr, dims, workspace, workspace_bytes,
+             stream, PA_STAGE_ALL);
+}
+
+pa_status pa_paged_attention_ex(const void* query, const void* key, const void* value, void* key_cache,
+                                void* value_cache, const int32_t* cumulative_sequence_length,
+                                const int32_t* past_seqlens, const int32_t* block_table, const int32_t* slot_mapping,
+                                int32_t num_heads, int32_t kv_num_heads, float scale, void* output, float* lse,
+                                const pa_qk_prep* prep, const pa_dims* dims, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  return run(query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
+             slot_mapping, num_heads, kv_num_heads, scale, output, lse, prep, dims, workspace, workspace_bytes, stream,
              PA_STAGE_ALL);
 }
 

@@ -66,7 +66,7 @@ struct __align__(32) PrefillTile {
 
 struct WsLayout {
   size_t header, items, cta_begin, unit_done, tiles, tiles_unsorted, part_o, part_lse, mirror_base, mirror_seq,
-      mirror, total;
+      mirror, qprep, total;
   int32_t max_items, max_tiles;
 };
 
@@ -78,10 +78,11 @@ __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + 
 //    into at most kMaxDecCtas contiguous ranges, so items <= kMaxDecCtas + units;
 //  - decode items, forced split length S: at most ceil(max_kv / S) per unit;
 //  - prefill tiles: sum_b ceil(q_b / 128) <= N / 128 + B.
-// mirror_keys: rows of the fp16 copy of V that bf16 prefill reads (0: none).
+// mirror_keys: rows of the fp16 copy of V that bf16 prefill reads (0: none); qprep_values:
+// 16-bit values of the prepared query rows (0: no Q/K preparation).
 __host__ __device__ inline WsLayout ws_layout(int32_t N, int32_t B, int32_t kvh, int32_t hs,
                                                int32_t max_blocks, int32_t bs, int32_t forced_split,
-                                               int64_t mirror_keys) {
+                                               int64_t mirror_keys, int64_t qprep_values) {
   WsLayout L;
   const int64_t units = (int64_t)B * kvh;
   int64_t items;
@@ -102,6 +103,7 @@ __host__ __device__ inline WsLayout ws_layout(int32_t N, int32_t B, int32_t kvh,
   L.mirror_base = off; off = align_up(off + sizeof(int32_t) * ((size_t)B + 1), 256);
   L.mirror_seq = off; off = align_up(off + 2 * sizeof(int32_t) * ((size_t)B + 1), 256);
   L.mirror = off; off = align_up(off + (size_t)mirror_keys * kvh * hs * 2, 256);
+  L.qprep = off; off = align_up(off + (size_t)qprep_values * 2, 256);
   L.total = off;
   return L;
 }
@@ -119,6 +121,16 @@ struct Args {
   const int32_t* slot_mapping;
   void* output;
   float* lse;             // (N, nh) natural-log lse of each output row, or null
+  // Q/K preparation in the cache-write stage (prep != 0): RMSNorm weights (or null), the
+  // rotary dimension, its fp32 frequency table, and the prepared query rows (N, nh, hs)
+  int32_t prep;
+  int32_t bf16;           // T is bf16 (else fp16)
+  int32_t rotary_dim;
+  float norm_eps;
+  const uint16_t* q_norm_w;
+  const uint16_t* k_norm_w;
+  uint16_t* qprep;
+  float inv_freq[64];
   int32_t N, B, nh, kvh, G, hs, num_blocks, bs, max_blocks;
   int32_t q_stride;       // elements per query row
   int32_t kv_row;         // kvh * hs

@@ -397,7 +397,121 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
 // One warp per token: the slot is found once (slot_mapping[i], or the token's logical
 // position past_seqlens[b] + j through block_table), then the lanes copy the token's K and
 // V rows with 16-byte loads and stores, all loads of a row issued before its stores. -1
-// skips the token; out-of-range slots and blocks are skipped and flagged.
+// skips the token; out-of-range slots and blocks are skipped and flagged. With the Q/K
+// preparation the warp also prepares the token's query heads (into the workspace) and
+// key heads (into the cache) on the way.
+
+// RMSNorm and rotary embedding of one head vector spread over the warp, lane l holding
+// components [E l, E l + E): x_c <- x_c / sqrt(mean x^2 + eps) * w_c (when w), then the
+// pair (u, u + d/2) rotated by the angle whose cos / sin this lane holds (rot lanes).
+template <int HS>
+__device__ __forceinline__ void prep_vector(float (&x)[HS / 32], bool norm, const float (&w)[HS / 32], float eps,
+                                            bool rot, bool first, int partner, const float (&cs)[HS / 32],
+                                            const float (&sn)[HS / 32]) {
+  constexpr int E = HS / 32;
+  if (norm) {
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float r = 1.f / sqrtf(ss / HS + eps);
+#pragma unroll
+    for (int e = 0; e < E; ++e) x[e] = x[e] * r * w[e];
+  }
+  float px[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) px[e] = __shfl_sync(0xffffffffu, x[e], partner);
+  if (rot) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) x[e] = first ? x[e] * cs[e] - px[e] * sn[e] : x[e] * cs[e] + px[e] * sn[e];
+  }
+}
+
+template <int HS>
+__device__ __forceinline__ void load_vec(const uint16_t* src, bool bf16, float (&x)[HS / 32]) {
+  constexpr int E = HS / 32;
+  uint32_t wds[E / 2];
+  if constexpr (E == 4) {
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(src));
+    wds[0] = v.x;
+    wds[1] = v.y;
+  } else {
+    wds[0] = __ldg(reinterpret_cast<const uint32_t*>(src));
+  }
+#pragma unroll
+  for (int k = 0; k < E / 2; ++k) {
+    if (bf16) {
+      x[2 * k] = __uint_as_float(wds[k] << 16);
+      x[2 * k + 1] = __uint_as_float(wds[k] & 0xFFFF0000u);
+    } else {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wds[k]));
+      x[2 * k] = f.x;
+      x[2 * k + 1] = f.y;
+    }
+  }
+}
+
+template <int HS>
+__device__ __forceinline__ void store_vec(uint16_t* dst, bool bf16, const float (&x)[HS / 32]) {
+  constexpr int E = HS / 32;
+  uint32_t wds[E / 2];
+#pragma unroll
+  for (int k = 0; k < E / 2; ++k) wds[k] = bf16 ? pack2<true>(x[2 * k], x[2 * k + 1]) : pack2<false>(x[2 * k], x[2 * k + 1]);
+  if constexpr (E == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(wds[0], wds[1]);
+  else *reinterpret_cast<uint32_t*>(dst) = wds[0];
+}
+
+// the prepared query heads of token tok into the workspace, and, when slot >= 0, its
+// prepared key heads and its V row into the caches
+template <int HS>
+__device__ void prep_token(const Args& a, int tok, int64_t pos, int64_t slot, int lane) {
+  constexpr int E = HS / 32;
+  const bool bf16 = a.bf16 != 0;
+  const int d = a.rotary_dim, half = d / 2;
+  const bool rot = d > 0 && lane * E < d;
+  const bool first = lane * E < half;
+  const int partner = rot ? (first ? lane + half / E : lane - half / E) : lane;
+  float cs[E], sn[E], wq[E], wk[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    cs[e] = 1.f;
+    sn[e] = 0.f;
+    if (rot) {
+      const int u = first ? lane * E + e : lane * E + e - half;
+      sincosf(__fmul_rn((float)pos, a.inv_freq[u]), &sn[e], &cs[e]);  // the fp32 rotary angle
+    }
+    wq[e] = a.q_norm_w ? (bf16 ? __uint_as_float((uint32_t)a.q_norm_w[lane * E + e] << 16)
+                               : __half2float(*reinterpret_cast<const __half*>(a.q_norm_w + lane * E + e)))
+                       : 1.f;
+    wk[e] = a.k_norm_w ? (bf16 ? __uint_as_float((uint32_t)a.k_norm_w[lane * E + e] << 16)
+                               : __half2float(*reinterpret_cast<const __half*>(a.k_norm_w + lane * E + e)))
+                       : 1.f;
+  }
+  const uint16_t* qrow = reinterpret_cast<const uint16_t*>(a.query) + (int64_t)tok * a.q_stride;
+  for (int h = 0; h < a.nh; ++h) {
+    float x[E];
+    load_vec<HS>(qrow + h * HS + lane * E, bf16, x);
+    prep_vector<HS>(x, a.q_norm_w != nullptr, wq, a.norm_eps, rot, first, partner, cs, sn);
+    store_vec<HS>(a.qprep + ((int64_t)tok * a.nh + h) * HS + lane * E, bf16, x);
+  }
+  if (slot < 0) return;
+  const uint16_t* krow = a.packed ? qrow + a.k_offset
+                                  : reinterpret_cast<const uint16_t*>(a.key) + (int64_t)tok * a.kv_row;
+  const uint16_t* vrow = a.packed ? qrow + a.v_offset
+                                  : reinterpret_cast<const uint16_t*>(a.value) + (int64_t)tok * a.kv_row;
+  uint16_t* kdst = reinterpret_cast<uint16_t*>(a.key_cache) + slot * a.kv_row;
+  uint16_t* vdst = reinterpret_cast<uint16_t*>(a.value_cache) + slot * a.kv_row;
+  for (int g = 0; g < a.kvh; ++g) {
+    float x[E];
+    load_vec<HS>(krow + g * HS + lane * E, bf16, x);
+    prep_vector<HS>(x, a.k_norm_w != nullptr, wk, a.norm_eps, rot, first, partner, cs, sn);
+    store_vec<HS>(kdst + g * HS + lane * E, bf16, x);
+  }
+  for (int c = lane; c < a.kv_row / 8; c += 32)
+    reinterpret_cast<uint4*>(vdst)[c] = __ldg(reinterpret_cast<const uint4*>(vrow) + c);
+}
+
 __global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
   pdl_wait();
   pdl_launch_dependents();
@@ -408,29 +522,38 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
   const int warps = (int)((gridDim.x * blockDim.x) >> 5);
   int b = 0;  // sequence of the previous token (tokens only grow within a warp)
   for (int tok = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); tok < a.N; tok += warps) {
-    int64_t slot;
-    if (a.slot_mapping) {
-      slot = a.slot_mapping[tok];
-    } else {
+    int64_t pos = 0;
+    if (!a.slot_mapping || a.prep) {
       int lo = b, hi = a.B - 1;  // last b with cum[b] <= tok
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (a.cum[mid] <= tok) lo = mid; else hi = mid - 1;
       }
       b = lo;
-      const int p = a.past[b] + (tok - a.cum[b]);
-      const int blk = a.block_table[(int64_t)b * a.max_blocks + p / a.bs];
+      pos = (int64_t)a.past[b] + (tok - a.cum[b]);
+    }
+    int64_t slot;
+    if (a.slot_mapping) {
+      slot = a.slot_mapping[tok];
+    } else {
+      const int blk = a.block_table[(int64_t)b * a.max_blocks + pos / a.bs];
       if (blk < 0 || blk >= a.num_blocks) {
         if (lane == 0) atomicOr(&a.hdr->error, PA_DEVERR_BAD_BLOCK);
-        continue;
+        slot = -1;
+      } else {
+        slot = (int64_t)blk * a.bs + pos % a.bs;
       }
-      slot = (int64_t)blk * a.bs + p % a.bs;
     }
-    if (slot == -1) continue;
-    if (slot < 0 || slot >= nslots) {
+    if (slot != -1 && (slot < 0 || slot >= nslots)) {
       if (lane == 0) atomicOr(&a.hdr->error, PA_DEVERR_BAD_SLOT);
+      slot = -1;
+    }
+    if (a.prep) {  // (the query rows are prepared even where the K/V write is skipped)
+      if (a.hs == 128) prep_token<128>(a, tok, pos, slot, lane);
+      else prep_token<64>(a, tok, pos, slot, lane);
       continue;
     }
+    if (slot == -1) continue;
     const uint16_t *src_k, *src_v;
     if (a.packed) {
       src_k = reinterpret_cast<const uint16_t*>(a.query) + (int64_t)tok * a.q_stride + a.k_offset;
