@@ -72,6 +72,8 @@ def _bind(path: str):
     lib.oracle_qk_prep.restype = ctypes.c_int
     lib.oracle_round_array.argtypes = [ctypes.c_int, p, ctypes.c_int64, p]
     lib.oracle_round_array.restype = None
+    lib.oracle_apply_gate.argtypes = [ctypes.c_int, ctypes.c_int64, p, p, p, p]
+    lib.oracle_apply_gate.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -241,11 +243,29 @@ def apply_qk_prep(p, prep):
     return r
 
 
-def paged_attention(p, nthreads: int = 0, prep=None):
+def apply_gate(out, gate_bits, dtype: str):
+    """out (fp64, any shape) times sigmoid(gate) elementwise (oracle_apply_gate): returns
+    (gated fp64, gated bits rounded to T)."""
+    out = np.ascontiguousarray(out, dtype=np.float64)
+    g = np.ascontiguousarray(gate_bits, dtype=np.uint16).reshape(out.shape)
+    gated = np.zeros(out.shape, dtype=np.float64)
+    bits = np.zeros(out.shape, dtype=np.uint16)
+    rc = _load().oracle_apply_gate(1 if dtype == "bf16" else 0, int(out.size), _ptr(out), _ptr(g), _ptr(gated),
+                                   _ptr(bits))
+    if rc:
+        raise OracleError(rc)
+    return gated, bits
+
+
+def paged_attention(p, nthreads: int = 0, prep=None, gate=None):
     """The whole operator: returns dict(key_cache, value_cache, out, lse, out_bits). With
-    `prep`, the query and key rows are prepared (RMSNorm, rotary embedding) first."""
+    `prep`, the query and key rows are prepared (RMSNorm, rotary embedding) first; with
+    `gate` (bits, (N, nh*hs)), the output is multiplied by sigmoid(gate) before rounding."""
     if prep is not None:
         p = apply_qk_prep(p, prep)
     kc, vc = scatter(p)
     out, lse, bits = attention(p, kc, vc, nthreads)
+    if gate is not None:
+        out, b = apply_gate(out, gate, p.dtype)
+        bits = b.reshape(bits.shape)
     return {"key_cache": kc, "value_cache": vc, "out": out, "lse": lse, "out_bits": bits}

@@ -419,3 +419,20 @@ int oracle_qk_prep(int dtype, int32_t N, int32_t B, int32_t nh, int32_t kvh, int
 void oracle_round_array(int dtype, const double* x, int64_t n, uint16_t* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = dtype ? oracle_double_to_bf16(x[i]) : oracle_double_to_f16(x[i]);
 }
+
+/* ---- output gate --------------------------------------------------------------------------
+ * Not part of the operator statement: Qwen3.5's full-attention layers multiply the
+ * attention output elementwise by a sigmoid gate ("Add Qwen3.8 packed hybrid PagedAttention
+ * export for ORT GenAI Engine": the layer's output is gated by a sigmoid). For every output
+ * element, gated = out / (1 + exp(-gate)) in fp64, then rounded once to T. n values. */
+int oracle_apply_gate(int dtype, int64_t n, const double* out, const uint16_t* gate, double* gated,
+                      uint16_t* bits) {
+  double* tab = make_table(dtype);
+  if (!tab) return ORACLE_NO_MEMORY;
+  for (int64_t i = 0; i < n; ++i) {
+    gated[i] = out[i] / (1.0 + exp(-tab[gate[i]]));
+    bits[i] = dtype ? oracle_double_to_bf16(gated[i]) : oracle_double_to_f16(gated[i]);
+  }
+  free(tab);
+  return ORACLE_OK;
+}

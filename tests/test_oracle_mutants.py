@@ -42,9 +42,9 @@ MUTANTS = [
     ("RMSNorm eps dropped", "r = 1.0 / sqrt(ss / hs + eps);", "r = 1.0 / sqrt(ss / hs);"),
     ("position without past_seqlens", "const int64_t pos = (int64_t)past[lo] + (i - cum[lo]);",
      "const int64_t pos = (int64_t)(i - cum[lo]);"),
+    ("gate sign flipped", "gated[i] = out[i] / (1.0 + exp(-tab[gate[i]]));", "gated[i] = out[i] / (1.0 + exp(tab[gate[i]]));"),
+    ("gate without the one", "gated[i] = out[i] / (1.0 + exp(-tab[gate[i]]));", "gated[i] = out[i] / exp(-tab[gate[i]]);"),
 ]
-
-PREP_MUTANTS = MUTANTS[-7:]
 
 # a fast battery of pins (each raises on failure)
 BATTERY = [
@@ -66,6 +66,8 @@ BATTERY = [
     lambda: prep_pins.test_rms_norm_with_unit_and_general_weights(),
     lambda: prep_pins.test_single_component_rotates_into_its_half_partner(1),
     lambda: prep_pins.test_single_component_rotates_into_its_half_partner(7),
+    lambda: prep_pins.test_gate_closed_forms("fp16"),
+    lambda: prep_pins.test_gate_symmetry(),
 ]
 
 

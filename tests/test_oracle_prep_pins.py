@@ -125,3 +125,36 @@ def test_operator_with_preparation_is_the_operator_on_prepared_rows():
     a = oracle.paged_attention(p, prep=prep)
     b = oracle.paged_attention(oracle.apply_qk_prep(p, prep))
     assert np.array_equal(a["out_bits"], b["out_bits"]) and np.array_equal(a["key_cache"], b["key_cache"])
+
+
+# ---- the output gate: out * sigmoid(gate) ----
+
+def _gated(dtype, gate_value):
+    p = _problem(dtype=dtype)
+    base = oracle.paged_attention(p)
+    N, nh, hs = p.num_tokens, p.num_heads, p.head_size
+    g = np.full((N, nh * hs), gate_value)
+    gb = oracle.double_to_bf16(g) if dtype == "bf16" else oracle.double_to_f16(g)
+    return base, oracle.paged_attention(p, gate=gb.reshape(N, nh * hs))
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_gate_closed_forms(dtype):
+    base, open_ = _gated(dtype, 40.0)        # sigmoid(40) = 1 - 4e-18: the ungated output
+    assert np.array_equal(open_["out_bits"], base["out_bits"])
+    base, half = _gated(dtype, 0.0)          # sigmoid(0) = 1/2 exactly
+    assert np.array_equal(half["out"], base["out"] / 2)
+    assert np.array_equal(half["lse"], base["lse"])  # the gate does not touch lse
+    _, shut = _gated(dtype, -60.0)           # sigmoid(-60) ~ 9e-27: zero in T
+    assert np.all(np.abs(shut["out"]) < 1e-20)
+
+
+def test_gate_symmetry():
+    # sigmoid(g) + sigmoid(-g) = 1: the two gated outputs add up to the ungated one
+    p = _problem(dtype="fp16")
+    N, nh, hs = p.num_tokens, p.num_heads, p.head_size
+    g = np.linspace(-6, 6, N * nh * hs).reshape(N, nh * hs)
+    plus = oracle.paged_attention(p, gate=oracle.double_to_f16(g).reshape(N, -1))
+    minus = oracle.paged_attention(p, gate=oracle.double_to_f16(-g).reshape(N, -1))
+    base = oracle.paged_attention(p)
+    assert np.allclose(plus["out"] + minus["out"], base["out"], rtol=1e-12, atol=1e-15)
