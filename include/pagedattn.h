@@ -32,7 +32,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 3
+#define PA_ABI_VERSION 4
 
 typedef enum pa_status {
   PA_OK = 0,
@@ -80,7 +80,7 @@ typedef struct pa_dims {
 } pa_dims;
 
 /*
- * Q/K preparation before the cache write (pa_paged_attention_ex): not part of the
+ * Q/K preparation before the cache write (pa_extensions.qk_prep): not part of the
  * operator statement, but the step the Qwen3.8 export issue ("Add Qwen3.8 packed hybrid
  * PagedAttention export for ORT GenAI Engine") runs right before PagedAttention and the
  * README ("Description") lists as not done by its package. For row j of sequence b, at
@@ -231,19 +231,27 @@ pa_status pa_paged_attention_lse(const void* query, const void* key, const void*
                                  const pa_dims* dims, void* workspace, size_t workspace_bytes,
                                  void* stream);
 
-/*
- * pa_paged_attention with both extensions: lse (see pa_paged_attention_lse; may be NULL)
- * and prep, the Q/K preparation above (may be NULL; when given, dims->qk_prep must be
- * non-zero and the workspace sized with it, else PA_ERR_INVALID_ARGUMENT; an unsupported
- * rotary_dim is PA_ERR_UNSUPPORTED). The norm weights must be 16-byte aligned.
- */
+/* Optional extensions of one call (pa_paged_attention_ex); every member may be NULL. */
+typedef struct pa_extensions {
+  float* lse;                 /* fp32 (N, num_heads): each output row's log-sum-exp, as pa_paged_attention_lse */
+  const pa_qk_prep* qk_prep;  /* the Q/K preparation above; dims->qk_prep must then be non-zero and the
+                                 workspace sized with it, else PA_ERR_INVALID_ARGUMENT; an unsupported
+                                 rotary_dim is PA_ERR_UNSUPPORTED; norm weights 16-byte aligned */
+  const void* output_gate;    /* T (N, num_heads*head_size), 16-byte aligned: every output element is
+                                 multiplied by sigmoid of the matching gate element before the final
+                                 rounding (the sigmoid-gated output of Qwen3.5's full-attention layers,
+                                 "Add Qwen3.8 packed hybrid PagedAttention export for ORT GenAI Engine");
+                                 lse is not gated */
+} pa_extensions;
+
+/* pa_paged_attention with the extensions in `ext` (NULL: none). */
 pa_status pa_paged_attention_ex(const void* query, const void* key, const void* value,
                                 void* key_cache, void* value_cache,
                                 const int32_t* cumulative_sequence_length,
                                 const int32_t* past_seqlens, const int32_t* block_table,
                                 const int32_t* slot_mapping, int32_t num_heads,
-                                int32_t kv_num_heads, float scale, void* output, float* lse,
-                                const pa_qk_prep* prep, const pa_dims* dims, void* workspace,
+                                int32_t kv_num_heads, float scale, void* output,
+                                const pa_extensions* ext, const pa_dims* dims, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
 /* Static description of a status code. Never NULL. */

@@ -109,3 +109,44 @@ def test_long_context_positions():
     p = w.make_problem(name="prep-long", seed=55, dtype="bf16", num_heads=8, kv_num_heads=2, head_size=128,
                        block_size=16, past=[131000, 90000], q_lens=[1, 1])
     check(p, dict(q_norm_weight=None, k_norm_weight=_weights(p, 0.8, 1.2), eps=1e-6, rotary_dim=128, theta=1e6))
+
+
+# ---- the output gate ----
+
+def _gate_bits(p, seed):
+    g = w.uniform(seed, 1, p.num_tokens * p.num_heads * p.head_size) * 8.0 - 4.0
+    g = oracle.double_to_bf16(g) if p.dtype == "bf16" else oracle.double_to_f16(g)
+    return g.reshape(p.num_tokens, p.num_heads * p.head_size)
+
+
+GATE_CASES = {
+    "decode-splits": (lambda: w.make_problem(name="g-dec", seed=61, dtype="fp16", num_heads=32, kv_num_heads=8,
+                                             head_size=128, block_size=64, past=[3000, 17, 600], q_lens=[1, 2, 4]),
+                      {"decode_split_keys": 64}),
+    "decode-auto-bf16": (lambda: w.make_problem(name="g-dec2", seed=62, dtype="bf16", num_heads=16, kv_num_heads=4,
+                                                head_size=128, block_size=16, past=[4000, 1], q_lens=[1, 1]), {}),
+    "prefill-bf16": (lambda: w.make_problem(name="g-pre", seed=63, dtype="bf16", num_heads=16, kv_num_heads=4,
+                                            head_size=128, block_size=256, past=[0, 300], q_lens=[300, 129]), {}),
+    "mixed-64": (lambda: w.make_problem(name="g-mix", seed=64, dtype="fp16", num_heads=8, kv_num_heads=2,
+                                        head_size=64, block_size=32, past=[100, 5, 40], q_lens=[70, 3, 1]), {}),
+}
+
+
+@pytest.mark.parametrize("name", sorted(GATE_CASES))
+def test_output_gate(name):
+    make, opts = GATE_CASES[name]
+    p = make()
+    gb = _gate_bits(p, 70)
+    ref = oracle.paged_attention(p, gate=gb)
+    d = upload(p)
+    gate = torch.from_numpy(gb.view(np.int16)).cuda().view(TORCH_DT[p.dtype])
+    lse = torch.empty((p.num_tokens, p.num_heads), dtype=torch.float32, device="cuda")
+    out = pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
+                             d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], d["slot_mapping"],
+                             num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, scale=p.scale, lse=lse,
+                             output_gate=gate, **opts)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits_of(d["key_cache"]), ref["key_cache"])
+    assert_close(bits_of(out).reshape(p.num_tokens, p.num_heads, p.head_size), ref["out"], p.dtype, name)
+    lg = lse.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(lg - ref["lse"]) <= 5e-4 + 1e-5 * np.abs(ref["lse"]))  # lse is not gated

@@ -51,6 +51,10 @@ class PaQkPrep(ctypes.Structure):
                 ("reserved", ctypes.c_int32)]
 
 
+class PaExtensions(ctypes.Structure):
+    _fields_ = [("lse", ctypes.c_void_p), ("qk_prep", ctypes.POINTER(PaQkPrep)), ("output_gate", ctypes.c_void_p)]
+
+
 def load_library():
     """Load libpagedattn.so (raises if it has not been built)."""
     global _lib
@@ -70,7 +74,7 @@ def load_library():
     lib.pa_paged_attention_stages.restype = ctypes.c_int
     lib.pa_paged_attention_lse.argtypes = common[:13] + [p] + common[13:]
     lib.pa_paged_attention_lse.restype = ctypes.c_int
-    lib.pa_paged_attention_ex.argtypes = common[:13] + [p, ctypes.POINTER(PaQkPrep)] + common[13:]
+    lib.pa_paged_attention_ex.argtypes = common[:13] + [ctypes.POINTER(PaExtensions)] + common[13:]
     lib.pa_paged_attention_ex.restype = ctypes.c_int
     lib.pa_status_string.argtypes = [ctypes.c_int]
     lib.pa_status_string.restype = ctypes.c_char_p
@@ -125,7 +129,8 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
                     output: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                     decode_split_keys: int = 0, route: int = ROUTE_AUTO, max_query_len: int = 0,
                     stages: int = STAGE_ALL, stream: Optional[torch.cuda.Stream] = None,
-                    lse: Optional[torch.Tensor] = None, qk_prep: Optional[dict] = None) -> torch.Tensor:
+                    lse: Optional[torch.Tensor] = None, qk_prep: Optional[dict] = None,
+                    output_gate: Optional[torch.Tensor] = None) -> torch.Tensor:
     """com.microsoft.PagedAttention on CUDA tensors. Writes key_cache / value_cache in
     place and returns ``output`` (num_tokens, num_heads * head_size).
 
@@ -136,7 +141,9 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
     ``qk_prep`` (optional, whole calls only): dict(q_norm_weight=tensor (head_size,) of the
     query dtype or None, k_norm_weight=... or None, eps=float, rotary_dim=int, theta=float):
     RMSNorm of the query and key heads, then the rotary embedding at each row's position,
-    before the cache write (pa_qk_prep)."""
+    before the cache write (pa_qk_prep).
+    ``output_gate`` (optional, whole calls only, shape and dtype of the output): the output is
+    multiplied by sigmoid(output_gate) elementwise before the final rounding."""
     lib = load_library()
     if query.dtype not in _DTYPES:
         raise TypeError("query must be float16 or bfloat16")
@@ -152,6 +159,11 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
             raise ValueError("lse must be float32 (num_tokens, num_heads)")
         if stages != STAGE_ALL:
             raise ValueError("lse is exported by whole calls only")
+    if output_gate is not None:
+        if output_gate.dtype != query.dtype or output_gate.numel() != query.shape[0] * num_heads * key_cache.shape[3]:
+            raise ValueError("output_gate must have the output's shape and dtype")
+        if stages != STAGE_ALL:
+            raise ValueError("output_gate applies to whole calls only")
     prep = None
     if qk_prep is not None:
         if stages != STAGE_ALL:
@@ -167,7 +179,7 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
                         float(qk_prep.get("eps", 1e-6)), float(qk_prep.get("theta", 10000.0)),
                         int(qk_prep.get("rotary_dim", 0)), 0)
     for t in (query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
-              slot_mapping, output, workspace, lse):
+              slot_mapping, output, workspace, lse, output_gate):
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError("all tensors must be contiguous CUDA tensors")
     N = query.shape[0]
@@ -188,11 +200,14 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
         ws = lib.pa_workspace_size(ctypes.byref(dims), num_heads, kv_num_heads)
         workspace = torch.empty(max(int(ws), 256), dtype=torch.uint8, device=query.device)
     s = (stream or torch.cuda.current_stream(query.device)).cuda_stream
-    if prep is not None:
+    if prep is not None or output_gate is not None:
+        ext = PaExtensions(None if lse is None else lse.data_ptr(),
+                           ctypes.pointer(prep) if prep is not None else None,
+                           None if output_gate is None else output_gate.data_ptr())
         st = lib.pa_paged_attention_ex(
             _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
             _ptr(cumulative_sequence_length), _ptr(past_seqlens), _ptr(block_table), _ptr(slot_mapping),
-            int(num_heads), int(kv_num_heads), float(scale), _ptr(output), _ptr(lse), ctypes.byref(prep),
+            int(num_heads), int(kv_num_heads), float(scale), _ptr(output), ctypes.byref(ext),
             ctypes.byref(dims), _ptr(workspace), int(workspace.numel()), ctypes.c_void_p(s))
     elif lse is not None:
         st = lib.pa_paged_attention_lse(
@@ -211,5 +226,5 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
     return output
 
 
-__all__ = ["paged_attention", "workspace_size", "make_dims", "PaQkPrep", "read_device_error", "kernel_launch_count",
+__all__ = ["paged_attention", "workspace_size", "make_dims", "PaQkPrep", "PaExtensions", "read_device_error", "kernel_launch_count",
            "load_library", "PagedAttentionError", "PaDims", "LIBRARY_PATH"]

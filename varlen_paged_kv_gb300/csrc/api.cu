@@ -231,8 +231,8 @@ namespace {
 pa_status run(const void* query, const void* key, const void* value, void* key_cache, void* value_cache,
               const int32_t* cumulative_sequence_length, const int32_t* past_seqlens, const int32_t* block_table,
               const int32_t* slot_mapping, int32_t num_heads, int32_t kv_num_heads, float scale, void* output,
-              float* lse, const pa_qk_prep* prep, const pa_dims* dims, void* workspace, size_t workspace_bytes,
-              void* stream, uint32_t stages) {
+              float* lse, const pa_qk_prep* prep, const void* gate, const pa_dims* dims, void* workspace,
+              size_t workspace_bytes, void* stream, uint32_t stages) {
   pa_status st = check_dims(dims, num_heads, kv_num_heads);
   if (st != PA_OK) return st;
   if (prep) {
@@ -254,6 +254,7 @@ pa_status run(const void* query, const void* key, const void* value, void* key_c
     return PA_ERR_INVALID_ARGUMENT;
   if (!aligned(query, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) || !aligned(output, 16) ||
       (key && (!aligned(key, 16) || !aligned(value, 16))) || (lse && !aligned(lse, 4)) ||
+      (gate && !aligned(gate, 16)) ||
       !aligned(cumulative_sequence_length, 4) ||
       !aligned(past_seqlens, 4) || !aligned(block_table, 4) || (slot_mapping && !aligned(slot_mapping, 4)) ||
       !aligned(workspace, 256))
@@ -276,6 +277,7 @@ pa_status run(const void* query, const void* key, const void* value, void* key_c
   a.slot_mapping = slot_mapping;
   a.output = output;
   a.lse = lse;
+  a.gate = static_cast<const uint16_t*>(gate);
   a.N = N;
   a.B = B;
   a.nh = num_heads;
@@ -338,8 +340,8 @@ pa_status pa_paged_attention_stages(const void* query, const void* key, const vo
                                     void* output, const pa_dims* dims, void* workspace, size_t workspace_bytes,
                                     void* stream, uint32_t stages) {
   return run(query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
-             slot_mapping, num_heads, kv_num_heads, scale, output, nullptr, nullptr, dims, workspace, workspace_bytes,
-             stream, stages);
+             slot_mapping, num_heads, kv_num_heads, scale, output, nullptr, nullptr, nullptr, dims, workspace,
+             workspace_bytes, stream, stages);
 }
 
 pa_status pa_paged_attention(const void* query, const void* key, const void* value, void* key_cache,
@@ -348,8 +350,8 @@ pa_status pa_paged_attention(const void* query, const void* key, const void* val
                              int32_t num_heads, int32_t kv_num_heads, float scale, void* output,
                              const pa_dims* dims, void* workspace, size_t workspace_bytes, void* stream) {
   return run(query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
-             slot_mapping, num_heads, kv_num_heads, scale, output, nullptr, nullptr, dims, workspace, workspace_bytes,
-             stream, PA_STAGE_ALL);
+             slot_mapping, num_heads, kv_num_heads, scale, output, nullptr, nullptr, nullptr, dims, workspace,
+             workspace_bytes, stream, PA_STAGE_ALL);
 }
 
 pa_status pa_paged_attention_lse(const void* query, const void* key, const void* value, void* key_cache,
@@ -359,18 +361,19 @@ pa_status pa_paged_attention_lse(const void* query, const void* key, const void*
                                  void* output, float* lse, const pa_dims* dims, void* workspace,
                                  size_t workspace_bytes, void* stream) {
   return run(query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
-             slot_mapping, num_heads, kv_num_heads, scale, output, lse, nullptr, dims, workspace, workspace_bytes,
-             stream, PA_STAGE_ALL);
+             slot_mapping, num_heads, kv_num_heads, scale, output, lse, nullptr, nullptr, dims, workspace,
+             workspace_bytes, stream, PA_STAGE_ALL);
 }
 
 pa_status pa_paged_attention_ex(const void* query, const void* key, const void* value, void* key_cache,
                                 void* value_cache, const int32_t* cumulative_sequence_length,
                                 const int32_t* past_seqlens, const int32_t* block_table, const int32_t* slot_mapping,
-                                int32_t num_heads, int32_t kv_num_heads, float scale, void* output, float* lse,
-                                const pa_qk_prep* prep, const pa_dims* dims, void* workspace, size_t workspace_bytes,
-                                void* stream) {
+                                int32_t num_heads, int32_t kv_num_heads, float scale, void* output,
+                                const pa_extensions* ext, const pa_dims* dims, void* workspace,
+                                size_t workspace_bytes, void* stream) {
   return run(query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
-             slot_mapping, num_heads, kv_num_heads, scale, output, lse, prep, dims, workspace, workspace_bytes, stream,
+             slot_mapping, num_heads, kv_num_heads, scale, output, ext ? ext->lse : nullptr,
+             ext ? ext->qk_prep : nullptr, ext ? ext->output_gate : nullptr, dims, workspace, workspace_bytes, stream,
              PA_STAGE_ALL);
 }
 

@@ -121,6 +121,7 @@ struct Args {
   const int32_t* slot_mapping;
   void* output;
   float* lse;             // (N, nh) natural-log lse of each output row, or null
+  const uint16_t* gate;   // (N, nh * hs) output gate (output *= sigmoid(gate)), or null
   // Q/K preparation in the cache-write stage (prep != 0): RMSNorm weights (or null), the
   // rotary dimension, its fp32 frequency table, and the prepared query rows (N, nh, hs)
   int32_t prep;
@@ -329,6 +330,19 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
   int old;
   asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
+}
+
+// x[0..7] times sigmoid of the 8 gate values (T) at g (16-byte aligned): x / (1 + e^-gate)
+template <bool BF16>
+__device__ __forceinline__ void apply_gate8(const uint16_t* g, float* x) {
+  const uint4 w = __ldg(reinterpret_cast<const uint4*>(g));
+  const uint32_t gw[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const uint32_t b = (gw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+    const float gf = BF16 ? __uint_as_float(b << 16) : __half2float(__ushort_as_half((unsigned short)b));
+    x[e] = x[e] / (1.f + __expf(-gf));
+  }
 }
 
 // one lane of the (fully active) warp, chosen by the hardware; the rest of the warp skips

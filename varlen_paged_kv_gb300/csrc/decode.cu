@@ -348,11 +348,16 @@ __global__ void __launch_bounds__(160, 2)
         if (mine) {
 #pragma unroll
           for (int v = 0; v < CW; v += 8) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = src[v + e] * inv;
+            if (a.gate)  // output gate: times sigmoid(gate), elementwise
+              apply_gate8<BF16>(a.gate + ((int64_t)tok * a.nh + head) * HS + col + v, x);
             uint4 pk;
-            pk.x = pack2<BF16>(src[v + 0] * inv, src[v + 1] * inv);
-            pk.y = pack2<BF16>(src[v + 2] * inv, src[v + 3] * inv);
-            pk.z = pack2<BF16>(src[v + 4] * inv, src[v + 5] * inv);
-            pk.w = pack2<BF16>(src[v + 6] * inv, src[v + 7] * inv);
+            pk.x = pack2<BF16>(x[0], x[1]);
+            pk.y = pack2<BF16>(x[2], x[3]);
+            pk.z = pack2<BF16>(x[4], x[5]);
+            pk.w = pack2<BF16>(x[6], x[7]);
             *reinterpret_cast<uint4*>(dst + v) = pk;
           }
         }
@@ -403,11 +408,15 @@ __global__ void __launch_bounds__(160, 2)
           if (a.lse && (t & 7) == 0) a.lse[(int64_t)tok * a.nh + head] = Mx + fast_log2(den) * 0.69314718055994531f;
 #pragma unroll
           for (int v = 0; v < CW; v += 8) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = acc[v + e] * dinv;
+            if (a.gate) apply_gate8<BF16>(a.gate + ((int64_t)tok * a.nh + head) * HS + col + v, x);
             uint4 pk;
-            pk.x = pack2<BF16>(acc[v + 0] * dinv, acc[v + 1] * dinv);
-            pk.y = pack2<BF16>(acc[v + 2] * dinv, acc[v + 3] * dinv);
-            pk.z = pack2<BF16>(acc[v + 4] * dinv, acc[v + 5] * dinv);
-            pk.w = pack2<BF16>(acc[v + 6] * dinv, acc[v + 7] * dinv);
+            pk.x = pack2<BF16>(x[0], x[1]);
+            pk.y = pack2<BF16>(x[2], x[3]);
+            pk.z = pack2<BF16>(x[4], x[5]);
+            pk.w = pack2<BF16>(x[6], x[7]);
             *reinterpret_cast<uint4*>(dst + v) = pk;
           }
         }

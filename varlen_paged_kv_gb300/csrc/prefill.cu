@@ -495,6 +495,12 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           tc_fence_before();
           mbar_arrive(&o_free[x]);
           if (store) {
+            if (a.gate) {  // output gate: times sigmoid(gate), elementwise
+              const uint16_t* gsrc =
+                  a.gate + ((int64_t)(c0 + tile.j0 + row) * a.nh + h) * HS + hsel * OCOLS;
+#pragma unroll
+              for (int v = 0; v < OCOLS; v += 8) apply_gate8<BF16>(gsrc + v, reinterpret_cast<float*>(ov + v));
+            }
 #pragma unroll
             for (int v = 0; v < OCOLS / 2; ++v)  // packed in place (word v from words 2v, 2v + 1)
               ov[v] = pack2<BF16>(__uint_as_float(ov[2 * v]) * inv, __uint_as_float(ov[2 * v + 1]) * inv);
