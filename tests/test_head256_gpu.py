@@ -1,0 +1,131 @@
+"""head_size 256 on the decode kernel: batches whose max_query_len bound proves every
+sequence decode-class (max_query_len * G <= 16) run with 256-wide heads, with and without
+forced splits, with lse, with the Q/K preparation and with the output gate. A 256-wide
+call without that bound is refused before any launch.
+
+Same bars as the other parity tests: caches bit for bit (prepared keys within one unit in
+the last place), outputs within 2e-3 + 1e-2 |oracle|, lse within 5e-4 + 1e-5 |oracle|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import varlen_paged_kv_gb300 as pa
+import workloads as w
+from gpu_utils import TORCH_DT, assert_close, bits_of, upload
+from helpers import bits_to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA is required for the gpu tests")
+    from varlen_paged_kv_gb300 import build
+    build.build()
+
+
+CASES = {
+    # name: (dtype, nh, kvh, bs, past, q_lens)
+    "gqa8-q-up-to-2": ("fp16", 16, 2, 64, [0, 5, 700, 3000], [1, 1, 2, 1]),
+    "mha-q16": ("bf16", 4, 4, 16, [33, 1000], [16, 3]),
+    "gqa16-long": ("bf16", 16, 1, 256, [4000, 0], [1, 1]),
+    "gqa4-ragged": ("fp16", 8, 2, 32, [129, 63, 1], [4, 2, 1]),
+}
+
+
+def _problem(name, seed=91):
+    dt, nh, kvh, bs, past, q = CASES[name]
+    return w.make_problem(name=name, seed=seed, dtype=dt, num_heads=nh, kv_num_heads=kvh, head_size=256,
+                          block_size=bs, past=past, q_lens=q, packed=False, slot_mode="omitted", drop_count=0,
+                          num_blocks=None)
+
+
+def _workspace(p, split=0, prep=False):
+    dims = pa.make_dims(p.num_tokens, p.batch_size, 256, p.num_blocks, p.block_size, p.max_blocks_per_sequence,
+                        TORCH_DT[p.dtype], split, pa.ROUTE_AUTO, int(p.q_lens.max()), prep)
+    n = pa.workspace_size(dims, p.num_heads, p.kv_num_heads)
+    assert n > 0
+    return torch.zeros(n, dtype=torch.uint8, device="cuda")
+
+
+def _check_keys(kc, ref_kc, dtype, exact):
+    if exact:
+        assert np.array_equal(kc, ref_kc), "key cache differs"
+        return
+    diff = kc != ref_kc
+    if diff.any():  # prepared keys: within one unit in the last place of T
+        g, r = bits_to_f64(kc[diff], dtype), bits_to_f64(ref_kc[diff], dtype)
+        ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(r), 1e-30))) - (7 if dtype == "bf16" else 10))
+        ulp = np.maximum(ulp, 2.0 ** (-133 if dtype == "bf16" else -24))
+        assert np.all(np.abs(g - r) <= ulp * 1.0000001), "a prepared key is more than one ulp off"
+        assert diff.mean() < 0.01
+
+
+@pytest.mark.parametrize("split", [0, 64])
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_head256_decode(name, split):
+    p = _problem(name)
+    ref = oracle.paged_attention(p)
+    d = upload(p)
+    ws = _workspace(p, split)
+    lse = torch.empty((p.num_tokens, p.num_heads), dtype=torch.float32, device="cuda")
+    out = pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
+                             d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], d["slot_mapping"],
+                             num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, scale=p.scale,
+                             decode_split_keys=split, workspace=ws, max_query_len=int(p.q_lens.max()), lse=lse)
+    assert pa.read_device_error(ws) == 0
+    _check_keys(bits_of(d["key_cache"]), ref["key_cache"], p.dtype, exact=True)
+    assert np.array_equal(bits_of(d["value_cache"]), ref["value_cache"]), "value cache differs"
+    assert_close(bits_of(out).reshape(p.num_tokens, p.num_heads, 256), ref["out"], p.dtype, name)
+    lg = lse.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(lg - ref["lse"]) <= 5e-4 + 1e-5 * np.abs(ref["lse"])), "lse differs"
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_head256_prep_and_gate(dtype):
+    # RMSNorm of both heads, rotary over the first 64 components, sigmoid output gate
+    p = w.make_problem(name="h256-prep", seed=92, dtype=dtype, num_heads=16, kv_num_heads=2, head_size=256,
+                       block_size=64, past=[100, 2000, 7], q_lens=[1, 2, 1], packed=False, slot_mode="omitted",
+                       drop_count=0, num_blocks=None)
+    to_t = oracle.double_to_bf16 if dtype == "bf16" else oracle.double_to_f16
+    prep_bits = dict(q_norm_weight=to_t(np.linspace(0.5, 1.5, 256)), k_norm_weight=to_t(np.linspace(1.2, 0.8, 256)),
+                     eps=1e-6, rotary_dim=64, theta=1.0e7)
+    g = w.uniform(93, 1, p.num_tokens * p.num_heads * 256) * 8.0 - 4.0
+    gate_bits = to_t(g).reshape(p.num_tokens, p.num_heads * 256)
+    ref = oracle.paged_attention(p, prep=prep_bits, gate=gate_bits)
+    d = upload(p)
+    dev = lambda b: torch.from_numpy(b.view(np.int16)).cuda().view(TORCH_DT[dtype])
+    prep = dict(q_norm_weight=dev(prep_bits["q_norm_weight"]), k_norm_weight=dev(prep_bits["k_norm_weight"]),
+                eps=1e-6, rotary_dim=64, theta=1.0e7)
+    ws = _workspace(p, 0, prep=True)
+    lse = torch.empty((p.num_tokens, p.num_heads), dtype=torch.float32, device="cuda")
+    out = pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
+                             d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], d["slot_mapping"],
+                             num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, scale=p.scale, workspace=ws,
+                             max_query_len=int(p.q_lens.max()), lse=lse, qk_prep=prep, output_gate=dev(gate_bits))
+    assert pa.read_device_error(ws) == 0
+    _check_keys(bits_of(d["key_cache"]), ref["key_cache"], dtype, exact=False)
+    assert np.array_equal(bits_of(d["value_cache"]), ref["value_cache"]), "value cache differs"
+    assert_close(bits_of(out).reshape(p.num_tokens, p.num_heads, 256), ref["out"], dtype, "h256-prep")
+    lg = lse.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(lg - ref["lse"]) <= 5e-4 + 1e-5 * np.abs(ref["lse"])), "lse differs"
+
+
+def test_head256_without_a_decode_bound_is_refused():
+    # q_len 3 with G = 8 is 24 rows: more than one decode item holds, so the call is refused
+    p = w.make_problem(name="h256-refuse", seed=94, dtype="fp16", num_heads=16, kv_num_heads=2, head_size=256,
+                       block_size=64, past=[10], q_lens=[3], packed=False, slot_mode="omitted", drop_count=0,
+                       num_blocks=None)
+    d = upload(p)
+    before = bits_of(d["key_cache"]).copy()
+    for bound in (0, 3):
+        with pytest.raises(pa.PagedAttentionError):
+            pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
+                               d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"],
+                               d["slot_mapping"], num_heads=p.num_heads, kv_num_heads=p.kv_num_heads,
+                               max_query_len=bound, workspace=torch.zeros(1 << 20, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert np.array_equal(bits_of(d["key_cache"]), before), "a refused call wrote the cache"

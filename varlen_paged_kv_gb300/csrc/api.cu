@@ -107,7 +107,11 @@ pa_status check_dims(const pa_dims* d, int32_t nh, int32_t kvh) {
   if (nh <= 0 || kvh <= 0 || nh % kvh != 0) return PA_ERR_INVALID_ARGUMENT;
   if (d->block_size <= 0 || d->head_size <= 0) return PA_ERR_INVALID_ARGUMENT;
   if (d->dtype != PA_FLOAT16 && d->dtype != PA_BFLOAT16) return PA_ERR_UNSUPPORTED;
-  if (d->head_size != 64 && d->head_size != 128) return PA_ERR_UNSUPPORTED;
+  if (d->head_size != 64 && d->head_size != 128 && d->head_size != 256) return PA_ERR_UNSUPPORTED;
+  // head_size 256 runs on the decode kernel only: a call must prove every sequence decode-class
+  if (d->head_size == 256 && (d->route != PA_ROUTE_AUTO || d->max_query_len <= 0 ||
+                              (int64_t)d->max_query_len * (nh / kvh) > pa::kDecRows))
+    return PA_ERR_UNSUPPORTED;
   if (d->block_size % 16 != 0) return PA_ERR_UNSUPPORTED;
   if (d->route != PA_ROUTE_AUTO && d->route != PA_ROUTE_ALL_PREFILL) return PA_ERR_INVALID_ARGUMENT;
   if (d->decode_split_keys < 0 || d->decode_split_keys % pa::kDecTile != 0) return PA_ERR_INVALID_ARGUMENT;
@@ -143,7 +147,7 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
                      cudaStream_t stream) {
   DeviceInfo info;
   if (!device_info(&info)) return cuda_fail(cudaGetLastError(), "device query");
-  args.dec_ctas = std::min(pa::kDecCtasPerSm * info.sms, pa::kMaxDecCtas);
+  args.dec_ctas = std::min(pa::dec_ctas_per_sm(args.hs) * info.sms, pa::kMaxDecCtas);
   const pa_dtype dt = (pa_dtype)d->dtype;
   const bool bf16 = dt == PA_BFLOAT16;
   const int hs = args.hs;

@@ -19,7 +19,9 @@ constexpr int kDecTile = 64;          // keys per decode pipeline stage
 constexpr int kDecStages = 3;         // decode K/V ring depth
 constexpr int kDecWarps = 4;          // decode consumer warps (16 keys of a tile each)
 constexpr int kDecRows = 16;          // query rows per decode work item (one m16 MMA tile)
-constexpr int kDecCtasPerSm = 2;      // resident decode CTAs per SM (shared-memory bound)
+constexpr int kDecCtasPerSm = 2;      // resident decode CTAs per SM (shared-memory bound), head_size <= 128
+// head_size 256: a 3-stage ring of 64-key K and V tiles is 192 KB, one CTA per SM
+__host__ __device__ constexpr int dec_ctas_per_sm(int hs) { return hs == 256 ? 1 : kDecCtasPerSm; }
 constexpr int kMaxDecCtas = 1024;     // upper bound of the decode grid
 constexpr int kPreTileQ = 128;        // query rows per prefill tile (MMA M)
 constexpr int kPreTileK = 128;        // keys per prefill KV tile (MMA N of Q K^T, K of P V)
@@ -131,7 +133,7 @@ struct Args {
   const uint16_t* q_norm_w;
   const uint16_t* k_norm_w;
   uint16_t* qprep;
-  float inv_freq[64];
+  float inv_freq[128];   // rotary inverse frequencies, one per rotated pair (rotary_dim / 2 <= 128)
   int32_t N, B, nh, kvh, G, hs, num_blocks, bs, max_blocks;
   int32_t q_stride;       // elements per query row
   int32_t kv_row;         // kvh * hs

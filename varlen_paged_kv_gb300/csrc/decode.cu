@@ -75,7 +75,7 @@ __device__ __forceinline__ void load_q(const Args& a, const DecodeItem& item, in
 }
 
 template <int HS, bool BF16>
-__global__ void __launch_bounds__(160, 2)
+__global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
     decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const int seg_rows) {
   using L = DecSmem<HS>;
@@ -439,6 +439,8 @@ static cudaError_t launch_decode_t(const Args& a, const CUtensorMap& tk, const C
 cudaError_t launch_decode(const Args& a, bool bf16, const CUtensorMap& tk, const CUtensorMap& tv, int seg,
                           cudaStream_t s) {
   if (a.hs == 64) return bf16 ? launch_decode_t<64, true>(a, tk, tv, seg, s) : launch_decode_t<64, false>(a, tk, tv, seg, s);
+  if (a.hs == 256)
+    return bf16 ? launch_decode_t<256, true>(a, tk, tv, seg, s) : launch_decode_t<256, false>(a, tk, tv, seg, s);
   return bf16 ? launch_decode_t<128, true>(a, tk, tv, seg, s) : launch_decode_t<128, false>(a, tk, tv, seg, s);
 }
 

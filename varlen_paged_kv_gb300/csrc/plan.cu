@@ -432,7 +432,13 @@ template <int HS>
 __device__ __forceinline__ void load_vec(const uint16_t* src, bool bf16, float (&x)[HS / 32]) {
   constexpr int E = HS / 32;
   uint32_t wds[E / 2];
-  if constexpr (E == 4) {
+  if constexpr (E == 8) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
+    wds[0] = v.x;
+    wds[1] = v.y;
+    wds[2] = v.z;
+    wds[3] = v.w;
+  } else if constexpr (E == 4) {
     const uint2 v = __ldg(reinterpret_cast<const uint2*>(src));
     wds[0] = v.x;
     wds[1] = v.y;
@@ -458,7 +464,8 @@ __device__ __forceinline__ void store_vec(uint16_t* dst, bool bf16, const float 
   uint32_t wds[E / 2];
 #pragma unroll
   for (int k = 0; k < E / 2; ++k) wds[k] = bf16 ? pack2<true>(x[2 * k], x[2 * k + 1]) : pack2<false>(x[2 * k], x[2 * k + 1]);
-  if constexpr (E == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(wds[0], wds[1]);
+  if constexpr (E == 8) *reinterpret_cast<uint4*>(dst) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+  else if constexpr (E == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(wds[0], wds[1]);
   else *reinterpret_cast<uint32_t*>(dst) = wds[0];
 }
 
@@ -550,6 +557,7 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
     }
     if (a.prep) {  // (the query rows are prepared even where the K/V write is skipped)
       if (a.hs == 128) prep_token<128>(a, tok, pos, slot, lane);
+      else if (a.hs == 256) prep_token<256>(a, tok, pos, slot, lane);
       else prep_token<64>(a, tok, pos, slot, lane);
       continue;
     }
