@@ -1,7 +1,8 @@
-"""head_size 256 on the decode kernel: batches whose max_query_len bound proves every
-sequence decode-class (max_query_len * G <= 16) run with 256-wide heads, with and without
-forced splits, with lse, with the Q/K preparation and with the output gate. A 256-wide
-call without that bound is refused before any launch.
+"""head_size 256: the decode kernel (one CTA per SM) and the 256-wide prefill kernel (one
+head per unit, two S buffers in TMEM), through the C ABI against the oracle: decode-only
+batches with and without forced splits, prefill and chunked prefill (fp16, bf16 with the
+fp16 V copy and bf16 on the two-product path), packed rows with dropped slots, mixed
+batches, lse, the Q/K preparation and the output gate.
 
 Same bars as the other parity tests: caches bit for bit (prepared keys within one unit in
 the last place), outputs within 2e-3 + 1e-2 |oracle|, lse within 5e-4 + 1e-5 |oracle|.
@@ -114,18 +115,61 @@ def test_head256_prep_and_gate(dtype):
     assert np.all(np.abs(lg - ref["lse"]) <= 5e-4 + 1e-5 * np.abs(ref["lse"])), "lse differs"
 
 
-def test_head256_without_a_decode_bound_is_refused():
-    # q_len 3 with G = 8 is 24 rows: more than one decode item holds, so the call is refused
-    p = w.make_problem(name="h256-refuse", seed=94, dtype="fp16", num_heads=16, kv_num_heads=2, head_size=256,
-                       block_size=64, past=[10], q_lens=[3], packed=False, slot_mode="omitted", drop_count=0,
-                       num_blocks=None)
+PREFILL = {
+    # name: (dtype, nh, kvh, bs, past, q_lens, packed, drops)
+    "ragged-fp16": ("fp16", 8, 2, 256, [0, 0], [300, 129], False, 0),
+    "chunked-bf16-copy": ("bf16", 16, 2, 64, [1000, 17, 255], [200, 64, 130], False, 0),
+    "bf16-two-product": ("bf16", 4, 1, 128, [2500], [257], False, 0),
+    "mixed-packed-drops": ("fp16", 8, 2, 32, [0, 900, 50, 3000], [130, 1, 40, 2], True, 9),
+    "mha-pages16": ("bf16", 4, 4, 16, [5, 0], [140, 33], False, 0),
+}
+
+
+def _prefill_problem(name, seed=95):
+    dt, nh, kvh, bs, past, q, packed, drops = PREFILL[name]
+    return w.make_problem(name=name, seed=seed, dtype=dt, num_heads=nh, kv_num_heads=kvh, head_size=256,
+                          block_size=bs, past=past, q_lens=q, packed=packed,
+                          slot_mode="explicit" if drops else "omitted", drop_count=drops, num_blocks=None)
+
+
+@pytest.mark.parametrize("route", [pa.ROUTE_AUTO, pa.ROUTE_ALL_PREFILL])
+@pytest.mark.parametrize("name", sorted(PREFILL))
+def test_head256_prefill(name, route):
+    p = _prefill_problem(name)
+    ref = oracle.paged_attention(p)
     d = upload(p)
-    before = bits_of(d["key_cache"]).copy()
-    for bound in (0, 3):
-        with pytest.raises(pa.PagedAttentionError):
-            pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
-                               d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"],
-                               d["slot_mapping"], num_heads=p.num_heads, kv_num_heads=p.kv_num_heads,
-                               max_query_len=bound, workspace=torch.zeros(1 << 20, dtype=torch.uint8, device="cuda"))
+    lse = torch.empty((p.num_tokens, p.num_heads), dtype=torch.float32, device="cuda")
+    out = pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
+                             d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], d["slot_mapping"],
+                             num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, scale=p.scale, route=route, lse=lse)
     torch.cuda.synchronize()
-    assert np.array_equal(bits_of(d["key_cache"]), before), "a refused call wrote the cache"
+    assert np.array_equal(bits_of(d["key_cache"]), ref["key_cache"]), "key cache differs"
+    assert np.array_equal(bits_of(d["value_cache"]), ref["value_cache"]), "value cache differs"
+    assert_close(bits_of(out).reshape(p.num_tokens, p.num_heads, 256), ref["out"], p.dtype, name)
+    lg = lse.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(lg - ref["lse"]) <= 5e-4 + 1e-5 * np.abs(ref["lse"])), "lse differs"
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_head256_prefill_prep_and_gate(dtype):
+    p = w.make_problem(name="h256-prep-pre", seed=96, dtype=dtype, num_heads=8, kv_num_heads=2, head_size=256,
+                       block_size=64, past=[0, 300], q_lens=[260, 70], packed=False, slot_mode="omitted",
+                       drop_count=0, num_blocks=None)
+    to_t = oracle.double_to_bf16 if dtype == "bf16" else oracle.double_to_f16
+    prep_bits = dict(q_norm_weight=to_t(np.linspace(0.5, 1.5, 256)), k_norm_weight=to_t(np.linspace(1.2, 0.8, 256)),
+                     eps=1e-6, rotary_dim=64, theta=1.0e7)
+    g = w.uniform(97, 1, p.num_tokens * p.num_heads * 256) * 8.0 - 4.0
+    gate_bits = to_t(g).reshape(p.num_tokens, p.num_heads * 256)
+    ref = oracle.paged_attention(p, prep=prep_bits, gate=gate_bits)
+    d = upload(p)
+    dev = lambda b: torch.from_numpy(b.view(np.int16)).cuda().view(TORCH_DT[dtype])
+    prep = dict(q_norm_weight=dev(prep_bits["q_norm_weight"]), k_norm_weight=dev(prep_bits["k_norm_weight"]),
+                eps=1e-6, rotary_dim=64, theta=1.0e7)
+    out = pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
+                             d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], d["slot_mapping"],
+                             num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, scale=p.scale, qk_prep=prep,
+                             output_gate=dev(gate_bits))
+    torch.cuda.synchronize()
+    _check_keys(bits_of(d["key_cache"]), ref["key_cache"], dtype, exact=False)
+    assert np.array_equal(bits_of(d["value_cache"]), ref["value_cache"]), "value cache differs"
+    assert_close(bits_of(out).reshape(p.num_tokens, p.num_heads, 256), ref["out"], dtype, "h256-prep-pre")

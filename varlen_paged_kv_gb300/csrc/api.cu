@@ -108,10 +108,6 @@ pa_status check_dims(const pa_dims* d, int32_t nh, int32_t kvh) {
   if (d->block_size <= 0 || d->head_size <= 0) return PA_ERR_INVALID_ARGUMENT;
   if (d->dtype != PA_FLOAT16 && d->dtype != PA_BFLOAT16) return PA_ERR_UNSUPPORTED;
   if (d->head_size != 64 && d->head_size != 128 && d->head_size != 256) return PA_ERR_UNSUPPORTED;
-  // head_size 256 runs on the decode kernel only: a call must prove every sequence decode-class
-  if (d->head_size == 256 && (d->route != PA_ROUTE_AUTO || d->max_query_len <= 0 ||
-                              (int64_t)d->max_query_len * (nh / kvh) > pa::kDecRows))
-    return PA_ERR_UNSUPPORTED;
   if (d->block_size % 16 != 0) return PA_ERR_UNSUPPORTED;
   if (d->route != PA_ROUTE_AUTO && d->route != PA_ROUTE_ALL_PREFILL) return PA_ERR_INVALID_ARGUMENT;
   if (d->decode_split_keys < 0 || d->decode_split_keys % pa::kDecTile != 0) return PA_ERR_INVALID_ARGUMENT;
@@ -195,7 +191,8 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
     } else {
       tvm = tv;  // never read
     }
-    const int heads_per_unit = (args.G % 2 == 0) ? 2 : 1;  // two heads of one KV group share a unit
+    // two heads of one KV group share a unit (one head for 256-wide heads: TMEM holds one O)
+    const int heads_per_unit = (args.G % 2 == 0 && hs != 256) ? 2 : 1;
     const int grid = (int)std::min<int64_t>((int64_t)args.max_tiles * (args.nh / heads_per_unit), info.sms);
     if (grid > 0) {
       ++g_launches;

@@ -229,12 +229,37 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Actual&&>(args)...);
 }
 
+// ---- the prefill kernels' persistent unit order ----
+// Unit k of this CTA. Units are dealt out in rounds of gridDim.x, alternately in CTA order
+// and in reverse; with the units sorted by decreasing cost this pairs a CTA's expensive
+// units with cheap ones, and the per-CTA totals come out close to those of the greedy
+// longest-first assignment (a plain round robin gives the first CTAs the most work in
+// every round). Strictly increasing in k, so a CTA's loop ends at its first unit past the
+// end.
+__device__ __forceinline__ int snake_unit(int k) {
+  const int g = (int)gridDim.x;
+  return k * g + ((k & 1) ? g - 1 - (int)blockIdx.x : (int)blockIdx.x);
+}
+
+// the record of unit u (all zeros past the end)
+__device__ __forceinline__ PrefillTile load_tile(const Args& a, int u, int n_units, int units_per_tile) {
+  if (u >= n_units) return PrefillTile{};
+  return a.tiles[u / units_per_tile];
+}
+
+// TMEM column (relative to S) of P for the 16 keys of block kk of a 128-key tile: the P of
+// keys [32c, 32c + 32) replaces the S columns of those keys, hi pairs in the first 16
+// columns and lo pairs (bf16) in the last 16.
+__device__ __forceinline__ uint32_t p_col(int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); }
+
 // ---- host launchers, one per kernel family (defined next to their kernels) -----------------
 cudaError_t launch_plan(const Args& a, cudaStream_t s);
 cudaError_t launch_cache_write(const Args& a, int grid, cudaStream_t s);
 cudaError_t launch_v_mirror(const Args& a, int grid, cudaStream_t s);
 cudaError_t launch_prefill(const Args& a, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const CUtensorMap& tvm, int seg, int grid, cudaStream_t s);
+cudaError_t launch_prefill256(const Args& a, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& tv, const CUtensorMap& tvm, int seg, int grid, cudaStream_t s);
 cudaError_t launch_decode(const Args& a, bool bf16, const CUtensorMap& tk, const CUtensorMap& tv, int seg,
                           cudaStream_t s);
 

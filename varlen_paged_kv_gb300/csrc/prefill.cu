@@ -46,28 +46,6 @@ constexpr int kSoftWarpsPerHead = 8;  // two warps per TMEM lane quarter, 64 sco
 __device__ __forceinline__ uint32_t s_col(int x) { return x ? 128u : 0u; }
 __device__ __forceinline__ uint32_t o_col(int x) { return x ? 384u : 256u; }
 
-// TMEM column (relative to S) of P for the 16 keys of block kk of a 128-key tile: the P of
-// keys [32c, 32c + 32) replaces the S columns of those keys, hi pairs in the first 16
-// columns and lo pairs (bf16) in the last 16.
-__device__ __forceinline__ uint32_t p_col(int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); }
-
-// Unit k of this CTA. Units are dealt out in rounds of gridDim.x, alternately in CTA order
-// and in reverse; with the units sorted by decreasing cost this pairs a CTA's expensive
-// units with cheap ones, and the per-CTA totals come out close to those of the greedy
-// longest-first assignment (a plain round robin gives the first CTAs the most work in
-// every round). Strictly increasing in k, so a CTA's loop ends at its first unit past the
-// end.
-__device__ __forceinline__ int snake_unit(int k) {
-  const int g = (int)gridDim.x;
-  return k * g + ((k & 1) ? g - 1 - (int)blockIdx.x : (int)blockIdx.x);
-}
-
-// the record of unit u (all zeros past the end)
-__device__ __forceinline__ PrefillTile load_tile(const Args& a, int u, int n_units, int units_per_tile) {
-  if (u >= n_units) return PrefillTile{};
-  return a.tiles[u / units_per_tile];
-}
-
 template <int HS, bool BF16>
 __global__ void __launch_bounds__(kPreThreads, 1)
     prefill_kernel(const Args a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -540,6 +518,7 @@ static cudaError_t launch_prefill_t(const Args& a, const CUtensorMap& tq, const 
 
 cudaError_t launch_prefill(const Args& a, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& tvm, int seg, int grid, cudaStream_t s) {
+  if (a.hs == 256) return launch_prefill256(a, bf16, tq, tk, tv, tvm, seg, grid, s);
   if (a.hs == 64)
     return bf16 ? launch_prefill_t<64, true>(a, tq, tk, tv, tvm, seg, grid, s)
                 : launch_prefill_t<64, false>(a, tq, tk, tv, tvm, seg, grid, s);
