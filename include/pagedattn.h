@@ -61,9 +61,7 @@ typedef enum pa_dtype {
 typedef struct pa_dims {
   int32_t num_tokens;              /* N: rows of query, key, value, output and slot_mapping */
   int32_t batch_size;              /* B: sequences; cumulative_sequence_length has B + 1 entries */
-  int32_t head_size;               /* 64 or 128; 256 on the decode kernel only (route AUTO with a
-                                      max_query_len proving every sequence decode-class, else
-                                      PA_ERR_UNSUPPORTED) */
+  int32_t head_size;               /* 64, 128 or 256 */
   int32_t num_blocks;              /* pages in each cache */
   int32_t block_size;              /* tokens per page: a positive multiple of 16 */
   int32_t max_blocks_per_sequence; /* columns of block_table */
