@@ -22,6 +22,11 @@ constexpr int kDecRows = 16;          // query rows per decode work item (one m1
 constexpr int kDecCtasPerSm = 2;      // resident decode CTAs per SM (shared-memory bound), head_size <= 128
 // head_size 256: a 3-stage ring of 64-key K and V tiles is 192 KB, one CTA per SM
 __host__ __device__ constexpr int dec_ctas_per_sm(int hs) { return hs == 256 ? 1 : kDecCtasPerSm; }
+// What an item costs a decode CTA beyond streaming its keys (the warps' combine, the write
+// of the row or partial, the merge, the refill of the ring at the next item), in 64-key
+// tiles streamed in the same time (measured: about 5 us per item against 1.4 us per tile
+// at head_size 256 with one CTA per SM, 1.5-2 us against 1.4 us at 128 with two).
+__host__ __device__ constexpr int dec_item_cost_tiles(int hs) { return hs == 256 ? 3 : 1; }
 constexpr int kMaxDecCtas = 1024;     // upper bound of the decode grid
 constexpr int kPreTileQ = 128;        // query rows per prefill tile (MMA M)
 constexpr int kPreTileK = 128;        // keys per prefill KV tile (MMA N of Q K^T, K of P V)
@@ -163,19 +168,28 @@ struct Args {
 
 // ---- shared-memory layouts (bytes) of the attention kernels --------------------------
 // Decode: a ring of K+V tiles, the warp-combine buffer, per-warp (m, l), barriers.
+// The consumer warps combine their partial states in kCombBufs shared-memory buffers: warp
+// w adds into buffer w % kCombBufs, the buffers' warps in turn, and the writer sums the
+// buffers in order. At head_size 256 (one CTA per SM) there is room for two buffers next to
+// the 3-stage ring (two rounds instead of four); below, two CTAs share an SM and one buffer
+// takes the four warps in turn.
 template <int HS>
 struct DecSmem {
+  static constexpr int kStages = kDecStages;
+  static constexpr int kCombBufs = HS == 256 ? 2 : 1;
   static constexpr int kHalves = HS / 64;
   static constexpr int kTileBytes = kDecTile * HS * 2;      // one K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kCombStride = HS + 4;                 // floats; the pad spreads rows over banks
-  static constexpr int kComb = kDecStages * kStageBytes;     // float [16][kCombStride]
-  static constexpr int kMw = kComb + kDecRows * kCombStride * 4;  // float [4][16]
+  static constexpr int kComb = kStages * kStageBytes;        // float [kCombBufs][16][kCombStride]
+  static constexpr int kMw = kComb + kCombBufs * kDecRows * kCombStride * 4;  // float [4][16]
   static constexpr int kLw = kMw + kDecWarps * kDecRows * 4; // float [4][16]
   static constexpr int kBars = kLw + kDecWarps * kDecRows * 4;
-  static constexpr int kAbort = kBars + 2 * kDecStages * 8;
+  static constexpr int kAbort = kBars + 2 * kStages * 8;
   static constexpr int kBytes = kAbort + 16 + 1024;          // + alignment slack
 };
+static_assert(DecSmem<256>::kBytes <= 232448 && 2 * (DecSmem<128>::kBytes + 1024) <= 233472,
+              "decode shared memory");
 
 // Prefill: Q tile, two K and two V tiles, barriers, the TMEM address slot.
 template <int HS>
@@ -457,6 +471,11 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x
                ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
                : "memory");
 }
+// one 128-byte line of global memory into L2 (a hint: no data returned, no fault)
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -14,7 +14,8 @@
 //     softmax in registers (row max over the quad by shuffles, base-2 exponentials; for
 //     bf16 the weights P enter P V as a bf16 hi + lo pair, two products);
 //   - at the end of the item the four warps' (m, l, O) are combined in a fixed order in
-//     shared memory. An item that is its whole unit writes the output row rounded once to
+//     shared memory (at head_size 256 in two buffers, warps 0 + 2 and 1 + 3, which the
+//     writer adds). An item that is its whole unit writes the output row rounded once to
 //     T; otherwise it writes its normalised fp32 partial row and natural-log lse, and the
 //     last item of the unit to finish (an atomic arrival count) merges the unit's partials
 //     in key order: the (out, lse) reduction of the WS2 CP-Aware Attention Contract,
@@ -88,14 +89,14 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
   float* mw = reinterpret_cast<float*>(smem + L::kMw);
   float* lw = reinterpret_cast<float*>(smem + L::kLw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBars);
-  uint64_t* empty = full + kDecStages;
+  uint64_t* empty = full + L::kStages;
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
   volatile int* s_last = reinterpret_cast<volatile int*>(smem + L::kAbort + 4);
   uint32_t* err = &a.hdr->error;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kDecStages; ++s) {
+    for (int s = 0; s < L::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kDecWarps);
     }
@@ -121,11 +122,22 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
     for (int it = it_begin; it < it_end; ++it) {
       const DecodeItem item = next;  // loaded one item ahead
       next = load_item(a, it + 1, it_end);
+      {
+        // this item's query rows into L2: the producer runs a ring's depth of tiles ahead
+        // of the consumers, so their Q loads at the item's start find the rows there
+        // (q_len tokens x G heads x HS contiguous values each)
+        constexpr int kLine = 128;
+        const int lines = a.G * HS * 2 / kLine;
+        const char* q0 = reinterpret_cast<const char*>(a.query) +
+                         ((int64_t)item.c0 * a.q_stride + (int64_t)item.g * a.G * HS) * 2;
+        for (int i = lane; i < item.q_len * lines; i += 32)
+          prefetch_l2(q0 + (int64_t)(i / lines) * a.q_stride * 2 + (i % lines) * kLine);
+      }
       const int kv_len = item.past + item.q_len;
       const int* bt = a.block_table + (int64_t)item.b * a.max_blocks;
       for (int k0 = item.key_begin; k0 < item.key_end; k0 += kDecTile, ++cnt) {
-        const int s = cnt % kDecStages;
-        const uint32_t ph = (cnt / kDecStages) & 1;
+        const int s = cnt % L::kStages;
+        const uint32_t ph = (cnt / L::kStages) & 1;
         if (lane == 0) {
           mbar_wait(&empty[s], ph ^ 1, abort, err);
           mbar_arrive_expect_tx(&full[s], L::kStageBytes);
@@ -175,8 +187,8 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
     for (int d = 0; d < ND; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
 
     for (int k0 = item.key_begin; k0 < item.key_end; k0 += kDecTile, ++cnt) {
-      const int s = cnt % kDecStages;
-      const uint32_t ph = (cnt / kDecStages) & 1;
+      const int s = cnt % L::kStages;
+      const uint32_t ph = (cnt / L::kStages) & 1;
       mbar_wait(&full[s], ph, abort, err);
       const int kw = k0 + 16 * w;  // first key of this warp's 16
       if (kw < item.key_end) {
@@ -308,25 +320,31 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
     row_stats(mw, lw, r1, M1, L1);
     const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M0);
     const float f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M1);
+    {
+      // round rr: warps rr * B .. rr * B + B - 1 write (first round) or add their partials
+      // into buffers 0 .. B - 1; buffer b ends up holding warps b, b + B, ... in that order
+      constexpr int B = L::kCombBufs;
+      float* cw = comb + (w % B) * (kDecRows * kCombStride);
 #pragma unroll 1
-    for (int ww = 0; ww < kDecWarps; ++ww) {
-      if (w == ww) {
+      for (int rr = 0; rr < kDecWarps / B; ++rr) {
+        if (w / B == rr) {
 #pragma unroll
-        for (int d = 0; d < ND; ++d) {
-          float2* c0p = reinterpret_cast<float2*>(comb + r0 * kCombStride + d * 8 + tq * 2);
-          float2* c1p = reinterpret_cast<float2*>(comb + r1 * kCombStride + d * 8 + tq * 2);
-          const float2 a0 = make_float2(o[d][0] * f0, o[d][1] * f0), a1 = make_float2(o[d][2] * f1, o[d][3] * f1);
-          if (ww == 0) {
-            *c0p = a0;
-            *c1p = a1;
-          } else {
-            const float2 b0 = *c0p, b1 = *c1p;
-            *c0p = make_float2(b0.x + a0.x, b0.y + a0.y);
-            *c1p = make_float2(b1.x + a1.x, b1.y + a1.y);
+          for (int d = 0; d < ND; ++d) {
+            float2* c0p = reinterpret_cast<float2*>(cw + r0 * kCombStride + d * 8 + tq * 2);
+            float2* c1p = reinterpret_cast<float2*>(cw + r1 * kCombStride + d * 8 + tq * 2);
+            const float2 a0 = make_float2(o[d][0] * f0, o[d][1] * f0), a1 = make_float2(o[d][2] * f1, o[d][3] * f1);
+            if (rr == 0) {
+              *c0p = a0;
+              *c1p = a1;
+            } else {
+              const float2 b0 = *c0p, b1 = *c1p;
+              *c0p = make_float2(b0.x + a0.x, b0.y + a0.y);
+              *c1p = make_float2(b1.x + a1.x, b1.y + a1.y);
+            }
           }
         }
+        consumer_bar();
       }
-      consumer_bar();
     }
     // ---- write: thread t owns row t / 8, HS / 8 consecutive columns ----
     {
@@ -342,6 +360,14 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
       if (mine) row_stats(mw, lw, row, M, Lr);
       const float inv = Lr > 0.f ? 1.f / Lr : 0.f;
       const float* src = comb + row * kCombStride + col;
+      // the combined (unnormalised) O of this thread's row and column v: the warps'
+      // partials added in warp order
+      auto cval = [&](int v) {
+        float x = src[v];
+#pragma unroll
+        for (int bb = 1; bb < L::kCombBufs; ++bb) x += src[bb * (kDecRows * kCombStride) + v];
+        return x;
+      };
       if (item.n_split == 1) {
         if (mine && a.lse && (t & 7) == 0)  // natural log; M is the base-2 max of s * scale
           a.lse[(int64_t)tok * a.nh + head] = Lr > 0.f ? (M + fast_log2(Lr)) * 0.69314718055994531f : -INFINITY;
@@ -350,7 +376,7 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
           for (int v = 0; v < CW; v += 8) {
             float x[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = src[v + e] * inv;
+            for (int e = 0; e < 8; ++e) x[e] = cval(v + e) * inv;
             if (a.gate)  // output gate: times sigmoid(gate), elementwise
               apply_gate8<BF16>(a.gate + ((int64_t)tok * a.nh + head) * HS + col + v, x);
             uint4 pk;
@@ -367,7 +393,7 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
 #pragma unroll
           for (int v = 0; v < CW; v += 4)
             *reinterpret_cast<float4*>(pdst + v) =
-                make_float4(src[v] * inv, src[v + 1] * inv, src[v + 2] * inv, src[v + 3] * inv);
+                make_float4(cval(v) * inv, cval(v + 1) * inv, cval(v + 2) * inv, cval(v + 3) * inv);
           if ((t & 7) == 0)
             a.part_lse[(int64_t)it * kDecRows + row] =
                 Lr > 0.f ? (M + fast_log2(Lr)) * 0.69314718055994531f : -INFINITY;

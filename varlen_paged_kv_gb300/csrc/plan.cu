@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
     if (q < 0 || a.past[b] < 0 || kv > max_kv || (a.max_query_len > 0 && q > a.max_query_len)) {
       atomicOr(&s_bad, 1);
     } else if (is_decode_class(q, a)) {
-      dec_tiles += ceil_div(kv, kDecTile);
+      dec_tiles += ceil_div(kv, kDecTile) + dec_item_cost_tiles(a.hs);
     }
   }
 #pragma unroll
@@ -193,8 +193,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
     return;
   }
   const bool balanced = a.forced_split <= 0;
-  // The W decode key tiles of all units, laid end to end, are cut into P equal ranges:
-  // CTA c owns tiles [s_start[c], s_start[c + 1]), s_start[c] = floor(c W / P).
+  // The decode units, laid end to end, each as V virtual tiles (the cost of an item beyond
+  // its keys) followed by its key tiles, span W tiles; they are cut into P equal ranges:
+  // CTA c owns [s_start[c], s_start[c + 1]), s_start[c] = floor(c W / P), and processes the
+  // key tiles inside it. So a CTA whose range starts more units pays for them with fewer
+  // keys, and the CTAs finish together.
+  const int V = dec_item_cost_tiles(a.hs);
   int64_t* s_start = reinterpret_cast<int64_t*>(s_key);   // [kMaxDecCtas + 1]
   int* s_T = reinterpret_cast<int*>(s_start + (kMaxDecCtas + 1));  // [kPlanThreads] first tile of (b, head 0)
   int* s_nt = s_T + kPlanThreads;     // [kPlanThreads] tiles per unit (0: not decode)
@@ -227,7 +231,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
       dec = is_decode_class(q, a);
       if (dec) {
         nt = ceil_div(kv, kDecTile);
-        v[0] = (int)(nt * a.kvh);
+        v[0] = (int)((nt + V) * a.kvh);
       } else if (q > 0) {
         v[1] = (int)ceil_div(q, kPreTileQ);
       }
@@ -275,10 +279,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
         n_u = s_nt[sb];
         if (n_u > 0) {
           kv_u = s_kv[sb];
-          u0 = s_T[sb] + (int64_t)g * n_u;
+          u0 = s_T[sb] + (int64_t)g * (n_u + V);  // the unit's span starts here; its keys at u0 + V
           if (balanced) {
-            c0 = cta_of(u0);
-            c1 = cta_of(u0 + n_u - 1);
+            c0 = cta_of(u0 + V);
+            c1 = cta_of(u0 + V + n_u - 1);
             w = c1 - c0 + 1;
           } else {
             w = (int)ceil_div(kv_u, a.forced_split);
@@ -292,15 +296,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
         const int bb = base + sb, unit_first = idx;
         const int row0 = s_c0[sb], past = s_past[sb], q_u = kv_u - past;
         if (balanced) {
-          const int64_t u1 = u0 + n_u;
+          const int64_t k0 = u0 + V, k1 = k0 + n_u;  // the unit's key tiles
           int64_t cs = s_start[c0];
           for (int c = c0; c <= c1; ++c, ++idx) {
             const int64_t ce = s_start[c + 1];
-            const int64_t lo = max(u0, cs), hi = min(u1, ce);
+            const int64_t lo = max(k0, cs), hi = min(k1, ce);
             if (idx < a.max_items)
-              store_item(a.items + idx, bb, g, (int)((lo - u0) * kDecTile), (int)min((hi - u0) * kDecTile, (int64_t)kv_u),
+              store_item(a.items + idx, bb, g, (int)((lo - k0) * kDecTile), (int)min((hi - k0) * kDecTile, (int64_t)kv_u),
                          unit_first, w, row0, q_u, past);
-            if (cs >= u0) s_cta_begin[c] = idx;  // CTA c's range starts in this unit
+            if (cs >= u0) s_cta_begin[c] = idx;  // CTA c's range starts in this unit's span
             cs = ce;
           }
         } else {
