@@ -74,6 +74,16 @@ def _bind(path: str):
     lib.oracle_round_array.restype = None
     lib.oracle_apply_gate.argtypes = [ctypes.c_int, ctypes.c_int64, p, p, p, p]
     lib.oracle_apply_gate.restype = ctypes.c_int
+    i64 = ctypes.c_int64
+    lib.oracle_quantize_rows.argtypes = [ctypes.c_int, ctypes.c_int, i64, i32, i32, p, i64, p, p]
+    lib.oracle_quantize_rows.restype = ctypes.c_int
+    lib.oracle_scatter_codes.argtypes = [i32] * 5 + [i64] + [p] * 8
+    lib.oracle_scatter_codes.restype = ctypes.c_int
+    lib.oracle_attention_q.argtypes = ([ctypes.c_int, ctypes.c_int] + [i32] * 9 + [p] * 8 + [f32, p, p, p, ctypes.c_int])
+    lib.oracle_attention_q.restype = ctypes.c_int
+    lib.oracle_attention_rows_q.argtypes = ([ctypes.c_int, ctypes.c_int] + [i32] * 9 + [p] * 8 + [f32, i32] + [p] * 4 +
+                                            [ctypes.c_int])
+    lib.oracle_attention_rows_q.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -257,14 +267,110 @@ def apply_gate(out, gate_bits, dtype: str):
     return gated, bits
 
 
+# ---- integer KV caches (INT8 / INT4 codes with per-(KV head, channel) fp32 scales) -------
+
+KV_KIND = {"int8": 1, "int4": 2}
+
+
+def quantize_rows(x_bits, dtype: str, fmt: str, kvh: int, hs: int, scale) -> np.ndarray:
+    """Rows of kvh*hs values of T (bits, (n, kvh*hs) or wider rows sliced by the caller) to
+    code rows (oracle_quantize_rows): uint8 (n, kvh*hs) for int8, (n, kvh*hs/2) for int4."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    n = int(x.shape[0])
+    rb = kvh * hs if fmt == "int8" else kvh * hs // 2
+    codes = np.zeros((n, rb), dtype=np.uint8)
+    rc = _load().oracle_quantize_rows(1 if dtype == "bf16" else 0, KV_KIND[fmt], n, kvh, hs, _ptr(x),
+                                      int(x.shape[1]) if x.ndim == 2 else kvh * hs,
+                                      _ptr(_c(scale, np.float32)), _ptr(codes))
+    if rc:
+        raise OracleError(rc)
+    return codes
+
+
+def kv_rows(p):
+    """This call's K and V rows (bits, (N, kvh*hs) each), from the packed rows if packed."""
+    nh, kvh, hs = int(p.num_heads), int(p.kv_num_heads), int(p.head_size)
+    if p.key is None:
+        q = np.asarray(p.query, dtype=np.uint16)
+        return q[:, nh * hs:(nh + kvh) * hs], q[:, (nh + kvh) * hs:]
+    return p.key, p.value
+
+
+def scatter_codes(p, k_codes, v_codes):
+    """The cache write of an integer-cache problem on copies of its code caches."""
+    lib = _load()
+    N, B, nh, kvh, hs, nblk, bs, mb = _dims(p)
+    kc = np.array(p.key_cache, dtype=np.uint8, copy=True)
+    vc = np.array(p.value_cache, dtype=np.uint8, copy=True)
+    rb = int(np.asarray(k_codes).shape[1]) if N else (kvh * hs if p.kv_quant == "int8" else kvh * hs // 2)
+    rc = lib.oracle_scatter_codes(N, B, nblk, bs, mb, rb, _ptr(_c(k_codes, np.uint8)), _ptr(_c(v_codes, np.uint8)),
+                                  _ptr(kc), _ptr(vc), _ptr(_c(p.cumulative_sequence_length, np.int32)),
+                                  _ptr(_c(p.past_seqlens, np.int32)), _ptr(_c(p.block_table, np.int32)),
+                                  _ptr(_c(p.slot_mapping, np.int32)))
+    if rc:
+        raise OracleError(rc)
+    return kc, vc
+
+
+def attention_q(p, key_cache, value_cache, nthreads: int = 0):
+    """Attention over integer caches (after the write). Returns (out, lse, out_bits)."""
+    lib = _load()
+    N, B, nh, kvh, hs, nblk, bs, mb = _dims(p)
+    q = _c(p.query, np.uint16)
+    out = np.zeros((N, nh, hs), dtype=np.float64)
+    lse = np.zeros((N, nh), dtype=np.float64)
+    bits = np.zeros((N, nh * hs), dtype=np.uint16)
+    rc = lib.oracle_attention_q(1 if p.dtype == "bf16" else 0, KV_KIND[p.kv_quant], N, B, nh, kvh, hs, nblk, bs, mb,
+                                int(q.shape[1]), _ptr(q), _ptr(_c(key_cache, np.uint8)),
+                                _ptr(_c(value_cache, np.uint8)), _ptr(_c(p.k_scale, np.float32)),
+                                _ptr(_c(p.v_scale, np.float32)), _ptr(_c(p.cumulative_sequence_length, np.int32)),
+                                _ptr(_c(p.past_seqlens, np.int32)), _ptr(_c(p.block_table, np.int32)),
+                                float(p.scale), _ptr(out), _ptr(lse), _ptr(bits), nthreads)
+    if rc:
+        raise OracleError(rc)
+    return out, lse, bits
+
+
+def attention_rows_q(p, key_cache, value_cache, tokens, heads, nthreads: int = 0):
+    """attention_q for selected (token, head) pairs only. Returns (out (n, hs), lse (n,))."""
+    lib = _load()
+    N, B, nh, kvh, hs, nblk, bs, mb = _dims(p)
+    q = _c(p.query, np.uint16)
+    tokens = _c(tokens, np.int32)
+    heads = _c(heads, np.int32)
+    n = int(tokens.shape[0])
+    out = np.zeros((n, hs), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    rc = lib.oracle_attention_rows_q(1 if p.dtype == "bf16" else 0, KV_KIND[p.kv_quant], N, B, nh, kvh, hs, nblk,
+                                     bs, mb, int(q.shape[1]), _ptr(q), _ptr(_c(key_cache, np.uint8)),
+                                     _ptr(_c(value_cache, np.uint8)), _ptr(_c(p.k_scale, np.float32)),
+                                     _ptr(_c(p.v_scale, np.float32)),
+                                     _ptr(_c(p.cumulative_sequence_length, np.int32)),
+                                     _ptr(_c(p.past_seqlens, np.int32)), _ptr(_c(p.block_table, np.int32)),
+                                     float(p.scale), n, _ptr(tokens), _ptr(heads), _ptr(out), _ptr(lse), nthreads)
+    if rc:
+        raise OracleError(rc)
+    return out, lse
+
+
 def paged_attention(p, nthreads: int = 0, prep=None, gate=None):
     """The whole operator: returns dict(key_cache, value_cache, out, lse, out_bits). With
     `prep`, the query and key rows are prepared (RMSNorm, rotary embedding) first; with
-    `gate` (bits, (N, nh*hs)), the output is multiplied by sigmoid(gate) before rounding."""
+    `gate` (bits, (N, nh*hs)), the output is multiplied by sigmoid(gate) before rounding.
+    An integer-cache problem (p.kv_quant) quantizes this call's K and V rows with its
+    scales, writes the codes and attends over code * scale."""
     if prep is not None:
         p = apply_qk_prep(p, prep)
-    kc, vc = scatter(p)
-    out, lse, bits = attention(p, kc, vc, nthreads)
+    if p.kv_quant is not None:
+        kr, vr = kv_rows(p)
+        kvh, hs = int(p.kv_num_heads), int(p.head_size)
+        kq = quantize_rows(kr, p.dtype, p.kv_quant, kvh, hs, p.k_scale)
+        vq = quantize_rows(vr, p.dtype, p.kv_quant, kvh, hs, p.v_scale)
+        kc, vc = scatter_codes(p, kq, vq)
+        out, lse, bits = attention_q(p, kc, vc, nthreads)
+    else:
+        kc, vc = scatter(p)
+        out, lse, bits = attention(p, kc, vc, nthreads)
     if gate is not None:
         out, b = apply_gate(out, gate, p.dtype)
         bits = b.reshape(bits.shape)

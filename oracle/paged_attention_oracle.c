@@ -136,17 +136,13 @@ static int check_batch(int32_t N, int32_t B, int32_t nh, int32_t kvh, int32_t hs
 
 /* ---- step 1: cache write -------------------------------------------------------- */
 
-int oracle_scatter(int32_t N, int32_t B, int32_t nh, int32_t kvh, int32_t hs, int32_t num_blocks,
-                   int32_t bs, int32_t max_blocks, const uint16_t* query, const uint16_t* key,
-                   const uint16_t* value, uint16_t* key_cache, uint16_t* value_cache,
-                   const int32_t* cum, const int32_t* past, const int32_t* block_table,
-                   const int32_t* slot_mapping) {
-  int rc = check_batch(N, B, nh, kvh, hs, num_blocks, bs, max_blocks, cum, past);
-  if (rc) return rc;
-  const int64_t row = (int64_t)kvh * hs;              /* one token's K (or V) row */
+/* The cache slot of every new token (-1: write suppressed), checked: a slot outside the
+ * cache, two tokens writing one slot, or a block_table entry outside the pool for a
+ * derived slot are errors. */
+static int resolve_slots(int32_t B, int32_t num_blocks, int32_t bs, int32_t max_blocks, const int32_t* cum,
+                         const int32_t* past, const int32_t* block_table, const int32_t* slot_mapping,
+                         int64_t* slots) {
   const int64_t nslots = (int64_t)num_blocks * bs;
-  const int packed = key == NULL;
-  const int64_t qw = packed ? (int64_t)(nh + 2 * kvh) * hs : (int64_t)nh * hs;
   unsigned char* used = (unsigned char*)calloc(nslots > 0 ? (size_t)nslots : 1, 1);
   if (!used) return ORACLE_NO_MEMORY;
   for (int b = 0; b < B; ++b) {
@@ -160,36 +156,153 @@ int oracle_scatter(int32_t N, int32_t B, int32_t nh, int32_t kvh, int32_t hs, in
         if (blk < 0 || blk >= num_blocks) { free(used); return ORACLE_BAD_BLOCK; }
         slot = blk * bs + p % bs;
       }
+      slots[i] = slot;
       if (slot == -1) continue;                                 /* write suppressed */
       if (slot < 0 || slot >= nslots) { free(used); return ORACLE_BAD_SLOT; }
       if (used[slot]) { free(used); return ORACLE_DUPLICATE_SLOT; }
       used[slot] = 1;
-      const uint16_t* k_src = packed ? query + i * qw + (int64_t)nh * hs : key + i * row;
-      const uint16_t* v_src = packed ? query + i * qw + (int64_t)(nh + kvh) * hs : value + i * row;
-      /* cache[slot / bs][slot % bs][:][:] is the contiguous row at flat slot index */
-      memcpy(key_cache + slot * row, k_src, (size_t)row * 2);
-      memcpy(value_cache + slot * row, v_src, (size_t)row * 2);
     }
   }
   free(used);
   return ORACLE_OK;
 }
 
+int oracle_scatter(int32_t N, int32_t B, int32_t nh, int32_t kvh, int32_t hs, int32_t num_blocks,
+                   int32_t bs, int32_t max_blocks, const uint16_t* query, const uint16_t* key,
+                   const uint16_t* value, uint16_t* key_cache, uint16_t* value_cache,
+                   const int32_t* cum, const int32_t* past, const int32_t* block_table,
+                   const int32_t* slot_mapping) {
+  int rc = check_batch(N, B, nh, kvh, hs, num_blocks, bs, max_blocks, cum, past);
+  if (rc) return rc;
+  const int64_t row = (int64_t)kvh * hs;              /* one token's K (or V) row */
+  const int packed = key == NULL;
+  const int64_t qw = packed ? (int64_t)(nh + 2 * kvh) * hs : (int64_t)nh * hs;
+  int64_t* slots = (int64_t*)malloc((size_t)(N > 0 ? N : 1) * sizeof(int64_t));
+  if (!slots) return ORACLE_NO_MEMORY;
+  rc = resolve_slots(B, num_blocks, bs, max_blocks, cum, past, block_table, slot_mapping, slots);
+  for (int64_t i = 0; i < N && !rc; ++i) {
+    const int64_t slot = slots[i];
+    if (slot == -1) continue;
+    const uint16_t* k_src = packed ? query + i * qw + (int64_t)nh * hs : key + i * row;
+    const uint16_t* v_src = packed ? query + i * qw + (int64_t)(nh + kvh) * hs : value + i * row;
+    /* cache[slot / bs][slot % bs][:][:] is the contiguous row at flat slot index */
+    memcpy(key_cache + slot * row, k_src, (size_t)row * 2);
+    memcpy(value_cache + slot * row, v_src, (size_t)row * 2);
+  }
+  free(slots);
+  return rc;
+}
+
+/* ---- INT8 / INT4 per-channel KV cache -------------------------------------------------
+ * An extension: the Mobius issue ("Add Qwen3.8 packed hybrid PagedAttention export for ORT
+ * GenAI Engine", its scope list) asks for an INT8/INT4 per-channel paged KV cache with
+ * calibrated scale loading and gives no format. Reading: the caches hold integer codes;
+ * K and V each come with a caller-given fp32 scale per (KV head, channel), fixed by
+ * calibration; symmetric, no zero point. A value x of T is stored as
+ *   code = min(max(rint(fl32(x) / s), -Q), Q),   Q = 127 (INT8) or 7 (INT4),
+ * the fp32 quotient correctly rounded, rint rounding half to even (a NaN quotient gives
+ * -Q: max(NaN, -Q) is -Q), and attention reads the value code * s, formed in fp64.
+ * INT8 codes are bytes, two's complement; INT4 codes are packed two per byte, channel 2i
+ * in the low nibble and 2i + 1 in the high nibble, two's complement. Slots, -1, the read
+ * path and the attention are the operator's, on those values.
+ */
+static int quant_code(float x, float s, int qmax) {
+  float r = rintf(x / s);
+  r = fmaxf(r, (float)-qmax);
+  r = fminf(r, (float)qmax);
+  return (int)r;
+}
+
+/* n rows of kvh * hs values of type T (row i at x + i * x_stride) to code rows: INT8
+ * (kind 1) kvh * hs bytes, INT4 (kind 2) kvh * hs / 2 bytes per row. */
+int oracle_quantize_rows(int dtype, int kind, int64_t n, int32_t kvh, int32_t hs, const uint16_t* x,
+                         int64_t x_stride, const float* scale, uint8_t* codes) {
+  if (n < 0 || kvh <= 0 || hs <= 0 || (kind != 1 && kind != 2) || (kind == 2 && hs % 2)) return ORACLE_BAD_SHAPE;
+  double* tab = make_table(dtype);
+  if (!tab) return ORACLE_NO_MEMORY;
+  const int qmax = kind == 1 ? 127 : 7;
+  const int64_t rb = kind == 1 ? (int64_t)kvh * hs : (int64_t)kvh * hs / 2;  /* bytes per code row */
+  memset(codes, 0, (size_t)(n * rb));
+  for (int64_t i = 0; i < n; ++i)
+    for (int32_t g = 0; g < kvh; ++g)
+      for (int32_t d = 0; d < hs; ++d) {
+        const float v = (float)tab[x[i * x_stride + (int64_t)g * hs + d]];  /* exact: T is inside fp32 */
+        const int code = quant_code(v, scale[(int64_t)g * hs + d], qmax);
+        if (kind == 1) {
+          codes[i * rb + (int64_t)g * hs + d] = (uint8_t)(int8_t)code;
+        } else {
+          uint8_t* byte = codes + i * rb + ((int64_t)g * hs + d) / 2;
+          *byte |= (uint8_t)((code & 0x0F) << ((d & 1) ? 4 : 0));
+        }
+      }
+  free(tab);
+  return ORACLE_OK;
+}
+
+/* The cache write for code caches: the code rows (row_bytes each, token i's K at
+ * k_codes + i * row_bytes) copied to their slots. */
+int oracle_scatter_codes(int32_t N, int32_t B, int32_t num_blocks, int32_t bs, int32_t max_blocks,
+                         int64_t row_bytes, const uint8_t* k_codes, const uint8_t* v_codes, uint8_t* key_cache,
+                         uint8_t* value_cache, const int32_t* cum, const int32_t* past, const int32_t* block_table,
+                         const int32_t* slot_mapping) {
+  if (N < 0 || B < 0 || num_blocks < 0 || bs <= 0 || max_blocks < 0 || row_bytes <= 0) return ORACLE_BAD_SHAPE;
+  if (cum[0] != 0 || cum[B] != N) return ORACLE_BAD_CUM;
+  for (int b = 0; b < B; ++b) {
+    if (cum[b + 1] < cum[b] || past[b] < 0) return ORACLE_BAD_CUM;
+    if (((int64_t)past[b] + (cum[b + 1] - cum[b]) + bs - 1) / bs > max_blocks) return ORACLE_TOO_LONG;
+  }
+  int64_t* slots = (int64_t*)malloc((size_t)(N > 0 ? N : 1) * sizeof(int64_t));
+  if (!slots) return ORACLE_NO_MEMORY;
+  int rc = resolve_slots(B, num_blocks, bs, max_blocks, cum, past, block_table, slot_mapping, slots);
+  for (int64_t i = 0; i < N && !rc; ++i) {
+    if (slots[i] == -1) continue;
+    memcpy(key_cache + slots[i] * row_bytes, k_codes + i * row_bytes, (size_t)row_bytes);
+    memcpy(value_cache + slots[i] * row_bytes, v_codes + i * row_bytes, (size_t)row_bytes);
+  }
+  free(slots);
+  return rc;
+}
+
 /* ---- step 2: attention for one (token, head) ----------------------------------- */
+
+/* Where attention reads K or V: a cache of 16-bit values of type T (value table tab), or a
+ * cache of integer codes with a per-(KV head, channel) fp32 scale (the quantized caches
+ * below; kind 1 = INT8, 2 = INT4). */
+typedef struct {
+  int kind;
+  const uint16_t* bits;  /* kind 0 */
+  const double* tab;
+  const uint8_t* codes;  /* kinds 1, 2 */
+  const float* scale;    /* (kvh, hs) */
+} KvView;
+
+/* the INT4 code of channel d in a row of packed codes: channel 2i in the low nibble of
+ * byte i, 2i+1 in the high nibble, two's complement */
+static int int4_code(const uint8_t* row, int32_t d) {
+  int nib = (d & 1) ? row[d / 2] >> 4 : row[d / 2] & 0x0F;
+  return nib >= 8 ? nib - 16 : nib;
+}
+
+/* the value attention reads for channel d of KV head g in flat cache row `row` */
+static double kv_value(const KvView* v, int64_t row, int32_t g, int32_t kvh, int32_t hs, int32_t d) {
+  if (v->kind == 0) return v->tab[v->bits[(row * kvh + g) * hs + d]];
+  const double s = (double)v->scale[(int64_t)g * hs + d];
+  if (v->kind == 1) return (double)(int8_t)v->codes[(row * kvh + g) * hs + d] * s;
+  return (double)int4_code(v->codes + (row * kvh + g) * (hs / 2), d) * s;
+}
 
 /* Attention of packed query row i (sequence b, position j in it) for head h. rows[t] is
  * the flat cache row of logical key t. Writes hs outputs and the lse. scores is
  * scratch of at least past_b + j + 1 doubles. */
 static void attend_one(const double* tab, const uint16_t* query, int64_t qw, int32_t i, int32_t h,
                        int32_t g, int32_t kvh, int32_t hs, int64_t limit, const int64_t* rows,
-                       const uint16_t* key_cache, const uint16_t* value_cache, double scale,
-                       double* scores, double* out, double* lse) {
+                       const KvView* kv_k, const KvView* kv_v, double scale, double* scores, double* out,
+                       double* lse) {
   const uint16_t* q = query + (int64_t)i * qw + (int64_t)h * hs;
   double m = -INFINITY;
   for (int64_t t = 0; t <= limit; ++t) {
-    const uint16_t* k = key_cache + (rows[t] * kvh + g) * hs;
     double dot = 0.0;
-    for (int d = 0; d < hs; ++d) dot += tab[q[d]] * tab[k[d]];
+    for (int d = 0; d < hs; ++d) dot += tab[q[d]] * kv_value(kv_k, rows[t], g, kvh, hs, d);
     scores[t] = scale * dot;
     if (scores[t] > m) m = scores[t];
   }
@@ -198,8 +311,7 @@ static void attend_one(const double* tab, const uint16_t* query, int64_t qw, int
   for (int64_t t = 0; t <= limit; ++t) {
     double w = exp(scores[t] - m);
     den += w;
-    const uint16_t* v = value_cache + (rows[t] * kvh + g) * hs;
-    for (int d = 0; d < hs; ++d) out[d] += w * tab[v[d]];
+    for (int d = 0; d < hs; ++d) out[d] += w * kv_value(kv_v, rows[t], g, kvh, hs, d);
   }
   for (int d = 0; d < hs; ++d) out[d] /= den;
   *lse = m + log(den);
@@ -220,18 +332,14 @@ static double resolve_scale(float scale, int32_t hs) {
   return scale == 0.0f ? 1.0 / sqrt((double)hs) : (double)scale;
 }
 
-/* Attention for every packed row and head. out: N x nh x hs doubles; lse: N x nh;
- * out_bits (optional): N x nh x hs 16-bit results rounded once. The caches passed in
- * are the ones after the cache write. nthreads <= 0: the OpenMP default. */
-int oracle_attention(int dtype, int32_t N, int32_t B, int32_t nh, int32_t kvh, int32_t hs,
-                     int32_t num_blocks, int32_t bs, int32_t max_blocks, int32_t query_width,
-                     const uint16_t* query, const uint16_t* key_cache, const uint16_t* value_cache,
-                     const int32_t* cum, const int32_t* past, const int32_t* block_table, float scale,
-                     double* out, double* lse, uint16_t* out_bits, int nthreads) {
-  int rc = check_batch(N, B, nh, kvh, hs, num_blocks, bs, max_blocks, cum, past);
-  if (rc) return rc;
-  double* tab = make_table(dtype);
-  if (!tab) return ORACLE_NO_MEMORY;
+/* Attention for every packed row and head, K and V read through the views. out: N x nh x
+ * hs doubles; lse: N x nh; out_bits (optional): N x nh x hs 16-bit results rounded once.
+ * The caches are the ones after the cache write. nthreads <= 0: the OpenMP default. */
+static int attention_all(int dtype, int32_t B, int32_t nh, int32_t kvh, int32_t hs,
+                         int32_t num_blocks, int32_t bs, int32_t max_blocks, int32_t query_width,
+                         const uint16_t* query, const double* tab, const KvView* kv_k, const KvView* kv_v,
+                         const int32_t* cum, const int32_t* past, const int32_t* block_table, float scale,
+                         double* out, double* lse, uint16_t* out_bits, int nthreads) {
   const int32_t G = nh / kvh;
   const double sc = resolve_scale(scale, hs);
   int err = ORACLE_OK;
@@ -256,8 +364,8 @@ int oracle_attention(int dtype, int32_t N, int32_t B, int32_t nh, int32_t kvh, i
         for (int32_t j = 0; j < q_len; ++j) {
           int32_t i = cum[b] + j;
           double* o = out + ((int64_t)i * nh + h) * hs;
-          attend_one(tab, query, query_width, i, h, h / G, kvh, hs, (int64_t)past[b] + j, rows,
-                     key_cache, value_cache, sc, scores, o, lse + (int64_t)i * nh + h);
+          attend_one(tab, query, query_width, i, h, h / G, kvh, hs, (int64_t)past[b] + j, rows, kv_k, kv_v, sc,
+                     scores, o, lse + (int64_t)i * nh + h);
           if (out_bits)
             for (int d = 0; d < hs; ++d)
               out_bits[((int64_t)i * nh + h) * hs + d] =
@@ -268,26 +376,18 @@ int oracle_attention(int dtype, int32_t N, int32_t B, int32_t nh, int32_t kvh, i
       free(scores);
     }
   }
-  free(tab);
   return err;
 }
 
 /* The same attention for a list of (token, head) pairs only: out n_sel x hs, lse n_sel.
  * Lets large workloads be checked on sampled outputs. */
-int oracle_attention_rows(int dtype, int32_t N, int32_t B, int32_t nh, int32_t kvh, int32_t hs,
-                          int32_t num_blocks, int32_t bs, int32_t max_blocks, int32_t query_width,
-                          const uint16_t* query, const uint16_t* key_cache,
-                          const uint16_t* value_cache, const int32_t* cum, const int32_t* past,
-                          const int32_t* block_table, float scale, int32_t n_sel,
-                          const int32_t* sel_token, const int32_t* sel_head, double* out,
-                          double* lse, int nthreads) {
-  int rc = check_batch(N, B, nh, kvh, hs, num_blocks, bs, max_blocks, cum, past);
-  if (rc) return rc;
+static int attention_sel(int32_t N, int32_t nh, int32_t kvh, int32_t hs, int32_t num_blocks,
+                         int32_t bs, int32_t max_blocks, int32_t query_width, const uint16_t* query,
+                         const double* tab, const KvView* kv_k, const KvView* kv_v, const int32_t* cum,
+                         const int32_t* past, const int32_t* block_table, float scale, int32_t n_sel,
+                         const int32_t* sel_token, const int32_t* sel_head, double* out, double* lse, int nthreads) {
   for (int32_t s = 0; s < n_sel; ++s)
-    if (sel_token[s] < 0 || sel_token[s] >= N || sel_head[s] < 0 || sel_head[s] >= nh)
-      return ORACLE_BAD_SHAPE;
-  double* tab = make_table(dtype);
-  if (!tab) return ORACLE_NO_MEMORY;
+    if (sel_token[s] < 0 || sel_token[s] >= N || sel_head[s] < 0 || sel_head[s] >= nh) return ORACLE_BAD_SHAPE;
   const int32_t G = nh / kvh;
   const double sc = resolve_scale(scale, hs);
   int err = ORACLE_OK;
@@ -310,14 +410,84 @@ int oracle_attention_rows(int dtype, int32_t N, int32_t B, int32_t nh, int32_t k
 #pragma omp atomic write
       err = ORACLE_BAD_BLOCK;
     } else {
-      attend_one(tab, query, query_width, i, h, h / G, kvh, hs, L - 1, rows, key_cache,
-                 value_cache, sc, scores, out + (int64_t)s * hs, lse + s);
+      attend_one(tab, query, query_width, i, h, h / G, kvh, hs, L - 1, rows, kv_k, kv_v, sc, scores,
+                 out + (int64_t)s * hs, lse + s);
     }
     free(rows);
     free(scores);
   }
-  free(tab);
   return err;
+}
+
+/* Attention over 16-bit caches of type T (see attention_all). */
+int oracle_attention(int dtype, int32_t N, int32_t B, int32_t nh, int32_t kvh, int32_t hs,
+                     int32_t num_blocks, int32_t bs, int32_t max_blocks, int32_t query_width,
+                     const uint16_t* query, const uint16_t* key_cache, const uint16_t* value_cache,
+                     const int32_t* cum, const int32_t* past, const int32_t* block_table, float scale,
+                     double* out, double* lse, uint16_t* out_bits, int nthreads) {
+  int rc = check_batch(N, B, nh, kvh, hs, num_blocks, bs, max_blocks, cum, past);
+  if (rc) return rc;
+  double* tab = make_table(dtype);
+  if (!tab) return ORACLE_NO_MEMORY;
+  const KvView vk = {0, key_cache, tab, NULL, NULL}, vv = {0, value_cache, tab, NULL, NULL};
+  rc = attention_all(dtype, B, nh, kvh, hs, num_blocks, bs, max_blocks, query_width, query, tab, &vk, &vv, cum,
+                     past, block_table, scale, out, lse, out_bits, nthreads);
+  free(tab);
+  return rc;
+}
+
+int oracle_attention_rows(int dtype, int32_t N, int32_t B, int32_t nh, int32_t kvh, int32_t hs,
+                          int32_t num_blocks, int32_t bs, int32_t max_blocks, int32_t query_width,
+                          const uint16_t* query, const uint16_t* key_cache,
+                          const uint16_t* value_cache, const int32_t* cum, const int32_t* past,
+                          const int32_t* block_table, float scale, int32_t n_sel,
+                          const int32_t* sel_token, const int32_t* sel_head, double* out,
+                          double* lse, int nthreads) {
+  int rc = check_batch(N, B, nh, kvh, hs, num_blocks, bs, max_blocks, cum, past);
+  if (rc) return rc;
+  double* tab = make_table(dtype);
+  if (!tab) return ORACLE_NO_MEMORY;
+  const KvView vk = {0, key_cache, tab, NULL, NULL}, vv = {0, value_cache, tab, NULL, NULL};
+  rc = attention_sel(N, nh, kvh, hs, num_blocks, bs, max_blocks, query_width, query, tab, &vk, &vv, cum, past,
+                     block_table, scale, n_sel, sel_token, sel_head, out, lse, nthreads);
+  free(tab);
+  return rc;
+}
+
+/* Attention over code caches (kind 1 INT8, 2 INT4) with their fp32 scales (kvh, hs). */
+int oracle_attention_q(int dtype, int kind, int32_t N, int32_t B, int32_t nh, int32_t kvh, int32_t hs,
+                       int32_t num_blocks, int32_t bs, int32_t max_blocks, int32_t query_width, const uint16_t* query,
+                       const uint8_t* key_codes, const uint8_t* value_codes, const float* k_scale,
+                       const float* v_scale, const int32_t* cum, const int32_t* past, const int32_t* block_table,
+                       float scale, double* out, double* lse, uint16_t* out_bits, int nthreads) {
+  if ((kind != 1 && kind != 2) || (kind == 2 && hs % 2)) return ORACLE_BAD_SHAPE;
+  int rc = check_batch(N, B, nh, kvh, hs, num_blocks, bs, max_blocks, cum, past);
+  if (rc) return rc;
+  double* tab = make_table(dtype);
+  if (!tab) return ORACLE_NO_MEMORY;
+  const KvView vk = {kind, NULL, NULL, key_codes, k_scale}, vv = {kind, NULL, NULL, value_codes, v_scale};
+  rc = attention_all(dtype, B, nh, kvh, hs, num_blocks, bs, max_blocks, query_width, query, tab, &vk, &vv, cum, past,
+                     block_table, scale, out, lse, out_bits, nthreads);
+  free(tab);
+  return rc;
+}
+
+int oracle_attention_rows_q(int dtype, int kind, int32_t N, int32_t B, int32_t nh, int32_t kvh, int32_t hs,
+                            int32_t num_blocks, int32_t bs, int32_t max_blocks, int32_t query_width,
+                            const uint16_t* query, const uint8_t* key_codes, const uint8_t* value_codes,
+                            const float* k_scale, const float* v_scale, const int32_t* cum, const int32_t* past,
+                            const int32_t* block_table, float scale, int32_t n_sel, const int32_t* sel_token,
+                            const int32_t* sel_head, double* out, double* lse, int nthreads) {
+  if ((kind != 1 && kind != 2) || (kind == 2 && hs % 2)) return ORACLE_BAD_SHAPE;
+  int rc = check_batch(N, B, nh, kvh, hs, num_blocks, bs, max_blocks, cum, past);
+  if (rc) return rc;
+  double* tab = make_table(dtype);
+  if (!tab) return ORACLE_NO_MEMORY;
+  const KvView vk = {kind, NULL, NULL, key_codes, k_scale}, vv = {kind, NULL, NULL, value_codes, v_scale};
+  rc = attention_sel(N, nh, kvh, hs, num_blocks, bs, max_blocks, query_width, query, tab, &vk, &vv, cum, past,
+                     block_table, scale, n_sel, sel_token, sel_head, out, lse, nthreads);
+  free(tab);
+  return rc;
 }
 
 int oracle_max_threads(void) {

@@ -12,6 +12,7 @@ import pytest
 import oracle
 import test_oracle_pins as pins
 import test_oracle_prep_pins as prep_pins
+import test_oracle_quant_pins as qpins
 
 MUTANTS = [
     ("GQA head mapping h % kvh instead of h / G", "h / G", "h % kvh"),
@@ -26,13 +27,14 @@ MUTANTS = [
      "query + i * qw + (int64_t)(nh - 1) * hs : key"),
     ("-1 slots not skipped", "if (slot == -1) continue;", ""),
     ("rounding truncates", "if (rem > half || (rem == half && (kept & 1))) kept += 1;", ""),
-    ("PV unweighted", "out[d] += w * tab[v[d]];", "out[d] += tab[v[d]];"),
+    ("PV unweighted", "out[d] += w * kv_value(kv_v, rows[t], g, kvh, hs, d);",
+     "out[d] += kv_value(kv_v, rows[t], g, kvh, hs, d);"),
     ("normalisation dropped", "for (int d = 0; d < hs; ++d) out[d] /= den;", ""),
     ("fp16 exponent bias off by one", "ldexp((double)(m | 0x400), e - 25)", "ldexp((double)(m | 0x400), e - 24)"),
     ("bf16 decoded as the low half", "int sign = (h >> 15) & 1, e = (h >> 7) & 0xFF, m = h & 0x7F;",
      "int sign = (h >> 15) & 1, e = (h >> 6) & 0xFF, m = h & 0x3F;"),
-    ("V read from the K cache", "const uint16_t* v = value_cache + (rows[t] * kvh + g) * hs;",
-     "const uint16_t* v = key_cache + (rows[t] * kvh + g) * hs;"),
+    ("V read from the K cache", "vv = {0, value_cache, tab, NULL, NULL};\n  rc = attention_all(",
+     "vv = {0, key_cache, tab, NULL, NULL};\n  rc = attention_all("),
     ("rotation sign flipped", "y[u] = a * ca[u] - b * sa[u];", "y[u] = a * ca[u] + b * sa[u];"),
     ("rotation pairs neighbours", "const double a = y[u], b = y[u + d / 2];\n    y[u] = a * ca[u] - b * sa[u];\n    y[u + d / 2] = b * ca[u] + a * sa[u];",
      "if (2 * u + 1 >= d) continue;\n    const double a = y[2 * u], b = y[2 * u + 1];\n    y[2 * u] = a * ca[u] - b * sa[u];\n    y[2 * u + 1] = b * ca[u] + a * sa[u];"),
@@ -44,6 +46,19 @@ MUTANTS = [
      "const int64_t pos = (int64_t)(i - cum[lo]);"),
     ("gate sign flipped", "gated[i] = out[i] / (1.0 + exp(-tab[gate[i]]));", "gated[i] = out[i] / (1.0 + exp(tab[gate[i]]));"),
     ("gate without the one", "gated[i] = out[i] / (1.0 + exp(-tab[gate[i]]));", "gated[i] = out[i] / exp(-tab[gate[i]]);"),
+    ("quantization truncates", "float r = rintf(x / s);", "float r = truncf(x / s);"),
+    ("quantization multiplies by the scale", "float r = rintf(x / s);", "float r = rintf(x * s);"),
+    ("quantization clamps one past Q", "r = fmaxf(r, (float)-qmax);", "r = fmaxf(r, (float)(-qmax - 1));"),
+    ("quantization with KV head 0's scales", "scale[(int64_t)g * hs + d], qmax)", "scale[d], qmax)"),
+    ("INT4 written high nibble first", "((d & 1) ? 4 : 0)", "((d & 1) ? 0 : 4)"),
+    ("INT4 read high nibble first", "int nib = (d & 1) ? row[d / 2] >> 4 : row[d / 2] & 0x0F;",
+     "int nib = (d & 1) ? row[d / 2] & 0x0F : row[d / 2] >> 4;"),
+    ("INT4 read without the sign", "return nib >= 8 ? nib - 16 : nib;", "return nib;"),
+    ("INT8 read unsigned", "(double)(int8_t)v->codes[", "(double)v->codes["),
+    ("dequantized with KV head 0's scales", "const double s = (double)v->scale[(int64_t)g * hs + d];",
+     "const double s = (double)v->scale[d];"),
+    ("V codes written into the K cache", "memcpy(value_cache + slots[i] * row_bytes, v_codes",
+     "memcpy(value_cache + slots[i] * row_bytes, k_codes"),
 ]
 
 # a fast battery of pins (each raises on failure)
@@ -68,6 +83,21 @@ BATTERY = [
     lambda: prep_pins.test_single_component_rotates_into_its_half_partner(7),
     lambda: prep_pins.test_gate_closed_forms("fp16"),
     lambda: prep_pins.test_gate_symmetry(),
+    lambda: qpins.test_exact_multiples_give_their_integer("int8", "fp16"),
+    lambda: qpins.test_exact_multiples_give_their_integer("int4", "bf16"),
+    lambda: qpins.test_halfway_values_round_to_even("int8"),
+    lambda: qpins.test_saturation_zero_and_nan("int8"),
+    lambda: qpins.test_saturation_zero_and_nan("int4"),
+    lambda: qpins.test_quantization_matches_numpy_float32("int8", "bf16"),
+    lambda: qpins.test_quantization_matches_numpy_float32("int4", "fp16"),
+    lambda: qpins.test_int4_nibble_order_by_hand(),
+    lambda: qpins.test_int8_bytes_by_hand(),
+    lambda: qpins.test_attention_equals_the_16bit_operator_on_exact_values("int8", "fp16"),
+    lambda: qpins.test_attention_equals_the_16bit_operator_on_exact_values("int4", "bf16"),
+    lambda: qpins.test_one_key_returns_its_dequantized_value("int8"),
+    lambda: qpins.test_one_key_returns_its_dequantized_value("int4"),
+    lambda: qpins.test_scores_use_the_k_scale_of_each_channel("int4"),
+    lambda: qpins.test_cache_write_places_code_rows_and_skips_dropped_slots("int8"),
 ]
 
 

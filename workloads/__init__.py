@@ -32,6 +32,10 @@ _lib = None
 
 # stream ids (one per drawn array)
 S_PAST, S_QLEN, S_PAGES, S_QUERY, S_KEY, S_VALUE, S_KCACHE, S_VCACHE, S_DROP, S_ORDER = range(1, 11)
+S_KSCALE, S_VSCALE = 11, 12
+
+# integer KV caches: the largest code magnitude of each format (symmetric codes)
+KV_QMAX = {"int8": 127, "int4": 7}
 
 DTYPE_CODE = {"fp16": 0, "bf16": 1}
 
@@ -105,6 +109,21 @@ def uniform_int(seed: int, stream: int, n: int, lo: int, hi: int) -> np.ndarray:
     return (lo + np.floor(u * (hi - lo + 1))).astype(np.int64).clip(lo, hi)
 
 
+def code_bytes(seed: int, stream: int, shape, fmt: str) -> np.ndarray:
+    """Seeded contents of an integer cache of `shape` (..., hs) values: codes uniform in
+    [-qmax, qmax], as bytes: int8 one two's complement byte per value, int4 two values per
+    byte (even channel in the low nibble), shape (..., hs / 2)."""
+    qm = KV_QMAX[fmt]
+    n = int(np.prod(shape))
+    nbytes = n if fmt == "int8" else n // 2
+    raw = u64(seed, stream, (nbytes + 7) // 8).view(np.uint8)[:nbytes].astype(np.int32)
+    if fmt == "int8":
+        return ((raw % (2 * qm + 1)) - qm).astype(np.int8).view(np.uint8).reshape(shape)
+    lo = ((raw & 0x0F) % (2 * qm + 1)) - qm
+    hi = ((raw >> 4) % (2 * qm + 1)) - qm
+    return ((lo & 0x0F) | ((hi & 0x0F) << 4)).astype(np.uint8).reshape(tuple(shape[:-1]) + (shape[-1] // 2,))
+
+
 def permutation(seed: int, stream: int, n: int) -> np.ndarray:
     """A seeded permutation of range(n): stable argsort of n 64-bit draws."""
     return np.argsort(u64(seed, stream, n), kind="stable").astype(np.int64)
@@ -134,6 +153,13 @@ class Problem:
     scale: float = 0.0
     seed: int = 0
     notes: dict = field(default_factory=dict)
+    # integer KV caches: "int8" | "int4" | None (caches of type T). With a format the caches
+    # hold code bytes, uint8 (num_blocks, block_size, kvh, hs) for int8 and
+    # (num_blocks, block_size, kvh, hs / 2) for int4 (channel 2i in the low nibble), and
+    # k_scale / v_scale are the fp32 per-(KV head, channel) scales (kvh, hs).
+    kv_quant: Optional[str] = None
+    k_scale: Optional[np.ndarray] = None
+    v_scale: Optional[np.ndarray] = None
 
     @property
     def batch_size(self) -> int:
@@ -180,6 +206,7 @@ def make_problem(
     max_blocks_per_sequence: Optional[int] = None,
     table_fill: str = "pad",         # "pad": -1 after the active pages | "perm": all entries distinct ids
     scale: float = 0.0,
+    kv_quant: Optional[str] = None,  # "int8" | "int4": integer caches with per-channel scales
 ) -> Problem:
     past = np.asarray(past, dtype=np.int64)
     q_lens = np.asarray(q_lens, dtype=np.int64)
@@ -222,8 +249,18 @@ def make_problem(
     if not packed:
         key = draw(S_KEY, (N, kvh * hs))
         value = draw(S_VALUE, (N, kvh * hs))
-    kc = draw(S_KCACHE, (num_blocks, bs, kvh, hs))
-    vc = draw(S_VCACHE, (num_blocks, bs, kvh, hs))
+    k_scale = v_scale = None
+    if kv_quant is None:
+        kc = draw(S_KCACHE, (num_blocks, bs, kvh, hs))
+        vc = draw(S_VCACHE, (num_blocks, bs, kvh, hs))
+    else:
+        kc = code_bytes(seed, S_KCACHE, (num_blocks, bs, kvh, hs), kv_quant)
+        vc = code_bytes(seed, S_VCACHE, (num_blocks, bs, kvh, hs), kv_quant)
+        # calibrated scales: a per-channel range of 2..4 (the draws are N(0, 1)) over the
+        # largest code
+        qm = KV_QMAX[kv_quant]
+        k_scale = ((2.0 + 2.0 * uniform(seed, S_KSCALE, kvh * hs)) / qm).astype(np.float32).reshape(kvh, hs)
+        v_scale = ((2.0 + 2.0 * uniform(seed, S_VSCALE, kvh * hs)) / qm).astype(np.float32).reshape(kvh, hs)
 
     slot = None
     if slot_mode == "explicit":
@@ -241,6 +278,7 @@ def make_problem(
         num_blocks=num_blocks, past_seqlens=past.astype(np.int32), q_lens=q_lens.astype(np.int32),
         cumulative_sequence_length=cum, block_table=bt, query=query, key=key, value=value,
         key_cache=kc, value_cache=vc, slot_mapping=slot, scale=scale, seed=seed,
+        kv_quant=kv_quant, k_scale=k_scale, v_scale=v_scale,
     )
 
 
