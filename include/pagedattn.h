@@ -32,7 +32,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 4
+#define PA_ABI_VERSION 5
 
 typedef enum pa_status {
   PA_OK = 0,
@@ -46,6 +46,26 @@ typedef enum pa_dtype {
   PA_FLOAT16 = 0,
   PA_BFLOAT16 = 1
 } pa_dtype;
+
+/*
+ * Element type of the two caches (pa_dims.kv_dtype). PA_KV_SAME: T, as in the operator
+ * statement. The integer formats are an extension (the Mobius issue's scope list asks for an
+ * INT8/INT4 per-channel paged KV cache with calibrated scale loading; no page gives a
+ * format): the caches hold integer codes, and K and V each come with a caller-given fp32
+ * scale per (KV head, channel), pa_extensions.k_scale / v_scale, fixed by calibration;
+ * symmetric, no zero point. This call's K and V rows (of T) are stored as
+ *   code = min(max(rint(fl32(x) / s), -Q), Q)   (IEEE fp32 quotient, rint half to even)
+ * with Q = 127 (PA_KV_INT8: one two's complement byte per value) or 7 (PA_KV_INT4: two
+ * values per byte, channel 2i in the low nibble, 2i + 1 in the high nibble, two's
+ * complement), and attention reads the value code * s. A cache is then
+ * (num_blocks, block_size, kv_num_heads, head_size) bytes for INT8 and
+ * (num_blocks, block_size, kv_num_heads, head_size / 2) bytes for INT4.
+ */
+typedef enum pa_kv_dtype {
+  PA_KV_SAME = 0,
+  PA_KV_INT8 = 1,
+  PA_KV_INT4 = 2
+} pa_kv_dtype;
 
 /* Bits of the device error word (pa_read_device_error). */
 #define PA_DEVERR_BAD_BATCH 1u  /* cumulative_sequence_length / past_seqlens inconsistent: nothing was computed or written */
@@ -77,6 +97,9 @@ typedef struct pa_dims {
                                       PA_DEVERR_BAD_BATCH. */
   int32_t qk_prep;                 /* non-zero: calls pass a pa_qk_prep, and the workspace also holds the
                                       prepared query rows (num_tokens * num_heads * head_size values of T) */
+  int32_t kv_dtype;                /* pa_kv_dtype of the caches: INT8 with head_size 64, 128 or 256,
+                                      INT4 with 128 or 256 (else PA_ERR_UNSUPPORTED); integer caches
+                                      need pa_paged_attention_ex with both scales */
 } pa_dims;
 
 /*
@@ -242,6 +265,9 @@ typedef struct pa_extensions {
                                  rounding (the sigmoid-gated output of Qwen3.5's full-attention layers,
                                  "Add Qwen3.8 packed hybrid PagedAttention export for ORT GenAI Engine");
                                  lse is not gated */
+  const float* k_scale;       /* fp32 (kv_num_heads, head_size), 16-byte aligned: the K scales of integer
+                                 caches (dims->kv_dtype != PA_KV_SAME), finite and positive; NULL otherwise */
+  const float* v_scale;       /* the same for V */
 } pa_extensions;
 
 /* pa_paged_attention with the extensions in `ext` (NULL: none). */

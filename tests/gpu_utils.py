@@ -30,14 +30,24 @@ def upload(p):
         query=to_dev(p.query, p.dtype),
         key=None if p.key is None else to_dev(p.key, p.dtype),
         value=None if p.value is None else to_dev(p.value, p.dtype),
-        key_cache=to_dev(p.key_cache, p.dtype),
-        value_cache=to_dev(p.value_cache, p.dtype),
+        key_cache=to_dev(p.key_cache, p.dtype) if p.kv_quant is None else torch.from_numpy(
+            np.ascontiguousarray(p.key_cache, dtype=np.uint8)).to(device="cuda"),
+        value_cache=to_dev(p.value_cache, p.dtype) if p.kv_quant is None else torch.from_numpy(
+            np.ascontiguousarray(p.value_cache, dtype=np.uint8)).to(device="cuda"),
         cumulative_sequence_length=idx_dev(p.cumulative_sequence_length),
         past_seqlens=idx_dev(p.past_seqlens),
         block_table=idx_dev(p.block_table),
         slot_mapping=idx_dev(p.slot_mapping),
     )
+    if p.kv_quant is not None:  # integer caches: their per-channel scales
+        d["k_scale"] = torch.from_numpy(np.ascontiguousarray(p.k_scale, dtype=np.float32)).cuda()
+        d["v_scale"] = torch.from_numpy(np.ascontiguousarray(p.v_scale, dtype=np.float32)).cuda()
     return d
+
+
+def cache_bytes(t: torch.Tensor) -> np.ndarray:
+    """A cache's contents as the oracle holds them: 16-bit bits, or code bytes."""
+    return t.cpu().numpy() if t.dtype == torch.uint8 else bits_of(t)
 
 
 def run_gpu(p, *, decode_split_keys=0, route=pa.ROUTE_AUTO, dev=None):

@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.pa_abi_version() == 4
+    assert lib.pa_abi_version() == 5
     for code in range(5):
         assert lib.pa_status_string(code)
     assert lib.pa_status_string(99) == b"unknown status"
@@ -93,6 +93,30 @@ def test_lse_entry_point_checks_before_any_launch(lib):
     assert call(p(FAKE + 2)) == 1                                         # misaligned lse
     assert call(p(FAKE), pa.make_dims(64, 64, 80, 607, 256, 17, torch.float16)) == 2   # head_size
     assert call(p(FAKE), pa.make_dims(0, 0, 128, 607, 256, 17, torch.float16)) == 0   # nothing to do
+
+
+def test_integer_cache_checks_before_any_launch(lib):
+    p = ctypes.c_void_p
+    dec = dict(max_query_len=1)  # decode-only: integer caches run on the decode kernel
+
+    def dims(hs=128, fmt=pa.KV_INT8, **kw):
+        return pa.make_dims(64, 64, hs, 607, 256, 17, torch.float16, kv_dtype=fmt, **{**dec, **kw})
+
+    def call(d, k_scale=FAKE, v_scale=FAKE):
+        ext = pa.PaExtensions(None, None, None, k_scale, v_scale)
+        ws = max(lib.pa_workspace_size(ctypes.byref(d), 32, 8), 1 << 20)
+        return lib.pa_paged_attention_ex(p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE),
+                                         None, 32, 8, 0.0, p(FAKE), ctypes.byref(ext), ctypes.byref(d), p(FAKE), ws,
+                                         None)
+    assert pa.workspace_size(dims(), 32, 8) > pa.workspace_size(dims(fmt=pa.KV_SAME), 32, 8)  # scaled Q rows
+    assert pa.workspace_size(dims(hs=64, fmt=pa.KV_INT4), 32, 8) == 0    # INT4 needs head_size 128 or 256
+    assert pa.workspace_size(dims(fmt=3), 32, 8) == 0                    # unknown format
+    assert pa.workspace_size(dims(max_query_len=0), 32, 8) == 0          # prefill possible
+    assert pa.workspace_size(dims(max_query_len=5), 32, 8) == 0          # 5 * 4 rows > 16
+    assert call(dims(hs=64, fmt=pa.KV_INT4)) == 2
+    assert call(dims(), k_scale=None) == 1                               # scales required
+    assert call(dims(), v_scale=FAKE + 4) == 1                           # misaligned scale
+    assert call(dims(fmt=pa.KV_SAME)) == 1                               # scales without integer caches
 
 
 def test_python_binding_refuses_cpu_tensors(lib):

@@ -1,0 +1,153 @@
+"""INT8 / INT4 per-channel KV caches on the decode kernel, through the C ABI against the
+oracle (oracle_quantize_rows, oracle_attention_q; pinned in test_oracle_quant_pins.py).
+
+The cache write quantizes this call's K and V rows with the same rule as the oracle (IEEE
+fp32 quotient, rint half to even, clamp), so the code caches must match bit for bit. The
+attention reads the codes as exact fp16 integers, folds the K scales into an fp16 copy of
+the query rows (with a power-of-two row exponent) and the V scales into the output, so the
+outputs must meet the usual bound |gpu - oracle| <= 2e-3 + 1e-2 |oracle|, and lse its
+5e-4 + 1e-5 |oracle| widened by the scores' error bound of the fp16 scaled query rows
+(score_error_bound: relative 2^-11 per product term).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import varlen_paged_kv_gb300 as pa
+import workloads as w
+from gpu_utils import TORCH_DT, assert_close, bits_of, cache_bytes, upload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA is required for the gpu tests")
+    from varlen_paged_kv_gb300 import build
+    build.build()
+
+
+CASES = {
+    # name: (fmt, dtype, nh, kvh, hs, bs, past, q_lens, packed, drops)
+    "int8-gqa4-fp16": ("int8", "fp16", 32, 8, 128, 256, [0, 5, 300, 1000], [1, 1, 2, 4], False, 0),
+    "int8-gqa8-bf16-pages16": ("int8", "bf16", 16, 2, 128, 16, [4000, 17, 1], [1, 2, 1], False, 0),
+    "int8-mha-q16-hs64": ("int8", "fp16", 8, 8, 64, 32, [100, 33], [16, 7], False, 0),
+    "int8-hs256-bf16": ("int8", "bf16", 16, 2, 256, 64, [700, 3000, 0], [1, 2, 1], False, 0),
+    "int8-packed-drops": ("int8", "fp16", 32, 8, 128, 64, [900, 50, 3000, 7], [1, 2, 4, 3], True, 3),
+    "int4-gqa4-fp16": ("int4", "fp16", 32, 8, 128, 256, [0, 5, 300, 1000], [1, 1, 2, 4], False, 0),
+    "int4-gqa16-bf16": ("int4", "bf16", 16, 1, 128, 64, [500, 1, 2500], [1, 1, 1], False, 0),
+    "int4-hs256-fp16": ("int4", "fp16", 16, 2, 256, 32, [129, 63, 1], [2, 1, 1], False, 0),
+    "int4-packed-drops-bf16": ("int4", "bf16", 32, 8, 128, 16, [60, 4, 2000], [2, 4, 1], True, 2),
+}
+
+
+def _problem(name, seed=31):
+    fmt, dt, nh, kvh, hs, bs, past, q, packed, drops = CASES[name]
+    return w.make_problem(name=name, seed=seed, dtype=dt, num_heads=nh, kv_num_heads=kvh, head_size=hs,
+                          block_size=bs, past=past, q_lens=q, packed=packed,
+                          slot_mode="explicit" if drops else "omitted", drop_count=drops, kv_quant=fmt)
+
+
+def _run(p, split=0, **kw):
+    d = upload(p)
+    lse = torch.empty((p.num_tokens, p.num_heads), dtype=torch.float32, device="cuda")
+    dims = pa.make_dims(p.num_tokens, p.batch_size, p.head_size, p.num_blocks, p.block_size,
+                        p.max_blocks_per_sequence, TORCH_DT[p.dtype], split, pa.ROUTE_AUTO, int(p.q_lens.max()),
+                        "qk_prep" in kw, p.kv_quant)
+    ws = torch.zeros(pa.workspace_size(dims, p.num_heads, p.kv_num_heads), dtype=torch.uint8, device="cuda")
+    out = pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
+                             d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], d["slot_mapping"],
+                             num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, scale=p.scale, workspace=ws,
+                             decode_split_keys=split, max_query_len=int(p.q_lens.max()), lse=lse,
+                             kv_quant=p.kv_quant, k_scale=d["k_scale"], v_scale=d["v_scale"], **kw)
+    assert pa.read_device_error(ws) == 0
+    return d, out, lse
+
+
+def _codes(raw, fmt, hs):
+    """Integer codes (..., hs) of a code cache (..., row bytes)."""
+    if fmt == "int8":
+        return raw.view(np.int8).astype(np.float64)
+    c = np.stack([raw & 15, raw >> 4], axis=-1).reshape(raw.shape[:-1] + (hs,)).astype(np.int64)
+    return np.where(c >= 8, c - 16, c).astype(np.float64)
+
+
+def score_error_bound(p, key_cache):
+    """Per (row, head): the scores' error from the fp16 scaled query rows, an fp16 rounding
+    (relative 2^-11) of every term q_c * s_c: scale * 2^-11 * max_t sum_c |q_c k_tc|."""
+    nh, kvh, hs, bs = p.num_heads, p.kv_num_heads, p.head_size, p.block_size
+    k = _codes(key_cache, p.kv_quant, hs).reshape(-1, kvh, hs) * p.k_scale[None].astype(np.float64)
+    q = (oracle.bf16_to_double if p.dtype == "bf16" else oracle.f16_to_double)(p.query[:, :nh * hs])
+    q = np.abs(q.reshape(-1, nh, hs))
+    sc = p.scale if p.scale else 1.0 / np.sqrt(hs)
+    out = np.zeros((p.num_tokens, nh))
+    for b in range(p.batch_size):
+        c0, past = int(p.cumulative_sequence_length[b]), int(p.past_seqlens[b])
+        for j in range(int(p.q_lens[b])):
+            keys = np.arange(past + j + 1)
+            rows = p.block_table[b, keys // bs].astype(np.int64) * bs + keys % bs
+            kk = np.abs(k[rows])  # (L, kvh, hs)
+            for h in range(nh):
+                out[c0 + j, h] = sc * 2.0 ** -11 * np.max(kk[:, h // (nh // kvh)] @ q[c0 + j, h])
+    return out
+
+
+def _check(p, ref, d, out, lse, exact_codes=True, prepared=None):
+    kc, vc = cache_bytes(d["key_cache"]), cache_bytes(d["value_cache"])
+    assert np.array_equal(vc, ref["value_cache"]), "value codes differ"
+    if exact_codes:
+        assert np.array_equal(kc, ref["key_cache"]), "key codes differ"
+    assert_close(bits_of(out).reshape(p.num_tokens, p.num_heads, p.head_size), ref["out"], p.dtype, p.name)
+    lg = lse.cpu().numpy().astype(np.float64)
+    bound = 5e-4 + 1e-5 * np.abs(ref["lse"]) + score_error_bound(prepared or p, ref["key_cache"])
+    assert np.all(np.abs(lg - ref["lse"]) <= bound), "lse differs"
+
+
+@pytest.mark.parametrize("split", [0, 64])
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_integer_cache_decode(name, split):
+    p = _problem(name)
+    ref = oracle.paged_attention(p)
+    d, out, lse = _run(p, split)
+    _check(p, ref, d, out, lse)
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int4"])
+def test_integer_cache_with_prep_and_gate(fmt):
+    p = w.make_problem(name="q-prep", seed=33, dtype="bf16", num_heads=16, kv_num_heads=2, head_size=128,
+                       block_size=64, past=[100, 2000, 7], q_lens=[1, 2, 1], kv_quant=fmt)
+    to_t = oracle.double_to_bf16
+    prep_bits = dict(q_norm_weight=to_t(np.linspace(0.5, 1.5, 128)), k_norm_weight=to_t(np.linspace(1.2, 0.8, 128)),
+                     eps=1e-6, rotary_dim=64, theta=1.0e6)
+    gate_bits = to_t(w.uniform(34, 1, p.num_tokens * 16 * 128) * 8.0 - 4.0).reshape(p.num_tokens, 16 * 128)
+    ref = oracle.paged_attention(p, prep=prep_bits, gate=gate_bits)
+    dev = lambda b: torch.from_numpy(b.view(np.int16)).cuda().view(torch.bfloat16)
+    prep = dict(q_norm_weight=dev(prep_bits["q_norm_weight"]), k_norm_weight=dev(prep_bits["k_norm_weight"]),
+                eps=1e-6, rotary_dim=64, theta=1.0e6)
+    d, out, lse = _run(p, qk_prep=prep, output_gate=dev(gate_bits))
+    _check(p, ref, d, out, lse, exact_codes=False, prepared=oracle.apply_qk_prep(p, prep_bits))
+    # prepared keys are computed in fp32 here and in fp64 by the oracle, then rounded to T:
+    # where the two roundings differ the code may differ by one
+    kc = cache_bytes(d["key_cache"]).reshape(-1)
+    rk = ref["key_cache"].reshape(-1)
+    if fmt == "int8":
+        a, b = kc.view(np.int8).astype(int), rk.view(np.int8).astype(int)
+    else:
+        a = np.stack([(kc & 15), (kc >> 4)]).astype(int)
+        b = np.stack([(rk & 15), (rk >> 4)]).astype(int)
+        a, b = np.where(a >= 8, a - 16, a), np.where(b >= 8, b - 16, b)
+    assert np.all(np.abs(a - b) <= 1) and np.mean(a != b) < 0.01
+
+
+def test_integer_cache_needs_a_decode_bound():
+    p = _problem("int8-gqa4-fp16")
+    d = upload(p)
+    with pytest.raises(pa.PagedAttentionError) as e:
+        pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
+                           d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], d["slot_mapping"],
+                           num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, kv_quant="int8",
+                           k_scale=d["k_scale"], v_scale=d["v_scale"],
+                           workspace=torch.zeros(1 << 20, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == 2

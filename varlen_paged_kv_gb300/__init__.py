@@ -26,6 +26,8 @@ DEVERR_BAD_BATCH, DEVERR_BAD_BLOCK, DEVERR_BAD_SLOT, DEVERR_TIMEOUT = 1, 2, 4, 8
 _STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARGUMENT", 2: "PA_ERR_UNSUPPORTED",
            3: "PA_ERR_WORKSPACE_TOO_SMALL", 4: "PA_ERR_CUDA"}
 _DTYPES = {torch.float16: 0, torch.bfloat16: 1}
+KV_SAME, KV_INT8, KV_INT4 = 0, 1, 2
+_KV_FORMATS = {None: KV_SAME, "int8": KV_INT8, "int4": KV_INT4}
 
 _lib = None
 
@@ -42,7 +44,8 @@ class PagedAttentionError(RuntimeError):
 class PaDims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_tokens", "batch_size", "head_size", "num_blocks", "block_size",
-        "max_blocks_per_sequence", "dtype", "decode_split_keys", "route", "max_query_len", "qk_prep")]
+        "max_blocks_per_sequence", "dtype", "decode_split_keys", "route", "max_query_len", "qk_prep",
+        "kv_dtype")]
 
 
 class PaQkPrep(ctypes.Structure):
@@ -52,7 +55,8 @@ class PaQkPrep(ctypes.Structure):
 
 
 class PaExtensions(ctypes.Structure):
-    _fields_ = [("lse", ctypes.c_void_p), ("qk_prep", ctypes.POINTER(PaQkPrep)), ("output_gate", ctypes.c_void_p)]
+    _fields_ = [("lse", ctypes.c_void_p), ("qk_prep", ctypes.POINTER(PaQkPrep)), ("output_gate", ctypes.c_void_p),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
 
 
 def load_library():
@@ -91,11 +95,11 @@ def load_library():
 
 
 def make_dims(num_tokens, batch_size, head_size, num_blocks, block_size, max_blocks_per_sequence, dtype,
-              decode_split_keys=0, route=ROUTE_AUTO, max_query_len=0, qk_prep=False) -> PaDims:
+              decode_split_keys=0, route=ROUTE_AUTO, max_query_len=0, qk_prep=False, kv_dtype=KV_SAME) -> PaDims:
     code = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
     return PaDims(int(num_tokens), int(batch_size), int(head_size), int(num_blocks), int(block_size),
                   int(max_blocks_per_sequence), code, int(decode_split_keys), int(route), int(max_query_len),
-                  int(bool(qk_prep)))
+                  int(bool(qk_prep)), int(_KV_FORMATS.get(kv_dtype, kv_dtype)))
 
 
 def workspace_size(dims: PaDims, num_heads: int, kv_num_heads: int) -> int:
@@ -130,7 +134,8 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
                     decode_split_keys: int = 0, route: int = ROUTE_AUTO, max_query_len: int = 0,
                     stages: int = STAGE_ALL, stream: Optional[torch.cuda.Stream] = None,
                     lse: Optional[torch.Tensor] = None, qk_prep: Optional[dict] = None,
-                    output_gate: Optional[torch.Tensor] = None) -> torch.Tensor:
+                    output_gate: Optional[torch.Tensor] = None, kv_quant: Optional[str] = None,
+                    k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None) -> torch.Tensor:
     """com.microsoft.PagedAttention on CUDA tensors. Writes key_cache / value_cache in
     place and returns ``output`` (num_tokens, num_heads * head_size).
 
@@ -143,13 +148,32 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
     RMSNorm of the query and key heads, then the rotary embedding at each row's position,
     before the cache write (pa_qk_prep).
     ``output_gate`` (optional, whole calls only, shape and dtype of the output): the output is
-    multiplied by sigmoid(output_gate) elementwise before the final rounding."""
+    multiplied by sigmoid(output_gate) elementwise before the final rounding.
+    ``kv_quant`` (optional, whole calls only): "int8" or "int4" integer caches (uint8 tensors
+    (num_blocks, block_size, kv_num_heads, head_size), or head_size / 2 for int4) with the
+    float32 (kv_num_heads, head_size) per-channel scales ``k_scale`` and ``v_scale``: this
+    call's K and V rows are stored as codes, attention reads code * scale."""
     lib = load_library()
     if query.dtype not in _DTYPES:
         raise TypeError("query must be float16 or bfloat16")
-    for name, t in (("key", key), ("value", value), ("key_cache", key_cache), ("value_cache", value_cache)):
+    if kv_quant not in _KV_FORMATS:
+        raise ValueError("kv_quant must be None, 'int8' or 'int4'")
+    cache_dtype = query.dtype if kv_quant is None else torch.uint8
+    for name, t in (("key", key), ("value", value)):
         if t is not None and t.dtype != query.dtype:
             raise TypeError(f"{name} must have the dtype of query")
+    for name, t in (("key_cache", key_cache), ("value_cache", value_cache)):
+        if t.dtype != cache_dtype:
+            raise TypeError(f"{name} must be {cache_dtype}")
+    head_size = key_cache.shape[3] * (2 if kv_quant == "int4" else 1)
+    if kv_quant is not None:
+        if stages != STAGE_ALL:
+            raise ValueError("integer caches apply to whole calls only")
+        for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+            if t is None or t.dtype != torch.float32 or tuple(t.shape) != (kv_num_heads, head_size):
+                raise ValueError(f"{name} must be float32 (kv_num_heads, head_size)")
+    elif k_scale is not None or v_scale is not None:
+        raise ValueError("k_scale / v_scale need integer caches (kv_quant)")
     for name, t in (("cumulative_sequence_length", cumulative_sequence_length), ("past_seqlens", past_seqlens),
                     ("block_table", block_table), ("slot_mapping", slot_mapping)):
         if t is not None and t.dtype != torch.int32:
@@ -160,7 +184,7 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
         if stages != STAGE_ALL:
             raise ValueError("lse is exported by whole calls only")
     if output_gate is not None:
-        if output_gate.dtype != query.dtype or output_gate.numel() != query.shape[0] * num_heads * key_cache.shape[3]:
+        if output_gate.dtype != query.dtype or output_gate.numel() != query.shape[0] * num_heads * head_size:
             raise ValueError("output_gate must have the output's shape and dtype")
         if stages != STAGE_ALL:
             raise ValueError("output_gate applies to whole calls only")
@@ -170,7 +194,7 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
             raise ValueError("qk_prep applies to whole calls only")
         for k in ("q_norm_weight", "k_norm_weight"):
             t = qk_prep.get(k)
-            if t is not None and (t.dtype != query.dtype or t.numel() != key_cache.shape[3] or not t.is_cuda or
+            if t is not None and (t.dtype != query.dtype or t.numel() != head_size or not t.is_cuda or
                                   not t.is_contiguous()):
                 raise ValueError(f"{k} must be a contiguous CUDA tensor of head_size values of the query dtype")
         def addr(t):
@@ -179,31 +203,34 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
                         float(qk_prep.get("eps", 1e-6)), float(qk_prep.get("theta", 10000.0)),
                         int(qk_prep.get("rotary_dim", 0)), 0)
     for t in (query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
-              slot_mapping, output, workspace, lse, output_gate):
+              slot_mapping, output, workspace, lse, output_gate, k_scale, v_scale):
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError("all tensors must be contiguous CUDA tensors")
     N = query.shape[0]
     B = past_seqlens.shape[0]
-    num_blocks, block_size, kvh_c, head_size = key_cache.shape
+    num_blocks, block_size, kvh_c = key_cache.shape[:3]
     if kvh_c != kv_num_heads or value_cache.shape != key_cache.shape:
-        raise ValueError("cache shape must be (num_blocks, block_size, kv_num_heads, head_size)")
+        raise ValueError("cache shape must be (num_blocks, block_size, kv_num_heads, head_size) "
+                         "(head_size / 2 bytes for int4)")
     width = (num_heads + 2 * kv_num_heads) * head_size if key is None else num_heads * head_size
     if query.shape[1] != width:
         raise ValueError(f"query rows must have {width} elements")
     if cumulative_sequence_length.shape[0] != B + 1 or block_table.shape[0] != B:
         raise ValueError("cumulative_sequence_length must have batch_size + 1 entries, block_table batch_size rows")
     dims = make_dims(N, B, head_size, num_blocks, block_size, block_table.shape[1], query.dtype,
-                     decode_split_keys, route, max_query_len, qk_prep is not None)
+                     decode_split_keys, route, max_query_len, qk_prep is not None, _KV_FORMATS[kv_quant])
     if output is None:
         output = torch.empty((N, num_heads * head_size), dtype=query.dtype, device=query.device)
     if workspace is None:
         ws = lib.pa_workspace_size(ctypes.byref(dims), num_heads, kv_num_heads)
         workspace = torch.empty(max(int(ws), 256), dtype=torch.uint8, device=query.device)
     s = (stream or torch.cuda.current_stream(query.device)).cuda_stream
-    if prep is not None or output_gate is not None:
+    if prep is not None or output_gate is not None or kv_quant is not None:
         ext = PaExtensions(None if lse is None else lse.data_ptr(),
                            ctypes.pointer(prep) if prep is not None else None,
-                           None if output_gate is None else output_gate.data_ptr())
+                           None if output_gate is None else output_gate.data_ptr(),
+                           None if k_scale is None else k_scale.data_ptr(),
+                           None if v_scale is None else v_scale.data_ptr())
         st = lib.pa_paged_attention_ex(
             _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
             _ptr(cumulative_sequence_length), _ptr(past_seqlens), _ptr(block_table), _ptr(slot_mapping),
@@ -226,5 +253,5 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
     return output
 
 
-__all__ = ["paged_attention", "workspace_size", "make_dims", "PaQkPrep", "PaExtensions", "read_device_error", "kernel_launch_count",
+__all__ = ["KV_SAME", "KV_INT8", "KV_INT4", "paged_attention", "workspace_size", "make_dims", "PaQkPrep", "PaExtensions", "read_device_error", "kernel_launch_count",
            "load_library", "PagedAttentionError", "PaDims", "LIBRARY_PATH"]

@@ -108,6 +108,12 @@ pa_status check_dims(const pa_dims* d, int32_t nh, int32_t kvh) {
   if (d->block_size <= 0 || d->head_size <= 0) return PA_ERR_INVALID_ARGUMENT;
   if (d->dtype != PA_FLOAT16 && d->dtype != PA_BFLOAT16) return PA_ERR_UNSUPPORTED;
   if (d->head_size != 64 && d->head_size != 128 && d->head_size != 256) return PA_ERR_UNSUPPORTED;
+  if (d->kv_dtype != PA_KV_SAME && d->kv_dtype != PA_KV_INT8 && d->kv_dtype != PA_KV_INT4) return PA_ERR_UNSUPPORTED;
+  if (d->kv_dtype == PA_KV_INT4 && d->head_size == 64) return PA_ERR_UNSUPPORTED;
+  // integer caches run on the decode kernel: the call must prove every sequence decode-class
+  if (d->kv_dtype != PA_KV_SAME && (d->route != PA_ROUTE_AUTO || d->max_query_len <= 0 ||
+                                    (int64_t)d->max_query_len * (nh / kvh) > pa::kDecRows))
+    return PA_ERR_UNSUPPORTED;
   if (d->block_size % 16 != 0) return PA_ERR_UNSUPPORTED;
   if (d->route != PA_ROUTE_AUTO && d->route != PA_ROUTE_ALL_PREFILL) return PA_ERR_INVALID_ARGUMENT;
   if (d->decode_split_keys < 0 || d->decode_split_keys % pa::kDecTile != 0) return PA_ERR_INVALID_ARGUMENT;
@@ -134,9 +140,28 @@ int64_t mirror_keys(const pa_dims* d, int32_t nh, int32_t kvh) {
   return std::min<int64_t>(4 * (int64_t)d->num_tokens, (int64_t)d->num_blocks * d->block_size);
 }
 
-// 16-bit values of the prepared query rows the workspace holds (dims->qk_prep)
+// 16-bit values of the prepared (dims->qk_prep) or scaled (integer caches) query rows the
+// workspace holds, and the scaled rows' exponents
 int64_t qprep_values(const pa_dims* d, int32_t nh) {
-  return d->qk_prep ? (int64_t)d->num_tokens * nh * d->head_size : 0;
+  return (d->qk_prep || d->kv_dtype != PA_KV_SAME) ? (int64_t)d->num_tokens * nh * d->head_size : 0;
+}
+int64_t qexp_values(const pa_dims* d, int32_t nh) {
+  return d->kv_dtype != PA_KV_SAME ? (int64_t)d->num_tokens * nh : 0;
+}
+
+// 3-D map over an integer cache viewed as (row bytes, kv_heads, slots), uint8 elements; box =
+// min(row bytes, 128) x 1 x rows with the swizzle of that width
+bool code_cache_map(CUtensorMap* m, void* base, int row_bytes, int kvh, int64_t slots, int rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const int box = row_bytes < 128 ? row_bytes : 128;
+  cuuint64_t dims[3] = {(cuuint64_t)row_bytes, (cuuint64_t)kvh, (cuuint64_t)slots};
+  cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)kvh * row_bytes};
+  cuuint32_t boxd[3] = {(cuuint32_t)box, 1, (cuuint32_t)rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, boxd, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             box == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* kc, void* vc, uint32_t stages,
@@ -168,9 +193,9 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
       if (cudaError_t e = pa::launch_v_mirror(args, (int)vb, stream)) return cuda_fail(e, "v_mirror_kernel launch");
     }
   }
-  // attention reads the prepared query rows when the cache-write stage prepared them
+  // attention reads the prepared (or scaled) query rows when the cache-write stage wrote them
   pa::Args aq = args;
-  if (args.prep) {
+  if (args.prep || args.kvq) {
     aq.query = args.qprep;
     aq.q_stride = args.nh * hs;
     query = args.qprep;
@@ -203,7 +228,12 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
   if ((stages & PA_STAGE_DECODE) && can_decode && args.N > 0 && slots > 0) {
     const int seg = gcd(d->block_size, pa::kDecTile);
     CUtensorMap tk, tv;
-    if (!cache_map(&tk, kc, dt, hs, args.kvh, slots, seg) || !cache_map(&tv, vc, dt, hs, args.kvh, slots, seg)) {
+    const int row_bytes = args.kvq == PA_KV_INT8 ? hs : hs / 2;
+    const bool ok = args.kvq ? code_cache_map(&tk, kc, row_bytes, args.kvh, slots, seg) &&
+                                   code_cache_map(&tv, vc, row_bytes, args.kvh, slots, seg)
+                             : cache_map(&tk, kc, dt, hs, args.kvh, slots, seg) &&
+                                   cache_map(&tv, vc, dt, hs, args.kvh, slots, seg);
+    if (!ok) {
       g_last_error = "cuTensorMapEncodeTiled failed (decode maps)";
       return PA_ERR_CUDA;
     }
@@ -221,7 +251,8 @@ size_t pa_workspace_size(const pa_dims* dims, int32_t num_heads, int32_t kv_num_
   if (check_dims(dims, num_heads, kv_num_heads) != PA_OK) return 0;
   return pa::ws_layout(dims->num_tokens, dims->batch_size, kv_num_heads, dims->head_size,
                        dims->max_blocks_per_sequence, dims->block_size, dims->decode_split_keys,
-                       mirror_keys(dims, num_heads, kv_num_heads), qprep_values(dims, num_heads))
+                       mirror_keys(dims, num_heads, kv_num_heads), qprep_values(dims, num_heads),
+                       qexp_values(dims, num_heads))
       .total;
 }
 
@@ -232,10 +263,15 @@ namespace {
 pa_status run(const void* query, const void* key, const void* value, void* key_cache, void* value_cache,
               const int32_t* cumulative_sequence_length, const int32_t* past_seqlens, const int32_t* block_table,
               const int32_t* slot_mapping, int32_t num_heads, int32_t kv_num_heads, float scale, void* output,
-              float* lse, const pa_qk_prep* prep, const void* gate, const pa_dims* dims, void* workspace,
-              size_t workspace_bytes, void* stream, uint32_t stages) {
+              float* lse, const pa_qk_prep* prep, const void* gate, const float* k_scale, const float* v_scale,
+              const pa_dims* dims, void* workspace, size_t workspace_bytes, void* stream, uint32_t stages) {
   pa_status st = check_dims(dims, num_heads, kv_num_heads);
   if (st != PA_OK) return st;
+  if (dims->kv_dtype != PA_KV_SAME) {
+    if (!k_scale || !v_scale || !aligned(k_scale, 16) || !aligned(v_scale, 16)) return PA_ERR_INVALID_ARGUMENT;
+  } else if (k_scale || v_scale) {
+    return PA_ERR_INVALID_ARGUMENT;
+  }
   if (prep) {
     if (!dims->qk_prep || prep->reserved != 0) return PA_ERR_INVALID_ARGUMENT;
     const int32_t d = prep->rotary_dim, step = dims->head_size / 16;
@@ -263,7 +299,8 @@ pa_status run(const void* query, const void* key, const void* value, void* key_c
   if (dims->max_blocks_per_sequence == 0 || dims->num_blocks == 0) return PA_ERR_INVALID_ARGUMENT;
   const int64_t mkeys = mirror_keys(dims, num_heads, kv_num_heads);
   const pa::WsLayout L = pa::ws_layout(N, B, kv_num_heads, hs, dims->max_blocks_per_sequence, dims->block_size,
-                                       dims->decode_split_keys, mkeys, qprep_values(dims, num_heads));
+                                       dims->decode_split_keys, mkeys, qprep_values(dims, num_heads),
+                                       qexp_values(dims, num_heads));
   if (workspace_bytes < L.total) return PA_ERR_WORKSPACE_TOO_SMALL;
 
   pa::Args a{};
@@ -324,6 +361,13 @@ pa_status run(const void* query, const void* key, const void* value, void* key_c
     for (int u = 0; u < prep->rotary_dim / 2; ++u)
       a.inv_freq[u] = (float)pow((double)prep->rope_theta, -2.0 * u / prep->rotary_dim);
   }
+  if (dims->kv_dtype != PA_KV_SAME) {
+    a.kvq = dims->kv_dtype;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.qprep = reinterpret_cast<uint16_t*>(ws + L.qprep);
+    a.qexp = reinterpret_cast<int32_t*>(ws + L.qexp);
+  }
   a.max_items = L.max_items;
   a.max_tiles = L.max_tiles;
 
@@ -341,8 +385,8 @@ pa_status pa_paged_attention_stages(const void* query, const void* key, const vo
                                     void* output, const pa_dims* dims, void* workspace, size_t workspace_bytes,
                                     void* stream, uint32_t stages) {
   return run(query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
-             slot_mapping, num_heads, kv_num_heads, scale, output, nullptr, nullptr, nullptr, dims, workspace,
-             workspace_bytes, stream, stages);
+             slot_mapping, num_heads, kv_num_heads, scale, output, nullptr, nullptr, nullptr, nullptr, nullptr, dims,
+             workspace, workspace_bytes, stream, stages);
 }
 
 pa_status pa_paged_attention(const void* query, const void* key, const void* value, void* key_cache,
@@ -351,8 +395,8 @@ pa_status pa_paged_attention(const void* query, const void* key, const void* val
                              int32_t num_heads, int32_t kv_num_heads, float scale, void* output,
                              const pa_dims* dims, void* workspace, size_t workspace_bytes, void* stream) {
   return run(query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
-             slot_mapping, num_heads, kv_num_heads, scale, output, nullptr, nullptr, nullptr, dims, workspace,
-             workspace_bytes, stream, PA_STAGE_ALL);
+             slot_mapping, num_heads, kv_num_heads, scale, output, nullptr, nullptr, nullptr, nullptr, nullptr, dims,
+             workspace, workspace_bytes, stream, PA_STAGE_ALL);
 }
 
 pa_status pa_paged_attention_lse(const void* query, const void* key, const void* value, void* key_cache,
@@ -362,8 +406,8 @@ pa_status pa_paged_attention_lse(const void* query, const void* key, const void*
                                  void* output, float* lse, const pa_dims* dims, void* workspace,
                                  size_t workspace_bytes, void* stream) {
   return run(query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
-             slot_mapping, num_heads, kv_num_heads, scale, output, lse, nullptr, nullptr, dims, workspace,
-             workspace_bytes, stream, PA_STAGE_ALL);
+             slot_mapping, num_heads, kv_num_heads, scale, output, lse, nullptr, nullptr, nullptr, nullptr, dims,
+             workspace, workspace_bytes, stream, PA_STAGE_ALL);
 }
 
 pa_status pa_paged_attention_ex(const void* query, const void* key, const void* value, void* key_cache,
@@ -374,8 +418,8 @@ pa_status pa_paged_attention_ex(const void* query, const void* key, const void* 
                                 size_t workspace_bytes, void* stream) {
   return run(query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
              slot_mapping, num_heads, kv_num_heads, scale, output, ext ? ext->lse : nullptr,
-             ext ? ext->qk_prep : nullptr, ext ? ext->output_gate : nullptr, dims, workspace, workspace_bytes, stream,
-             PA_STAGE_ALL);
+             ext ? ext->qk_prep : nullptr, ext ? ext->output_gate : nullptr, ext ? ext->k_scale : nullptr,
+             ext ? ext->v_scale : nullptr, dims, workspace, workspace_bytes, stream, PA_STAGE_ALL);
 }
 
 const char* pa_last_error(void) { return g_last_error; }

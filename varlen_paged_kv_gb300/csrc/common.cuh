@@ -73,7 +73,7 @@ struct __align__(32) PrefillTile {
 
 struct WsLayout {
   size_t header, items, cta_begin, unit_done, tiles, tiles_unsorted, part_o, part_lse, mirror_base, mirror_seq,
-      mirror, qprep, total;
+      mirror, qprep, qexp, total;
   int32_t max_items, max_tiles;
 };
 
@@ -86,10 +86,12 @@ __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + 
 //  - decode items, forced split length S: at most ceil(max_kv / S) per unit;
 //  - prefill tiles: sum_b ceil(q_b / 128) <= N / 128 + B.
 // mirror_keys: rows of the fp16 copy of V that bf16 prefill reads (0: none); qprep_values:
-// 16-bit values of the prepared query rows (0: no Q/K preparation).
+// 16-bit values of the prepared query rows (0: no Q/K preparation and no integer caches);
+// qexp_values: the per-row exponents of the scaled query rows of integer caches (0: none).
 __host__ __device__ inline WsLayout ws_layout(int32_t N, int32_t B, int32_t kvh, int32_t hs,
                                                int32_t max_blocks, int32_t bs, int32_t forced_split,
-                                               int64_t mirror_keys, int64_t qprep_values) {
+                                               int64_t mirror_keys, int64_t qprep_values,
+                                               int64_t qexp_values = 0) {
   WsLayout L;
   const int64_t units = (int64_t)B * kvh;
   int64_t items;
@@ -111,6 +113,7 @@ __host__ __device__ inline WsLayout ws_layout(int32_t N, int32_t B, int32_t kvh,
   L.mirror_seq = off; off = align_up(off + 2 * sizeof(int32_t) * ((size_t)B + 1), 256);
   L.mirror = off; off = align_up(off + (size_t)mirror_keys * kvh * hs * 2, 256);
   L.qprep = off; off = align_up(off + (size_t)qprep_values * 2, 256);
+  L.qexp = off; off = align_up(off + (size_t)qexp_values * 4, 256);
   L.total = off;
   return L;
 }
@@ -138,6 +141,13 @@ struct Args {
   const uint16_t* q_norm_w;
   const uint16_t* k_norm_w;
   uint16_t* qprep;
+  // Integer caches (kvq = 1 INT8, 2 INT4; 0: caches of T): the fp32 (kvh, hs) scales, and
+  // per query row (token, head) the exponent E of its scaled copy: the attention kernels
+  // read Q' = fp16(q * k_scale * 2^-E) from qprep and multiply the scores by 2^E
+  int32_t kvq;
+  const float* k_scale;
+  const float* v_scale;
+  int32_t* qexp;
   float inv_freq[128];   // rotary inverse frequencies, one per rotated pair (rotary_dim / 2 <= 128)
   int32_t N, B, nh, kvh, G, hs, num_blocks, bs, max_blocks;
   int32_t q_stride;       // elements per query row
@@ -173,12 +183,19 @@ struct Args {
 // buffers in order. At head_size 256 (one CTA per SM) there is room for two buffers next to
 // the 3-stage ring (two rounds instead of four); below, two CTAs share an SM and one buffer
 // takes the four warps in turn.
-template <int HS>
+//
+// Integer caches (KQ = 1 INT8, 2 INT4) have rows of HS or HS / 2 bytes, so a stage is half or
+// a quarter of the 16-bit one and the ring is that much deeper (the same bytes in flight).
+// A row is TMA'd in boxes of kBoxBytes (at most 128) with the matching swizzle.
+template <int HS, int KQ = 0>
 struct DecSmem {
-  static constexpr int kStages = kDecStages;
+  static constexpr int kRowBytes = KQ == 0 ? HS * 2 : KQ == 1 ? HS : HS / 2;
+  static constexpr int kBoxBytes = kRowBytes < 128 ? kRowBytes : 128;
+  static constexpr int kBoxes = kRowBytes / kBoxBytes;
+  static constexpr int kStages = KQ == 0 ? kDecStages : KQ == 1 ? 2 * kDecStages : 4 * kDecStages;
   static constexpr int kCombBufs = HS == 256 ? 2 : 1;
   static constexpr int kHalves = HS / 64;
-  static constexpr int kTileBytes = kDecTile * HS * 2;      // one K (or V) tile
+  static constexpr int kTileBytes = kDecTile * kRowBytes;   // one K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kCombStride = HS + 4;                 // floats; the pad spreads rows over banks
   static constexpr int kComb = kStages * kStageBytes;        // float [kCombBufs][16][kCombStride]
@@ -188,7 +205,9 @@ struct DecSmem {
   static constexpr int kAbort = kBars + 2 * kStages * 8;
   static constexpr int kBytes = kAbort + 16 + 1024;          // + alignment slack
 };
-static_assert(DecSmem<256>::kBytes <= 232448 && 2 * (DecSmem<128>::kBytes + 1024) <= 233472,
+static_assert(DecSmem<256>::kBytes <= 232448 && 2 * (DecSmem<128>::kBytes + 1024) <= 233472 &&
+                  DecSmem<256, 1>::kBytes <= 232448 && DecSmem<256, 2>::kBytes <= 232448 &&
+                  2 * (DecSmem<128, 1>::kBytes + 1024) <= 233472 && 2 * (DecSmem<128, 2>::kBytes + 1024) <= 233472,
               "decode shared memory");
 
 // Prefill: Q tile, two K and two V tiles, barriers, the TMEM address slot.
@@ -471,6 +490,67 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x
                ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
                : "memory");
 }
+// ---- integer cache codes to fp16 pairs (exact: the codes are small integers) ---------------
+// A biased code u (INT8: code + 128, INT4: code + 8) placed in the low bits of an fp16 with
+// the bit pattern 0x6400 (1024.0) reads 1024 + u; subtracting 1024 + bias leaves the code.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// (a & mask) | 0x64006400 in one instruction
+__device__ __forceinline__ uint32_t nib_pair_f16(uint32_t a) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(0x000F000Fu), "r"(0x64006400u));
+  return r;
+}
+constexpr uint32_t kF16Magic = 0x64646464u;   // fp16 high bytes 0x64
+constexpr uint32_t kF16Int8Bias = 0x64806480u; // 1152.0 (1024 + 128) in both halves
+constexpr uint32_t kF16Int4Bias = 0x64086408u; // 1032.0 (1024 + 8)
+
+// four INT8 codes (bytes 0..3 of w) as fp16 pairs (byte 0, byte 1) and (byte 2, byte 3)
+__device__ __forceinline__ void s8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x = w ^ 0x80808080u;
+  lo = hsub2_u32(prmt(x, kF16Magic, 0x5140u), kF16Int8Bias);
+  hi = hsub2_u32(prmt(x, kF16Magic, 0x7362u), kF16Int8Bias);
+}
+// byte i of w0 and byte i of w1 (two keys, one channel) as one fp16 pair, i = 0..3
+__device__ __forceinline__ void s8_key_pairs(uint32_t w0, uint32_t w1, uint32_t (&p)[4]) {
+  const uint32_t x0 = w0 ^ 0x80808080u, x1 = w1 ^ 0x80808080u;
+  const uint32_t a = prmt(x0, x1, 0x5140u), b = prmt(x0, x1, 0x7362u);  // interleaved by key
+  p[0] = hsub2_u32(prmt(a, kF16Magic, 0x5140u), kF16Int8Bias);
+  p[1] = hsub2_u32(prmt(a, kF16Magic, 0x7362u), kF16Int8Bias);
+  p[2] = hsub2_u32(prmt(b, kF16Magic, 0x5140u), kF16Int8Bias);
+  p[3] = hsub2_u32(prmt(b, kF16Magic, 0x7362u), kF16Int8Bias);
+}
+// eight INT4 codes (nibble j = channel j of w) as the fp16 pairs (0, 4), (1, 5), (2, 6), (3, 7)
+__device__ __forceinline__ void s4x8_to_f16(uint32_t w, uint32_t (&p)[4]) {
+  const uint32_t x = w ^ 0x88888888u;
+  p[0] = hsub2_u32(nib_pair_f16(x), kF16Int4Bias);
+  p[1] = hsub2_u32(nib_pair_f16(x >> 4), kF16Int4Bias);
+  p[2] = hsub2_u32(nib_pair_f16(x >> 8), kF16Int4Bias);
+  p[3] = hsub2_u32(nib_pair_f16(x >> 12), kF16Int4Bias);
+}
+// channel i of w0 and channel i of w1 (two keys, eight INT4 channels each) as one fp16 pair
+__device__ __forceinline__ void s4_key_pairs(uint32_t w0, uint32_t w1, uint32_t (&p)[8]) {
+  const uint32_t x0 = w0 ^ 0x88888888u, x1 = w1 ^ 0x88888888u;
+  const uint32_t a = prmt(x0, x1, 0x6420u);  // bytes: w0 ch0|1, w0 ch4|5, w1 ch0|1, w1 ch4|5
+  const uint32_t b = prmt(x0, x1, 0x7531u);  // bytes: w0 ch2|3, w0 ch6|7, w1 ch2|3, w1 ch6|7
+  p[0] = hsub2_u32(nib_pair_f16(a), kF16Int4Bias);
+  p[1] = hsub2_u32(nib_pair_f16(a >> 4), kF16Int4Bias);
+  p[4] = hsub2_u32(nib_pair_f16(a >> 8), kF16Int4Bias);
+  p[5] = hsub2_u32(nib_pair_f16(a >> 12), kF16Int4Bias);
+  p[2] = hsub2_u32(nib_pair_f16(b), kF16Int4Bias);
+  p[3] = hsub2_u32(nib_pair_f16(b >> 4), kF16Int4Bias);
+  p[6] = hsub2_u32(nib_pair_f16(b >> 8), kF16Int4Bias);
+  p[7] = hsub2_u32(nib_pair_f16(b >> 12), kF16Int4Bias);
+}
+
 // one 128-byte line of global memory into L2 (a hint: no data returned, no fault)
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");

@@ -75,12 +75,82 @@ __device__ __forceinline__ void load_q(const Args& a, const DecodeItem& item, in
   }
 }
 
-template <int HS, bool BF16>
+// ---- integer caches ------------------------------------------------------------------------
+// Tiles of code rows (P bytes per row in a box, 64 rows per box; 128-byte swizzle for
+// P = 128, 64-byte swizzle for P = 64): the shared address of byte b of row r.
+template <int P>
+__device__ __forceinline__ uint32_t code_addr(uint32_t base, int r, int b) {
+  const int box = b / P, wb = b % P, c = wb >> 4;
+  const int cs = P == 128 ? (c ^ (r & 7)) : (c ^ ((r >> 1) & 3));
+  return base + box * (kDecTile * P) + r * P + (cs << 4) + (wb & 15);
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// The channel order of the MMA operands on integer caches (Q K^T sums over channels and
+// P V keeps each channel's column apart, so any fixed assignment works when Q and the
+// output follow it). Q K^T, INT8: k-step ks, thread tq takes channels 16ks + 4tq .. + 3 (one
+// 32-bit word of a key row) as k = 2tq, 2tq+1 (b0) and 2tq+8, 2tq+9 (b1). INT4: a word holds
+// channels 32k2 + 8tq .. + 7 for the k-steps 2k2 (channels +0/+4 as b0, +1/+5 as b1) and
+// 2k2 + 1 (+2/+6, +3/+7). P V: n-tile d column n is channel 32(d/4) + 4n + d%4 (INT8) or
+// 64(d/8) + 8n + d%8 (INT4), so a thread's word of one key row feeds 4 (8) n-tiles.
+template <int KQ>
+__device__ __forceinline__ int out_channel(int d, int n) {
+  return KQ == 1 ? 32 * (d >> 2) + 4 * n + (d & 3) : 64 * (d >> 3) + 8 * n + (d & 7);
+}
+
+// Q' fragments (the scaled query rows, fp16, in the channel order above) of an item and the
+// softmax constants of its two rows: scale * log2(e) * 2^E (E the row's exponent)
+template <int HS, int KQ>
+__device__ __forceinline__ void load_q_int(const Args& a, const DecodeItem& item, int r0, int r1, int tq,
+                                           uint32_t (&qa)[HS / 16][4], float& c0, float& c1) {
+  const int n_rows = item.q_len * a.G;
+  const uint16_t* q = reinterpret_cast<const uint16_t*>(a.query);
+  const uint16_t* p[2] = {nullptr, nullptr};
+  int ex[2] = {0, 0};
+  const int rr[2] = {r0, r1};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    if (rr[i] < n_rows) {
+      const int64_t row = (int64_t)(item.c0 + rr[i] / a.G) * a.nh + item.g * a.G + rr[i] % a.G;
+      p[i] = q + row * HS;
+      ex[i] = __ldg(a.qexp + row);
+    }
+  }
+  c0 = ldexpf(a.scale_log2, ex[0]);
+  c1 = ldexpf(a.scale_log2, ex[1]);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    if constexpr (KQ == 1) {
+#pragma unroll
+      for (int ks = 0; ks < HS / 16; ++ks) {
+        const uint2 v = p[i] ? __ldg(reinterpret_cast<const uint2*>(p[i] + 16 * ks + 4 * tq)) : make_uint2(0, 0);
+        qa[ks][i] = v.x;
+        qa[ks][2 + i] = v.y;
+      }
+    } else {
+#pragma unroll
+      for (int k2 = 0; k2 < HS / 32; ++k2) {
+        const uint4 v = p[i] ? __ldg(reinterpret_cast<const uint4*>(p[i] + 32 * k2 + 8 * tq)) : make_uint4(0, 0, 0, 0);
+        qa[2 * k2][i] = prmt(v.x, v.z, 0x5410u);
+        qa[2 * k2][2 + i] = prmt(v.x, v.z, 0x7632u);
+        qa[2 * k2 + 1][i] = prmt(v.y, v.w, 0x5410u);
+        qa[2 * k2 + 1][2 + i] = prmt(v.y, v.w, 0x7632u);
+      }
+    }
+  }
+}
+
+template <int HS, bool BF16, int KQ>
 __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
     decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const int seg_rows) {
-  using L = DecSmem<HS>;
+  using L = DecSmem<HS, KQ>;
   constexpr int NKS = HS / 16;  // k-steps of Q K^T
+  constexpr int P = L::kBoxBytes;
   constexpr int ND = HS / 8;    // n-tiles of P V
   constexpr int kCombStride = L::kCombStride;
   extern __shared__ uint8_t smem_raw[];
@@ -151,11 +221,12 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
             if (blk >= 0 && blk < a.num_blocks) z = blk * a.bs + key % a.bs;
             else atomicOr(err, PA_DEVERR_BAD_BLOCK);
           }
-          uint8_t* kdst = smem + s * L::kStageBytes + lane * seg_rows * 128;
+          uint8_t* kdst = smem + s * L::kStageBytes + lane * seg_rows * P;
+          constexpr int kBoxX = KQ == 0 ? P / 2 : P;  // box width in map elements
 #pragma unroll
-          for (int h = 0; h < L::kHalves; ++h) {
-            tma_load_3d(kdst + h * kDecTile * 128, &tmK, &full[s], h * 64, item.g, z);
-            tma_load_3d(kdst + L::kTileBytes + h * kDecTile * 128, &tmV, &full[s], h * 64, item.g, z);
+          for (int h = 0; h < L::kBoxes; ++h) {
+            tma_load_3d(kdst + h * kDecTile * P, &tmK, &full[s], h * kBoxX, item.g, z);
+            tma_load_3d(kdst + L::kTileBytes + h * kDecTile * P, &tmV, &full[s], h * kBoxX, item.g, z);
           }
         }
         __syncwarp();
@@ -176,7 +247,9 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
     const int c0 = item.c0, q_len = item.q_len, past = item.past;
     const int n_rows = q_len * a.G;
     uint32_t qa[NKS][4];
-    load_q<HS>(a, item, r0, r1, tq, qa);
+    float cr0 = a.scale_log2, cr1 = a.scale_log2;  // the two rows' softmax constants
+    if constexpr (KQ == 0) load_q<HS>(a, item, r0, r1, tq, qa);
+    else load_q_int<HS, KQ>(a, item, r0, r1, tq, qa, cr0, cr1);
     // causal limits (inclusive) of the two rows; padding rows borrow the last row's
     const int lim0 = past + min(r0 / a.G, q_len - 1);
     const int lim1 = past + min(r1 / a.G, q_len - 1);
@@ -198,7 +271,7 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
         float sc[2][4];
 #pragma unroll
         for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-        {
+        if constexpr (KQ == 0) {
           const int mi = lane >> 3, rr = lane & 7;
           const int kr = 16 * w + (mi >> 1) * 8 + rr;  // key row inside the tile
 #pragma unroll
@@ -210,6 +283,28 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
             mma16816<BF16>(sc[0], qa[ks], b0, b1);
             mma16816<BF16>(sc[1], qa[ks], b2, b3);
           }
+        } else if constexpr (KQ == 1) {
+          const int kr = 16 * w + gq;  // key rows of the two n-tiles: kr, kr + 8
+#pragma unroll
+          for (int ks = 0; ks < NKS; ++ks) {
+            uint32_t b0, b1, b2, b3;
+            s8x4_to_f16(lds32(code_addr<P>(kb, kr, 16 * ks + 4 * tq)), b0, b1);
+            s8x4_to_f16(lds32(code_addr<P>(kb, kr + 8, 16 * ks + 4 * tq)), b2, b3);
+            mma16816<false>(sc[0], qa[ks], b0, b1);
+            mma16816<false>(sc[1], qa[ks], b2, b3);
+          }
+        } else {
+          const int kr = 16 * w + gq;
+#pragma unroll
+          for (int k2 = 0; k2 < NKS / 2; ++k2) {
+            uint32_t u[4], v[4];
+            s4x8_to_f16(lds32(code_addr<P>(kb, kr, 16 * k2 + 4 * tq)), u);
+            s4x8_to_f16(lds32(code_addr<P>(kb, kr + 8, 16 * k2 + 4 * tq)), v);
+            mma16816<false>(sc[0], qa[2 * k2], u[0], u[1]);
+            mma16816<false>(sc[0], qa[2 * k2 + 1], u[2], u[3]);
+            mma16816<false>(sc[1], qa[2 * k2], v[0], v[1]);
+            mma16816<false>(sc[1], qa[2 * k2 + 1], v[2], v[3]);
+          }
         }
         // ---- online softmax (base 2) ----
         const bool ragged = (k0 + kDecTile > item.key_end) || (k0 + kDecTile - 1 > past);
@@ -218,7 +313,7 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
         for (int n = 0; n < 2; ++n) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            float v = sc[n][e] * a.scale_log2;
+            float v = sc[n][e] * (e < 2 ? cr0 : cr1);
             if (ragged) {
               const int key = kw + n * 8 + tq * 2 + (e & 1);
               const int lim = e < 2 ? lim0 : lim1;
@@ -251,7 +346,7 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
         l1 = l1 * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
         // P as the MMA A fragment; bf16 carries it as hi + lo (two products), fp16 as one
         uint32_t pa[4], pl[4];
-        if constexpr (BF16) {
+        if constexpr (BF16 && KQ == 0) {
           split_bf16x2(p[0][0], p[0][1], pa[0], pl[0]);
           split_bf16x2(p[0][2], p[0][3], pa[1], pl[1]);
           split_bf16x2(p[1][0], p[1][1], pa[2], pl[2]);
@@ -271,13 +366,36 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
         }
         // ---- O (16 x HS) += P (16 x 16) V (16 x HS) ----
         // keys this thread contributes in the transposed V fragments: kw + 2tq + {0,1}, +8
-        uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
-        if (ragged) {  // keys past the item may be unwritten cache slots: keep NaN out of 0 * V
-          const int ka = kw + tq * 2, kb2 = ka + 8;
-          vmask_lo = (ka < item.key_end ? 0x0000ffffu : 0u) | (ka + 1 < item.key_end ? 0xffff0000u : 0u);
-          vmask_hi = (kb2 < item.key_end ? 0x0000ffffu : 0u) | (kb2 + 1 < item.key_end ? 0xffff0000u : 0u);
-        }
-        {
+        if constexpr (KQ == 1) {
+          // (codes are finite: keys past the item contribute 0 * code = 0)
+          const int ka = 16 * w + 2 * tq;  // this thread's keys: ka, ka + 1 (b0), ka + 8, ka + 9 (b1)
+#pragma unroll
+          for (int D = 0; D < HS / 32; ++D) {
+            const int byte = 32 * D + 4 * gq;
+            uint32_t lo[4], hi[4];
+            s8_key_pairs(lds32(code_addr<P>(vb, ka, byte)), lds32(code_addr<P>(vb, ka + 1, byte)), lo);
+            s8_key_pairs(lds32(code_addr<P>(vb, ka + 8, byte)), lds32(code_addr<P>(vb, ka + 9, byte)), hi);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mma16816<false>(o[4 * D + i], pa, lo[i], hi[i]);
+          }
+        } else if constexpr (KQ == 2) {
+          const int ka = 16 * w + 2 * tq;
+#pragma unroll
+          for (int D = 0; D < HS / 64; ++D) {
+            const int byte = 32 * D + 4 * gq;
+            uint32_t lo[8], hi[8];
+            s4_key_pairs(lds32(code_addr<P>(vb, ka, byte)), lds32(code_addr<P>(vb, ka + 1, byte)), lo);
+            s4_key_pairs(lds32(code_addr<P>(vb, ka + 8, byte)), lds32(code_addr<P>(vb, ka + 9, byte)), hi);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mma16816<false>(o[8 * D + i], pa, lo[i], hi[i]);
+          }
+        } else {
+          uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
+          if (ragged) {  // keys past the item may be unwritten cache slots: keep NaN out of 0 * V
+            const int ka = kw + tq * 2, kb2 = ka + 8;
+            vmask_lo = (ka < item.key_end ? 0x0000ffffu : 0u) | (ka + 1 < item.key_end ? 0xffff0000u : 0u);
+            vmask_hi = (kb2 < item.key_end ? 0x0000ffffu : 0u) | (kb2 + 1 < item.key_end ? 0xffff0000u : 0u);
+          }
           const int mi = lane >> 3, rr = lane & 7;
           const int kr = 16 * w + (mi & 1) * 8 + rr;
 #pragma unroll
@@ -330,16 +448,33 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
         if (w / B == rr) {
 #pragma unroll
           for (int d = 0; d < ND; ++d) {
-            float2* c0p = reinterpret_cast<float2*>(cw + r0 * kCombStride + d * 8 + tq * 2);
-            float2* c1p = reinterpret_cast<float2*>(cw + r1 * kCombStride + d * 8 + tq * 2);
-            const float2 a0 = make_float2(o[d][0] * f0, o[d][1] * f0), a1 = make_float2(o[d][2] * f1, o[d][3] * f1);
-            if (rr == 0) {
-              *c0p = a0;
-              *c1p = a1;
-            } else {
-              const float2 b0 = *c0p, b1 = *c1p;
-              *c0p = make_float2(b0.x + a0.x, b0.y + a0.y);
-              *c1p = make_float2(b1.x + a1.x, b1.y + a1.y);
+            if constexpr (KQ == 0) {
+              float2* c0p = reinterpret_cast<float2*>(cw + r0 * kCombStride + d * 8 + tq * 2);
+              float2* c1p = reinterpret_cast<float2*>(cw + r1 * kCombStride + d * 8 + tq * 2);
+              const float2 a0 = make_float2(o[d][0] * f0, o[d][1] * f0), a1 = make_float2(o[d][2] * f1, o[d][3] * f1);
+              if (rr == 0) {
+                *c0p = a0;
+                *c1p = a1;
+              } else {
+                const float2 b0 = *c0p, b1 = *c1p;
+                *c0p = make_float2(b0.x + a0.x, b0.y + a0.y);
+                *c1p = make_float2(b1.x + a1.x, b1.y + a1.y);
+              }
+            } else {  // integer caches: the columns' channels in natural order
+              const int ch0 = out_channel<KQ>(d, 2 * tq), ch1 = out_channel<KQ>(d, 2 * tq + 1);
+              float* c0p = cw + r0 * kCombStride;
+              float* c1p = cw + r1 * kCombStride;
+              if (rr == 0) {
+                c0p[ch0] = o[d][0] * f0;
+                c0p[ch1] = o[d][1] * f0;
+                c1p[ch0] = o[d][2] * f1;
+                c1p[ch1] = o[d][3] * f1;
+              } else {
+                c0p[ch0] += o[d][0] * f0;
+                c0p[ch1] += o[d][1] * f0;
+                c1p[ch0] += o[d][2] * f1;
+                c1p[ch1] += o[d][3] * f1;
+              }
             }
           }
         }
@@ -377,6 +512,10 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
             float x[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = cval(v + e) * inv;
+            if constexpr (KQ != 0) {  // integer caches: the V scales of the output channels
+#pragma unroll
+              for (int e = 0; e < 8; ++e) x[e] *= __ldg(a.v_scale + item.g * HS + col + v + e);
+            }
             if (a.gate)  // output gate: times sigmoid(gate), elementwise
               apply_gate8<BF16>(a.gate + ((int64_t)tok * a.nh + head) * HS + col + v, x);
             uint4 pk;
@@ -437,6 +576,10 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
             float x[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = acc[v + e] * dinv;
+            if constexpr (KQ != 0) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) x[e] *= __ldg(a.v_scale + item.g * HS + col + v + e);
+            }
             if (a.gate) apply_gate8<BF16>(a.gate + ((int64_t)tok * a.nh + head) * HS + col + v, x);
             uint4 pk;
             pk.x = pack2<BF16>(x[0], x[1]);
@@ -453,21 +596,33 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
 }
 
 // ---- host launchers (kernels are launched from the translation unit that defines them) ----
-template <int HS, bool BF16>
+template <int HS, bool BF16, int KQ>
 static cudaError_t launch_decode_t(const Args& a, const CUtensorMap& tk, const CUtensorMap& tv, int seg,
                                    cudaStream_t s) {
-  constexpr int smem = DecSmem<HS>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<HS, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  constexpr int smem = DecSmem<HS, KQ>::kBytes;
+  cudaError_t e =
+      cudaFuncSetAttribute(decode_kernel<HS, BF16, KQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_kernel<HS, BF16>, dim3(a.dec_ctas), dim3(160), smem, s, a, tk, tv, seg);
+  return launch_pdl(decode_kernel<HS, BF16, KQ>, dim3(a.dec_ctas), dim3(160), smem, s, a, tk, tv, seg);
+}
+
+template <int KQ>
+static cudaError_t launch_decode_kq(const Args& a, bool bf16, const CUtensorMap& tk, const CUtensorMap& tv, int seg,
+                                    cudaStream_t s) {
+  if (a.hs == 256)
+    return bf16 ? launch_decode_t<256, true, KQ>(a, tk, tv, seg, s) : launch_decode_t<256, false, KQ>(a, tk, tv, seg, s);
+  if constexpr (KQ != 2) {  // (INT4 needs head_size 128 or 256)
+    if (a.hs == 64)
+      return bf16 ? launch_decode_t<64, true, KQ>(a, tk, tv, seg, s) : launch_decode_t<64, false, KQ>(a, tk, tv, seg, s);
+  }
+  return bf16 ? launch_decode_t<128, true, KQ>(a, tk, tv, seg, s) : launch_decode_t<128, false, KQ>(a, tk, tv, seg, s);
 }
 
 cudaError_t launch_decode(const Args& a, bool bf16, const CUtensorMap& tk, const CUtensorMap& tv, int seg,
                           cudaStream_t s) {
-  if (a.hs == 64) return bf16 ? launch_decode_t<64, true>(a, tk, tv, seg, s) : launch_decode_t<64, false>(a, tk, tv, seg, s);
-  if (a.hs == 256)
-    return bf16 ? launch_decode_t<256, true>(a, tk, tv, seg, s) : launch_decode_t<256, false>(a, tk, tv, seg, s);
-  return bf16 ? launch_decode_t<128, true>(a, tk, tv, seg, s) : launch_decode_t<128, false>(a, tk, tv, seg, s);
+  if (a.kvq == 1) return launch_decode_kq<1>(a, bf16, tk, tv, seg, s);
+  if (a.kvq == 2) return launch_decode_kq<2>(a, bf16, tk, tv, seg, s);
+  return launch_decode_kq<0>(a, bf16, tk, tv, seg, s);
 }
 
 }  // namespace pa

@@ -475,15 +475,29 @@ __device__ __forceinline__ void store_vec(uint16_t* dst, bool bf16, const float 
 
 // the prepared query heads of token tok into the workspace, and, when slot >= 0, its
 // prepared key heads and its V row into the caches
+// The preparation's per-lane tables for a token at position pos: whether and how this lane's
+// components rotate, cos / sin of their fp32 angles, and the norm weights.
 template <int HS>
-__device__ void prep_token(const Args& a, int tok, int64_t pos, int64_t slot, int lane) {
+struct PrepLane {
+  bool rot, first;
+  int partner;
+  float cs[HS / 32], sn[HS / 32], wq[HS / 32], wk[HS / 32];
+};
+
+template <int HS>
+__device__ __forceinline__ void prep_lane(const Args& a, int64_t pos, int lane, PrepLane<HS>& t) {
   constexpr int E = HS / 32;
   const bool bf16 = a.bf16 != 0;
   const int d = a.rotary_dim, half = d / 2;
   const bool rot = d > 0 && lane * E < d;
   const bool first = lane * E < half;
-  const int partner = rot ? (first ? lane + half / E : lane - half / E) : lane;
-  float cs[E], sn[E], wq[E], wk[E];
+  t.rot = rot;
+  t.first = first;
+  t.partner = rot ? (first ? lane + half / E : lane - half / E) : lane;
+  float* cs = t.cs;
+  float* sn = t.sn;
+  float* wq = t.wq;
+  float* wk = t.wk;
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     cs[e] = 1.f;
@@ -499,11 +513,19 @@ __device__ void prep_token(const Args& a, int tok, int64_t pos, int64_t slot, in
                                : __half2float(*reinterpret_cast<const __half*>(a.k_norm_w + lane * E + e)))
                        : 1.f;
   }
+}
+
+template <int HS>
+__device__ void prep_token(const Args& a, int tok, int64_t pos, int64_t slot, int lane) {
+  constexpr int E = HS / 32;
+  const bool bf16 = a.bf16 != 0;
+  PrepLane<HS> t;
+  prep_lane<HS>(a, pos, lane, t);
   const uint16_t* qrow = reinterpret_cast<const uint16_t*>(a.query) + (int64_t)tok * a.q_stride;
   for (int h = 0; h < a.nh; ++h) {
     float x[E];
     load_vec<HS>(qrow + h * HS + lane * E, bf16, x);
-    prep_vector<HS>(x, a.q_norm_w != nullptr, wq, a.norm_eps, rot, first, partner, cs, sn);
+    prep_vector<HS>(x, a.q_norm_w != nullptr, t.wq, a.norm_eps, t.rot, t.first, t.partner, t.cs, t.sn);
     store_vec<HS>(a.qprep + ((int64_t)tok * a.nh + h) * HS + lane * E, bf16, x);
   }
   if (slot < 0) return;
@@ -516,11 +538,112 @@ __device__ void prep_token(const Args& a, int tok, int64_t pos, int64_t slot, in
   for (int g = 0; g < a.kvh; ++g) {
     float x[E];
     load_vec<HS>(krow + g * HS + lane * E, bf16, x);
-    prep_vector<HS>(x, a.k_norm_w != nullptr, wk, a.norm_eps, rot, first, partner, cs, sn);
+    prep_vector<HS>(x, a.k_norm_w != nullptr, t.wk, a.norm_eps, t.rot, t.first, t.partner, t.cs, t.sn);
     store_vec<HS>(kdst + g * HS + lane * E, bf16, x);
   }
   for (int c = lane; c < a.kv_row / 8; c += 32)
     reinterpret_cast<uint4*>(vdst)[c] = __ldg(reinterpret_cast<const uint4*>(vrow) + c);
+}
+
+// ---- integer caches: this call's K and V rows as codes, the query rows scaled -------------
+
+__device__ __forceinline__ float round_t(float x, bool bf16) {
+  return bf16 ? __bfloat162float(__float2bfloat16_rn(x)) : __half2float(__float2half_rn(x));
+}
+
+// the code of x for scale s: min(max(rint(x / s), -Q), Q) with the IEEE fp32 quotient
+__device__ __forceinline__ int quant_code(float x, float s, float qmax) {
+  return (int)fminf(fmaxf(rintf(__fdiv_rn(x, s)), -qmax), qmax);
+}
+
+// E consecutive codes of one lane: INT8 one byte each, INT4 one nibble each (first channel
+// in the low nibble), little-endian
+template <int E, int KQ>
+__device__ __forceinline__ void store_codes(uint8_t* dst, const int (&c)[E]) {
+  if constexpr (KQ == 1) {
+    uint32_t w[(E + 3) / 4] = {};
+#pragma unroll
+    for (int e = 0; e < E; ++e) w[e / 4] |= (uint32_t)(c[e] & 0xFF) << (8 * (e % 4));
+    if constexpr (E == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    else if constexpr (E == 4) *reinterpret_cast<uint32_t*>(dst) = w[0];
+    else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)w[0];
+  } else {
+    uint32_t w = 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) w |= (uint32_t)(c[e] & 0xF) << (4 * e);
+    if constexpr (E == 8) *reinterpret_cast<uint32_t*>(dst) = w;
+    else if constexpr (E == 4) *reinterpret_cast<uint16_t*>(dst) = (uint16_t)w;
+    else *dst = (uint8_t)w;
+  }
+}
+
+template <int HS, int KQ>
+__device__ __forceinline__ void quant_row(const Args& a, const uint16_t* src, const float* scale, uint8_t* dst,
+                                          int lane, bool prep, const float (&w)[HS / 32], const PrepLane<HS>& t) {
+  constexpr int E = HS / 32;
+  const bool bf16 = a.bf16 != 0;
+  float x[E];
+  load_vec<HS>(src + lane * E, bf16, x);
+  if (prep) {  // the prepared key, rounded to T, is what is quantized
+    prep_vector<HS>(x, a.k_norm_w != nullptr, w, a.norm_eps, t.rot, t.first, t.partner, t.cs, t.sn);
+#pragma unroll
+    for (int e = 0; e < E; ++e) x[e] = round_t(x[e], bf16);
+  }
+  int c[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) c[e] = quant_code(x[e], __ldg(scale + lane * E + e), KQ == 1 ? 127.f : 7.f);
+  store_codes<E, KQ>(dst + lane * E * (KQ == 1 ? 2 : 1) / 2, c);
+}
+
+// One token of a call with integer caches (a warp): every query head scaled by the K scales
+// of its KV head (after the preparation, if any) and written as fp16 with a power-of-two
+// row exponent, then, unless the write is suppressed, the K and V rows as codes.
+template <int HS, int KQ>
+__device__ void quant_token(const Args& a, int tok, int64_t pos, int64_t slot, int lane) {
+  constexpr int E = HS / 32;
+  const bool bf16 = a.bf16 != 0;
+  const bool prep = a.prep != 0;
+  PrepLane<HS> t;
+  if (prep) prep_lane<HS>(a, pos, lane, t);
+  const uint16_t* qrow = reinterpret_cast<const uint16_t*>(a.query) + (int64_t)tok * a.q_stride;
+  for (int h = 0; h < a.nh; ++h) {
+    float x[E];
+    load_vec<HS>(qrow + h * HS + lane * E, bf16, x);
+    if (prep) {
+      prep_vector<HS>(x, a.q_norm_w != nullptr, t.wq, a.norm_eps, t.rot, t.first, t.partner, t.cs, t.sn);
+#pragma unroll
+      for (int e = 0; e < E; ++e) x[e] = round_t(x[e], bf16);
+    }
+    // q * k_scale, brought to magnitudes in [2^14, 2^15) by 2^-ex: fp16 then keeps 11 bits
+    // of every element without overflow, and the attention kernels multiply the scores by
+    // 2^ex (exact)
+    const float* ks = a.k_scale + (h / a.G) * HS + lane * E;
+    float m = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      x[e] *= __ldg(ks + e);
+      m = fmaxf(m, fabsf(x[e]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const int ex = (m > 0.f && m <= 3.4028234e38f) ? ilogbf(m) - 14 : 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) x[e] = ldexpf(x[e], -ex);
+    store_vec<HS>(a.qprep + ((int64_t)tok * a.nh + h) * HS + lane * E, false, x);
+    if (lane == 0) a.qexp[(int64_t)tok * a.nh + h] = ex;
+  }
+  if (slot < 0) return;
+  const uint16_t* krow = a.packed ? qrow + a.k_offset
+                                  : reinterpret_cast<const uint16_t*>(a.key) + (int64_t)tok * a.kv_row;
+  const uint16_t* vrow = a.packed ? qrow + a.v_offset
+                                  : reinterpret_cast<const uint16_t*>(a.value) + (int64_t)tok * a.kv_row;
+  constexpr int RB = KQ == 1 ? HS : HS / 2;  // bytes of one KV head's code row
+  uint8_t* kdst = reinterpret_cast<uint8_t*>(a.key_cache) + slot * a.kvh * RB;
+  uint8_t* vdst = reinterpret_cast<uint8_t*>(a.value_cache) + slot * a.kvh * RB;
+  for (int g = 0; g < a.kvh; ++g) {
+    quant_row<HS, KQ>(a, krow + g * HS, a.k_scale + g * HS, kdst + g * RB, lane, prep, t.wk, t);
+    quant_row<HS, KQ>(a, vrow + g * HS, a.v_scale + g * HS, vdst + g * RB, lane, false, t.wk, t);
+  }
 }
 
 __global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
@@ -558,6 +681,17 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
     if (slot != -1 && (slot < 0 || slot >= nslots)) {
       if (lane == 0) atomicOr(&a.hdr->error, PA_DEVERR_BAD_SLOT);
       slot = -1;
+    }
+    if (a.kvq) {  // (the query rows are scaled even where the K/V write is skipped)
+      if (a.kvq == 1) {
+        if (a.hs == 128) quant_token<128, 1>(a, tok, pos, slot, lane);
+        else if (a.hs == 256) quant_token<256, 1>(a, tok, pos, slot, lane);
+        else quant_token<64, 1>(a, tok, pos, slot, lane);
+      } else {
+        if (a.hs == 128) quant_token<128, 2>(a, tok, pos, slot, lane);
+        else quant_token<256, 2>(a, tok, pos, slot, lane);
+      }
+      continue;
     }
     if (a.prep) {  // (the query rows are prepared even where the K/V write is skipped)
       if (a.hs == 128) prep_token<128>(a, tok, pos, slot, lane);
