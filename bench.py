@@ -44,8 +44,10 @@ METRIC = "paged-attn decode KV GB/s & prefill TFLOP/s vs GB300 peak; packed toke
 # ---- algorithmic work of one step ---------------------------------------------------------
 
 def kv_history_bytes(p) -> int:
-    """K and V of every sequence's history (past + new rows), each element read once."""
-    return int(p.kv_lens.sum()) * p.kv_num_heads * p.head_size * 2 * 2
+    """K and V of every sequence's history (past + new rows), each element read once: two
+    bytes per element for 16-bit caches, one per INT8 code, half a byte per INT4 code."""
+    row = p.head_size * 2 if p.kv_quant is None else (p.head_size if p.kv_quant == "int8" else p.head_size // 2)
+    return int(p.kv_lens.sum()) * p.kv_num_heads * row * 2
 
 
 def step_bytes(p) -> int:
@@ -158,14 +160,22 @@ class Runner:
 
         self.host = {k: getattr(p, k) for k in ("query", "key", "value")}
         self.q, self.k, self.v = t16(p.query), (None if p.key is None else t16(p.key)), (None if p.value is None else t16(p.value))
-        self.kc, self.vc = t16(p.key_cache), t16(p.value_cache)
+        if p.kv_quant is None:
+            self.kc, self.vc = t16(p.key_cache), t16(p.value_cache)
+            self.ext = None
+        else:  # integer caches: code bytes, per-channel fp32 scales through pa_extensions
+            self.kc = torch.from_numpy(np.ascontiguousarray(p.key_cache)).to(device)
+            self.vc = torch.from_numpy(np.ascontiguousarray(p.value_cache)).to(device)
+            self.k_scale = torch.from_numpy(np.ascontiguousarray(p.k_scale, dtype=np.float32)).to(device)
+            self.v_scale = torch.from_numpy(np.ascontiguousarray(p.v_scale, dtype=np.float32)).to(device)
+            self.ext = pa.PaExtensions(None, None, None, self.k_scale.data_ptr(), self.v_scale.data_ptr())
         self.cum, self.past = t32(p.cumulative_sequence_length), t32(p.past_seqlens)
         self.bt, self.sm = t32(p.block_table), t32(p.slot_mapping)
         self.out = torch.empty((p.num_tokens, p.num_heads * p.head_size), dtype=dt, device=device)
         # the caller knows its batch composition: pass the bound on new tokens per sequence
         self.max_q = int(p.q_lens.max()) if p.batch_size else 0
         self.dims = pa.make_dims(p.num_tokens, p.batch_size, p.head_size, p.num_blocks, p.block_size,
-                                 p.max_blocks_per_sequence, dt, max_query_len=self.max_q)
+                                 p.max_blocks_per_sequence, dt, max_query_len=self.max_q, kv_dtype=p.kv_quant)
         self.ws = torch.zeros(pa.workspace_size(self.dims, p.num_heads, p.kv_num_heads), dtype=torch.uint8,
                               device=device)
         self.stream = torch.cuda.current_stream(device)
@@ -181,9 +191,14 @@ class Runner:
                      self.ws.numel(), vp(self.stream.cuda_stream))
 
     def call(self, stages):
-        st = self.lib.pa_paged_attention_stages(*self.args, stages)
+        if self.ext is not None:  # whole calls only (pa_paged_attention_ex)
+            assert stages == self.pa.STAGE_ALL
+            a = self.args
+            st = self.lib.pa_paged_attention_ex(*a[:13], ctypes.byref(self.ext), *a[13:])
+        else:
+            st = self.lib.pa_paged_attention_stages(*self.args, stages)
         if st:
-            raise RuntimeError(f"pa_paged_attention_stages: status {st}")
+            raise RuntimeError(f"pa_paged_attention: status {st}")
 
     def step(self):
         self.call(self.pa.STAGE_ALL)
@@ -279,9 +294,11 @@ class Runner:
                 ready[k].record(up)
             comp.wait_event(ready[k])
             comp.wait_event(drained[k])  # step i-2's output has left this buffer
+            quant = {} if p.kv_quant is None else dict(kv_quant=p.kv_quant, k_scale=self.k_scale,
+                                                          v_scale=self.v_scale)
             pa.paged_attention(d["query"], d["key"], d["value"], self.kc, self.vc, d["cum"], d["past"], d["bt"],
                                d["sm"], num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, scale=p.scale,
-                               output=outs[k], workspace=self.ws, max_query_len=self.max_q)
+                               output=outs[k], workspace=self.ws, max_query_len=self.max_q, **quant)
             computed[k].record(comp)
             with torch.cuda.stream(down):
                 down.wait_event(computed[k])
@@ -352,14 +369,18 @@ def reduce_over_ranks(local_seconds: float, local_units: float):
     return float(t.item()), float(u.item())
 
 
-def oracle_baseline(p, reps=1):
+def oracle_baseline(p, budget_s=10.0, max_reps=200):
+    """The oracle on the whole workload, repeated until about budget_s seconds of host work
+    (at most max_reps runs). Returns (seconds per run, runs, threads)."""
     import oracle
     oracle.build()
+    reps = 0
     t0 = time.perf_counter()
-    for _ in range(reps):
+    while reps < max_reps and (reps == 0 or time.perf_counter() - t0 < budget_s):
         oracle.paged_attention(p)
+        reps += 1
     dt = (time.perf_counter() - t0) / reps
-    return dt, oracle.max_threads()
+    return dt, reps, oracle.max_threads()
 
 
 WORKLOAD_TEXT = {
@@ -380,6 +401,12 @@ def measure(r, steps, warmup, pk, clocks=None):
     kernel launches in the whole-step timed region)."""
     q = r.p
     sec, per_step = r.whole(steps, warmup, clocks=clocks)
+    if q.kv_quant is not None:
+        # pa_paged_attention_ex runs whole calls only: the step bounds the decode kernel
+        roof = kernel_roofline(q, "hbm", sec, pk)
+        roof["kernel"] = "whole step (plan, cache write, decode_kernel on %s codes)" % q.kv_quant
+        roof["ms_per_launch"] = round(sec * 1e3, 4)
+        return sec, roof, per_step * steps
     if prefill_sequences(q):
         _, kt, _ = r.timed(steps, warmup, r.pa.STAGE_PREFILL)
         roof = kernel_roofline(q, "tensor", kt, pk)
@@ -420,7 +447,10 @@ def run_cuda(args):
     pk = peaks()
 
     k = args.workload
-    p = wl.config(k) if rank == 0 else wl.make_problem(**_rank_recipe(k, rank))
+    if args.kv_quant:
+        p = wl.config_kv_quant(k, args.kv_quant)
+    else:
+        p = wl.config(k) if rank == 0 else wl.make_problem(**_rank_recipe(k, rank))
     r = Runner(p, device)
     sampler = ClockSampler(local)
     if world > 1:
@@ -436,7 +466,9 @@ def run_cuda(args):
         "metric": METRIC, "value": round(value, 1), "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(sec_max * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": p.dtype, "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[k], "name": p.name, "num_tokens": p.num_tokens,
+        "config": {"workload": WORKLOAD_TEXT[k] if not args.kv_quant else
+                   WORKLOAD_TEXT[k].replace(", fp16,", ", fp16 queries, %s per-channel KV caches," % args.kv_quant),
+                   "name": p.name, "num_tokens": p.num_tokens,
                    "batch_size": p.batch_size, "num_blocks": p.num_blocks,
                    "kv_history_bytes_per_step": kv_history_bytes(p),
                    "causal_flops_per_step": causal_flops(p),
@@ -450,7 +482,7 @@ def run_cuda(args):
         "gpu_launches": int(launches),
         "clocks": sampler.summary(),
     }
-    if rank == 0 and not args.no_secondary:
+    if rank == 0 and not args.no_secondary and not args.kv_quant:
         sec_lines = {}
         for kk in SECONDARY:
             if kk == k:
@@ -468,16 +500,30 @@ def run_cuda(args):
             sec_lines[q.name] = entry
             del rq
             torch.cuda.empty_cache()
+        for fmt in ("int8", "int4"):
+            q = wl.config_kv_quant(MAIN, fmt)
+            rq = Runner(q, device)
+            s, roof_q, _ = measure(rq, max(args.steps // 10, 10), args.warmup, pk)
+            v, u = headline(q, s)
+            fp16 = wl.config(MAIN)
+            sec_lines[q.name] = {
+                "workload": WORKLOAD_TEXT[MAIN].replace(", fp16,", ", fp16 queries, %s per-channel KV caches," % fmt),
+                "value": round(v, 1), "unit": u + " (code bytes)", "ms_per_step": round(s * 1e3, 4),
+                "fp16_equivalent_kv_gb_s": round(kv_history_bytes(fp16) / s / 1e9, 1),
+                "speedup_vs_fp16_step": round(sec / s, 3) if k == MAIN else None,
+                "roofline": roof_q}
+            del rq
+            torch.cuda.empty_cache()
         line["secondary"] = sec_lines
     if rank == 0 and args.no_cpu_baseline:
         line["cpu_baseline"] = None
         print(json.dumps(line), flush=True)
     elif rank == 0:
-        dt, cores = oracle_baseline(p)
+        dt, reps, cores = oracle_baseline(p)
         cv, cu = headline(p, dt)
         line["cpu_baseline"] = {"value": round(cv, 4), "unit": cu, "cores": cores, "kind": "oracle",
-                                "sample": "the whole %s workload (cache write + attention), fp64 C oracle, one run, "
-                                          "%.2f s" % (p.name, dt)}
+                                "sample": "the whole %s workload (cache write + attention), fp64 C oracle, %d runs "
+                                          "of %.3f s each" % (p.name, reps, dt)}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -534,6 +580,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--workload", type=int, default=MAIN, choices=[2, 3, 4, 5],
                     help="workload of the headline line (2: the decode batch the metric is quoted on)")
+    ap.add_argument("--kv-quant", choices=["int8", "int4"], default=None,
+                    help="the headline workload with integer KV caches (workload 2 only; profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -181,9 +181,8 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
   const bool can_decode = d->route == PA_ROUTE_AUTO;
   const bool can_prefill = prefill_possible(d, args.G);
   if ((stages & PA_STAGE_CACHE_WRITE) && args.N > 0) {
-    const int64_t blocks = std::min<int64_t>(((int64_t)args.N + 7) / 8, (int64_t)info.sms * 8);  // a warp per token
     ++g_launches;
-    if (cudaError_t e = pa::launch_cache_write(args, (int)blocks, stream)) return cuda_fail(e, "cache_write_kernel launch");
+    if (cudaError_t e = pa::launch_cache_write(args, info.sms, stream)) return cuda_fail(e, "cache_write_kernel launch");
     if (can_prefill && args.mirror_keys > 0 && slots > 0) {
       // bf16: the fp16 copy of the prefill sequences' V, read from the cache just written
       // (the planner decides whether it is made and used)

@@ -287,7 +287,7 @@ __device__ __forceinline__ uint32_t p_col(int kk) { return (uint32_t)((kk >> 1) 
 
 // ---- host launchers, one per kernel family (defined next to their kernels) -----------------
 cudaError_t launch_plan(const Args& a, cudaStream_t s);
-cudaError_t launch_cache_write(const Args& a, int grid, cudaStream_t s);
+cudaError_t launch_cache_write(const Args& a, int sms, cudaStream_t s);
 cudaError_t launch_v_mirror(const Args& a, int grid, cudaStream_t s);
 cudaError_t launch_prefill(const Args& a, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const CUtensorMap& tvm, int seg, int grid, cudaStream_t s);

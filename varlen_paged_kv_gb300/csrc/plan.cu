@@ -18,6 +18,8 @@
 // scheduled and PA_DEVERR_BAD_BATCH is raised.
 #include <limits.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace pa {
@@ -398,12 +400,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
 }
 
 // ---- cache write ----------------------------------------------------------------------------
-// One warp per token: the slot is found once (slot_mapping[i], or the token's logical
-// position past_seqlens[b] + j through block_table), then the lanes copy the token's K and
-// V rows with 16-byte loads and stores, all loads of a row issued before its stores. -1
-// skips the token; out-of-range slots and blocks are skipped and flagged. With the Q/K
-// preparation the warp also prepares the token's query heads (into the workspace) and
-// key heads (into the cache) on the way.
+// The bit copy, one warp per token: the slot is found once (slot_mapping[i], or the token's
+// logical position past_seqlens[b] + j through block_table), then the lanes copy the
+// token's K and V rows with 16-byte loads and stores, all loads of a row issued before its
+// stores. -1 skips the token; out-of-range slots and blocks are skipped and flagged. With
+// the Q/K preparation or integer caches, one warp per query head of the token (prepared or
+// scaled into the workspace) and one per KV head (prepared or quantized into the caches).
 
 // RMSNorm and rotary embedding of one head vector spread over the warp, lane l holding
 // components [E l, E l + E): x_c <- x_c / sqrt(mean x^2 + eps) * w_c (when w), then the
@@ -473,8 +475,6 @@ __device__ __forceinline__ void store_vec(uint16_t* dst, bool bf16, const float 
   else *reinterpret_cast<uint32_t*>(dst) = wds[0];
 }
 
-// the prepared query heads of token tok into the workspace, and, when slot >= 0, its
-// prepared key heads and its V row into the caches
 // The preparation's per-lane tables for a token at position pos: whether and how this lane's
 // components rotate, cos / sin of their fp32 angles, and the norm weights.
 template <int HS>
@@ -515,34 +515,37 @@ __device__ __forceinline__ void prep_lane(const Args& a, int64_t pos, int lane, 
   }
 }
 
+// Unit u of token tok (a warp): u < nh, query head u prepared into the workspace; else KV
+// head g = u - nh, when slot >= 0, its prepared key head into the key cache and its V head
+// copied into the value cache.
 template <int HS>
-__device__ void prep_token(const Args& a, int tok, int64_t pos, int64_t slot, int lane) {
+__device__ void prep_unit(const Args& a, int tok, int64_t pos, int64_t slot, int u, int lane) {
   constexpr int E = HS / 32;
   const bool bf16 = a.bf16 != 0;
+  if (u >= a.nh && slot < 0) return;
   PrepLane<HS> t;
   prep_lane<HS>(a, pos, lane, t);
   const uint16_t* qrow = reinterpret_cast<const uint16_t*>(a.query) + (int64_t)tok * a.q_stride;
-  for (int h = 0; h < a.nh; ++h) {
-    float x[E];
-    load_vec<HS>(qrow + h * HS + lane * E, bf16, x);
+  float x[E];
+  if (u < a.nh) {
+    load_vec<HS>(qrow + u * HS + lane * E, bf16, x);
     prep_vector<HS>(x, a.q_norm_w != nullptr, t.wq, a.norm_eps, t.rot, t.first, t.partner, t.cs, t.sn);
-    store_vec<HS>(a.qprep + ((int64_t)tok * a.nh + h) * HS + lane * E, bf16, x);
+    store_vec<HS>(a.qprep + ((int64_t)tok * a.nh + u) * HS + lane * E, bf16, x);
+    return;
   }
-  if (slot < 0) return;
+  const int g = u - a.nh;
   const uint16_t* krow = a.packed ? qrow + a.k_offset
                                   : reinterpret_cast<const uint16_t*>(a.key) + (int64_t)tok * a.kv_row;
   const uint16_t* vrow = a.packed ? qrow + a.v_offset
                                   : reinterpret_cast<const uint16_t*>(a.value) + (int64_t)tok * a.kv_row;
-  uint16_t* kdst = reinterpret_cast<uint16_t*>(a.key_cache) + slot * a.kv_row;
-  uint16_t* vdst = reinterpret_cast<uint16_t*>(a.value_cache) + slot * a.kv_row;
-  for (int g = 0; g < a.kvh; ++g) {
-    float x[E];
-    load_vec<HS>(krow + g * HS + lane * E, bf16, x);
-    prep_vector<HS>(x, a.k_norm_w != nullptr, t.wk, a.norm_eps, t.rot, t.first, t.partner, t.cs, t.sn);
-    store_vec<HS>(kdst + g * HS + lane * E, bf16, x);
-  }
-  for (int c = lane; c < a.kv_row / 8; c += 32)
-    reinterpret_cast<uint4*>(vdst)[c] = __ldg(reinterpret_cast<const uint4*>(vrow) + c);
+  uint16_t* kdst = reinterpret_cast<uint16_t*>(a.key_cache) + slot * a.kv_row + g * HS;
+  uint16_t* vdst = reinterpret_cast<uint16_t*>(a.value_cache) + slot * a.kv_row + g * HS;
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (lane < HS / 8) v = __ldg(reinterpret_cast<const uint4*>(vrow + g * HS) + lane);
+  load_vec<HS>(krow + g * HS + lane * E, bf16, x);
+  prep_vector<HS>(x, a.k_norm_w != nullptr, t.wk, a.norm_eps, t.rot, t.first, t.partner, t.cs, t.sn);
+  store_vec<HS>(kdst + lane * E, bf16, x);
+  if (lane < HS / 8) reinterpret_cast<uint4*>(vdst)[lane] = v;
 }
 
 // ---- integer caches: this call's K and V rows as codes, the query rows scaled -------------
@@ -595,18 +598,21 @@ __device__ __forceinline__ void quant_row(const Args& a, const uint16_t* src, co
   store_codes<E, KQ>(dst + lane * E * (KQ == 1 ? 2 : 1) / 2, c);
 }
 
-// One token of a call with integer caches (a warp): every query head scaled by the K scales
-// of its KV head (after the preparation, if any) and written as fp16 with a power-of-two
-// row exponent, then, unless the write is suppressed, the K and V rows as codes.
+// Unit u of token tok for integer caches (a warp): u < nh, query head u scaled by the K
+// scales of its KV head (after the preparation, if any) and written as fp16 with a
+// power-of-two row exponent; else KV head g = u - nh, unless the write is suppressed, its
+// K and V rows as codes.
 template <int HS, int KQ>
-__device__ void quant_token(const Args& a, int tok, int64_t pos, int64_t slot, int lane) {
+__device__ void quant_unit(const Args& a, int tok, int64_t pos, int64_t slot, int u, int lane) {
   constexpr int E = HS / 32;
   const bool bf16 = a.bf16 != 0;
   const bool prep = a.prep != 0;
+  if (u >= a.nh && slot < 0) return;
   PrepLane<HS> t;
   if (prep) prep_lane<HS>(a, pos, lane, t);
   const uint16_t* qrow = reinterpret_cast<const uint16_t*>(a.query) + (int64_t)tok * a.q_stride;
-  for (int h = 0; h < a.nh; ++h) {
+  if (u < a.nh) {
+    const int h = u;
     float x[E];
     load_vec<HS>(qrow + h * HS + lane * E, bf16, x);
     if (prep) {
@@ -631,8 +637,9 @@ __device__ void quant_token(const Args& a, int tok, int64_t pos, int64_t slot, i
     for (int e = 0; e < E; ++e) x[e] = ldexpf(x[e], -ex);
     store_vec<HS>(a.qprep + ((int64_t)tok * a.nh + h) * HS + lane * E, false, x);
     if (lane == 0) a.qexp[(int64_t)tok * a.nh + h] = ex;
+    return;
   }
-  if (slot < 0) return;
+  const int g = u - a.nh;
   const uint16_t* krow = a.packed ? qrow + a.k_offset
                                   : reinterpret_cast<const uint16_t*>(a.key) + (int64_t)tok * a.kv_row;
   const uint16_t* vrow = a.packed ? qrow + a.v_offset
@@ -640,65 +647,88 @@ __device__ void quant_token(const Args& a, int tok, int64_t pos, int64_t slot, i
   constexpr int RB = KQ == 1 ? HS : HS / 2;  // bytes of one KV head's code row
   uint8_t* kdst = reinterpret_cast<uint8_t*>(a.key_cache) + slot * a.kvh * RB;
   uint8_t* vdst = reinterpret_cast<uint8_t*>(a.value_cache) + slot * a.kvh * RB;
-  for (int g = 0; g < a.kvh; ++g) {
-    quant_row<HS, KQ>(a, krow + g * HS, a.k_scale + g * HS, kdst + g * RB, lane, prep, t.wk, t);
-    quant_row<HS, KQ>(a, vrow + g * HS, a.v_scale + g * HS, vdst + g * RB, lane, false, t.wk, t);
-  }
+  quant_row<HS, KQ>(a, krow + g * HS, a.k_scale + g * HS, kdst + g * RB, lane, prep, t.wk, t);
+  quant_row<HS, KQ>(a, vrow + g * HS, a.v_scale + g * HS, vdst + g * RB, lane, false, t.wk, t);
 }
 
+// The slot of token tok (slot_mapping[tok], or its logical position through block_table),
+// -1 for a suppressed write or an out-of-range block or slot (those also flagged); pos is
+// the token's logical position when the caller needs it (no slot_mapping, or prep). b is
+// the sequence of the warp's previous token, tokens only grow within a warp.
+__device__ __forceinline__ int64_t resolve_slot(const Args& a, int tok, bool need_pos, int& b, int64_t& pos,
+                                                int lane) {
+  pos = 0;
+  if (!a.slot_mapping || need_pos) {
+    int lo = b, hi = a.B - 1;  // last b with cum[b] <= tok
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.cum[mid] <= tok) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    pos = (int64_t)a.past[b] + (tok - a.cum[b]);
+  }
+  int64_t slot;
+  if (a.slot_mapping) {
+    slot = a.slot_mapping[tok];
+  } else {
+    const int blk = a.block_table[(int64_t)b * a.max_blocks + pos / a.bs];
+    if (blk < 0 || blk >= a.num_blocks) {
+      if (lane == 0) atomicOr(&a.hdr->error, PA_DEVERR_BAD_BLOCK);
+      slot = -1;
+    } else {
+      slot = (int64_t)blk * a.bs + pos % a.bs;
+    }
+  }
+  if (slot != -1 && (slot < 0 || slot >= (int64_t)a.num_blocks * a.bs)) {
+    if (lane == 0) atomicOr(&a.hdr->error, PA_DEVERR_BAD_SLOT);
+    slot = -1;
+  }
+  return slot;
+}
+
+// One instantiation per kind of write, so that the plain bit copy keeps the few registers
+// it needs and stays many warps deep: 0 = bit copy, one warp per token; 1 = Q/K
+// preparation and 2 = integer caches, one warp per (token, unit), the units being the
+// token's nh query heads and then its kvh KV heads (each a short dependent chain of a load,
+// warp reductions and a store, so the units of a token run in parallel, not one after the
+// other).
+template <int MODE>
 __global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
   pdl_wait();
   pdl_launch_dependents();
   if (!a.hdr->valid) return;
   const int lane = threadIdx.x & 31;
-  const int chunks = a.kv_row / 8;  // 16-byte chunks in one K (or V) row
-  const int64_t nslots = (int64_t)a.num_blocks * a.bs;
   const int warps = (int)((gridDim.x * blockDim.x) >> 5);
-  int b = 0;  // sequence of the previous token (tokens only grow within a warp)
-  for (int tok = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); tok < a.N; tok += warps) {
-    int64_t pos = 0;
-    if (!a.slot_mapping || a.prep) {
-      int lo = b, hi = a.B - 1;  // last b with cum[b] <= tok
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (a.cum[mid] <= tok) lo = mid; else hi = mid - 1;
+  const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  int b = 0;
+  if constexpr (MODE != 0) {
+    const int U = a.nh + a.kvh;
+    const int64_t total = (int64_t)a.N * U;
+    for (int64_t wi = gw; wi < total; wi += warps) {
+      const int tok = (int)(wi / U), u = (int)(wi - (int64_t)tok * U);
+      int64_t pos;
+      const int64_t slot = resolve_slot(a, tok, true, b, pos, lane);
+      if constexpr (MODE == 2) {  // (the query rows are scaled even where the K/V write is skipped)
+        if (a.kvq == 1) {
+          if (a.hs == 128) quant_unit<128, 1>(a, tok, pos, slot, u, lane);
+          else if (a.hs == 256) quant_unit<256, 1>(a, tok, pos, slot, u, lane);
+          else quant_unit<64, 1>(a, tok, pos, slot, u, lane);
+        } else {
+          if (a.hs == 128) quant_unit<128, 2>(a, tok, pos, slot, u, lane);
+          else quant_unit<256, 2>(a, tok, pos, slot, u, lane);
+        }
+      } else {  // (the query rows are prepared even where the K/V write is skipped)
+        if (a.hs == 128) prep_unit<128>(a, tok, pos, slot, u, lane);
+        else if (a.hs == 256) prep_unit<256>(a, tok, pos, slot, u, lane);
+        else prep_unit<64>(a, tok, pos, slot, u, lane);
       }
-      b = lo;
-      pos = (int64_t)a.past[b] + (tok - a.cum[b]);
     }
-    int64_t slot;
-    if (a.slot_mapping) {
-      slot = a.slot_mapping[tok];
-    } else {
-      const int blk = a.block_table[(int64_t)b * a.max_blocks + pos / a.bs];
-      if (blk < 0 || blk >= a.num_blocks) {
-        if (lane == 0) atomicOr(&a.hdr->error, PA_DEVERR_BAD_BLOCK);
-        slot = -1;
-      } else {
-        slot = (int64_t)blk * a.bs + pos % a.bs;
-      }
-    }
-    if (slot != -1 && (slot < 0 || slot >= nslots)) {
-      if (lane == 0) atomicOr(&a.hdr->error, PA_DEVERR_BAD_SLOT);
-      slot = -1;
-    }
-    if (a.kvq) {  // (the query rows are scaled even where the K/V write is skipped)
-      if (a.kvq == 1) {
-        if (a.hs == 128) quant_token<128, 1>(a, tok, pos, slot, lane);
-        else if (a.hs == 256) quant_token<256, 1>(a, tok, pos, slot, lane);
-        else quant_token<64, 1>(a, tok, pos, slot, lane);
-      } else {
-        if (a.hs == 128) quant_token<128, 2>(a, tok, pos, slot, lane);
-        else quant_token<256, 2>(a, tok, pos, slot, lane);
-      }
-      continue;
-    }
-    if (a.prep) {  // (the query rows are prepared even where the K/V write is skipped)
-      if (a.hs == 128) prep_token<128>(a, tok, pos, slot, lane);
-      else if (a.hs == 256) prep_token<256>(a, tok, pos, slot, lane);
-      else prep_token<64>(a, tok, pos, slot, lane);
-      continue;
-    }
+    return;
+  }
+  const int chunks = a.kv_row / 8;  // 16-byte chunks in one K (or V) row
+  for (int tok = gw; tok < a.N; tok += warps) {
+    int64_t pos;
+    const int64_t slot = resolve_slot(a, tok, false, b, pos, lane);
     if (slot == -1) continue;
     const uint16_t *src_k, *src_v;
     if (a.packed) {
@@ -792,8 +822,13 @@ cudaError_t launch_plan(const Args& a, cudaStream_t s) {
   return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, a);
 }
 
-cudaError_t launch_cache_write(const Args& a, int grid, cudaStream_t s) {
-  return launch_pdl(cache_write_kernel, dim3(grid), dim3(256), 0, s, a);
+cudaError_t launch_cache_write(const Args& a, int sms, cudaStream_t s) {
+  // a warp per token (bit copy) or per (token, unit): at most 8 blocks of 8 warps per SM
+  const int64_t warps = (int64_t)a.N * ((a.kvq || a.prep) ? a.nh + a.kvh : 1);
+  const int grid = (int)std::min<int64_t>((warps + 7) / 8, (int64_t)sms * 8);
+  if (a.kvq) return launch_pdl(cache_write_kernel<2>, dim3(grid), dim3(256), 0, s, a);
+  if (a.prep) return launch_pdl(cache_write_kernel<1>, dim3(grid), dim3(256), 0, s, a);
+  return launch_pdl(cache_write_kernel<0>, dim3(grid), dim3(256), 0, s, a);
 }
 
 cudaError_t launch_v_mirror(const Args& a, int grid, cudaStream_t s) {

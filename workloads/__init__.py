@@ -332,3 +332,16 @@ def config(k: int) -> Problem:
             head_size=128, block_size=16, past=past, q_lens=np.ones(8, np.int64),
             max_blocks_per_sequence=(131072 + 1 + 15) // 16)
     raise ValueError(f"no workload {k}")
+
+
+def config_kv_quant(k: int, fmt: str) -> Problem:
+    """Workload k's batch (same seed, lengths, pages and queries) with integer caches of
+    format fmt ("int8" | "int4") and per-channel scales in place of the 16-bit caches."""
+    if k != 2:
+        raise ValueError("integer caches are decode-only: workload 2")
+    seed = 1000 + k
+    past = uniform_int(seed, S_PAST, 64, 512, 4096)
+    return make_problem(
+        name=f"{CONFIG_NAMES[2]}-{fmt}", seed=seed, dtype="fp16", num_heads=32, kv_num_heads=8,
+        head_size=128, block_size=256, past=past, q_lens=np.ones(64, np.int64),
+        max_blocks_per_sequence=(4096 + 1 + 255) // 256, kv_quant=fmt)
