@@ -160,7 +160,10 @@ bool code_cache_map(CUtensorMap* m, void* base, int row_bytes, int kvh, int64_t 
   cuuint32_t boxd[3] = {(cuuint32_t)box, 1, (cuuint32_t)rows};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, boxd, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             box == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             box == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             // a box row is one head's code row: fetch what it covers (the next head's row
+             // at the next 128 or 64 bytes belongs to another CTA's tile)
+             box == 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_64B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -84,22 +84,35 @@ __device__ __forceinline__ uint32_t code_addr(uint32_t base, int r, int b) {
   const int cs = P == 128 ? (c ^ (r & 7)) : (c ^ ((r >> 1) & 3));
   return base + box * (kDecTile * P) + r * P + (cs << 4) + (wb & 15);
 }
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
+// R bytes (16 or 8) of shared memory as R / 4 words
+template <int R>
+__device__ __forceinline__ void lds_run(uint32_t addr, uint32_t (&w)[R / 4]) {
+  if constexpr (R == 16)
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
+  else
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "r"(addr));
 }
 
 // The channel order of the MMA operands on integer caches (Q K^T sums over channels and
 // P V keeps each channel's column apart, so any fixed assignment works when Q and the
-// output follow it). Q K^T, INT8: k-step ks, thread tq takes channels 16ks + 4tq .. + 3 (one
-// 32-bit word of a key row) as k = 2tq, 2tq+1 (b0) and 2tq+8, 2tq+9 (b1). INT4: a word holds
-// channels 32k2 + 8tq .. + 7 for the k-steps 2k2 (channels +0/+4 as b0, +1/+5 as b1) and
-// 2k2 + 1 (+2/+6, +3/+7). P V: n-tile d column n is channel 32(d/4) + 4n + d%4 (INT8) or
-// 64(d/8) + 8n + d%8 (INT4), so a thread's word of one key row feeds 4 (8) n-tiles.
-template <int KQ>
+// output follow it), chosen so that each thread reads its codes of a key row as one run of
+// 16 (or 8) bytes, conflict-free in the swizzled tiles at head_size 128:
+//  - Q K^T: thread tq owns channels [HS/4 tq, HS/4 (tq + 1)) of a key row. INT8: k-step ks
+//    takes the 32-bit word ks of them, channels HS/4 tq + 4ks + {0, 1} as b0 (k = 2tq,
+//    2tq+1) and + {2, 3} as b1 (k = 2tq+8, 2tq+9). INT4: word i holds channels
+//    HS/4 tq + 8i .. + 7 for the k-steps 2i (channels +0/+4 as b0, +1/+5 as b1) and 2i + 1
+//    (+2/+6, +3/+7).
+//  - P V: n-tile d column n is channel out_channel(d, n); thread gq (column gq of every
+//    n-tile) reads G consecutive INT8 channels per G n-tiles (one 128-byte box each), or
+//    its HS/8 consecutive INT4 channels.
+template <int HS, int KQ>
 __device__ __forceinline__ int out_channel(int d, int n) {
-  return KQ == 1 ? 32 * (d >> 2) + 4 * n + (d & 3) : 64 * (d >> 3) + 8 * n + (d & 7);
+  if constexpr (KQ == 1) {
+    constexpr int G = HS / 8 < 16 ? HS / 8 : 16;
+    return (d / G) * (8 * G) + G * n + d % G;
+  } else {
+    return (HS / 8) * n + d;
+  }
 }
 
 // Q' fragments (the scaled query rows, fp16, in the channel order above) of an item and the
@@ -127,14 +140,14 @@ __device__ __forceinline__ void load_q_int(const Args& a, const DecodeItem& item
     if constexpr (KQ == 1) {
 #pragma unroll
       for (int ks = 0; ks < HS / 16; ++ks) {
-        const uint2 v = p[i] ? __ldg(reinterpret_cast<const uint2*>(p[i] + 16 * ks + 4 * tq)) : make_uint2(0, 0);
+        const uint2 v = p[i] ? __ldg(reinterpret_cast<const uint2*>(p[i] + (HS / 4) * tq + 4 * ks)) : make_uint2(0, 0);
         qa[ks][i] = v.x;
         qa[ks][2 + i] = v.y;
       }
     } else {
 #pragma unroll
       for (int k2 = 0; k2 < HS / 32; ++k2) {
-        const uint4 v = p[i] ? __ldg(reinterpret_cast<const uint4*>(p[i] + 32 * k2 + 8 * tq)) : make_uint4(0, 0, 0, 0);
+        const uint4 v = p[i] ? __ldg(reinterpret_cast<const uint4*>(p[i] + (HS / 4) * tq + 8 * k2)) : make_uint4(0, 0, 0, 0);
         qa[2 * k2][i] = prmt(v.x, v.z, 0x5410u);
         qa[2 * k2][2 + i] = prmt(v.x, v.z, 0x7632u);
         qa[2 * k2 + 1][i] = prmt(v.y, v.w, 0x5410u);
@@ -286,24 +299,37 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
         } else if constexpr (KQ == 1) {
           const int kr = 16 * w + gq;  // key rows of the two n-tiles: kr, kr + 8
 #pragma unroll
-          for (int ks = 0; ks < NKS; ++ks) {
-            uint32_t b0, b1, b2, b3;
-            s8x4_to_f16(lds32(code_addr<P>(kb, kr, 16 * ks + 4 * tq)), b0, b1);
-            s8x4_to_f16(lds32(code_addr<P>(kb, kr + 8, 16 * ks + 4 * tq)), b2, b3);
-            mma16816<false>(sc[0], qa[ks], b0, b1);
-            mma16816<false>(sc[1], qa[ks], b2, b3);
+          for (int j = 0; j < NKS / 4; ++j) {  // 16 bytes of each row: 4 k-steps
+            uint32_t u[4], v[4];
+            lds_run<16>(code_addr<P>(kb, kr, (HS / 4) * tq + 16 * j), u);
+            lds_run<16>(code_addr<P>(kb, kr + 8, (HS / 4) * tq + 16 * j), v);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint32_t b0, b1, b2, b3;
+              s8x4_to_f16(u[i], b0, b1);
+              s8x4_to_f16(v[i], b2, b3);
+              mma16816<false>(sc[0], qa[4 * j + i], b0, b1);
+              mma16816<false>(sc[1], qa[4 * j + i], b2, b3);
+            }
           }
         } else {
           const int kr = 16 * w + gq;
 #pragma unroll
-          for (int k2 = 0; k2 < NKS / 2; ++k2) {
+          for (int j = 0; j < NKS / 8; ++j) {  // 16 bytes of each row: 8 k-steps
             uint32_t u[4], v[4];
-            s4x8_to_f16(lds32(code_addr<P>(kb, kr, 16 * k2 + 4 * tq)), u);
-            s4x8_to_f16(lds32(code_addr<P>(kb, kr + 8, 16 * k2 + 4 * tq)), v);
-            mma16816<false>(sc[0], qa[2 * k2], u[0], u[1]);
-            mma16816<false>(sc[0], qa[2 * k2 + 1], u[2], u[3]);
-            mma16816<false>(sc[1], qa[2 * k2], v[0], v[1]);
-            mma16816<false>(sc[1], qa[2 * k2 + 1], v[2], v[3]);
+            lds_run<16>(code_addr<P>(kb, kr, (HS / 8) * tq + 16 * j), u);
+            lds_run<16>(code_addr<P>(kb, kr + 8, (HS / 8) * tq + 16 * j), v);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int k2 = 4 * j + i;
+              uint32_t uu[4], vv[4];
+              s4x8_to_f16(u[i], uu);
+              s4x8_to_f16(v[i], vv);
+              mma16816<false>(sc[0], qa[2 * k2], uu[0], uu[1]);
+              mma16816<false>(sc[0], qa[2 * k2 + 1], uu[2], uu[3]);
+              mma16816<false>(sc[1], qa[2 * k2], vv[0], vv[1]);
+              mma16816<false>(sc[1], qa[2 * k2 + 1], vv[2], vv[3]);
+            }
           }
         }
         // ---- online softmax (base 2) ----
@@ -357,37 +383,54 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
           pa[2] = pack2<false>(p[1][0], p[1][1]);
           pa[3] = pack2<false>(p[1][2], p[1][3]);
         }
+        if (!__all_sync(0xffffffffu, al0 == 1.f && al1 == 1.f)) {  // (no row's max grew: O stays)
 #pragma unroll
-        for (int d = 0; d < ND; ++d) {
-          o[d][0] *= al0;
-          o[d][1] *= al0;
-          o[d][2] *= al1;
-          o[d][3] *= al1;
+          for (int d = 0; d < ND; ++d) {
+            o[d][0] *= al0;
+            o[d][1] *= al0;
+            o[d][2] *= al1;
+            o[d][3] *= al1;
+          }
         }
         // ---- O (16 x HS) += P (16 x 16) V (16 x HS) ----
         // keys this thread contributes in the transposed V fragments: kw + 2tq + {0,1}, +8
         if constexpr (KQ == 1) {
           // (codes are finite: keys past the item contribute 0 * code = 0)
           const int ka = 16 * w + 2 * tq;  // this thread's keys: ka, ka + 1 (b0), ka + 8, ka + 9 (b1)
+          constexpr int G = HS / 8 < 16 ? HS / 8 : 16;  // channels (bytes) of a run
 #pragma unroll
-          for (int D = 0; D < HS / 32; ++D) {
-            const int byte = 32 * D + 4 * gq;
-            uint32_t lo[4], hi[4];
-            s8_key_pairs(lds32(code_addr<P>(vb, ka, byte)), lds32(code_addr<P>(vb, ka + 1, byte)), lo);
-            s8_key_pairs(lds32(code_addr<P>(vb, ka + 8, byte)), lds32(code_addr<P>(vb, ka + 9, byte)), hi);
+          for (int D = 0; D < ND / G; ++D) {
+            const int byte = D * 8 * G + G * gq;
+            uint32_t w0[G / 4], w1[G / 4], w8[G / 4], w9[G / 4];
+            lds_run<G>(code_addr<P>(vb, ka, byte), w0);
+            lds_run<G>(code_addr<P>(vb, ka + 1, byte), w1);
+            lds_run<G>(code_addr<P>(vb, ka + 8, byte), w8);
+            lds_run<G>(code_addr<P>(vb, ka + 9, byte), w9);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) mma16816<false>(o[4 * D + i], pa, lo[i], hi[i]);
+            for (int i = 0; i < G / 4; ++i) {
+              uint32_t lo[4], hi[4];
+              s8_key_pairs(w0[i], w1[i], lo);
+              s8_key_pairs(w8[i], w9[i], hi);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) mma16816<false>(o[D * G + 4 * i + e], pa, lo[e], hi[e]);
+            }
           }
         } else if constexpr (KQ == 2) {
           const int ka = 16 * w + 2 * tq;
+          constexpr int R = HS / 16;  // bytes of the thread's HS / 8 channels in a key row
+          const int byte = R * gq;
+          uint32_t w0[R / 4], w1[R / 4], w8[R / 4], w9[R / 4];
+          lds_run<R>(code_addr<P>(vb, ka, byte), w0);
+          lds_run<R>(code_addr<P>(vb, ka + 1, byte), w1);
+          lds_run<R>(code_addr<P>(vb, ka + 8, byte), w8);
+          lds_run<R>(code_addr<P>(vb, ka + 9, byte), w9);
 #pragma unroll
-          for (int D = 0; D < HS / 64; ++D) {
-            const int byte = 32 * D + 4 * gq;
+          for (int i = 0; i < R / 4; ++i) {
             uint32_t lo[8], hi[8];
-            s4_key_pairs(lds32(code_addr<P>(vb, ka, byte)), lds32(code_addr<P>(vb, ka + 1, byte)), lo);
-            s4_key_pairs(lds32(code_addr<P>(vb, ka + 8, byte)), lds32(code_addr<P>(vb, ka + 9, byte)), hi);
+            s4_key_pairs(w0[i], w1[i], lo);
+            s4_key_pairs(w8[i], w9[i], hi);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mma16816<false>(o[8 * D + i], pa, lo[i], hi[i]);
+            for (int e = 0; e < 8; ++e) mma16816<false>(o[8 * i + e], pa, lo[e], hi[e]);
           }
         } else {
           uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
@@ -461,7 +504,7 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
                 *c1p = make_float2(b1.x + a1.x, b1.y + a1.y);
               }
             } else {  // integer caches: the columns' channels in natural order
-              const int ch0 = out_channel<KQ>(d, 2 * tq), ch1 = out_channel<KQ>(d, 2 * tq + 1);
+              const int ch0 = out_channel<HS, KQ>(d, 2 * tq), ch1 = out_channel<HS, KQ>(d, 2 * tq + 1);
               float* c0p = cw + r0 * kCombStride;
               float* c1p = cw + r1 * kCombStride;
               if (rr == 0) {
