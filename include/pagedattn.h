@@ -32,7 +32,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 5
+#define PA_ABI_VERSION 6
 
 typedef enum pa_status {
   PA_OK = 0,
@@ -100,6 +100,12 @@ typedef struct pa_dims {
   int32_t kv_dtype;                /* pa_kv_dtype of the caches: INT8 with head_size 64, 128 or 256,
                                       INT4 with 128 or 256 (else PA_ERR_UNSUPPORTED); integer caches
                                       need pa_paged_attention_ex with both scales */
+  int32_t decode_sms;              /* 0 (normal): when a whole call has both prefill-class and
+                                      decode-class rows, the planner splits the SMs so that the
+                                      prefill kernel (tensor-bound) and the decode kernel (HBM-bound)
+                                      run at the same time, choosing the decode share from a model of
+                                      their rates. > 0 fixes that share at this many SMs (at most all
+                                      but one): a tuning and test hook. Results do not depend on it. */
 } pa_dims;
 
 /*

@@ -210,6 +210,33 @@ def test_balanced_partition_splits_long_units_across_ctas():
     assert np.array_equal(a["out_bits"], b["out_bits"])
 
 
+# A whole call with prefill-class and decode-class rows runs the two attention kernels at the
+# same time on SMs the planner splits between them (pa_dims.decode_sms fixes the decode share).
+# Results must not depend on the split, from one decode SM to all but one.
+MIXED = {
+    "mixed-packed-drops": lambda: _case("mixed-packed-drops"),
+    "mixed-long-decode-bf16": lambda: w.make_problem(
+        name="mixed-long-decode-bf16", seed=13, dtype="bf16", num_heads=32, kv_num_heads=8, head_size=128,
+        block_size=16, past=[9000, 0, 4000, 700, 12000, 33], q_lens=[1, 300, 2, 1, 4, 129]),
+    "mixed-head64": lambda: w.make_problem(
+        name="mixed-head64", seed=14, dtype="fp16", num_heads=8, kv_num_heads=2, head_size=64,
+        block_size=32, past=[2000, 10, 0], q_lens=[1, 200, 3]),
+}
+
+
+@pytest.mark.parametrize("dsm", [0, 1, 5, 76, 151, 4096])
+@pytest.mark.parametrize("name", sorted(MIXED))
+def test_mixed_batches_on_split_sms(name, dsm):
+    check(MIXED[name](), decode_sms=dsm)
+
+
+def test_split_sms_are_bitwise_deterministic():
+    p = MIXED["mixed-long-decode-bf16"]()
+    a = run_gpu(p)
+    b = run_gpu(p)
+    assert np.array_equal(a["out_bits"], b["out_bits"])
+
+
 # ---- device-side error reporting (no faults) ----------------------------------------------------
 
 def test_out_of_range_block_is_reported_and_read_as_zeros():

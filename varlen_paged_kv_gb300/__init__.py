@@ -45,7 +45,7 @@ class PaDims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_tokens", "batch_size", "head_size", "num_blocks", "block_size",
         "max_blocks_per_sequence", "dtype", "decode_split_keys", "route", "max_query_len", "qk_prep",
-        "kv_dtype")]
+        "kv_dtype", "decode_sms")]
 
 
 class PaQkPrep(ctypes.Structure):
@@ -95,11 +95,12 @@ def load_library():
 
 
 def make_dims(num_tokens, batch_size, head_size, num_blocks, block_size, max_blocks_per_sequence, dtype,
-              decode_split_keys=0, route=ROUTE_AUTO, max_query_len=0, qk_prep=False, kv_dtype=KV_SAME) -> PaDims:
+              decode_split_keys=0, route=ROUTE_AUTO, max_query_len=0, qk_prep=False, kv_dtype=KV_SAME,
+              decode_sms=0) -> PaDims:
     code = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
     return PaDims(int(num_tokens), int(batch_size), int(head_size), int(num_blocks), int(block_size),
                   int(max_blocks_per_sequence), code, int(decode_split_keys), int(route), int(max_query_len),
-                  int(bool(qk_prep)), int(_KV_FORMATS.get(kv_dtype, kv_dtype)))
+                  int(bool(qk_prep)), int(_KV_FORMATS.get(kv_dtype, kv_dtype)), int(decode_sms))
 
 
 def workspace_size(dims: PaDims, num_heads: int, kv_num_heads: int) -> int:
@@ -135,7 +136,8 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
                     stages: int = STAGE_ALL, stream: Optional[torch.cuda.Stream] = None,
                     lse: Optional[torch.Tensor] = None, qk_prep: Optional[dict] = None,
                     output_gate: Optional[torch.Tensor] = None, kv_quant: Optional[str] = None,
-                    k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None) -> torch.Tensor:
+                    k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
+                    decode_sms: int = 0) -> torch.Tensor:
     """com.microsoft.PagedAttention on CUDA tensors. Writes key_cache / value_cache in
     place and returns ``output`` (num_tokens, num_heads * head_size).
 
@@ -218,7 +220,8 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
     if cumulative_sequence_length.shape[0] != B + 1 or block_table.shape[0] != B:
         raise ValueError("cumulative_sequence_length must have batch_size + 1 entries, block_table batch_size rows")
     dims = make_dims(N, B, head_size, num_blocks, block_size, block_table.shape[1], query.dtype,
-                     decode_split_keys, route, max_query_len, qk_prep is not None, _KV_FORMATS[kv_quant])
+                     decode_split_keys, route, max_query_len, qk_prep is not None, _KV_FORMATS[kv_quant],
+                     decode_sms)
     if output is None:
         output = torch.empty((N, num_heads * head_size), dtype=query.dtype, device=query.device)
     if workspace is None:

@@ -172,6 +172,10 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
   DeviceInfo info;
   if (!device_info(&info)) return cuda_fail(cudaGetLastError(), "device query");
   args.dec_ctas = std::min(pa::dec_ctas_per_sm(args.hs) * info.sms, pa::kMaxDecCtas);
+  args.sms = info.sms;
+  // a whole call may run its prefill and decode kernels side by side on split SMs; a call of
+  // some stages only runs each kernel on the whole GPU
+  args.split_sms = stages == PA_STAGE_ALL;
   const pa_dtype dt = (pa_dtype)d->dtype;
   const bool bf16 = dt == PA_BFLOAT16;
   const int hs = args.hs;
@@ -202,6 +206,7 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
     aq.q_stride = args.nh * hs;
     query = args.qprep;
   }
+  bool prefill_launched = false;
   if ((stages & PA_STAGE_PREFILL) && can_prefill && args.N > 0 && slots > 0) {
     const int seg = gcd(d->block_size, pa::kPreTileK);
     CUtensorMap tq, tk, tv, tvm;
@@ -225,6 +230,7 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
       ++g_launches;
       if (cudaError_t e = pa::launch_prefill(aq, bf16, tq, tk, tv, tvm, seg, grid, stream))
         return cuda_fail(e, "prefill_kernel launch");
+      prefill_launched = true;
     }
   }
   if ((stages & PA_STAGE_DECODE) && can_decode && args.N > 0 && slots > 0) {
@@ -240,6 +246,7 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
       return PA_ERR_CUDA;
     }
     ++g_launches;
+    aq.dec_after_prefill = prefill_launched;  // runs beside this call's prefill kernel
     if (cudaError_t e = pa::launch_decode(aq, bf16, tk, tv, seg, stream)) return cuda_fail(e, "decode_kernel launch");
   }
   return PA_OK;
@@ -333,6 +340,7 @@ pa_status run(const void* query, const void* key, const void* value, void* key_c
   a.k_offset = a.packed ? num_heads * hs : 0;
   a.v_offset = a.packed ? (num_heads + kv_num_heads) * hs : 0;
   a.forced_split = dims->decode_split_keys;
+  a.decode_sms = dims->decode_sms;
   a.route = dims->route;
   a.max_query_len = dims->max_query_len;
   a.out_v8 = aligned(output, 32);

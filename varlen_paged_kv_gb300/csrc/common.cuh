@@ -28,6 +28,11 @@ __host__ __device__ constexpr int dec_ctas_per_sm(int hs) { return hs == 256 ? 1
 // at head_size 256 with one CTA per SM, 1.5-2 us against 1.4 us at 128 with two).
 __host__ __device__ constexpr int dec_item_cost_tiles(int hs) { return hs == 256 ? 3 : 1; }
 constexpr int kMaxDecCtas = 1024;     // upper bound of the decode grid
+// rates of the planner's model that splits the SMs between the prefill and the decode
+// kernel of a call with both kinds of rows (measured on GB300 at head_size 128)
+constexpr float kSplitPreFlops = 8.0e12f;   // prefill FLOP/s per SM, 128 x 128 tiles counted whole
+constexpr float kSplitDecBytes = 68.0e9f;   // decode K/V bytes/s per SM while HBM is not the limit
+constexpr float kSplitHbmBytes = 5.9e12f;   // decode K/V bytes/s of the whole chip
 constexpr int kPreTileQ = 128;        // query rows per prefill tile (MMA M)
 constexpr int kPreTileK = 128;        // keys per prefill KV tile (MMA N of Q K^T, K of P V)
 constexpr int kSortCap = 4096;        // prefill tiles the planner sorts by cost
@@ -43,7 +48,8 @@ struct WsHeader {
   uint32_t v_mirror_bad;    // set by the copy kernel when a value does not fit fp16
   int32_t mirror_rows;      // rows of the copy in use
   int32_t mirror_seqs;      // sequences copied (entries of mirror_seq)
-  int32_t pad[55];
+  int32_t pre_ctas;         // prefill CTAs that take units (0: the whole grid); the others exit
+  int32_t pad[54];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
@@ -159,6 +165,14 @@ struct Args {
   int32_t route;
   int32_t max_query_len;  // > 0: host bound on every q_len (checked by the planner)
   int32_t dec_ctas;       // decode grid size
+  int32_t sms;            // SMs of the device
+  // A whole call that launches both attention kernels may run them at the same time: the
+  // planner gives the decode work d SMs (decode_sms > 0 fixes d) and the prefill kernel the
+  // other SMs; the decode kernel, launched after the prefill kernel, then does not wait for
+  // it to finish before starting (dec_after_prefill), only before exiting.
+  int32_t split_sms;
+  int32_t decode_sms;
+  int32_t dec_after_prefill;
   int32_t out_v8;         // output 32-byte aligned (prefill stores 32-byte chunks)
   float scale_log2;       // scale * log2(e)
   WsHeader* hdr;
@@ -225,6 +239,7 @@ struct PreSmem {
   static constexpr int kNumBars = 18;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
+  static constexpr int kPreCtas = kAbort + 4;  // CTAs of the grid that take units
   // row-max exchange between the two warps that share a TMEM lane quarter:
   // float [tile parity][head][row][column half]
   static constexpr int kXmax = kAbort + 12;
@@ -269,9 +284,15 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // longest-first assignment (a plain round robin gives the first CTAs the most work in
 // every round). Strictly increasing in k, so a CTA's loop ends at its first unit past the
 // end.
-__device__ __forceinline__ int snake_unit(int k) {
-  const int g = (int)gridDim.x;
+__device__ __forceinline__ int snake_unit(int k, int g) {
   return k * g + ((k & 1) ? g - 1 - (int)blockIdx.x : (int)blockIdx.x);
+}
+
+// CTAs of a prefill grid that take units: the planner's share when it split the SMs
+// between the prefill and the decode kernels of one call, else the whole grid
+__device__ __forceinline__ int prefill_ctas(const Args& a) {
+  const int p = a.split_sms ? a.hdr->pre_ctas : 0;
+  return p > 0 && p < (int)gridDim.x ? p : (int)gridDim.x;
 }
 
 // the record of unit u (all zeros past the end)

@@ -187,9 +187,18 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
     fence_mbar_init();
   }
   __syncthreads();
-  pdl_wait();  // the work lists and caches written by the earlier kernels of this call
+  // the work lists and caches written by the earlier kernels of this call. Launched after
+  // this call's prefill kernel, which starts its dependents only once its own wait for
+  // those kernels has returned, the kernel runs beside the prefill (on the SMs the planner
+  // took from it) and waits for it only before exiting, so that the next call still finds
+  // both finished.
+  const bool beside_prefill = a.dec_after_prefill != 0;
+  if (!beside_prefill) pdl_wait();
   pdl_launch_dependents();
-  if (!a.hdr->valid) return;  // a refused batch: the item ranges are not this call's
+  if (!a.hdr->valid) {  // a refused batch: the item ranges are not this call's
+    if (beside_prefill) pdl_wait();
+    return;
+  }
   const int it_begin = a.cta_begin[blockIdx.x], it_end = a.cta_begin[blockIdx.x + 1];
 
   if (warp == kDecWarps) {
@@ -636,6 +645,7 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
     }
     consumer_bar();  // comb, mw, lw are reused by the next item
   }
+  if (beside_prefill) pdl_wait();
 }
 
 // ---- host launchers (kernels are launched from the translation unit that defines them) ----

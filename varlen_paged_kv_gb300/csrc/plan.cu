@@ -152,15 +152,18 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
   __shared__ long long s_w64[32];
   __shared__ long long s_mirror_carry;
   __shared__ int s_mseq_carry;
+  __shared__ unsigned long long s_pre_tiles;  // (query tile, key tile) pairs of prefill-class rows
+  __shared__ unsigned long long s_split;      // best (model time bits, decode SMs)
 
   const int tid = threadIdx.x;
   WsHeader* hdr = a.hdr;
-  const int64_t P = a.dec_ctas;
   pdl_wait();  // the previous call's kernels may still read this workspace
   pdl_launch_dependents();
   if (tid == 0) {
     s_bad = 0;
     s_dec_tiles = 0;
+    s_pre_tiles = 0;
+    s_split = ~0ull;
     s_carry[0] = s_carry[1] = s_carry[2] = 0;
     s_mirror_carry = 0;
     s_mseq_carry = 0;
@@ -169,13 +172,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
     hdr->v_mirror_bad = 0;
     hdr->mirror_rows = 0;
   }
-  for (int c = tid; c <= P; c += blockDim.x) s_cta_begin[c] = INT_MAX;
+  for (int c = tid; c <= a.dec_ctas; c += blockDim.x) s_cta_begin[c] = INT_MAX;
   __syncthreads();
 
   // ---- validate the batch description; count the decode key tiles ----
   const int64_t max_kv = (int64_t)a.max_blocks * a.bs;
   if (tid == 0 && (a.cum[0] != 0 || a.cum[a.B] != a.N)) s_bad = 1;
-  long long dec_tiles = 0;
+  long long dec_tiles = 0, pre_tiles = 0;
   for (int b = tid; b < a.B; b += blockDim.x) {
     const int64_t q = (int64_t)a.cum[b + 1] - a.cum[b];
     const int64_t kv = (int64_t)a.past[b] + q;
@@ -183,17 +186,47 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
       atomicOr(&s_bad, 1);
     } else if (is_decode_class(q, a)) {
       dec_tiles += ceil_div(kv, kDecTile) + dec_item_cost_tiles(a.hs);
+    } else if (q > 0 && a.split_sms) {
+      // key tiles seen by the query tiles t = 0 .. T-1: ceil((past + 128 (t + 1)) / 128) =
+      // c + t + 1 with c = ceil(past / 128) for all but the last, which sees ceil(kv / 128)
+      static_assert(kPreTileQ == kPreTileK, "the closed form assumes square tiles");
+      const int64_t T = ceil_div(q, kPreTileQ), c = ceil_div(kv - q, kPreTileK);
+      pre_tiles += (T - 1) * T / 2 + (T - 1) * c + ceil_div(kv, kPreTileK);
     }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) dec_tiles += __shfl_xor_sync(0xffffffffu, dec_tiles, o);
+  for (int o = 16; o > 0; o >>= 1) {
+    dec_tiles += __shfl_xor_sync(0xffffffffu, dec_tiles, o);
+    pre_tiles += __shfl_xor_sync(0xffffffffu, pre_tiles, o);
+  }
   if ((tid & 31) == 0 && dec_tiles) atomicAdd(&s_dec_tiles, (unsigned long long)dec_tiles);
+  if ((tid & 31) == 0 && pre_tiles) atomicAdd(&s_pre_tiles, (unsigned long long)pre_tiles);
   for (int u = tid; u < a.B * a.kvh; u += blockDim.x) a.unit_done[u] = 0;
   __syncthreads();
   if (s_bad) {
     if (tid == 0) refuse(hdr);
     return;
   }
+  // ---- SMs of the two attention kernels of a whole call with prefill and decode rows ----
+  // The prefill kernel keeps S - d SMs and the decode work is cut for the other d, so the
+  // tensor-bound prefill and the HBM-bound decode run at the same time. d minimises the
+  // larger of the two times of a model with rates measured on GB300: prefill at
+  // kSplitPreFlops per SM (128 x 128 tiles counted whole), decode at kSplitDecBytes per SM
+  // up to kSplitHbmBytes for the chip.
+  const int S = a.sms;
+  const bool split = a.split_sms && s_dec_tiles > 0 && s_pre_tiles > 0 && S > 1;
+  if (split && a.decode_sms <= 0 && tid < S - 1) {
+    const int d = tid + 1;
+    const float flops = (float)s_pre_tiles * (float)a.nh * (float)(kPreTileQ * kPreTileK) * (float)a.hs * 4.f;
+    const float bytes = (float)s_dec_tiles * (float)a.kvh * (float)(kDecTile * a.hs * 2 * 2);
+    const float tp = flops / ((float)(S - d) * kSplitPreFlops);
+    const float td = bytes / fminf(kSplitHbmBytes, (float)d * kSplitDecBytes);
+    atomicMin(&s_split, ((unsigned long long)__float_as_uint(fmaxf(tp, td)) << 32) | (unsigned)d);
+  }
+  __syncthreads();
+  int dec_sms = S;
+  if (split) dec_sms = a.decode_sms > 0 ? min(a.decode_sms, S - 1) : (int)(s_split & 0xFFFFFFFFull);
+  const int64_t P = split ? min((int64_t)dec_sms * dec_ctas_per_sm(a.hs), (int64_t)a.dec_ctas) : a.dec_ctas;
   const bool balanced = a.forced_split <= 0;
   // The decode units, laid end to end, each as V virtual tiles (the cost of an item beyond
   // its keys) followed by its key tiles, span W tiles; they are cut into P equal ranges:
@@ -351,7 +384,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
     for (int64_t c = tid; c <= P; c += blockDim.x) s_cta_begin[c] = (int)(c * n_items / P);
   }
   __syncthreads();
-  for (int c = tid; c <= P; c += blockDim.x) a.cta_begin[c] = s_cta_begin[c];
+  for (int c = tid; c <= a.dec_ctas; c += blockDim.x) a.cta_begin[c] = c <= P ? s_cta_begin[c] : n_items;
 
   // ---- prefill tiles: sort by KV-tile count, descending (ties: list order) ----
   if (n_tiles <= kSortCap) {
@@ -396,6 +429,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
     hdr->n_decode_items = n_items;
     hdr->n_prefill_tiles = n_tiles;
     hdr->dec_ctas = (int)P;
+    hdr->pre_ctas = split ? S - dec_sms : 0;
   }
 }
 

@@ -109,7 +109,14 @@ __global__ void __launch_bounds__(kPreThreads, 1)
   const bool v16 = BF16 && a.hdr->v_mirror && !a.hdr->v_mirror_bad;
   const int hpu = pair ? 2 : 1;
   const int units_per_tile = a.nh / hpu;
-  const int n_units = a.hdr->n_prefill_tiles * units_per_tile;
+  // units dealt to the CTAs that take work; the others (the planner gave their SMs to the
+  // decode kernel of this call) run no loop and release their TMEM at once
+  // (the count is kept in shared memory and read where a unit index is formed: a register
+  // held across the kernel pushes the softmax warps over their register budget)
+  volatile int* pre_ctas = reinterpret_cast<volatile int*>(smem + L::kPreCtas);
+  if (threadIdx.x == 0) *pre_ctas = prefill_ctas(a);
+  __syncthreads();
+  const int n_units = (int)blockIdx.x < *pre_ctas ? a.hdr->n_prefill_tiles * units_per_tile : 0;
   const int64_t cache_rows = (int64_t)a.num_blocks * a.bs;
 
   if (warp == 0) {
@@ -123,13 +130,13 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     const int nseg = kPreTileK / seg_rows;
     uint32_t gs = 0, unit_cnt = 0;
     // records of the current and the next two units, each loaded two units ahead of use
-    PrefillTile next = load_tile(a, snake_unit(0), n_units, units_per_tile);
-    PrefillTile next2 = load_tile(a, snake_unit(1), n_units, units_per_tile);
-    for (int u = snake_unit(0); u < n_units; u = snake_unit(++unit_cnt)) {
+    PrefillTile next = load_tile(a, snake_unit(0, *pre_ctas), n_units, units_per_tile);
+    PrefillTile next2 = load_tile(a, snake_unit(1, *pre_ctas), n_units, units_per_tile);
+    for (int u = snake_unit(0, *pre_ctas); u < n_units; u = snake_unit(++unit_cnt, *pre_ctas)) {
       const PrefillTile tile = next;
       next = next2;
-      const int un = snake_unit(unit_cnt + 1);
-      next2 = load_tile(a, snake_unit(unit_cnt + 2), n_units, units_per_tile);
+      const int un = snake_unit(unit_cnt + 1, *pre_ctas);
+      next2 = load_tile(a, snake_unit(unit_cnt + 2, *pre_ctas), n_units, units_per_tile);
       const int h0 = (u % units_per_tile) * hpu, g = h0 / a.G;
       const int c0 = tile.c0, q_len = tile.q_len, past = tile.past;
       const int kv_len = past + q_len;
@@ -199,10 +206,10 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     const uint64_t kdesc0 = sdesc_sw128(smem_u32(smem + L::kK0), 16, 1024);
     const uint64_t vdesc0 = sdesc_sw128(smem_u32(smem + L::kV0), L::kHalfBytes, 1024);
     uint32_t gs = 0, unit_cnt = 0;
-    PrefillTile next = load_tile(a, snake_unit(0), n_units, units_per_tile);
-    for (int u = snake_unit(0); u < n_units; u = snake_unit(++unit_cnt)) {
+    PrefillTile next = load_tile(a, snake_unit(0, *pre_ctas), n_units, units_per_tile);
+    for (int u = snake_unit(0, *pre_ctas); u < n_units; u = snake_unit(++unit_cnt, *pre_ctas)) {
       const PrefillTile tile = next;  // loaded one unit ahead
-      next = load_tile(a, snake_unit(unit_cnt + 1), n_units, units_per_tile);
+      next = load_tile(a, snake_unit(unit_cnt + 1, *pre_ctas), n_units, units_per_tile);
       const int kv_len = tile.past + tile.q_len;
       const int n_kv = tile.n_kv;
       mbar_wait(q_full, unit_cnt & 1, abort, err);
@@ -315,8 +322,8 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       const int pair_bar = 2 + x * 4 + quarter;  // named barrier of the two warps of this lane quarter
       const float c = a.scale_log2;
       uint32_t gs = 0;
-      PrefillTile next = load_tile(a, snake_unit(0), n_units, units_per_tile);
-      for (int k = 0, u = snake_unit(0); u < n_units; u = snake_unit(++k)) {
+      PrefillTile next = load_tile(a, snake_unit(0, *pre_ctas), n_units, units_per_tile);
+      for (int k = 0, u = snake_unit(0, *pre_ctas); u < n_units; u = snake_unit(++k, *pre_ctas)) {
         const PrefillTile tile = next;  // loaded during the previous unit's epilogue
         const int h = (u % units_per_tile) * hpu + x;
         const int c0 = tile.c0, q_len = tile.q_len, past = tile.past;
@@ -452,7 +459,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         // ---- epilogue: wait for the last P V, normalise, store the valid rows ----
         // (the next unit's record is loaded here, where few registers are live, and
         // arrives while this unit's output is written)
-        next = load_tile(a, snake_unit(k + 1), n_units, units_per_tile);
+        next = load_tile(a, snake_unit(k + 1, *pre_ctas), n_units, units_per_tile);
         mbar_wait(&o_done[x], (gs + n_kv - 1) & 1, abort, err);
         tc_fence_after();
         {

@@ -46,8 +46,9 @@ struct Smem {
   static constexpr int kNumBars = 2 + 2 * kChunks + 2 + 3;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
+  static constexpr int kPreCtas = kAbort + 4;  // CTAs of the grid that take units
   // row-max exchange between the two warps of a lane quarter: float [tile parity][row][half]
-  static constexpr int kXmax = (kAbort + 4 + 15) / 16 * 16;
+  static constexpr int kXmax = (kPreCtas + 4 + 15) / 16 * 16;
   // row-sum exchange at the end of a unit: float [row][half]
   static constexpr int kXsum = kXmax + 2 * kPreTileQ * 2 * 4;
   static constexpr int kBytes = kXsum + kPreTileQ * 2 * 4 + 1024;  // + alignment slack
@@ -111,7 +112,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   // value fp16 cannot hold (then bf16 V, P as hi + lo)
   const bool v16 = BF16 && a.hdr->v_mirror && !a.hdr->v_mirror_bad;
   const int units_per_tile = a.nh;  // one head per unit
-  const int n_units = a.hdr->n_prefill_tiles * units_per_tile;
+  // units dealt to the CTAs that take work; the others (the planner gave their SMs to the
+  // decode kernel of this call) run no loop and release their TMEM at once
+  // (the count is kept in shared memory and read where a unit index is formed: a register
+  // held across the kernel pushes the softmax warps over their register budget)
+  volatile int* pre_ctas = reinterpret_cast<volatile int*>(smem + L::kPreCtas);
+  if (threadIdx.x == 0) *pre_ctas = prefill_ctas(a);
+  __syncthreads();
+  const int n_units = (int)blockIdx.x < *pre_ctas ? a.hdr->n_prefill_tiles * units_per_tile : 0;
   const int64_t cache_rows = (int64_t)a.num_blocks * a.bs;
 
   if (warp == 0) {
@@ -124,13 +132,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int nseg = kPreTileK / seg_rows;
     uint32_t gc = 0, unit_cnt = 0;
-    PrefillTile next = load_tile(a, snake_unit(0), n_units, units_per_tile);
-    PrefillTile next2 = load_tile(a, snake_unit(1), n_units, units_per_tile);
-    for (int u = snake_unit(0); u < n_units; u = snake_unit(++unit_cnt)) {
+    PrefillTile next = load_tile(a, snake_unit(0, *pre_ctas), n_units, units_per_tile);
+    PrefillTile next2 = load_tile(a, snake_unit(1, *pre_ctas), n_units, units_per_tile);
+    for (int u = snake_unit(0, *pre_ctas); u < n_units; u = snake_unit(++unit_cnt, *pre_ctas)) {
       const PrefillTile tile = next;
       next = next2;
-      const int un = snake_unit(unit_cnt + 1);
-      next2 = load_tile(a, snake_unit(unit_cnt + 2), n_units, units_per_tile);
+      const int un = snake_unit(unit_cnt + 1, *pre_ctas);
+      next2 = load_tile(a, snake_unit(unit_cnt + 2, *pre_ctas), n_units, units_per_tile);
       const int h = u % units_per_tile, g = h / a.G;
       const int kv_len = tile.past + tile.q_len;
       const int n_kv = tile.n_kv;
@@ -194,10 +202,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t vdesc0 = sdesc_sw128(smem_u32(smem + L::kCh0), L::kSlab, 1024);
     constexpr uint32_t kSlab16 = L::kSlab >> 4;
     uint32_t gc = 0, gs = 0, unit_cnt = 0;
-    PrefillTile next = load_tile(a, snake_unit(0), n_units, units_per_tile);
-    for (int u = snake_unit(0); u < n_units; u = snake_unit(++unit_cnt)) {
+    PrefillTile next = load_tile(a, snake_unit(0, *pre_ctas), n_units, units_per_tile);
+    for (int u = snake_unit(0, *pre_ctas); u < n_units; u = snake_unit(++unit_cnt, *pre_ctas)) {
       const PrefillTile tile = next;  // loaded one unit ahead
-      next = load_tile(a, snake_unit(unit_cnt + 1), n_units, units_per_tile);
+      next = load_tile(a, snake_unit(unit_cnt + 1, *pre_ctas), n_units, units_per_tile);
       const int kv_len = tile.past + tile.q_len;
       const int n_kv = tile.n_kv;
       mbar_wait(q_full, unit_cnt & 1, abort, err);
@@ -302,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pair_bar = 2 + quarter;  // named barrier of the two warps of this lane quarter
     const float c = a.scale_log2;
     uint32_t gs = 0;
-    PrefillTile next = load_tile(a, snake_unit(0), n_units, units_per_tile);
-    for (int k = 0, u = snake_unit(0); u < n_units; u = snake_unit(++k)) {
+    PrefillTile next = load_tile(a, snake_unit(0, *pre_ctas), n_units, units_per_tile);
+    for (int k = 0, u = snake_unit(0, *pre_ctas); u < n_units; u = snake_unit(++k, *pre_ctas)) {
       const PrefillTile tile = next;  // loaded during the previous unit's epilogue
       const int h = u % units_per_tile;
       const int c0 = tile.c0, q_len = tile.q_len, past = tile.past;
@@ -435,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(p_full);
       }
       // ---- epilogue: wait for the last P V, normalise, store the valid rows ----
-      next = load_tile(a, snake_unit(k + 1), n_units, units_per_tile);
+      next = load_tile(a, snake_unit(k + 1, *pre_ctas), n_units, units_per_tile);
       mbar_wait(o_done, (gs + n_kv - 1) & 1, abort, err);
       tc_fence_after();
       {
