@@ -30,8 +30,8 @@ __host__ __device__ constexpr int dec_item_cost_tiles(int hs) { return hs == 256
 constexpr int kMaxDecCtas = 1024;     // upper bound of the decode grid
 // rates of the planner's model that splits the SMs between the prefill and the decode
 // kernel of a call with both kinds of rows (measured on GB300 at head_size 128)
-constexpr float kSplitPreFlops = 8.0e12f;   // prefill FLOP/s per SM, 128 x 128 tiles counted whole
-constexpr float kSplitDecBytes = 68.0e9f;   // decode K/V bytes/s per SM while HBM is not the limit
+constexpr float kSplitPreFlops = 8.2e12f;   // prefill FLOP/s per SM, 128 x 128 tiles counted whole
+constexpr float kSplitDecBytes = 85.0e9f;   // decode K/V bytes/s per SM while HBM is not the limit
 constexpr float kSplitHbmBytes = 5.9e12f;   // decode K/V bytes/s of the whole chip
 constexpr int kPreTileQ = 128;        // query rows per prefill tile (MMA M)
 constexpr int kPreTileK = 128;        // keys per prefill KV tile (MMA N of Q K^T, K of P V)

@@ -261,7 +261,24 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
   const int w = warp;
   const int tq = lane & 3, gq = lane >> 2;  // quad position, row within the 8-row group
   const int r0 = gq, r1 = gq + 8;           // the two rows this thread holds in MMA fragments
-  uint32_t cnt = 0;
+  int stage = 0;  // ring slot and phase of the next tile
+  uint32_t phase = 0;
+  // integer caches: this thread's byte offsets inside a stage's K tile (its runs of key row
+  // 16w + gq; row + 8 has the same swizzle, 8 rows further) and V tile (its runs of key rows
+  // 16w + 2tq and 16w + 2tq + 1; rows + 8 likewise)
+  constexpr int KRUN = KQ == 1 ? HS / 4 : HS / 8;             // bytes of a K run
+  constexpr int VG = KQ == 1 ? (HS / 8 < 16 ? HS / 8 : 16) : HS / 16;  // bytes of a V run
+  constexpr int NVR = KQ == 1 ? (HS / 8) / VG : 1;           // V runs per key row
+  uint32_t koff[KQ == 0 ? 1 : KRUN / 16], voff[2][NVR];
+  if constexpr (KQ != 0) {
+#pragma unroll
+    for (int j = 0; j < KRUN / 16; ++j) koff[j] = code_addr<P>(0, 16 * w + gq, KRUN * tq + 16 * j);
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+      for (int D = 0; D < NVR; ++D)
+        voff[e][D] = code_addr<P>(0, 16 * w + 2 * tq + e, KQ == 1 ? D * 8 * VG + VG * gq : VG * gq);
+  }
   DecodeItem next = load_item(a, it_begin, it_end);
   for (int it = it_begin; it < it_end; ++it) {
     const DecodeItem item = next;  // loaded one item ahead
@@ -281,10 +298,9 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
 #pragma unroll
     for (int d = 0; d < ND; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
 
-    for (int k0 = item.key_begin; k0 < item.key_end; k0 += kDecTile, ++cnt) {
-      const int s = cnt % L::kStages;
-      const uint32_t ph = (cnt / L::kStages) & 1;
-      mbar_wait(&full[s], ph, abort, err);
+    for (int k0 = item.key_begin; k0 < item.key_end; k0 += kDecTile) {
+      const int s = stage;
+      mbar_wait(&full[s], phase, abort, err);
       const int kw = k0 + 16 * w;  // first key of this warp's 16
       if (kw < item.key_end) {
         const uint32_t kb = smem_u32(smem + s * L::kStageBytes);
@@ -306,12 +322,11 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
             mma16816<BF16>(sc[1], qa[ks], b2, b3);
           }
         } else if constexpr (KQ == 1) {
-          const int kr = 16 * w + gq;  // key rows of the two n-tiles: kr, kr + 8
 #pragma unroll
           for (int j = 0; j < NKS / 4; ++j) {  // 16 bytes of each row: 4 k-steps
             uint32_t u[4], v[4];
-            lds_run<16>(code_addr<P>(kb, kr, (HS / 4) * tq + 16 * j), u);
-            lds_run<16>(code_addr<P>(kb, kr + 8, (HS / 4) * tq + 16 * j), v);
+            lds_run<16>(kb + koff[j], u);           // key row 16w + gq
+            lds_run<16>(kb + koff[j] + 8 * P, v);   // key row 16w + gq + 8
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               uint32_t b0, b1, b2, b3;
@@ -322,12 +337,11 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
             }
           }
         } else {
-          const int kr = 16 * w + gq;
 #pragma unroll
           for (int j = 0; j < NKS / 8; ++j) {  // 16 bytes of each row: 8 k-steps
             uint32_t u[4], v[4];
-            lds_run<16>(code_addr<P>(kb, kr, (HS / 8) * tq + 16 * j), u);
-            lds_run<16>(code_addr<P>(kb, kr + 8, (HS / 8) * tq + 16 * j), v);
+            lds_run<16>(kb + koff[j], u);
+            lds_run<16>(kb + koff[j] + 8 * P, v);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int k2 = 4 * j + i;
@@ -405,16 +419,15 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
         // keys this thread contributes in the transposed V fragments: kw + 2tq + {0,1}, +8
         if constexpr (KQ == 1) {
           // (codes are finite: keys past the item contribute 0 * code = 0)
-          const int ka = 16 * w + 2 * tq;  // this thread's keys: ka, ka + 1 (b0), ka + 8, ka + 9 (b1)
-          constexpr int G = HS / 8 < 16 ? HS / 8 : 16;  // channels (bytes) of a run
+          // this thread's keys: ka = 16w + 2tq, ka + 1 (b0), ka + 8, ka + 9 (b1)
+          constexpr int G = VG;  // channels (bytes) of a run
 #pragma unroll
           for (int D = 0; D < ND / G; ++D) {
-            const int byte = D * 8 * G + G * gq;
             uint32_t w0[G / 4], w1[G / 4], w8[G / 4], w9[G / 4];
-            lds_run<G>(code_addr<P>(vb, ka, byte), w0);
-            lds_run<G>(code_addr<P>(vb, ka + 1, byte), w1);
-            lds_run<G>(code_addr<P>(vb, ka + 8, byte), w8);
-            lds_run<G>(code_addr<P>(vb, ka + 9, byte), w9);
+            lds_run<G>(vb + voff[0][D], w0);
+            lds_run<G>(vb + voff[1][D], w1);
+            lds_run<G>(vb + voff[0][D] + 8 * P, w8);
+            lds_run<G>(vb + voff[1][D] + 8 * P, w9);
 #pragma unroll
             for (int i = 0; i < G / 4; ++i) {
               uint32_t lo[4], hi[4];
@@ -425,14 +438,12 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
             }
           }
         } else if constexpr (KQ == 2) {
-          const int ka = 16 * w + 2 * tq;
-          constexpr int R = HS / 16;  // bytes of the thread's HS / 8 channels in a key row
-          const int byte = R * gq;
+          constexpr int R = VG;  // bytes of the thread's HS / 8 channels in a key row
           uint32_t w0[R / 4], w1[R / 4], w8[R / 4], w9[R / 4];
-          lds_run<R>(code_addr<P>(vb, ka, byte), w0);
-          lds_run<R>(code_addr<P>(vb, ka + 1, byte), w1);
-          lds_run<R>(code_addr<P>(vb, ka + 8, byte), w8);
-          lds_run<R>(code_addr<P>(vb, ka + 9, byte), w9);
+          lds_run<R>(vb + voff[0][0], w0);
+          lds_run<R>(vb + voff[1][0], w1);
+          lds_run<R>(vb + voff[0][0] + 8 * P, w8);
+          lds_run<R>(vb + voff[1][0] + 8 * P, w9);
 #pragma unroll
           for (int i = 0; i < R / 4; ++i) {
             uint32_t lo[8], hi[8];
@@ -442,35 +453,42 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
             for (int e = 0; e < 8; ++e) mma16816<false>(o[8 * i + e], pa, lo[e], hi[e]);
           }
         } else {
-          uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
-          if (ragged) {  // keys past the item may be unwritten cache slots: keep NaN out of 0 * V
-            const int ka = kw + tq * 2, kb2 = ka + 8;
-            vmask_lo = (ka < item.key_end ? 0x0000ffffu : 0u) | (ka + 1 < item.key_end ? 0xffff0000u : 0u);
-            vmask_hi = (kb2 < item.key_end ? 0x0000ffffu : 0u) | (kb2 + 1 < item.key_end ? 0xffff0000u : 0u);
-          }
           const int mi = lane >> 3, rr = lane & 7;
           const int kr = 16 * w + (mi & 1) * 8 + rr;
+          // keys past the item may be unwritten cache slots: on the item's last tile their V
+          // is cleared, so that no NaN reaches 0 * V (the other tiles skip the masking)
+          auto pv = [&](uint32_t mlo, uint32_t mhi) {
 #pragma unroll
-          for (int dp = 0; dp < ND / 2; ++dp) {
-            const int c = 2 * dp + (mi >> 1);
-            const uint32_t addr = vb + (c >> 3) * (kDecTile * 128) + kr * 128 + (((c & 7) ^ (kr & 7)) << 4);
-            uint32_t v0, v1, v2, v3;
-            ldsm_x4_t(addr, v0, v1, v2, v3);
-            v0 &= vmask_lo;
-            v2 &= vmask_lo;
-            v1 &= vmask_hi;
-            v3 &= vmask_hi;
-            mma16816<BF16>(o[2 * dp], pa, v0, v1);
-            mma16816<BF16>(o[2 * dp + 1], pa, v2, v3);
-            if constexpr (BF16) {
-              mma16816<BF16>(o[2 * dp], pl, v0, v1);
-              mma16816<BF16>(o[2 * dp + 1], pl, v2, v3);
+            for (int dp = 0; dp < ND / 2; ++dp) {
+              const int c = 2 * dp + (mi >> 1);
+              const uint32_t addr = vb + (c >> 3) * (kDecTile * 128) + kr * 128 + (((c & 7) ^ (kr & 7)) << 4);
+              uint32_t v0, v1, v2, v3;
+              ldsm_x4_t(addr, v0, v1, v2, v3);
+              v0 &= mlo;
+              v2 &= mlo;
+              v1 &= mhi;
+              v3 &= mhi;
+              mma16816<BF16>(o[2 * dp], pa, v0, v1);
+              mma16816<BF16>(o[2 * dp + 1], pa, v2, v3);
+              if constexpr (BF16) {
+                mma16816<BF16>(o[2 * dp], pl, v0, v1);
+                mma16816<BF16>(o[2 * dp + 1], pl, v2, v3);
+              }
             }
-          }
+          };
+          const int ka = kw + tq * 2, kb2 = ka + 8;
+          const uint32_t mlo = (ka < item.key_end ? 0x0000ffffu : 0u) | (ka + 1 < item.key_end ? 0xffff0000u : 0u);
+          const uint32_t mhi = (kb2 < item.key_end ? 0x0000ffffu : 0u) | (kb2 + 1 < item.key_end ? 0xffff0000u : 0u);
+          if (HS == 256 || k0 + kDecTile > item.key_end) pv(mlo, mhi);  // (one copy of the loop at 256)
+          else pv(0xffffffffu, 0xffffffffu);
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
+      if (++stage == L::kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
     }
 
     // ---- combine the four warps' partial states in a fixed order ----
