@@ -187,7 +187,7 @@ def test_max_query_len_hint_skips_prefill_and_is_checked():
                              d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], None,
                              num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, workspace=ws, max_query_len=4)
     assert pa.read_device_error(ws) == 0
-    assert pa.kernel_launch_count() - n0 == 3  # plan, cache write, decode
+    assert pa.kernel_launch_count() - n0 == 2  # the counters' reset, the self-planned decode kernel
     assert_close(bits_of(out).reshape(p.num_tokens, p.num_heads, p.head_size), ref["out"], p.dtype, "hint")
     # a bound below the real q_len is refused on the device, nothing written
     d = upload(p)
@@ -386,6 +386,61 @@ def test_refused_batch_runs_no_stale_plan():
     assert pa.read_device_error(ws) & pa.DEVERR_BAD_BATCH
     assert np.array_equal(bits_of(d["key_cache"]), before[0]) and np.array_equal(bits_of(d["value_cache"]), before[1])
     assert torch.all(out == 7.0)
+
+
+# ---- decode-only batches the decode kernel plans itself -------------------------------------
+# A whole call whose host bound proves every sequence decode-class, with derived slots and at
+# most 256 sequences, runs no planner and no cache-write kernel: each decode CTA cuts its share
+# of the partition from the batch description and writes the new K/V rows of the tiles it loads.
+SELF = {
+    "self-gqa4-pages16": dict(dtype="fp16", num_heads=32, kv_num_heads=8, head_size=128, block_size=16,
+                              past=list(range(0, 4000, 100)), q_lens=[1 + (i % 4) for i in range(40)]),
+    "self-mha-q16-hs64": dict(dtype="bf16", num_heads=8, kv_num_heads=8, head_size=64, block_size=32,
+                              past=[0, 31, 32, 500, 1023], q_lens=[16, 1, 16, 7, 2]),
+    "self-gqa8-empty-seqs": dict(dtype="bf16", num_heads=16, kv_num_heads=2, head_size=128, block_size=64,
+                                 past=[5, 0, 300, 0, 63, 1000], q_lens=[0, 1, 2, 0, 1, 2]),
+    "self-skewed-long": dict(dtype="fp16", num_heads=32, kv_num_heads=8, head_size=128, block_size=16,
+                             past=[60000, 3, 100000, 0, 17, 5000], q_lens=[1, 1, 2, 1, 1, 1]),
+    "self-256-seqs": dict(dtype="fp16", num_heads=16, kv_num_heads=2, head_size=128, block_size=256,
+                          past=[(37 * i) % 2000 for i in range(256)], q_lens=[1] * 256),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SELF))
+def test_self_planned_decode_only_batches(name):
+    p = w.make_problem(name=name, seed=21, **SELF[name])
+    ref = oracle.paged_attention(p)
+    d = upload(p)
+    ws = make_workspace(p)
+    lse = torch.empty((p.num_tokens, p.num_heads), dtype=torch.float32, device="cuda")
+    n0 = pa.kernel_launch_count()
+    out = pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
+                             d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], None,
+                             num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, workspace=ws,
+                             max_query_len=int(p.q_lens.max()), lse=lse)
+    assert pa.kernel_launch_count() - n0 == 2
+    assert pa.read_device_error(ws) == 0
+    assert np.array_equal(bits_of(d["key_cache"]), ref["key_cache"]), "key cache differs"
+    assert np.array_equal(bits_of(d["value_cache"]), ref["value_cache"]), "value cache differs"
+    assert_close(bits_of(out).reshape(p.num_tokens, p.num_heads, p.head_size), ref["out"], p.dtype, name)
+    lg = lse.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(lg - ref["lse"]) <= 5e-4 + 1e-5 * np.abs(ref["lse"])), "lse differs"
+
+
+def test_self_planned_calls_repeat_bitwise():
+    # the merge counters are reset by each call: a second call on the same workspace gives the
+    # same bits
+    p = w.make_problem(name="self-skewed-long", seed=22, **SELF["self-skewed-long"])
+    d = upload(p)
+    ws = make_workspace(p)
+    outs = []
+    for _ in range(3):
+        outs.append(bits_of(pa.paged_attention(
+            d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"], d["cumulative_sequence_length"],
+            d["past_seqlens"], d["block_table"], None, num_heads=p.num_heads, kv_num_heads=p.kv_num_heads,
+            workspace=ws, max_query_len=int(p.q_lens.max()))))
+    assert pa.read_device_error(ws) == 0
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
 
 
 # ---- batches larger than one planner round (1024 sequences) and than the tile sort ----

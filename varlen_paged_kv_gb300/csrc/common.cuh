@@ -28,6 +28,7 @@ __host__ __device__ constexpr int dec_ctas_per_sm(int hs) { return hs == 256 ? 1
 // at head_size 256 with one CTA per SM, 1.5-2 us against 1.4 us at 128 with two).
 __host__ __device__ constexpr int dec_item_cost_tiles(int hs) { return hs == 256 ? 3 : 1; }
 constexpr int kMaxDecCtas = 1024;     // upper bound of the decode grid
+constexpr int kSelfMaxB = 256;        // sequences of a decode-only batch the decode kernel plans itself
 // rates of the planner's model that splits the SMs between the prefill and the decode
 // kernel of a call with both kinds of rows (measured on GB300 at head_size 128)
 constexpr float kSplitPreFlops = 8.2e12f;   // prefill FLOP/s per SM, 128 x 128 tiles counted whole
@@ -173,6 +174,10 @@ struct Args {
   int32_t split_sms;
   int32_t decode_sms;
   int32_t dec_after_prefill;
+  // decode-only batch with derived slots and at most kSelfMaxB sequences: no plan and no
+  // cache-write kernel; each decode CTA cuts its own share of the balanced partition from
+  // the batch description and writes the new K/V rows of the tiles it loads
+  int32_t self_plan;
   int32_t out_v8;         // output 32-byte aligned (prefill stores 32-byte chunks)
   float scale_log2;       // scale * log2(e)
   WsHeader* hdr;
@@ -201,7 +206,7 @@ struct Args {
 // Integer caches (KQ = 1 INT8, 2 INT4) have rows of HS or HS / 2 bytes, so a stage is half or
 // a quarter of the 16-bit one and the ring is that much deeper (the same bytes in flight).
 // A row is TMA'd in boxes of kBoxBytes (at most 128) with the matching swizzle.
-template <int HS, int KQ = 0>
+template <int HS, int KQ = 0, bool SELF = false>
 struct DecSmem {
   static constexpr int kRowBytes = KQ == 0 ? HS * 2 : KQ == 1 ? HS : HS / 2;
   static constexpr int kBoxBytes = kRowBytes < 128 ? kRowBytes : 128;
@@ -217,11 +222,16 @@ struct DecSmem {
   static constexpr int kLw = kMw + kDecWarps * kDecRows * 4; // float [4][16]
   static constexpr int kBars = kLw + kDecWarps * kDecRows * 4;
   static constexpr int kAbort = kBars + 2 * kStages * 8;
-  static constexpr int kBytes = kAbort + 16 + 1024;          // + alignment slack
+  // self-planned batches: int64 T[kSelfMaxB + 1], int64 meta[8], int cum[kSelfMaxB + 1],
+  // int past[kSelfMaxB]
+  static constexpr int kSelf = (kAbort + 16 + 15) / 16 * 16;
+  static constexpr int kSelfBytes = !SELF ? 0 : ((kSelfMaxB + 1 + 8) * 8 + (2 * kSelfMaxB + 1) * 4 + 15) / 16 * 16;
+  static constexpr int kBytes = kSelf + kSelfBytes + 1024;   // + alignment slack
 };
 static_assert(DecSmem<256>::kBytes <= 232448 && 2 * (DecSmem<128>::kBytes + 1024) <= 233472 &&
                   DecSmem<256, 1>::kBytes <= 232448 && DecSmem<256, 2>::kBytes <= 232448 &&
-                  2 * (DecSmem<128, 1>::kBytes + 1024) <= 233472 && 2 * (DecSmem<128, 2>::kBytes + 1024) <= 233472,
+                  2 * (DecSmem<128, 1>::kBytes + 1024) <= 233472 && 2 * (DecSmem<128, 2>::kBytes + 1024) <= 233472 &&
+                  2 * (DecSmem<128, 0, true>::kBytes + 1024) <= 233472,
               "decode shared memory");
 
 // Prefill: Q tile, two K and two V tiles, barriers, the TMEM address slot.
@@ -309,6 +319,7 @@ __device__ __forceinline__ uint32_t p_col(int kk) { return (uint32_t)((kk >> 1) 
 // ---- host launchers, one per kernel family (defined next to their kernels) -----------------
 cudaError_t launch_plan(const Args& a, cudaStream_t s);
 cudaError_t launch_cache_write(const Args& a, int sms, cudaStream_t s);
+cudaError_t launch_decode_prep(const Args& a, cudaStream_t s);
 cudaError_t launch_v_mirror(const Args& a, int grid, cudaStream_t s);
 cudaError_t launch_prefill(const Args& a, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const CUtensorMap& tvm, int seg, int grid, cudaStream_t s);
@@ -487,6 +498,9 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -53,6 +53,216 @@ __device__ __forceinline__ DecodeItem load_item(const Args& a, int it, int it_en
   return d;
 }
 
+// ---- decode-only batches planned by the decode kernel itself ----
+// With derived slots, at most kSelfMaxB sequences and a host bound proving every sequence
+// decode-class, no plan and no cache-write kernel run: each CTA reads the batch description
+// into shared memory (cum[0..B], past[0..B), and T[0..B], the first virtual tile of each
+// sequence's units), cuts the same balanced partition as the planner (unit (b, g) spans
+// V + n_b tiles, V standing for an item's fixed cost, then its n_b key tiles; CTA c owns the
+// tiles [floor(c W / P), floor((c + 1) W / P))) and generates its items in order. The new
+// K/V rows of a tile are written by the CTA that loads the tile, just before the load.
+// meta: [0] R0, [1] R1 (this CTA's tiles), [2] W, [3] first candidate sequence, [4] its
+// first candidate head, [5] nonzero for a refused batch, [6] this CTA's items.
+struct SelfView {
+  int* cum;
+  int* past;
+  int64_t* T;
+  int64_t* meta;
+};
+
+__device__ __forceinline__ SelfView self_view(uint8_t* base) {
+  SelfView v;
+  v.T = reinterpret_cast<int64_t*>(base);                // kSelfMaxB + 1
+  v.meta = v.T + (kSelfMaxB + 1);                         // 6 (8 reserved)
+  v.cum = reinterpret_cast<int*>(v.meta + 8);             // kSelfMaxB + 1
+  v.past = v.cum + (kSelfMaxB + 1);                       // kSelfMaxB
+  return v;
+}
+
+// the CTA whose tile range holds virtual tile t: the largest c with floor(c W / P) <= t
+__device__ __forceinline__ int self_cta_of(int64_t t, int64_t W, int64_t P) {
+  return (int)min(P - 1, ((t + 1) * P - 1) / W);
+}
+
+// The items of a CTA of a self-planned batch in key order, each with the slot of its partial
+// result: 2c for the CTA's first item, 2c + 1 for its other split item (a unit cut across
+// CTAs c0 .. c1 leaves its pieces in the slots unit_first, then 2c for the CTAs after c0).
+// (The planner's items carry their list index as the slot.)
+template <int HS>
+struct SelfGen {
+  int b, g;  // the next candidate unit (the rest is read from the shared batch view)
+
+  __device__ explicit SelfGen(const SelfView& v) : b((int)v.meta[3]), g((int)v.meta[4]) {}
+
+  __device__ bool next(const Args& a, const SelfView& v, DecodeItem& d, int& slot) {
+    constexpr int V = dec_item_cost_tiles(HS);
+    const int64_t P = gridDim.x;
+    const int* cum = v.cum;
+    const int* past = v.past;
+    const int64_t* T = v.T;
+    const int64_t R0 = v.meta[0], R1 = v.meta[1], W = v.meta[2];
+    while (b < a.B) {
+      const int bb = b, gg = g;
+      const int q = cum[bb + 1] - cum[bb];
+      if (q < 1) {
+        ++b;
+        g = 0;
+        continue;
+      }
+      const int ps = past[bb], kv = ps + q;
+      const int64_t n = ceil_div((int64_t)kv, kDecTile);
+      const int64_t span0 = T[bb] + (int64_t)gg * (n + V), ks = span0 + V, ke = ks + n;
+      if (ks >= R1) {  // later units start later still
+        b = a.B;
+        return false;
+      }
+      if (++g == a.kvh) {
+        g = 0;
+        ++b;
+      }
+      if (ke <= R0) continue;
+      const int c0 = self_cta_of(ks, W, P), c1 = self_cta_of(ke - 1, W, P);
+      d.b = bb;
+      d.g = gg;
+      d.key_begin = (int)((max(ks, R0) - ks) * kDecTile);
+      d.key_end = (int)min((min(ke, R1) - ks) * kDecTile, (int64_t)kv);
+      d.unit_first = 2 * c0 + ((int64_t)c0 * W / P >= span0 ? 0 : 1);
+      d.n_split = c1 - c0 + 1;
+      d.c0 = cum[bb];
+      d.q_len = q;
+      d.past = ps;
+      d.pad[0] = d.pad[1] = d.pad[2] = 0;
+      slot = 2 * (int)blockIdx.x + (R0 >= span0 ? 0 : 1);
+      return true;
+    }
+    return false;
+  }
+};
+
+// Reads and checks the batch, lays out the units and finds this CTA's range (all threads;
+// only the batch description is read, which the previous kernels of the stream never write)
+template <int HS>
+__device__ void self_plan_prologue(const Args& a, const SelfView& v) {
+  const int tid = threadIdx.x, B = a.B;
+  constexpr int V = dec_item_cost_tiles(HS);
+  for (int b = tid; b <= B; b += blockDim.x) v.cum[b] = a.cum[b];
+  for (int b = tid; b < B; b += blockDim.x) v.past[b] = a.past[b];
+  __syncthreads();
+  if (tid < 32) {  // one warp: each lane sums the spans of kSelfMaxB / 32 sequences, then a scan
+    constexpr int PER = kSelfMaxB / 32;
+    int64_t span[PER], sum = 0;
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int b = tid * PER + i;
+      span[i] = 0;
+      if (b < B) {
+        const int64_t q = (int64_t)v.cum[b + 1] - v.cum[b], past = v.past[b], kv = past + q;
+        if (q < 0 || past < 0 || kv > (int64_t)a.max_blocks * a.bs || (a.max_query_len > 0 && q > a.max_query_len))
+          bad = true;
+        else if (q >= 1)
+          span[i] = (ceil_div(kv, kDecTile) + V) * a.kvh;
+      }
+      sum += span[i];
+    }
+    int64_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (tid >= o) incl += y;
+    }
+    int64_t run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int b = tid * PER + i;
+      if (b < B) v.T[b] = run;
+      run += span[i];
+    }
+    bad = __any_sync(0xffffffffu, bad) || v.cum[0] != 0 || v.cum[B] != a.N;
+    if (tid == 31) v.T[B] = incl;
+    if (tid == 0) v.meta[5] = bad;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const int64_t W = v.T[B], P = gridDim.x, c = blockIdx.x;
+    const int64_t R0 = W > 0 ? c * W / P : 0, R1 = W > 0 ? (c + 1) * W / P : 0;
+    int lo = 0, hi = B - 1;  // the last b with T[b] <= R0
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (v.T[mid] <= R0) lo = mid; else hi = mid - 1;
+    }
+    int g0 = 0;
+    const int64_t q = (int64_t)v.cum[lo + 1] - v.cum[lo];
+    if (q >= 1) {
+      const int64_t n = ceil_div((int64_t)v.past[lo] + q, kDecTile);
+      g0 = (int)min((R0 - v.T[lo]) / (n + V), (int64_t)a.kvh - 1);
+    }
+    v.meta[0] = R0;
+    v.meta[1] = R1;
+    v.meta[2] = W;
+    v.meta[3] = lo;
+    v.meta[4] = g0;
+    int count = 0;  // this CTA's items
+    if (!v.meta[5]) {
+      SelfGen<HS> gen(v);
+      DecodeItem d;
+      int slot;
+      while (gen.next(a, v, d, slot)) ++count;
+    }
+    v.meta[6] = count;
+  }
+  __syncthreads();
+}
+
+// the partial-result slot of piece s2 of an item's unit
+template <bool SELF>
+__device__ __forceinline__ int piece_slot(const DecodeItem& d, int s2) {
+  return !SELF ? d.unit_first + s2 : s2 == 0 ? d.unit_first : 2 * ((d.unit_first >> 1) + s2);
+}
+
+// This call's K and V rows among the keys [k0, k0 + 64) of an item of a self-planned batch,
+// copied from the inputs into the caches (head item.g) by the producer warp before it loads
+// the tile: each new key of head g is read only by the CTA whose range holds its tile. An
+// out-of-range block is skipped (the tile load reads it as zeros and flags it).
+template <int HS>
+__device__ __forceinline__ void write_new_rows(const Args& a, const DecodeItem& item, int k0, int lane) {
+  const int kv_len = item.past + item.q_len;
+  const int n0 = max(k0, max(item.key_begin, item.past));
+  const int n1 = min(k0 + kDecTile, min(item.key_end, kv_len));
+  if (n1 <= n0) return;
+  constexpr int CH = HS / 8;             // 16-byte chunks of one head's row
+  const int total = (n1 - n0) * 2 * CH;  // K and V chunks
+  const int* bt = a.block_table + (int64_t)item.b * a.max_blocks;
+  for (int i0 = 0; i0 < total; i0 += 4 * 32) {  // four chunks per lane in flight
+    uint4 v[4];
+    uint4* dst[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = i0 + lane + 32 * r;
+      dst[r] = nullptr;
+      if (i < total) {
+        const int rr = i / (2 * CH), rem = i % (2 * CH), which = rem / CH, ch = rem % CH;
+        const int key = n0 + rr;
+        const int blk = bt[key / a.bs];
+        if (blk >= 0 && blk < a.num_blocks) {
+          const int64_t tok = item.c0 + (key - item.past);
+          const uint16_t* src =
+              a.packed ? reinterpret_cast<const uint16_t*>(a.query) + tok * a.q_stride + (which ? a.v_offset : a.k_offset)
+                       : reinterpret_cast<const uint16_t*>(which ? a.value : a.key) + tok * a.kv_row;
+          v[r] = __ldg(reinterpret_cast<const uint4*>(src + item.g * HS) + ch);
+          dst[r] = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(which ? a.value_cache : a.key_cache) +
+                                            ((int64_t)blk * a.bs + key % a.bs) * a.kv_row + item.g * HS) + ch;
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+      if (dst[r]) *dst[r] = v[r];
+  }
+  fence_proxy_async_global();  // the rows, seen by the tile's TMA load
+  __syncwarp();
+}
+
 // Q fragments of an item (A operand, row-major 16 x HS, row r = j * G + hq), straight from
 // global memory; rows past the item's q_len * G are zeros
 template <int HS>
@@ -157,11 +367,11 @@ __device__ __forceinline__ void load_q_int(const Args& a, const DecodeItem& item
   }
 }
 
-template <int HS, bool BF16, int KQ>
+template <int HS, bool BF16, int KQ, bool SELF>
 __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
     decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const int seg_rows) {
-  using L = DecSmem<HS, KQ>;
+  using L = DecSmem<HS, KQ, SELF>;
   constexpr int NKS = HS / 16;  // k-steps of Q K^T
   constexpr int P = L::kBoxBytes;
   constexpr int ND = HS / 8;    // n-tiles of P V
@@ -193,13 +403,24 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
   // took from it) and waits for it only before exiting, so that the next call still finds
   // both finished.
   const bool beside_prefill = a.dec_after_prefill != 0;
+  // a self-planned batch: the partition is cut before the wait (the kernel before this one
+  // releases it only once all earlier work of the stream is done, and only the batch
+  // description is read); the wait is then for the reset of the merge counters
+  constexpr bool self = SELF;
+  const SelfView sv = self_view(smem + L::kSelf);
+  if constexpr (SELF) self_plan_prologue<HS>(a, sv);
   if (!beside_prefill) pdl_wait();
   pdl_launch_dependents();
-  if (!a.hdr->valid) {  // a refused batch: the item ranges are not this call's
+  if (self ? sv.meta[5] != 0 : !a.hdr->valid) {  // a refused batch: nothing is written
+    if (self && blockIdx.x == 0 && threadIdx.x == 0) {
+      atomicOr(err, PA_DEVERR_BAD_BATCH);
+      a.hdr->valid = 0;
+    }
     if (beside_prefill) pdl_wait();
     return;
   }
-  const int it_begin = a.cta_begin[blockIdx.x], it_end = a.cta_begin[blockIdx.x + 1];
+  const int it_begin = self ? 0 : a.cta_begin[blockIdx.x];
+  const int it_end = self ? (int)sv.meta[6] : a.cta_begin[blockIdx.x + 1];
 
   if (warp == kDecWarps) {
     // ================= producer warp: TMA page loads =================
@@ -210,10 +431,18 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
     const int nseg = kDecTile / seg_rows;
     const int oob = a.num_blocks * a.bs;  // a row coordinate past the end: TMA fills zeros
     uint32_t cnt = 0;
-    DecodeItem next = load_item(a, it_begin, it_end);
+    SelfGen<HS> gen(sv);  // (self-planned batches)
+    int next_slot = 0;
+    DecodeItem next;
+    if constexpr (SELF) gen.next(a, sv, next, next_slot);
+    else next = load_item(a, it_begin, it_end);
     for (int it = it_begin; it < it_end; ++it) {
       const DecodeItem item = next;  // loaded one item ahead
-      next = load_item(a, it + 1, it_end);
+      if constexpr (SELF) {
+        if (it + 1 < it_end) gen.next(a, sv, next, next_slot);
+      } else {
+        next = load_item(a, it + 1, it_end);
+      }
       {
         // this item's query rows into L2: the producer runs a ring's depth of tiles ahead
         // of the consumers, so their Q loads at the item's start find the rows there
@@ -230,12 +459,14 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
       for (int k0 = item.key_begin; k0 < item.key_end; k0 += kDecTile, ++cnt) {
         const int s = cnt % L::kStages;
         const uint32_t ph = (cnt / L::kStages) & 1;
+        if constexpr (SELF) write_new_rows<HS>(a, item, k0, lane);
         if (lane == 0) {
           mbar_wait(&empty[s], ph ^ 1, abort, err);
           mbar_arrive_expect_tx(&full[s], L::kStageBytes);
         }
         __syncwarp();
         if (lane < nseg) {
+          if constexpr (SELF) fence_proxy_async_global();  // (the rows written above, before the load)
           const int key = k0 + lane * seg_rows;
           int z = oob;
           if (key < kv_len) {
@@ -279,10 +510,19 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
       for (int D = 0; D < NVR; ++D)
         voff[e][D] = code_addr<P>(0, 16 * w + 2 * tq + e, KQ == 1 ? D * 8 * VG + VG * gq : VG * gq);
   }
-  DecodeItem next = load_item(a, it_begin, it_end);
-  for (int it = it_begin; it < it_end; ++it) {
+  SelfGen<HS> gen(sv);  // (self-planned batches)
+  int next_slot = 0;
+  DecodeItem next;
+  if constexpr (SELF) gen.next(a, sv, next, next_slot);
+  else next = load_item(a, it_begin, it_end);
+  for (int it_i = it_begin; it_i < it_end; ++it_i) {
     const DecodeItem item = next;  // loaded one item ahead
-    next = load_item(a, it + 1, it_end);
+    const int it = SELF ? next_slot : it_i;  // the slot of this item's partial result
+    if constexpr (SELF) {
+      if (it_i + 1 < it_end) gen.next(a, sv, next, next_slot);
+    } else {
+      next = load_item(a, it_i + 1, it_end);
+    }
     const int c0 = item.c0, q_len = item.q_len, past = item.past;
     const int n_rows = q_len * a.G;
     uint32_t qa[NKS][4];
@@ -619,13 +859,13 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
           // the unit's other items have all arrived: merge its partials in key order
           float Mx = -INFINITY;
           for (int s2 = 0; s2 < item.n_split; ++s2)
-            Mx = fmaxf(Mx, __ldcg(a.part_lse + (int64_t)(item.unit_first + s2) * kDecRows + row));
+            Mx = fmaxf(Mx, __ldcg(a.part_lse + (int64_t)piece_slot<SELF>(item, s2) * kDecRows + row));
           float acc[CW];
 #pragma unroll
           for (int v = 0; v < CW; ++v) acc[v] = 0.f;
           float den = 0.f;
           for (int s2 = 0; s2 < item.n_split; ++s2) {
-            const int64_t pr = (int64_t)(item.unit_first + s2) * kDecRows + row;
+            const int64_t pr = (int64_t)piece_slot<SELF>(item, s2) * kDecRows + row;
             const float lse = __ldcg(a.part_lse + pr);
             const float wgt = lse == -INFINITY ? 0.f : fast_exp2((lse - Mx) * 1.4426950408889634f);
             den += wgt;
@@ -666,15 +906,45 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
   if (beside_prefill) pdl_wait();
 }
 
+// Ahead of a self-planned decode-only call (one CTA): the header reset for this call (the
+// error word describes the most recent call) and the merge counters of the batch's
+// (sequence, KV head) units zeroed. Its dependents start once the previous call's kernels
+// are done, so the decode kernel can cut its partition from the batch description while
+// this kernel runs.
+__global__ void __launch_bounds__(256) decode_prep_kernel(const Args a) {
+  pdl_wait();  // the previous call's kernels may still use this workspace
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    WsHeader* hdr = a.hdr;
+    hdr->error = 0;
+    hdr->valid = 1;  // (the decode kernel clears it for a refused batch)
+    hdr->n_decode_items = 0;
+    hdr->n_prefill_tiles = 0;
+    hdr->dec_ctas = a.dec_ctas;
+    hdr->v_mirror = 0;
+    hdr->v_mirror_bad = 0;
+    hdr->mirror_rows = 0;
+    hdr->pre_ctas = 0;
+  }
+  for (int u = threadIdx.x; u < a.B * a.kvh; u += blockDim.x) a.unit_done[u] = 0;
+}
+
 // ---- host launchers (kernels are launched from the translation unit that defines them) ----
-template <int HS, bool BF16, int KQ>
+cudaError_t launch_decode_prep(const Args& a, cudaStream_t s) {
+  return launch_pdl(decode_prep_kernel, dim3(1), dim3(256), 0, s, a);
+}
+
+template <int HS, bool BF16, int KQ, bool SELF = false>
 static cudaError_t launch_decode_t(const Args& a, const CUtensorMap& tk, const CUtensorMap& tv, int seg,
                                    cudaStream_t s) {
-  constexpr int smem = DecSmem<HS, KQ>::kBytes;
+  if constexpr (KQ == 0 && HS != 256 && !SELF) {  // self-planned decode-only batches: their own instantiation
+    if (a.self_plan) return launch_decode_t<HS, BF16, KQ, true>(a, tk, tv, seg, s);
+  }
+  constexpr int smem = DecSmem<HS, KQ, SELF>::kBytes;
   cudaError_t e =
-      cudaFuncSetAttribute(decode_kernel<HS, BF16, KQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      cudaFuncSetAttribute(decode_kernel<HS, BF16, KQ, SELF>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_kernel<HS, BF16, KQ>, dim3(a.dec_ctas), dim3(160), smem, s, a, tk, tv, seg);
+  return launch_pdl(decode_kernel<HS, BF16, KQ, SELF>, dim3(a.dec_ctas), dim3(160), smem, s, a, tk, tv, seg);
 }
 
 template <int KQ>

@@ -106,10 +106,18 @@ __device__ void block_scan_i64(int64_t v, int64_t* ex, int64_t* tot, long long* 
   __syncthreads();
 }
 
-// In-place suffix minimum of v[0 .. n) (n <= blockDim.x) across the block.
+// In-place suffix minimum of v[0 .. n) (n <= 4 blockDim.x) across the block: thread t takes
+// the run v[k t .. k t + k), k = ceil(n / blockDim.x), and the runs' minima are scanned.
 __device__ void block_suffix_min(int* v, int n, int* s_w) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
-  int x = tid < n ? v[tid] : INT_MAX;
+  const int k = (n + (int)blockDim.x - 1) / (int)blockDim.x;  // 1 .. 4
+  int run[4];
+  int x = INT_MAX;  // minimum of this thread's run
+#pragma unroll
+  for (int j = 3; j >= 0; --j) {
+    run[j] = j < k && k * tid + j < n ? v[k * tid + j] : INT_MAX;
+    x = min(x, run[j]);
+  }
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int y = __shfl_down_sync(0xffffffffu, x, o);
@@ -128,7 +136,16 @@ __device__ void block_suffix_min(int* v, int n, int* s_w) {
   }
   __syncthreads();
   if (wid + 1 < nw) x = min(x, s_w[wid + 1]);
-  if (tid < n) v[tid] = x;
+  // x: the minimum of the runs from this thread's on; the run's own suffix minima, each
+  // joined with the minimum of the later runs
+  int after = __shfl_down_sync(0xffffffffu, x, 1);
+  if (lane == 31) after = wid + 1 < nw ? s_w[wid + 1] : INT_MAX;
+  __syncthreads();  // every thread has read v and s_w
+#pragma unroll
+  for (int j = 3; j >= 0; --j) {
+    after = min(after, run[j]);
+    if (j < k && k * tid + j < n) v[k * tid + j] = after;
+  }
   __syncthreads();
 }
 
@@ -157,6 +174,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
 
   const int tid = threadIdx.x;
   WsHeader* hdr = a.hdr;
+  // the batch description into L2 while the previous kernel drains (a hint: the loads below
+  // come after the wait)
+  for (int i = tid * 32; i <= a.B; i += blockDim.x * 32) {
+    prefetch_l2(a.cum + i);
+    if (i < a.B) prefetch_l2(a.past + i);
+  }
   pdl_wait();  // the previous call's kernels may still read this workspace
   pdl_launch_dependents();
   if (tid == 0) {
@@ -215,13 +238,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
   // up to kSplitHbmBytes for the chip.
   const int S = a.sms;
   const bool split = a.split_sms && s_dec_tiles > 0 && s_pre_tiles > 0 && S > 1;
-  if (split && a.decode_sms <= 0 && tid < S - 1) {
-    const int d = tid + 1;
+  if (split && a.decode_sms <= 0) {
     const float flops = (float)s_pre_tiles * (float)a.nh * (float)(kPreTileQ * kPreTileK) * (float)a.hs * 4.f;
     const float bytes = (float)s_dec_tiles * (float)a.kvh * (float)(kDecTile * a.hs * 2 * 2);
-    const float tp = flops / ((float)(S - d) * kSplitPreFlops);
-    const float td = bytes / fminf(kSplitHbmBytes, (float)d * kSplitDecBytes);
-    atomicMin(&s_split, ((unsigned long long)__float_as_uint(fmaxf(tp, td)) << 32) | (unsigned)d);
+    for (int d = tid + 1; d < S; d += blockDim.x) {
+      const float tp = flops / ((float)(S - d) * kSplitPreFlops);
+      const float td = bytes / fminf(kSplitHbmBytes, (float)d * kSplitDecBytes);
+      atomicMin(&s_split, ((unsigned long long)__float_as_uint(fmaxf(tp, td)) << 32) | (unsigned)d);
+    }
   }
   __syncthreads();
   int dec_sms = S;
@@ -242,7 +266,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
   int* s_past = s_c0 + kPlanThreads;  // [kPlanThreads] history
   static_assert((kMaxDecCtas + 1) * 8 + 5 * kPlanThreads * 4 <= kSortCap * 8, "tables fit s_key");
   const int64_t W = (int64_t)s_dec_tiles * a.kvh;
-  for (int64_t c = tid; c <= P; c += blockDim.x) s_start[c] = c * W / P;  // one division per thread
+  {
+    // floor(c W / P) = c (W / P) + floor(c (W % P) / P): one 64-bit division per thread, then
+    // 32-bit arithmetic per entry (c (W % P) < P^2 <= 2^20)
+    const int64_t wq = W / P;
+    const uint32_t wr = (uint32_t)(W - wq * P);
+    for (int64_t c = tid; c <= P; c += blockDim.x) s_start[c] = c * wq + (uint32_t)c * wr / (uint32_t)P;
+  }
   const float pw = W > 0 ? (float)P / (float)W : 0.f;
   // the CTA whose range holds tile t (the largest c with s_start[c] <= t): a float
   // estimate corrected against the table
@@ -689,16 +719,29 @@ __device__ void quant_unit(const Args& a, int tok, int64_t pos, int64_t slot, in
 // -1 for a suppressed write or an out-of-range block or slot (those also flagged); pos is
 // the token's logical position when the caller needs it (no slot_mapping, or prep). b is
 // the sequence of the warp's previous token, tokens only grow within a warp.
+// The last b in [b0, B) with cum[b] <= tok (given cum[b0] <= tok), found by the warp: each
+// step has the 32 lanes test 32 evenly spaced entries of the range and keeps the bracket
+// of the last one that holds, so up to 32^k sequences take k dependent loads instead of a
+// binary search's log2 of them. Empty sequences (cum[b] = cum[b + 1]) are passed over.
+__device__ __forceinline__ int warp_find_seq(const int* cum, int b0, int B, int tok, int lane) {
+  int lo = b0, n = B - b0;
+  while (n > 32) {
+    const int stride = (n + 31) >> 5;
+    const int idx = lo + lane * stride;
+    const unsigned m = __ballot_sync(0xffffffffu, idx < lo + n && cum[idx] <= tok);
+    const int k = 31 - __clz(m);  // lane 0 holds: cum[lo] <= tok
+    lo += k * stride;
+    n = min(stride, n - k * stride);
+  }
+  const unsigned m = __ballot_sync(0xffffffffu, lane < n && cum[lo + lane] <= tok);
+  return lo + 31 - __clz(m);
+}
+
 __device__ __forceinline__ int64_t resolve_slot(const Args& a, int tok, bool need_pos, int& b, int64_t& pos,
                                                 int lane) {
   pos = 0;
   if (!a.slot_mapping || need_pos) {
-    int lo = b, hi = a.B - 1;  // last b with cum[b] <= tok
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (a.cum[mid] <= tok) lo = mid; else hi = mid - 1;
-    }
-    b = lo;
+    b = warp_find_seq(a.cum, b, a.B, tok, lane);
     pos = (int64_t)a.past[b] + (tok - a.cum[b]);
   }
   int64_t slot;
@@ -728,12 +771,29 @@ __device__ __forceinline__ int64_t resolve_slot(const Args& a, int tok, bool nee
 // other).
 template <int MODE>
 __global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
-  pdl_wait();
-  pdl_launch_dependents();
-  if (!a.hdr->valid) return;
   const int lane = threadIdx.x & 31;
   const int warps = (int)((gridDim.x * blockDim.x) >> 5);
   const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  if constexpr (MODE == 0) {
+    // this warp's first token's K and V rows and the batch description into L2 while the
+    // earlier kernels finish (hints only: every load below comes after the wait)
+    if (gw < a.N) {
+      const int lines = a.kv_row * 2 / 128;  // 128-byte lines of one K (or V) row
+      const char* src = a.packed ? reinterpret_cast<const char*>(a.query) + ((int64_t)gw * a.q_stride + a.k_offset) * 2
+                                 : reinterpret_cast<const char*>(a.key) + (int64_t)gw * a.kv_row * 2;
+      const int64_t vdelta = a.packed ? (int64_t)(a.v_offset - a.k_offset) * 2
+                                      : reinterpret_cast<const char*>(a.value) - reinterpret_cast<const char*>(a.key);
+      for (int i = lane; i < 2 * lines; i += 32) prefetch_l2(src + (i >= lines ? vdelta : 0) + (i % lines) * 128);
+    }
+    if (threadIdx.x < 32)
+      for (int i = lane * 32; i <= a.B; i += 32 * 32) {
+        prefetch_l2(a.cum + i);
+        if (i < a.B) prefetch_l2(a.past + i);
+      }
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  if (!a.hdr->valid) return;
   int b = 0;
   if constexpr (MODE != 0) {
     const int U = a.nh + a.kvh;
