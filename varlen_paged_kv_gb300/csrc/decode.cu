@@ -62,7 +62,7 @@ __device__ __forceinline__ DecodeItem load_item(const Args& a, int it, int it_en
 // tiles [floor(c W / P), floor((c + 1) W / P))) and generates its items in order. The new
 // K/V rows of a tile are written by the CTA that loads the tile, just before the load.
 // meta: [0] R0, [1] R1 (this CTA's tiles), [2] W, [3] first candidate sequence, [4] its
-// first candidate head, [5] nonzero for a refused batch, [6] this CTA's items.
+// first candidate head, [5] nonzero for a refused batch, [6] this CTA's items, [7] W / P.
 struct SelfView {
   int* cum;
   int* past;
@@ -79,9 +79,20 @@ __device__ __forceinline__ SelfView self_view(uint8_t* base) {
   return v;
 }
 
-// the CTA whose tile range holds virtual tile t: the largest c with floor(c W / P) <= t
+// the CTA whose tile range holds virtual tile t: the largest c with floor(c W / P) <= t, i.e.
+// floor(((t + 1) P - 1) / W), below P <= 1024: a float estimate set right by integer steps
 __device__ __forceinline__ int self_cta_of(int64_t t, int64_t W, int64_t P) {
-  return (int)min(P - 1, ((t + 1) * P - 1) / W);
+  const int64_t n = (t + 1) * P - 1;
+  int64_t q = (int64_t)((float)n / (float)W);
+  while (q > 0 && q * W > n) --q;
+  while ((q + 1) * W <= n) ++q;
+  return (int)min(P - 1, q);
+}
+
+// floor(c W / P) = c floor(W / P) + floor(c (W mod P) / P), with wq = floor(W / P) given
+// (c (W mod P) < P^2 <= 2^20 stays in 32 bits)
+__device__ __forceinline__ int64_t self_start(int64_t c, int64_t W, int64_t P, int64_t wq) {
+  return c * wq + (int64_t)((uint32_t)c * (uint32_t)(W - wq * P) / (uint32_t)P);
 }
 
 // The items of a CTA of a self-planned batch in key order, each with the slot of its partial
@@ -100,7 +111,7 @@ struct SelfGen {
     const int* cum = v.cum;
     const int* past = v.past;
     const int64_t* T = v.T;
-    const int64_t R0 = v.meta[0], R1 = v.meta[1], W = v.meta[2];
+    const int64_t R0 = v.meta[0], R1 = v.meta[1], W = v.meta[2], wq = v.meta[7];
     while (b < a.B) {
       const int bb = b, gg = g;
       const int q = cum[bb + 1] - cum[bb];
@@ -126,7 +137,7 @@ struct SelfGen {
       d.g = gg;
       d.key_begin = (int)((max(ks, R0) - ks) * kDecTile);
       d.key_end = (int)min((min(ke, R1) - ks) * kDecTile, (int64_t)kv);
-      d.unit_first = 2 * c0 + ((int64_t)c0 * W / P >= span0 ? 0 : 1);
+      d.unit_first = 2 * c0 + (self_start(c0, W, P, wq) >= span0 ? 0 : 1);
       d.n_split = c1 - c0 + 1;
       d.c0 = cum[bb];
       d.q_len = q;
@@ -185,7 +196,8 @@ __device__ void self_plan_prologue(const Args& a, const SelfView& v) {
   __syncthreads();
   if (tid == 0) {
     const int64_t W = v.T[B], P = gridDim.x, c = blockIdx.x;
-    const int64_t R0 = W > 0 ? c * W / P : 0, R1 = W > 0 ? (c + 1) * W / P : 0;
+    const int64_t wq = W / P;
+    const int64_t R0 = W > 0 ? self_start(c, W, P, wq) : 0, R1 = W > 0 ? self_start(c + 1, W, P, wq) : 0;
     int lo = 0, hi = B - 1;  // the last b with T[b] <= R0
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -202,6 +214,7 @@ __device__ void self_plan_prologue(const Args& a, const SelfView& v) {
     v.meta[2] = W;
     v.meta[3] = lo;
     v.meta[4] = g0;
+    v.meta[7] = wq;
     int count = 0;  // this CTA's items
     if (!v.meta[5]) {
       SelfGen<HS> gen(v);
