@@ -68,6 +68,8 @@ CASES = {
     "gqa8-q2": ("bf16", 32, 4, 128, 16, [60], [2], False, 0),
     "rows-over-16-go-prefill": ("fp16", 32, 8, 128, 32, [40], [5], True, 0),
     "bf16-long-history-chunk": ("bf16", 8, 2, 128, 128, [2500], [257], False, 0),
+    # explicit slots with drops: the fp16 V copy is made by its own kernel after the cache write
+    "bf16-prefill-explicit-slots": ("bf16", 16, 4, 128, 64, [300, 0, 70], [200, 129, 1], False, 7),
 }
 
 

@@ -202,7 +202,8 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
   if ((stages & PA_STAGE_CACHE_WRITE) && args.N > 0) {
     ++g_launches;
     if (cudaError_t e = pa::launch_cache_write(args, info.sms, stream)) return cuda_fail(e, "cache_write_kernel launch");
-    if (can_prefill && args.mirror_keys > 0 && slots > 0) {
+    if (can_prefill && args.mirror_keys > 0 && slots > 0 && (args.slot_mapping != nullptr || args.prep || args.kvq)) {
+      // (with derived slots the bit-copy cache write makes the copy itself)
       // bf16: the fp16 copy of the prefill sequences' V, read from the cache just written
       // (the planner decides whether it is made and used)
       const int64_t warps = (int64_t)args.mirror_keys;

@@ -314,6 +314,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
         mrow0 = (int)mb;
         a.mirror_base[b] = (int)mb;
         a.mirror_seq[s_mseq_carry + ex[2]] = make_int2(b, (int)mb);
+      } else if (b < a.B) {
+        a.mirror_base[b] = -1;  // no copy of this sequence's V
       }
     }
     s_T[tid] = carry0 + ex[0];
@@ -417,7 +419,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
   for (int c = tid; c <= a.dec_ctas; c += blockDim.x) a.cta_begin[c] = c <= P ? s_cta_begin[c] : n_items;
 
   // ---- prefill tiles: sort by KV-tile count, descending (ties: list order) ----
-  if (n_tiles <= kSortCap) {
+  if (n_tiles <= 256) {
+    // few tiles: each takes the place of its rank among the (distinct) keys, two barriers
+    unsigned long long key = ~0ull;
+    if (tid < n_tiles)
+      key = ((unsigned long long)(0xFFFFFFFFull - (unsigned long long)a.tiles_unsorted[tid].n_kv) << 32) |
+            (unsigned)tid;
+    if (tid < n_tiles) s_key[tid] = key;
+    __syncthreads();
+    if (tid < n_tiles) {
+      int rank = 0;
+      for (int j = 0; j < n_tiles; ++j) rank += s_key[j] < key;
+      a.tiles[rank] = a.tiles_unsorted[tid];
+    }
+  } else if (n_tiles <= kSortCap) {
     int n2 = 1;
     while (n2 < n_tiles) n2 <<= 1;
     for (int i = tid; i < n2; i += blockDim.x) {
@@ -460,6 +475,62 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
     hdr->n_prefill_tiles = n_tiles;
     hdr->dec_ctas = (int)P;
     hdr->pre_ctas = split ? S - dec_sms : 0;
+  }
+}
+
+// ---- fp16 copy of V for bf16 prefill ----------------------------------------------------
+// Row r of the copy is key r - mirror_base[b] of prefill-class sequence b, read from the
+// value cache after this call's cache write (so through block_table, as the attention
+// reads it). One warp per row, 16-byte loads and stores. A value fp16 cannot represent
+// (|v| >= 65520, inf, NaN) sets v_mirror_bad, and the prefill kernel then reads the bf16
+// cache instead; a block outside the pool is flagged and its rows are zeros (as the
+// attention reads them from the cache).
+
+// bf16 -> fp16 of the 16-byte chunk w (8 values), folding |fp16| bits into big
+__device__ __forceinline__ uint4 chunk_to_f16(uint4 w, uint32_t& big) {
+  w.x = bf16x2_to_f16x2(w.x);
+  w.y = bf16x2_to_f16x2(w.y);
+  w.z = bf16x2_to_f16x2(w.z);
+  w.w = bf16x2_to_f16x2(w.w);
+  big = max_u16x2(big, max_u16x2(max_u16x2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
+                                 max_u16x2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu)));
+  return w;
+}
+
+// copy row r of the fp16 V copy from the value cache (a warp); with history_only, rows of
+// this call's keys (position >= past) are left to the cache write, which copies them from
+// the inputs
+__device__ __forceinline__ void mirror_row(const Args& a, int r, int n_seqs, bool history_only, int lane,
+                                           uint32_t& big) {
+  const int chunks = a.kv_row / 8;  // 16-byte chunks of a row
+  int lo = 0, hi = n_seqs - 1;      // the last copied sequence whose first row is <= r
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.mirror_seq[mid].y <= r) lo = mid; else hi = mid - 1;
+  }
+  const int b = a.mirror_seq[lo].x;
+  const int key = r - a.mirror_seq[lo].y;
+  if (history_only && key >= a.past[b]) return;
+  const int blk = a.block_table[(int64_t)b * a.max_blocks + key / a.bs];
+  const uint4* src = nullptr;
+  if (blk >= 0 && blk < a.num_blocks)
+    src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.value_cache) +
+                                         ((int64_t)blk * a.bs + key % a.bs) * a.kv_row);
+  else if (lane == 0)
+    atomicOr(&a.hdr->error, PA_DEVERR_BAD_BLOCK);
+  uint4* dst = reinterpret_cast<uint4*>(a.mirror + (int64_t)r * a.kv_row);
+  for (int c0 = lane; c0 < chunks; c0 += 128) {  // four loads in flight before the stores
+    uint4 w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = c0 + 32 * j;
+      w[j] = (src && c < chunks) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 f = chunk_to_f16(w[j], big);
+      if (c0 + 32 * j < chunks) dst[c0 + 32 * j] = f;
+    }
   }
 }
 
@@ -820,10 +891,25 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
     return;
   }
   const int chunks = a.kv_row / 8;  // 16-byte chunks in one K (or V) row
+  // bf16 with derived slots: the fp16 copy of the prefill-class sequences' V is written here,
+  // each new row from the input it comes from (this call writes every derived position, and
+  // no other position), the older rows from the cache below; no copy kernel runs
+  const bool mirror = MODE == 0 && a.mirror_keys > 0 && !a.slot_mapping && a.hdr->v_mirror;
+  uint32_t big = 0;  // per-half max of |fp16| bits of this lane's copied values
   for (int tok = gw; tok < a.N; tok += warps) {
     int64_t pos;
     const int64_t slot = resolve_slot(a, tok, false, b, pos, lane);
-    if (slot == -1) continue;
+    int mrow = -1;  // the token's row of the fp16 V copy
+    if (mirror) {
+      const int base = a.mirror_base[b];
+      if (base >= 0) mrow = base + (int)pos;
+    }
+    if (slot == -1) {  // (derived slots: a block outside the pool, which reads as zeros)
+      if (mrow >= 0)
+        for (int c = lane; c < chunks; c += 32)
+          reinterpret_cast<uint4*>(a.mirror + (int64_t)mrow * a.kv_row)[c] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
     const uint16_t *src_k, *src_v;
     if (a.packed) {
       src_k = reinterpret_cast<const uint16_t*>(a.query) + (int64_t)tok * a.q_stride + a.k_offset;
@@ -850,19 +936,18 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
         if (c < chunks) {
           dst_k[c] = k[j];
           dst_v[c] = v[j];
+          if (mrow >= 0) reinterpret_cast<uint4*>(a.mirror + (int64_t)mrow * a.kv_row)[c] = chunk_to_f16(v[j], big);
         }
       }
     }
   }
+  if (mirror) {  // the copy's rows of keys before this call
+    const int rows = a.hdr->mirror_rows, n = a.hdr->mirror_seqs;
+    for (int r = gw; r < rows; r += warps) mirror_row(a, r, n, true, lane, big);
+  }
+  if ((big & 0xFFFFu) >= 0x7C00u || (big >> 16) >= 0x7C00u) atomicOr(&a.hdr->v_mirror_bad, 1u);
 }
 
-// ---- fp16 copy of V for bf16 prefill ----------------------------------------------------
-// Row r of the copy is key r - mirror_base[b] of prefill-class sequence b, read from the
-// value cache after this call's cache write (so through block_table, as the attention
-// reads it). One warp per row, 16-byte loads and stores. A value fp16 cannot represent
-// (|v| >= 65520, inf, NaN) sets v_mirror_bad, and the prefill kernel then reads the bf16
-// cache instead; a block outside the pool is flagged and its rows are zeros (as the
-// attention reads them from the cache).
 __global__ void __launch_bounds__(256) v_mirror_kernel(const Args a) {
   pdl_wait();
   pdl_launch_dependents();
@@ -870,44 +955,10 @@ __global__ void __launch_bounds__(256) v_mirror_kernel(const Args a) {
   if (!hdr->valid || !hdr->v_mirror) return;
   const int rows = hdr->mirror_rows;
   const int lane = threadIdx.x & 31;
-  const int chunks = a.kv_row / 8;  // 16-byte chunks of a row
-  uint32_t big = 0;                 // per-half max of |fp16| bits over this lane's values
+  uint32_t big = 0;  // per-half max of |fp16| bits over this lane's values
   const int n = hdr->mirror_seqs;
-  for (int r = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); r < rows; r += (int)((gridDim.x * blockDim.x) >> 5)) {
-    int lo = 0, hi = n - 1;  // the last copied sequence whose first row is <= r
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (a.mirror_seq[mid].y <= r) lo = mid; else hi = mid - 1;
-    }
-    const int b = a.mirror_seq[lo].x;
-    const int key = r - a.mirror_seq[lo].y;
-    const int blk = a.block_table[(int64_t)b * a.max_blocks + key / a.bs];
-    const uint4* src = nullptr;
-    if (blk >= 0 && blk < a.num_blocks)
-      src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.value_cache) +
-                                           ((int64_t)blk * a.bs + key % a.bs) * a.kv_row);
-    else if (lane == 0)
-      atomicOr(&a.hdr->error, PA_DEVERR_BAD_BLOCK);
-    uint4* dst = reinterpret_cast<uint4*>(a.mirror + (int64_t)r * a.kv_row);
-    for (int c0 = lane; c0 < chunks; c0 += 128) {  // four loads in flight before the stores
-      uint4 w[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int c = c0 + 32 * j;
-        w[j] = (src && c < chunks) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        w[j].x = bf16x2_to_f16x2(w[j].x);
-        w[j].y = bf16x2_to_f16x2(w[j].y);
-        w[j].z = bf16x2_to_f16x2(w[j].z);
-        w[j].w = bf16x2_to_f16x2(w[j].w);
-        big = max_u16x2(big, max_u16x2(max_u16x2(w[j].x & 0x7FFF7FFFu, w[j].y & 0x7FFF7FFFu),
-                                       max_u16x2(w[j].z & 0x7FFF7FFFu, w[j].w & 0x7FFF7FFFu)));
-        if (c0 + 32 * j < chunks) dst[c0 + 32 * j] = w[j];
-      }
-    }
-  }
+  for (int r = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); r < rows; r += (int)((gridDim.x * blockDim.x) >> 5))
+    mirror_row(a, r, n, false, lane, big);
   if ((big & 0xFFFFu) >= 0x7C00u || (big >> 16) >= 0x7C00u) atomicOr(&a.hdr->v_mirror_bad, 1u);
 }
 
