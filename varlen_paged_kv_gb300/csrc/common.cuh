@@ -549,10 +549,13 @@ constexpr uint32_t kF16Int8Bias = 0x64806480u; // 1152.0 (1024 + 128) in both ha
 constexpr uint32_t kF16Int4Bias = 0x64086408u; // 1032.0 (1024 + 8)
 
 // four INT8 codes (bytes 0..3 of w) as fp16 pairs (byte 0, byte 1) and (byte 2, byte 3)
-__device__ __forceinline__ void s8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+// four INT8 codes (bytes 0..3 of w) as the exact fp16 integers code + 1152, pairs (byte 0,
+// byte 1) and (byte 2, byte 3): the bias is left in (a constant per query row once summed
+// against the query, which the softmax does not see)
+__device__ __forceinline__ void s8x4_to_f16_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t x = w ^ 0x80808080u;
-  lo = hsub2_u32(prmt(x, kF16Magic, 0x5140u), kF16Int8Bias);
-  hi = hsub2_u32(prmt(x, kF16Magic, 0x7362u), kF16Int8Bias);
+  lo = prmt(x, kF16Magic, 0x5140u);
+  hi = prmt(x, kF16Magic, 0x7362u);
 }
 // byte i of w0 and byte i of w1 (two keys, one channel) as one fp16 pair, i = 0..3
 __device__ __forceinline__ void s8_key_pairs(uint32_t w0, uint32_t w1, uint32_t (&p)[4]) {

@@ -227,6 +227,36 @@ __device__ void self_plan_prologue(const Args& a, const SelfView& v) {
   __syncthreads();
 }
 
+// (INT8 caches) The bias of a query row's scores, in natural-log units. INT8 keys enter
+// Q K^T as the fp16 integers code + 1152, which adds 1152 sum_c Q'_c to every score of the
+// row: the softmax, the four warps' combine and the split merge only compare scores and lse
+// of one row and do not see it; the exported lse has it taken off. Eight threads per row
+// (t & 7), each summing HS / 8 values of the scaled query row; all 32 lanes take part.
+template <int HS>
+__device__ __forceinline__ float int8_row_bias(const Args& a, int tok, int head, int t, bool valid) {
+  float s = 0.f;
+  int e = 0;
+  if (valid) {
+    const int64_t row = (int64_t)tok * a.nh + head;
+    const uint4* q = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.query) + row * HS +
+                                                    (t & 7) * (HS / 8));
+#pragma unroll
+    for (int i = 0; i < HS / 64; ++i) {
+      const uint4 w = __ldg(q + i);
+      const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        s += __half2float(__ushort_as_half((unsigned short)(x[j] & 0xFFFFu))) +
+             __half2float(__ushort_as_half((unsigned short)(x[j] >> 16)));
+    }
+    e = __ldg(a.qexp + row);
+  }
+  s += __shfl_xor_sync(0xffffffffu, s, 1);
+  s += __shfl_xor_sync(0xffffffffu, s, 2);
+  s += __shfl_xor_sync(0xffffffffu, s, 4);
+  return 1152.f * s * ldexpf(a.scale_log2, e) * 0.69314718055994531f;
+}
+
 // the partial-result slot of piece s2 of an item's unit
 template <bool SELF>
 __device__ __forceinline__ int piece_slot(const DecodeItem& d, int s2) {
@@ -583,8 +613,8 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               uint32_t b0, b1, b2, b3;
-              s8x4_to_f16(u[i], b0, b1);
-              s8x4_to_f16(v[i], b2, b3);
+              s8x4_to_f16_biased(u[i], b0, b1);
+              s8x4_to_f16_biased(v[i], b2, b3);
               mma16816<false>(sc[0], qa[4 * j + i], b0, b1);
               mma16816<false>(sc[1], qa[4 * j + i], b2, b3);
             }
@@ -826,9 +856,14 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
         for (int bb = 1; bb < L::kCombBufs; ++bb) x += src[bb * (kDecRows * kCombStride) + v];
         return x;
       };
+      float lbias = 0.f;  // (INT8) the row's key bias, taken off the exported lse
+      if constexpr (KQ == 1) {
+        if (a.lse) lbias = int8_row_bias<HS>(a, tok, head, t, mine);
+      }
       if (item.n_split == 1) {
         if (mine && a.lse && (t & 7) == 0)  // natural log; M is the base-2 max of s * scale
-          a.lse[(int64_t)tok * a.nh + head] = Lr > 0.f ? (M + fast_log2(Lr)) * 0.69314718055994531f : -INFINITY;
+          a.lse[(int64_t)tok * a.nh + head] =
+              Lr > 0.f ? (M + fast_log2(Lr)) * 0.69314718055994531f - lbias : -INFINITY;
         if (mine) {
 #pragma unroll
           for (int v = 0; v < CW; v += 8) {
@@ -893,7 +928,7 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
             }
           }
           const float dinv = 1.f / den;
-          if (a.lse && (t & 7) == 0) a.lse[(int64_t)tok * a.nh + head] = Mx + fast_log2(den) * 0.69314718055994531f;
+          if (a.lse && (t & 7) == 0) a.lse[(int64_t)tok * a.nh + head] = Mx + fast_log2(den) * 0.69314718055994531f - lbias;
 #pragma unroll
           for (int v = 0; v < CW; v += 8) {
             float x[8];
