@@ -737,14 +737,14 @@ __device__ __forceinline__ void quant_row(const Args& a, const uint16_t* src, co
 // scales of its KV head (after the preparation, if any) and written as fp16 with a
 // power-of-two row exponent; else KV head g = u - nh, unless the write is suppressed, its
 // K and V rows as codes.
-template <int HS, int KQ>
+template <int HS, int KQ, bool PREP>
 __device__ void quant_unit(const Args& a, int tok, int64_t pos, int64_t slot, int u, int lane) {
   constexpr int E = HS / 32;
   const bool bf16 = a.bf16 != 0;
-  const bool prep = a.prep != 0;
+  constexpr bool prep = PREP;
   if (u >= a.nh && slot < 0) return;
   PrepLane<HS> t;
-  if (prep) prep_lane<HS>(a, pos, lane, t);
+  if constexpr (PREP) prep_lane<HS>(a, pos, lane, t);
   const uint16_t* qrow = reinterpret_cast<const uint16_t*>(a.query) + (int64_t)tok * a.q_stride;
   if (u < a.nh) {
     const int h = u;
@@ -834,12 +834,11 @@ __device__ __forceinline__ int64_t resolve_slot(const Args& a, int tok, bool nee
   return slot;
 }
 
-// One instantiation per kind of write, so that the plain bit copy keeps the few registers
-// it needs and stays many warps deep: 0 = bit copy, one warp per token; 1 = Q/K
-// preparation and 2 = integer caches, one warp per (token, unit), the units being the
-// token's nh query heads and then its kvh KV heads (each a short dependent chain of a load,
-// warp reductions and a store, so the units of a token run in parallel, not one after the
-// other).
+// One instantiation per kind of write, so that each keeps only the registers it needs and
+// stays many warps deep: 0 = bit copy, one warp per token; 1 = Q/K preparation, 2 = integer
+// caches, 3 = both, one warp per (token, unit), the units being the token's nh query heads
+// and then its kvh KV heads (each a short dependent chain of a load, warp reductions and a
+// store, so the units of a token run in parallel, not one after the other).
 template <int MODE>
 __global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
   const int lane = threadIdx.x & 31;
@@ -873,14 +872,15 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
       const int tok = (int)(wi / U), u = (int)(wi - (int64_t)tok * U);
       int64_t pos;
       const int64_t slot = resolve_slot(a, tok, true, b, pos, lane);
-      if constexpr (MODE == 2) {  // (the query rows are scaled even where the K/V write is skipped)
+      if constexpr (MODE >= 2) {  // (the query rows are scaled even where the K/V write is skipped)
+        constexpr bool PREP = MODE == 3;
         if (a.kvq == 1) {
-          if (a.hs == 128) quant_unit<128, 1>(a, tok, pos, slot, u, lane);
-          else if (a.hs == 256) quant_unit<256, 1>(a, tok, pos, slot, u, lane);
-          else quant_unit<64, 1>(a, tok, pos, slot, u, lane);
+          if (a.hs == 128) quant_unit<128, 1, PREP>(a, tok, pos, slot, u, lane);
+          else if (a.hs == 256) quant_unit<256, 1, PREP>(a, tok, pos, slot, u, lane);
+          else quant_unit<64, 1, PREP>(a, tok, pos, slot, u, lane);
         } else {
-          if (a.hs == 128) quant_unit<128, 2>(a, tok, pos, slot, u, lane);
-          else quant_unit<256, 2>(a, tok, pos, slot, u, lane);
+          if (a.hs == 128) quant_unit<128, 2, PREP>(a, tok, pos, slot, u, lane);
+          else quant_unit<256, 2, PREP>(a, tok, pos, slot, u, lane);
         }
       } else {  // (the query rows are prepared even where the K/V write is skipped)
         if (a.hs == 128) prep_unit<128>(a, tok, pos, slot, u, lane);
@@ -971,7 +971,7 @@ cudaError_t launch_cache_write(const Args& a, int sms, cudaStream_t s) {
   // a warp per token (bit copy) or per (token, unit): at most 8 blocks of 8 warps per SM
   const int64_t warps = (int64_t)a.N * ((a.kvq || a.prep) ? a.nh + a.kvh : 1);
   const int grid = (int)std::min<int64_t>((warps + 7) / 8, (int64_t)sms * 8);
-  if (a.kvq) return launch_pdl(cache_write_kernel<2>, dim3(grid), dim3(256), 0, s, a);
+  if (a.kvq) return launch_pdl(a.prep ? cache_write_kernel<3> : cache_write_kernel<2>, dim3(grid), dim3(256), 0, s, a);
   if (a.prep) return launch_pdl(cache_write_kernel<1>, dim3(grid), dim3(256), 0, s, a);
   return launch_pdl(cache_write_kernel<0>, dim3(grid), dim3(256), 0, s, a);
 }
