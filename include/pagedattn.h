@@ -93,12 +93,13 @@ typedef struct pa_dims {
                                       (the CPU-resident launch bound of the packed contract's
                                       attention_metadata). With route AUTO and max_query_len *
                                       (num_heads / kv_num_heads) <= 16 no prefill kernel is launched; if in
-                                      addition slot_mapping is NULL, batch_size <= 256, head_size <= 128,
-                                      the caches hold T and no Q/K preparation is asked for, a whole call
-                                      runs two kernels only (a reset of the workspace's counters, then the
-                                      decode kernel, which plans its own share of the work and writes this
-                                      call's K/V rows itself). The device checks the bound: a sequence above
-                                      it is a PA_DEVERR_BAD_BATCH and nothing is written. */
+                                      addition slot_mapping is NULL, batch_size <= 256 and head_size <= 128,
+                                      no planner runs: a reset of the workspace's counters, then the decode
+                                      kernel, which plans its own share of the work (with caches of T and
+                                      no Q/K preparation it also writes this call's K/V rows itself, two
+                                      kernels in all; else the cache-write kernel runs between the two and
+                                      checks the batch itself). The device checks the bound: a sequence
+                                      above it is a PA_DEVERR_BAD_BATCH and nothing is written. */
   int32_t qk_prep;                 /* non-zero: calls pass a pa_qk_prep, and the workspace also holds the
                                       prepared query rows (num_tokens * num_heads * head_size values of T) */
   int32_t kv_dtype;                /* pa_kv_dtype of the caches: INT8 with head_size 64, 128 or 256,

@@ -151,3 +151,27 @@ def test_integer_cache_needs_a_decode_bound():
                            k_scale=d["k_scale"], v_scale=d["v_scale"],
                            workspace=torch.zeros(1 << 20, dtype=torch.uint8, device="cuda"))
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int4"])
+def test_refused_self_planned_batch_writes_nothing(fmt):
+    # a decode-only call with no planner: an inconsistent batch (the last offset one short of
+    # the token count) must leave both code caches and the output untouched
+    p = w.make_problem(name="q-refuse", seed=35, dtype="fp16", num_heads=16, kv_num_heads=4, head_size=128,
+                       block_size=32, past=[40, 700, 3], q_lens=[1, 2, 1], kv_quant=fmt)
+    p.cumulative_sequence_length = p.cumulative_sequence_length.copy()
+    p.cumulative_sequence_length[-1] -= 1
+    d = upload(p)
+    before = cache_bytes(d["key_cache"]).copy(), cache_bytes(d["value_cache"]).copy()
+    dims = pa.make_dims(p.num_tokens, p.batch_size, p.head_size, p.num_blocks, p.block_size,
+                        p.max_blocks_per_sequence, TORCH_DT[p.dtype], 0, pa.ROUTE_AUTO, 2, False, fmt)
+    ws = torch.zeros(pa.workspace_size(dims, p.num_heads, p.kv_num_heads), dtype=torch.uint8, device="cuda")
+    out = torch.full((p.num_tokens, p.num_heads * p.head_size), 7.0, dtype=TORCH_DT[p.dtype], device="cuda")
+    pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
+                       d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], None,
+                       num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, output=out, workspace=ws,
+                       max_query_len=2, kv_quant=fmt, k_scale=d["k_scale"], v_scale=d["v_scale"])
+    assert pa.read_device_error(ws) & pa.DEVERR_BAD_BATCH
+    assert np.array_equal(cache_bytes(d["key_cache"]), before[0])
+    assert np.array_equal(cache_bytes(d["value_cache"]), before[1])
+    assert torch.all(out == 7.0)

@@ -150,3 +150,14 @@ def test_output_gate(name):
     assert_close(bits_of(out).reshape(p.num_tokens, p.num_heads, p.head_size), ref["out"], p.dtype, name)
     lg = lse.cpu().numpy().astype(np.float64)
     assert np.all(np.abs(lg - ref["lse"]) <= 5e-4 + 1e-5 * np.abs(ref["lse"]))  # lse is not gated
+
+
+def test_self_planned_decode_with_prep():
+    # a decode-only call with the host bound and derived slots: no planner; the cache-write
+    # kernel prepares Q and K, the decode kernel cuts its own share of the partition
+    p = w.make_problem(name="prep-self", seed=56, dtype="fp16", num_heads=32, kv_num_heads=8, head_size=128,
+                       block_size=16, past=[2900, 0, 17, 600, 1, 64], q_lens=[1, 2, 1, 4, 3, 1])
+    n0 = pa.kernel_launch_count()
+    check(p, dict(q_norm_weight=_weights(p, 0.5, 1.5), k_norm_weight=_weights(p, 1.2, 0.8), eps=1e-6,
+                  rotary_dim=128, theta=1e6), max_query_len=int(p.q_lens.max()))
+    assert pa.kernel_launch_count() - n0 == 3

@@ -184,11 +184,15 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
   // A whole decode-only call (proven by the host bound) with derived slots and a small batch
   // needs no planner and no cache-write kernel: a one-CTA reset, then the decode kernel plans
   // its own share and writes the new rows of the tiles it loads.
+  // (With the Q/K preparation or integer caches the cache-write kernel still runs: it writes
+  // the prepared or scaled query rows and the rows' codes, checking the batch itself.)
   const bool self_plan = stages == PA_STAGE_ALL && d->route == PA_ROUTE_AUTO && d->max_query_len > 0 &&
                          (int64_t)d->max_query_len * args.G <= pa::kDecRows && args.slot_mapping == nullptr &&
-                         !args.prep && !args.kvq && args.forced_split <= 0 && args.B >= 1 && args.B <= pa::kSelfMaxB &&
-                         hs <= 128 && args.N > 0 && slots > 0;
-  if (self_plan) stages = PA_STAGE_DECODE;
+                         args.forced_split <= 0 && args.B >= 1 && args.B <= pa::kSelfMaxB && hs <= 128 && args.N > 0 &&
+                         slots > 0;
+  const bool self_write_rows = self_plan && !args.prep && !args.kvq;
+  if (self_plan) stages = self_write_rows ? PA_STAGE_DECODE : PA_STAGE_CACHE_WRITE | PA_STAGE_DECODE;
+  args.self_plan = self_plan;  // (the cache-write kernel checks the batch itself)
   if (self_plan) {
     ++g_launches;
     if (cudaError_t e = pa::launch_decode_prep(args, stream)) return cuda_fail(e, "decode_prep_kernel launch");
@@ -261,6 +265,7 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
     ++g_launches;
     aq.dec_after_prefill = prefill_launched;  // runs beside this call's prefill kernel
     aq.self_plan = self_plan;
+    aq.self_write_rows = self_write_rows;
     if (cudaError_t e = pa::launch_decode(aq, bf16, tk, tv, seg, stream)) return cuda_fail(e, "decode_kernel launch");
   }
   return PA_OK;

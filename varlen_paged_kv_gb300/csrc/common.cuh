@@ -178,6 +178,8 @@ struct Args {
   // cache-write kernel; each decode CTA cuts its own share of the balanced partition from
   // the batch description and writes the new K/V rows of the tiles it loads
   int32_t self_plan;
+  int32_t self_write_rows;  // self-planned and the decode kernel writes this call's K/V rows
+                            // (else the cache-write kernel writes them, checking the batch itself)
   int32_t out_v8;         // output 32-byte aligned (prefill stores 32-byte chunks)
   float scale_log2;       // scale * log2(e)
   WsHeader* hdr;
@@ -231,7 +233,9 @@ struct DecSmem {
 static_assert(DecSmem<256>::kBytes <= 232448 && 2 * (DecSmem<128>::kBytes + 1024) <= 233472 &&
                   DecSmem<256, 1>::kBytes <= 232448 && DecSmem<256, 2>::kBytes <= 232448 &&
                   2 * (DecSmem<128, 1>::kBytes + 1024) <= 233472 && 2 * (DecSmem<128, 2>::kBytes + 1024) <= 233472 &&
-                  2 * (DecSmem<128, 0, true>::kBytes + 1024) <= 233472,
+                  2 * (DecSmem<128, 0, true>::kBytes + 1024) <= 233472 &&
+                  2 * (DecSmem<128, 1, true>::kBytes + 1024) <= 233472 &&
+                  2 * (DecSmem<128, 2, true>::kBytes + 1024) <= 233472,
               "decode shared memory");
 
 // Prefill: Q tile, two K and two V tiles, barriers, the TMEM address slot.

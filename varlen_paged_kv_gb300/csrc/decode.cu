@@ -502,14 +502,18 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
       for (int k0 = item.key_begin; k0 < item.key_end; k0 += kDecTile, ++cnt) {
         const int s = cnt % L::kStages;
         const uint32_t ph = (cnt / L::kStages) & 1;
-        if constexpr (SELF) write_new_rows<HS>(a, item, k0, lane);
+        if constexpr (SELF && KQ == 0) {
+          if (a.self_write_rows) write_new_rows<HS>(a, item, k0, lane);
+        }
         if (lane == 0) {
           mbar_wait(&empty[s], ph ^ 1, abort, err);
           mbar_arrive_expect_tx(&full[s], L::kStageBytes);
         }
         __syncwarp();
         if (lane < nseg) {
-          if constexpr (SELF) fence_proxy_async_global();  // (the rows written above, before the load)
+          if constexpr (SELF && KQ == 0) {
+            if (a.self_write_rows) fence_proxy_async_global();  // (the rows written above, before the load)
+          }
           const int key = k0 + lane * seg_rows;
           int z = oob;
           if (key < kv_len) {
@@ -985,7 +989,7 @@ cudaError_t launch_decode_prep(const Args& a, cudaStream_t s) {
 template <int HS, bool BF16, int KQ, bool SELF = false>
 static cudaError_t launch_decode_t(const Args& a, const CUtensorMap& tk, const CUtensorMap& tv, int seg,
                                    cudaStream_t s) {
-  if constexpr (KQ == 0 && HS != 256 && !SELF) {  // self-planned decode-only batches: their own instantiation
+  if constexpr (HS != 256 && !SELF) {  // self-planned decode-only batches: their own instantiation
     if (a.self_plan) return launch_decode_t<HS, BF16, KQ, true>(a, tk, tv, seg, s);
   }
   constexpr int smem = DecSmem<HS, KQ, SELF>::kBytes;

@@ -864,6 +864,19 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
   pdl_wait();
   pdl_launch_dependents();
   if (!a.hdr->valid) return;
+  if constexpr (MODE != 0) {
+    if (a.self_plan) {
+      // no planner ran: refuse an inconsistent batch here as well (the decode kernel, which
+      // checks it too, reports it), so that nothing is written
+      bool bad = threadIdx.x == 0 && (a.cum[0] != 0 || a.cum[a.B] != a.N);
+      for (int bb = threadIdx.x; bb < a.B; bb += blockDim.x) {
+        const int64_t q = (int64_t)a.cum[bb + 1] - a.cum[bb], kv = (int64_t)a.past[bb] + q;
+        bad |= q < 0 || a.past[bb] < 0 || kv > (int64_t)a.max_blocks * a.bs ||
+               (a.max_query_len > 0 && q > a.max_query_len);
+      }
+      if (__syncthreads_or(bad)) return;
+    }
+  }
   int b = 0;
   if constexpr (MODE != 0) {
     const int U = a.nh + a.kvh;
