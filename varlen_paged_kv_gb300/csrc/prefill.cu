@@ -379,9 +379,10 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           // word (or, against bf16 V, the bf16 hi and lo words) of each key pair replaces
           // that pair's two score registers ----
           const float neg_m = -m_used;
+          bool p_done = false;
           if constexpr (BF16) {
-            float lc[2] = {0.f, 0.f};
-            if (!v16) {
+            if (!v16) {  // against bf16 V: P as hi and lo bf16 parts
+              float lc[2] = {0.f, 0.f};
 #pragma unroll
               for (int g2 = 0; g2 < COLS / 16; ++g2) {
                 uint32_t* q = r + g2 * 16;
@@ -397,25 +398,13 @@ __global__ void __launch_bounds__(kPreThreads, 1)
                 tmem_st_x8_nowait(s_base + p_col(kk), q[0], q[2], q[4], q[6], q[8], q[10], q[12], q[14]);
                 tmem_st_x8_nowait(s_base + p_col(kk) + 16, q[1], q[3], q[5], q[7], q[9], q[11], q[13], q[15]);
               }
-            } else {
-#pragma unroll
-              for (int g2 = 0; g2 < COLS / 16; ++g2) {
-                uint32_t* q = r + g2 * 16;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                  const float p0 = fast_exp2(fmaf(__uint_as_float(q[2 * e]), c, neg_m));
-                  const float p1 = fast_exp2(fmaf(__uint_as_float(q[2 * e + 1]), c, neg_m));
-                  lc[0] += p0;
-                  lc[1] += p1;
-                  q[2 * e] = pack2<false>(p0, p1);
-                }
-                const int kk = hsel * (COLS / 16) + g2;
-                tmem_st_x8_nowait(s_base + p_col(kk), q[0], q[2], q[4], q[6], q[8], q[10], q[12], q[14]);
-              }
+              l += lc[0] + lc[1];
+              p_done = true;
             }
-            l += lc[0] + lc[1];
-          } else {
-            // s * c - m and the row sums on packed fp32 pairs (one instruction per key pair)
+          }
+          if (!p_done) {
+            // fp16 P (fp16 V, or the fp16 copy of bf16 V): s * c - m and the row sums on packed
+            // fp32 pairs (one instruction per key pair)
             const uint64_t c2 = f2_make(c, c), nm2 = f2_make(neg_m, neg_m);
             uint64_t lsum[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
 #pragma unroll
@@ -423,8 +412,9 @@ __global__ void __launch_bounds__(kPreThreads, 1)
               uint32_t* q = r + g2 * 16;
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
+                const uint64_t x2 = f2_fma(f2_make(__uint_as_float(q[2 * e]), __uint_as_float(q[2 * e + 1])), c2, nm2);
                 float x0, x1;
-                f2_split(f2_fma(f2_make(__uint_as_float(q[2 * e]), __uint_as_float(q[2 * e + 1])), c2, nm2), x0, x1);
+                f2_split(x2, x0, x1);
                 const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
                 lsum[e & 1] = f2_add(lsum[e & 1], f2_make(p0, p1));
                 q[2 * e] = pack2<false>(p0, p1);
