@@ -25,8 +25,9 @@ __host__ __device__ constexpr int dec_ctas_per_sm(int hs) { return hs == 256 ? 1
 // What an item costs a decode CTA beyond streaming its keys (the warps' combine, the write
 // of the row or partial, the merge, the refill of the ring at the next item), in 64-key
 // tiles streamed in the same time (measured: about 5 us per item against 1.4 us per tile
-// at head_size 256 with one CTA per SM, 1.5-2 us against 1.4 us at 128 with two).
-__host__ __device__ constexpr int dec_item_cost_tiles(int hs) { return hs == 256 ? 3 : 1; }
+// at head_size 256 with one CTA per SM; at 128 with two, per-CTA timestamps fitted about
+// 4 us per item against 1.2 us per tile, the CTAs with the most items finishing last).
+__host__ __device__ constexpr int dec_item_cost_tiles(int /*hs*/) { return 3; }
 constexpr int kMaxDecCtas = 1024;     // upper bound of the decode grid
 constexpr int kSelfMaxB = 256;        // sequences of a decode-only batch the decode kernel plans itself
 // rates of the planner's model that splits the SMs between the prefill and the decode
