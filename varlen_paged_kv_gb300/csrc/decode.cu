@@ -908,28 +908,42 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
         }
         consumer_bar();
         if (*s_last && mine) {
-          // the unit's other items have all arrived: merge its partials in key order
+          // the unit's other items have all arrived: merge its partials in key order, two
+          // pieces per step with a running max (both pieces' lse and rows are loaded together,
+          // one L2 round trip per step: this merge usually ends the CTA's work)
           float Mx = -INFINITY;
-          for (int s2 = 0; s2 < item.n_split; ++s2)
-            Mx = fmaxf(Mx, __ldcg(a.part_lse + (int64_t)piece_slot<SELF>(item, s2) * kDecRows + row));
           float acc[CW];
 #pragma unroll
           for (int v = 0; v < CW; ++v) acc[v] = 0.f;
           float den = 0.f;
-          for (int s2 = 0; s2 < item.n_split; ++s2) {
-            const int64_t pr = (int64_t)piece_slot<SELF>(item, s2) * kDecRows + row;
-            const float lse = __ldcg(a.part_lse + pr);
-            const float wgt = lse == -INFINITY ? 0.f : fast_exp2((lse - Mx) * 1.4426950408889634f);
-            den += wgt;
-            const float4* ps = reinterpret_cast<const float4*>(a.part_o + pr * HS + col);
+          for (int s2 = 0; s2 < item.n_split; s2 += 2) {
+            const bool two = s2 + 1 < item.n_split;
+            const int64_t pa = (int64_t)piece_slot<SELF>(item, s2) * kDecRows + row;
+            const int64_t pb = two ? (int64_t)piece_slot<SELF>(item, s2 + 1) * kDecRows + row : pa;
+            const float la = __ldcg(a.part_lse + pa);
+            const float lb = two ? __ldcg(a.part_lse + pb) : -INFINITY;
+            const float4* psa = reinterpret_cast<const float4*>(a.part_o + pa * HS + col);
+            const float4* psb = reinterpret_cast<const float4*>(a.part_o + pb * HS + col);
+            float4 xa[CW / 4], xb[CW / 4];
 #pragma unroll
             for (int v = 0; v < CW / 4; ++v) {
-              const float4 x4 = __ldcg(ps + v);
-              acc[4 * v + 0] += wgt * x4.x;
-              acc[4 * v + 1] += wgt * x4.y;
-              acc[4 * v + 2] += wgt * x4.z;
-              acc[4 * v + 3] += wgt * x4.w;
+              xa[v] = __ldcg(psa + v);
+              xb[v] = __ldcg(psb + v);  // (piece a again when there is no second piece: weight 0)
             }
+            const float Mn = fmaxf(Mx, fmaxf(la, lb));
+            if (Mn == -INFINITY) continue;  // no key so far
+            const float sc = Mx == -INFINITY ? 0.f : fast_exp2((Mx - Mn) * 1.4426950408889634f);
+            const float wa = la == -INFINITY ? 0.f : fast_exp2((la - Mn) * 1.4426950408889634f);
+            const float wb = lb == -INFINITY ? 0.f : fast_exp2((lb - Mn) * 1.4426950408889634f);
+            den = (den * sc + wa) + wb;
+#pragma unroll
+            for (int v = 0; v < CW / 4; ++v) {
+              acc[4 * v + 0] = (acc[4 * v + 0] * sc + wa * xa[v].x) + wb * xb[v].x;
+              acc[4 * v + 1] = (acc[4 * v + 1] * sc + wa * xa[v].y) + wb * xb[v].y;
+              acc[4 * v + 2] = (acc[4 * v + 2] * sc + wa * xa[v].z) + wb * xb[v].z;
+              acc[4 * v + 3] = (acc[4 * v + 3] * sc + wa * xa[v].w) + wb * xb[v].w;
+            }
+            Mx = Mn;
           }
           const float dinv = 1.f / den;
           if (a.lse && (t & 7) == 0) a.lse[(int64_t)tok * a.nh + head] = Mx + fast_log2(den) * 0.69314718055994531f - lbias;
