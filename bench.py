@@ -319,8 +319,8 @@ class Runner:
 # (profiles/<kernel>_<workload>.md), with a hash of the kernel's sources at capture time:
 # the figure is reported only while the sources are unchanged, else traffic is null.
 NCU_TRAFFIC = {
-    ("decode_kernel", "decode-b64"): (622987264, "c3a996cfe6693505"),
-    ("prefill_kernel", "causal-prefill-4x2048"): (136311040, "abf5de6b6649881d"),
+    ("decode_kernel", "decode-b64"): (622765056, "65be048ea4a7824c"),
+    ("prefill_kernel", "causal-prefill-4x2048"): (136483584, "490538c01a1b4bf6"),
 }
 KERNEL_SOURCES = {"decode_kernel": ("decode.cu", "common.cuh"), "prefill_kernel": ("prefill.cu", "common.cuh")}
 
