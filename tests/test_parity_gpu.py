@@ -249,6 +249,20 @@ def test_out_of_range_block_is_reported_and_read_as_zeros():
     assert r["err"] & pa.DEVERR_BAD_BLOCK
 
 
+def test_errors_of_a_copy_beside_the_planner_are_kept():
+    # fp16 bit copies run beside this call's planner, which resets the error word: their
+    # bad-block and bad-slot bits are added only after it
+    p = _case("chunked-prefill")
+    p.block_table = p.block_table.copy()
+    p.block_table[1, 0] = 10 ** 6
+    assert run_gpu(p)["err"] & pa.DEVERR_BAD_BLOCK
+    q = _case("mixed-packed-drops")
+    q.slot_mapping = q.slot_mapping.copy()
+    live = int(np.flatnonzero(q.slot_mapping >= 0)[0])
+    q.slot_mapping[live] = q.num_blocks * q.block_size + 5
+    assert run_gpu(q)["err"] & pa.DEVERR_BAD_SLOT
+
+
 def test_inconsistent_batch_is_refused_without_writes():
     p = _case("chunked-prefill")
     p.cumulative_sequence_length = p.cumulative_sequence_length.copy()

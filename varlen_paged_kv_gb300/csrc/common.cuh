@@ -30,6 +30,7 @@ __host__ __device__ constexpr int dec_ctas_per_sm(int hs) { return hs == 256 ? 1
 __host__ __device__ constexpr int dec_item_cost_tiles(int /*hs*/) { return 3; }
 constexpr int kMaxDecCtas = 1024;     // upper bound of the decode grid
 constexpr int kSelfMaxB = 256;        // sequences of a decode-only batch the decode kernel plans itself
+constexpr int kEarlyWriteMaxB = 1024; // sequences a bit-copy cache write checks per CTA to run beside the planner
 // rates of the planner's model that splits the SMs between the prefill and the decode
 // kernel of a call with both kinds of rows (measured on GB300 at head_size 128)
 constexpr float kSplitPreFlops = 8.2e12f;   // prefill FLOP/s per SM, 128 x 128 tiles counted whole
@@ -180,6 +181,9 @@ struct Args {
   // the batch description and writes the new K/V rows of the tiles it loads
   int32_t self_plan;
   int32_t self_write_rows;  // self-planned and the decode kernel writes this call's K/V rows
+  int32_t cw_early;         // bit-copy cache write launched right after this call's planner:
+                            // it copies the rows while the planner runs (checking the batch
+                            // itself) and waits for the plan only before the fp16 V copy
                             // (else the cache-write kernel writes them, checking the batch itself)
   int32_t out_v8;         // output 32-byte aligned (prefill stores 32-byte chunks)
   float scale_log2;       // scale * log2(e)

@@ -787,7 +787,9 @@ __device__ void quant_unit(const Args& a, int tok, int64_t pos, int64_t slot, in
 }
 
 // The slot of token tok (slot_mapping[tok], or its logical position through block_table),
-// -1 for a suppressed write or an out-of-range block or slot (those also flagged); pos is
+// -1 for a suppressed write or an out-of-range block or slot (those also flagged: in the
+// error word, or with DEFER in errs, which the caller adds to the word once the planner has
+// reset it); pos is
 // the token's logical position when the caller needs it (no slot_mapping, or prep). b is
 // the sequence of the warp's previous token, tokens only grow within a warp.
 // The last b in [b0, B) with cum[b] <= tok (given cum[b0] <= tok), found by the warp: each
@@ -808,8 +810,14 @@ __device__ __forceinline__ int warp_find_seq(const int* cum, int b0, int B, int 
   return lo + 31 - __clz(m);
 }
 
+template <bool DEFER = false>
 __device__ __forceinline__ int64_t resolve_slot(const Args& a, int tok, bool need_pos, int& b, int64_t& pos,
-                                                int lane) {
+                                                uint32_t& errs) {
+  const int lane = threadIdx.x & 31;
+  auto flag = [&](uint32_t bit) {
+    if constexpr (DEFER) errs |= bit;
+    else if (lane == 0) atomicOr(&a.hdr->error, bit);
+  };
   pos = 0;
   if (!a.slot_mapping || need_pos) {
     b = warp_find_seq(a.cum, b, a.B, tok, lane);
@@ -821,30 +829,33 @@ __device__ __forceinline__ int64_t resolve_slot(const Args& a, int tok, bool nee
   } else {
     const int blk = a.block_table[(int64_t)b * a.max_blocks + pos / a.bs];
     if (blk < 0 || blk >= a.num_blocks) {
-      if (lane == 0) atomicOr(&a.hdr->error, PA_DEVERR_BAD_BLOCK);
+      flag(PA_DEVERR_BAD_BLOCK);
       slot = -1;
     } else {
       slot = (int64_t)blk * a.bs + pos % a.bs;
     }
   }
   if (slot != -1 && (slot < 0 || slot >= (int64_t)a.num_blocks * a.bs)) {
-    if (lane == 0) atomicOr(&a.hdr->error, PA_DEVERR_BAD_SLOT);
+    flag(PA_DEVERR_BAD_SLOT);
     slot = -1;
   }
   return slot;
 }
 
 // One instantiation per kind of write, so that each keeps only the registers it needs and
-// stays many warps deep: 0 = bit copy, one warp per token; 1 = Q/K preparation, 2 = integer
+// stays many warps deep (at most 64 registers: four blocks of 256 per SM): 0 = bit copy,
+// one warp per token, 4 = the same beside this call's planner; 1 = Q/K preparation, 2 = integer
 // caches, 3 = both, one warp per (token, unit), the units being the token's nh query heads
 // and then its kvh KV heads (each a short dependent chain of a load, warp reductions and a
 // store, so the units of a token run in parallel, not one after the other).
 template <int MODE>
-__global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
+__global__ void __launch_bounds__(256, 4) cache_write_kernel(const Args a) {
+  constexpr bool COPY = MODE == 0 || MODE == 4;  // bit copy
+  constexpr bool early = MODE == 4;
   const int lane = threadIdx.x & 31;
   const int warps = (int)((gridDim.x * blockDim.x) >> 5);
   const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-  if constexpr (MODE == 0) {
+  if constexpr (COPY) {
     // this warp's first token's K and V rows and the batch description into L2 while the
     // earlier kernels finish (hints only: every load below comes after the wait)
     if (gw < a.N) {
@@ -861,10 +872,29 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
         if (i < a.B) prefetch_l2(a.past + i);
       }
   }
-  pdl_wait();
-  pdl_launch_dependents();
-  if (!a.hdr->valid) return;
-  if constexpr (MODE != 0) {
+  // A bit copy launched right after this call's planner starts once the planner's own wait
+  // has returned (so every earlier call is finished) and copies the rows beside it, after
+  // checking the batch as the planner does, so that a refused batch writes nothing; it waits
+  // for the plan before the fp16 V copy, its error bits (the planner resets the word) and
+  // its exit, so its completion still implies the planner's.
+  uint32_t errs = 0;  // (lane 0 of each warp flags bad blocks and slots)
+  if constexpr (early) {
+    bool bad = threadIdx.x == 0 && (a.cum[0] != 0 || a.cum[a.B] != a.N);
+    for (int bb = threadIdx.x; bb < a.B; bb += blockDim.x) {
+      const int64_t q = (int64_t)a.cum[bb + 1] - a.cum[bb], kv = (int64_t)a.past[bb] + q;
+      bad |= q < 0 || a.past[bb] < 0 || kv > (int64_t)a.max_blocks * a.bs ||
+             (a.max_query_len > 0 && q > a.max_query_len);
+    }
+    if (__syncthreads_or(bad)) {
+      pdl_wait();
+      return;
+    }
+  } else {
+    pdl_wait();
+    pdl_launch_dependents();
+    if (!a.hdr->valid) return;
+  }
+  if constexpr (!COPY) {
     if (a.self_plan) {
       // no planner ran: refuse an inconsistent batch here as well (the decode kernel, which
       // checks it too, reports it), so that nothing is written
@@ -877,14 +907,14 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
       if (__syncthreads_or(bad)) return;
     }
   }
-  int b = 0;
-  if constexpr (MODE != 0) {
+  if constexpr (!COPY) {
+    int b = 0;
     const int U = a.nh + a.kvh;
     const int64_t total = (int64_t)a.N * U;
     for (int64_t wi = gw; wi < total; wi += warps) {
       const int tok = (int)(wi / U), u = (int)(wi - (int64_t)tok * U);
       int64_t pos;
-      const int64_t slot = resolve_slot(a, tok, true, b, pos, lane);
+      const int64_t slot = resolve_slot(a, tok, true, b, pos, errs);  // (after the wait: flagged at once)
       if constexpr (MODE >= 2) {  // (the query rows are scaled even where the K/V write is skipped)
         constexpr bool PREP = MODE == 3;
         if (a.kvq == 1) {
@@ -904,55 +934,77 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const Args a) {
     return;
   }
   const int chunks = a.kv_row / 8;  // 16-byte chunks in one K (or V) row
-  // bf16 with derived slots: the fp16 copy of the prefill-class sequences' V is written here,
-  // each new row from the input it comes from (this call writes every derived position, and
-  // no other position), the older rows from the cache below; no copy kernel runs
-  const bool mirror = MODE == 0 && a.mirror_keys > 0 && !a.slot_mapping && a.hdr->v_mirror;
   uint32_t big = 0;  // per-half max of |fp16| bits of this lane's copied values
-  for (int tok = gw; tok < a.N; tok += warps) {
-    int64_t pos;
-    const int64_t slot = resolve_slot(a, tok, false, b, pos, lane);
-    int mrow = -1;  // the token's row of the fp16 V copy
-    if (mirror) {
-      const int base = a.mirror_base[b];
-      if (base >= 0) mrow = base + (int)pos;
-    }
-    if (slot == -1) {  // (derived slots: a block outside the pool, which reads as zeros)
-      if (mrow >= 0)
-        for (int c = lane; c < chunks; c += 32)
-          reinterpret_cast<uint4*>(a.mirror + (int64_t)mrow * a.kv_row)[c] = make_uint4(0, 0, 0, 0);
-      continue;
-    }
-    const uint16_t *src_k, *src_v;
-    if (a.packed) {
-      src_k = reinterpret_cast<const uint16_t*>(a.query) + (int64_t)tok * a.q_stride + a.k_offset;
-      src_v = reinterpret_cast<const uint16_t*>(a.query) + (int64_t)tok * a.q_stride + a.v_offset;
-    } else {
-      src_k = reinterpret_cast<const uint16_t*>(a.key) + (int64_t)tok * a.kv_row;
-      src_v = reinterpret_cast<const uint16_t*>(a.value) + (int64_t)tok * a.kv_row;
-    }
-    uint4* dst_k = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.key_cache) + slot * a.kv_row);
-    uint4* dst_v = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.value_cache) + slot * a.kv_row);
-    for (int c0 = lane; c0 < chunks; c0 += 128) {
-      uint4 k[4], v[4];
+  // One pass over this warp's tokens: the K and V rows into the cache (kv) and, for bf16 with
+  // derived slots, the fp16 copy of the prefill-class sequences' V (mirror): each new row
+  // from the input it comes from (this call writes every derived position, and no other
+  // position), the older rows from the cache afterwards; no copy kernel runs.
+  auto pass = [&](auto kv_c, auto mirror_c, auto defer_c) {  // (compile-time flags: each pass keeps only its registers)
+    constexpr bool kv = decltype(kv_c)::value, mirror = decltype(mirror_c)::value;
+    int b = 0;
+    for (int tok = gw; tok < a.N; tok += warps) {
+      int64_t pos;
+      const int64_t slot = resolve_slot<decltype(defer_c)::value>(a, tok, false, b, pos, errs);
+      int mrow = -1;  // the token's row of the fp16 V copy
+      if constexpr (mirror) {
+        const int base = a.mirror_base[b];
+        if (base >= 0) mrow = base + (int)pos;
+      }
+      if (slot == -1) {  // (derived slots: a block outside the pool, which reads as zeros)
+        if (mrow >= 0)
+          for (int c = lane; c < chunks; c += 32)
+            reinterpret_cast<uint4*>(a.mirror + (int64_t)mrow * a.kv_row)[c] = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      if (!kv && mrow < 0) continue;
+      const uint16_t *src_k, *src_v;
+      if (a.packed) {
+        src_k = reinterpret_cast<const uint16_t*>(a.query) + (int64_t)tok * a.q_stride + a.k_offset;
+        src_v = reinterpret_cast<const uint16_t*>(a.query) + (int64_t)tok * a.q_stride + a.v_offset;
+      } else {
+        src_k = reinterpret_cast<const uint16_t*>(a.key) + (int64_t)tok * a.kv_row;
+        src_v = reinterpret_cast<const uint16_t*>(a.value) + (int64_t)tok * a.kv_row;
+      }
+      uint4* dst_k = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.key_cache) + slot * a.kv_row);
+      uint4* dst_v = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.value_cache) + slot * a.kv_row);
+      for (int c0 = lane; c0 < chunks; c0 += 128) {
+        uint4 k[4], v[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int c = c0 + 32 * j;
-        if (c < chunks) {
-          k[j] = __ldg(reinterpret_cast<const uint4*>(src_k) + c);
-          v[j] = __ldg(reinterpret_cast<const uint4*>(src_v) + c);
+        for (int j = 0; j < 4; ++j) {
+          const int c = c0 + 32 * j;
+          if (c < chunks) {
+            if constexpr (kv) k[j] = __ldg(reinterpret_cast<const uint4*>(src_k) + c);
+            v[j] = __ldg(reinterpret_cast<const uint4*>(src_v) + c);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = c0 + 32 * j;
+          if (c < chunks) {
+            if constexpr (kv) {
+              dst_k[c] = k[j];
+              dst_v[c] = v[j];
+            }
+            if (mrow >= 0) reinterpret_cast<uint4*>(a.mirror + (int64_t)mrow * a.kv_row)[c] = chunk_to_f16(v[j], big);
+          }
         }
       }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int c = c0 + 32 * j;
-        if (c < chunks) {
-          dst_k[c] = k[j];
-          dst_v[c] = v[j];
-          if (mrow >= 0) reinterpret_cast<uint4*>(a.mirror + (int64_t)mrow * a.kv_row)[c] = chunk_to_f16(v[j], big);
-        }
-      }
     }
+  };
+  using yes = std::true_type;
+  using no = std::false_type;
+  if constexpr (early) {
+    pass(yes{}, no{}, yes{});  // (errors kept in errs: the planner resets the error word)
+    pdl_wait();  // the plan: the V copy's layout, and the error word reset
+    pdl_launch_dependents();
+    if (lane == 0 && errs) atomicOr(&a.hdr->error, errs);
+  }
+  const bool mirror = a.mirror_keys > 0 && !a.slot_mapping && a.hdr->v_mirror;
+  if constexpr (!early) {
+    if (mirror) pass(yes{}, yes{}, no{});
+    else pass(yes{}, no{}, no{});
+  } else if (mirror) {
+    pass(no{}, yes{}, no{});  // (the input V rows were just read: mostly L2 hits)
   }
   if (mirror) {  // the copy's rows of keys before this call
     const int rows = a.hdr->mirror_rows, n = a.hdr->mirror_seqs;
@@ -986,6 +1038,7 @@ cudaError_t launch_cache_write(const Args& a, int sms, cudaStream_t s) {
   const int grid = (int)std::min<int64_t>((warps + 7) / 8, (int64_t)sms * 8);
   if (a.kvq) return launch_pdl(a.prep ? cache_write_kernel<3> : cache_write_kernel<2>, dim3(grid), dim3(256), 0, s, a);
   if (a.prep) return launch_pdl(cache_write_kernel<1>, dim3(grid), dim3(256), 0, s, a);
+  if (a.cw_early) return launch_pdl(cache_write_kernel<4>, dim3(grid), dim3(256), 0, s, a);
   return launch_pdl(cache_write_kernel<0>, dim3(grid), dim3(256), 0, s, a);
 }
 
