@@ -205,12 +205,8 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
   const bool can_prefill = prefill_possible(d, args.G);
   if ((stages & PA_STAGE_CACHE_WRITE) && args.N > 0) {
     ++g_launches;
-    // the bit copy right after this call's planner copies the rows beside it, unless it also
-    // makes the fp16 V copy (bf16 with derived slots: that copy needs the plan, and taking it
-    // in a second pass over the rows cost more than the overlap saved on the causal prefill)
-    const bool fused_copy = args.mirror_keys > 0 && args.slot_mapping == nullptr;
-    args.cw_early = (stages & PA_STAGE_PLAN) && !args.prep && !args.kvq && !fused_copy &&
-                    args.B <= pa::kEarlyWriteMaxB;
+    // the bit copy right after this call's planner copies the rows beside it
+    args.cw_early = (stages & PA_STAGE_PLAN) && !args.prep && !args.kvq && args.B <= pa::kEarlyWriteMaxB;
     if (cudaError_t e = pa::launch_cache_write(args, info.sms, stream)) return cuda_fail(e, "cache_write_kernel launch");
     args.cw_early = 0;
     if (can_prefill && args.mirror_keys > 0 && slots > 0 && (args.slot_mapping != nullptr || args.prep || args.kvq)) {

@@ -842,16 +842,38 @@ __device__ __forceinline__ int64_t resolve_slot(const Args& a, int tok, bool nee
   return slot;
 }
 
+// The first row of sequence b in the fp16 V copy, worked out by a warp as the planner lays
+// the copy out (the keys of every prefill-class sequence in sequence order; the copy is made
+// only if all of them fit), or -1 for a sequence without a copy: the bit copy beside the
+// planner writes the copy of this call's rows without waiting for the plan.
+__device__ __forceinline__ int own_mirror_base(const Args& a, int b, int lane) {
+  int64_t before = 0, total = 0, mine = 0;
+  for (int i = lane; i < a.B; i += 32) {
+    const int64_t q = (int64_t)a.cum[i + 1] - a.cum[i];
+    const int64_t rows = (q > 0 && !is_decode_class(q, a)) ? (int64_t)a.past[i] + q : 0;
+    total += rows;
+    if (i < b) before += rows;
+    if (i == b) mine = rows;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    total += __shfl_xor_sync(0xffffffffu, total, o);
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+    mine += __shfl_xor_sync(0xffffffffu, mine, o);
+  }
+  return (mine > 0 && total <= a.mirror_keys) ? (int)before : -1;
+}
+
 // One instantiation per kind of write, so that each keeps only the registers it needs and
 // stays many warps deep (at most 64 registers: four blocks of 256 per SM): 0 = bit copy,
-// one warp per token, 4 = the same beside this call's planner; 1 = Q/K preparation, 2 = integer
+// one warp per token, 4 = the same beside this call's planner, 5 = that with the fp16 V copy; 1 = Q/K preparation, 2 = integer
 // caches, 3 = both, one warp per (token, unit), the units being the token's nh query heads
 // and then its kvh KV heads (each a short dependent chain of a load, warp reductions and a
 // store, so the units of a token run in parallel, not one after the other).
 template <int MODE>
 __global__ void __launch_bounds__(256, 4) cache_write_kernel(const Args a) {
-  constexpr bool COPY = MODE == 0 || MODE == 4;  // bit copy
-  constexpr bool early = MODE == 4;
+  constexpr bool COPY = MODE == 0 || MODE >= 4;  // bit copy
+  constexpr bool early = MODE >= 4;
   const int lane = threadIdx.x & 31;
   const int warps = (int)((gridDim.x * blockDim.x) >> 5);
   const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
@@ -939,16 +961,25 @@ __global__ void __launch_bounds__(256, 4) cache_write_kernel(const Args a) {
   // derived slots, the fp16 copy of the prefill-class sequences' V (mirror): each new row
   // from the input it comes from (this call writes every derived position, and no other
   // position), the older rows from the cache afterwards; no copy kernel runs.
-  auto pass = [&](auto kv_c, auto mirror_c, auto defer_c) {  // (compile-time flags: each pass keeps only its registers)
-    constexpr bool kv = decltype(kv_c)::value, mirror = decltype(mirror_c)::value;
-    int b = 0;
+  // (compile-time flags, so that each pass keeps only its registers; mirror: 0 none, 1 by the
+  // planner's layout, 2 by the layout worked out here)
+  auto pass = [&](auto kv_c, auto mirror_c, auto defer_c) {
+    constexpr bool kv = decltype(kv_c)::value;
+    constexpr int mirror = decltype(mirror_c)::value;
+    int b = 0, mb = -1, mb_of = -1;  // (the last sequence's first copy row)
     for (int tok = gw; tok < a.N; tok += warps) {
       int64_t pos;
       const int64_t slot = resolve_slot<decltype(defer_c)::value>(a, tok, false, b, pos, errs);
       int mrow = -1;  // the token's row of the fp16 V copy
-      if constexpr (mirror) {
+      if constexpr (mirror == 1) {
         const int base = a.mirror_base[b];
         if (base >= 0) mrow = base + (int)pos;
+      } else if constexpr (mirror == 2) {
+        if (b != mb_of) {
+          mb = own_mirror_base(a, b, lane);
+          mb_of = b;
+        }
+        if (mb >= 0) mrow = mb + (int)pos;
       }
       if (slot == -1) {  // (derived slots: a block outside the pool, which reads as zeros)
         if (mrow >= 0)
@@ -993,18 +1024,21 @@ __global__ void __launch_bounds__(256, 4) cache_write_kernel(const Args a) {
   };
   using yes = std::true_type;
   using no = std::false_type;
+  using m0 = std::integral_constant<int, 0>;
+  using m1 = std::integral_constant<int, 1>;
+  using m2 = std::integral_constant<int, 2>;
   if constexpr (early) {
-    pass(yes{}, no{}, yes{});  // (errors kept in errs: the planner resets the error word)
-    pdl_wait();  // the plan: the V copy's layout, and the error word reset
+    // (errors kept in errs: the planner resets the error word)
+    if constexpr (MODE == 5) pass(yes{}, m2{}, yes{});
+    else pass(yes{}, m0{}, yes{});
+    pdl_wait();  // the plan (the copy's history rows), and the error word reset
     pdl_launch_dependents();
     if (lane == 0 && errs) atomicOr(&a.hdr->error, errs);
   }
   const bool mirror = a.mirror_keys > 0 && !a.slot_mapping && a.hdr->v_mirror;
   if constexpr (!early) {
-    if (mirror) pass(yes{}, yes{}, no{});
-    else pass(yes{}, no{}, no{});
-  } else if (mirror) {
-    pass(no{}, yes{}, no{});  // (the input V rows were just read: mostly L2 hits)
+    if (mirror) pass(yes{}, m1{}, no{});
+    else pass(yes{}, m0{}, no{});
   }
   if (mirror) {  // the copy's rows of keys before this call
     const int rows = a.hdr->mirror_rows, n = a.hdr->mirror_seqs;
@@ -1038,7 +1072,9 @@ cudaError_t launch_cache_write(const Args& a, int sms, cudaStream_t s) {
   const int grid = (int)std::min<int64_t>((warps + 7) / 8, (int64_t)sms * 8);
   if (a.kvq) return launch_pdl(a.prep ? cache_write_kernel<3> : cache_write_kernel<2>, dim3(grid), dim3(256), 0, s, a);
   if (a.prep) return launch_pdl(cache_write_kernel<1>, dim3(grid), dim3(256), 0, s, a);
-  if (a.cw_early) return launch_pdl(cache_write_kernel<4>, dim3(grid), dim3(256), 0, s, a);
+  if (a.cw_early)
+    return launch_pdl(a.mirror_keys > 0 && !a.slot_mapping ? cache_write_kernel<5> : cache_write_kernel<4>, dim3(grid),
+                      dim3(256), 0, s, a);
   return launch_pdl(cache_write_kernel<0>, dim3(grid), dim3(256), 0, s, a);
 }
 
