@@ -95,7 +95,8 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        # the raw samples of the timed region (the JSON line carries their summary)
+        self.path = os.path.join(ROOT, "_build", f"clocks_gpu{gpu_index}.csv")
 
     def __enter__(self):
         os.makedirs(os.path.dirname(self.path), exist_ok=True)
