@@ -795,7 +795,21 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
     row_stats(mw, lw, r1, M1, L1);
     const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M0);
     const float f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M1);
-    {
+    // An item of at most kDecRows / kDecWarps rows (one decode token of up to four heads): the
+    // four warps' rows fit the buffer side by side, warp w's at rows 4w .. 4w + 3, so they
+    // are written in one round and the write below adds them in warp order (the order, and
+    // so the rounding, of the rounds).
+    constexpr int kCompactRows = kDecRows / kDecWarps;
+    const bool compact = KQ == 0 && L::kCombBufs == 1 && n_rows <= kCompactRows;
+    if (compact) {
+      if (gq < kCompactRows) {
+        float* cw = comb + (w * kCompactRows + r0) * kCombStride + tq * 2;
+#pragma unroll
+        for (int d = 0; d < ND; ++d)
+          *reinterpret_cast<float2*>(cw + d * 8) = make_float2(o[d][0] * f0, o[d][1] * f0);
+      }
+      consumer_bar();
+    } else {
       // round rr: warps rr * B .. rr * B + B - 1 write (first round) or add their partials
       // into buffers 0 .. B - 1; buffer b ends up holding warps b, b + B, ... in that order
       constexpr int B = L::kCombBufs;
@@ -856,6 +870,11 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
       // partials added in warp order
       auto cval = [&](int v) {
         float x = src[v];
+        if (compact) {  // (row < kCompactRows)
+#pragma unroll
+          for (int ww = 1; ww < kDecWarps; ++ww) x += src[ww * kCompactRows * kCombStride + v];
+          return x;
+        }
 #pragma unroll
         for (int bb = 1; bb < L::kCombBufs; ++bb) x += src[bb * (kDecRows * kCombStride) + v];
         return x;
