@@ -19,6 +19,7 @@
 #include <limits.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -866,10 +867,11 @@ __device__ __forceinline__ int own_mirror_base(const Args& a, int b, int lane) {
 
 // One instantiation per kind of write, so that each keeps only the registers it needs and
 // stays many warps deep (at most 64 registers: four blocks of 256 per SM): 0 = bit copy,
-// one warp per token, 4 = the same beside this call's planner, 5 = that with the fp16 V copy; 1 = Q/K preparation, 2 = integer
-// caches, 3 = both, one warp per (token, unit), the units being the token's nh query heads
-// and then its kvh KV heads (each a short dependent chain of a load, warp reductions and a
-// store, so the units of a token run in parallel, not one after the other).
+// one warp per token, 4 = the same beside this call's planner, 5 = that with the fp16 V
+// copy; 1 = Q/K preparation, 2 = integer caches, 3 = both, one warp per (token, unit), the
+// units being the token's nh query heads and then its kvh KV heads (each a short dependent
+// chain of a load, warp reductions and a store, so the units of a token run in parallel,
+// not one after the other).
 template <int MODE>
 __global__ void __launch_bounds__(256, 4) cache_write_kernel(const Args a) {
   constexpr bool COPY = MODE == 0 || MODE >= 4;  // bit copy
@@ -879,7 +881,7 @@ __global__ void __launch_bounds__(256, 4) cache_write_kernel(const Args a) {
   const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   if constexpr (COPY) {
     // this warp's first token's K and V rows and the batch description into L2 while the
-    // earlier kernels finish (hints only: every load below comes after the wait)
+    // earlier kernels finish (hints only)
     if (gw < a.N) {
       const int lines = a.kv_row * 2 / 128;  // 128-byte lines of one K (or V) row
       const char* src = a.packed ? reinterpret_cast<const char*>(a.query) + ((int64_t)gw * a.q_stride + a.k_offset) * 2
