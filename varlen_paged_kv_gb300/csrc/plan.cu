@@ -5,9 +5,10 @@
 //     KV head) pair is a unit of ceil(kv_len / 64) key tiles. The units' tiles, laid end
 //     to end, are cut into dec_ctas equal contiguous ranges, one per resident decode CTA;
 //     a unit crossing a cut becomes several items whose partial results are merged by
-//     the last of them to finish. Every CTA thus streams the same number of keys
-//     (within one tile). With a forced split length the units are instead cut every S
-//     keys and the items dealt to the CTAs in contiguous blocks (a test hook);
+//     the last of them to finish. Each unit also counts a fixed cost of a few tiles, so a
+//     CTA with more items streams fewer keys and the CTAs finish together. With a forced
+//     split length the units are instead cut every S keys and the items dealt to the CTAs
+//     in contiguous blocks (a test hook);
 //   - prefill-class sequences: 128-row query tiles, sorted by their number of 128-key KV
 //     tiles, largest first, so the persistent prefill grid takes the long causal tiles
 //     first (longest-processing-time order).
@@ -16,6 +17,8 @@
 // inconsistent (cum not a prefix sum ending at N, a negative past, a sequence longer than
 // its block_table row, a q_len above the host's max_query_len bound) nothing is
 // scheduled and PA_DEVERR_BAD_BATCH is raised.
+// The file also holds the cache write (the K/V scatter, with the Q/K preparation or the
+// integer codes when asked for, and the fp16 V copy of bf16 prefill sequences).
 #include <limits.h>
 
 #include <algorithm>
