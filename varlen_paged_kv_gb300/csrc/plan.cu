@@ -1072,9 +1072,10 @@ cudaError_t launch_plan(const Args& a, cudaStream_t s) {
 }
 
 cudaError_t launch_cache_write(const Args& a, int sms, cudaStream_t s) {
-  // a warp per token (bit copy) or per (token, unit): at most 8 blocks of 8 warps per SM
+  // a warp per token (bit copy) or per (token, unit): one resident wave of 8-warp blocks
+  // (four per SM at 64 registers), each warp looping over its share
   const int64_t warps = (int64_t)a.N * ((a.kvq || a.prep) ? a.nh + a.kvh : 1);
-  const int grid = (int)std::min<int64_t>((warps + 7) / 8, (int64_t)sms * 8);
+  const int grid = (int)std::min<int64_t>((warps + 7) / 8, (int64_t)sms * 4);
   if (a.kvq) return launch_pdl(a.prep ? cache_write_kernel<3> : cache_write_kernel<2>, dim3(grid), dim3(256), 0, s, a);
   if (a.prep) return launch_pdl(cache_write_kernel<1>, dim3(grid), dim3(256), 0, s, a);
   if (a.cw_early)
