@@ -263,12 +263,16 @@ def test_errors_of_a_copy_beside_the_planner_are_kept():
     assert run_gpu(q)["err"] & pa.DEVERR_BAD_SLOT
 
 
-def test_inconsistent_batch_is_refused_without_writes():
-    p = _case("chunked-prefill")
+@pytest.mark.parametrize("name", ["chunked-prefill", "bf16-long-history-chunk"])
+def test_inconsistent_batch_is_refused_without_writes(name):
+    # (fp16: the bit copy beside the planner; bf16 with derived slots: the one that also
+    # makes the fp16 V copy)
+    p = _case(name)
     p.cumulative_sequence_length = p.cumulative_sequence_length.copy()
     p.cumulative_sequence_length[-1] -= 1  # does not end at num_tokens
     d = upload(p)
     before = bits_of(d["key_cache"]).copy()
+    before_v = bits_of(d["value_cache"]).copy()
     ws = make_workspace(p)
     out = torch.full((p.num_tokens, p.num_heads * p.head_size), 7.0, dtype=d["query"].dtype, device="cuda")
     pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
@@ -276,6 +280,7 @@ def test_inconsistent_batch_is_refused_without_writes():
                        num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, output=out, workspace=ws)
     assert pa.read_device_error(ws) & pa.DEVERR_BAD_BATCH
     assert np.array_equal(bits_of(d["key_cache"]), before)
+    assert np.array_equal(bits_of(d["value_cache"]), before_v)
     assert torch.all(out == 7.0)
 
 
