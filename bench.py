@@ -9,8 +9,10 @@ The other workloads (causal prefill 4 x 2048 bf16, the mixed continuous batch, l
 decode with 16-token pages) are measured in the same run under "secondary".
 
 Timing: the step time comes from K whole steps, one call each, between CUDA events on
-the launching stream; the dominant kernel's time from K more steps split into three calls
-around that kernel (the kernel bracketed by its own events); e2e from pipelined steps
+the launching stream; the dominant kernel's time from K more steps of the same program split
+into calls around that kernel (the kernel bracketed by its own events: the self-planned
+decode kernel of decode-only steps, the prefill kernel of prefill steps, the two attention
+kernels that run side by side in a mixed step); e2e from at least 100 pipelined steps
 through the Python API with pinned host buffers (wall clock).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -192,8 +194,10 @@ class Runner:
                      self.ws.numel(), vp(self.stream.cuda_stream))
 
     def call(self, stages):
-        if self.ext is not None:  # whole calls only (pa_paged_attention_ex)
-            assert stages == self.pa.STAGE_ALL
+        if stages == 0:
+            return
+        if self.ext is not None:  # (integer caches: pa_paged_attention_ex, its stages field)
+            self.ext.stages = stages
             a = self.args
             st = self.lib.pa_paged_attention_ex(*a[:13], ctypes.byref(self.ext), *a[13:])
         else:
@@ -204,14 +208,15 @@ class Runner:
     def step(self):
         self.call(self.pa.STAGE_ALL)
 
-    def timed(self, steps, warmup, kernel_stage, clocks=None):
-        """Times `steps` steps; kernel_stage's launches are bracketed by their own events.
-        Returns (seconds per step, seconds per kernel launch, launches per step)."""
+    def timed(self, steps, warmup, kernel_stages, clocks=None):
+        """Times `steps` steps of the whole call's program, each split into three calls: the
+        stages before `kernel_stages`, those stages (bracketed by their own events), the
+        stages after. Returns (seconds per step, seconds per bracketed launch, launches)."""
         torch, pa = self.torch, self.pa
         stages = (pa.STAGE_PLAN, pa.STAGE_CACHE_WRITE, pa.STAGE_PREFILL, pa.STAGE_DECODE)
-        before = [s for s in stages if s < kernel_stage]
-        after = [s for s in stages if s > kernel_stage]
-        mask_before, mask_after = sum(before), sum(after)
+        low = kernel_stages & -kernel_stages
+        mask_before = sum(s for s in stages if s < low)
+        mask_after = sum(s for s in stages if s > kernel_stages)
         for _ in range(warmup):
             self.step()
         torch.cuda.synchronize()
@@ -225,7 +230,7 @@ class Runner:
         for i in range(steps):
             self.call(mask_before)
             ev[i][0].record(self.stream)
-            self.call(kernel_stage)
+            self.call(kernel_stages)
             ev[i][1].record(self.stream)
             self.call(mask_after)
         end.record(self.stream)
@@ -319,11 +324,13 @@ class Runner:
 # DRAM bytes (read + write) of one launch of the dominant kernel, from one ncu capture
 # (profiles/<kernel>_<workload>.md), with a hash of the kernel's sources at capture time:
 # the figure is reported only while the sources are unchanged, else traffic is null.
+# ("decode_kernel_self": the self-planned instantiation that decode-only steps run.)
 NCU_TRAFFIC = {
-    ("decode_kernel", "decode-b64"): (622877440, "5d6f214d12f1b701"),
     ("prefill_kernel", "causal-prefill-4x2048"): (137497088, "7e299115223b5f83"),
 }
-KERNEL_SOURCES = {"decode_kernel": ("decode.cu", "common.cuh"), "prefill_kernel": ("prefill.cu", "common.cuh")}
+KERNEL_SOURCES = {"decode_kernel": ("decode.cu", "common.cuh"), "decode_kernel_self": ("decode.cu", "common.cuh"),
+                  "prefill_kernel": ("prefill.cu", "common.cuh"),
+                  "prefill_kernel+decode_kernel": ("prefill.cu", "decode.cu", "common.cuh")}
 
 
 def source_hash(kernel):
@@ -341,17 +348,17 @@ def ncu_traffic(kernel, name):
     return entry[0]
 
 
-def kernel_roofline(p, kind, seconds_per_launch, pk):
+def kernel_roofline(p, kind, seconds_per_launch, pk, kernel):
     if kind == "hbm":
         units = kv_history_bytes(p)
         achieved = units / seconds_per_launch / 1e9
         return {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": ncu_traffic("decode_kernel", p.name),
+                "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": ncu_traffic(kernel, p.name),
                 "peak_source": f"{pk['source']} hbm_gbs", "algorithmic_bytes_per_launch": units}
     flops = causal_flops(p, prefill_sequences(p))
     achieved = flops / seconds_per_launch / 1e12
     return {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": ncu_traffic("prefill_kernel", p.name),
+            "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": ncu_traffic(kernel, p.name),
             "peak_source": f"{pk['source']} bf16_tflops (burst; fp16 nominal rate equals bf16)",
             "algorithmic_flops_per_launch": flops}
 
@@ -402,21 +409,29 @@ def measure(r, steps, warmup, pk, clocks=None):
     kernel launches in the whole-step timed region)."""
     q = r.p
     sec, per_step = r.whole(steps, warmup, clocks=clocks)
-    if q.kv_quant is not None:
-        # pa_paged_attention_ex runs whole calls only: the step bounds the decode kernel
-        roof = kernel_roofline(q, "hbm", sec, pk)
-        roof["kernel"] = "whole step (plan, cache write, decode_kernel on %s codes)" % q.kv_quant
-        roof["ms_per_launch"] = round(sec * 1e3, 4)
-        return sec, roof, per_step * steps
-    if prefill_sequences(q):
-        _, kt, _ = r.timed(steps, warmup, r.pa.STAGE_PREFILL)
-        roof = kernel_roofline(q, "tensor", kt, pk)
+    pa = r.pa
+    if prefill_sequences(q) and decode_sequences(q):
+        # a mixed step runs its two attention kernels side by side on split SMs: time the pair
+        _, kt, _ = r.timed(steps, warmup, pa.STAGE_PREFILL | pa.STAGE_DECODE)
+        roof = kernel_roofline(q, "tensor", kt, pk, "prefill_kernel+decode_kernel")
+        roof["kernel"] = ("prefill_kernel (tcgen05/TMEM, TMA) beside decode_kernel (split-KV) on split SMs; "
+                          "achieved = the prefill rows' causal FLOPs / the pair's time")
+    elif prefill_sequences(q):
+        _, kt, _ = r.timed(steps, warmup, pa.STAGE_PREFILL)
+        roof = kernel_roofline(q, "tensor", kt, pk, "prefill_kernel")
         roof["kernel"] = "prefill_kernel (tcgen05/TMEM, TMA)"
     else:
-        _, kt, _ = r.timed(steps, warmup, r.pa.STAGE_DECODE)
-        roof = kernel_roofline(q, "hbm", kt, pk)
-        roof["kernel"] = "decode_kernel (split-KV, TMA + mma.sync)"
+        # decode-only with the host bound: the self-planned decode kernel the whole step runs
+        _, kt, _ = r.timed(steps, warmup, pa.STAGE_DECODE)
+        roof = kernel_roofline(q, "hbm", kt, pk, "decode_kernel_self")
+        roof["kernel"] = ("decode_kernel (self-planned, split-KV, TMA + mma.sync%s)"
+                          % ("" if q.kv_quant is None else ", on %s codes" % q.kv_quant))
     roof["ms_per_launch"] = round(kt * 1e3, 4)
+    # The bracketing events serialise the bracketed launches with the rest of the stream; in
+    # back-to-back steps a kernel's prologue overlaps its predecessor (programmatic dependent
+    # launch), so a launch can take longer than the step period. The rate over the whole step:
+    units = roof.get("algorithmic_bytes_per_launch") or roof.get("algorithmic_flops_per_launch")
+    roof["achieved_over_step"] = round(units / sec / (1e9 if roof["bound"] == "hbm" else 1e12), 1)
     return sec, roof, per_step * steps
 
 
@@ -461,7 +476,7 @@ def run_cuda(args):
     value, unit = headline(p, sec)
     sec_max, value_all = reduce_over_ranks(sec, value * sec)   # units of work summed over ranks
     value = value_all / sec_max
-    e2e_sec, h2d, d2h = r.e2e(max(args.steps // 4, 10), args.warmup)
+    e2e_sec, h2d, d2h = r.e2e(max(args.steps // 4, 100), args.warmup)
     e2e_max, e2e_units = reduce_over_ranks(e2e_sec, headline(p, e2e_sec)[0] * e2e_sec)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": unit, "n_gpus": world, "steps": args.steps,

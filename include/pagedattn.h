@@ -13,8 +13,9 @@
  *     T (pa_dtype); index tensors are int32. Every T pointer must be 16-byte aligned,
  *     every int32 pointer 4-byte aligned.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is enqueued
- *     asynchronously; apart from pa_read_device_error no call synchronises, reads device
- *     memory back, or allocates, so a call can be captured in a CUDA graph.
+ *     asynchronously; apart from pa_read_device_error and
+ *     pa_static_workspace_read_device_error no call synchronises, reads device memory
+ *     back, or allocates, so a call can be captured in a CUDA graph.
  *   - Argument errors are found on the host before anything is launched and reported as
  *     PA_ERR_* codes. Inconsistencies that only device data can reveal (a
  *     cumulative_sequence_length that is not a prefix sum, an out-of-range block or
@@ -32,7 +33,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 6
+#define PA_ABI_VERSION 7
 
 typedef enum pa_status {
   PA_OK = 0,
@@ -209,10 +210,15 @@ pa_status pa_paged_attention(const void* query, const void* key, const void* val
  *   - Allocates nothing and calls no allocating routine. The first call on each device
  *     looks up the built-in array's device address (cudaGetSymbolAddress) and caches it;
  *     make that first call before any stream capture.
- *   - All calls on a device share the one array and it keeps the last call's contents;
- *     each call's plan stage rewrites everything later stages read, so nothing needs
- *     clearing. Calls whose GPU work overlaps race on the array: order them (one stream,
- *     or synchronise between them).
+ *   - All calls on a device share the one array and it keeps the last call's contents.
+ *     Each call's first kernel (the planner, or the one-CTA reset of a decode-only call
+ *     whose decode kernel plans itself) rewrites the header, the device error word and
+ *     the merge counters, and the call writes every other field before it reads it, so
+ *     nothing needs clearing. Calls whose GPU work overlaps race on the array: order them
+ *     (one stream, or synchronise between them).
+ *   - Problems only device data reveals (a block or slot out of range, an inconsistent
+ *     batch) set bits of the array's device error word, as with a caller workspace; read
+ *     them with pa_static_workspace_read_device_error.
  */
 pa_status pa_paged_attention_static_workspace(const void* query, const void* key, const void* value,
                                               void* key_cache, void* value_cache,
@@ -221,6 +227,14 @@ pa_status pa_paged_attention_static_workspace(const void* query, const void* key
                                               const int32_t* slot_mapping, int32_t num_heads,
                                               int32_t kv_num_heads, float scale, void* output,
                                               const pa_dims* dims, void* stream);
+
+/*
+ * pa_read_device_error for the built-in workspace of pa_paged_attention_static_workspace:
+ * waits for `stream`, copies the device error word (PA_DEVERR_* bits of the most recent
+ * call on the current device) into *error_bits, then clears it. Synchronises; allocates
+ * nothing. Like that entry point it has no counterpart on the pages.
+ */
+pa_status pa_static_workspace_read_device_error(void* stream, uint32_t* error_bits);
 
 /* Stages of pa_paged_attention, in the order they must run. */
 #define PA_STAGE_PLAN 1u        /* device work partitioner: classify sequences, build work lists */
@@ -233,10 +247,16 @@ pa_status pa_paged_attention_static_workspace(const void* query, const void* key
 
 /*
  * Same arguments as pa_paged_attention; runs only the stages in `stages` (PA_STAGE_*
- * bits), in the order above. A stage reads what earlier stages left in the workspace,
- * so a caller that splits a call across several pa_paged_attention_stages calls must
- * pass the same arguments and workspace to each and keep them in stage order. Used to
- * time or test one kernel at a time. Otherwise identical to pa_paged_attention.
+ * bits), in the order above. The kernels are those the whole call would run (the same
+ * program: the same work partition, the same SM split of a mixed batch), and `stages`
+ * picks which of them this call launches. For a decode-only call that the decode kernel
+ * plans itself (see pa_dims.max_query_len) PA_STAGE_PLAN is the reset of the workspace's
+ * counters and PA_STAGE_PREFILL is empty; PA_STAGE_CACHE_WRITE is empty too when the
+ * decode kernel writes this call's rows. The two attention kernels of a mixed batch run
+ * side by side only when one call launches both. A stage reads what earlier stages left
+ * in the workspace, so a caller that splits a call across several calls must pass the
+ * same arguments and workspace to each and keep them in stage order. Used to time one
+ * kernel of a step with events around it. Otherwise identical to pa_paged_attention.
  */
 pa_status pa_paged_attention_stages(const void* query, const void* key, const void* value,
                                     void* key_cache, void* value_cache,
@@ -279,6 +299,7 @@ typedef struct pa_extensions {
   const float* k_scale;       /* fp32 (kv_num_heads, head_size), 16-byte aligned: the K scales of integer
                                  caches (dims->kv_dtype != PA_KV_SAME), finite and positive; NULL otherwise */
   const float* v_scale;       /* the same for V */
+  uint32_t stages;            /* 0: the whole call; else PA_STAGE_* bits, as pa_paged_attention_stages */
 } pa_extensions;
 
 /* pa_paged_attention with the extensions in `ext` (NULL: none). */
@@ -304,6 +325,18 @@ const char* pa_last_error(void);
  * *error_bits, then clears it. This is the only entry point that synchronises.
  */
 pa_status pa_read_device_error(void* workspace, void* stream, uint32_t* error_bits);
+
+/*
+ * Test hook of the coverage build (libpagedattn_cov.so, compiled with PA_COVERAGE; the
+ * product library returns PA_ERR_UNSUPPORTED). From the next call on, every (query row i,
+ * head h, key t) that an attention kernel lets into its softmax adds one to the device int32
+ * counts[(i * num_heads + h) * max_keys + t]; keys t >= max_keys add to the overflow counter
+ * counts[num_tokens * num_heads * max_keys]. The caller zeroes the array. A correct work
+ * partition counts every key 0 .. past_seqlens[b] + j of row j of sequence b exactly once
+ * and nothing else. NULL switches counting off. No page describes a partitioner; this is
+ * how the partition is checked (every (row, head, key) covered once).
+ */
+pa_status pa_debug_coverage(int32_t* counts, int32_t max_keys);
 
 /* Number of kernels this library has launched in this process (monotonic). */
 uint64_t pa_kernel_launch_count(void);

@@ -50,24 +50,24 @@ def cache_bytes(t: torch.Tensor) -> np.ndarray:
     return t.cpu().numpy() if t.dtype == torch.uint8 else bits_of(t)
 
 
-def run_gpu(p, *, decode_split_keys=0, route=pa.ROUTE_AUTO, dev=None, decode_sms=0):
+def run_gpu(p, *, decode_split_keys=0, route=pa.ROUTE_AUTO, dev=None, decode_sms=0, max_query_len=0):
     """Runs the operator once. Returns dict(out_bits (N, nh*hs), key_cache, value_cache (bits),
     err (device error bits), dev (the uploaded tensors, caches updated in place))."""
     d = dev if dev is not None else upload(p)
-    ws = make_workspace(p, decode_split_keys, route)
+    ws = make_workspace(p, decode_split_keys, route, max_query_len)
     out = pa.paged_attention(
         d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"], d["cumulative_sequence_length"],
         d["past_seqlens"], d["block_table"], d["slot_mapping"], num_heads=p.num_heads,
         kv_num_heads=p.kv_num_heads, scale=p.scale, decode_split_keys=decode_split_keys, route=route,
-        workspace=ws, decode_sms=decode_sms)
+        workspace=ws, decode_sms=decode_sms, max_query_len=max_query_len)
     err = pa.read_device_error(ws)
     return dict(out_bits=bits_of(out), key_cache=bits_of(d["key_cache"]), value_cache=bits_of(d["value_cache"]),
                 err=err, dev=d)
 
 
-def make_workspace(p, decode_split_keys=0, route=pa.ROUTE_AUTO):
+def make_workspace(p, decode_split_keys=0, route=pa.ROUTE_AUTO, max_query_len=0):
     dims = pa.make_dims(p.num_tokens, p.batch_size, p.head_size, p.num_blocks, p.block_size,
-                        p.max_blocks_per_sequence, TORCH_DT[p.dtype], decode_split_keys, route)
+                        p.max_blocks_per_sequence, TORCH_DT[p.dtype], decode_split_keys, route, max_query_len)
     n = pa.workspace_size(dims, p.num_heads, p.kv_num_heads)
     assert n > 0
     return torch.zeros(n, dtype=torch.uint8, device="cuda")

@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.pa_abi_version() == 6
+    assert lib.pa_abi_version() == 7
     for code in range(5):
         assert lib.pa_status_string(code)
     assert lib.pa_status_string(99) == b"unknown status"

@@ -175,3 +175,13 @@ def test_refused_self_planned_batch_writes_nothing(fmt):
     assert np.array_equal(cache_bytes(d["key_cache"]), before[0])
     assert np.array_equal(cache_bytes(d["value_cache"]), before[1])
     assert torch.all(out == 7.0)
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int4"])
+def test_full_size_decode_batch_on_integer_caches(fmt):
+    # the 64-sequence decode batch as bench.py times it: every code byte and every output
+    # element against the oracle
+    p = w.config_kv_quant(2, fmt)
+    ref = oracle.paged_attention(p)
+    d, out, lse = _run(p)
+    _check(p, ref, d, out, lse)

@@ -56,7 +56,7 @@ class PaQkPrep(ctypes.Structure):
 
 class PaExtensions(ctypes.Structure):
     _fields_ = [("lse", ctypes.c_void_p), ("qk_prep", ctypes.POINTER(PaQkPrep)), ("output_gate", ctypes.c_void_p),
-                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p), ("stages", ctypes.c_uint32)]
 
 
 def load_library():
@@ -144,14 +144,16 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
     ``max_query_len`` (optional) is a host-side bound on every sequence's new-token count;
     it lets decode-only batches skip the prefill launch and is checked on the device.
     ``lse`` (optional, float32 (num_tokens, num_heads)) receives each output row's natural-log
-    log-sum-exp of the scaled scores (whole calls only).
-    ``qk_prep`` (optional, whole calls only): dict(q_norm_weight=tensor (head_size,) of the
+    log-sum-exp of the scaled scores.
+    ``stages`` (PA_STAGE_* bits) launches only those kernels of the call's program, as
+    pa_paged_attention_stages does.
+    ``qk_prep`` (optional): dict(q_norm_weight=tensor (head_size,) of the
     query dtype or None, k_norm_weight=... or None, eps=float, rotary_dim=int, theta=float):
     RMSNorm of the query and key heads, then the rotary embedding at each row's position,
     before the cache write (pa_qk_prep).
-    ``output_gate`` (optional, whole calls only, shape and dtype of the output): the output is
+    ``output_gate`` (optional, shape and dtype of the output): the output is
     multiplied by sigmoid(output_gate) elementwise before the final rounding.
-    ``kv_quant`` (optional, whole calls only): "int8" or "int4" integer caches (uint8 tensors
+    ``kv_quant`` (optional): "int8" or "int4" integer caches (uint8 tensors
     (num_blocks, block_size, kv_num_heads, head_size), or head_size / 2 for int4) with the
     float32 (kv_num_heads, head_size) per-channel scales ``k_scale`` and ``v_scale``: this
     call's K and V rows are stored as codes, attention reads code * scale."""
@@ -169,8 +171,6 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
             raise TypeError(f"{name} must be {cache_dtype}")
     head_size = key_cache.shape[3] * (2 if kv_quant == "int4" else 1)
     if kv_quant is not None:
-        if stages != STAGE_ALL:
-            raise ValueError("integer caches apply to whole calls only")
         for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
             if t is None or t.dtype != torch.float32 or tuple(t.shape) != (kv_num_heads, head_size):
                 raise ValueError(f"{name} must be float32 (kv_num_heads, head_size)")
@@ -183,17 +183,11 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
     if lse is not None:
         if lse.dtype != torch.float32 or tuple(lse.shape) != (query.shape[0], num_heads):
             raise ValueError("lse must be float32 (num_tokens, num_heads)")
-        if stages != STAGE_ALL:
-            raise ValueError("lse is exported by whole calls only")
     if output_gate is not None:
         if output_gate.dtype != query.dtype or output_gate.numel() != query.shape[0] * num_heads * head_size:
             raise ValueError("output_gate must have the output's shape and dtype")
-        if stages != STAGE_ALL:
-            raise ValueError("output_gate applies to whole calls only")
     prep = None
     if qk_prep is not None:
-        if stages != STAGE_ALL:
-            raise ValueError("qk_prep applies to whole calls only")
         for k in ("q_norm_weight", "k_norm_weight"):
             t = qk_prep.get(k)
             if t is not None and (t.dtype != query.dtype or t.numel() != head_size or not t.is_cuda or
@@ -228,12 +222,13 @@ def paged_attention(query: torch.Tensor, key: Optional[torch.Tensor], value: Opt
         ws = lib.pa_workspace_size(ctypes.byref(dims), num_heads, kv_num_heads)
         workspace = torch.empty(max(int(ws), 256), dtype=torch.uint8, device=query.device)
     s = (stream or torch.cuda.current_stream(query.device)).cuda_stream
-    if prep is not None or output_gate is not None or kv_quant is not None:
+    if (prep is not None or output_gate is not None or kv_quant is not None or
+            (lse is not None and stages != STAGE_ALL)):
         ext = PaExtensions(None if lse is None else lse.data_ptr(),
                            ctypes.pointer(prep) if prep is not None else None,
                            None if output_gate is None else output_gate.data_ptr(),
                            None if k_scale is None else k_scale.data_ptr(),
-                           None if v_scale is None else v_scale.data_ptr())
+                           None if v_scale is None else v_scale.data_ptr(), int(stages))
         st = lib.pa_paged_attention_ex(
             _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
             _ptr(cumulative_sequence_length), _ptr(past_seqlens), _ptr(block_table), _ptr(slot_mapping),

@@ -39,22 +39,30 @@ def _deps():
     return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+# the coverage-counting debug library (pa_debug_coverage), built on demand by its test
+COV_LIB = os.path.join(HERE, "libpagedattn_cov.so")
+
+
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and not ptxas_info and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, coverage: bool = False) -> str:
+    lib = COV_LIB if coverage else LIB
+    if not force and not ptxas_info and up_to_date(lib):
+        return lib
+    build_dir = os.path.join(BUILD, "cov") if coverage else BUILD
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if coverage:
+        extra = extra + ["-DPA_COVERAGE=1"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -68,12 +76,12 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             if log.strip():
                 print(log)
     objs = [o for o, _ in results]
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

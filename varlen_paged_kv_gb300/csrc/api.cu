@@ -12,6 +12,9 @@
 namespace {
 
 std::atomic<uint64_t> g_launches{0};
+// coverage counters of the PA_COVERAGE debug library (pa_debug_coverage)
+std::atomic<int32_t*> g_cov{nullptr};
+std::atomic<int32_t> g_cov_keys{0};
 thread_local const char* g_last_error = "no error";
 
 // record a failing CUDA call's message (per host thread) and map it to PA_ERR_CUDA
@@ -173,29 +176,35 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
   if (!device_info(&info)) return cuda_fail(cudaGetLastError(), "device query");
   args.dec_ctas = std::min(pa::dec_ctas_per_sm(args.hs) * info.sms, pa::kMaxDecCtas);
   args.sms = info.sms;
-  // a whole call may run its prefill and decode kernels side by side on split SMs; a call of
-  // some stages only runs each kernel on the whole GPU
-  args.split_sms = stages == PA_STAGE_ALL;
+  // The program of a call (which kernels, on which SMs) follows from its arguments alone;
+  // `stages` only picks which of its kernels this call launches. A call with prefill-class
+  // and decode-class rows may run its two attention kernels side by side on split SMs (the
+  // planner decides); they run side by side when one call launches both.
+  args.split_sms = 1;
   const pa_dtype dt = (pa_dtype)d->dtype;
   const bool bf16 = dt == PA_BFLOAT16;
   const int hs = args.hs;
   const int64_t slots = (int64_t)d->num_blocks * d->block_size;
 
-  // A whole decode-only call (proven by the host bound) with derived slots and a small batch
+  // A decode-only call (proven by the host bound) with derived slots and a small batch
   // needs no planner and no cache-write kernel: a one-CTA reset, then the decode kernel plans
   // its own share and writes the new rows of the tiles it loads.
   // (With the Q/K preparation or integer caches the cache-write kernel still runs: it writes
   // the prepared or scaled query rows and the rows' codes, checking the batch itself.)
-  const bool self_plan = stages == PA_STAGE_ALL && d->route == PA_ROUTE_AUTO && d->max_query_len > 0 &&
+  // Its stages: PA_STAGE_PLAN is that reset, PA_STAGE_CACHE_WRITE is empty when the decode
+  // kernel writes the rows, PA_STAGE_DECODE is the self-planned decode kernel.
+  const bool self_plan = d->route == PA_ROUTE_AUTO && d->max_query_len > 0 &&
                          (int64_t)d->max_query_len * args.G <= pa::kDecRows && args.slot_mapping == nullptr &&
                          args.forced_split <= 0 && args.B >= 1 && args.B <= pa::kSelfMaxB && hs <= 128 && args.N > 0 &&
                          slots > 0;
   const bool self_write_rows = self_plan && !args.prep && !args.kvq;
-  if (self_plan) stages = self_write_rows ? PA_STAGE_DECODE : PA_STAGE_CACHE_WRITE | PA_STAGE_DECODE;
   args.self_plan = self_plan;  // (the cache-write kernel checks the batch itself)
   if (self_plan) {
-    ++g_launches;
-    if (cudaError_t e = pa::launch_decode_prep(args, stream)) return cuda_fail(e, "decode_prep_kernel launch");
+    if (stages & PA_STAGE_PLAN) {
+      ++g_launches;
+      if (cudaError_t e = pa::launch_decode_prep(args, stream)) return cuda_fail(e, "decode_prep_kernel launch");
+    }
+    stages &= self_write_rows ? PA_STAGE_DECODE : PA_STAGE_CACHE_WRITE | PA_STAGE_DECODE;
   }
   if (stages & PA_STAGE_PLAN) {
     ++g_launches;
@@ -402,6 +411,8 @@ pa_status run(const void* query, const void* key, const void* value, void* key_c
   }
   a.max_items = L.max_items;
   a.max_tiles = L.max_tiles;
+  a.cov = g_cov.load();
+  a.cov_keys = g_cov_keys.load();
 
   return launch_all(a, dims, query, key_cache, value_cache, stages, static_cast<cudaStream_t>(stream));
 }
@@ -451,7 +462,8 @@ pa_status pa_paged_attention_ex(const void* query, const void* key, const void* 
   return run(query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens, block_table,
              slot_mapping, num_heads, kv_num_heads, scale, output, ext ? ext->lse : nullptr,
              ext ? ext->qk_prep : nullptr, ext ? ext->output_gate : nullptr, ext ? ext->k_scale : nullptr,
-             ext ? ext->v_scale : nullptr, dims, workspace, workspace_bytes, stream, PA_STAGE_ALL);
+             ext ? ext->v_scale : nullptr, dims, workspace, workspace_bytes, stream,
+             ext && ext->stages ? ext->stages : PA_STAGE_ALL);
 }
 
 const char* pa_last_error(void) { return g_last_error; }
@@ -479,6 +491,19 @@ pa_status pa_read_device_error(void* workspace, void* stream, uint32_t* error_bi
 }
 
 uint64_t pa_kernel_launch_count(void) { return g_launches.load(); }
+
+pa_status pa_debug_coverage(int32_t* counts, int32_t max_keys) {
+#ifdef PA_COVERAGE
+  if (counts && max_keys <= 0) return PA_ERR_INVALID_ARGUMENT;
+  g_cov_keys = counts ? max_keys : 0;
+  g_cov = counts;
+  return PA_OK;
+#else
+  (void)counts;
+  (void)max_keys;
+  return PA_ERR_UNSUPPORTED;
+#endif
+}
 
 int32_t pa_abi_version(void) { return PA_ABI_VERSION; }
 

@@ -200,7 +200,24 @@ struct Args {
   uint16_t* mirror;       // fp16 copy of the V history of the prefill-class sequences (bf16)
   int32_t mirror_keys;    // rows the copy holds (0: no copy)
   int32_t max_items, max_tiles;
+  // coverage counters (a library built with PA_COVERAGE; null otherwise): see cov_count
+  int32_t* cov;
+  int32_t cov_keys;
 };
+
+// Coverage counting, compiled only into the debug library built with PA_COVERAGE: every
+// (query row, head, key) that an attention kernel lets into its softmax adds one to
+// cov[(row * nh + head) * cov_keys + key] (keys from cov_keys on to the overflow counter
+// cov[N * nh * cov_keys]), so that a test can check that the work partition and the
+// kernels' loop bounds and masks take every key of every row's causal range exactly once.
+#ifdef PA_COVERAGE
+__device__ __forceinline__ void cov_count(const Args& a, int64_t row, int h, int key) {
+  if (!a.cov) return;
+  const int64_t i = key < a.cov_keys ? (row * a.nh + h) * (int64_t)a.cov_keys + key
+                                     : (int64_t)a.N * a.nh * a.cov_keys;
+  atomicAdd(a.cov + i, 1);
+}
+#endif
 
 // ---- shared-memory layouts (bytes) of the attention kernels --------------------------
 // Decode: a ring of K+V tiles, the warp-combine buffer, per-warp (m, l), barriers.

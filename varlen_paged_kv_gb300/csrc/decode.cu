@@ -660,6 +660,16 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
             x[n][e] = v;
           }
         }
+#ifdef PA_COVERAGE
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int key = kw + n * 8 + tq * 2 + (e & 1), r = e < 2 ? r0 : r1;
+            const bool in = !(ragged && (key >= item.key_end || key > (e < 2 ? lim0 : lim1)));
+            if (in && r < n_rows) cov_count(a, c0 + r / a.G, item.g * a.G + r % a.G, key);
+          }
+#endif
         float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
         float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));

@@ -347,6 +347,11 @@ __global__ void __launch_bounds__(kPreThreads, 1)
             for (int e = 0; e < COLS; ++e)
               if (key0 + e > lim) r[e] = __float_as_uint(sentinel);
           }
+#ifdef PA_COVERAGE
+          if (tile.j0 + row < q_len)
+            for (int e = 0; e < COLS; ++e)
+              if (!(masked && key0 + e > lim)) cov_count(a, c0 + tile.j0 + row, h, key0 + e);
+#endif
           // ---- the row's max of s * c, on raw s (max, or min for c < 0), four chains ----
           float mc[4] = {sentinel, sentinel, sentinel, sentinel};
           if (c > 0.f) {

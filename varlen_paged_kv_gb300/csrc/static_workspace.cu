@@ -10,11 +10,16 @@
 // The array's host-side name is only a stand-in for the symbol, never a device address,
 // so the device address is looked up with cudaGetSymbolAddress once per device (with that
 // device current) and cached; the first call on each device does this lookup. Every call
-// on a device shares the same array and leaves its contents behind; the plan stage
-// rewrites every workspace field the later stages read (including the error word and the
-// merge counters), so nothing has to be cleared between calls. Calls whose GPU work
-// overlaps (different streams, or different host threads without ordering) race on the
-// array and must be serialised by the caller.
+// on a device shares the same array and leaves its contents behind. Each call's first
+// kernel - the planner, or, for a decode-only call whose decode kernel plans itself, the
+// one-CTA reset before it - rewrites the header, the error word and the merge counters,
+// and every other field a later kernel reads is written earlier in the same call, so
+// nothing has to be cleared between calls. Calls whose GPU work overlaps (different
+// streams, or different host threads without ordering) race on the array and must be
+// serialised by the caller.
+//
+// pa_static_workspace_read_device_error gives these callers the device error word that
+// pa_read_device_error gives callers with their own workspace.
 #include <mutex>
 
 #include "common.cuh"
@@ -61,4 +66,11 @@ extern "C" pa_status pa_paged_attention_static_workspace(
   return pa_paged_attention(query, key, value, key_cache, value_cache, cumulative_sequence_length, past_seqlens,
                             block_table, slot_mapping, num_heads, kv_num_heads, scale, output, dims, ws,
                             (size_t)PA_STATIC_WORKSPACE_BYTES, stream);
+}
+
+extern "C" pa_status pa_static_workspace_read_device_error(void* stream, uint32_t* error_bits) {
+  if (!error_bits) return PA_ERR_INVALID_ARGUMENT;
+  void* ws = nullptr;
+  if (pa_status st = static_workspace_address(&ws)) return st;
+  return pa_read_device_error(ws, stream, error_bits);  // (the word is the array's first field)
 }
