@@ -134,3 +134,11 @@ def test_integer_cache_decode_partition(lib, fmt):
               past=[5000, 3, 800, 0], q_lens=[1, 2, 4, 1], kv_quant=fmt)
     check_exactly_once(lib, p, max_q=4)
     check_exactly_once(lib, p, max_q=4, split=64)
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int4"])
+def test_integer_cache_prefill_units(lib, fmt):
+    p = _prob("cov-int-prefill", dtype="bf16", num_heads=16, kv_num_heads=4, head_size=128, block_size=32,
+              past=[0, 700, 5], q_lens=[200, 1, 130], kv_quant=fmt)
+    check_exactly_once(lib, p, max_q=200)
+    check_exactly_once(lib, p, max_q=200, route=pa.ROUTE_ALL_PREFILL)

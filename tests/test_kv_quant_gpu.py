@@ -1,5 +1,8 @@
-"""INT8 / INT4 per-channel KV caches on the decode kernel, through the C ABI against the
-oracle (oracle_quantize_rows, oracle_attention_q; pinned in test_oracle_quant_pins.py).
+"""INT8 / INT4 per-channel KV caches on both attention kernels, through the C ABI against
+the oracle (oracle_quantize_rows, oracle_attention_q; pinned in test_oracle_quant_pins.py):
+decode-only batches on the decode kernel, and chunked-prefill and mixed batches whose
+prefill-class rows run on the tcgen05 prefill kernel (code tiles turned into fp16 in shared
+memory).
 
 The cache write quantizes this call's K and V rows with the same rule as the oracle (IEEE
 fp32 quotient, rint half to even, clamp), so the code caches must match bit for bit. The
@@ -50,18 +53,19 @@ def _problem(name, seed=31):
                           slot_mode="explicit" if drops else "omitted", drop_count=drops, kv_quant=fmt)
 
 
-def _run(p, split=0, **kw):
+def _run(p, split=0, route=pa.ROUTE_AUTO, decode_sms=0, **kw):
     d = upload(p)
     lse = torch.empty((p.num_tokens, p.num_heads), dtype=torch.float32, device="cuda")
     dims = pa.make_dims(p.num_tokens, p.batch_size, p.head_size, p.num_blocks, p.block_size,
-                        p.max_blocks_per_sequence, TORCH_DT[p.dtype], split, pa.ROUTE_AUTO, int(p.q_lens.max()),
-                        "qk_prep" in kw, p.kv_quant)
+                        p.max_blocks_per_sequence, TORCH_DT[p.dtype], split, route, int(p.q_lens.max()),
+                        "qk_prep" in kw, p.kv_quant, decode_sms)
     ws = torch.zeros(pa.workspace_size(dims, p.num_heads, p.kv_num_heads), dtype=torch.uint8, device="cuda")
     out = pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
                              d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], d["slot_mapping"],
                              num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, scale=p.scale, workspace=ws,
-                             decode_split_keys=split, max_query_len=int(p.q_lens.max()), lse=lse,
-                             kv_quant=p.kv_quant, k_scale=d["k_scale"], v_scale=d["v_scale"], **kw)
+                             decode_split_keys=split, max_query_len=int(p.q_lens.max()), lse=lse, route=route,
+                             decode_sms=decode_sms, kv_quant=p.kv_quant, k_scale=d["k_scale"], v_scale=d["v_scale"],
+                             **kw)
     assert pa.read_device_error(ws) == 0
     return d, out, lse
 
@@ -141,8 +145,62 @@ def test_integer_cache_with_prep_and_gate(fmt):
     assert np.all(np.abs(a - b) <= 1) and np.mean(a != b) < 0.01
 
 
-def test_integer_cache_needs_a_decode_bound():
-    p = _problem("int8-gqa4-fp16")
+# prefill-class rows on integer caches: (fmt, dtype, nh, kvh, hs, bs, past, q_lens, packed, drops)
+PREFILL_CASES = {
+    "int8-chunked-fp16": ("int8", "fp16", 32, 8, 128, 256, [1000, 17, 255], [200, 64, 513], False, 0),
+    "int8-mixed-packed-drops-bf16": ("int8", "bf16", 32, 8, 128, 64, [0, 900, 50, 3000], [130, 1, 40, 2], True, 9),
+    "int8-hs64-pages16": ("int8", "fp16", 8, 2, 64, 16, [0, 5, 100], [70, 3, 300], False, 0),
+    "int8-odd-group-bf16": ("int8", "bf16", 6, 2, 128, 32, [40, 0], [150, 129], False, 0),
+    "int4-chunked-bf16": ("int4", "bf16", 16, 4, 128, 32, [0, 300, 2000], [300, 129, 17], False, 0),
+    "int4-mixed-packed-drops-fp16": ("int4", "fp16", 32, 8, 128, 16, [60, 4, 2000, 0], [2, 40, 1, 129], True, 5),
+    "int4-one-kv-head": ("int4", "fp16", 16, 1, 128, 64, [500, 0], [100, 20], False, 0),
+    "int8-one-kv-head-hs64": ("int8", "bf16", 4, 1, 64, 16, [33, 0], [40, 200], False, 0),
+}
+
+
+def _prefill_problem(name, seed=37):
+    fmt, dt, nh, kvh, hs, bs, past, q, packed, drops = PREFILL_CASES[name]
+    return w.make_problem(name=name, seed=seed, dtype=dt, num_heads=nh, kv_num_heads=kvh, head_size=hs,
+                          block_size=bs, past=past, q_lens=q, packed=packed,
+                          slot_mode="explicit" if drops else "omitted", drop_count=drops, kv_quant=fmt)
+
+
+@pytest.mark.parametrize("route", [pa.ROUTE_AUTO, pa.ROUTE_ALL_PREFILL])
+@pytest.mark.parametrize("name", sorted(PREFILL_CASES))
+def test_integer_cache_prefill_rows(name, route):
+    p = _prefill_problem(name)
+    ref = oracle.paged_attention(p)
+    d, out, lse = _run(p, route=route)
+    _check(p, ref, d, out, lse)
+
+
+@pytest.mark.parametrize("dsm", [1, 76])
+def test_integer_cache_mixed_batch_on_split_sms(dsm):
+    p = _prefill_problem("int8-mixed-packed-drops-bf16")
+    ref = oracle.paged_attention(p)
+    d, out, lse = _run(p, decode_sms=dsm, split=64)
+    _check(p, ref, d, out, lse)
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int4"])
+def test_integer_cache_prefill_with_prep_and_gate(fmt):
+    p = w.make_problem(name="q-prep-prefill", seed=38, dtype="fp16", num_heads=16, kv_num_heads=4, head_size=128,
+                       block_size=32, past=[0, 700, 5], q_lens=[200, 1, 130], kv_quant=fmt)
+    to_t = oracle.double_to_f16
+    prep_bits = dict(q_norm_weight=to_t(np.linspace(0.5, 1.5, 128)), k_norm_weight=to_t(np.linspace(1.2, 0.8, 128)),
+                     eps=1e-6, rotary_dim=128, theta=1.0e4)
+    gate_bits = to_t(w.uniform(39, 1, p.num_tokens * 16 * 128) * 8.0 - 4.0).reshape(p.num_tokens, 16 * 128)
+    ref = oracle.paged_attention(p, prep=prep_bits, gate=gate_bits)
+    dev = lambda b: torch.from_numpy(b.view(np.int16)).cuda().view(torch.float16)
+    prep = dict(q_norm_weight=dev(prep_bits["q_norm_weight"]), k_norm_weight=dev(prep_bits["k_norm_weight"]),
+                eps=1e-6, rotary_dim=128, theta=1.0e4)
+    d, out, lse = _run(p, qk_prep=prep, output_gate=dev(gate_bits))
+    _check(p, ref, d, out, lse, exact_codes=False, prepared=oracle.apply_qk_prep(p, prep_bits))
+
+
+def test_integer_cache_256_wide_heads_need_a_decode_bound():
+    # 256-wide heads on integer caches run on the decode kernel only
+    p = _problem("int8-hs256-bf16")
     d = upload(p)
     with pytest.raises(pa.PagedAttentionError) as e:
         pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],

@@ -113,9 +113,10 @@ pa_status check_dims(const pa_dims* d, int32_t nh, int32_t kvh) {
   if (d->head_size != 64 && d->head_size != 128 && d->head_size != 256) return PA_ERR_UNSUPPORTED;
   if (d->kv_dtype != PA_KV_SAME && d->kv_dtype != PA_KV_INT8 && d->kv_dtype != PA_KV_INT4) return PA_ERR_UNSUPPORTED;
   if (d->kv_dtype == PA_KV_INT4 && d->head_size == 64) return PA_ERR_UNSUPPORTED;
-  // integer caches run on the decode kernel: the call must prove every sequence decode-class
-  if (d->kv_dtype != PA_KV_SAME && (d->route != PA_ROUTE_AUTO || d->max_query_len <= 0 ||
-                                    (int64_t)d->max_query_len * (nh / kvh) > pa::kDecRows))
+  // integer caches at head_size 256 run on the decode kernel only: the call must prove every
+  // sequence decode-class
+  if (d->kv_dtype != PA_KV_SAME && d->head_size == 256 &&
+      (d->route != PA_ROUTE_AUTO || d->max_query_len <= 0 || (int64_t)d->max_query_len * (nh / kvh) > pa::kDecRows))
     return PA_ERR_UNSUPPORTED;
   if (d->block_size % 16 != 0) return PA_ERR_UNSUPPORTED;
   if (d->route != PA_ROUTE_AUTO && d->route != PA_ROUTE_ALL_PREFILL) return PA_ERR_INVALID_ARGUMENT;
@@ -139,7 +140,7 @@ bool prefill_possible(const pa_dims* d, int32_t G) {
 // represent, takes the two-product path on the bf16 cache instead (same results within
 // rounding, slower).
 int64_t mirror_keys(const pa_dims* d, int32_t nh, int32_t kvh) {
-  if (d->dtype != PA_BFLOAT16 || !prefill_possible(d, nh / kvh)) return 0;
+  if (d->dtype != PA_BFLOAT16 || d->kv_dtype != PA_KV_SAME || !prefill_possible(d, nh / kvh)) return 0;
   return std::min<int64_t>(4 * (int64_t)d->num_tokens, (int64_t)d->num_blocks * d->block_size);
 }
 
@@ -167,6 +168,21 @@ bool code_cache_map(CUtensorMap* m, void* base, int row_bytes, int kvh, int64_t 
              // a box row is one head's code row: fetch what it covers (the next head's row
              // at the next 128 or 64 bytes belongs to another CTA's tile)
              box == 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_64B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D map over an integer cache viewed as (kv_heads * row bytes, slots), uint8 elements; box =
+// 128 bytes x rows from a head's row start (that head's code row, then the next head's, read
+// and not used; zeros past the last head), 128-byte swizzle: the prefill kernel's code tiles
+bool code_tile_map(CUtensorMap* m, void* base, int row_bytes, int kvh, int64_t slots, int rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kvh * row_bytes, (cuuint64_t)slots};
+  cuuint64_t strides[1] = {(cuuint64_t)kvh * row_bytes};
+  cuuint32_t boxd[2] = {128, (cuuint32_t)rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, boxd, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -239,8 +255,15 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
   if ((stages & PA_STAGE_PREFILL) && can_prefill && args.N > 0 && slots > 0) {
     const int seg = gcd(d->block_size, pa::kPreTileK);
     CUtensorMap tq, tk, tv, tvm;
-    if (!query_map(&tq, query, dt, aq.q_stride, args.N) || !cache_map(&tk, kc, dt, hs, args.kvh, slots, seg) ||
-        !cache_map(&tv, vc, dt, hs, args.kvh, slots, seg)) {
+    // (integer caches: the scaled query rows are fp16, the caches code bytes)
+    const int row_bytes = args.kvq == PA_KV_INT8 ? hs : hs / 2;
+    const bool ok = args.kvq ? query_map(&tq, query, PA_FLOAT16, aq.q_stride, args.N) &&
+                                   code_tile_map(&tk, kc, row_bytes, args.kvh, slots, seg) &&
+                                   code_tile_map(&tv, vc, row_bytes, args.kvh, slots, seg)
+                             : query_map(&tq, query, dt, aq.q_stride, args.N) &&
+                                   cache_map(&tk, kc, dt, hs, args.kvh, slots, seg) &&
+                                   cache_map(&tv, vc, dt, hs, args.kvh, slots, seg);
+    if (!ok) {
       g_last_error = "cuTensorMapEncodeTiled failed (prefill maps)";
       return PA_ERR_CUDA;
     }

@@ -271,8 +271,8 @@ struct PreSmem {
   static constexpr int kV0 = kK0 + 2 * kKVBytes;
   static constexpr int kBars = kV0 + 2 * kKVBytes;
   // q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2], and per head (A, B):
-  // s_full, p_full, o_done, o_free
-  static constexpr int kNumBars = 18;
+  // s_full, p_full, o_done, o_free; integer caches: kc_full[2], vc_full[2] (code rows landed)
+  static constexpr int kNumBars = 22;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kPreCtas = kAbort + 4;  // CTAs of the grid that take units

@@ -31,8 +31,20 @@
 //               by V separately, so the weights keep ~16 significant bits instead of 8.
 //               At the end of the unit the partner threads add their row sums and each
 //               normalises and stores its half of the row of O.
-//   warps 18,19 idle (the block is a whole number of warpgroups).
+//   warps 18,19 idle (the block is a whole number of warpgroups); with integer caches they
+//               are the converters below.
 // TMEM: S_A at column 0, S_B at 128, O_A at 256, O_B at 384 (512 columns allocated).
+//
+// Integer caches (KQ = 1 INT8, 2 INT4): the tensor cores multiply fp16 values, so the codes
+// are turned into fp16 in shared memory. The producer's TMA lands each tile's code rows in
+// the last 64-column slab of the tile's fp16 buffer, one 128-byte row per key (the KV head's
+// code bytes, then the next head's, unused); warps 18 and 19 rewrite every row in place as
+// the exact fp16 integers of its codes (a warp reads whole rows before writing any of them)
+// and release the tile to the MMA. Q K^T then multiplies the query rows the cache-write
+// stage scaled by the K scales (fp16, with a power-of-two exponent per row that the row's
+// softmax constant takes back) by the codes; P V multiplies fp16 P by the V codes, and the
+// epilogue applies the V scales per channel. The scores and output are those of the
+// operator on the values code * scale.
 #include "common.cuh"
 
 namespace pa {
@@ -46,7 +58,54 @@ constexpr int kSoftWarpsPerHead = 8;  // two warps per TMEM lane quarter, 64 sco
 __device__ __forceinline__ uint32_t s_col(int x) { return x ? 128u : 0u; }
 __device__ __forceinline__ uint32_t o_col(int x) { return x ? 384u : 256u; }
 
-template <int HS, bool BF16>
+// The converter warps' work on one K or V tile of an integer cache: row r's code bytes sit
+// at the start of the 128-byte row r of the tile's last slab (128-byte swizzle: 16-byte
+// chunk j at position j ^ (r & 7)); they become the row's HS fp16 values at row r of every
+// slab. Each lane takes one 16-byte code chunk (16 INT8 or 32 INT4 channels); a warp reads
+// all of its rows' chunks before it writes, so only a row's own codes are overwritten, and
+// only after they are read. cw: this converter warp (0 or 1).
+template <int HS, int KQ>
+__device__ __forceinline__ void convert_code_tile(uint8_t* tile, int cw, int lane) {
+  constexpr int RB = KQ == 1 ? HS : HS / 2;                       // code bytes per row
+  constexpr int CH = RB / 16;                                      // code chunks per row
+  constexpr int ROWS = 32 / CH;                                    // rows per warp round
+  constexpr int CODES = KQ == 1 ? 16 : 32;                         // channels per code chunk
+  constexpr int SLAB = (HS / 64 - 1) * kPreTileK * 128;            // the slab the codes land in
+  const int rr = lane / CH, j = lane % CH;
+#pragma unroll 1
+  for (int r0 = cw * ROWS; r0 < kPreTileK; r0 += 2 * ROWS) {
+    const int r = r0 + rr;
+    const uint4 c = *reinterpret_cast<const uint4*>(tile + SLAB + r * 128 + ((j ^ (r & 7)) << 4));
+    __syncwarp();
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t f[CODES / 2];  // fp16 pairs of consecutive channels
+    if constexpr (KQ == 1) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {  // channels 4i .. 4i + 3 of the chunk
+        const uint32_t x = w[i] ^ 0x80808080u;
+        f[2 * i] = hsub2_u32(prmt(x, kF16Magic, 0x5140u), kF16Int8Bias);
+        f[2 * i + 1] = hsub2_u32(prmt(x, kF16Magic, 0x7362u), kF16Int8Bias);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {  // channels 8i .. 8i + 7: byte b holds 2b (low), 2b + 1 (high)
+        const uint32_t x = w[i] ^ 0x88888888u, x4 = x >> 4;
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          f[4 * i + b] = hsub2_u32(nib_pair_f16(prmt(x, x4, (uint32_t)(b | ((4 + b) << 8)))), kF16Int4Bias);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < CODES / 8; ++q) {  // 8 channels per 16-byte fp16 chunk
+      const int ch = CODES * j + 8 * q;
+      const int cc = (ch & 63) >> 3;
+      *reinterpret_cast<uint4*>(tile + (ch >> 6) * (kPreTileK * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) =
+          make_uint4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+    }
+  }
+}
+
+template <int HS, bool BF16, int KQ>
 __global__ void __launch_bounds__(kPreThreads, 1)
     prefill_kernel(const Args a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmVm,
@@ -54,9 +113,13 @@ __global__ void __launch_bounds__(kPreThreads, 1)
   using L = PreSmem<HS>;
   constexpr int HALVES = HS / 64;
   constexpr int KSTEPS = HS / 16;  // k-steps of Q K^T
-  constexpr uint32_t IDESC_QK = idesc_f16(BF16, kPreTileQ, kPreTileK, false);
-  constexpr uint32_t IDESC_PV = idesc_f16(BF16, kPreTileQ, HS, true);
-  constexpr uint32_t IDESC_PV16 = idesc_f16(false, kPreTileQ, HS, true);  // fp16 P times the fp16 V copy
+  // the MMA operand type: T, except on integer caches (fp16 scaled queries and fp16 codes);
+  // BF16 is the type of the output
+  constexpr bool MB = BF16 && KQ == 0;
+  constexpr uint32_t IDESC_QK = idesc_f16(MB, kPreTileQ, kPreTileK, false);
+  constexpr uint32_t IDESC_PV = idesc_f16(MB, kPreTileQ, HS, true);
+  constexpr uint32_t IDESC_PV16 = idesc_f16(false, kPreTileQ, HS, true);  // fp16 P times fp16 V (copy or codes)
+  constexpr int RB = KQ == 1 ? HS : HS / 2;  // code bytes of one KV head's row
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -71,6 +134,8 @@ __global__ void __launch_bounds__(kPreThreads, 1)
   uint64_t* p_full = bars + 12;
   uint64_t* o_done = bars + 14;
   uint64_t* o_free = bars + 16;
+  uint64_t* kc_full = bars + 18;  // integer caches: a tile's code rows landed
+  uint64_t* vc_full = bars + 20;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
   uint32_t* err = &a.hdr->error;
@@ -80,9 +145,11 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&k_full[i], 1);
+      mbar_init(&k_full[i], KQ ? 2 : 1);  // (integer caches: the two converter warps)
       mbar_init(&k_empty[i], 1);
-      mbar_init(&v_full[i], 1);
+      mbar_init(&v_full[i], KQ ? 2 : 1);
+      mbar_init(&kc_full[i], 1);
+      mbar_init(&vc_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 32 * kSoftWarpsPerHead);
@@ -106,7 +173,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
   const bool pair = (a.G & 1) == 0;  // two query heads of one KV head per unit
   // bf16: V from the fp16 copy (one fp16 P V product per 16 keys), unless the planner found
   // no room for it or the copy met a value fp16 cannot hold (then bf16 V, P as hi + lo)
-  const bool v16 = BF16 && a.hdr->v_mirror && !a.hdr->v_mirror_bad;
+  const bool v16 = MB && a.hdr->v_mirror && !a.hdr->v_mirror_bad;
   const int hpu = pair ? 2 : 1;
   const int units_per_tile = a.nh / hpu;
   // units dealt to the CTAs that take work; the others (the planner gave their SMs to the
@@ -172,6 +239,28 @@ __global__ void __launch_bounds__(kPreThreads, 1)
             else if (!v16) atomicOr(err, PA_DEVERR_BAD_BLOCK);  // (the copy kernel flags it otherwise)
             zv = v16 ? mirror_row0 + key : z;
           }
+        }
+        if constexpr (KQ != 0) {
+          // code rows (128 bytes from this head's row start) into the tiles' last slabs
+          constexpr int kCodeSlab = (HALVES - 1) * L::kHalfBytes;
+          if (lane == 0) {
+            mbar_wait(&k_empty[st], ph ^ 1, abort, err);
+            mbar_arrive_expect_tx(&kc_full[st], kPreTileK * 128);
+          }
+          __syncwarp();
+          if (lane < nseg)
+            tma_load_2d(smem + L::kK0 + st * L::kKVBytes + kCodeSlab + lane * seg_rows * 128, &tmK, &kc_full[st],
+                        g * RB, z);
+          if (lane == 0) {
+            mbar_wait(&v_empty[st], ph ^ 1, abort, err);
+            mbar_arrive_expect_tx(&vc_full[st], kPreTileK * 128);
+          }
+          __syncwarp();
+          if (lane < nseg)
+            tma_load_2d(smem + L::kV0 + st * L::kKVBytes + kCodeSlab + lane * seg_rows * 128, &tmV, &vc_full[st],
+                        g * RB, z);
+          __syncwarp();
+          continue;
         }
         if (lane == 0) {
           mbar_wait(&k_empty[st], ph ^ 1, abort, err);
@@ -247,7 +336,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         tc_fence_after();
         uint8_t* vtile = smem + L::kV0 + st * L::kKVBytes;
         const int valid = kv_len - i * kPreTileK;  // keys of this tile inside the sequence
-        if (x == 0 && valid < kPreTileK) {
+        if (KQ == 0 && x == 0 && valid < kPreTileK) {  // (codes are finite)
           // keys past the sequence may be unwritten cache rows; P is 0 there but 0 * NaN
           // is not, so clear those V rows (whole 128-byte rows: the swizzle stays inside)
           const int rows = kPreTileK - valid;
@@ -266,7 +355,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         if (elect_one()) {
           // 16 keys of V per MMA: rows 16kk.. (K dimension, 8-row atoms 1024 B apart), the
           // two 64-column slabs of head_size 16 KB apart (MN dimension)
-          if (BF16 && !v16) {
+          if (MB && !v16) {
 #pragma unroll
             for (int kk = 0; kk < kPreTileK / 16; ++kk) {
               const uint64_t vdesc = vd + (uint64_t)(kk * ((16 * 128) >> 4));
@@ -320,7 +409,6 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       float* xmax = reinterpret_cast<float*>(smem + L::kXmax);
       float* xsum = reinterpret_cast<float*>(smem + L::kXsum);
       const int pair_bar = 2 + x * 4 + quarter;  // named barrier of the two warps of this lane quarter
-      const float c = a.scale_log2;
       uint32_t gs = 0;
       PrefillTile next = load_tile(a, snake_unit(0, *pre_ctas), n_units, units_per_tile);
       for (int k = 0, u = snake_unit(0, *pre_ctas); u < n_units; u = snake_unit(++k, *pre_ctas)) {
@@ -331,6 +419,11 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         const int n_kv = tile.n_kv;
         const int lim = min(past + tile.j0 + row, kv_len - 1);  // last key this row sees
         const int lim_tile0 = past + tile.j0;                   // the smallest limit of the unit
+        // the softmax constant scale * log2(e); integer caches: times 2^E, the exponent the
+        // cache-write stage took out of this row's scaled query (rows past the sequence: 1)
+        float c = a.scale_log2;
+        if constexpr (KQ != 0)
+          if (tile.j0 + row < q_len) c = ldexpf(c, __ldg(a.qexp + (int64_t)(c0 + tile.j0 + row) * a.nh + h));
         float m_used = -INFINITY, l = 0.f;
         for (int t = 0; t < n_kv; ++t) {
           const uint32_t gt = gs + t;
@@ -385,7 +478,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           // that pair's two score registers ----
           const float neg_m = -m_used;
           bool p_done = false;
-          if constexpr (BF16) {
+          if constexpr (MB) {
             if (!v16) {  // against bf16 V: P as hi and lo bf16 parts
               float lc[2] = {0.f, 0.f};
 #pragma unroll
@@ -481,9 +574,18 @@ __global__ void __launch_bounds__(kPreThreads, 1)
 #pragma unroll
               for (int v = 0; v < OCOLS; v += 8) apply_gate8<BF16>(gsrc + v, reinterpret_cast<float*>(ov + v));
             }
+            if constexpr (KQ != 0) {  // integer caches: times the V scales of this row's channels
+              const float2* vs = reinterpret_cast<const float2*>(a.v_scale + (h / a.G) * HS + hsel * OCOLS);
 #pragma unroll
-            for (int v = 0; v < OCOLS / 2; ++v)  // packed in place (word v from words 2v, 2v + 1)
-              ov[v] = pack2<BF16>(__uint_as_float(ov[2 * v]) * inv, __uint_as_float(ov[2 * v + 1]) * inv);
+              for (int v = 0; v < OCOLS / 2; ++v) {
+                const float2 s2 = __ldg(vs + v);
+                ov[v] = pack2<BF16>(__uint_as_float(ov[2 * v]) * s2.x * inv, __uint_as_float(ov[2 * v + 1]) * s2.y * inv);
+              }
+            } else {
+#pragma unroll
+              for (int v = 0; v < OCOLS / 2; ++v)  // packed in place (word v from words 2v, 2v + 1)
+                ov[v] = pack2<BF16>(__uint_as_float(ov[2 * v]) * inv, __uint_as_float(ov[2 * v + 1]) * inv);
+            }
             if (a.out_v8) {  // 32-byte stores where the output allows them: half the store wavefronts
 #pragma unroll
               for (int v = 0; v < OCOLS / 2; v += 8) st_global_v8(dst + 2 * v, &ov[v]);
@@ -499,6 +601,32 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     }
   }
 
+  if constexpr (KQ != 0) {
+    if (warp >= 2 + 2 * kSoftWarpsPerHead) {
+      // ======================= converters: warps 18, 19 (integer caches) =======================
+      // the tiles in the producer's order: K then V of every KV tile of every unit
+      const int cw = warp - (2 + 2 * kSoftWarpsPerHead);
+      uint32_t gs = 0, unit_cnt = 0;
+      for (int u = snake_unit(0, *pre_ctas); u < n_units; u = snake_unit(++unit_cnt, *pre_ctas)) {
+        const int n_kv = load_tile(a, u, n_units, units_per_tile).n_kv;
+        for (int t = 0; t < n_kv; ++t, ++gs) {
+          const int st = gs & 1;
+          const uint32_t ph = (gs >> 1) & 1;
+          mbar_wait(&kc_full[st], ph, abort, err);
+          convert_code_tile<HS, KQ>(smem + L::kK0 + st * L::kKVBytes, cw, lane);
+          fence_proxy_async_smem();  // (the MMA reads the tile through the async proxy)
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&k_full[st]);
+          mbar_wait(&vc_full[st], ph, abort, err);
+          convert_code_tile<HS, KQ>(smem + L::kV0 + st * L::kKVBytes, cw, lane);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&v_full[st]);
+        }
+      }
+    }
+  }
+
   // ---- teardown ----
   tc_fence_before();
   __syncthreads();
@@ -509,23 +637,34 @@ __global__ void __launch_bounds__(kPreThreads, 1)
 }
 
 // ---- host launcher ----
-template <int HS, bool BF16>
+template <int HS, bool BF16, int KQ>
 static cudaError_t launch_prefill_t(const Args& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                     const CUtensorMap& tvm, int seg, int grid, cudaStream_t s) {
   constexpr int smem = PreSmem<HS>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<HS, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(prefill_kernel<HS, BF16, KQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(prefill_kernel<HS, BF16>, dim3(grid), dim3(kPreThreads), smem, s, a, tq, tk, tv, tvm, seg);
+  return launch_pdl(prefill_kernel<HS, BF16, KQ>, dim3(grid), dim3(kPreThreads), smem, s, a, tq, tk, tv, tvm, seg);
+}
+
+template <int KQ>
+static cudaError_t launch_prefill_kq(const Args& a, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk,
+                                     const CUtensorMap& tv, const CUtensorMap& tvm, int seg, int grid, cudaStream_t s) {
+  if constexpr (KQ != 2) {  // (INT4 needs head_size 128 or more)
+    if (a.hs == 64)
+      return bf16 ? launch_prefill_t<64, true, KQ>(a, tq, tk, tv, tvm, seg, grid, s)
+                  : launch_prefill_t<64, false, KQ>(a, tq, tk, tv, tvm, seg, grid, s);
+  }
+  return bf16 ? launch_prefill_t<128, true, KQ>(a, tq, tk, tv, tvm, seg, grid, s)
+              : launch_prefill_t<128, false, KQ>(a, tq, tk, tv, tvm, seg, grid, s);
 }
 
 cudaError_t launch_prefill(const Args& a, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& tvm, int seg, int grid, cudaStream_t s) {
   if (a.hs == 256) return launch_prefill256(a, bf16, tq, tk, tv, tvm, seg, grid, s);
-  if (a.hs == 64)
-    return bf16 ? launch_prefill_t<64, true>(a, tq, tk, tv, tvm, seg, grid, s)
-                : launch_prefill_t<64, false>(a, tq, tk, tv, tvm, seg, grid, s);
-  return bf16 ? launch_prefill_t<128, true>(a, tq, tk, tv, tvm, seg, grid, s)
-              : launch_prefill_t<128, false>(a, tq, tk, tv, tvm, seg, grid, s);
+  if (a.kvq == 1) return launch_prefill_kq<1>(a, bf16, tq, tk, tv, tvm, seg, grid, s);
+  if (a.kvq == 2) return launch_prefill_kq<2>(a, bf16, tq, tk, tv, tvm, seg, grid, s);
+  return launch_prefill_kq<0>(a, bf16, tq, tk, tv, tvm, seg, grid, s);
 }
 
 }  // namespace pa
