@@ -97,7 +97,7 @@ def test_lse_entry_point_checks_before_any_launch(lib):
 
 def test_integer_cache_checks_before_any_launch(lib):
     p = ctypes.c_void_p
-    dec = dict(max_query_len=1)  # decode-only (256-wide heads on integer caches need it)
+    dec = dict(max_query_len=1)  # decode-only
 
     def dims(hs=128, fmt=pa.KV_INT8, **kw):
         return pa.make_dims(64, 64, hs, 607, 256, 17, torch.float16, kv_dtype=fmt, **{**dec, **kw})
@@ -113,9 +113,7 @@ def test_integer_cache_checks_before_any_launch(lib):
     assert pa.workspace_size(dims(fmt=3), 32, 8) == 0                    # unknown format
     assert pa.workspace_size(dims(max_query_len=0), 32, 8) > 0           # prefill rows: the prefill kernel
     assert pa.workspace_size(dims(max_query_len=5, fmt=pa.KV_INT4), 32, 8) > 0
-    assert pa.workspace_size(dims(hs=256, max_query_len=0), 32, 8) == 0  # 256 wide: decode kernel only
-    assert pa.workspace_size(dims(hs=256, max_query_len=5), 32, 8) == 0  # 5 * 4 rows > 16
-    assert pa.workspace_size(dims(hs=256), 32, 8) > 0
+    assert pa.workspace_size(dims(hs=256, max_query_len=0), 32, 8) > 0
     assert call(dims(hs=64, fmt=pa.KV_INT4)) == 2
     assert call(dims(), k_scale=None) == 1                               # scales required
     assert call(dims(), v_scale=FAKE + 4) == 1                           # misaligned scale

@@ -142,3 +142,6 @@ def test_integer_cache_prefill_units(lib, fmt):
               past=[0, 700, 5], q_lens=[200, 1, 130], kv_quant=fmt)
     check_exactly_once(lib, p, max_q=200)
     check_exactly_once(lib, p, max_q=200, route=pa.ROUTE_ALL_PREFILL)
+    q = _prob("cov-int-prefill-256", dtype="fp16", num_heads=8, kv_num_heads=2, head_size=256, block_size=32,
+              past=[0, 300, 5], q_lens=[150, 1, 130], kv_quant=fmt)
+    check_exactly_once(lib, q, max_q=150)

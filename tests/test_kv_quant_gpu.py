@@ -155,6 +155,9 @@ PREFILL_CASES = {
     "int4-mixed-packed-drops-fp16": ("int4", "fp16", 32, 8, 128, 16, [60, 4, 2000, 0], [2, 40, 1, 129], True, 5),
     "int4-one-kv-head": ("int4", "fp16", 16, 1, 128, 64, [500, 0], [100, 20], False, 0),
     "int8-one-kv-head-hs64": ("int8", "bf16", 4, 1, 64, 16, [33, 0], [40, 200], False, 0),
+    "int8-hs256-chunked-bf16": ("int8", "bf16", 16, 2, 256, 64, [700, 0, 129], [130, 300, 2], False, 0),
+    "int4-hs256-packed-drops-fp16": ("int4", "fp16", 8, 2, 256, 32, [0, 2000, 63], [200, 1, 129], True, 4),
+    "int4-hs256-one-kv-head": ("int4", "bf16", 8, 1, 256, 16, [10, 0], [50, 17], False, 0),
 }
 
 
@@ -196,19 +199,6 @@ def test_integer_cache_prefill_with_prep_and_gate(fmt):
                 eps=1e-6, rotary_dim=128, theta=1.0e4)
     d, out, lse = _run(p, qk_prep=prep, output_gate=dev(gate_bits))
     _check(p, ref, d, out, lse, exact_codes=False, prepared=oracle.apply_qk_prep(p, prep_bits))
-
-
-def test_integer_cache_256_wide_heads_need_a_decode_bound():
-    # 256-wide heads on integer caches run on the decode kernel only
-    p = _problem("int8-hs256-bf16")
-    d = upload(p)
-    with pytest.raises(pa.PagedAttentionError) as e:
-        pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
-                           d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], d["slot_mapping"],
-                           num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, kv_quant="int8",
-                           k_scale=d["k_scale"], v_scale=d["v_scale"],
-                           workspace=torch.zeros(1 << 20, dtype=torch.uint8, device="cuda"))
-    assert e.value.status == 2
 
 
 @pytest.mark.parametrize("fmt", ["int8", "int4"])

@@ -113,11 +113,6 @@ pa_status check_dims(const pa_dims* d, int32_t nh, int32_t kvh) {
   if (d->head_size != 64 && d->head_size != 128 && d->head_size != 256) return PA_ERR_UNSUPPORTED;
   if (d->kv_dtype != PA_KV_SAME && d->kv_dtype != PA_KV_INT8 && d->kv_dtype != PA_KV_INT4) return PA_ERR_UNSUPPORTED;
   if (d->kv_dtype == PA_KV_INT4 && d->head_size == 64) return PA_ERR_UNSUPPORTED;
-  // integer caches at head_size 256 run on the decode kernel only: the call must prove every
-  // sequence decode-class
-  if (d->kv_dtype != PA_KV_SAME && d->head_size == 256 &&
-      (d->route != PA_ROUTE_AUTO || d->max_query_len <= 0 || (int64_t)d->max_query_len * (nh / kvh) > pa::kDecRows))
-    return PA_ERR_UNSUPPORTED;
   if (d->block_size % 16 != 0) return PA_ERR_UNSUPPORTED;
   if (d->route != PA_ROUTE_AUTO && d->route != PA_ROUTE_ALL_PREFILL) return PA_ERR_INVALID_ARGUMENT;
   if (d->decode_split_keys < 0 || d->decode_split_keys % pa::kDecTile != 0) return PA_ERR_INVALID_ARGUMENT;

@@ -615,6 +615,53 @@ __device__ __forceinline__ void s4_key_pairs(uint32_t w0, uint32_t w1, uint32_t 
   p[7] = hsub2_u32(nib_pair_f16(b >> 12), kF16Int4Bias);
 }
 
+// The converter warps' work on one K or V tile of an integer cache: row r's code bytes sit
+// at the start of the 128-byte row r of the tile's last slab (128-byte swizzle: 16-byte
+// chunk j at position j ^ (r & 7)); they become the row's HS fp16 values at row r of every
+// slab. Each lane takes one 16-byte code chunk (16 INT8 or 32 INT4 channels); a warp reads
+// all of its rows' chunks before it writes, so only a row's own codes are overwritten, and
+// only after they are read. cw: this converter warp (0 or 1).
+template <int HS, int KQ>
+__device__ __forceinline__ void convert_code_tile(uint8_t* tile, int cw, int lane) {
+  constexpr int RB = KQ == 1 ? HS : HS / 2;                       // code bytes per row
+  constexpr int CH = RB / 16;                                      // code chunks per row
+  constexpr int ROWS = 32 / CH;                                    // rows per warp round
+  constexpr int CODES = KQ == 1 ? 16 : 32;                         // channels per code chunk
+  constexpr int SLAB = (HS / 64 - 1) * kPreTileK * 128;            // the slab the codes land in
+  const int rr = lane / CH, j = lane % CH;
+#pragma unroll 1
+  for (int r0 = cw * ROWS; r0 < kPreTileK; r0 += 2 * ROWS) {
+    const int r = r0 + rr;
+    const uint4 c = *reinterpret_cast<const uint4*>(tile + SLAB + r * 128 + ((j ^ (r & 7)) << 4));
+    __syncwarp();
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t f[CODES / 2];  // fp16 pairs of consecutive channels
+    if constexpr (KQ == 1) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {  // channels 4i .. 4i + 3 of the chunk
+        const uint32_t x = w[i] ^ 0x80808080u;
+        f[2 * i] = hsub2_u32(prmt(x, kF16Magic, 0x5140u), kF16Int8Bias);
+        f[2 * i + 1] = hsub2_u32(prmt(x, kF16Magic, 0x7362u), kF16Int8Bias);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {  // channels 8i .. 8i + 7: byte b holds 2b (low), 2b + 1 (high)
+        const uint32_t x = w[i] ^ 0x88888888u, x4 = x >> 4;
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          f[4 * i + b] = hsub2_u32(nib_pair_f16(prmt(x, x4, (uint32_t)(b | ((4 + b) << 8)))), kF16Int4Bias);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < CODES / 8; ++q) {  // 8 channels per 16-byte fp16 chunk
+      const int ch = CODES * j + 8 * q;
+      const int cc = (ch & 63) >> 3;
+      *reinterpret_cast<uint4*>(tile + (ch >> 6) * (kPreTileK * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) =
+          make_uint4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+    }
+  }
+}
+
 // one 128-byte line of global memory into L2 (a hint: no data returned, no fault)
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");

@@ -23,7 +23,10 @@
 //               lazy rescale with threshold 2^8, P over S as fp16, or bf16 hi + lo against
 //               bf16 V); at the end of the unit each thread normalises and stores its 128 of
 //               the row's 256 output columns.
-//   warps 10,11 idle (the block is a whole number of warpgroups).
+//   warps 10,11 idle (the block is a whole number of warpgroups); with integer caches they
+//               turn the code rows of each chunk into fp16 in place, as the converters of the
+//               128-wide kernel do (a chunk's 128 channels are 128 INT8 or 64 INT4 code bytes
+//               of each key row, landed in the chunk's second slab).
 #include "common.cuh"
 
 namespace pa {
@@ -42,8 +45,9 @@ struct Smem {
   static constexpr int kQ = 0;                     // four slabs
   static constexpr int kCh0 = kQ + 4 * kSlab;
   static constexpr int kBars = kCh0 + kChunks * kChunkBytes;
-  // q_full, q_empty, ch_full[kChunks], ch_empty[kChunks], s_full[2], p_full, o_done, o_free
-  static constexpr int kNumBars = 2 + 2 * kChunks + 2 + 3;
+  // q_full, q_empty, ch_full[kChunks], ch_empty[kChunks], s_full[2], p_full, o_done, o_free,
+  // integer caches: chc_full[kChunks] (a chunk's code rows landed)
+  static constexpr int kNumBars = 2 + 2 * kChunks + 2 + 3 + kChunks;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kPreCtas = kAbort + 4;  // CTAs of the grid that take units
@@ -56,14 +60,18 @@ struct Smem {
 static_assert(Smem::kBytes <= 232448, "shared memory of one CTA");
 static_assert(kPreTileQ == 128 && kPreTileK == 128, "tile shape");
 
-template <bool BF16>
+template <bool BF16, int KQ>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill256_kernel(const Args a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmVm,
                       const int seg_rows) {
   using L = Smem;
-  constexpr uint32_t IDESC_QK = idesc_f16(BF16, kPreTileQ, kPreTileK, false);
-  constexpr uint32_t IDESC_PV = idesc_f16(BF16, kPreTileQ, 128, true);
+  // the MMA operand type: T, except on integer caches (fp16 scaled queries and fp16 codes);
+  // BF16 is the type of the output
+  constexpr bool MB = BF16 && KQ == 0;
+  constexpr int RB = KQ == 1 ? kHS : kHS / 2;  // code bytes of one KV head's row
+  constexpr uint32_t IDESC_QK = idesc_f16(MB, kPreTileQ, kPreTileK, false);
+  constexpr uint32_t IDESC_PV = idesc_f16(MB, kPreTileQ, 128, true);
   constexpr uint32_t IDESC_PV16 = idesc_f16(false, kPreTileQ, 128, true);  // fp16 P times the fp16 V copy
 
   extern __shared__ uint8_t smem_raw[];
@@ -77,6 +85,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + 2;
   uint64_t* o_done = s_full + 3;
   uint64_t* o_free = s_full + 4;
+  uint64_t* chc_full = s_full + 5;  // [kChunks]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
   uint32_t* err = &a.hdr->error;
@@ -86,8 +95,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int i = 0; i < kChunks; ++i) {
-      mbar_init(&ch_full[i], 1);
+      mbar_init(&ch_full[i], KQ ? 2 : 1);  // (integer caches: the two converter warps)
       mbar_init(&ch_empty[i], 1);
+      mbar_init(&chc_full[i], 1);
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
@@ -110,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // bf16: V from the fp16 copy unless the planner found no room for it or the copy met a
   // value fp16 cannot hold (then bf16 V, P as hi + lo)
-  const bool v16 = BF16 && a.hdr->v_mirror && !a.hdr->v_mirror_bad;
+  const bool v16 = MB && a.hdr->v_mirror && !a.hdr->v_mirror_bad;
   const int units_per_tile = a.nh;  // one head per unit
   // units dealt to the CTAs that take work; the others (the planner gave their SMs to the
   // decode kernel of this call) run no loop and release their TMEM at once
@@ -174,6 +184,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 2; ++c, ++gc) {
           const int slot = gc % kChunks;
           const uint32_t ph = (gc / kChunks) & 1;
+          if constexpr (KQ != 0) {  // the chunk's code rows (128 bytes from its channels' start)
+            if (lane == 0) {
+              mbar_wait(&ch_empty[slot], ph ^ 1, abort, err);
+              mbar_arrive_expect_tx(&chc_full[slot], kPreTileK * 128);
+            }
+            __syncwarp();
+            if (lane < nseg)
+              tma_load_2d(smem + L::kCh0 + slot * L::kChunkBytes + L::kSlab + lane * seg_rows * 128, map,
+                          &chc_full[slot], g * RB + c * (RB / 2), row);
+            __syncwarp();
+            continue;
+          }
           if (lane == 0) {
             mbar_wait(&ch_empty[slot], ph ^ 1, abort, err);
             mbar_arrive_expect_tx(&ch_full[slot], L::kChunkBytes);
@@ -249,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int slot = gc % kChunks;
           mbar_wait(&ch_full[slot], (gc / kChunks) & 1, abort, err);
           tc_fence_after();
-          if (valid < kPreTileK) {
+          if (KQ == 0 && valid < kPreTileK) {  // (codes are finite)
             // keys past the sequence may be unwritten cache rows; P is 0 there but 0 * NaN
             // is not, so clear those V rows (whole 128-byte rows: the swizzle stays inside)
             uint8_t* vchunk = smem + L::kCh0 + slot * L::kChunkBytes;
@@ -267,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (elect_one()) {
             // 16 keys of V per MMA (8-row atoms 1024 B apart), the chunk's two 64-column
             // slabs kSlab apart along N
-            if (BF16 && !v16) {
+            if (MB && !v16) {
 #pragma unroll
               for (int kk = 0; kk < kPreTileK / 16; ++kk) {
                 const uint64_t vdesc = vd + (uint64_t)(kk * ((16 * 128) >> 4));
@@ -308,7 +330,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* xmax = reinterpret_cast<float*>(smem + L::kXmax);
     float* xsum = reinterpret_cast<float*>(smem + L::kXsum);
     const int pair_bar = 2 + quarter;  // named barrier of the two warps of this lane quarter
-    const float c = a.scale_log2;
     uint32_t gs = 0;
     PrefillTile next = load_tile(a, snake_unit(0, *pre_ctas), n_units, units_per_tile);
     for (int k = 0, u = snake_unit(0, *pre_ctas); u < n_units; u = snake_unit(++k, *pre_ctas)) {
@@ -319,6 +340,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_kv = tile.n_kv;
       const int lim = min(past + tile.j0 + row, kv_len - 1);  // last key this row sees
       const int lim_tile0 = past + tile.j0;                   // the smallest limit of the unit
+      // the softmax constant scale * log2(e); integer caches: times 2^E, the exponent the
+      // cache-write stage took out of this row's scaled query (rows past the sequence: 1)
+      float c = a.scale_log2;
+      if constexpr (KQ != 0)
+        if (tile.j0 + row < q_len) c = ldexpf(c, __ldg(a.qexp + (int64_t)(c0 + tile.j0 + row) * a.nh + h));
       float m_used = -INFINITY, l = 0.f;
       for (int t = 0; t < n_kv; ++t) {
         const uint32_t gt = gs + t;
@@ -371,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // ---- P = exp2(s * c - m) over S, 16 keys at a time ----
         const float neg_m = -m_used;
-        if constexpr (BF16) {
+        if constexpr (MB) {
           float lc[2] = {0.f, 0.f};
           if (!v16) {
 #pragma unroll
@@ -472,9 +498,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int v = 0; v < 64; v += 8) apply_gate8<BF16>(gsrc + v, reinterpret_cast<float*>(ov + v));
           }
+          if constexpr (KQ != 0) {  // integer caches: times the V scales of these channels
+            const float2* vs =
+                reinterpret_cast<const float2*>(a.v_scale + (h / a.G) * kHS + hsel * OCOLS + half * 64);
 #pragma unroll
-          for (int v = 0; v < 32; ++v)
-            pk[half * 32 + v] = pack2<BF16>(__uint_as_float(ov[2 * v]) * inv, __uint_as_float(ov[2 * v + 1]) * inv);
+            for (int v = 0; v < 32; ++v) {
+              const float2 s2 = __ldg(vs + v);
+              pk[half * 32 + v] =
+                  pack2<BF16>(__uint_as_float(ov[2 * v]) * s2.x * inv, __uint_as_float(ov[2 * v + 1]) * s2.y * inv);
+            }
+          } else {
+#pragma unroll
+            for (int v = 0; v < 32; ++v)
+              pk[half * 32 + v] = pack2<BF16>(__uint_as_float(ov[2 * v]) * inv, __uint_as_float(ov[2 * v + 1]) * inv);
+          }
         }
         tc_fence_before();
         mbar_arrive(o_free);
@@ -494,6 +531,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if constexpr (KQ != 0) {
+    if (warp >= 2 + kSoftWarps) {
+      // ======================= converters: warps 10, 11 (integer caches) =======================
+      // the chunks in the producer's order: 4 per KV tile (K_t's two, V_{t-1}'s two, ...)
+      const int cw = warp - (2 + kSoftWarps);
+      uint32_t gc = 0, unit_cnt = 0;
+      for (int u = snake_unit(0, *pre_ctas); u < n_units; u = snake_unit(++unit_cnt, *pre_ctas)) {
+        const int chunks = 4 * load_tile(a, u, n_units, units_per_tile).n_kv;
+        for (int i = 0; i < chunks; ++i, ++gc) {
+          const int slot = gc % kChunks;
+          mbar_wait(&chc_full[slot], (gc / kChunks) & 1, abort, err);
+          convert_code_tile<128, KQ>(smem + L::kCh0 + slot * L::kChunkBytes, cw, lane);
+          fence_proxy_async_smem();  // (the MMA reads the chunk through the async proxy)
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ch_full[slot]);
+        }
+      }
+    }
+  }
+
   // ---- teardown ----
   tc_fence_before();
   __syncthreads();
@@ -503,20 +560,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool BF16>
+template <bool BF16, int KQ>
 cudaError_t launch_t(const Args& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const CUtensorMap& tvm, int seg, int grid, cudaStream_t s) {
   constexpr int smem = Smem::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(prefill256_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(prefill256_kernel<BF16, KQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(prefill256_kernel<BF16>, dim3(grid), dim3(kThreads), smem, s, a, tq, tk, tv, tvm, seg);
+  return launch_pdl(prefill256_kernel<BF16, KQ>, dim3(grid), dim3(kThreads), smem, s, a, tq, tk, tv, tvm, seg);
+}
+
+template <int KQ>
+cudaError_t launch_kq(const Args& a, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                      const CUtensorMap& tvm, int seg, int grid, cudaStream_t s) {
+  return bf16 ? launch_t<true, KQ>(a, tq, tk, tv, tvm, seg, grid, s)
+              : launch_t<false, KQ>(a, tq, tk, tv, tvm, seg, grid, s);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill256(const Args& a, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk,
                               const CUtensorMap& tv, const CUtensorMap& tvm, int seg, int grid, cudaStream_t s) {
-  return bf16 ? launch_t<true>(a, tq, tk, tv, tvm, seg, grid, s) : launch_t<false>(a, tq, tk, tv, tvm, seg, grid, s);
+  if (a.kvq == 1) return launch_kq<1>(a, bf16, tq, tk, tv, tvm, seg, grid, s);
+  if (a.kvq == 2) return launch_kq<2>(a, bf16, tq, tk, tv, tvm, seg, grid, s);
+  return launch_kq<0>(a, bf16, tq, tk, tv, tvm, seg, grid, s);
 }
 
 }  // namespace pa
