@@ -399,7 +399,25 @@ WORKLOAD_TEXT = {
        "U[1024,16384]), 32/8 heads, head_size 128, 256-token pages, fp16, packed [Q|K|V], 10% slots -1",
     5: "long-context decode: B=8, 1 new token each, past U[32768,131072], 32/8 heads, head_size 128, "
        "16-token pages, bf16",
+    "causal-prefill-explicit-slots": "causal prefill: B=4 x 2048 new tokens, past 0, 32/8 heads, head_size 128, "
+                                     "256-token pages, bf16, explicit slot_mapping (the fp16 V copy kernel runs)",
+    "causal-prefill-hs256": "causal prefill: B=4 x 2048 new tokens, past 0, 16/2 heads, head_size 256, "
+                            "256-token pages, bf16",
+    "decode-b64-hs256": "decode batch: B=64, 1 new token each, past U[512,4096], 16/2 heads, head_size 256, "
+                        "256-token pages, fp16, slots derived",
 }
+
+
+def quant_text(k, fmt):
+    return WORKLOAD_TEXT[k].replace(", fp16,", ", fp16 queries, %s per-channel KV caches," % fmt)
+
+
+def load_workload(k, kv_quant=None):
+    """(problem, key) of a workload number (2..5), a variant name, or k with integer caches."""
+    if k in wl.VARIANTS:
+        return wl.variant(k), k
+    k = int(k)
+    return (wl.config_kv_quant(k, kv_quant) if kv_quant else wl.config(k)), k
 
 
 def measure(r, steps, warmup, pk, clocks=None):
@@ -462,11 +480,11 @@ def run_cuda(args):
         dist.barrier()
     pk = peaks()
 
-    k = args.workload
-    if args.kv_quant:
-        p = wl.config_kv_quant(k, args.kv_quant)
+    if rank == 0 or args.kv_quant or args.workload in wl.VARIANTS:
+        p, k = load_workload(args.workload, args.kv_quant)
     else:
-        p = wl.config(k) if rank == 0 else wl.make_problem(**_rank_recipe(k, rank))
+        k = int(args.workload)
+        p = wl.make_problem(**_rank_recipe(k, rank))
     r = Runner(p, device)
     sampler = ClockSampler(local)
     if world > 1:
@@ -482,8 +500,7 @@ def run_cuda(args):
         "metric": METRIC, "value": round(value, 1), "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(sec_max * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": p.dtype, "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[k] if not args.kv_quant else
-                   WORKLOAD_TEXT[k].replace(", fp16,", ", fp16 queries, %s per-channel KV caches," % args.kv_quant),
+        "config": {"workload": WORKLOAD_TEXT[k] if not args.kv_quant else quant_text(k, args.kv_quant),
                    "name": p.name, "num_tokens": p.num_tokens,
                    "batch_size": p.batch_size, "num_blocks": p.num_blocks,
                    "kv_history_bytes_per_step": kv_history_bytes(p),
@@ -523,11 +540,23 @@ def run_cuda(args):
             v, u = headline(q, s)
             fp16 = wl.config(MAIN)
             sec_lines[q.name] = {
-                "workload": WORKLOAD_TEXT[MAIN].replace(", fp16,", ", fp16 queries, %s per-channel KV caches," % fmt),
+                "workload": quant_text(MAIN, fmt),
                 "value": round(v, 1), "unit": u + " (code bytes)", "ms_per_step": round(s * 1e3, 4),
                 "fp16_equivalent_kv_gb_s": round(kv_history_bytes(fp16) / s / 1e9, 1),
                 "speedup_vs_fp16_step": round(sec / s, 3) if k == MAIN else None,
                 "roofline": roof_q}
+            del rq
+            torch.cuda.empty_cache()
+        # the mixed batch on INT8 caches (its prefill rows on the prefill kernel's code-tile
+        # path) and the 256-wide heads of both kernels
+        for key in ("int8-mixed", "causal-prefill-hs256", "decode-b64-hs256"):
+            q = wl.config_kv_quant(4, "int8") if key == "int8-mixed" else wl.variant(key)
+            rq = Runner(q, device)
+            s, roof_q, _ = measure(rq, max(args.steps // 10, 10), args.warmup, pk)
+            v, u = headline(q, s)
+            sec_lines[q.name] = {"workload": quant_text(4, "int8") if key == "int8-mixed" else WORKLOAD_TEXT[key],
+                                 "value": round(v, 1), "unit": u, "ms_per_step": round(s * 1e3, 4),
+                                 "packed_tokens_per_s": round(q.num_tokens / s, 1), "roofline": roof_q}
             del rq
             torch.cuda.empty_cache()
         line["secondary"] = sec_lines
@@ -566,7 +595,7 @@ def run_reference(args):
         return
     import oracle
     oracle.build()
-    p = wl.config(args.workload)
+    p, key = load_workload(args.workload, args.kv_quant)
     for _ in range(args.warmup):
         oracle.paged_attention(p)
     t0 = time.perf_counter()
@@ -578,7 +607,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": unit, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": p.name},
+        "config": {"workload": WORKLOAD_TEXT[key] if not args.kv_quant else quant_text(key, args.kv_quant),
+                   "name": p.name},
         "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": oracle.max_threads(), "kind": "oracle",
                          "sample": "the whole %s workload per step (cache write + attention)" % p.name},
         "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -594,10 +624,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
-    ap.add_argument("--workload", type=int, default=MAIN, choices=[2, 3, 4, 5],
-                    help="workload of the headline line (2: the decode batch the metric is quoted on)")
+    ap.add_argument("--workload", default=str(MAIN), choices=["2", "3", "4", "5", *wl.VARIANTS],
+                    help="workload of the headline line (2: the decode batch the metric is quoted on; the "
+                         "variants serve profiling runs)")
     ap.add_argument("--kv-quant", choices=["int8", "int4"], default=None,
-                    help="the headline workload with integer KV caches (workload 2 only; profiling runs)")
+                    help="the workload with integer KV caches (workloads 2 and 4; profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

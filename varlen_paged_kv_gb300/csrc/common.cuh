@@ -618,9 +618,13 @@ __device__ __forceinline__ void s4_key_pairs(uint32_t w0, uint32_t w1, uint32_t 
 // The converter warps' work on one K or V tile of an integer cache: row r's code bytes sit
 // at the start of the 128-byte row r of the tile's last slab (128-byte swizzle: 16-byte
 // chunk j at position j ^ (r & 7)); they become the row's HS fp16 values at row r of every
-// slab. Each lane takes one 16-byte code chunk (16 INT8 or 32 INT4 channels); a warp reads
-// all of its rows' chunks before it writes, so only a row's own codes are overwritten, and
-// only after they are read. cw: this converter warp (0 or 1).
+// slab, as exact fp16 integers. (Leaving the conversion's offset in V, a constant to take off
+// the normalised output, would save an instruction per pair, but the offset multiplies the
+// difference between the fp16 weights the MMA sums and the fp32 row sum that normalises them:
+// about 1152 * 2^-12 of a code. So V is exact, like K.) Each lane takes one 16-byte code chunk
+// (16 INT8 or 32 INT4 channels) of a row in each of UNR rounds, reading all of them before
+// writing any, so only a row's own codes are overwritten and only after the whole warp has
+// read them. cw: this converter warp (0 or 1).
 template <int HS, int KQ>
 __device__ __forceinline__ void convert_code_tile(uint8_t* tile, int cw, int lane) {
   constexpr int RB = KQ == 1 ? HS : HS / 2;                       // code bytes per row
@@ -628,36 +632,46 @@ __device__ __forceinline__ void convert_code_tile(uint8_t* tile, int cw, int lan
   constexpr int ROWS = 32 / CH;                                    // rows per warp round
   constexpr int CODES = KQ == 1 ? 16 : 32;                         // channels per code chunk
   constexpr int SLAB = (HS / 64 - 1) * kPreTileK * 128;            // the slab the codes land in
+  constexpr int UNR = 4;                                           // rounds read before writing
+  static_assert(kPreTileK % (2 * ROWS * UNR) == 0, "rounds per tile");
   const int rr = lane / CH, j = lane % CH;
 #pragma unroll 1
-  for (int r0 = cw * ROWS; r0 < kPreTileK; r0 += 2 * ROWS) {
-    const int r = r0 + rr;
-    const uint4 c = *reinterpret_cast<const uint4*>(tile + SLAB + r * 128 + ((j ^ (r & 7)) << 4));
-    __syncwarp();
-    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-    uint32_t f[CODES / 2];  // fp16 pairs of consecutive channels
-    if constexpr (KQ == 1) {
+  for (int r0 = cw * ROWS * UNR; r0 < kPreTileK; r0 += 2 * ROWS * UNR) {
+    uint4 c[UNR];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {  // channels 4i .. 4i + 3 of the chunk
-        const uint32_t x = w[i] ^ 0x80808080u;
-        f[2 * i] = hsub2_u32(prmt(x, kF16Magic, 0x5140u), kF16Int8Bias);
-        f[2 * i + 1] = hsub2_u32(prmt(x, kF16Magic, 0x7362u), kF16Int8Bias);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {  // channels 8i .. 8i + 7: byte b holds 2b (low), 2b + 1 (high)
-        const uint32_t x = w[i] ^ 0x88888888u, x4 = x >> 4;
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-          f[4 * i + b] = hsub2_u32(nib_pair_f16(prmt(x, x4, (uint32_t)(b | ((4 + b) << 8)))), kF16Int4Bias);
-      }
+    for (int u = 0; u < UNR; ++u) {
+      const int r = r0 + u * ROWS + rr;
+      c[u] = *reinterpret_cast<const uint4*>(tile + SLAB + r * 128 + ((j ^ (r & 7)) << 4));
     }
+    __syncwarp();
 #pragma unroll
-    for (int q = 0; q < CODES / 8; ++q) {  // 8 channels per 16-byte fp16 chunk
-      const int ch = CODES * j + 8 * q;
-      const int cc = (ch & 63) >> 3;
-      *reinterpret_cast<uint4*>(tile + (ch >> 6) * (kPreTileK * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) =
-          make_uint4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+    for (int u = 0; u < UNR; ++u) {
+      const int r = r0 + u * ROWS + rr;
+      const uint32_t w[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
+      uint32_t f[CODES / 2];  // fp16 pairs of consecutive channels
+      if constexpr (KQ == 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {  // channels 4i .. 4i + 3 of the chunk
+          const uint32_t x = w[i] ^ 0x80808080u;
+          f[2 * i] = hsub2_u32(prmt(x, kF16Magic, 0x5140u), kF16Int8Bias);
+          f[2 * i + 1] = hsub2_u32(prmt(x, kF16Magic, 0x7362u), kF16Int8Bias);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {  // channels 8i .. 8i + 7: byte b holds 2b (low), 2b + 1 (high)
+          const uint32_t x = w[i] ^ 0x88888888u, x4 = x >> 4;
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            f[4 * i + b] = hsub2_u32(nib_pair_f16(prmt(x, x4, (uint32_t)(b | ((4 + b) << 8)))), kF16Int4Bias);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < CODES / 8; ++q) {  // 8 channels per 16-byte fp16 chunk
+        const int ch = CODES * j + 8 * q;
+        const int cc = (ch & 63) >> 3;
+        *reinterpret_cast<uint4*>(tile + (ch >> 6) * (kPreTileK * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) =
+            make_uint4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+      }
     }
   }
 }

@@ -771,9 +771,16 @@ __device__ void quant_unit(const Args& a, int tok, int64_t pos, int64_t slot, in
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const int ex = (m > 0.f && m <= 3.4028234e38f) ? ilogbf(m) - 14 : 0;
+    // ex = floor(log2 m) - 14, from the exponent field of a normal m
+    const uint32_t mb = __float_as_uint(m);
+    const int ex = !(m > 0.f && m <= 3.4028234e38f) ? 0 : mb >= 0x00800000u ? (int)(mb >> 23) - 127 - 14 : ilogbf(m) - 14;
+    // x * 2^-ex as two multiplications by normal powers of two (|ex| <= 163): exact where the
+    // result is normal; a value it would take out of the normal range is far below the
+    // row's largest and rounds to fp16 zero either way
+    const int n0 = -ex / 2, n1 = -ex - n0;
+    const float s0 = __uint_as_float((uint32_t)(n0 + 127) << 23), s1 = __uint_as_float((uint32_t)(n1 + 127) << 23);
 #pragma unroll
-    for (int e = 0; e < E; ++e) x[e] = ldexpf(x[e], -ex);
+    for (int e = 0; e < E; ++e) x[e] = x[e] * s0 * s1;
     store_vec<HS>(a.qprep + ((int64_t)tok * a.nh + h) * HS + lane * E, false, x);
     if (lane == 0) a.qexp[(int64_t)tok * a.nh + h] = ex;
     return;
@@ -871,10 +878,9 @@ __device__ __forceinline__ int own_mirror_base(const Args& a, int b, int lane) {
 // One instantiation per kind of write, so that each keeps only the registers it needs and
 // stays many warps deep (at most 64 registers: four blocks of 256 per SM): 0 = bit copy,
 // one warp per token, 4 = the same beside this call's planner, 5 = that with the fp16 V
-// copy; 1 = Q/K preparation, 2 = integer caches, 3 = both, one warp per (token, unit), the
+// copy; 1 = Q/K preparation, 2 = integer caches, 3 = both, over (token, unit) tasks, the
 // units being the token's nh query heads and then its kvh KV heads (each a short dependent
-// chain of a load, warp reductions and a store, so the units of a token run in parallel,
-// not one after the other).
+// chain of a load, warp reductions and a store); each warp takes a contiguous run of them.
 template <int MODE>
 __global__ void __launch_bounds__(256, 4) cache_write_kernel(const Args a) {
   constexpr bool COPY = MODE == 0 || MODE >= 4;  // bit copy
@@ -938,10 +944,29 @@ __global__ void __launch_bounds__(256, 4) cache_write_kernel(const Args a) {
     int b = 0;
     const int U = a.nh + a.kvh;
     const int64_t total = (int64_t)a.N * U;
-    for (int64_t wi = gw; wi < total; wi += warps) {
+    // Each warp takes a contiguous run of (token, unit) tasks: it resolves a token's slot once,
+    // and when it starts on a token it asks for the token's rows in L2, so that the loads of
+    // the token's units (one after the other, each a chain of load, reduction and store)
+    // find them there.
+    const int64_t per = (total + warps - 1) / warps;
+    const int64_t w0 = (int64_t)gw * per, w1 = min(total, w0 + per);
+    int cur = -1;
+    int64_t pos = 0, slot = -1;
+    for (int64_t wi = w0; wi < w1; ++wi) {
       const int tok = (int)(wi / U), u = (int)(wi - (int64_t)tok * U);
-      int64_t pos;
-      const int64_t slot = resolve_slot(a, tok, true, b, pos, errs);  // (after the wait: flagged at once)
+      if (tok != cur) {
+        cur = tok;
+        const char* q = reinterpret_cast<const char*>(a.query) + (int64_t)tok * a.q_stride * 2;
+        const int qlines = a.q_stride * 2 / 128;  // (packed rows hold K and V too)
+        for (int i = lane; i < qlines; i += 32) prefetch_l2(q + i * 128);
+        if (!a.packed) {
+          const int kvlines = a.kv_row * 2 / 128;
+          for (int i = lane; i < 2 * kvlines; i += 32)
+            prefetch_l2(reinterpret_cast<const char*>(i < kvlines ? a.key : a.value) +
+                        ((int64_t)tok * a.kv_row * 2 + (i % kvlines) * 128));
+        }
+        slot = resolve_slot(a, tok, true, b, pos, errs);  // (after the wait: flagged at once)
+      }
       if constexpr (MODE >= 2) {  // (the query rows are scaled even where the K/V write is skipped)
         constexpr bool PREP = MODE == 3;
         if (a.kvq == 1) {

@@ -521,20 +521,28 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           tc_fence_before();
           mbar_arrive(&o_free[x]);
           if (store) {
-            if (a.gate) {  // output gate: times sigmoid(gate), elementwise
-              const uint16_t* gsrc =
-                  a.gate + ((int64_t)(c0 + tile.j0 + row) * a.nh + h) * HS + hsel * OCOLS;
+            const uint16_t* gsrc = a.gate + ((int64_t)(c0 + tile.j0 + row) * a.nh + h) * HS + hsel * OCOLS;
+            if constexpr (KQ != 0) {
+              // integer caches: O holds sum p code over the V codes; the row's output is O / l
+              // times the V scale of each channel (then the gate), 8 at a time, packed in place
+              // (word v from words 2v, 2v + 1)
+              const float4* vs = reinterpret_cast<const float4*>(a.v_scale + (h / a.G) * HS + hsel * OCOLS);
 #pragma unroll
-              for (int v = 0; v < OCOLS; v += 8) apply_gate8<BF16>(gsrc + v, reinterpret_cast<float*>(ov + v));
-            }
-            if constexpr (KQ != 0) {  // integer caches: times the V scales of this row's channels
-              const float2* vs = reinterpret_cast<const float2*>(a.v_scale + (h / a.G) * HS + hsel * OCOLS);
+              for (int v = 0; v < OCOLS; v += 8) {
+                const float4 s0 = __ldg(vs + v / 4), s1 = __ldg(vs + v / 4 + 1);
+                const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+                float x[8];
 #pragma unroll
-              for (int v = 0; v < OCOLS / 2; ++v) {
-                const float2 s2 = __ldg(vs + v);
-                ov[v] = pack2<BF16>(__uint_as_float(ov[2 * v]) * s2.x * inv, __uint_as_float(ov[2 * v + 1]) * s2.y * inv);
+                for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(ov[v + e]) * inv * sv[e];
+                if (a.gate) apply_gate8<BF16>(gsrc + v, x);
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) ov[(v + e) / 2] = pack2<BF16>(x[e], x[e + 1]);
               }
             } else {
+              if (a.gate) {  // output gate: times sigmoid(gate), elementwise
+#pragma unroll
+                for (int v = 0; v < OCOLS; v += 8) apply_gate8<BF16>(gsrc + v, reinterpret_cast<float*>(ov + v));
+              }
 #pragma unroll
               for (int v = 0; v < OCOLS / 2; ++v)  // packed in place (word v from words 2v, 2v + 1)
                 ov[v] = pack2<BF16>(__uint_as_float(ov[2 * v]) * inv, __uint_as_float(ov[2 * v + 1]) * inv);

@@ -493,25 +493,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int half = 0; half < 2; ++half) {
           uint32_t ov[64];
           tmem_ld_x64(o_tmem + half * 64, ov);
+          if constexpr (KQ != 0) {
+            // integer caches: O holds sum p code over the V codes; the row's output is O / l
+            // times the V scale of each channel (then the gate), 8 at a time
+            const float4* vs =
+                reinterpret_cast<const float4*>(a.v_scale + (h / a.G) * kHS + hsel * OCOLS + half * 64);
+#pragma unroll
+            for (int v = 0; v < 64; v += 8) {
+              const float4 s0 = __ldg(vs + v / 4), s1 = __ldg(vs + v / 4 + 1);
+              const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+              float x[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(ov[v + e]) * inv * sv[e];
+              if (store && a.gate) apply_gate8<BF16>(a.gate + orow * kHS + hsel * OCOLS + half * 64 + v, x);
+#pragma unroll
+              for (int e = 0; e < 8; e += 2) pk[half * 32 + (v + e) / 2] = pack2<BF16>(x[e], x[e + 1]);
+            }
+            continue;
+          }
           if (store && a.gate) {  // output gate: times sigmoid(gate), elementwise
             const uint16_t* gsrc = a.gate + orow * kHS + hsel * OCOLS + half * 64;
 #pragma unroll
             for (int v = 0; v < 64; v += 8) apply_gate8<BF16>(gsrc + v, reinterpret_cast<float*>(ov + v));
           }
-          if constexpr (KQ != 0) {  // integer caches: times the V scales of these channels
-            const float2* vs =
-                reinterpret_cast<const float2*>(a.v_scale + (h / a.G) * kHS + hsel * OCOLS + half * 64);
 #pragma unroll
-            for (int v = 0; v < 32; ++v) {
-              const float2 s2 = __ldg(vs + v);
-              pk[half * 32 + v] =
-                  pack2<BF16>(__uint_as_float(ov[2 * v]) * s2.x * inv, __uint_as_float(ov[2 * v + 1]) * s2.y * inv);
-            }
-          } else {
-#pragma unroll
-            for (int v = 0; v < 32; ++v)
-              pk[half * 32 + v] = pack2<BF16>(__uint_as_float(ov[2 * v]) * inv, __uint_as_float(ov[2 * v + 1]) * inv);
-          }
+          for (int v = 0; v < 32; ++v)
+            pk[half * 32 + v] = pack2<BF16>(__uint_as_float(ov[2 * v]) * inv, __uint_as_float(ov[2 * v + 1]) * inv);
         }
         tc_fence_before();
         mbar_arrive(o_free);

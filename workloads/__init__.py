@@ -313,18 +313,7 @@ def config(k: int) -> Problem:
             head_size=128, block_size=256, past=np.zeros(4, np.int64),
             q_lens=np.full(4, 2048, np.int64))
     if k == 4:
-        past_chunk = uniform_int(seed, S_PAST, 8, 0, 8192)
-        past_dec = uniform_int(seed, S_QLEN, 24, 1024, 16384)
-        past = np.concatenate([past_chunk, past_dec])
-        q = np.concatenate([np.full(8, 512, np.int64), np.ones(24, np.int64)])
-        order = permutation(seed, S_ORDER, 32)
-        past, q = past[order], q[order]
-        N = int(q.sum())
-        return make_problem(
-            name=CONFIG_NAMES[4], seed=seed, dtype="fp16", num_heads=32, kv_num_heads=8,
-            head_size=128, block_size=256, past=past, q_lens=q, packed=True,
-            slot_mode="explicit", drop_count=N // 10,
-            max_blocks_per_sequence=(16384 + 1 + 255) // 256)
+        return _mixed(seed, CONFIG_NAMES[4], "fp16")
     if k == 5:
         past = uniform_int(seed, S_PAST, 8, 32768, 131072)
         return make_problem(
@@ -336,12 +325,56 @@ def config(k: int) -> Problem:
 
 def config_kv_quant(k: int, fmt: str) -> Problem:
     """Workload k's batch (same seed, lengths, pages and queries) with integer caches of
-    format fmt ("int8" | "int4") and per-channel scales in place of the 16-bit caches."""
-    if k != 2:
-        raise ValueError("integer caches are decode-only: workload 2")
+    format fmt ("int8" | "int4") and per-channel scales in place of the 16-bit caches: the
+    decode batch (k = 2) or the mixed continuous batch (k = 4)."""
     seed = 1000 + k
-    past = uniform_int(seed, S_PAST, 64, 512, 4096)
+    if k == 2:
+        past = uniform_int(seed, S_PAST, 64, 512, 4096)
+        return make_problem(
+            name=f"{CONFIG_NAMES[2]}-{fmt}", seed=seed, dtype="fp16", num_heads=32, kv_num_heads=8,
+            head_size=128, block_size=256, past=past, q_lens=np.ones(64, np.int64),
+            max_blocks_per_sequence=(4096 + 1 + 255) // 256, kv_quant=fmt)
+    if k == 4:
+        return _mixed(seed, f"{CONFIG_NAMES[4]}-{fmt}", "fp16", kv_quant=fmt)
+    raise ValueError("integer-cache variants exist for workloads 2 and 4")
+
+
+def _mixed(seed, name, dtype, kv_quant=None):
+    """The mixed continuous batch's recipe (8 chunks of 512 with past U[0, 8192] and 24 decode
+    rows with past U[1024, 16384] in seeded order, packed rows, 10% of the slots -1)."""
+    past_chunk = uniform_int(seed, S_PAST, 8, 0, 8192)
+    past_dec = uniform_int(seed, S_QLEN, 24, 1024, 16384)
+    past = np.concatenate([past_chunk, past_dec])
+    q = np.concatenate([np.full(8, 512, np.int64), np.ones(24, np.int64)])
+    order = permutation(seed, S_ORDER, 32)
+    past, q = past[order], q[order]
+    N = int(q.sum())
     return make_problem(
-        name=f"{CONFIG_NAMES[2]}-{fmt}", seed=seed, dtype="fp16", num_heads=32, kv_num_heads=8,
-        head_size=128, block_size=256, past=past, q_lens=np.ones(64, np.int64),
-        max_blocks_per_sequence=(4096 + 1 + 255) // 256, kv_quant=fmt)
+        name=name, seed=seed, dtype=dtype, num_heads=32, kv_num_heads=8,
+        head_size=128, block_size=256, past=past, q_lens=q, packed=True,
+        slot_mode="explicit", drop_count=N // 10,
+        max_blocks_per_sequence=(16384 + 1 + 255) // 256, kv_quant=kv_quant)
+
+
+# Further batches of the same recipes, for measurements of kernels the five workloads do not
+# run: the causal prefill with an explicit slot_mapping (for bf16 the fp16 copy of V is then
+# made by its own kernel after the cache write), and 256-wide heads (Qwen3.5's full-attention
+# layers: 16 query and 2 KV heads of 256).
+VARIANTS = ("causal-prefill-explicit-slots", "causal-prefill-hs256", "decode-b64-hs256")
+
+
+def variant(name: str) -> Problem:
+    if name == "causal-prefill-explicit-slots":
+        return make_problem(
+            name=name, seed=1104, dtype="bf16", num_heads=32, kv_num_heads=8, head_size=128, block_size=256,
+            past=np.zeros(4, np.int64), q_lens=np.full(4, 2048, np.int64), slot_mode="explicit")
+    if name == "causal-prefill-hs256":
+        return make_problem(
+            name=name, seed=1103, dtype="bf16", num_heads=16, kv_num_heads=2, head_size=256, block_size=256,
+            past=np.zeros(4, np.int64), q_lens=np.full(4, 2048, np.int64))
+    if name == "decode-b64-hs256":
+        past = uniform_int(1102, S_PAST, 64, 512, 4096)
+        return make_problem(
+            name=name, seed=1102, dtype="fp16", num_heads=16, kv_num_heads=2, head_size=256, block_size=256,
+            past=past, q_lens=np.ones(64, np.int64), max_blocks_per_sequence=(4096 + 1 + 255) // 256)
+    raise ValueError(f"no variant {name}")
