@@ -27,7 +27,9 @@ __host__ __device__ constexpr int dec_ctas_per_sm(int hs) { return hs == 256 ? 1
 // tiles streamed in the same time (measured: about 5 us per item against 1.4 us per tile
 // at head_size 256 with one CTA per SM; at 128 with two, per-CTA timestamps fitted about
 // 4 us per item against 1.2 us per tile, the CTAs with the most items finishing last).
-__host__ __device__ constexpr int dec_item_cost_tiles(int /*hs*/) { return 3; }
+// On integer caches a tile streams in about 1.0 us (the codes' conversion, not HBM, bounds it)
+// against an item cost of about 5 us, so an item counts 5 tiles there.
+__host__ __device__ constexpr int dec_item_cost_tiles(int /*hs*/, int kq = 0) { return kq ? 5 : 3; }
 constexpr int kMaxDecCtas = 1024;     // upper bound of the decode grid
 constexpr int kSelfMaxB = 256;        // sequences of a decode-only batch the decode kernel plans itself
 constexpr int kEarlyWriteMaxB = 1024; // sequences a bit-copy cache write checks per CTA to run beside the planner

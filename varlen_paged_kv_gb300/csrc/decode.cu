@@ -108,7 +108,7 @@ struct SelfGen {
   __device__ explicit SelfGen(const SelfView& v) : b((int)v.meta[3]), g((int)v.meta[4]) {}
 
   __device__ bool next(const Args& a, const SelfView& v, DecodeItem& d, int& slot) {
-    constexpr int V = dec_item_cost_tiles(HS);
+    const int V = dec_item_cost_tiles(HS, a.kvq);
     const int64_t P = gridDim.x;
     const int* cum = v.cum;
     const int* past = v.past;
@@ -157,7 +157,7 @@ struct SelfGen {
 template <int HS>
 __device__ void self_plan_prologue(const Args& a, const SelfView& v) {
   const int tid = threadIdx.x, B = a.B;
-  constexpr int V = dec_item_cost_tiles(HS);
+  const int V = dec_item_cost_tiles(HS, a.kvq);
   for (int b = tid; b <= B; b += blockDim.x) v.cum[b] = a.cum[b];
   for (int b = tid; b < B; b += blockDim.x) v.past[b] = a.past[b];
   __syncthreads();
@@ -812,13 +812,22 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
     // are written in one round and the write below adds them in warp order (the order, and
     // so the rounding, of the rounds).
     constexpr int kCompactRows = kDecRows / kDecWarps;
-    const bool compact = KQ == 0 && L::kCombBufs == 1 && n_rows <= kCompactRows;
+    const bool compact = L::kCombBufs == 1 && n_rows <= kCompactRows;
     if (compact) {
       if (gq < kCompactRows) {
-        float* cw = comb + (w * kCompactRows + r0) * kCombStride + tq * 2;
+        if constexpr (KQ == 0) {
+          float* cw = comb + (w * kCompactRows + r0) * kCombStride + tq * 2;
 #pragma unroll
-        for (int d = 0; d < ND; ++d)
-          *reinterpret_cast<float2*>(cw + d * 8) = make_float2(o[d][0] * f0, o[d][1] * f0);
+          for (int d = 0; d < ND; ++d)
+            *reinterpret_cast<float2*>(cw + d * 8) = make_float2(o[d][0] * f0, o[d][1] * f0);
+        } else {  // integer caches: the columns' channels in natural order
+          float* cw = comb + (w * kCompactRows + r0) * kCombStride;
+#pragma unroll
+          for (int d = 0; d < ND; ++d) {
+            cw[out_channel<HS, KQ>(d, 2 * tq)] = o[d][0] * f0;
+            cw[out_channel<HS, KQ>(d, 2 * tq + 1)] = o[d][1] * f0;
+          }
+        }
       }
       consumer_bar();
     } else {

@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
     if (q < 0 || a.past[b] < 0 || kv > max_kv || (a.max_query_len > 0 && q > a.max_query_len)) {
       atomicOr(&s_bad, 1);
     } else if (is_decode_class(q, a)) {
-      dec_tiles += ceil_div(kv, kDecTile) + dec_item_cost_tiles(a.hs);
+      dec_tiles += ceil_div(kv, kDecTile) + dec_item_cost_tiles(a.hs, a.kvq);
     } else if (q > 0 && a.split_sms) {
       // key tiles seen by the query tiles t = 0 .. T-1: ceil((past + 128 (t + 1)) / 128) =
       // c + t + 1 with c = ceil(past / 128) for all but the last, which sees ceil(kv / 128)
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
   // CTA c owns [s_start[c], s_start[c + 1]), s_start[c] = floor(c W / P), and processes the
   // key tiles inside it. So a CTA whose range starts more units pays for them with fewer
   // keys, and the CTAs finish together.
-  const int V = dec_item_cost_tiles(a.hs);
+  const int V = dec_item_cost_tiles(a.hs, a.kvq);
   int64_t* s_start = reinterpret_cast<int64_t*>(s_key);   // [kMaxDecCtas + 1]
   int* s_T = reinterpret_cast<int*>(s_start + (kMaxDecCtas + 1));  // [kPlanThreads] first tile of (b, head 0)
   int* s_nt = s_T + kPlanThreads;     // [kPlanThreads] tiles per unit (0: not decode)
