@@ -888,16 +888,23 @@ __global__ void __launch_bounds__(256, 4) cache_write_kernel(const Args a) {
   const int lane = threadIdx.x & 31;
   const int warps = (int)((gridDim.x * blockDim.x) >> 5);
   const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  // bit copy: each warp takes a contiguous run of tokens [tok0, tok1), so that consecutive
+  // tokens of a sequence reuse its lookup (and usually its page)
+  const int per_warp = (a.N + warps - 1) / warps;
+  const int tok0 = min(a.N, gw * per_warp), tok1 = min(a.N, tok0 + per_warp);
   if constexpr (COPY) {
-    // this warp's first token's K and V rows and the batch description into L2 while the
-    // earlier kernels finish (hints only)
-    if (gw < a.N) {
+    // this warp's tokens' K and V rows and the batch description into L2 while the earlier
+    // kernels finish and the tokens' slots are resolved (hints only)
+    {
       const int lines = a.kv_row * 2 / 128;  // 128-byte lines of one K (or V) row
-      const char* src = a.packed ? reinterpret_cast<const char*>(a.query) + ((int64_t)gw * a.q_stride + a.k_offset) * 2
-                                 : reinterpret_cast<const char*>(a.key) + (int64_t)gw * a.kv_row * 2;
       const int64_t vdelta = a.packed ? (int64_t)(a.v_offset - a.k_offset) * 2
                                       : reinterpret_cast<const char*>(a.value) - reinterpret_cast<const char*>(a.key);
-      for (int i = lane; i < 2 * lines; i += 32) prefetch_l2(src + (i >= lines ? vdelta : 0) + (i % lines) * 128);
+      for (int i = lane; i < 2 * lines * (tok1 - tok0); i += 32) {
+        const int tk = tok0 + i / (2 * lines), li = i % (2 * lines);
+        const char* src = a.packed ? reinterpret_cast<const char*>(a.query) + ((int64_t)tk * a.q_stride + a.k_offset) * 2
+                                   : reinterpret_cast<const char*>(a.key) + (int64_t)tk * a.kv_row * 2;
+        prefetch_l2(src + (li >= lines ? vdelta : 0) + (li % lines) * 128);
+      }
     }
     if (threadIdx.x < 32)
       for (int i = lane * 32; i <= a.B; i += 32 * 32) {
@@ -997,7 +1004,7 @@ __global__ void __launch_bounds__(256, 4) cache_write_kernel(const Args a) {
     constexpr bool kv = decltype(kv_c)::value;
     constexpr int mirror = decltype(mirror_c)::value;
     int b = 0, mb = -1, mb_of = -1;  // (the last sequence's first copy row)
-    for (int tok = gw; tok < a.N; tok += warps) {
+    for (int tok = tok0; tok < tok1; ++tok) {
       int64_t pos;
       const int64_t slot = resolve_slot<decltype(defer_c)::value>(a, tok, false, b, pos, errs);
       int mrow = -1;  // the token's row of the fp16 V copy
