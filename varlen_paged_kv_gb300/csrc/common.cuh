@@ -585,14 +585,15 @@ __device__ __forceinline__ void s8x4_to_f16_biased(uint32_t w, uint32_t& lo, uin
   lo = prmt(x, kF16Magic, 0x5140u);
   hi = prmt(x, kF16Magic, 0x7362u);
 }
-// byte i of w0 and byte i of w1 (two keys, one channel) as one fp16 pair, i = 0..3
-__device__ __forceinline__ void s8_key_pairs(uint32_t w0, uint32_t w1, uint32_t (&p)[4]) {
+// byte i of w0 and byte i of w1 (two keys, one channel) as one fp16 pair, i = 0..3, as the
+// exact fp16 integers code + 1152 (the consumer takes the offset off)
+__device__ __forceinline__ void s8_key_pairs_biased(uint32_t w0, uint32_t w1, uint32_t (&p)[4]) {
   const uint32_t x0 = w0 ^ 0x80808080u, x1 = w1 ^ 0x80808080u;
   const uint32_t a = prmt(x0, x1, 0x5140u), b = prmt(x0, x1, 0x7362u);  // interleaved by key
-  p[0] = hsub2_u32(prmt(a, kF16Magic, 0x5140u), kF16Int8Bias);
-  p[1] = hsub2_u32(prmt(a, kF16Magic, 0x7362u), kF16Int8Bias);
-  p[2] = hsub2_u32(prmt(b, kF16Magic, 0x5140u), kF16Int8Bias);
-  p[3] = hsub2_u32(prmt(b, kF16Magic, 0x7362u), kF16Int8Bias);
+  p[0] = prmt(a, kF16Magic, 0x5140u);
+  p[1] = prmt(a, kF16Magic, 0x7362u);
+  p[2] = prmt(b, kF16Magic, 0x5140u);
+  p[3] = prmt(b, kF16Magic, 0x7362u);
 }
 // eight INT4 codes (nibble j = channel j of w) as the fp16 pairs (0, 4), (1, 5), (2, 6), (3, 7)
 __device__ __forceinline__ void s4x8_to_f16(uint32_t w, uint32_t (&p)[4]) {

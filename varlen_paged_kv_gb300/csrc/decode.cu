@@ -690,8 +690,6 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
           p[n][2] = fast_exp2(x[n][2] - ms1);
           p[n][3] = fast_exp2(x[n][3] - ms1);
         }
-        l0 = l0 * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-        l1 = l1 * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
         // P as the MMA A fragment; bf16 carries it as hi + lo (two products), fp16 as one
         uint32_t pa[4], pl[4];
         if constexpr (BF16 && KQ == 0) {
@@ -704,6 +702,21 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
           pa[1] = pack2<false>(p[0][2], p[0][3]);
           pa[2] = pack2<false>(p[1][0], p[1][1]);
           pa[3] = pack2<false>(p[1][2], p[1][3]);
+        }
+        if constexpr (KQ == 1) {
+          // INT8 caches: the V codes enter P V with the conversion's offset (code + 1152), which
+          // the output takes off after dividing by the row sum; that sum must then add exactly
+          // the fp16 weights the MMA multiplies. (At INT4's coarser scales the offset's share of
+          // the tensor core's fp32 rounding shows in the output: INT4 V codes stay exact.)
+          const float2 q0 = __half22float2(*reinterpret_cast<const __half2*>(&pa[0]));
+          const float2 q1 = __half22float2(*reinterpret_cast<const __half2*>(&pa[1]));
+          const float2 q2 = __half22float2(*reinterpret_cast<const __half2*>(&pa[2]));
+          const float2 q3 = __half22float2(*reinterpret_cast<const __half2*>(&pa[3]));
+          l0 = l0 * al0 + ((q0.x + q0.y) + (q2.x + q2.y));
+          l1 = l1 * al1 + ((q1.x + q1.y) + (q3.x + q3.y));
+        } else {
+          l0 = l0 * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+          l1 = l1 * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
         }
         if (!__all_sync(0xffffffffu, al0 == 1.f && al1 == 1.f)) {  // (no row's max grew: O stays)
 #pragma unroll
@@ -730,8 +743,8 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
 #pragma unroll
             for (int i = 0; i < G / 4; ++i) {
               uint32_t lo[4], hi[4];
-              s8_key_pairs(w0[i], w1[i], lo);
-              s8_key_pairs(w8[i], w9[i], hi);
+              s8_key_pairs_biased(w0[i], w1[i], lo);
+              s8_key_pairs_biased(w8[i], w9[i], hi);
 #pragma unroll
               for (int e = 0; e < 4; ++e) mma16816<false>(o[D * G + 4 * i + e], pa, lo[e], hi[e]);
             }
@@ -916,7 +929,8 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
             for (int e = 0; e < 8; ++e) x[e] = cval(v + e) * inv;
             if constexpr (KQ != 0) {  // integer caches: the V scales of the output channels
 #pragma unroll
-              for (int e = 0; e < 8; ++e) x[e] *= __ldg(a.v_scale + item.g * HS + col + v + e);
+              for (int e = 0; e < 8; ++e)  // (INT8: the V codes' offset off) then the V scales
+                x[e] = (KQ == 1 ? x[e] - 1152.f : x[e]) * __ldg(a.v_scale + item.g * HS + col + v + e);
             }
             if (a.gate)  // output gate: times sigmoid(gate), elementwise
               apply_gate8<BF16>(a.gate + ((int64_t)tok * a.nh + head) * HS + col + v, x);
@@ -994,7 +1008,8 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
             for (int e = 0; e < 8; ++e) x[e] = acc[v + e] * dinv;
             if constexpr (KQ != 0) {
 #pragma unroll
-              for (int e = 0; e < 8; ++e) x[e] *= __ldg(a.v_scale + item.g * HS + col + v + e);
+              for (int e = 0; e < 8; ++e)  // (INT8: the V codes' offset off) then the V scales
+                x[e] = (KQ == 1 ? x[e] - 1152.f : x[e]) * __ldg(a.v_scale + item.g * HS + col + v + e);
             }
             if (a.gate) apply_gate8<BF16>(a.gate + ((int64_t)tok * a.nh + head) * HS + col + v, x);
             uint4 pk;
