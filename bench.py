@@ -326,10 +326,17 @@ class Runner:
 # the figure is reported only while the sources are unchanged, else traffic is null.
 # ("decode_kernel_self": the self-planned instantiation that decode-only steps run.)
 NCU_TRAFFIC = {
-    ("prefill_kernel", "causal-prefill-4x2048"): (137497088, "7e299115223b5f83"),
+    ("decode_kernel_self", "decode-b64"): (618578432 + 4103424, "ec414d405b7637a0"),
+    ("decode_kernel_self", "long-decode-b8-bs16"): (2279043584 + 3350272, "ec414d405b7637a0"),
+    ("decode_kernel_self", "decode-b64-int8"): (309909248 + 3940352, "ec414d405b7637a0"),
+    ("decode_kernel_self", "decode-b64-int4"): (155559424 + 3653888, "ec414d405b7637a0"),
+    ("prefill_kernel", "causal-prefill-4x2048"): (104697856 + 31982848, "653c243942d368cb"),
+    # the two attention kernels of a mixed step (prefill 193.2 + 15.7 MB, decode 775.9 + 0.5 MB)
+    ("prefill_kernel+decode_kernel", "mixed-8x512-chunks+24-decode"): (193237248 + 15672832 + 775852800 + 464384,
+                                                                        "9e22602355205d7b"),
 }
 KERNEL_SOURCES = {"decode_kernel": ("decode.cu", "common.cuh"), "decode_kernel_self": ("decode.cu", "common.cuh"),
-                  "prefill_kernel": ("prefill.cu", "common.cuh"),
+                  "prefill_kernel": ("prefill.cu", "common.cuh"), "prefill256_kernel": ("prefill256.cu", "common.cuh"),
                   "prefill_kernel+decode_kernel": ("prefill.cu", "decode.cu", "common.cuh")}
 
 
@@ -436,14 +443,18 @@ def measure(r, steps, warmup, pk, clocks=None):
                           "achieved = the prefill rows' causal FLOPs / the pair's time")
     elif prefill_sequences(q):
         _, kt, _ = r.timed(steps, warmup, pa.STAGE_PREFILL)
-        roof = kernel_roofline(q, "tensor", kt, pk, "prefill_kernel")
-        roof["kernel"] = "prefill_kernel (tcgen05/TMEM, TMA)"
+        name = "prefill256_kernel" if q.head_size == 256 else "prefill_kernel"
+        roof = kernel_roofline(q, "tensor", kt, pk, name)
+        roof["kernel"] = name + " (tcgen05/TMEM, TMA)"
     else:
-        # decode-only with the host bound: the self-planned decode kernel the whole step runs
+        # decode-only with the host bound: the decode kernel the whole step runs (self-planned
+        # up to head_size 128)
         _, kt, _ = r.timed(steps, warmup, pa.STAGE_DECODE)
-        roof = kernel_roofline(q, "hbm", kt, pk, "decode_kernel_self")
-        roof["kernel"] = ("decode_kernel (self-planned, split-KV, TMA + mma.sync%s)"
-                          % ("" if q.kv_quant is None else ", on %s codes" % q.kv_quant))
+        self_planned = q.head_size <= 128
+        roof = kernel_roofline(q, "hbm", kt, pk, "decode_kernel_self" if self_planned else "decode_kernel")
+        roof["kernel"] = ("decode_kernel (%ssplit-KV, TMA + mma.sync%s)"
+                          % ("self-planned, " if self_planned else "",
+                             "" if q.kv_quant is None else ", on %s codes" % q.kv_quant))
     roof["ms_per_launch"] = round(kt * 1e3, 4)
     # The bracketing events serialise the bracketed launches with the rest of the stream; in
     # back-to-back steps a kernel's prologue overlaps its predecessor (programmatic dependent
