@@ -448,9 +448,9 @@ def measure(r, steps, warmup, pk, clocks=None):
         roof["kernel"] = name + " (tcgen05/TMEM, TMA)"
     else:
         # decode-only with the host bound: the decode kernel the whole step runs (self-planned
-        # up to head_size 128)
+        # up to 256 sequences, 64 at head_size 256)
         _, kt, _ = r.timed(steps, warmup, pa.STAGE_DECODE)
-        self_planned = q.head_size <= 128
+        self_planned = q.batch_size <= (64 if q.head_size == 256 else 256)
         roof = kernel_roofline(q, "hbm", kt, pk, "decode_kernel_self" if self_planned else "decode_kernel")
         roof["kernel"] = ("decode_kernel (%ssplit-KV, TMA + mma.sync%s)"
                           % ("self-planned, " if self_planned else "",

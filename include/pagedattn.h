@@ -94,8 +94,8 @@ typedef struct pa_dims {
                                       (the CPU-resident launch bound of the packed contract's
                                       attention_metadata). With route AUTO and max_query_len *
                                       (num_heads / kv_num_heads) <= 16 no prefill kernel is launched; if in
-                                      addition slot_mapping is NULL, batch_size <= 256 and head_size <= 128,
-                                      no planner runs: a reset of the workspace's counters, then the decode
+                                      addition slot_mapping is NULL and batch_size <= 256 (64 at
+                                      head_size 256), no planner runs: a reset of the workspace's counters, then the decode
                                       kernel, which plans its own share of the work (with caches of T and
                                       no Q/K preparation it also writes this call's K/V rows itself, two
                                       kernels in all; else the cache-write kernel runs between the two and

@@ -5,8 +5,9 @@ for every (row, head, key) that an attention kernel lets into its softmax, one i
 array (pa_debug_coverage). Row j of sequence b must count each key 0 .. past_b + j exactly
 once and nothing else, whatever the partition: forced split lengths, the balanced cut with
 skewed units cut across CTAs, mixed batches on split SMs at several decode shares, the
-decode kernel's own partition of a decode-only call, the prefill kernel's units (ragged
-tails, chunks with history, 64/128/256-wide heads) and integer caches.
+decode kernel's own partition of a decode-only call (128 and 256 wide), the prefill
+kernel's units (ragged tails, chunks with history, 64/128/256-wide heads) and integer
+caches.
 """
 import ctypes
 
@@ -108,6 +109,13 @@ def test_decode_partition(lib, split):
 def test_self_planned_decode_partition(lib):
     p = _prob("cov-self", **DECODE)
     check_exactly_once(lib, p, max_q=int(p.q_lens.max()))
+
+
+@pytest.mark.parametrize("fmt", [None, "int4"])
+def test_self_planned_decode_partition_256(lib, fmt):
+    p = _prob("cov-self-256", dtype="bf16", num_heads=16, kv_num_heads=2, head_size=256, block_size=16,
+              past=[5000, 3, 700, 0, 2048, 64], q_lens=[1, 2, 1, 1, 3, 1], kv_quant=fmt)
+    check_exactly_once(lib, p, max_q=3)
 
 
 @pytest.mark.parametrize("dsm", [0, 1, 40, 151])

@@ -34,6 +34,9 @@ CASES = {
     "mha-q16": ("bf16", 4, 4, 16, [33, 1000], [16, 3]),
     "gqa16-long": ("bf16", 16, 1, 256, [4000, 0], [1, 1]),
     "gqa4-ragged": ("fp16", 8, 2, 32, [129, 63, 1], [4, 2, 1]),
+    # 64 sequences, the most the 256-wide decode kernel plans itself, and 65, planned on the host
+    "gqa8-b64": ("bf16", 16, 2, 16, [(37 * i) % 300 for i in range(64)], [1 + (i % 5 == 0) for i in range(64)]),
+    "gqa8-b65": ("fp16", 16, 2, 16, [(41 * i) % 280 for i in range(65)], [1 + (i % 7 == 0) for i in range(65)]),
 }
 
 

@@ -486,3 +486,31 @@ def test_more_prefill_tiles_than_the_sort_holds():
     p = w.make_problem(name="many-tiles", seed=42, dtype="fp16", num_heads=8, kv_num_heads=2, head_size=64,
                        block_size=16, past=past, q_lens=np.full(B, 5, np.int64))
     check(p)
+
+
+# ---- a call split into stage groups runs the whole call's program ----------------------------
+
+@pytest.mark.parametrize("name,max_q,groups", [
+    ("decode-q-up-to-4", 4, [pa.STAGE_PLAN | pa.STAGE_CACHE_WRITE, pa.STAGE_DECODE]),  # self-planned
+    ("decode-q-up-to-4", 4, [pa.STAGE_PLAN, pa.STAGE_CACHE_WRITE, pa.STAGE_PREFILL, pa.STAGE_DECODE]),
+    ("mixed-packed-drops", 0, [pa.STAGE_PLAN | pa.STAGE_CACHE_WRITE, pa.STAGE_PREFILL | pa.STAGE_DECODE]),
+    ("mixed-packed-drops", 0, [pa.STAGE_PLAN, pa.STAGE_CACHE_WRITE, pa.STAGE_PREFILL, pa.STAGE_DECODE]),
+    ("bf16-long-history-chunk", 0, [pa.STAGE_PLAN | pa.STAGE_CACHE_WRITE, pa.STAGE_PREFILL, pa.STAGE_DECODE]),
+])
+def test_stage_split_calls_match_the_whole_call(name, max_q, groups):
+    p = _case(name)
+    whole = run_gpu(p, max_query_len=max_q)
+    d = upload(p)
+    ws = make_workspace(p, 0, pa.ROUTE_AUTO, max_q)
+    out = torch.empty((p.num_tokens, p.num_heads * p.head_size), dtype=d["query"].dtype, device="cuda")
+    for st in groups:
+        pa.paged_attention(d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"],
+                           d["cumulative_sequence_length"], d["past_seqlens"], d["block_table"], d["slot_mapping"],
+                           num_heads=p.num_heads, kv_num_heads=p.kv_num_heads, scale=p.scale, output=out,
+                           workspace=ws, max_query_len=max_q, stages=st)
+    assert pa.read_device_error(ws) == 0
+    assert np.array_equal(bits_of(d["key_cache"]), whole["key_cache"])
+    assert np.array_equal(bits_of(d["value_cache"]), whole["value_cache"])
+    # the split-SM program of a mixed batch runs its two attention kernels side by side only
+    # when one call launches both; the partition and the arithmetic are the same either way
+    assert np.array_equal(bits_of(out), whole["out_bits"])

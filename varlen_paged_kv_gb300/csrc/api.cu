@@ -206,7 +206,7 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
   // kernel writes the rows, PA_STAGE_DECODE is the self-planned decode kernel.
   const bool self_plan = d->route == PA_ROUTE_AUTO && d->max_query_len > 0 &&
                          (int64_t)d->max_query_len * args.G <= pa::kDecRows && args.slot_mapping == nullptr &&
-                         args.forced_split <= 0 && args.B >= 1 && args.B <= pa::kSelfMaxB && hs <= 128 && args.N > 0 &&
+                         args.forced_split <= 0 && args.B >= 1 && args.B <= pa::self_max_b(hs) && args.N > 0 &&
                          slots > 0;
   const bool self_write_rows = self_plan && !args.prep && !args.kvq;
   args.self_plan = self_plan;  // (the cache-write kernel checks the batch itself)

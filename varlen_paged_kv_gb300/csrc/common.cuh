@@ -32,6 +32,9 @@ __host__ __device__ constexpr int dec_ctas_per_sm(int hs) { return hs == 256 ? 1
 __host__ __device__ constexpr int dec_item_cost_tiles(int /*hs*/, int kq = 0) { return kq ? 5 : 3; }
 constexpr int kMaxDecCtas = 1024;     // upper bound of the decode grid
 constexpr int kSelfMaxB = 256;        // sequences of a decode-only batch the decode kernel plans itself
+// (at head_size 256, whose one CTA per SM holds a 192 KB ring, 64: the batch view fits beside
+// the two combine buffers)
+__host__ __device__ constexpr int self_max_b(int hs) { return hs == 256 ? 64 : kSelfMaxB; }
 constexpr int kEarlyWriteMaxB = 1024; // sequences a bit-copy cache write checks per CTA to run beside the planner
 // rates of the planner's model that splits the SMs between the prefill and the decode
 // kernel of a call with both kinds of rows (measured on GB300 at head_size 128)
@@ -238,20 +241,25 @@ struct DecSmem {
   static constexpr int kBoxBytes = kRowBytes < 128 ? kRowBytes : 128;
   static constexpr int kBoxes = kRowBytes / kBoxBytes;
   static constexpr int kStages = KQ == 0 ? kDecStages : KQ == 1 ? 2 * kDecStages : 4 * kDecStages;
-  static constexpr int kCombBufs = HS == 256 ? 2 : 1;
+  // (the self-planned 256-wide INT4 kernel, whose ring is deepest, gives its second buffer's
+  // room to the batch view)
+  static constexpr int kCombBufs = HS == 256 && !(SELF && KQ == 2) ? 2 : 1;
   static constexpr int kHalves = HS / 64;
   static constexpr int kTileBytes = kDecTile * kRowBytes;   // one K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kCombStride = HS + 4;                 // floats; the pad spreads rows over banks
+  // floats; the pad spreads rows over banks (2 for the self-planned 256-wide kernel, whose
+  // batch view takes the last bytes of shared memory)
+  static constexpr int kCombStride = HS + (HS == 256 && SELF ? 2 : 4);
   static constexpr int kComb = kStages * kStageBytes;        // float [kCombBufs][16][kCombStride]
   static constexpr int kMw = kComb + kCombBufs * kDecRows * kCombStride * 4;  // float [4][16]
   static constexpr int kLw = kMw + kDecWarps * kDecRows * 4; // float [4][16]
   static constexpr int kBars = kLw + kDecWarps * kDecRows * 4;
   static constexpr int kAbort = kBars + 2 * kStages * 8;
-  // self-planned batches: int64 T[kSelfMaxB + 1], int64 meta[8], int cum[kSelfMaxB + 1],
-  // int past[kSelfMaxB]
+  // self-planned batches: int64 T[MB + 1], int64 meta[8], int cum[MB + 1], int past[MB],
+  // MB = self_max_b(HS)
   static constexpr int kSelf = (kAbort + 16 + 15) / 16 * 16;
-  static constexpr int kSelfBytes = !SELF ? 0 : ((kSelfMaxB + 1 + 8) * 8 + (2 * kSelfMaxB + 1) * 4 + 15) / 16 * 16;
+  static constexpr int kSelfBytes =
+      !SELF ? 0 : ((self_max_b(HS) + 1 + 8) * 8 + (2 * self_max_b(HS) + 1) * 4 + 15) / 16 * 16;
   static constexpr int kBytes = kSelf + kSelfBytes + 1024;   // + alignment slack
 };
 static_assert(DecSmem<256>::kBytes <= 232448 && 2 * (DecSmem<128>::kBytes + 1024) <= 233472 &&
@@ -259,7 +267,8 @@ static_assert(DecSmem<256>::kBytes <= 232448 && 2 * (DecSmem<128>::kBytes + 1024
                   2 * (DecSmem<128, 1>::kBytes + 1024) <= 233472 && 2 * (DecSmem<128, 2>::kBytes + 1024) <= 233472 &&
                   2 * (DecSmem<128, 0, true>::kBytes + 1024) <= 233472 &&
                   2 * (DecSmem<128, 1, true>::kBytes + 1024) <= 233472 &&
-                  2 * (DecSmem<128, 2, true>::kBytes + 1024) <= 233472,
+                  2 * (DecSmem<128, 2, true>::kBytes + 1024) <= 233472 && DecSmem<256, 0, true>::kBytes <= 232448 &&
+                  DecSmem<256, 1, true>::kBytes <= 232448 && DecSmem<256, 2, true>::kBytes <= 232448,
               "decode shared memory");
 
 // Prefill: Q tile, two K and two V tiles, barriers, the TMEM address slot.

@@ -56,7 +56,7 @@ __device__ __forceinline__ DecodeItem load_item(const Args& a, int it, int it_en
 }
 
 // ---- decode-only batches planned by the decode kernel itself ----
-// With derived slots, at most kSelfMaxB sequences and a host bound proving every sequence
+// With derived slots, at most self_max_b(HS) sequences and a host bound proving every sequence
 // decode-class, no plan and no cache-write kernel run: each CTA reads the batch description
 // into shared memory (cum[0..B], past[0..B), and T[0..B], the first virtual tile of each
 // sequence's units), cuts the same balanced partition as the planner (unit (b, g) spans
@@ -72,12 +72,14 @@ struct SelfView {
   int64_t* meta;
 };
 
+template <int HS>
 __device__ __forceinline__ SelfView self_view(uint8_t* base) {
+  constexpr int MB = self_max_b(HS);
   SelfView v;
-  v.T = reinterpret_cast<int64_t*>(base);                // kSelfMaxB + 1
-  v.meta = v.T + (kSelfMaxB + 1);                         // 6 (8 reserved)
-  v.cum = reinterpret_cast<int*>(v.meta + 8);             // kSelfMaxB + 1
-  v.past = v.cum + (kSelfMaxB + 1);                       // kSelfMaxB
+  v.T = reinterpret_cast<int64_t*>(base);                // MB + 1
+  v.meta = v.T + (MB + 1);                                // 6 (8 reserved)
+  v.cum = reinterpret_cast<int*>(v.meta + 8);             // MB + 1
+  v.past = v.cum + (MB + 1);                              // MB
   return v;
 }
 
@@ -161,8 +163,8 @@ __device__ void self_plan_prologue(const Args& a, const SelfView& v) {
   for (int b = tid; b <= B; b += blockDim.x) v.cum[b] = a.cum[b];
   for (int b = tid; b < B; b += blockDim.x) v.past[b] = a.past[b];
   __syncthreads();
-  if (tid < 32) {  // one warp: each lane sums the spans of kSelfMaxB / 32 sequences, then a scan
-    constexpr int PER = kSelfMaxB / 32;
+  if (tid < 32) {  // one warp: each lane sums the spans of self_max_b / 32 sequences, then a scan
+    constexpr int PER = self_max_b(HS) / 32;
     int64_t span[PER], sum = 0;
     bool bad = false;
 #pragma unroll
@@ -452,7 +454,7 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
   // releases it only once all earlier work of the stream is done, and only the batch
   // description is read); the wait is then for the reset of the merge counters
   constexpr bool self = SELF;
-  const SelfView sv = self_view(smem + L::kSelf);
+  const SelfView sv = self_view<HS>(smem + L::kSelf);
   if constexpr (SELF) self_plan_prologue<HS>(a, sv);
   if (!beside_prefill) pdl_wait();
   pdl_launch_dependents();
@@ -1058,7 +1060,7 @@ cudaError_t launch_decode_prep(const Args& a, cudaStream_t s) {
 template <int HS, bool BF16, int KQ, bool SELF = false>
 static cudaError_t launch_decode_t(const Args& a, const CUtensorMap& tk, const CUtensorMap& tv, int seg,
                                    cudaStream_t s) {
-  if constexpr (HS != 256 && !SELF) {  // self-planned decode-only batches: their own instantiation
+  if constexpr (!SELF) {  // self-planned decode-only batches: their own instantiation
     if (a.self_plan) return launch_decode_t<HS, BF16, KQ, true>(a, tk, tv, seg, s);
   }
   constexpr int smem = DecSmem<HS, KQ, SELF>::kBytes;
