@@ -185,7 +185,7 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
                      cudaStream_t stream) {
   DeviceInfo info;
   if (!device_info(&info)) return cuda_fail(cudaGetLastError(), "device query");
-  args.dec_ctas = std::min(pa::dec_ctas_per_sm(args.hs) * info.sms, pa::kMaxDecCtas);
+  args.dec_ctas = std::min(pa::dec_ctas_per_sm(args.hs, args.kvq) * info.sms, pa::kMaxDecCtas);
   args.sms = info.sms;
   // The program of a call (which kernels, on which SMs) follows from its arguments alone;
   // `stages` only picks which of its kernels this call launches. A call with prefill-class

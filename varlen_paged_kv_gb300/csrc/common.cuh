@@ -20,8 +20,12 @@ constexpr int kDecStages = 3;         // decode K/V ring depth
 constexpr int kDecWarps = 4;          // decode consumer warps (16 keys of a tile each)
 constexpr int kDecRows = 16;          // query rows per decode work item (one m16 MMA tile)
 constexpr int kDecCtasPerSm = 2;      // resident decode CTAs per SM (shared-memory bound), head_size <= 128
-// head_size 256: a 3-stage ring of 64-key K and V tiles is 192 KB, one CTA per SM
-__host__ __device__ constexpr int dec_ctas_per_sm(int hs) { return hs == 256 ? 1 : kDecCtasPerSm; }
+// head_size 256: a 3-stage ring of 64-key K and V tiles is 192 KB, one CTA per SM. Integer
+// caches below 256: three (their tiles are half or a quarter of the bytes, and the codes'
+// conversion is latency-bound, so a third CTA's warps hide more of it)
+__host__ __device__ constexpr int dec_ctas_per_sm(int hs, int kq = 0) {
+  return hs == 256 ? 1 : kq ? 3 : kDecCtasPerSm;
+}
 // What an item costs a decode CTA beyond streaming its keys (the warps' combine, the write
 // of the row or partial, the merge, the refill of the ring at the next item), in 64-key
 // tiles streamed in the same time (measured: about 5 us per item against 1.4 us per tile
@@ -240,13 +244,16 @@ struct DecSmem {
   static constexpr int kRowBytes = KQ == 0 ? HS * 2 : KQ == 1 ? HS : HS / 2;
   static constexpr int kBoxBytes = kRowBytes < 128 ? kRowBytes : 128;
   static constexpr int kBoxes = kRowBytes / kBoxBytes;
-  static constexpr int kStages = KQ == 0 ? kDecStages : KQ == 1 ? 2 * kDecStages : 4 * kDecStages;
   // (the self-planned 256-wide INT4 kernel, whose ring is deepest, gives its second buffer's
   // room to the batch view)
   static constexpr int kCombBufs = HS == 256 && !(SELF && KQ == 2) ? 2 : 1;
   static constexpr int kHalves = HS / 64;
   static constexpr int kTileBytes = kDecTile * kRowBytes;   // one K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;
+  // ring depth: kDecStages stages on fp16 caches; integer caches fill the same 192 KB at
+  // head_size 256 (one CTA per SM) and 48 KB below (three CTAs per SM)
+  static constexpr int kStages =
+      KQ == 0 ? kDecStages : (HS == 256 ? 3 * 65536 : 3 * 16384) / kStageBytes;
   // floats; the pad spreads rows over banks (2 for the self-planned 256-wide kernel, whose
   // batch view takes the last bytes of shared memory)
   static constexpr int kCombStride = HS + (HS == 256 && SELF ? 2 : 4);
@@ -260,14 +267,20 @@ struct DecSmem {
   static constexpr int kSelf = (kAbort + 16 + 15) / 16 * 16;
   static constexpr int kSelfBytes =
       !SELF ? 0 : ((self_max_b(HS) + 1 + 8) * 8 + (2 * self_max_b(HS) + 1) * 4 + 15) / 16 * 16;
-  static constexpr int kBytes = kSelf + kSelfBytes + 1024;   // + alignment slack
+  // integer caches at three CTAs per SM: the item's Q' fragments in shared memory
+  // (uint4 [HS / 16][32], k-step by lane), not in registers
+  static constexpr bool kQSmem = KQ != 0 && HS <= 128;
+  static constexpr int kQ = kSelf + kSelfBytes;
+  static constexpr int kQBytes = kQSmem ? HS / 16 * 32 * 16 : 0;
+  static constexpr int kBytes = kQ + kQBytes + 1024;   // + alignment slack
 };
 static_assert(DecSmem<256>::kBytes <= 232448 && 2 * (DecSmem<128>::kBytes + 1024) <= 233472 &&
                   DecSmem<256, 1>::kBytes <= 232448 && DecSmem<256, 2>::kBytes <= 232448 &&
-                  2 * (DecSmem<128, 1>::kBytes + 1024) <= 233472 && 2 * (DecSmem<128, 2>::kBytes + 1024) <= 233472 &&
+                  3 * (DecSmem<128, 1>::kBytes + 1024) <= 233472 && 3 * (DecSmem<128, 2>::kBytes + 1024) <= 233472 &&
                   2 * (DecSmem<128, 0, true>::kBytes + 1024) <= 233472 &&
-                  2 * (DecSmem<128, 1, true>::kBytes + 1024) <= 233472 &&
-                  2 * (DecSmem<128, 2, true>::kBytes + 1024) <= 233472 && DecSmem<256, 0, true>::kBytes <= 232448 &&
+                  3 * (DecSmem<128, 1, true>::kBytes + 1024) <= 233472 &&
+                  3 * (DecSmem<128, 2, true>::kBytes + 1024) <= 233472 &&
+                  3 * (DecSmem<64, 1, true>::kBytes + 1024) <= 233472 && DecSmem<256, 0, true>::kBytes <= 232448 &&
                   DecSmem<256, 1, true>::kBytes <= 232448 && DecSmem<256, 2, true>::kBytes <= 232448,
               "decode shared memory");
 

@@ -373,8 +373,9 @@ __device__ __forceinline__ int out_channel(int d, int n) {
 }
 
 // Q' fragments (the scaled query rows, fp16, in the channel order above) of an item and the
-// softmax constants of its two rows: scale * log2(e) * 2^E (E the row's exponent)
-template <int HS, int KQ>
+// softmax constants of its two rows: scale * log2(e) * 2^E (E the row's exponent). Without
+// LOAD_Q only the constants.
+template <int HS, int KQ, bool LOAD_Q = true>
 __device__ __forceinline__ void load_q_int(const Args& a, const DecodeItem& item, int r0, int r1, int tq,
                                            uint32_t (&qa)[HS / 16][4], float& c0, float& c1) {
   const int n_rows = item.q_len * a.G;
@@ -392,30 +393,34 @@ __device__ __forceinline__ void load_q_int(const Args& a, const DecodeItem& item
   }
   c0 = ldexpf(a.scale_log2, ex[0]);
   c1 = ldexpf(a.scale_log2, ex[1]);
+  if constexpr (LOAD_Q) {
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    if constexpr (KQ == 1) {
+    for (int i = 0; i < 2; ++i) {
+      if constexpr (KQ == 1) {
 #pragma unroll
-      for (int ks = 0; ks < HS / 16; ++ks) {
-        const uint2 v = p[i] ? __ldg(reinterpret_cast<const uint2*>(p[i] + (HS / 4) * tq + 4 * ks)) : make_uint2(0, 0);
-        qa[ks][i] = v.x;
-        qa[ks][2 + i] = v.y;
-      }
-    } else {
+        for (int ks = 0; ks < HS / 16; ++ks) {
+          const uint2 v =
+              p[i] ? __ldg(reinterpret_cast<const uint2*>(p[i] + (HS / 4) * tq + 4 * ks)) : make_uint2(0, 0);
+          qa[ks][i] = v.x;
+          qa[ks][2 + i] = v.y;
+        }
+      } else {
 #pragma unroll
-      for (int k2 = 0; k2 < HS / 32; ++k2) {
-        const uint4 v = p[i] ? __ldg(reinterpret_cast<const uint4*>(p[i] + (HS / 4) * tq + 8 * k2)) : make_uint4(0, 0, 0, 0);
-        qa[2 * k2][i] = prmt(v.x, v.z, 0x5410u);
-        qa[2 * k2][2 + i] = prmt(v.x, v.z, 0x7632u);
-        qa[2 * k2 + 1][i] = prmt(v.y, v.w, 0x5410u);
-        qa[2 * k2 + 1][2 + i] = prmt(v.y, v.w, 0x7632u);
+        for (int k2 = 0; k2 < HS / 32; ++k2) {
+          const uint4 v =
+              p[i] ? __ldg(reinterpret_cast<const uint4*>(p[i] + (HS / 4) * tq + 8 * k2)) : make_uint4(0, 0, 0, 0);
+          qa[2 * k2][i] = prmt(v.x, v.z, 0x5410u);
+          qa[2 * k2][2 + i] = prmt(v.x, v.z, 0x7632u);
+          qa[2 * k2 + 1][i] = prmt(v.y, v.w, 0x5410u);
+          qa[2 * k2 + 1][2 + i] = prmt(v.y, v.w, 0x7632u);
+        }
       }
     }
   }
 }
 
 template <int HS, bool BF16, int KQ, bool SELF>
-__global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
+__global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
     decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const int seg_rows) {
   using L = DecSmem<HS, KQ, SELF>;
@@ -426,6 +431,7 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   float* comb = reinterpret_cast<float*>(smem + L::kComb);
+  uint4* qsm = reinterpret_cast<uint4*>(smem + L::kQ);  // (integer caches at three CTAs per SM)
   float* mw = reinterpret_cast<float*>(smem + L::kMw);
   float* lw = reinterpret_cast<float*>(smem + L::kLw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBars);
@@ -578,8 +584,31 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
     const int n_rows = q_len * a.G;
     uint32_t qa[NKS][4];
     float cr0 = a.scale_log2, cr1 = a.scale_log2;  // the two rows' softmax constants
-    if constexpr (KQ == 0) load_q<HS>(a, item, r0, r1, tq, qa);
-    else load_q_int<HS, KQ>(a, item, r0, r1, tq, qa, cr0, cr1);
+    if constexpr (KQ == 0) {
+      load_q<HS>(a, item, r0, r1, tq, qa);
+    } else if constexpr (L::kQSmem) {
+      // the four warps' fragments are the same: warp 0 loads them into shared memory (the
+      // last item's were read before the barrier that closed its key loop)
+      if (w == 0) {
+        load_q_int<HS, KQ>(a, item, r0, r1, tq, qa, cr0, cr1);
+#pragma unroll
+        for (int ks = 0; ks < NKS; ++ks) qsm[ks * 32 + lane] = make_uint4(qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+      } else {
+        load_q_int<HS, KQ, false>(a, item, r0, r1, tq, qa, cr0, cr1);
+      }
+      consumer_bar();
+    } else {
+      load_q_int<HS, KQ>(a, item, r0, r1, tq, qa, cr0, cr1);
+    }
+    // k-step ks of Q' (integer caches)
+    auto qfrag = [&](int ks, uint32_t (&f)[4]) {
+      if constexpr (L::kQSmem) {
+        const uint4 v = qsm[ks * 32 + lane];
+        f[0] = v.x, f[1] = v.y, f[2] = v.z, f[3] = v.w;
+      } else {
+        f[0] = qa[ks][0], f[1] = qa[ks][1], f[2] = qa[ks][2], f[3] = qa[ks][3];
+      }
+    };
     // causal limits (inclusive) of the two rows; padding rows borrow the last row's
     const int lim0 = past + min(r0 / a.G, q_len - 1);
     const int lim1 = past + min(r1 / a.G, q_len - 1);
@@ -620,11 +649,12 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
             lds_run<16>(kb + koff[j] + 8 * P, v);   // key row 16w + gq + 8
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              uint32_t b0, b1, b2, b3;
+              uint32_t b0, b1, b2, b3, f[4];
               s8x4_to_f16_biased(u[i], b0, b1);
               s8x4_to_f16_biased(v[i], b2, b3);
-              mma16816<false>(sc[0], qa[4 * j + i], b0, b1);
-              mma16816<false>(sc[1], qa[4 * j + i], b2, b3);
+              qfrag(4 * j + i, f);
+              mma16816<false>(sc[0], f, b0, b1);
+              mma16816<false>(sc[1], f, b2, b3);
             }
           }
         } else {
@@ -636,13 +666,15 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS))
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int k2 = 4 * j + i;
-              uint32_t uu[4], vv[4];
+              uint32_t uu[4], vv[4], f0[4], f1[4];
               s4x8_to_f16(u[i], uu);
               s4x8_to_f16(v[i], vv);
-              mma16816<false>(sc[0], qa[2 * k2], uu[0], uu[1]);
-              mma16816<false>(sc[0], qa[2 * k2 + 1], uu[2], uu[3]);
-              mma16816<false>(sc[1], qa[2 * k2], vv[0], vv[1]);
-              mma16816<false>(sc[1], qa[2 * k2 + 1], vv[2], vv[3]);
+              qfrag(2 * k2, f0);
+              qfrag(2 * k2 + 1, f1);
+              mma16816<false>(sc[0], f0, uu[0], uu[1]);
+              mma16816<false>(sc[0], f1, uu[2], uu[3]);
+              mma16816<false>(sc[1], f0, vv[0], vv[1]);
+              mma16816<false>(sc[1], f1, vv[2], vv[3]);
             }
           }
         }

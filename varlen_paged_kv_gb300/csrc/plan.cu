@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
   __syncthreads();
   int dec_sms = S;
   if (split) dec_sms = a.decode_sms > 0 ? min(a.decode_sms, S - 1) : (int)(s_split & 0xFFFFFFFFull);
-  const int64_t P = split ? min((int64_t)dec_sms * dec_ctas_per_sm(a.hs), (int64_t)a.dec_ctas) : a.dec_ctas;
+  const int64_t P = split ? min((int64_t)dec_sms * dec_ctas_per_sm(a.hs, a.kvq), (int64_t)a.dec_ctas) : a.dec_ctas;
   const bool balanced = a.forced_split <= 0;
   // The decode units, laid end to end, each as V virtual tiles (the cost of an item beyond
   // its keys) followed by its key tiles, span W tiles; they are cut into P equal ranges:
