@@ -114,8 +114,17 @@ def test_self_planned_decode_partition(lib):
 @pytest.mark.parametrize("fmt", [None, "int4"])
 def test_self_planned_decode_partition_256(lib, fmt):
     p = _prob("cov-self-256", dtype="bf16", num_heads=16, kv_num_heads=2, head_size=256, block_size=16,
-              past=[5000, 3, 700, 0, 2048, 64], q_lens=[1, 2, 1, 1, 3, 1], kv_quant=fmt)
-    check_exactly_once(lib, p, max_q=3)
+              past=[5000, 3, 700, 0, 2048, 64], q_lens=[1, 2, 1, 1, 2, 1], kv_quant=fmt)
+    check_exactly_once(lib, p, max_q=2)
+
+
+@pytest.mark.parametrize("hs,fmt", [(128, "int8"), (128, "int4"), (256, "int8")])
+def test_narrow_decode_partition(lib, hs, fmt):
+    # integer caches, at most 8 rows per item: the transposed (narrow) form of the decode kernel
+    p = _prob("cov-narrow", dtype="fp16", num_heads=16, kv_num_heads=4, head_size=hs, block_size=32,
+              past=[5000, 3, 800, 0, 129], q_lens=[1, 2, 2, 1, 2], kv_quant=fmt)
+    check_exactly_once(lib, p, max_q=2)
+    check_exactly_once(lib, p, max_q=2, split=64)
 
 
 @pytest.mark.parametrize("dsm", [0, 1, 40, 151])

@@ -43,6 +43,13 @@ CASES = {
     "int4-gqa16-bf16": ("int4", "bf16", 16, 1, 128, 64, [500, 1, 2500], [1, 1, 1], False, 0),
     "int4-hs256-fp16": ("int4", "fp16", 16, 2, 256, 32, [129, 63, 1], [2, 1, 1], False, 0),
     "int4-packed-drops-bf16": ("int4", "bf16", 32, 8, 128, 16, [60, 4, 2000], [2, 4, 1], True, 2),
+    # at most 8 query rows per item (q_len * G <= 8): the decode kernel's narrow form
+    "int8-narrow-gqa4-q2-fp16": ("int8", "fp16", 32, 8, 128, 64, [0, 5, 300, 1000, 4097], [1, 2, 1, 2, 1], False, 0),
+    "int8-narrow-gqa8-hs256-bf16": ("int8", "bf16", 16, 2, 256, 32, [700, 3000, 0], [1, 1, 1], False, 0),
+    "int8-narrow-mha-q8-hs64": ("int8", "fp16", 8, 8, 64, 32, [100, 33, 0], [8, 3, 1], False, 0),
+    "int8-narrow-packed-drops": ("int8", "fp16", 32, 8, 128, 64, [900, 50, 3000, 7], [1, 2, 2, 1], True, 2),
+    "int4-narrow-gqa4-q2-bf16": ("int4", "bf16", 32, 8, 128, 16, [60, 4, 2000, 0], [2, 1, 2, 1], False, 0),
+    "int4-narrow-gqa2-q4-hs256": ("int4", "fp16", 8, 4, 256, 64, [129, 63, 1, 500], [4, 1, 3, 2], False, 0),
 }
 
 

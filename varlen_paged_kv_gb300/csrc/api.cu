@@ -209,6 +209,8 @@ pa_status launch_all(pa::Args& args, const pa_dims* d, const void* query, void* 
                          args.forced_split <= 0 && args.B >= 1 && args.B <= pa::self_max_b(hs) && args.N > 0 &&
                          slots > 0;
   const bool self_write_rows = self_plan && !args.prep && !args.kvq;
+  // integer caches with every decode item at most 8 rows: the decode kernel's narrow form
+  args.dec_narrow = args.kvq && d->max_query_len > 0 && (int64_t)d->max_query_len * args.G <= 8;
   args.self_plan = self_plan;  // (the cache-write kernel checks the batch itself)
   if (self_plan) {
     if (stages & PA_STAGE_PLAN) {

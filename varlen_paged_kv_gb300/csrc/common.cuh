@@ -190,6 +190,7 @@ struct Args {
   // the batch description and writes the new K/V rows of the tiles it loads
   int32_t self_plan;
   int32_t self_write_rows;  // self-planned and the decode kernel writes this call's K/V rows
+  int32_t dec_narrow;       // integer caches, every decode item at most 8 query rows (host bound)
   int32_t cw_early;         // bit-copy cache write launched right after this call's planner:
                             // it copies the rows while the planner runs (checking the batch
                             // itself) and waits for the plan only before the fp16 V copy
@@ -711,6 +712,13 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 }
 
 // ---- warp-level tensor core path (decode) -------------------------------------------------
+// the 8 x 8 16-bit matrix held one row pair per thread (thread 4i + j: row i, columns 2j,
+// 2j + 1), transposed
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)

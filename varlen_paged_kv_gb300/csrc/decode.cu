@@ -419,11 +419,46 @@ __device__ __forceinline__ void load_q_int(const Args& a, const DecodeItem& item
   }
 }
 
-template <int HS, bool BF16, int KQ, bool SELF>
+// Items of at most 8 query rows on integer caches ("narrow"): S^T = K Q'^T and
+// O^T += V^T P^T, keys and channels as the MMA rows (M = 16), the query rows as its columns
+// (N = 8), half the MMAs of the row-major form. Q' is the B operand: k-step ks of row gq is
+// the pair of words of q_frags_int's channel order (INT8: channels HS/4 tq + 4 ks .. + 3;
+// INT4: the two pairs its prmt forms). Also the softmax constants of the thread's rows ra, rb.
+template <int HS, int KQ>
+__device__ __forceinline__ void load_q_narrow(const Args& a, const DecodeItem& item, int gq, int ra, int rb,
+                                              int tq, uint32_t (&qb)[HS / 16][2], float& c0, float& c1) {
+  const int n_rows = item.q_len * a.G;
+  const uint16_t* q = reinterpret_cast<const uint16_t*>(a.query);
+  auto qrow = [&](int r) { return (int64_t)(item.c0 + r / a.G) * a.nh + item.g * a.G + r % a.G; };
+  c0 = ldexpf(a.scale_log2, ra < n_rows ? __ldg(a.qexp + qrow(ra)) : 0);
+  c1 = ldexpf(a.scale_log2, rb < n_rows ? __ldg(a.qexp + qrow(rb)) : 0);
+  const uint16_t* p = gq < n_rows ? q + qrow(gq) * HS : nullptr;
+  if constexpr (KQ == 1) {
+#pragma unroll
+    for (int ks = 0; ks < HS / 16; ++ks) {
+      const uint2 v = p ? __ldg(reinterpret_cast<const uint2*>(p + (HS / 4) * tq + 4 * ks)) : make_uint2(0, 0);
+      qb[ks][0] = v.x;
+      qb[ks][1] = v.y;
+    }
+  } else {
+#pragma unroll
+    for (int k2 = 0; k2 < HS / 32; ++k2) {
+      const uint4 v =
+          p ? __ldg(reinterpret_cast<const uint4*>(p + (HS / 4) * tq + 8 * k2)) : make_uint4(0, 0, 0, 0);
+      qb[2 * k2][0] = prmt(v.x, v.z, 0x5410u);
+      qb[2 * k2][1] = prmt(v.x, v.z, 0x7632u);
+      qb[2 * k2 + 1][0] = prmt(v.y, v.w, 0x5410u);
+      qb[2 * k2 + 1][1] = prmt(v.y, v.w, 0x7632u);
+    }
+  }
+}
+
+template <int HS, bool BF16, int KQ, bool SELF, bool NARROW>
 __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
     decode_kernel(const Args a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const int seg_rows) {
   using L = DecSmem<HS, KQ, SELF>;
+  static_assert(!NARROW || KQ != 0, "the narrow form is built for integer caches");
   constexpr int NKS = HS / 16;  // k-steps of Q K^T
   constexpr int P = L::kBoxBytes;
   constexpr int ND = HS / 8;    // n-tiles of P V
@@ -583,9 +618,14 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
     const int c0 = item.c0, q_len = item.q_len, past = item.past;
     const int n_rows = q_len * a.G;
     uint32_t qa[NKS][4];
+    uint32_t qb[NARROW ? NKS : 1][2];  // (narrow items)
     float cr0 = a.scale_log2, cr1 = a.scale_log2;  // the two rows' softmax constants
+    // the thread's two rows: r0, r1 (row-major form), or 2tq, 2tq + 1 (narrow: columns of S^T)
+    const int ra = NARROW ? 2 * tq : r0, rb = NARROW ? 2 * tq + 1 : r1;
     if constexpr (KQ == 0) {
       load_q<HS>(a, item, r0, r1, tq, qa);
+    } else if constexpr (NARROW) {
+      load_q_narrow<HS, KQ>(a, item, gq, ra, rb, tq, qb, cr0, cr1);
     } else if constexpr (L::kQSmem) {
       // the four warps' fragments are the same: warp 0 loads them into shared memory (the
       // last item's were read before the barrier that closed its key loop)
@@ -605,18 +645,19 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
       if constexpr (L::kQSmem) {
         const uint4 v = qsm[ks * 32 + lane];
         f[0] = v.x, f[1] = v.y, f[2] = v.z, f[3] = v.w;
-      } else {
+      } else if constexpr (!NARROW) {
         f[0] = qa[ks][0], f[1] = qa[ks][1], f[2] = qa[ks][2], f[3] = qa[ks][3];
       }
     };
     // causal limits (inclusive) of the two rows; padding rows borrow the last row's
-    const int lim0 = past + min(r0 / a.G, q_len - 1);
-    const int lim1 = past + min(r1 / a.G, q_len - 1);
+    const int lim0 = past + min(ra / a.G, q_len - 1);
+    const int lim1 = past + min(rb / a.G, q_len - 1);
 
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float o[ND][4];
+    constexpr int NO = NARROW ? ND / 2 : ND;  // accumulator tiles: O (16 x 8) or O^T (16 x 8)
+    float o[NO][4];
 #pragma unroll
-    for (int d = 0; d < ND; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
+    for (int d = 0; d < NO; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
 
     for (int k0 = item.key_begin; k0 < item.key_end; k0 += kDecTile) {
       const int s = stage;
@@ -625,208 +666,340 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
       if (kw < item.key_end) {
         const uint32_t kb = smem_u32(smem + s * L::kStageBytes);
         const uint32_t vb = kb + L::kTileBytes;
-        // ---- S (16 x 16) = Q K^T ----
-        float sc[2][4];
+        if constexpr (NARROW) {
+          // ---- S^T (16 keys x 8 rows) = K Q'^T: this thread's keys kw + gq, kw + gq + 8 and
+          // rows ra, rb; even and odd k-steps in two accumulator chains ----
+          float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+          if constexpr (KQ == 1) {
 #pragma unroll
-        for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-        if constexpr (KQ == 0) {
-          const int mi = lane >> 3, rr = lane & 7;
-          const int kr = 16 * w + (mi >> 1) * 8 + rr;  // key row inside the tile
+            for (int j = 0; j < NKS / 4; ++j) {
+              uint32_t u[4], v[4];
+              lds_run<16>(kb + koff[j], u);          // key row 16w + gq
+              lds_run<16>(kb + koff[j] + 8 * P, v);  // key row 16w + gq + 8
 #pragma unroll
-          for (int ks = 0; ks < NKS; ++ks) {
-            const int c = 2 * ks + (mi & 1);             // 16-byte chunk along head_size
-            const uint32_t addr = kb + (c >> 3) * (kDecTile * 128) + kr * 128 + (((c & 7) ^ (kr & 7)) << 4);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(addr, b0, b1, b2, b3);
-            mma16816<BF16>(sc[0], qa[ks], b0, b1);
-            mma16816<BF16>(sc[1], qa[ks], b2, b3);
-          }
-        } else if constexpr (KQ == 1) {
+              for (int i = 0; i < 4; ++i) {
+                uint32_t A[4];
+                s8x4_to_f16_biased(u[i], A[0], A[2]);
+                s8x4_to_f16_biased(v[i], A[1], A[3]);
+                mma16816<false>((i & 1) ? sb : sa, A, qb[4 * j + i][0], qb[4 * j + i][1]);
+              }
+            }
+          } else {
 #pragma unroll
-          for (int j = 0; j < NKS / 4; ++j) {  // 16 bytes of each row: 4 k-steps
-            uint32_t u[4], v[4];
-            lds_run<16>(kb + koff[j], u);           // key row 16w + gq
-            lds_run<16>(kb + koff[j] + 8 * P, v);   // key row 16w + gq + 8
+            for (int j = 0; j < NKS / 8; ++j) {
+              uint32_t u[4], v[4];
+              lds_run<16>(kb + koff[j], u);
+              lds_run<16>(kb + koff[j] + 8 * P, v);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint32_t b0, b1, b2, b3, f[4];
-              s8x4_to_f16_biased(u[i], b0, b1);
-              s8x4_to_f16_biased(v[i], b2, b3);
-              qfrag(4 * j + i, f);
-              mma16816<false>(sc[0], f, b0, b1);
-              mma16816<false>(sc[1], f, b2, b3);
+              for (int i = 0; i < 4; ++i) {
+                const int k2 = 4 * j + i;
+                uint32_t uu[4], vv[4];
+                s4x8_to_f16(u[i], uu);
+                s4x8_to_f16(v[i], vv);
+                const uint32_t A0[4] = {uu[0], vv[0], uu[1], vv[1]}, A1[4] = {uu[2], vv[2], uu[3], vv[3]};
+                mma16816<false>(sa, A0, qb[2 * k2][0], qb[2 * k2][1]);
+                mma16816<false>(sb, A1, qb[2 * k2 + 1][0], qb[2 * k2 + 1][1]);
+              }
             }
           }
-        } else {
-#pragma unroll
-          for (int j = 0; j < NKS / 8; ++j) {  // 16 bytes of each row: 8 k-steps
-            uint32_t u[4], v[4];
-            lds_run<16>(kb + koff[j], u);
-            lds_run<16>(kb + koff[j] + 8 * P, v);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int k2 = 4 * j + i;
-              uint32_t uu[4], vv[4], f0[4], f1[4];
-              s4x8_to_f16(u[i], uu);
-              s4x8_to_f16(v[i], vv);
-              qfrag(2 * k2, f0);
-              qfrag(2 * k2 + 1, f1);
-              mma16816<false>(sc[0], f0, uu[0], uu[1]);
-              mma16816<false>(sc[0], f1, uu[2], uu[3]);
-              mma16816<false>(sc[1], f0, vv[0], vv[1]);
-              mma16816<false>(sc[1], f1, vv[2], vv[3]);
-            }
-          }
-        }
-        // ---- online softmax (base 2) ----
-        const bool ragged = (k0 + kDecTile > item.key_end) || (k0 + kDecTile - 1 > past);
-        float x[2][4];
-#pragma unroll
-        for (int n = 0; n < 2; ++n) {
+          // ---- online softmax (base 2): x[e] is key kw + gq + 8 (e >> 1), row (e & 1 ? rb : ra) ----
+          const bool ragged = (k0 + kDecTile > item.key_end) || (k0 + kDecTile - 1 > past);
+          float x[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            float v = sc[n][e] * (e < 2 ? cr0 : cr1);
+            float v = (sa[e] + sb[e]) * ((e & 1) ? cr1 : cr0);
             if (ragged) {
-              const int key = kw + n * 8 + tq * 2 + (e & 1);
-              const int lim = e < 2 ? lim0 : lim1;
-              if (key >= item.key_end || key > lim) v = -INFINITY;
+              const int key = kw + gq + 8 * (e >> 1);
+              if (key >= item.key_end || key > ((e & 1) ? lim1 : lim0)) v = -INFINITY;
             }
-            x[n][e] = v;
+            x[e] = v;
           }
-        }
 #ifdef PA_COVERAGE
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
-#pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int key = kw + n * 8 + tq * 2 + (e & 1), r = e < 2 ? r0 : r1;
-            const bool in = !(ragged && (key >= item.key_end || key > (e < 2 ? lim0 : lim1)));
+            const int key = kw + gq + 8 * (e >> 1), r = (e & 1) ? rb : ra;
+            const bool in = !(ragged && (key >= item.key_end || key > ((e & 1) ? lim1 : lim0)));
             if (in && r < n_rows) cov_count(a, c0 + r / a.G, item.g * a.G + r % a.G, key);
           }
 #endif
-        float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-        float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float ms0 = mn0 == -INFINITY ? 0.f : mn0;  // a row with no key yet stays empty
-        const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = fast_exp2(m0 - ms0), al1 = fast_exp2(m1 - ms1);
-        m0 = mn0;
-        m1 = mn1;
-        float p[2][4];
+          // the rows' maxima over the warp's 16 keys: the lanes of one tq hold them
+          float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
 #pragma unroll
-        for (int n = 0; n < 2; ++n) {
-          p[n][0] = fast_exp2(x[n][0] - ms0);
-          p[n][1] = fast_exp2(x[n][1] - ms0);
-          p[n][2] = fast_exp2(x[n][2] - ms1);
-          p[n][3] = fast_exp2(x[n][3] - ms1);
-        }
-        // P as the MMA A fragment; bf16 carries it as hi + lo (two products), fp16 as one
-        uint32_t pa[4], pl[4];
-        if constexpr (BF16 && KQ == 0) {
-          split_bf16x2(p[0][0], p[0][1], pa[0], pl[0]);
-          split_bf16x2(p[0][2], p[0][3], pa[1], pl[1]);
-          split_bf16x2(p[1][0], p[1][1], pa[2], pl[2]);
-          split_bf16x2(p[1][2], p[1][3], pa[3], pl[3]);
-        } else {
-          pa[0] = pack2<false>(p[0][0], p[0][1]);
-          pa[1] = pack2<false>(p[0][2], p[0][3]);
-          pa[2] = pack2<false>(p[1][0], p[1][1]);
-          pa[3] = pack2<false>(p[1][2], p[1][3]);
-        }
-        if constexpr (KQ == 1) {
-          // INT8 caches: the V codes enter P V with the conversion's offset (code + 1152), which
-          // the output takes off after dividing by the row sum; that sum must then add exactly
-          // the fp16 weights the MMA multiplies. (At INT4's coarser scales the offset's share of
-          // the tensor core's fp32 rounding shows in the output: INT4 V codes stay exact.)
-          const float2 q0 = __half22float2(*reinterpret_cast<const __half2*>(&pa[0]));
-          const float2 q1 = __half22float2(*reinterpret_cast<const __half2*>(&pa[1]));
-          const float2 q2 = __half22float2(*reinterpret_cast<const __half2*>(&pa[2]));
-          const float2 q3 = __half22float2(*reinterpret_cast<const __half2*>(&pa[3]));
-          l0 = l0 * al0 + ((q0.x + q0.y) + (q2.x + q2.y));
-          l1 = l1 * al1 + ((q1.x + q1.y) + (q3.x + q3.y));
-        } else {
-          l0 = l0 * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-          l1 = l1 * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
-        }
-        if (!__all_sync(0xffffffffu, al0 == 1.f && al1 == 1.f)) {  // (no row's max grew: O stays)
-#pragma unroll
-          for (int d = 0; d < ND; ++d) {
-            o[d][0] *= al0;
-            o[d][1] *= al0;
-            o[d][2] *= al1;
-            o[d][3] *= al1;
+          for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
           }
-        }
-        // ---- O (16 x HS) += P (16 x 16) V (16 x HS) ----
-        // keys this thread contributes in the transposed V fragments: kw + 2tq + {0,1}, +8
-        if constexpr (KQ == 1) {
-          // (codes are finite: keys past the item contribute 0 * code = 0)
-          // this thread's keys: ka = 16w + 2tq, ka + 1 (b0), ka + 8, ka + 9 (b1)
-          constexpr int G = VG;  // channels (bytes) of a run
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+          const float ms0 = mn0 == -INFINITY ? 0.f : mn0;  // a row with no key yet stays empty
+          const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
+          const float al0 = fast_exp2(m0 - ms0), al1 = fast_exp2(m1 - ms1);
+          m0 = mn0;
+          m1 = mn1;
+          // P^T of keys gq and gq + 8, each an fp16 pair (row ra, row rb)
+          const uint32_t h0 = pack2<false>(fast_exp2(x[0] - ms0), fast_exp2(x[1] - ms1));
+          const uint32_t h1 = pack2<false>(fast_exp2(x[2] - ms0), fast_exp2(x[3] - ms1));
+          // the row sums add the fp16 weights the MMA multiplies (see the INT8 note below)
+          const float2 q0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
+          const float2 q1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
+          l0 = l0 * al0 + (q0.x + q1.x);
+          l1 = l1 * al1 + (q0.y + q1.y);
+          if (!__all_sync(0xffffffffu, al0 == 1.f && al1 == 1.f)) {  // (no row's max grew: O stays)
 #pragma unroll
-          for (int D = 0; D < ND / G; ++D) {
-            uint32_t w0[G / 4], w1[G / 4], w8[G / 4], w9[G / 4];
-            lds_run<G>(vb + voff[0][D], w0);
-            lds_run<G>(vb + voff[1][D], w1);
-            lds_run<G>(vb + voff[0][D] + 8 * P, w8);
-            lds_run<G>(vb + voff[1][D] + 8 * P, w9);
-#pragma unroll
-            for (int i = 0; i < G / 4; ++i) {
-              uint32_t lo[4], hi[4];
-              s8_key_pairs_biased(w0[i], w1[i], lo);
-              s8_key_pairs_biased(w8[i], w9[i], hi);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) mma16816<false>(o[D * G + 4 * i + e], pa, lo[e], hi[e]);
+            for (int d = 0; d < NO; ++d) {
+              o[d][0] *= al0;
+              o[d][1] *= al1;
+              o[d][2] *= al0;
+              o[d][3] *= al1;
             }
           }
-        } else if constexpr (KQ == 2) {
-          constexpr int R = VG;  // bytes of the thread's HS / 8 channels in a key row
-          uint32_t w0[R / 4], w1[R / 4], w8[R / 4], w9[R / 4];
-          lds_run<R>(vb + voff[0][0], w0);
-          lds_run<R>(vb + voff[1][0], w1);
-          lds_run<R>(vb + voff[0][0] + 8 * P, w8);
-          lds_run<R>(vb + voff[1][0] + 8 * P, w9);
+          // ---- O^T (16 channels x 8 rows per tile) += V^T P^T: the B operand is P (rows x
+          // keys), the two 8 x 8 blocks of P^T transposed; the A operand pairs the channel
+          // columns d, d + 1 of the row-major form (rows gq and gq + 8 of O^T tile d / 2) ----
+          const uint32_t pb0 = movmatrix_trans(h0), pb1 = movmatrix_trans(h1);
+          if constexpr (KQ == 1) {
+            constexpr int G = VG;
 #pragma unroll
-          for (int i = 0; i < R / 4; ++i) {
-            uint32_t lo[8], hi[8];
-            s4_key_pairs(w0[i], w1[i], lo);
-            s4_key_pairs(w8[i], w9[i], hi);
+            for (int D = 0; D < ND / G; ++D) {
+              uint32_t w0[G / 4], w1[G / 4], w8[G / 4], w9[G / 4];
+              lds_run<G>(vb + voff[0][D], w0);
+              lds_run<G>(vb + voff[1][D], w1);
+              lds_run<G>(vb + voff[0][D] + 8 * P, w8);
+              lds_run<G>(vb + voff[1][D] + 8 * P, w9);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) mma16816<false>(o[8 * i + e], pa, lo[e], hi[e]);
-          }
-        } else {
-          const int mi = lane >> 3, rr = lane & 7;
-          const int kr = 16 * w + (mi & 1) * 8 + rr;
-          // keys past the item may be unwritten cache slots: on the item's last tile their V
-          // is cleared, so that no NaN reaches 0 * V (the other tiles skip the masking)
-          auto pv = [&](uint32_t mlo, uint32_t mhi) {
+              for (int i = 0; i < G / 4; ++i) {
+                uint32_t lo[4], hi[4];
+                s8_key_pairs_biased(w0[i], w1[i], lo);
+                s8_key_pairs_biased(w8[i], w9[i], hi);
 #pragma unroll
-            for (int dp = 0; dp < ND / 2; ++dp) {
-              const int c = 2 * dp + (mi >> 1);
-              const uint32_t addr = vb + (c >> 3) * (kDecTile * 128) + kr * 128 + (((c & 7) ^ (kr & 7)) << 4);
-              uint32_t v0, v1, v2, v3;
-              ldsm_x4_t(addr, v0, v1, v2, v3);
-              v0 &= mlo;
-              v2 &= mlo;
-              v1 &= mhi;
-              v3 &= mhi;
-              mma16816<BF16>(o[2 * dp], pa, v0, v1);
-              mma16816<BF16>(o[2 * dp + 1], pa, v2, v3);
-              if constexpr (BF16) {
-                mma16816<BF16>(o[2 * dp], pl, v0, v1);
-                mma16816<BF16>(o[2 * dp + 1], pl, v2, v3);
+                for (int e = 0; e < 4; e += 2) {
+                  const uint32_t A[4] = {lo[e], lo[e + 1], hi[e], hi[e + 1]};
+                  mma16816<false>(o[(D * G + 4 * i + e) / 2], A, pb0, pb1);
+                }
               }
             }
-          };
-          const int ka = kw + tq * 2, kb2 = ka + 8;
-          const uint32_t mlo = (ka < item.key_end ? 0x0000ffffu : 0u) | (ka + 1 < item.key_end ? 0xffff0000u : 0u);
-          const uint32_t mhi = (kb2 < item.key_end ? 0x0000ffffu : 0u) | (kb2 + 1 < item.key_end ? 0xffff0000u : 0u);
-          if (HS == 256 || k0 + kDecTile > item.key_end) pv(mlo, mhi);  // (one copy of the loop at 256)
-          else pv(0xffffffffu, 0xffffffffu);
+          } else {
+            constexpr int R = VG;
+            uint32_t w0[R / 4], w1[R / 4], w8[R / 4], w9[R / 4];
+            lds_run<R>(vb + voff[0][0], w0);
+            lds_run<R>(vb + voff[1][0], w1);
+            lds_run<R>(vb + voff[0][0] + 8 * P, w8);
+            lds_run<R>(vb + voff[1][0] + 8 * P, w9);
+#pragma unroll
+            for (int i = 0; i < R / 4; ++i) {
+              uint32_t lo[8], hi[8];
+              s4_key_pairs(w0[i], w1[i], lo);
+              s4_key_pairs(w8[i], w9[i], hi);
+#pragma unroll
+              for (int e = 0; e < 8; e += 2) {
+                const uint32_t A[4] = {lo[e], lo[e + 1], hi[e], hi[e + 1]};
+                mma16816<false>(o[(8 * i + e) / 2], A, pb0, pb1);
+              }
+            }
+          }
+        } else {
+          // ---- S (16 x 16) = Q K^T ----
+          float sc[2][4];
+  #pragma unroll
+          for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+          if constexpr (KQ == 0) {
+            const int mi = lane >> 3, rr = lane & 7;
+            const int kr = 16 * w + (mi >> 1) * 8 + rr;  // key row inside the tile
+  #pragma unroll
+            for (int ks = 0; ks < NKS; ++ks) {
+              const int c = 2 * ks + (mi & 1);             // 16-byte chunk along head_size
+              const uint32_t addr = kb + (c >> 3) * (kDecTile * 128) + kr * 128 + (((c & 7) ^ (kr & 7)) << 4);
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4(addr, b0, b1, b2, b3);
+              mma16816<BF16>(sc[0], qa[ks], b0, b1);
+              mma16816<BF16>(sc[1], qa[ks], b2, b3);
+            }
+          } else if constexpr (KQ == 1) {
+  #pragma unroll
+            for (int j = 0; j < NKS / 4; ++j) {  // 16 bytes of each row: 4 k-steps
+              uint32_t u[4], v[4];
+              lds_run<16>(kb + koff[j], u);           // key row 16w + gq
+              lds_run<16>(kb + koff[j] + 8 * P, v);   // key row 16w + gq + 8
+  #pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                uint32_t b0, b1, b2, b3, f[4];
+                s8x4_to_f16_biased(u[i], b0, b1);
+                s8x4_to_f16_biased(v[i], b2, b3);
+                qfrag(4 * j + i, f);
+                mma16816<false>(sc[0], f, b0, b1);
+                mma16816<false>(sc[1], f, b2, b3);
+              }
+            }
+          } else {
+  #pragma unroll
+            for (int j = 0; j < NKS / 8; ++j) {  // 16 bytes of each row: 8 k-steps
+              uint32_t u[4], v[4];
+              lds_run<16>(kb + koff[j], u);
+              lds_run<16>(kb + koff[j] + 8 * P, v);
+  #pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int k2 = 4 * j + i;
+                uint32_t uu[4], vv[4], f0[4], f1[4];
+                s4x8_to_f16(u[i], uu);
+                s4x8_to_f16(v[i], vv);
+                qfrag(2 * k2, f0);
+                qfrag(2 * k2 + 1, f1);
+                mma16816<false>(sc[0], f0, uu[0], uu[1]);
+                mma16816<false>(sc[0], f1, uu[2], uu[3]);
+                mma16816<false>(sc[1], f0, vv[0], vv[1]);
+                mma16816<false>(sc[1], f1, vv[2], vv[3]);
+              }
+            }
+          }
+          // ---- online softmax (base 2) ----
+          const bool ragged = (k0 + kDecTile > item.key_end) || (k0 + kDecTile - 1 > past);
+          float x[2][4];
+  #pragma unroll
+          for (int n = 0; n < 2; ++n) {
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float v = sc[n][e] * (e < 2 ? cr0 : cr1);
+              if (ragged) {
+                const int key = kw + n * 8 + tq * 2 + (e & 1);
+                const int lim = e < 2 ? lim0 : lim1;
+                if (key >= item.key_end || key > lim) v = -INFINITY;
+              }
+              x[n][e] = v;
+            }
+          }
+  #ifdef PA_COVERAGE
+  #pragma unroll
+          for (int n = 0; n < 2; ++n)
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int key = kw + n * 8 + tq * 2 + (e & 1), r = e < 2 ? r0 : r1;
+              const bool in = !(ragged && (key >= item.key_end || key > (e < 2 ? lim0 : lim1)));
+              if (in && r < n_rows) cov_count(a, c0 + r / a.G, item.g * a.G + r % a.G, key);
+            }
+  #endif
+          float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+          float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+          const float ms0 = mn0 == -INFINITY ? 0.f : mn0;  // a row with no key yet stays empty
+          const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
+          const float al0 = fast_exp2(m0 - ms0), al1 = fast_exp2(m1 - ms1);
+          m0 = mn0;
+          m1 = mn1;
+          float p[2][4];
+  #pragma unroll
+          for (int n = 0; n < 2; ++n) {
+            p[n][0] = fast_exp2(x[n][0] - ms0);
+            p[n][1] = fast_exp2(x[n][1] - ms0);
+            p[n][2] = fast_exp2(x[n][2] - ms1);
+            p[n][3] = fast_exp2(x[n][3] - ms1);
+          }
+          // P as the MMA A fragment; bf16 carries it as hi + lo (two products), fp16 as one
+          uint32_t pa[4], pl[4];
+          if constexpr (BF16 && KQ == 0) {
+            split_bf16x2(p[0][0], p[0][1], pa[0], pl[0]);
+            split_bf16x2(p[0][2], p[0][3], pa[1], pl[1]);
+            split_bf16x2(p[1][0], p[1][1], pa[2], pl[2]);
+            split_bf16x2(p[1][2], p[1][3], pa[3], pl[3]);
+          } else {
+            pa[0] = pack2<false>(p[0][0], p[0][1]);
+            pa[1] = pack2<false>(p[0][2], p[0][3]);
+            pa[2] = pack2<false>(p[1][0], p[1][1]);
+            pa[3] = pack2<false>(p[1][2], p[1][3]);
+          }
+          if constexpr (KQ == 1) {
+            // INT8 caches: the V codes enter P V with the conversion's offset (code + 1152), which
+            // the output takes off after dividing by the row sum; that sum must then add exactly
+            // the fp16 weights the MMA multiplies. (At INT4's coarser scales the offset's share of
+            // the tensor core's fp32 rounding shows in the output: INT4 V codes stay exact.)
+            const float2 q0 = __half22float2(*reinterpret_cast<const __half2*>(&pa[0]));
+            const float2 q1 = __half22float2(*reinterpret_cast<const __half2*>(&pa[1]));
+            const float2 q2 = __half22float2(*reinterpret_cast<const __half2*>(&pa[2]));
+            const float2 q3 = __half22float2(*reinterpret_cast<const __half2*>(&pa[3]));
+            l0 = l0 * al0 + ((q0.x + q0.y) + (q2.x + q2.y));
+            l1 = l1 * al1 + ((q1.x + q1.y) + (q3.x + q3.y));
+          } else {
+            l0 = l0 * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+            l1 = l1 * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+          }
+          if (!__all_sync(0xffffffffu, al0 == 1.f && al1 == 1.f)) {  // (no row's max grew: O stays)
+  #pragma unroll
+            for (int d = 0; d < ND; ++d) {
+              o[d][0] *= al0;
+              o[d][1] *= al0;
+              o[d][2] *= al1;
+              o[d][3] *= al1;
+            }
+          }
+          // ---- O (16 x HS) += P (16 x 16) V (16 x HS) ----
+          // keys this thread contributes in the transposed V fragments: kw + 2tq + {0,1}, +8
+          if constexpr (KQ == 1) {
+            // (codes are finite: keys past the item contribute 0 * code = 0)
+            // this thread's keys: ka = 16w + 2tq, ka + 1 (b0), ka + 8, ka + 9 (b1)
+            constexpr int G = VG;  // channels (bytes) of a run
+  #pragma unroll
+            for (int D = 0; D < ND / G; ++D) {
+              uint32_t w0[G / 4], w1[G / 4], w8[G / 4], w9[G / 4];
+              lds_run<G>(vb + voff[0][D], w0);
+              lds_run<G>(vb + voff[1][D], w1);
+              lds_run<G>(vb + voff[0][D] + 8 * P, w8);
+              lds_run<G>(vb + voff[1][D] + 8 * P, w9);
+  #pragma unroll
+              for (int i = 0; i < G / 4; ++i) {
+                uint32_t lo[4], hi[4];
+                s8_key_pairs_biased(w0[i], w1[i], lo);
+                s8_key_pairs_biased(w8[i], w9[i], hi);
+  #pragma unroll
+                for (int e = 0; e < 4; ++e) mma16816<false>(o[D * G + 4 * i + e], pa, lo[e], hi[e]);
+              }
+            }
+          } else if constexpr (KQ == 2) {
+            constexpr int R = VG;  // bytes of the thread's HS / 8 channels in a key row
+            uint32_t w0[R / 4], w1[R / 4], w8[R / 4], w9[R / 4];
+            lds_run<R>(vb + voff[0][0], w0);
+            lds_run<R>(vb + voff[1][0], w1);
+            lds_run<R>(vb + voff[0][0] + 8 * P, w8);
+            lds_run<R>(vb + voff[1][0] + 8 * P, w9);
+  #pragma unroll
+            for (int i = 0; i < R / 4; ++i) {
+              uint32_t lo[8], hi[8];
+              s4_key_pairs(w0[i], w1[i], lo);
+              s4_key_pairs(w8[i], w9[i], hi);
+  #pragma unroll
+              for (int e = 0; e < 8; ++e) mma16816<false>(o[8 * i + e], pa, lo[e], hi[e]);
+            }
+          } else {
+            const int mi = lane >> 3, rr = lane & 7;
+            const int kr = 16 * w + (mi & 1) * 8 + rr;
+            // keys past the item may be unwritten cache slots: on the item's last tile their V
+            // is cleared, so that no NaN reaches 0 * V (the other tiles skip the masking)
+            auto pv = [&](uint32_t mlo, uint32_t mhi) {
+  #pragma unroll
+              for (int dp = 0; dp < ND / 2; ++dp) {
+                const int c = 2 * dp + (mi >> 1);
+                const uint32_t addr = vb + (c >> 3) * (kDecTile * 128) + kr * 128 + (((c & 7) ^ (kr & 7)) << 4);
+                uint32_t v0, v1, v2, v3;
+                ldsm_x4_t(addr, v0, v1, v2, v3);
+                v0 &= mlo;
+                v2 &= mlo;
+                v1 &= mhi;
+                v3 &= mhi;
+                mma16816<BF16>(o[2 * dp], pa, v0, v1);
+                mma16816<BF16>(o[2 * dp + 1], pa, v2, v3);
+                if constexpr (BF16) {
+                  mma16816<BF16>(o[2 * dp], pl, v0, v1);
+                  mma16816<BF16>(o[2 * dp + 1], pl, v2, v3);
+                }
+              }
+            };
+            const int ka = kw + tq * 2, kb2 = ka + 8;
+            const uint32_t mlo = (ka < item.key_end ? 0x0000ffffu : 0u) | (ka + 1 < item.key_end ? 0xffff0000u : 0u);
+            const uint32_t mhi = (kb2 < item.key_end ? 0x0000ffffu : 0u) | (kb2 + 1 < item.key_end ? 0xffff0000u : 0u);
+            if (HS == 256 || k0 + kDecTile > item.key_end) pv(mlo, mhi);  // (one copy of the loop at 256)
+            else pv(0xffffffffu, 0xffffffffu);
+          }
         }
       }
       __syncwarp();
@@ -838,86 +1011,135 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
     }
 
     // ---- combine the four warps' partial states in a fixed order ----
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    if (tq == 0) {
-      mw[w * kDecRows + r0] = m0;
-      mw[w * kDecRows + r1] = m1;
-      lw[w * kDecRows + r0] = l0;
-      lw[w * kDecRows + r1] = l1;
-    }
-    consumer_bar();
-    float M0, L0, M1, L1;
-    row_stats(mw, lw, r0, M0, L0);
-    row_stats(mw, lw, r1, M1, L1);
-    const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M0);
-    const float f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M1);
-    // An item of at most kDecRows / kDecWarps rows (one decode token of up to four heads): the
-    // four warps' rows fit the buffer side by side, warp w's at rows 4w .. 4w + 3, so they
-    // are written in one round and the write below adds them in warp order (the order, and
-    // so the rounding, of the rounds).
     constexpr int kCompactRows = kDecRows / kDecWarps;
-    const bool compact = L::kCombBufs == 1 && n_rows <= kCompactRows;
-    if (compact) {
-      if (gq < kCompactRows) {
-        if constexpr (KQ == 0) {
-          float* cw = comb + (w * kCompactRows + r0) * kCombStride + tq * 2;
-#pragma unroll
-          for (int d = 0; d < ND; ++d)
-            *reinterpret_cast<float2*>(cw + d * 8) = make_float2(o[d][0] * f0, o[d][1] * f0);
-        } else {  // integer caches: the columns' channels in natural order
-          float* cw = comb + (w * kCompactRows + r0) * kCombStride;
-#pragma unroll
-          for (int d = 0; d < ND; ++d) {
-            cw[out_channel<HS, KQ>(d, 2 * tq)] = o[d][0] * f0;
-            cw[out_channel<HS, KQ>(d, 2 * tq + 1)] = o[d][1] * f0;
-          }
-        }
+    bool compact = false;  // (row-major form, items of at most kCompactRows rows)
+    if constexpr (NARROW) {
+      // the rows' sums over the warp's keys (the lanes of one tq), then the row states
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 4);
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 8);
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 16);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 4);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 8);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 16);
+      if (gq == 0) {
+        mw[w * kDecRows + ra] = m0;
+        mw[w * kDecRows + rb] = m1;
+        lw[w * kDecRows + ra] = l0;
+        lw[w * kDecRows + rb] = l1;
       }
       consumer_bar();
-    } else {
-      // round rr: warps rr * B .. rr * B + B - 1 write (first round) or add their partials
-      // into buffers 0 .. B - 1; buffer b ends up holding warps b, b + B, ... in that order
-      constexpr int B = L::kCombBufs;
-      float* cw = comb + (w % B) * (kDecRows * kCombStride);
+      float M0, L0, M1, L1;
+      row_stats(mw, lw, ra, M0, L0);
+      row_stats(mw, lw, rb, M1, L1);
+      const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M0);
+      const float f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M1);
+      // warps 0 and 1 write rows 0 .. 7 and 8 .. 15 of the buffer, then warps 2 and 3 add
+      // theirs; the write below adds the two halves (the order, and so the rounding, fixed)
+      float* cw = comb + (w & 1) * 8 * kCombStride;
 #pragma unroll 1
-      for (int rr = 0; rr < kDecWarps / B; ++rr) {
-        if (w / B == rr) {
+      for (int rr = 0; rr < 2; ++rr) {
+        if ((w >> 1) == rr) {
+          float* pa0 = cw + ra * kCombStride;
+          float* pa1 = cw + rb * kCombStride;
 #pragma unroll
-          for (int d = 0; d < ND; ++d) {
-            if constexpr (KQ == 0) {
-              float2* c0p = reinterpret_cast<float2*>(cw + r0 * kCombStride + d * 8 + tq * 2);
-              float2* c1p = reinterpret_cast<float2*>(cw + r1 * kCombStride + d * 8 + tq * 2);
-              const float2 a0 = make_float2(o[d][0] * f0, o[d][1] * f0), a1 = make_float2(o[d][2] * f1, o[d][3] * f1);
-              if (rr == 0) {
-                *c0p = a0;
-                *c1p = a1;
-              } else {
-                const float2 b0 = *c0p, b1 = *c1p;
-                *c0p = make_float2(b0.x + a0.x, b0.y + a0.y);
-                *c1p = make_float2(b1.x + a1.x, b1.y + a1.y);
-              }
-            } else {  // integer caches: the columns' channels in natural order
-              const int ch0 = out_channel<HS, KQ>(d, 2 * tq), ch1 = out_channel<HS, KQ>(d, 2 * tq + 1);
-              float* c0p = cw + r0 * kCombStride;
-              float* c1p = cw + r1 * kCombStride;
-              if (rr == 0) {
-                c0p[ch0] = o[d][0] * f0;
-                c0p[ch1] = o[d][1] * f0;
-                c1p[ch0] = o[d][2] * f1;
-                c1p[ch1] = o[d][3] * f1;
-              } else {
-                c0p[ch0] += o[d][0] * f0;
-                c0p[ch1] += o[d][1] * f0;
-                c1p[ch0] += o[d][2] * f1;
-                c1p[ch1] += o[d][3] * f1;
-              }
+          for (int d = 0; d < NO; ++d) {
+            const int ch0 = out_channel<HS, KQ>(2 * d, gq), ch1 = out_channel<HS, KQ>(2 * d + 1, gq);
+            if (rr == 0) {
+              pa0[ch0] = o[d][0] * f0;
+              pa1[ch0] = o[d][1] * f1;
+              pa0[ch1] = o[d][2] * f0;
+              pa1[ch1] = o[d][3] * f1;
+            } else {
+              pa0[ch0] += o[d][0] * f0;
+              pa1[ch0] += o[d][1] * f1;
+              pa0[ch1] += o[d][2] * f0;
+              pa1[ch1] += o[d][3] * f1;
             }
           }
         }
         consumer_bar();
+      }
+    } else {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+      if (tq == 0) {
+        mw[w * kDecRows + r0] = m0;
+        mw[w * kDecRows + r1] = m1;
+        lw[w * kDecRows + r0] = l0;
+        lw[w * kDecRows + r1] = l1;
+      }
+      consumer_bar();
+      float M0, L0, M1, L1;
+      row_stats(mw, lw, r0, M0, L0);
+      row_stats(mw, lw, r1, M1, L1);
+      const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M0);
+      const float f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M1);
+      // An item of at most kDecRows / kDecWarps rows (one decode token of up to four heads): the
+      // four warps' rows fit the buffer side by side, warp w's at rows 4w .. 4w + 3, so they
+      // are written in one round and the write below adds them in warp order (the order, and
+      // so the rounding, of the rounds).
+      compact = L::kCombBufs == 1 && n_rows <= kCompactRows;
+      if (compact) {
+        if (gq < kCompactRows) {
+          if constexpr (KQ == 0) {
+            float* cw = comb + (w * kCompactRows + r0) * kCombStride + tq * 2;
+  #pragma unroll
+            for (int d = 0; d < ND; ++d)
+              *reinterpret_cast<float2*>(cw + d * 8) = make_float2(o[d][0] * f0, o[d][1] * f0);
+          } else {  // integer caches: the columns' channels in natural order
+            float* cw = comb + (w * kCompactRows + r0) * kCombStride;
+  #pragma unroll
+            for (int d = 0; d < ND; ++d) {
+              cw[out_channel<HS, KQ>(d, 2 * tq)] = o[d][0] * f0;
+              cw[out_channel<HS, KQ>(d, 2 * tq + 1)] = o[d][1] * f0;
+            }
+          }
+        }
+        consumer_bar();
+      } else {
+        // round rr: warps rr * B .. rr * B + B - 1 write (first round) or add their partials
+        // into buffers 0 .. B - 1; buffer b ends up holding warps b, b + B, ... in that order
+        constexpr int B = L::kCombBufs;
+        float* cw = comb + (w % B) * (kDecRows * kCombStride);
+  #pragma unroll 1
+        for (int rr = 0; rr < kDecWarps / B; ++rr) {
+          if (w / B == rr) {
+  #pragma unroll
+            for (int d = 0; d < ND; ++d) {
+              if constexpr (KQ == 0) {
+                float2* c0p = reinterpret_cast<float2*>(cw + r0 * kCombStride + d * 8 + tq * 2);
+                float2* c1p = reinterpret_cast<float2*>(cw + r1 * kCombStride + d * 8 + tq * 2);
+                const float2 a0 = make_float2(o[d][0] * f0, o[d][1] * f0), a1 = make_float2(o[d][2] * f1, o[d][3] * f1);
+                if (rr == 0) {
+                  *c0p = a0;
+                  *c1p = a1;
+                } else {
+                  const float2 b0 = *c0p, b1 = *c1p;
+                  *c0p = make_float2(b0.x + a0.x, b0.y + a0.y);
+                  *c1p = make_float2(b1.x + a1.x, b1.y + a1.y);
+                }
+              } else {  // integer caches: the columns' channels in natural order
+                const int ch0 = out_channel<HS, KQ>(d, 2 * tq), ch1 = out_channel<HS, KQ>(d, 2 * tq + 1);
+                float* c0p = cw + r0 * kCombStride;
+                float* c1p = cw + r1 * kCombStride;
+                if (rr == 0) {
+                  c0p[ch0] = o[d][0] * f0;
+                  c0p[ch1] = o[d][1] * f0;
+                  c1p[ch0] = o[d][2] * f1;
+                  c1p[ch1] = o[d][3] * f1;
+                } else {
+                  c0p[ch0] += o[d][0] * f0;
+                  c0p[ch1] += o[d][1] * f0;
+                  c1p[ch0] += o[d][2] * f1;
+                  c1p[ch1] += o[d][3] * f1;
+                }
+              }
+            }
+          }
+          consumer_bar();
+        }
       }
     }
     // ---- write: thread t owns row t / 8, HS / 8 consecutive columns ----
@@ -938,6 +1160,7 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
       // partials added in warp order
       auto cval = [&](int v) {
         float x = src[v];
+        if constexpr (NARROW) return x + src[8 * kCombStride + v];
         if (compact) {  // (row < kCompactRows)
 #pragma unroll
           for (int ww = 1; ww < kDecWarps; ++ww) x += src[ww * kCompactRows * kCombStride + v];
@@ -1089,17 +1312,20 @@ cudaError_t launch_decode_prep(const Args& a, cudaStream_t s) {
   return launch_pdl(decode_prep_kernel, dim3(1), dim3(256), 0, s, a);
 }
 
-template <int HS, bool BF16, int KQ, bool SELF = false>
+template <int HS, bool BF16, int KQ, bool SELF = false, bool NARROW = false>
 static cudaError_t launch_decode_t(const Args& a, const CUtensorMap& tk, const CUtensorMap& tv, int seg,
                                    cudaStream_t s) {
   if constexpr (!SELF) {  // self-planned decode-only batches: their own instantiation
-    if (a.self_plan) return launch_decode_t<HS, BF16, KQ, true>(a, tk, tv, seg, s);
+    if (a.self_plan) return launch_decode_t<HS, BF16, KQ, true, NARROW>(a, tk, tv, seg, s);
+  }
+  if constexpr (KQ != 0 && !NARROW) {  // items of at most 8 rows on integer caches
+    if (a.dec_narrow) return launch_decode_t<HS, BF16, KQ, SELF, true>(a, tk, tv, seg, s);
   }
   constexpr int smem = DecSmem<HS, KQ, SELF>::kBytes;
   cudaError_t e =
-      cudaFuncSetAttribute(decode_kernel<HS, BF16, KQ, SELF>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      cudaFuncSetAttribute(decode_kernel<HS, BF16, KQ, SELF, NARROW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_kernel<HS, BF16, KQ, SELF>, dim3(a.dec_ctas), dim3(160), smem, s, a, tk, tv, seg);
+  return launch_pdl(decode_kernel<HS, BF16, KQ, SELF, NARROW>, dim3(a.dec_ctas), dim3(160), smem, s, a, tk, tv, seg);
 }
 
 template <int KQ>
