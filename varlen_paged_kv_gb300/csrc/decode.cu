@@ -64,7 +64,7 @@ __device__ __forceinline__ DecodeItem load_item(const Args& a, int it, int it_en
 // tiles [floor(c W / P), floor((c + 1) W / P))) and generates its items in order. The new
 // K/V rows of a tile are written by the CTA that loads the tile, just before the load.
 // meta: [0] R0, [1] R1 (this CTA's tiles), [2] W, [3] first candidate sequence, [4] its
-// first candidate head, [5] nonzero for a refused batch, [6] this CTA's items, [7] W / P.
+// first candidate head, [5] nonzero for a refused batch, [7] W / P ([6] unused).
 struct SelfView {
   int* cum;
   int* past;
@@ -219,14 +219,6 @@ __device__ void self_plan_prologue(const Args& a, const SelfView& v) {
     v.meta[3] = lo;
     v.meta[4] = g0;
     v.meta[7] = wq;
-    int count = 0;  // this CTA's items
-    if (!v.meta[5]) {
-      SelfGen<HS> gen(v);
-      DecodeItem d;
-      int slot;
-      while (gen.next(a, v, d, slot)) ++count;
-    }
-    v.meta[6] = count;
   }
   __syncthreads();
 }
@@ -507,8 +499,9 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
     if (beside_prefill) pdl_wait();
     return;
   }
+  // the planner's items [it_begin, it_end), or (self-planned) the generator's until it ends
   const int it_begin = self ? 0 : a.cta_begin[blockIdx.x];
-  const int it_end = self ? (int)sv.meta[6] : a.cta_begin[blockIdx.x + 1];
+  const int it_end = self ? 0 : a.cta_begin[blockIdx.x + 1];
 
   if (warp == kDecWarps) {
     // ================= producer warp: TMA page loads =================
@@ -522,13 +515,15 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
     SelfGen<HS> gen(sv);  // (self-planned batches)
     int next_slot = 0;
     DecodeItem next;
-    if constexpr (SELF) gen.next(a, sv, next, next_slot);
-    else next = load_item(a, it_begin, it_end);
-    for (int it = it_begin; it < it_end; ++it) {
+    bool more;
+    if constexpr (SELF) more = gen.next(a, sv, next, next_slot);
+    else more = it_begin < it_end, next = load_item(a, it_begin, it_end);
+    for (int it = it_begin; more; ++it) {
       const DecodeItem item = next;  // loaded one item ahead
       if constexpr (SELF) {
-        if (it + 1 < it_end) gen.next(a, sv, next, next_slot);
+        more = gen.next(a, sv, next, next_slot);
       } else {
+        more = it + 1 < it_end;
         next = load_item(a, it + 1, it_end);
       }
       {
@@ -605,14 +600,16 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
   SelfGen<HS> gen(sv);  // (self-planned batches)
   int next_slot = 0;
   DecodeItem next;
-  if constexpr (SELF) gen.next(a, sv, next, next_slot);
-  else next = load_item(a, it_begin, it_end);
-  for (int it_i = it_begin; it_i < it_end; ++it_i) {
+  bool more;
+  if constexpr (SELF) more = gen.next(a, sv, next, next_slot);
+  else more = it_begin < it_end, next = load_item(a, it_begin, it_end);
+  for (int it_i = it_begin; more; ++it_i) {
     const DecodeItem item = next;  // loaded one item ahead
     const int it = SELF ? next_slot : it_i;  // the slot of this item's partial result
     if constexpr (SELF) {
-      if (it_i + 1 < it_end) gen.next(a, sv, next, next_slot);
+      more = gen.next(a, sv, next, next_slot);
     } else {
+      more = it_i + 1 < it_end;
       next = load_item(a, it_i + 1, it_end);
     }
     const int c0 = item.c0, q_len = item.q_len, past = item.past;
