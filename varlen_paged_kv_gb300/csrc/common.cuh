@@ -310,9 +310,9 @@ struct PreSmem {
 };
 
 // ---- programmatic dependent launch ---------------------------------------------------------
-// Every kernel is launched so that it may start while its predecessor in the stream is still
-// finishing: its launch and prologue (barrier set-up, TMEM allocation) overlap the
-// predecessor's tail. Each kernel calls pdl_wait() on every path before it first touches
+// Every kernel (but the prefill kernels on integer caches, see launch_prefill_t) is launched
+// so that it may start while its predecessor in the stream is still finishing: its launch
+// and prologue (barrier set-up, TMEM allocation) overlap the predecessor's tail. Each kernel calls pdl_wait() on every path before it first touches
 // memory that an earlier kernel reads or writes; that wait returns once the predecessor has
 // completed and its writes are visible, and since the predecessor waited for its own
 // predecessor, completion is transitive along the stream. pdl_launch_dependents() lets the
@@ -322,9 +322,12 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// A launch that may start before the previous kernel of the stream finishes (programmatic
+// dependent launch): its blocks wait (griddepcontrol.wait) for that kernel's results. With
+// pdl false an ordinary launch: the kernel starts once the previous one has finished.
 template <typename... KArgs, typename... Actual>
-inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                              Actual&&... args) {
+inline cudaError_t launch_pdl_if(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t s, Actual&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -334,8 +337,13 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Actual&&>(args)...);
+}
+template <typename... KArgs, typename... Actual>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Actual&&... args) {
+  return launch_pdl_if(true, kernel, grid, block, smem, s, static_cast<Actual&&>(args)...);
 }
 
 // ---- the prefill kernels' persistent unit order ----

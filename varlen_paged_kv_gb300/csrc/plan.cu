@@ -797,6 +797,112 @@ __device__ void quant_unit(const Args& a, int tok, int64_t pos, int64_t slot, in
   quant_row<HS, KQ>(a, vrow + g * HS, a.v_scale + g * HS, vdst + g * RB, lane, false, t.wk, t);
 }
 
+// Integer caches without the Q/K preparation, in wider tasks: a task covers 256 values of
+// one token, 8 per lane (one 16-byte load): 256 / HS consecutive query heads (scaled by the
+// K scales of their KV heads and written as fp16 with a power-of-two row exponent, as in
+// quant_unit) or 256 / HS consecutive KV heads' K and V rows (written as codes). A token's
+// tasks are its query tasks, then its KV tasks; the last of each kind may cover fewer heads.
+// Split into the loads and the rest, so that a warp keeps two tasks' loads in flight.
+template <int HS, int KQ>
+struct QuantTask {
+  static constexpr int LPH = HS / 8;    // lanes per head row
+  static constexpr int RPW = 32 / LPH;  // head rows per task
+  int tok, h;                            // this lane's head (query or KV)
+  bool kv, active;
+  int64_t slot;
+  uint4 x, y;  // this lane's 8 query values, or 8 K and 8 V values
+
+  __device__ __forceinline__ void load(const Args& a, int tok_, int u, int QT, int64_t slot_, int lane) {
+    tok = tok_;
+    kv = u >= QT;
+    h = (kv ? u - QT : u) * RPW + lane / LPH;
+    slot = slot_;
+    const uint16_t* qrow = reinterpret_cast<const uint16_t*>(a.query) + (int64_t)tok * a.q_stride;
+    const int off = h * HS + (lane % LPH) * 8;
+    if (!kv) {
+      active = h < a.nh;
+      if (active) x = __ldg(reinterpret_cast<const uint4*>(qrow + off));
+    } else {
+      active = h < a.kvh && slot >= 0;
+      if (active) {
+        const uint16_t* krow = a.packed ? qrow + a.k_offset
+                                        : reinterpret_cast<const uint16_t*>(a.key) + (int64_t)tok * a.kv_row;
+        const uint16_t* vrow = a.packed ? qrow + a.v_offset
+                                        : reinterpret_cast<const uint16_t*>(a.value) + (int64_t)tok * a.kv_row;
+        x = __ldg(reinterpret_cast<const uint4*>(krow + off));
+        y = __ldg(reinterpret_cast<const uint4*>(vrow + off));
+      }
+    }
+  }
+
+  static __device__ __forceinline__ void pair_f32(uint32_t w, bool bf16, float& lo, float& hi) {
+    if (bf16) {
+      lo = __uint_as_float(w << 16);
+      hi = __uint_as_float(w & 0xFFFF0000u);
+    } else {
+      lo = __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
+      hi = __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+    }
+  }
+  static __device__ __forceinline__ void to_f32(uint4 w, bool bf16, float (&v)[8]) {
+    pair_f32(w.x, bf16, v[0], v[1]);
+    pair_f32(w.y, bf16, v[2], v[3]);
+    pair_f32(w.z, bf16, v[4], v[5]);
+    pair_f32(w.w, bf16, v[6], v[7]);
+  }
+  static __device__ __forceinline__ void scales8(const float* p, float (&s)[8]) {
+    const float4 s0 = __ldg(reinterpret_cast<const float4*>(p)), s1 = __ldg(reinterpret_cast<const float4*>(p + 4));
+    s[0] = s0.x, s[1] = s0.y, s[2] = s0.z, s[3] = s0.w, s[4] = s1.x, s[5] = s1.y, s[6] = s1.z, s[7] = s1.w;
+  }
+
+  // (the whole warp: the query rows' maxima are reduced across each head's lanes)
+  __device__ __forceinline__ void finish(const Args& a, int lane) {
+    const bool bf16 = a.bf16 != 0;
+    const int c0 = (lane % LPH) * 8;  // this lane's first channel
+    if (!kv) {
+      float v[8], sc[8];
+      to_f32(active ? x : make_uint4(0, 0, 0, 0), bf16, v);
+      scales8(a.k_scale + (active ? (h / a.G) * HS : 0) + c0, sc);
+      float m = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        v[e] *= sc[e];
+        m = fmaxf(m, fabsf(v[e]));
+      }
+#pragma unroll
+      for (int o = 1; o < LPH; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (!active) return;
+      const uint32_t mb = __float_as_uint(m);
+      const int ex = !(m > 0.f && m <= 3.4028234e38f) ? 0 : mb >= 0x00800000u ? (int)(mb >> 23) - 127 - 14 : ilogbf(m) - 14;
+      const int n0 = -ex / 2, n1 = -ex - n0;
+      const float s0 = __uint_as_float((uint32_t)(n0 + 127) << 23), s1 = __uint_as_float((uint32_t)(n1 + 127) << 23);
+      uint32_t wds[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) wds[k] = pack2<false>(v[2 * k] * s0 * s1, v[2 * k + 1] * s0 * s1);
+      *reinterpret_cast<uint4*>(a.qprep + ((int64_t)tok * a.nh + h) * HS + c0) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+      if (lane % LPH == 0) a.qexp[(int64_t)tok * a.nh + h] = ex;
+      return;
+    }
+    if (!active) return;
+    constexpr int RB = KQ == 1 ? HS : HS / 2;  // bytes of one KV head's code row
+    const float qmax = KQ == 1 ? 127.f : 7.f;
+    float v[8], sc[8];
+    int c[8];
+    to_f32(x, bf16, v);
+    scales8(a.k_scale + h * HS + c0, sc);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) c[e] = quant_code(v[e], sc[e], qmax);
+    uint8_t* kdst = reinterpret_cast<uint8_t*>(a.key_cache) + (slot * a.kvh + h) * RB + c0 * RB / HS;
+    store_codes<8, KQ>(kdst, c);
+    to_f32(y, bf16, v);
+    scales8(a.v_scale + h * HS + c0, sc);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) c[e] = quant_code(v[e], sc[e], qmax);
+    uint8_t* vdst = reinterpret_cast<uint8_t*>(a.value_cache) + (slot * a.kvh + h) * RB + c0 * RB / HS;
+    store_codes<8, KQ>(vdst, c);
+  }
+};
+
 // The slot of token tok (slot_mapping[tok], or its logical position through block_table),
 // -1 for a suppressed write or an out-of-range block or slot (those also flagged: in the
 // error word, or with DEFER in errs, which the caller adds to the word once the planner has
@@ -851,6 +957,36 @@ __device__ __forceinline__ int64_t resolve_slot(const Args& a, int tok, bool nee
     slot = -1;
   }
   return slot;
+}
+
+// A warp's contiguous run of the QuantTask list (the tokens' query tasks, then their KV
+// tasks), two tasks at a time: both loads are issued before either task is finished. The
+// token's slot is resolved once, when the run reaches the token.
+template <int HS, int KQ>
+__device__ void quant_tasks(const Args& a, int gw, int warps, int lane, uint32_t& errs) {
+  using QT_ = QuantTask<HS, KQ>;
+  const int QT = (a.nh + QT_::RPW - 1) / QT_::RPW, KT = (a.kvh + QT_::RPW - 1) / QT_::RPW, T = QT + KT;
+  const int64_t total = (int64_t)a.N * T;
+  const int64_t per = (total + warps - 1) / warps;
+  const int64_t w0 = (int64_t)gw * per, w1 = min(total, w0 + per);
+  int b = 0, cur = -1;
+  int64_t pos = 0, slot = -1;
+  auto start = [&](QT_& t, int64_t wj) {
+    const int tok = (int)(wj / T), u = (int)(wj - (int64_t)tok * T);
+    if (tok != cur) {
+      cur = tok;
+      slot = resolve_slot(a, tok, false, b, pos, errs);
+    }
+    t.load(a, tok, u, QT, slot, lane);
+  };
+  for (int64_t wi = w0; wi < w1; wi += 2) {
+    const bool two = wi + 1 < w1;
+    QT_ t0, t1;
+    start(t0, wi);
+    if (two) start(t1, wi + 1);
+    t0.finish(a, lane);
+    if (two) t1.finish(a, lane);
+  }
 }
 
 // The first row of sequence b in the fp16 V copy, worked out by a warp as the planner lays
@@ -946,6 +1082,17 @@ __global__ void __launch_bounds__(256, 4) cache_write_kernel(const Args a) {
       }
       if (__syncthreads_or(bad)) return;
     }
+  }
+  if constexpr (MODE == 2) {  // integer caches without the preparation: the wider tasks
+    if (a.kvq == 1) {
+      if (a.hs == 128) quant_tasks<128, 1>(a, gw, warps, lane, errs);
+      else if (a.hs == 256) quant_tasks<256, 1>(a, gw, warps, lane, errs);
+      else quant_tasks<64, 1>(a, gw, warps, lane, errs);
+    } else {
+      if (a.hs == 128) quant_tasks<128, 2>(a, gw, warps, lane, errs);
+      else quant_tasks<256, 2>(a, gw, warps, lane, errs);
+    }
+    return;
   }
   if constexpr (!COPY) {
     int b = 0;
@@ -1106,7 +1253,9 @@ cudaError_t launch_plan(const Args& a, cudaStream_t s) {
 cudaError_t launch_cache_write(const Args& a, int sms, cudaStream_t s) {
   // a warp per token (bit copy) or per (token, unit): one resident wave of 8-warp blocks
   // (four per SM at 64 registers), each warp looping over its share
-  const int64_t warps = (int64_t)a.N * ((a.kvq || a.prep) ? a.nh + a.kvh : 1);
+  // (integer caches without the preparation: tasks of 256 values, two per warp at a time)
+  const int64_t warps = a.kvq && !a.prep ? ((int64_t)a.N * ((a.nh + a.kvh) * a.hs + 255) / 256 + 1) / 2
+                                         : (int64_t)a.N * ((a.kvq || a.prep) ? a.nh + a.kvh : 1);
   const int grid = (int)std::min<int64_t>((warps + 7) / 8, (int64_t)sms * 4);
   if (a.kvq) return launch_pdl(a.prep ? cache_write_kernel<3> : cache_write_kernel<2>, dim3(grid), dim3(256), 0, s, a);
   if (a.prep) return launch_pdl(cache_write_kernel<1>, dim3(grid), dim3(256), 0, s, a);

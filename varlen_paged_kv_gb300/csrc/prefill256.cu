@@ -574,7 +574,9 @@ cudaError_t launch_t(const Args& a, const CUtensorMap& tq, const CUtensorMap& tk
   cudaError_t e =
       cudaFuncSetAttribute(prefill256_kernel<BF16, KQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(prefill256_kernel<BF16, KQ>, dim3(grid), dim3(kThreads), smem, s, a, tq, tk, tv, tvm, seg);
+  // (integer caches: after the quantizing cache write has finished, as the 128-wide kernel)
+  return launch_pdl_if(KQ == 0, prefill256_kernel<BF16, KQ>, dim3(grid), dim3(kThreads), smem, s, a, tq, tk, tv,
+                       tvm, seg);
 }
 
 template <int KQ>
