@@ -326,14 +326,16 @@ class Runner:
 # the figure is reported only while the sources are unchanged, else traffic is null.
 # ("decode_kernel_self": the self-planned instantiation that decode-only steps run.)
 NCU_TRAFFIC = {
-    ("decode_kernel_self", "decode-b64"): (618578432 + 4103424, "ec414d405b7637a0"),
-    ("decode_kernel_self", "long-decode-b8-bs16"): (2279043584 + 3350272, "ec414d405b7637a0"),
-    ("decode_kernel_self", "decode-b64-int8"): (309909248 + 3940352, "ec414d405b7637a0"),
-    ("decode_kernel_self", "decode-b64-int4"): (155559424 + 3653888, "ec414d405b7637a0"),
-    ("prefill_kernel", "causal-prefill-4x2048"): (104697856 + 31982848, "653c243942d368cb"),
-    # the two attention kernels of a mixed step (prefill 193.2 + 15.7 MB, decode 775.9 + 0.5 MB)
-    ("prefill_kernel+decode_kernel", "mixed-8x512-chunks+24-decode"): (193237248 + 15672832 + 775852800 + 464384,
-                                                                        "9e22602355205d7b"),
+    ("decode_kernel_self", "decode-b64"): (618592000 + 4575744, "82ee04b0eb7dfff2"),
+    ("decode_kernel_self", "long-decode-b8-bs16"): (2279083776 + 3449088, "82ee04b0eb7dfff2"),
+    ("decode_kernel_self", "decode-b64-int8"): (310146560 + 3822592, "82ee04b0eb7dfff2"),
+    ("decode_kernel_self", "decode-b64-int4"): (155715584 + 3701760, "82ee04b0eb7dfff2"),
+    ("decode_kernel_self", "decode-b64-hs256"): (295606528 + 4131328, "82ee04b0eb7dfff2"),
+    ("prefill_kernel", "causal-prefill-4x2048"): (104478720 + 31718912, "8f0b518ec5af374f"),
+    ("prefill256_kernel", "causal-prefill-hs256"): (84037632 + 26018048, "7b964e02da23c06b"),
+    # the two attention kernels of a mixed step (prefill 188.7 + 15.1 MB, decode 775.7 + 0.6 MB)
+    ("prefill_kernel+decode_kernel", "mixed-8x512-chunks+24-decode"): (188687360 + 15142912 + 775707904 + 643328,
+                                                                        "18685b97e7e59d62"),
 }
 KERNEL_SOURCES = {"decode_kernel": ("decode.cu", "common.cuh"), "decode_kernel_self": ("decode.cu", "common.cuh"),
                   "prefill_kernel": ("prefill.cu", "common.cuh"), "prefill256_kernel": ("prefill256.cu", "common.cuh"),
