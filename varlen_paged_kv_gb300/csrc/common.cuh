@@ -483,6 +483,15 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
   return old;
 }
 
+__device__ __forceinline__ void red_add_release_gpu(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // x[0..7] times sigmoid of the 8 gate values (T) at g (16-byte aligned): x / (1 + e^-gate)
 template <bool BF16>
 __device__ __forceinline__ void apply_gate8(const uint16_t* g, float* x) {
@@ -553,6 +562,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // barrier `id` (1..15) among `count` threads (a multiple of 32)
+// Wait until the counter at p reaches need (acquire at gpu scope), at most ~2 s: on time-out
+// (or when another thread of the CTA already gave up, *abort != 0) it sets *abort and the
+// PA_DEVERR_TIMEOUT bit and returns false.
+__device__ __forceinline__ bool wait_count_acquire_gpu(const int* p, int need, volatile int* abort, uint32_t* err) {
+  if (ld_acquire_gpu(p) >= need) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(p) >= need) return true;
+    if ((it & 15) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        atomicOr(err, PA_DEVERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }

@@ -1197,34 +1197,56 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
           }
         }
       } else {
-        if (mine) {
-          float* pdst = a.part_o + ((int64_t)it * kDecRows + row) * HS + col;
+        // A unit the balanced partition cuts has its pieces in different CTAs: the first
+        // piece (keys from 0) is the last item of its CTA, the others are the first items of
+        // the next CTAs (or a later CTA's whole range). The first piece's CTA merges, once the
+        // others have arrived (by then they usually have: they were done early), from its own
+        // combine buffer and their partials; the others publish their partials and move on.
+        // With forced split lengths a CTA may hold several pieces of one unit: there the last
+        // piece to finish merges.
+        const bool balanced = a.forced_split <= 0;
+        const bool merger = balanced && item.key_begin == 0;
+        int* done = &a.unit_done[item.b * a.kvh + item.g];
+        const float own_lse = Lr > 0.f ? (M + fast_log2(Lr)) * 0.69314718055994531f : -INFINITY;
+        if (!merger) {
+          if (mine) {
+            float* pdst = a.part_o + ((int64_t)it * kDecRows + row) * HS + col;
 #pragma unroll
-          for (int v = 0; v < CW; v += 4)
-            *reinterpret_cast<float4*>(pdst + v) =
-                make_float4(cval(v) * inv, cval(v + 1) * inv, cval(v + 2) * inv, cval(v + 3) * inv);
-          if ((t & 7) == 0)
-            a.part_lse[(int64_t)it * kDecRows + row] =
-                Lr > 0.f ? (M + fast_log2(Lr)) * 0.69314718055994531f : -INFINITY;
+            for (int v = 0; v < CW; v += 4)
+              *reinterpret_cast<float4*>(pdst + v) =
+                  make_float4(cval(v) * inv, cval(v + 1) * inv, cval(v + 2) * inv, cval(v + 3) * inv);
+            if ((t & 7) == 0) a.part_lse[(int64_t)it * kDecRows + row] = own_lse;
+          }
+          consumer_bar();  // every consumer thread's partial is written
+          if (t == 0) {
+            // at gpu scope after the barrier: the release publishes the CTA's partial
+            // (cumulative over the writes the barrier ordered before it); with forced splits
+            // the acquire also orders the merge's reads of the other items' partials
+            if (balanced) red_add_release_gpu(done, 1);
+            else *s_last = atom_add_acq_rel_gpu(done, 1) == item.n_split - 1;
+          }
+          if (!balanced) consumer_bar();
+        } else {
+          // (acquire at gpu scope, then the barrier: the reads below follow the arrivals)
+          if (t == 0) *s_last = wait_count_acquire_gpu(done, item.n_split - 1, abort, err);
+          consumer_bar();
         }
-        consumer_bar();  // every consumer thread's partial is written
-        if (t == 0) {
-          // acq_rel at gpu scope after the barrier: the release publishes the CTA's partial
-          // (cumulative over the writes the barrier ordered before it), the acquire orders the
-          // merge's reads of the other items' partials after their arrivals
-          *s_last = atom_add_acq_rel_gpu(&a.unit_done[item.b * a.kvh + item.g], 1) == item.n_split - 1;
-        }
-        consumer_bar();
-        if (*s_last && mine) {
-          // the unit's other items have all arrived: merge its partials in key order, two
-          // pieces per step with a running max (both pieces' lse and rows are loaded together,
-          // one L2 round trip per step: this merge usually ends the CTA's work)
+        if ((merger || !balanced) && *s_last && mine) {
+          // merge the unit's pieces in key order with a running max: the merger's own piece
+          // from its combine buffer, then the partials two per step (both pieces' lse and rows
+          // loaded together, one L2 round trip per step: this merge usually ends the CTA's work)
           float Mx = -INFINITY;
           float acc[CW];
+          float den = 0.f;
 #pragma unroll
           for (int v = 0; v < CW; ++v) acc[v] = 0.f;
-          float den = 0.f;
-          for (int s2 = 0; s2 < item.n_split; s2 += 2) {
+          if (merger && own_lse != -INFINITY) {
+            Mx = own_lse;
+            den = 1.f;
+#pragma unroll
+            for (int v = 0; v < CW; ++v) acc[v] = cval(v) * inv;
+          }
+          for (int s2 = merger ? 1 : 0; s2 < item.n_split; s2 += 2) {
             const bool two = s2 + 1 < item.n_split;
             const int64_t pa = (int64_t)piece_slot<SELF>(item, s2) * kDecRows + row;
             const int64_t pb = two ? (int64_t)piece_slot<SELF>(item, s2 + 1) * kDecRows + row : pa;
