@@ -312,8 +312,9 @@ struct PreSmem {
 // ---- programmatic dependent launch ---------------------------------------------------------
 // Every kernel (but the prefill kernels on integer caches, see launch_prefill_t) is launched
 // so that it may start while its predecessor in the stream is still finishing: its launch
-// and prologue (barrier set-up, TMEM allocation) overlap the predecessor's tail. Each kernel calls pdl_wait() on every path before it first touches
-// memory that an earlier kernel reads or writes; that wait returns once the predecessor has
+// and prologue (barrier set-up, TMEM allocation) overlap the predecessor's tail. Each kernel
+// calls pdl_wait() on every path before it first touches memory that an earlier kernel
+// reads or writes; that wait returns once the predecessor has
 // completed and its writes are visible, and since the predecessor waited for its own
 // predecessor, completion is transitive along the stream. pdl_launch_dependents() lets the
 // next kernel launch (its CTAs then sit in their own pdl_wait until this grid completes).
