@@ -126,6 +126,33 @@ def test_integer_cache_decode(name, split):
 
 
 @pytest.mark.parametrize("fmt", ["int8", "int4"])
+def test_codes_at_and_next_to_ties(fmt):
+    # a code is rint (ties to even) of the correctly rounded quotient value / scale: new K and
+    # V values at exact half-integer multiples of power-of-two scales (past the saturation
+    # too), and a third of them one fp16 unit in the last place away on either side
+    p = w.make_problem(name="ties", seed=41, dtype="fp16", num_heads=8, kv_num_heads=2, head_size=128,
+                       block_size=16, past=[20, 7, 300], q_lens=[40, 30, 1], kv_quant=fmt)
+    qm = 127 if fmt == "int8" else 7
+    rng = np.random.default_rng(5)
+    kvh, hs, n = p.kv_num_heads, p.head_size, p.num_tokens
+    p.k_scale = (2.0 ** rng.integers(-8, -3, size=(kvh, hs))).astype(np.float32)
+    p.v_scale = (2.0 ** rng.integers(-8, -3, size=(kvh, hs))).astype(np.float32)
+
+    def values(scale):
+        half = rng.integers(-qm - 2, qm + 2, size=(n, kvh, hs)) + 0.5  # exact in fp16 times 2^-8..2^-4
+        bits = oracle.double_to_f16(half * scale[None].astype(np.float64)).reshape(n, kvh * hs)
+        step = rng.integers(-1, 2, size=bits.shape)  # one unit of the magnitude down, none, up
+        return (bits.astype(np.int64) + step).astype(np.uint16)
+
+    p.key = values(p.k_scale)
+    p.value = values(p.v_scale)
+    ref = oracle.paged_attention(p)
+    d, out, lse = _run(p)
+    assert np.array_equal(cache_bytes(d["key_cache"]), ref["key_cache"]), "key codes differ"
+    assert np.array_equal(cache_bytes(d["value_cache"]), ref["value_cache"]), "value codes differ"
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int4"])
 def test_integer_cache_with_prep_and_gate(fmt):
     p = w.make_problem(name="q-prep", seed=33, dtype="bf16", num_heads=16, kv_num_heads=2, head_size=128,
                        block_size=64, past=[100, 2000, 7], q_lens=[1, 2, 1], kv_quant=fmt)
