@@ -655,27 +655,30 @@ __device__ __forceinline__ void s8_key_pairs_biased(uint32_t w0, uint32_t w1, ui
   p[2] = prmt(b, kF16Magic, 0x5140u);
   p[3] = prmt(b, kF16Magic, 0x7362u);
 }
-// eight INT4 codes (nibble j = channel j of w) as the fp16 pairs (0, 4), (1, 5), (2, 6), (3, 7)
-__device__ __forceinline__ void s4x8_to_f16(uint32_t w, uint32_t (&p)[4]) {
+// eight INT4 codes as fp16 subnormals: (code + 8) 2^-24 (the bits of code + 8 as the fp16
+// bits), pairs (0, 4), (1, 5), (2, 6), (3, 7); the decode kernel's form. The offset, 8 units
+// of 2^-24 per channel, is of the codes' own size (so fp32 sums keep it to rounding), and
+// the kernel takes it off the scores' row constant and the output.
+__device__ __forceinline__ void s4x8_to_f16_sub(uint32_t w, uint32_t (&p)[4]) {
   const uint32_t x = w ^ 0x88888888u;
-  p[0] = hsub2_u32(nib_pair_f16(x), kF16Int4Bias);
-  p[1] = hsub2_u32(nib_pair_f16(x >> 4), kF16Int4Bias);
-  p[2] = hsub2_u32(nib_pair_f16(x >> 8), kF16Int4Bias);
-  p[3] = hsub2_u32(nib_pair_f16(x >> 12), kF16Int4Bias);
+  p[0] = x & 0x000F000Fu;
+  p[1] = (x >> 4) & 0x000F000Fu;
+  p[2] = (x >> 8) & 0x000F000Fu;
+  p[3] = (x >> 12) & 0x000F000Fu;
 }
-// channel i of w0 and channel i of w1 (two keys, eight INT4 channels each) as one fp16 pair
-__device__ __forceinline__ void s4_key_pairs(uint32_t w0, uint32_t w1, uint32_t (&p)[8]) {
+// channel i of w0 and channel i of w1 (two keys) as one fp16 pair of subnormals (code + 8) 2^-24
+__device__ __forceinline__ void s4_key_pairs_sub(uint32_t w0, uint32_t w1, uint32_t (&p)[8]) {
   const uint32_t x0 = w0 ^ 0x88888888u, x1 = w1 ^ 0x88888888u;
-  const uint32_t a = prmt(x0, x1, 0x6420u);  // bytes: w0 ch0|1, w0 ch4|5, w1 ch0|1, w1 ch4|5
-  const uint32_t b = prmt(x0, x1, 0x7531u);  // bytes: w0 ch2|3, w0 ch6|7, w1 ch2|3, w1 ch6|7
-  p[0] = hsub2_u32(nib_pair_f16(a), kF16Int4Bias);
-  p[1] = hsub2_u32(nib_pair_f16(a >> 4), kF16Int4Bias);
-  p[4] = hsub2_u32(nib_pair_f16(a >> 8), kF16Int4Bias);
-  p[5] = hsub2_u32(nib_pair_f16(a >> 12), kF16Int4Bias);
-  p[2] = hsub2_u32(nib_pair_f16(b), kF16Int4Bias);
-  p[3] = hsub2_u32(nib_pair_f16(b >> 4), kF16Int4Bias);
-  p[6] = hsub2_u32(nib_pair_f16(b >> 8), kF16Int4Bias);
-  p[7] = hsub2_u32(nib_pair_f16(b >> 12), kF16Int4Bias);
+  const uint32_t a = prmt(x0, x1, 0x6420u);
+  const uint32_t b = prmt(x0, x1, 0x7531u);
+  p[0] = a & 0x000F000Fu;
+  p[1] = (a >> 4) & 0x000F000Fu;
+  p[4] = (a >> 8) & 0x000F000Fu;
+  p[5] = (a >> 12) & 0x000F000Fu;
+  p[2] = b & 0x000F000Fu;
+  p[3] = (b >> 4) & 0x000F000Fu;
+  p[6] = (b >> 8) & 0x000F000Fu;
+  p[7] = (b >> 12) & 0x000F000Fu;
 }
 
 // The converter warps' work on one K or V tile of an integer cache: row r's code bytes sit

@@ -223,13 +223,14 @@ __device__ void self_plan_prologue(const Args& a, const SelfView& v) {
   __syncthreads();
 }
 
-// (INT8 caches) The bias of a query row's scores, in natural-log units. INT8 keys enter
-// Q K^T as the fp16 integers code + 1152, which adds 1152 sum_c Q'_c to every score of the
-// row: the softmax, the four warps' combine and the split merge only compare scores and lse
-// of one row and do not see it; the exported lse has it taken off. Eight threads per row
-// (t & 7), each summing HS / 8 values of the scaled query row; all 32 lanes take part.
-template <int HS>
-__device__ __forceinline__ float int8_row_bias(const Args& a, int tok, int head, int t, bool valid) {
+// (integer caches) The bias of a query row's scores, in natural-log units. INT8 keys enter
+// Q K^T as the fp16 integers code + 1152, INT4 keys as the fp16 subnormals (code + 8) 2^-24
+// (the row constant takes the 2^-24 back), which adds 1152 (or 8) sum_c Q'_c to every score
+// of the row: the softmax, the four warps' combine and the split merge only compare scores
+// and lse of one row and do not see it; the exported lse has it taken off. Eight threads per
+// row (t & 7), each summing HS / 8 values of the scaled query row; all 32 lanes take part.
+template <int HS, int KQ>
+__device__ __forceinline__ float key_row_bias(const Args& a, int tok, int head, int t, bool valid) {
   float s = 0.f;
   int e = 0;
   if (valid) {
@@ -250,7 +251,16 @@ __device__ __forceinline__ float int8_row_bias(const Args& a, int tok, int head,
   s += __shfl_xor_sync(0xffffffffu, s, 1);
   s += __shfl_xor_sync(0xffffffffu, s, 2);
   s += __shfl_xor_sync(0xffffffffu, s, 4);
-  return 1152.f * s * ldexpf(a.scale_log2, e) * 0.69314718055994531f;
+  return (KQ == 1 ? 1152.f : 8.f) * s * ldexpf(a.scale_log2, e) * 0.69314718055994531f;
+}
+
+// A V code from the normalised P V of integer caches: the conversion's offset taken off
+// (INT8: code + 1152; INT4: (code + 8) 2^-24)
+template <int KQ>
+__device__ __forceinline__ float v_code_value(float x) {
+  if constexpr (KQ == 1) return x - 1152.f;
+  else if constexpr (KQ == 2) return x * 0x1p24f - 8.f;
+  else return x;
 }
 
 // the partial-result slot of piece s2 of an item's unit
@@ -383,8 +393,9 @@ __device__ __forceinline__ void load_q_int(const Args& a, const DecodeItem& item
       ex[i] = __ldg(a.qexp + row);
     }
   }
-  c0 = ldexpf(a.scale_log2, ex[0]);
-  c1 = ldexpf(a.scale_log2, ex[1]);
+  constexpr int kSub = KQ == 2 ? 24 : 0;  // (INT4 keys as subnormals: 2^-24 per code unit)
+  c0 = ldexpf(a.scale_log2, ex[0] + kSub);
+  c1 = ldexpf(a.scale_log2, ex[1] + kSub);
   if constexpr (LOAD_Q) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -422,8 +433,9 @@ __device__ __forceinline__ void load_q_narrow(const Args& a, const DecodeItem& i
   const int n_rows = item.q_len * a.G;
   const uint16_t* q = reinterpret_cast<const uint16_t*>(a.query);
   auto qrow = [&](int r) { return (int64_t)(item.c0 + r / a.G) * a.nh + item.g * a.G + r % a.G; };
-  c0 = ldexpf(a.scale_log2, ra < n_rows ? __ldg(a.qexp + qrow(ra)) : 0);
-  c1 = ldexpf(a.scale_log2, rb < n_rows ? __ldg(a.qexp + qrow(rb)) : 0);
+  constexpr int kSub = KQ == 2 ? 24 : 0;  // (INT4 keys as subnormals: 2^-24 per code unit)
+  c0 = ldexpf(a.scale_log2, (ra < n_rows ? __ldg(a.qexp + qrow(ra)) : 0) + kSub);
+  c1 = ldexpf(a.scale_log2, (rb < n_rows ? __ldg(a.qexp + qrow(rb)) : 0) + kSub);
   const uint16_t* p = gq < n_rows ? q + qrow(gq) * HS : nullptr;
   if constexpr (KQ == 1) {
 #pragma unroll
@@ -691,8 +703,8 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
               for (int i = 0; i < 4; ++i) {
                 const int k2 = 4 * j + i;
                 uint32_t uu[4], vv[4];
-                s4x8_to_f16(u[i], uu);
-                s4x8_to_f16(v[i], vv);
+                s4x8_to_f16_sub(u[i], uu);
+                s4x8_to_f16_sub(v[i], vv);
                 const uint32_t A0[4] = {uu[0], vv[0], uu[1], vv[1]}, A1[4] = {uu[2], vv[2], uu[3], vv[3]};
                 mma16816<false>(sa, A0, qb[2 * k2][0], qb[2 * k2][1]);
                 mma16816<false>(sb, A1, qb[2 * k2 + 1][0], qb[2 * k2 + 1][1]);
@@ -735,7 +747,7 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
           // P^T of keys gq and gq + 8, each an fp16 pair (row ra, row rb)
           const uint32_t h0 = pack2<false>(fast_exp2(x[0] - ms0), fast_exp2(x[1] - ms1));
           const uint32_t h1 = pack2<false>(fast_exp2(x[2] - ms0), fast_exp2(x[3] - ms1));
-          // the row sums add the fp16 weights the MMA multiplies (see the INT8 note below)
+          // the row sums add the fp16 weights the MMA multiplies (see the integer-cache note below)
           const float2 q0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
           const float2 q1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
           l0 = l0 * al0 + (q0.x + q1.x);
@@ -784,8 +796,8 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
 #pragma unroll
             for (int i = 0; i < R / 4; ++i) {
               uint32_t lo[8], hi[8];
-              s4_key_pairs(w0[i], w1[i], lo);
-              s4_key_pairs(w8[i], w9[i], hi);
+              s4_key_pairs_sub(w0[i], w1[i], lo);
+              s4_key_pairs_sub(w8[i], w9[i], hi);
 #pragma unroll
               for (int e = 0; e < 8; e += 2) {
                 const uint32_t A[4] = {lo[e], lo[e + 1], hi[e], hi[e + 1]};
@@ -836,8 +848,8 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
               for (int i = 0; i < 4; ++i) {
                 const int k2 = 4 * j + i;
                 uint32_t uu[4], vv[4], f0[4], f1[4];
-                s4x8_to_f16(u[i], uu);
-                s4x8_to_f16(v[i], vv);
+                s4x8_to_f16_sub(u[i], uu);
+                s4x8_to_f16_sub(v[i], vv);
                 qfrag(2 * k2, f0);
                 qfrag(2 * k2 + 1, f1);
                 mma16816<false>(sc[0], f0, uu[0], uu[1]);
@@ -906,11 +918,10 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
             pa[2] = pack2<false>(p[1][0], p[1][1]);
             pa[3] = pack2<false>(p[1][2], p[1][3]);
           }
-          if constexpr (KQ == 1) {
-            // INT8 caches: the V codes enter P V with the conversion's offset (code + 1152), which
-            // the output takes off after dividing by the row sum; that sum must then add exactly
-            // the fp16 weights the MMA multiplies. (At INT4's coarser scales the offset's share of
-            // the tensor core's fp32 rounding shows in the output: INT4 V codes stay exact.)
+          if constexpr (KQ != 0) {
+            // integer caches: the V codes enter P V with the conversion's offset (INT8 code +
+            // 1152; INT4 (code + 8) 2^-24), which the output takes off after dividing by the row
+            // sum; that sum must then add exactly the fp16 weights the MMA multiplies
             const float2 q0 = __half22float2(*reinterpret_cast<const __half2*>(&pa[0]));
             const float2 q1 = __half22float2(*reinterpret_cast<const __half2*>(&pa[1]));
             const float2 q2 = __half22float2(*reinterpret_cast<const __half2*>(&pa[2]));
@@ -962,8 +973,8 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
   #pragma unroll
             for (int i = 0; i < R / 4; ++i) {
               uint32_t lo[8], hi[8];
-              s4_key_pairs(w0[i], w1[i], lo);
-              s4_key_pairs(w8[i], w9[i], hi);
+              s4_key_pairs_sub(w0[i], w1[i], lo);
+              s4_key_pairs_sub(w8[i], w9[i], hi);
   #pragma unroll
               for (int e = 0; e < 8; ++e) mma16816<false>(o[8 * i + e], pa, lo[e], hi[e]);
             }
@@ -1167,9 +1178,9 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
         for (int bb = 1; bb < L::kCombBufs; ++bb) x += src[bb * (kDecRows * kCombStride) + v];
         return x;
       };
-      float lbias = 0.f;  // (INT8) the row's key bias, taken off the exported lse
-      if constexpr (KQ == 1) {
-        if (a.lse) lbias = int8_row_bias<HS>(a, tok, head, t, mine);
+      float lbias = 0.f;  // (integer caches) the row's key bias, taken off the exported lse
+      if constexpr (KQ != 0) {
+        if (a.lse) lbias = key_row_bias<HS, KQ>(a, tok, head, t, mine);
       }
       if (item.n_split == 1) {
         if (mine && a.lse && (t & 7) == 0)  // natural log; M is the base-2 max of s * scale
@@ -1183,8 +1194,8 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
             for (int e = 0; e < 8; ++e) x[e] = cval(v + e) * inv;
             if constexpr (KQ != 0) {  // integer caches: the V scales of the output channels
 #pragma unroll
-              for (int e = 0; e < 8; ++e)  // (INT8: the V codes' offset off) then the V scales
-                x[e] = (KQ == 1 ? x[e] - 1152.f : x[e]) * __ldg(a.v_scale + item.g * HS + col + v + e);
+              for (int e = 0; e < 8; ++e)  // (the V codes' offset off) then the V scales
+                x[e] = v_code_value<KQ>(x[e]) * __ldg(a.v_scale + item.g * HS + col + v + e);
             }
             if (a.gate)  // output gate: times sigmoid(gate), elementwise
               apply_gate8<BF16>(a.gate + ((int64_t)tok * a.nh + head) * HS + col + v, x);
@@ -1284,8 +1295,8 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
             for (int e = 0; e < 8; ++e) x[e] = acc[v + e] * dinv;
             if constexpr (KQ != 0) {
 #pragma unroll
-              for (int e = 0; e < 8; ++e)  // (INT8: the V codes' offset off) then the V scales
-                x[e] = (KQ == 1 ? x[e] - 1152.f : x[e]) * __ldg(a.v_scale + item.g * HS + col + v + e);
+              for (int e = 0; e < 8; ++e)  // (the V codes' offset off) then the V scales
+                x[e] = v_code_value<KQ>(x[e]) * __ldg(a.v_scale + item.g * HS + col + v + e);
             }
             if (a.gate) apply_gate8<BF16>(a.gate + ((int64_t)tok * a.nh + head) * HS + col + v, x);
             uint4 pk;
