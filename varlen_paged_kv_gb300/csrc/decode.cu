@@ -1320,6 +1320,12 @@ __global__ void __launch_bounds__(160, dec_ctas_per_sm(HS, KQ))
 // are done, so the decode kernel can cut its partition from the batch description while
 // this kernel runs.
 __global__ void __launch_bounds__(256) decode_prep_kernel(const Args a) {
+  // the batch description into L2 while the previous call finishes (hints only): the decode
+  // kernel's prologue reads it next
+  for (int i = threadIdx.x * 32; i <= a.B; i += blockDim.x * 32) {
+    prefetch_l2(a.cum + i);
+    if (i < a.B) prefetch_l2(a.past + i);
+  }
   pdl_wait();  // the previous call's kernels may still use this workspace
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
