@@ -326,16 +326,19 @@ class Runner:
 # the figure is reported only while the sources are unchanged, else traffic is null.
 # ("decode_kernel_self": the self-planned instantiation that decode-only steps run.)
 NCU_TRAFFIC = {
-    ("decode_kernel_self", "decode-b64"): (618592000 + 4575744, "82ee04b0eb7dfff2"),
-    ("decode_kernel_self", "long-decode-b8-bs16"): (2279083776 + 3449088, "82ee04b0eb7dfff2"),
-    ("decode_kernel_self", "decode-b64-int8"): (310146560 + 3822592, "82ee04b0eb7dfff2"),
-    ("decode_kernel_self", "decode-b64-int4"): (155715584 + 3701760, "82ee04b0eb7dfff2"),
-    ("decode_kernel_self", "decode-b64-hs256"): (295606528 + 4131328, "82ee04b0eb7dfff2"),
-    ("prefill_kernel", "causal-prefill-4x2048"): (104478720 + 31718912, "8f0b518ec5af374f"),
-    ("prefill256_kernel", "causal-prefill-hs256"): (84037632 + 26018048, "7b964e02da23c06b"),
-    # the two attention kernels of a mixed step (prefill 188.7 + 15.1 MB, decode 775.7 + 0.6 MB)
-    ("prefill_kernel+decode_kernel", "mixed-8x512-chunks+24-decode"): (188687360 + 15142912 + 775707904 + 643328,
-                                                                        "18685b97e7e59d62"),
+    ("decode_kernel_self", "decode-b64"): (618571264 + 3949568, "60b03b0f6ae5b585"),
+    ("decode_kernel_self", "long-decode-b8-bs16"): (2279145216 + 3383808, "60b03b0f6ae5b585"),
+    ("decode_kernel_self", "decode-b64-int8"): (310127360 + 3813888, "60b03b0f6ae5b585"),
+    ("decode_kernel_self", "decode-b64-int4"): (155677184 + 3664128, "60b03b0f6ae5b585"),
+    ("decode_kernel_self", "decode-b64-hs256"): (295574016 + 4117248, "60b03b0f6ae5b585"),
+    ("prefill_kernel", "causal-prefill-4x2048"): (104553728 + 31587584, "e724878cd8a891bc"),
+    ("prefill256_kernel", "causal-prefill-hs256"): (84046592 + 25989888, "e86ef9114bf38318"),
+    # the two attention kernels of a mixed step (prefill 188.7 + 15.2 MB, decode 775.7 + 0.4 MB;
+    # on INT8 caches prefill 100.9 + 8.8 MB, decode 388.2 + 0.4 MB)
+    ("prefill_kernel+decode_kernel", "mixed-8x512-chunks+24-decode"): (188651520 + 15170816 + 775681792 + 366592,
+                                                                        "78b40566efefd9ca"),
+    ("prefill_kernel+decode_kernel", "mixed-8x512-chunks+24-decode-int8"): (100945152 + 8791040 + 388159232 + 444928,
+                                                                             "78b40566efefd9ca"),
 }
 KERNEL_SOURCES = {"decode_kernel": ("decode.cu", "common.cuh"), "decode_kernel_self": ("decode.cu", "common.cuh"),
                   "prefill_kernel": ("prefill.cu", "common.cuh"), "prefill256_kernel": ("prefill256.cu", "common.cuh"),
