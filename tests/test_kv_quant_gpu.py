@@ -152,10 +152,11 @@ def test_codes_at_and_next_to_ties(fmt):
     assert np.array_equal(cache_bytes(d["value_cache"]), ref["value_cache"]), "value codes differ"
 
 
+@pytest.mark.parametrize("q_lens", [[1, 2, 1], [1, 1, 1]])  # 16 rows per item at most; 8: the narrow form
 @pytest.mark.parametrize("fmt", ["int8", "int4"])
-def test_integer_cache_with_prep_and_gate(fmt):
+def test_integer_cache_with_prep_and_gate(fmt, q_lens):
     p = w.make_problem(name="q-prep", seed=33, dtype="bf16", num_heads=16, kv_num_heads=2, head_size=128,
-                       block_size=64, past=[100, 2000, 7], q_lens=[1, 2, 1], kv_quant=fmt)
+                       block_size=64, past=[100, 2000, 7], q_lens=q_lens, kv_quant=fmt)
     to_t = oracle.double_to_bf16
     prep_bits = dict(q_norm_weight=to_t(np.linspace(0.5, 1.5, 128)), k_norm_weight=to_t(np.linspace(1.2, 0.8, 128)),
                      eps=1e-6, rotary_dim=64, theta=1.0e6)
