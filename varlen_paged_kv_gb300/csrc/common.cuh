@@ -690,8 +690,11 @@ __device__ __forceinline__ void s4_key_pairs_sub(uint32_t w0, uint32_t w1, uint3
 // about 1152 * 2^-12 of a code. So V is exact, like K.) Each lane takes one 16-byte code chunk
 // (16 INT8 or 32 INT4 channels) of a row in each of UNR rounds, reading all of them before
 // writing any, so only a row's own codes are overwritten and only after the whole warp has
-// read them. cw: this converter warp (0 or 1).
-template <int HS, int KQ>
+// read them. cw: this converter warp (0 or 1). With SUB (the 128-wide kernel's K tiles) the
+// codes become the fp16 subnormals (code + 128) 2^-24 (INT4: (code + 8) 2^-24), the bits of
+// the biased code as the fp16's bits: no subtraction; the offset adds a constant per query
+// row to its scores, which the softmax does not see and the exported lse has taken off.
+template <int HS, int KQ, bool SUB = false>
 __device__ __forceinline__ void convert_code_tile(uint8_t* tile, int cw, int lane) {
   constexpr int RB = KQ == 1 ? HS : HS / 2;                       // code bytes per row
   constexpr int CH = RB / 16;                                      // code chunks per row
@@ -719,16 +722,23 @@ __device__ __forceinline__ void convert_code_tile(uint8_t* tile, int cw, int lan
 #pragma unroll
         for (int i = 0; i < 4; ++i) {  // channels 4i .. 4i + 3 of the chunk
           const uint32_t x = w[i] ^ 0x80808080u;
-          f[2 * i] = hsub2_u32(prmt(x, kF16Magic, 0x5140u), kF16Int8Bias);
-          f[2 * i + 1] = hsub2_u32(prmt(x, kF16Magic, 0x7362u), kF16Int8Bias);
+          if constexpr (SUB) {
+            f[2 * i] = prmt(x, 0u, 0x4140u);
+            f[2 * i + 1] = prmt(x, 0u, 0x4342u);
+          } else {
+            f[2 * i] = hsub2_u32(prmt(x, kF16Magic, 0x5140u), kF16Int8Bias);
+            f[2 * i + 1] = hsub2_u32(prmt(x, kF16Magic, 0x7362u), kF16Int8Bias);
+          }
         }
       } else {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {  // channels 8i .. 8i + 7: byte b holds 2b (low), 2b + 1 (high)
           const uint32_t x = w[i] ^ 0x88888888u, x4 = x >> 4;
 #pragma unroll
-          for (int b = 0; b < 4; ++b)
-            f[4 * i + b] = hsub2_u32(nib_pair_f16(prmt(x, x4, (uint32_t)(b | ((4 + b) << 8)))), kF16Int4Bias);
+          for (int b = 0; b < 4; ++b) {
+            const uint32_t nib = prmt(x, x4, (uint32_t)(b | ((4 + b) << 8)));
+            f[4 * i + b] = SUB ? nib & 0x000F000Fu : hsub2_u32(nib_pair_f16(nib), kF16Int4Bias);
+          }
         }
       }
 #pragma unroll

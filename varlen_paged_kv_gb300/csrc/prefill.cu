@@ -373,10 +373,11 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         const int lim = min(past + tile.j0 + row, kv_len - 1);  // last key this row sees
         const int lim_tile0 = past + tile.j0;                   // the smallest limit of the unit
         // the softmax constant scale * log2(e); integer caches: times 2^E, the exponent the
-        // cache-write stage took out of this row's scaled query (rows past the sequence: 1)
+        // cache-write stage took out of this row's scaled query, and 2^24, the unit of the
+        // K codes' subnormals (rows past the sequence: 1)
         float c = a.scale_log2;
         if constexpr (KQ != 0)
-          if (tile.j0 + row < q_len) c = ldexpf(c, __ldg(a.qexp + (int64_t)(c0 + tile.j0 + row) * a.nh + h));
+          if (tile.j0 + row < q_len) c = ldexpf(c, __ldg(a.qexp + (int64_t)(c0 + tile.j0 + row) * a.nh + h) + 24);
         float m_used = -INFINITY, l = 0.f;
         for (int t = 0; t < n_kv; ++t) {
           const uint32_t gt = gs + t;
@@ -510,8 +511,24 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           const float l_row = xs[0] + xs[1];
           const float inv = 1.f / l_row;
           const bool store = tile.j0 + row < q_len;
-          if (a.lse && store && hsel == 0)  // natural log; m_used is the base-2 max of s * scale
-            a.lse[(int64_t)(c0 + tile.j0 + row) * a.nh + h] = (m_used + fast_log2(l_row)) * 0.69314718055994531f;
+          if (a.lse && store && hsel == 0) {  // natural log; m_used is the base-2 max of s * scale
+            float bias = 0.f;  // (integer caches) the K codes' offset in the row's scores
+            if constexpr (KQ != 0) {
+              const int64_t qr = (int64_t)(c0 + tile.j0 + row) * a.nh + h;
+              const uint4* qp = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.query) + qr * HS);
+              float sq = 0.f;
+              for (int i = 0; i < HS / 8; ++i) {
+                const uint4 q4 = __ldg(qp + i);
+                const uint32_t qw[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  sq += __half2float(__ushort_as_half((unsigned short)(qw[e] & 0xFFFFu))) +
+                        __half2float(__ushort_as_half((unsigned short)(qw[e] >> 16)));
+              }
+              bias = (KQ == 1 ? 128.f : 8.f) * sq * ldexpf(a.scale_log2, __ldg(a.qexp + qr));
+            }
+            a.lse[(int64_t)(c0 + tile.j0 + row) * a.nh + h] = (m_used + fast_log2(l_row) - bias) * 0.69314718055994531f;
+          }
           uint16_t* dst =
               reinterpret_cast<uint16_t*>(a.output) + ((int64_t)(c0 + tile.j0 + row) * a.nh + h) * HS + hsel * OCOLS;
           // this thread's half row of O in registers, then O is released to the next unit
@@ -574,7 +591,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           const int st = gs & 1;
           const uint32_t ph = (gs >> 1) & 1;
           mbar_wait(&kc_full[st], ph, abort, err);
-          convert_code_tile<HS, KQ>(smem + L::kK0 + st * L::kKVBytes, cw, lane);
+          convert_code_tile<HS, KQ, true>(smem + L::kK0 + st * L::kKVBytes, cw, lane);
           fence_proxy_async_smem();  // (the MMA reads the tile through the async proxy)
           __syncwarp();
           if (lane == 0) mbar_arrive(&k_full[st]);
