@@ -326,19 +326,19 @@ class Runner:
 # the figure is reported only while the sources are unchanged, else traffic is null.
 # ("decode_kernel_self": the self-planned instantiation that decode-only steps run.)
 NCU_TRAFFIC = {
-    ("decode_kernel_self", "decode-b64"): (618571264 + 3949568, "60b03b0f6ae5b585"),
-    ("decode_kernel_self", "long-decode-b8-bs16"): (2279145216 + 3383808, "60b03b0f6ae5b585"),
-    ("decode_kernel_self", "decode-b64-int8"): (310127360 + 3813888, "60b03b0f6ae5b585"),
-    ("decode_kernel_self", "decode-b64-int4"): (155677184 + 3664128, "60b03b0f6ae5b585"),
-    ("decode_kernel_self", "decode-b64-hs256"): (295574016 + 4117248, "60b03b0f6ae5b585"),
-    ("prefill_kernel", "causal-prefill-4x2048"): (104553728 + 31587584, "e724878cd8a891bc"),
-    ("prefill256_kernel", "causal-prefill-hs256"): (84046592 + 25989888, "e86ef9114bf38318"),
-    # the two attention kernels of a mixed step (prefill 188.7 + 15.2 MB, decode 775.7 + 0.4 MB;
-    # on INT8 caches prefill 100.9 + 8.8 MB, decode 388.2 + 0.4 MB)
-    ("prefill_kernel+decode_kernel", "mixed-8x512-chunks+24-decode"): (188651520 + 15170816 + 775681792 + 366592,
-                                                                        "78b40566efefd9ca"),
-    ("prefill_kernel+decode_kernel", "mixed-8x512-chunks+24-decode-int8"): (100945152 + 8791040 + 388159232 + 444928,
-                                                                             "78b40566efefd9ca"),
+    ("decode_kernel_self", "decode-b64"): (618575104 + 3658496, "d2a44dccd99c9f24"),
+    ("decode_kernel_self", "long-decode-b8-bs16"): (2279131904 + 3412736, "d2a44dccd99c9f24"),
+    ("decode_kernel_self", "decode-b64-int8"): (310088704 + 3812864, "d2a44dccd99c9f24"),
+    ("decode_kernel_self", "decode-b64-int4"): (155679744 + 3673856, "d2a44dccd99c9f24"),
+    ("decode_kernel_self", "decode-b64-hs256"): (295574784 + 4252672, "d2a44dccd99c9f24"),
+    ("prefill_kernel", "causal-prefill-4x2048"): (104446976 + 31610368, "e153f56785dafd0e"),
+    ("prefill256_kernel", "causal-prefill-hs256"): (84022784 + 25982208, "ca9b5abc8949062e"),
+    # the two attention kernels of a mixed step (prefill 188.8 + 15.5 MB, decode 775.7 + 0.3 MB;
+    # on INT8 caches prefill 101.0 + 8.7 MB, decode 388.2 + 0.5 MB)
+    ("prefill_kernel+decode_kernel", "mixed-8x512-chunks+24-decode"): (188848640 + 15481600 + 775743232 + 322048,
+                                                                        "abf44e05ff8f6b81"),
+    ("prefill_kernel+decode_kernel", "mixed-8x512-chunks+24-decode-int8"): (100956672 + 8674816 + 388170240 + 463104,
+                                                                             "abf44e05ff8f6b81"),
 }
 KERNEL_SOURCES = {"decode_kernel": ("decode.cu", "common.cuh"), "decode_kernel_self": ("decode.cu", "common.cuh"),
                   "prefill_kernel": ("prefill.cu", "common.cuh"), "prefill256_kernel": ("prefill256.cu", "common.cuh"),

@@ -247,9 +247,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Args a) {
     const float bytes = (float)s_dec_tiles * (float)a.kvh * (float)(kDecTile * a.hs * 2 * 2);
     // (bytes counts 16-bit K/V. On integer caches the decode side streams a half or a quarter
     // of them, three CTAs per SM, and the prefill side converts codes: per SM the decode
-    // kernel gains about 30% (INT8) or 15% (INT4) on the prefill kernel, the optima measured
-    // on the mixed batch)
-    const float dec_rate = kSplitDecBytes * (a.kvq == 1 ? 1.3f : a.kvq == 2 ? 1.15f : 1.f);
+    // kernel gains about 20% on the prefill kernel, the optimum of a sweep on the mixed batch)
+    const float dec_rate = kSplitDecBytes * (a.kvq ? 1.2f : 1.f);
     const float hbm = kSplitHbmBytes * (a.kvq == 1 ? 2.f : a.kvq == 2 ? 4.f : 1.f);
     for (int d = tid + 1; d < S; d += blockDim.x) {
       const float tp = flops / ((float)(S - d) * kSplitPreFlops);
