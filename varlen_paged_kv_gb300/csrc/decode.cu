@@ -17,13 +17,18 @@
 //     shared memory (at head_size 256 in two buffers, warps 0 + 2 and 1 + 3, which the
 //     writer adds; an item of at most four rows in one round, the four warps' rows side by
 //     side, added by the writer in warp order). An item that is its whole unit writes the
-//     output row rounded once to T; otherwise it writes its normalised fp32 partial row and
-//     natural-log lse, and the last item of the unit to finish (an atomic arrival count)
-//     merges the unit's partials in key order: the (out, lse) reduction of the WS2
-//     CP-Aware Attention Contract, "Reduction Semantics" (fp32, fixed order, downcast at
-//     the final write).
+//     output row rounded once to T; otherwise the unit's pieces are merged in key order:
+//     the (out, lse) reduction of the WS2 CP-Aware Attention Contract, "Reduction
+//     Semantics" (fp32, fixed order, downcast at the final write). On the balanced cut the
+//     first piece's CTA merges, from its own combine buffer and the others' normalised fp32
+//     partial rows and natural-log lse, once their arrival count says they are written;
+//     with forced split lengths the last piece to finish merges.
+// Integer caches: the codes become fp16 in registers as the tiles are read (three CTAs per
+// SM below head_size 256); items of at most 8 rows take the "narrow" form, keys and
+// channels as the MMA rows and the query rows as its columns (half the MMAs).
 // CTA c processes the items [cta_begin[c], cta_begin[c+1]) that the planner cut so that
-// the CTAs finish together (each item counting a fixed cost of a few tiles beside its keys).
+// the CTAs finish together (each item counting a fixed cost of a few tiles beside its keys);
+// a decode-only batch with the host's bound cuts its own share (the self-planned form).
 #include "common.cuh"
 
 namespace pa {
