@@ -562,7 +562,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-// barrier `id` (1..15) among `count` threads (a multiple of 32)
 // Wait until the counter at p reaches need (acquire at gpu scope), at most ~2 s: on time-out
 // (or when another thread of the CTA already gave up, *abort != 0) it sets *abort and the
 // PA_DEVERR_TIMEOUT bit and returns false.
@@ -582,6 +581,7 @@ __device__ __forceinline__ bool wait_count_acquire_gpu(const int* p, int need, v
     }
   }
 }
+// barrier `id` (1..15) among `count` threads (a multiple of 32)
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
